@@ -1,0 +1,49 @@
+/*
+ * mamba_oracle.h - declarations of the f64 CPU oracle (test infrastructure
+ * only; see mamba_oracle.c).  All arrays are dense, row-major, f64:
+ *   activations x, u, dt, z, y : [B][T][Di]
+ *   B, C                       : [B][T][N]
+ *   A_log                      : [Di][N]
+ *   w                          : [Di][K]
+ *   bias, D, dt_bias           : [Di]           (NULL = 0)
+ *   conv state                 : [B][Di][K]     (slot 0 oldest)
+ *   ssm state                  : [B][Di][N]
+ * The *_step functions take the base of a [n_layers][B*Di*S] state buffer and
+ * update the slab of `layer` in place.  Return 0 on success, -1 on a bad
+ * argument.  `nthreads` only spreads independent (b, c) rows over threads.
+ */
+#ifndef MAMBA_ORACLE_H
+#define MAMBA_ORACLE_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+double oracle_softplus(double v);
+double oracle_silu(double x);
+
+int oracle_conv1d_silu_prefill(double* u, double* state_out, const double* x,
+                               const double* state_in, const double* w,
+                               const double* bias, long B, long T, long Di, long K,
+                               int nthreads);
+
+int oracle_selective_scan_prefill(double* y, double* state_out, const double* u,
+                                  const double* dt, const double* z, const double* Bm,
+                                  const double* Cm, const double* A_log, const double* D,
+                                  const double* dt_bias, const double* state_in, long B,
+                                  long T, long Di, long N, int nthreads);
+
+int oracle_conv1d_silu_step(double* u, double* conv_state, long layer, const double* x,
+                            const double* w, const double* bias, long B, long Di, long K,
+                            int nthreads);
+
+int oracle_ssm_step(double* y, double* ssm_state, long layer, const double* u,
+                    const double* dt, const double* z, const double* Bm, const double* Cm,
+                    const double* A_log, const double* D, const double* dt_bias, long B,
+                    long Di, long N, int nthreads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

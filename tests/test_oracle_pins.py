@@ -1,0 +1,290 @@
+"""Pins for the f64 CPU oracle, independent of the oracle's own code.
+
+Each test checks the oracle against something the pages or the mathematics fix
+(mamba-rs inference.rs / prefill.rs source views; the Mamba-1 recurrence):
+library special functions, the unrolled closed form of the recurrence, the
+geometric series for d_state = 1, continuation, T=1 prefill == step,
+delta -> 0, A -> -inf, linearity in (u, h0), row independence, and the conv's
+impulse response and shift-register state.  They are chosen so that a dropped
+term, a wrong sign, an off-by-one index or a transposed operand in the oracle
+fails at least one of them.
+"""
+import numpy as np
+import pytest
+from scipy.special import expit
+
+import oracle
+from selective_state_space_conv1d_gb300 import synth
+
+RNG = np.random.default_rng(1234)
+
+
+def _rand_scan_case(Bsz=2, T=24, Di=5, N=4, gate=True, state=True, seed=0):
+    r = np.random.default_rng(seed)
+    c = dict(
+        u=r.standard_normal((Bsz, T, Di)),
+        dt=0.3 * r.standard_normal((Bsz, T, Di)),
+        Bm=r.standard_normal((Bsz, T, N)),
+        Cm=r.standard_normal((Bsz, T, N)),
+        A_log=r.uniform(-1.0, 1.5, (Di, N)),
+        D=r.standard_normal(Di),
+        dt_bias=r.uniform(-3.0, 0.5, Di),
+        z=r.standard_normal((Bsz, T, Di)) if gate else None,
+        state_in=r.standard_normal((Bsz, Di, N)) if state else None,
+    )
+    return c
+
+
+def _unrolled(c):
+    """Brute force: y_t = sum_{s<=t} C_t (prod_{r=s+1..t} exp(d_r A)) d_s B_s u_s
+    + C_t (prod_{r<=t} exp(d_r A)) h0 + D u_t, gated; h_T likewise.  O(T^2 N)."""
+    u, dt, Bm, Cm = c["u"], c["dt"], c["Bm"], c["Cm"]
+    Bsz, T, Di = u.shape
+    N = Bm.shape[2]
+    A = -np.exp(c["A_log"])
+    delta = np.logaddexp(0.0, dt + c["dt_bias"][None, None, :])  # library softplus
+    h0 = c["state_in"] if c["state_in"] is not None else np.zeros((Bsz, Di, N))
+    y = np.zeros((Bsz, T, Di))
+    hT = np.zeros((Bsz, Di, N))
+    for b in range(Bsz):
+        for ch in range(Di):
+            dA = np.exp(delta[b, :, ch][:, None] * A[ch][None, :])  # [T, N]
+            for t in range(T + 1):
+                # state after tokens 0..t-1 (t == T gives the final state)
+                h = np.prod(dA[:t], axis=0) * h0[b, ch]
+                for s in range(t):
+                    h = h + np.prod(dA[s + 1:t], axis=0) * delta[b, s, ch] * Bm[b, s] * u[b, s, ch]
+                if t < T:
+                    # y_t uses the state after token t
+                    ht = np.prod(dA[: t + 1], axis=0) * h0[b, ch]
+                    for s in range(t + 1):
+                        ht = ht + np.prod(dA[s + 1:t + 1], axis=0) * delta[b, s, ch] * Bm[b, s] * u[b, s, ch]
+                    yt = Cm[b, t] @ ht + c["D"][ch] * u[b, t, ch]
+                    if c["z"] is not None:
+                        yt *= c["z"][b, t, ch] * expit(c["z"][b, t, ch])
+                    y[b, t, ch] = yt
+                else:
+                    hT[b, ch] = h
+    return y, hT
+
+
+def _scan(c, **over):
+    c = dict(c, **over)
+    return oracle.selective_scan_prefill(
+        c["u"], c["dt"], c["Bm"], c["Cm"], c["A_log"], D=c["D"], dt_bias=c["dt_bias"],
+        z=c["z"], state_in=c["state_in"], nthreads=2)
+
+
+# ---------------------------------------------------------------- functions --
+
+def test_softplus_matches_library_and_identity():
+    for v in [-750.0, -200.0, -40.0, -5.0, -1e-3, 0.0, 1e-8, 0.7, 5.0, 30.0, 700.0]:
+        assert oracle.softplus(v) == pytest.approx(np.logaddexp(0.0, v), rel=1e-15, abs=1e-300)
+        # softplus(v) - softplus(-v) = v
+        assert oracle.softplus(v) - oracle.softplus(-v) == pytest.approx(v, rel=1e-14, abs=1e-14)
+    assert oracle.softplus(0.0) == pytest.approx(np.log(2.0), rel=1e-16)
+
+
+def test_silu_matches_library():
+    for x in [-700.0, -30.0, -1.0, 0.0, 0.5, 3.0, 40.0]:
+        assert oracle.silu(x) == pytest.approx(x * expit(x), rel=1e-15, abs=1e-300)
+    assert oracle.silu(0.0) == 0.0
+
+
+# --------------------------------------------------------------------- scan --
+
+@pytest.mark.parametrize("gate,state", [(True, True), (False, False), (True, False)])
+def test_scan_matches_unrolled_brute_force(gate, state):
+    c = _rand_scan_case(Bsz=2, T=20, Di=3, N=4, gate=gate, state=state, seed=7)
+    y, hT = _scan(c)
+    y_ref, h_ref = _unrolled(c)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(hT, h_ref, rtol=1e-11, atol=1e-12)
+
+
+def test_scan_d_state_one_closed_form_geometric_series():
+    # constant delta, B, u; N = 1:  h_t = a^t h0 + b (1 - a^t) / (1 - a)
+    T, Di = 50, 3
+    A_log = np.array([[0.0], [0.7], [-0.4]])
+    dt_bias = np.array([0.2, -1.0, 0.0])
+    dtv, uv, Bv, Cv, h0 = 0.05, 0.8, -1.3, 0.6, np.array([0.4, -2.0, 1.5])
+    Dv = np.array([1.0, 0.5, -0.25])
+    u = np.full((1, T, Di), uv)
+    y, hT = oracle.selective_scan_prefill(
+        u, np.full((1, T, Di), dtv), np.full((1, T, 1), Bv), np.full((1, T, 1), Cv), A_log,
+        D=Dv, dt_bias=dt_bias, state_in=h0.reshape(1, Di, 1), nthreads=1)
+    delta = np.log1p(np.exp(dtv + dt_bias))
+    a = np.exp(-delta * np.exp(A_log[:, 0]))
+    bb = delta * Bv * uv
+    t = np.arange(1, T + 1)[:, None]
+    h = a ** t * h0 + bb * (1 - a ** t) / (1 - a)
+    np.testing.assert_allclose(y[0], Cv * h + Dv * uv, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(hT[0, :, 0], h[-1], rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("T1", [1, 7, 16])
+def test_scan_continuation_is_bitwise(T1):
+    c = _rand_scan_case(Bsz=2, T=29, Di=4, N=8, seed=3)
+    y, hT = _scan(c)
+    sl = lambda a, s: None if a is None else a[:, s]
+    c1 = {k: (sl(v, slice(0, T1)) if k in ("u", "dt", "Bm", "Cm", "z") else v) for k, v in c.items()}
+    c2 = {k: (sl(v, slice(T1, None)) if k in ("u", "dt", "Bm", "Cm", "z") else v) for k, v in c.items()}
+    y1, h1 = _scan(c1)
+    c2["state_in"] = h1
+    y2, h2 = _scan(c2)
+    assert np.array_equal(np.concatenate([y1, y2], axis=1), y)
+    assert np.array_equal(h2, hT)
+
+
+def test_scan_T1_prefill_equals_step_bitwise():
+    c = _rand_scan_case(Bsz=3, T=1, Di=6, N=16, seed=11)
+    y, hT = _scan(c)
+    L = 3
+    states = np.random.default_rng(5).standard_normal((L, 3, 6, 16))
+    states[1] = c["state_in"]
+    before = states.copy()
+    ys = oracle.ssm_step(c["u"][:, 0], c["dt"][:, 0], c["Bm"][:, 0], c["Cm"][:, 0], states, 1,
+                         c["A_log"], D=c["D"], dt_bias=c["dt_bias"], z=c["z"][:, 0])
+    assert np.array_equal(ys, y[:, 0])
+    assert np.array_equal(states[1], hT)
+    assert np.array_equal(states[0], before[0]) and np.array_equal(states[2], before[2])
+
+
+def test_scan_delta_to_zero_keeps_state():
+    c = _rand_scan_case(Bsz=1, T=10, Di=4, N=4, gate=False, state=True, seed=2)
+    c["dt"] = np.zeros_like(c["dt"])
+    c["dt_bias"] = np.full(4, -800.0)  # softplus(-800) == 0 in f64
+    y, hT = _scan(c)
+    assert np.array_equal(hT, c["state_in"])
+    expect = np.einsum("btn,bcn->btc", c["Cm"], c["state_in"]) + c["D"] * c["u"]
+    np.testing.assert_allclose(y, expect, rtol=1e-14, atol=1e-14)
+    # zero initial state: y = D * u exactly, state stays zero
+    y0, h0 = _scan(c, state_in=None)
+    assert np.array_equal(h0, np.zeros_like(h0))
+    np.testing.assert_array_equal(y0, c["D"] * c["u"])
+
+
+def test_scan_A_to_minus_infinity_is_memoryless():
+    c = _rand_scan_case(Bsz=2, T=12, Di=3, N=4, gate=False, state=True, seed=4)
+    c["A_log"] = np.full((3, 4), 80.0)  # A = -exp(80): exp(delta A) == 0
+    y, hT = _scan(c)
+    delta = np.logaddexp(0.0, c["dt"] + c["dt_bias"])
+    h = delta[..., None] * c["Bm"][:, :, None, :] * c["u"][..., None]  # [B, T, Di, N]
+    np.testing.assert_allclose(y, np.einsum("btn,btcn->btc", c["Cm"], h) + c["D"] * c["u"],
+                               rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(hT, h[:, -1], rtol=1e-13, atol=1e-14)
+
+
+def test_scan_is_linear_in_u_and_h0():
+    c1 = _rand_scan_case(Bsz=1, T=15, Di=3, N=4, gate=False, state=True, seed=21)
+    c2 = _rand_scan_case(Bsz=1, T=15, Di=3, N=4, gate=False, state=True, seed=22)
+    c2.update({k: c1[k] for k in ("dt", "Bm", "Cm", "A_log", "D", "dt_bias")})
+    al, be = 0.7, -1.9
+    y1, h1 = _scan(c1)
+    y2, h2 = _scan(c2)
+    y3, h3 = _scan(c1, u=al * c1["u"] + be * c2["u"], state_in=al * c1["state_in"] + be * c2["state_in"])
+    np.testing.assert_allclose(y3, al * y1 + be * y2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(h3, al * h1 + be * h2, rtol=1e-12, atol=1e-12)
+
+
+def test_scan_rows_are_independent_and_permute():
+    c = _rand_scan_case(Bsz=3, T=9, Di=6, N=4, seed=8)
+    y, hT = _scan(c)
+    perm = np.array([3, 0, 5, 1, 4, 2])
+    cp = dict(c)
+    for k in ("u", "dt", "z"):
+        cp[k] = c[k][:, :, perm]
+    for k in ("D", "dt_bias"):
+        cp[k] = c[k][perm]
+    cp["A_log"] = c["A_log"][perm]
+    cp["state_in"] = c["state_in"][:, perm]
+    yp, hp = _scan(cp)
+    assert np.array_equal(yp, y[:, :, perm]) and np.array_equal(hp, hT[:, perm])
+    # batch row 1 run alone
+    c1 = {k: (v[1:2] if k in ("u", "dt", "z", "Bm", "Cm", "state_in") else v) for k, v in c.items()}
+    y1, h1 = _scan(c1)
+    assert np.array_equal(y1[0], y[1]) and np.array_equal(h1[0], hT[1])
+
+
+def test_scan_gate_special_values():
+    c = _rand_scan_case(Bsz=1, T=6, Di=2, N=4, gate=True, state=True, seed=9)
+    y_nogate, _ = _scan(c, z=None)
+    y_zero, _ = _scan(c, z=np.zeros_like(c["z"]))
+    assert np.array_equal(y_zero, np.zeros_like(y_zero))
+    y_big, _ = _scan(c, z=np.full_like(c["z"], 800.0))  # SiLU(800) == 800 exactly
+    np.testing.assert_array_equal(y_big, y_nogate * 800.0)
+
+
+# --------------------------------------------------------------------- conv --
+
+def test_conv_impulse_response():
+    K, Di, T, t0 = 4, 3, 12, 5
+    w = RNG.uniform(-0.5, 0.5, (Di, K))
+    bias = np.array([0.0, 0.3, -0.2])
+    x = np.zeros((1, T, Di))
+    x[0, t0] = 1.0
+    u, st = oracle.conv1d_silu_prefill(x, w, bias, None, nthreads=1)
+    pre = np.tile(bias, (T, 1))
+    for j in range(K):
+        pre[t0 + j] = w[:, K - 1 - j] + bias  # the newest tap w[:, K-1] meets x_t
+    np.testing.assert_allclose(u[0], pre * expit(pre), rtol=1e-15, atol=1e-300)
+
+
+def test_conv_constant_input_and_state_semantics():
+    K, Di, T = 4, 2, 9
+    w = RNG.uniform(-0.5, 0.5, (Di, K))
+    bias = np.array([0.1, -0.4])
+    x = np.full((1, T, Di), 0.75)
+    u, st = oracle.conv1d_silu_prefill(x, w, bias, None, nthreads=1)
+    pre = bias + 0.75 * w.sum(1)
+    np.testing.assert_allclose(u[0, K - 1:], np.tile(pre * expit(pre), (T - K + 1, 1)), rtol=1e-15)
+    assert np.array_equal(st[0], np.full((Di, K), 0.75))
+
+
+@pytest.mark.parametrize("T", [1, 2, 3, 4, 7])
+def test_conv_state_out_is_last_K_of_state_then_inputs(T):
+    K, Di = 4, 3
+    w = RNG.uniform(-0.5, 0.5, (Di, K))
+    s0 = RNG.standard_normal((2, Di, K))
+    x = RNG.standard_normal((2, T, Di))
+    u, st = oracle.conv1d_silu_prefill(x, w, None, s0, nthreads=1)
+    seq = np.concatenate([s0, np.transpose(x, (0, 2, 1))], axis=2)  # [B, Di, K+T]
+    assert np.array_equal(st, seq[:, :, T:T + K])
+    # every output uses slots 1..K-1 of the state then the inputs: pre_t = sum_k w_k seq[t+1+k]
+    for t in range(T):
+        pre = np.einsum("ck,bck->bc", w, seq[:, :, t + 1:t + 1 + K])
+        np.testing.assert_allclose(u[:, t], pre * expit(pre), rtol=1e-14, atol=1e-15)
+
+
+def test_conv_continuation_and_step_bitwise():
+    K, Di, T = 4, 5, 13
+    w = RNG.uniform(-0.5, 0.5, (Di, K))
+    bias = RNG.standard_normal(Di)
+    s0 = RNG.standard_normal((2, Di, K))
+    x = RNG.standard_normal((2, T, Di))
+    u, st = oracle.conv1d_silu_prefill(x, w, bias, s0)
+    u1, st1 = oracle.conv1d_silu_prefill(x[:, :6], w, bias, s0)
+    u2, st2 = oracle.conv1d_silu_prefill(x[:, 6:], w, bias, st1)
+    assert np.array_equal(np.concatenate([u1, u2], 1), u) and np.array_equal(st2, st)
+    # T token steps on layer 1 of a 2-layer state equal the prefill
+    states = np.zeros((2, 2, Di, K))
+    states[1] = s0
+    for t in range(T):
+        ut = oracle.conv1d_silu_step(x[:, t], states, 1, w, bias)
+        assert np.array_equal(ut, u[:, t])
+    assert np.array_equal(states[1], st) and np.array_equal(states[0], np.zeros((2, Di, K)))
+
+
+# ---------------------------------------------------------------- workloads --
+
+def test_tiny_workload_runs_and_is_finite():
+    wl = synth.WORKLOADS[0]
+    p = synth.mixer_params(wl.seed, wl.d_inner, wl.d_state, wl.d_conv)
+    a = synth.prefill_inputs(wl.seed, wl.batch, wl.seqlen, wl.d_inner, wl.d_state)
+    u, cst = oracle.conv1d_silu_prefill(a["x"], p["conv_w"], p["conv_b"], None)
+    y, sst = oracle.selective_scan_prefill(u, a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                           p["dt_bias"], a["z"], None)
+    assert np.isfinite(y).all() and np.isfinite(sst).all() and np.isfinite(cst).all()
+    # delta lies in the log-uniform range widened by dt ~ N(0, 0.1^2)
+    delta = np.logaddexp(0.0, a["dt"].astype(np.float64) + p["dt_bias"])
+    assert 1e-4 < delta.min() and delta.max() < 0.3
