@@ -1,0 +1,644 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 Mamba-1 mixer core.
+
+Headline (one JSON line on rank 0): prefill tokens/s of one mamba-130m-shaped
+layer (batch 1, T 2048, d_inner 1536, d_state 16, d_conv 4, f32) -- one step is
+the conv1d+SiLU prefill followed by the selective-scan prefill, through the C
+ABI, on seeded synthetic inputs already resident in HBM.  The same line carries
+the decode workload (24 layers x batch 128 T=1 steps; decode steps/s) and the
+mamba-2.8b-shaped bf16 prefill under "extra", the HBM roofline of the dominant
+kernel, the end-to-end figure (host buffers, copies inside the timed region),
+the f64 CPU oracle timed on the host cores, and the SM clocks seen.
+
+Launch: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N > 1 runs under torch.distributed.run: every rank runs an independent replica
+on its own GPU (the mixer shards over batch and channels with no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s and decode steps/s (batch×layers) at 1 GB300; HBM GB/s % of peak"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = {
+    "scan": ["selective_state_space_conv1d_gb300/csrc/scan_prefill.cu",
+             "selective_state_space_conv1d_gb300/csrc/device_math.cuh"],
+    "conv": ["selective_state_space_conv1d_gb300/csrc/conv1d.cu",
+             "selective_state_space_conv1d_gb300/csrc/device_math.cuh"],
+    "step": ["selective_state_space_conv1d_gb300/csrc/ssm_step.cu",
+             "selective_state_space_conv1d_gb300/csrc/device_math.cuh"],
+}
+
+
+# ---------------------------------------------------------------- utilities --
+
+def source_hash(kind: str) -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES[kind]:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(kind: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it is for this source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(p) as f:
+            rec = json.load(f)[f"{kind}:{workload}"]
+    except Exception:
+        return None
+    if rec.get("source_hash") != source_hash(kind):
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_events(torch, n, external):
+    kw = {"enable_timing": True}
+    if external:
+        kw["external"] = True
+    return [torch.cuda.Event(**kw) for _ in range(n)]
+
+
+def external_events_supported(torch):
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        return True
+    except TypeError:
+        return False
+
+
+def capture(torch, fn):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    return g
+
+
+# ------------------------------------------------------------- workloads ----
+
+class PrefillSet:
+    """Device buffers of one prefill step (conv then scan), all resident in HBM."""
+
+    def __init__(self, torch, host, params, dtype, device):
+        td = torch.float32 if dtype == "f32" else torch.bfloat16
+        dev = lambda a, d=td: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device).to(d)
+        self.x, self.dt, self.z = dev(host["x"]), dev(host["dt"]), dev(host["z"])
+        self.B, self.C = dev(host["B"]), dev(host["C"])
+        self.u = torch.empty_like(self.x)
+        self.y = torch.empty(self.x.shape, device=device, dtype=torch.float32)
+        Bsz, T, Di = self.x.shape
+        N = self.B.shape[2]
+        K = params["conv_w"].shape[1]
+        self.conv_out = torch.empty((Bsz, Di, K), device=device)
+        self.ssm_out = torch.empty((Bsz, Di, N), device=device)
+        self.p = {k: dev(v, torch.float32) for k, v in params.items()}
+
+    @classmethod
+    def from_device(cls, torch, shape, N, params, dtype, device, seed):
+        """Large workloads: same distributions drawn with torch's device RNG."""
+        from selective_state_space_conv1d_gb300 import synth
+
+        self = cls.__new__(cls)
+        td = torch.float32 if dtype == "f32" else torch.bfloat16
+        Bsz, T, Di = shape
+        self.x = synth.torch_normal(shape, 1.0, seed + 1, device, td)
+        self.dt = synth.torch_normal(shape, 0.1, seed + 2, device, td)
+        self.z = synth.torch_normal(shape, 1.0, seed + 3, device, td)
+        self.B = synth.torch_normal((Bsz, T, N), 1.0, seed + 4, device, td)
+        self.C = synth.torch_normal((Bsz, T, N), 1.0, seed + 5, device, td)
+        self.u = torch.empty_like(self.x)
+        self.y = torch.empty(shape, device=device, dtype=torch.float32)
+        K = params["conv_w"].shape[1]
+        self.conv_out = torch.empty((Bsz, Di, K), device=device)
+        self.ssm_out = torch.empty((Bsz, Di, N), device=device)
+        self.p = {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(device)
+                  for k, v in params.items()}
+        return self
+
+    def conv(self, m):
+        m.mamba_conv1d_silu_prefill(self.u, self.x, self.p["conv_w"], self.p["conv_b"], None,
+                                    self.conv_out)
+
+    def scan(self, m):
+        m.mamba_selective_scan_prefill(self.y, self.u, self.dt, self.B, self.C, self.p["A_log"],
+                                       self.p["D"], self.p["dt_bias"], self.z, None, self.ssm_out)
+
+    def bytes_per_step(self):
+        """Algorithmic HBM bytes of (conv, scan): every input read once, every output written once."""
+        es = self.x.element_size()
+        Bsz, T, Di = self.x.shape
+        N = self.B.shape[2]
+        K = self.conv_out.shape[2]
+        conv = Bsz * T * Di * 2 * es + Bsz * Di * K * 4 + Di * (K + 1) * 4
+        scan = (Bsz * T * Di * (3 * es + self.y.element_size()) + Bsz * T * N * 2 * es
+                + Bsz * Di * N * 4 + Di * (N + 2) * 4)
+        return conv, scan
+
+
+def timed_graph_run(torch, m, sets, n_steps, per_graph, ext, clocks=None, dist=None):
+    """Run n_steps prefill steps as replays of captured graphs; returns timings."""
+    per_graph = max(1, min(per_graph, n_steps))
+
+    def build(nsteps, offset):
+        evs = make_events(torch, 2 * nsteps + 1, ext) if ext else None
+
+        def body():
+            for i in range(nsteps):
+                s = sets[(offset + i) % len(sets)]
+                if evs:
+                    evs[2 * i].record()
+                s.conv(m)
+                if evs:
+                    evs[2 * i + 1].record()
+                s.scan(m)
+            if evs:
+                evs[2 * nsteps].record()
+        return capture(torch, body), evs
+
+    g_main, ev_main = build(per_graph, 0)
+    reps, tail = divmod(n_steps, per_graph)
+    g_tail, ev_tail = build(tail, 0) if tail else (None, None)
+    g_main.replay()
+    if g_tail:
+        g_tail.replay()
+    torch.cuda.synchronize()
+
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+    start.record()
+    for _ in range(reps):
+        g_main.replay()
+    if g_tail:
+        g_tail.replay()
+    end.record()
+    torch.cuda.synchronize()
+    ck = clocks.stop() if clocks else None
+    if dist is not None:
+        dist.barrier()
+    total_ms = start.elapsed_time(end)
+    conv_ms, scan_ms = [], []
+    if ev_main:
+        for i in range(per_graph):
+            conv_ms.append(ev_main[2 * i].elapsed_time(ev_main[2 * i + 1]))
+            scan_ms.append(ev_main[2 * i + 1].elapsed_time(ev_main[2 * i + 2]))
+    return total_ms, conv_ms, scan_ms, ck
+
+
+def kernel_only_times(torch, m, sets, n, which):
+    """Fallback when graphs cannot hold timing events: time graphs of one kernel kind."""
+    def body():
+        for i in range(n):
+            getattr(sets[i % len(sets)], which)(m)
+    g = capture(torch, body)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) / n] * n
+
+
+def roofline(bytes_per_launch, ms, peak, peak_src, traffic):
+    gbs = bytes_per_launch / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(gbs / peak, 4), "traffic": traffic, "peak_source": peak_src,
+            "algorithmic_bytes_per_launch": int(bytes_per_launch), "avg_launch_ms": round(ms, 6)}
+
+
+def run_prefill(torch, m, synth, wl_index, steps, warmup, ext, device, dist, clocks, host_inputs=True):
+    wl = synth.WORKLOADS[wl_index]
+    Bsz, T, Di, N, K = wl.batch, wl.seqlen, wl.d_inner, wl.d_state, wl.d_conv
+    params = synth.mixer_params(wl.seed, Di, N, K)
+    props = torch.cuda.get_device_properties(device)
+    if host_inputs:
+        host = synth.prefill_inputs(wl.seed, Bsz, T, Di, N, wl.dtype, names=("x", "dt", "z", "B", "C"))
+        first = PrefillSet(torch, host, params, wl.dtype, device)
+    else:
+        host = None
+        first = PrefillSet.from_device(torch, (Bsz, T, Di), N, params, wl.dtype, device, wl.seed)
+    conv_b, scan_b = first.bytes_per_step()
+    set_bytes = conv_b + scan_b
+    l2 = getattr(props, "L2_cache_size", 126 * 2 ** 20)
+    n_sets = 1 if set_bytes > 3 * l2 else int(math.ceil(3 * l2 / set_bytes)) + 1
+    sets = [first]
+    for _ in range(n_sets - 1):
+        s = PrefillSet.__new__(PrefillSet)
+        s.__dict__.update({k: (v.clone() if hasattr(v, "clone") else v) for k, v in first.__dict__.items()})
+        s.p = first.p
+        sets.append(s)
+    # warm-up steps (eager), then graphs
+    for i in range(max(warmup, 3)):
+        sets[i % n_sets].conv(m)
+        sets[i % n_sets].scan(m)
+    torch.cuda.synchronize()
+    total_ms, conv_ms, scan_ms, ck = timed_graph_run(torch, m, sets, steps, 100, ext, clocks, dist)
+    if not scan_ms:
+        conv_ms = kernel_only_times(torch, m, sets, 100, "conv")
+        scan_ms = kernel_only_times(torch, m, sets, 100, "scan")
+    l2_note = (f"inputs > 3x L2 ({set_bytes / 1e6:.0f} MB per step)" if n_sets == 1 else
+               f"rotating {n_sets} resident buffer sets ({n_sets * set_bytes / 1e6:.0f} MB > 3x the "
+               f"{l2 / 1e6:.0f} MB L2)")
+    return {
+        "wl": wl, "sets": sets, "host": host, "params": params, "total_ms": total_ms,
+        "ms_per_step": total_ms / steps, "conv_ms": float(np.mean(conv_ms)),
+        "scan_ms": float(np.mean(scan_ms)), "conv_bytes": conv_b, "scan_bytes": scan_b,
+        "tokens_per_step": Bsz * T, "clocks": ck, "l2_note": l2_note,
+    }
+
+
+def run_e2e(torch, m, res, steps, device):
+    """Same metric through the public API with pinned host buffers: every step
+    copies its inputs host->device and reads y and both final states back."""
+    wl, host = res["wl"], res["host"]
+    s = res["sets"][0]
+    pin = lambda a, like: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(like.dtype).pin_memory()
+    hin = {k: pin(host[k], getattr(s, k)) for k in ("x", "dt", "z", "B", "C")}
+    hy = torch.empty(s.y.shape, dtype=s.y.dtype).pin_memory()
+    hc = torch.empty(s.conv_out.shape).pin_memory()
+    hs = torch.empty(s.ssm_out.shape).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in hin.values())
+    d2h = hy.numel() * hy.element_size() + hc.numel() * 4 + hs.numel() * 4
+
+    def step():
+        for k, t in hin.items():
+            getattr(s, k).copy_(t, non_blocking=True)
+        s.conv(m)
+        s.scan(m)
+        hy.copy_(s.y, non_blocking=True)
+        hc.copy_(s.conv_out, non_blocking=True)
+        hs.copy_(s.ssm_out, non_blocking=True)
+
+    per = 20
+    g = capture(torch, lambda: [step() for _ in range(per)])
+    g.replay()
+    torch.cuda.synchronize()
+    reps = max(1, steps // per)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (reps * per)
+    return {"value": round(res["tokens_per_step"] / (ms * 1e-3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": round(ms, 5), "api": "C ABI via the Python binding, pinned host buffers"}
+
+
+def run_decode(torch, m, synth, device, peak, peak_src, ext, n_steps=256):
+    """24-layer T=1 decode at batch 128 over a persistent state, graph-replayed."""
+    wl = synth.WORKLOADS[2]
+    L, Bsz, Di, N, K = wl.n_layers, wl.batch, wl.d_inner, wl.d_state, wl.d_conv
+    conv_h, ssm_h = synth.seeded_states(wl.seed, L, Bsz, Di, N, K)
+    conv = torch.from_numpy(conv_h).to(device)
+    ssm = torch.from_numpy(ssm_h).to(device)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+    params = [{k: dev(v) for k, v in synth.mixer_params(wl.seed, Di, N, K, layer=l).items()}
+              for l in range(L)]
+    shape = (n_steps, L, Bsz, Di)
+    x = synth.torch_normal(shape, 1.0, wl.seed + 11, device)
+    z = synth.torch_normal(shape, 1.0, wl.seed + 12, device)
+    dt = synth.torch_normal(shape, 0.1, wl.seed + 13, device)
+    Bm = synth.torch_normal((n_steps, L, Bsz, N), 1.0, wl.seed + 14, device)
+    Cm = synth.torch_normal((n_steps, L, Bsz, N), 1.0, wl.seed + 15, device)
+    u = torch.empty((L, Bsz, Di), device=device)
+    y = torch.empty((L, Bsz, Di), device=device)
+
+    def layer_step(s, l, evs=None, base=0):
+        p = params[l]
+        if evs:
+            evs[base].record()
+        m.mamba_conv1d_silu_step(u[l], x[s, l], conv, l, p["conv_w"], p["conv_b"])
+        if evs:
+            evs[base + 1].record()
+        m.mamba_ssm_step_batched(y[l], u[l], dt[s, l], Bm[s, l], Cm[s, l], ssm, l, p["A_log"],
+                                 p["D"], p["dt_bias"], z[s, l])
+        if evs:
+            evs[base + 2].record()
+
+    for s in range(3):  # warm-up steps
+        for l in range(L):
+            layer_step(s, l)
+    torch.cuda.synchronize()
+    g = capture(torch, lambda: [layer_step(s, l) for s in range(n_steps) for l in range(L)])
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 4
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms_step = a.elapsed_time(b) / (reps * n_steps)
+    # per-kernel durations from an instrumented replay of 8 steps
+    conv_ms, step_ms = [], []
+    if ext:
+        ns = 8
+        evs = make_events(torch, 3 * ns * L, ext)
+        gi = capture(torch, lambda: [layer_step(s, l, evs, 3 * (s * L + l)) for s in range(ns) for l in range(L)])
+        gi.replay()
+        torch.cuda.synchronize()
+        for i in range(ns * L):
+            conv_ms.append(evs[3 * i].elapsed_time(evs[3 * i + 1]))
+            step_ms.append(evs[3 * i + 1].elapsed_time(evs[3 * i + 2]))
+    rows = Bsz * Di
+    step_bytes = rows * (2 * 4 * N + 5 * 4) + Bsz * N * 2 * 4 + Di * (N + 2) * 4
+    conv_bytes = rows * (2 * 4 * K + 2 * 4) + Di * (K + 1) * 4
+    out = {
+        "workload": wl.name, "value": round(1e3 / ms_step, 2), "unit": "steps/s",
+        "ms_per_step": round(ms_step, 5),
+        "layer_token_updates_per_s": round(1e3 / ms_step * L * Bsz, 1),
+        "algorithmic_bytes_per_step": int(L * (step_bytes + conv_bytes)),
+        "hbm_gbs_per_step": round(L * (step_bytes + conv_bytes) / (ms_step * 1e-3) / 1e9, 1),
+        "config": {"n_layers": L, "batch": Bsz, "d_inner": Di, "d_state": N, "d_conv": K,
+                   "steps_per_replay": n_steps, "launch": "CUDA graph of 256 x 24 x 2 kernels",
+                   "l2": f"state {L * rows * (N + K) * 4 / 1e6:.0f} MB > L2"},
+        "gpu_launches": 2 * L * n_steps * reps,
+    }
+    out["frac_of_hbm_peak"] = round(out["hbm_gbs_per_step"] / peak, 4)
+    if step_ms:
+        out["roofline"] = roofline(step_bytes, float(np.mean(step_ms)), peak, peak_src,
+                                   ncu_traffic("step", wl.name))
+        out["conv_step_roofline"] = roofline(conv_bytes, float(np.mean(conv_ms)), peak, peak_src,
+                                             ncu_traffic("conv", wl.name + "-step"))
+    return out
+
+
+# ----------------------------------------------------------- CPU oracle arm --
+
+def oracle_prefill_sample(synth, wl_index, n_channels, nthreads):
+    """Run the f64 oracle (conv then scan) on the first n_channels channels of
+    the workload; returns (seconds, tokens-equivalent processed)."""
+    import oracle
+
+    wl = synth.WORKLOADS[wl_index]
+    Bsz, T, Di, N, K = wl.batch, wl.seqlen, wl.d_inner, wl.d_state, wl.d_conv
+    params = synth.mixer_params(wl.seed, Di, N, K)
+    host = synth.prefill_inputs(wl.seed, Bsz, T, Di, N, wl.dtype, names=("x", "dt", "z", "B", "C"))
+    sel = slice(0, n_channels)
+    x, dt, z = (np.ascontiguousarray(host[k][:, :, sel], np.float64) for k in ("x", "dt", "z"))
+    Bm, Cm = host["B"].astype(np.float64), host["C"].astype(np.float64)
+    p = {k: np.ascontiguousarray(v[sel], np.float64) for k, v in params.items()}
+    t0 = time.perf_counter()
+    u, _ = oracle.conv1d_silu_prefill(x, p["conv_w"], p["conv_b"], None, nthreads=nthreads)
+    oracle.selective_scan_prefill(u, dt, Bm, Cm, p["A_log"], p["D"], p["dt_bias"], z, None,
+                                  nthreads=nthreads)
+    dtm = time.perf_counter() - t0
+    return dtm, Bsz * T * n_channels / Di
+
+
+def cpu_baseline(synth, budget_s=10.0):
+    import oracle
+
+    nthreads = oracle.default_threads()
+    wl = synth.WORKLOADS[1]
+    total_s, total_tok, reps = 0.0, 0.0, 0
+    while total_s < budget_s:
+        s, tok = oracle_prefill_sample(synth, 1, wl.d_inner, nthreads)
+        total_s += s
+        total_tok += tok
+        reps += 1
+    return {"value": round(total_tok / total_s, 1), "unit": "tokens/s", "cores": nthreads,
+            "kind": "oracle",
+            "sample": f"{reps} full passes of the 130m-layer prefill (1x2048x1536, d_state 16): "
+                      f"f64 conv+scan, {total_s:.1f} s of wall time on {nthreads} threads"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: the f64 CPU oracle on this host's cores."""
+    from selective_state_space_conv1d_gb300 import synth
+    import oracle
+
+    if rank != 0:
+        return
+    nthreads = oracle.default_threads()
+    wl = synth.WORKLOADS[1]
+    n_steps = args.steps + args.warmup
+    # size the per-step sample so the whole run stays within ~2 minutes
+    one_s, _ = oracle_prefill_sample(synth, 1, 16, nthreads)
+    per_ch = one_s / 16
+    n_ch = int(max(1, min(wl.d_inner, (120.0 / max(n_steps, 1)) / max(per_ch, 1e-9))))
+    for _ in range(args.warmup):
+        oracle_prefill_sample(synth, 1, n_ch, nthreads)
+    tot_s, tot_tok = 0.0, 0.0
+    for _ in range(args.steps):
+        s, tok = oracle_prefill_sample(synth, 1, n_ch, nthreads)
+        tot_s += s
+        tot_tok += tok
+    value = tot_tok / tot_s
+    sample = (f"first {n_ch} of {wl.d_inner} channels of the 130m-layer prefill per step "
+              f"(1x2048, d_state 16), f64 conv+scan")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / max(args.steps, 1), 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "batch": wl.batch, "seq_len": wl.seqlen,
+                   "d_inner": wl.d_inner, "d_state": wl.d_state, "d_conv": wl.d_conv},
+        "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": nthreads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-extra", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+
+    import selective_state_space_conv1d_gb300 as m
+    from selective_state_space_conv1d_gb300 import synth
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as td
+
+        td.init_process_group("nccl", device_id=device)
+        dist = td
+    m.load()
+    ext = external_events_supported(torch)
+    peak, peak_src = hbm_peak()
+    clocks = ClockSampler(local_rank)
+
+    res = run_prefill(torch, m, synth, 1, args.steps, args.warmup, ext, device, dist, clocks)
+    total_ms = res["total_ms"]
+    if dist is not None:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * res["tokens_per_step"] * args.steps / (total_ms * 1e-3)
+    scan_roof = roofline(res["scan_bytes"], res["scan_ms"], peak, peak_src,
+                         ncu_traffic("scan", res["wl"].name))
+    conv_roof = roofline(res["conv_bytes"], res["conv_ms"], peak, peak_src,
+                         ncu_traffic("conv", res["wl"].name))
+    step_gbs = (res["conv_bytes"] + res["scan_bytes"]) / (ms_step * 1e-3) / 1e9
+
+    extra = {}
+    if not args.no_extra:
+        extra["decode_130m_b128_l24"] = run_decode(torch, m, synth, device, peak, peak_src, ext)
+        r3 = run_prefill(torch, m, synth, 3, 50, 3, ext, device, None, None, host_inputs=False)
+        extra["prefill_2p8b_bf16"] = {
+            "workload": r3["wl"].name, "value": round(r3["tokens_per_step"] / (r3["ms_per_step"] * 1e-3), 1),
+            "unit": "tokens/s", "ms_per_step": round(r3["ms_per_step"], 5),
+            "hbm_gbs_per_step": round((r3["conv_bytes"] + r3["scan_bytes"]) / (r3["ms_per_step"] * 1e-3) / 1e9, 1),
+            "roofline": roofline(r3["scan_bytes"], r3["scan_ms"], peak, peak_src,
+                                 ncu_traffic("scan", r3["wl"].name)),
+            "conv_roofline": roofline(r3["conv_bytes"], r3["conv_ms"], peak, peak_src,
+                                      ncu_traffic("conv", r3["wl"].name)),
+            "config": {"batch": 8, "seq_len": 4096, "d_inner": 5120, "d_state": 16, "d_conv": 4,
+                       "storage": "bf16 x/u/dt/z/B/C, f32 y/params/state", "l2": r3["l2_note"],
+                       "inputs": "torch device RNG, same distributions"},
+        }
+        del r3
+
+    e2e = run_e2e(torch, m, res, min(args.steps, 400), device)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(synth)
+
+    if rank == 0:
+        wl = res["wl"]
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded Philox inputs with the tiny-mixer distributions)",
+            "config": {"workload": wl.name, "batch": wl.batch, "seq_len": wl.seqlen,
+                       "d_inner": wl.d_inner, "d_state": wl.d_state, "d_conv": wl.d_conv,
+                       "step": "conv1d+SiLU prefill then selective-scan prefill (2 launches)",
+                       "parallelism": f"replicas x{world}", "l2": res["l2_note"],
+                       "launch": "CUDA graph replays of 100 steps"},
+            "hbm_gbs_per_step": round(step_gbs, 1),
+            "roofline": scan_roof,
+            "conv_roofline": conv_roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": res["clocks"],
+            "extra": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * mamba_ssm.h - C ABI of the GB300-native (sm_103a) Mamba-1 selective-SSM
+ * mixer core: causal depthwise conv1d + SiLU, the selective scan with SiLU(z)
+ * gate, and the batched T=1 decode steps on a persistent per-layer state.
+ *
+ * What is computed (Mamba-1, as the mamba-rs GPU inference engine runs it):
+ *
+ *   conv:  s = [conv_state[b][c][1..K-1], x[b][0..T-1][c]]
+ *          pre_t = bias[c] + sum_{k<K} w[c][k] * s[t+k]     (w[c][K-1] meets x_t)
+ *          u_t   = pre_t * sigmoid(pre_t)                    (SiLU)
+ *          conv_state' = last K entries of [conv_state[b][c][0..K-1], x[b][..][c]]
+ *   scan:  A = -exp(A_log),  delta_t = softplus(dt_t + dt_bias)
+ *          h_t = exp(delta_t A) (.) h_{t-1} + delta_t B_t u_t
+ *          y_t = C_t . h_t + D u_t,   out_t = y_t * SiLU(z_t)   (no gate if z == NULL)
+ *
+ * Sources (docs.rs source views of the `mamba-rs` crate):
+ *   - mamba-rs 0.5.1 src/mamba_ssm/gpu/inference.rs: `GpuInferenceState` (state
+ *     layout [n_layers][batch*d_inner*d_conv] / [n_layers][batch*d_inner*d_state],
+ *     f32, full d_conv-slot shift register; `conv_offset` / `ssm_offset`),
+ *     `GpuMambaInference::new` (A = -exp(A_log)), the f32 step chain F4-F10
+ *     and the mixed step chain (conv1d step with fused SiLU; SSM step with fused
+ *     gate; state stays f32 under bf16 activations; d_state <= 64 guard).
+ *   - mamba-rs 0.6.4 src/mamba_ssm/gpu/prefill.rs: `gpu_forward_inference_prefill`
+ *     (prefill builds on the persistent state, it does not zero it),
+ *     `prefill_body` F4a (conv over all T with fused SiLU, strided x lane),
+ *     F4c (softplus), F4d (scan, gate fused into the y store, strided gate and
+ *     B/C reads).
+ *
+ * Conventions (every entry point):
+ *   - Status: 0 (MAMBA_OK) or a negative MAMBA_ERR_* code.  On error nothing was
+ *     launched and mamba_last_error() (thread-local) says why.
+ *   - Arguments are checked on the host before any work: NULL required
+ *     pointers, negative sizes, unsupported d_state / d_conv / dtypes, strides
+ *     smaller than a row, 64-bit extent overflow and overlapping buffers.
+ *   - Memory: every pointer is a DEVICE pointer owned by the caller.  The
+ *     library allocates, frees and synchronises nothing; every call only
+ *     enqueues kernels on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns.  Results are ready when the stream reaches them.
+ *   - Layout: activations are row-major [batch][T][channels] with the channels
+ *     contiguous; element (b, t, c) lives at base + (b*T + t)*ld + c, so `ld`
+ *     (elements, >= channels) lets a caller pass a column slice of a wider
+ *     buffer (e.g. the x or z half of an in_proj output, or the B / C columns
+ *     of an x_proj output).  Parameters and states are f32.
+ *   - Dtypes: MAMBA_F32 or MAMBA_BF16 storage; all arithmetic is f32; a bf16
+ *     output is rounded once, to nearest even.
+ *   - Optional pointers: bias, D, dt_bias may be NULL (treated as 0); z may be
+ *     NULL (no gate); state_in may be NULL (zero state); state_out may be NULL
+ *     (final state discarded).  state_out may equal state_in (in place); no
+ *     other output may overlap any input or output.
+ *   - The device must be compute capability 10.3 (GB300, sm_103a).
+ */
+#ifndef MAMBA_SSM_H
+#define MAMBA_SSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MAMBA_API __attribute__((visibility("default")))
+#else
+#define MAMBA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MAMBA_OK 0
+#define MAMBA_ERR_INVALID_ARG (-1) /* bad pointer, size, stride, dtype or aliasing */
+#define MAMBA_ERR_UNSUPPORTED (-2) /* valid but not built: d_state, d_conv, device */
+#define MAMBA_ERR_CUDA (-3)        /* a CUDA runtime call or launch failed */
+
+#define MAMBA_F32 0
+#define MAMBA_BF16 1
+
+#define MAMBA_MAX_D_CONV 8 /* d_conv in 1..8 */
+/* d_state in {1, 2, 4, 8, 16, 32, 64} (mirrors the d_state <= 64 register
+ * contract of the fused step kernel in inference.rs, mixed step F8+F9+F10). */
+#define MAMBA_MAX_D_STATE 64
+
+/*
+ * Causal depthwise conv1d + SiLU over T tokens, continuing from a conv state.
+ * (prefill.rs `prefill_body` F4a, the conv1d burn-in launch with fused SiLU;
+ *  inference.rs `GpuInferenceState`: d_conv slots, slot 0 oldest.)
+ *
+ *   u              [B][T][Di] at ld_u (elements), dtype act_dtype      (out)
+ *   x              [B][T][Di] at ld_x, dtype act_dtype                 (in)
+ *   conv_state_in  [B][Di][K] f32, or NULL for a zero state            (in)
+ *   conv_state_out [B][Di][K] f32, or NULL; may equal conv_state_in    (out)
+ *   w              [Di][K] f32 taps; w[c][K-1] multiplies the newest x (in)
+ *   bias           [Di] f32 or NULL                                   (in)
+ * T == 0 copies conv_state_in to conv_state_out (zeros if in is NULL).
+ * Errors: MAMBA_ERR_INVALID_ARG for NULL u/x/w (when T > 0), ld < Di,
+ * u overlapping x; MAMBA_ERR_UNSUPPORTED for K outside 1..8.
+ */
+MAMBA_API int mamba_conv1d_silu_prefill(void* u, int64_t ld_u, const void* x, int64_t ld_x,
+                              int act_dtype, const float* conv_state_in,
+                              float* conv_state_out, const float* w, const float* bias,
+                              int64_t B, int64_t T, int64_t Di, int64_t K, void* stream);
+
+/*
+ * One T=1 conv1d + SiLU step, in place on the `layer` slab of a persistent
+ * conv state laid out [n_layers][B][Di][K] f32 (slab offset layer*B*Di*K).
+ * (inference.rs step chain F4 + F4b, fused as in the mixed step's
+ *  conv1d step with epilogue SiLU.)
+ *
+ *   u          [B][Di] dense, dtype act_dtype (out)
+ *   x          [B][Di] dense, dtype act_dtype (in)
+ *   conv_state base of [n_layers][B][Di][K] f32 (in/out, only slab `layer`)
+ *   w, bias    as for the prefill
+ * Errors: MAMBA_ERR_INVALID_ARG for layer outside [0, n_layers) or bad
+ * pointers / overlap; MAMBA_ERR_UNSUPPORTED for K outside 1..8.
+ */
+MAMBA_API int mamba_conv1d_silu_step(void* u, const void* x, int act_dtype, float* conv_state,
+                           int64_t layer, int64_t n_layers, const float* w,
+                           const float* bias, int64_t B, int64_t Di, int64_t K,
+                           void* stream);
+
+/*
+ * Selective scan over T tokens with SiLU(z) gate, continuing from a state and
+ * returning the state after the last token, so prefill(T1) then prefill(T2)
+ * equals prefill(T1 + T2) up to rounding.
+ * (prefill.rs `gpu_forward_inference_prefill` "do NOT zero, we build on top";
+ *  `prefill_body` F4c softplus and F4d scan with the gate fused into the y
+ *  store; inference.rs `GpuMambaInference::new` exp_negate.)
+ *
+ *   y      [B][T][Di] at ld_y, dtype y_dtype                       (out)
+ *   u      [B][T][Di] at ld_u, dtype in_dtype                      (in)
+ *   dt     [B][T][Di] at ld_dt (pre-bias; delta = softplus(dt + dt_bias))
+ *   z      [B][T][Di] at ld_z, or NULL for no gate
+ *   Bm, Cm [B][T][N] at ld_B / ld_C (elements, >= N)
+ *   A_log  [Di][N] f32;  D, dt_bias [Di] f32 or NULL
+ *   ssm_state_in  [B][Di][N] f32 or NULL (zeros)
+ *   ssm_state_out [B][Di][N] f32 or NULL; may equal ssm_state_in
+ * T == 0 copies the state.  Long, narrow shapes (few batch*channel rows) are
+ * split along T inside each CTA; the split changes rounding only.
+ * Errors: MAMBA_ERR_INVALID_ARG for NULL required pointers, ld < row width,
+ * y overlapping an input; MAMBA_ERR_UNSUPPORTED for N not in {1,2,4,...,64}.
+ */
+MAMBA_API int mamba_selective_scan_prefill(void* y, int64_t ld_y, int y_dtype, const void* u,
+                                 int64_t ld_u, const void* dt, int64_t ld_dt,
+                                 const void* z, int64_t ld_z, const void* Bm, int64_t ld_B,
+                                 const void* Cm, int64_t ld_C, int in_dtype,
+                                 const float* A_log, const float* D, const float* dt_bias,
+                                 const float* ssm_state_in, float* ssm_state_out, int64_t B,
+                                 int64_t T, int64_t Di, int64_t N, void* stream);
+
+/*
+ * Batched T=1 SSM step with fused gate, in place on the `layer` slab of a
+ * persistent state laid out [n_layers][B][Di][N] f32 (offset layer*B*Di*N).
+ * (inference.rs step chain F9 + F10, fused as in the mixed step's
+ *  gather + SSM step + gate kernel; `GpuInferenceState::ssm_offset`.)
+ *
+ *   y      [B][Di] dense, dtype y_dtype (out)
+ *   u, dt  [B][Di] dense, dtype in_dtype; z [B][Di] or NULL
+ *   Bm, Cm [B][N] dense, dtype in_dtype
+ *   A_log  [Di][N] f32; D, dt_bias [Di] f32 or NULL
+ *   ssm_state base of [n_layers][B][Di][N] f32 (in/out, only slab `layer`)
+ * The per-token arithmetic is the one the prefill uses, in the same order, so
+ * one step equals a T=1 prefill bit for bit.
+ * Errors: as for the prefill, plus layer outside [0, n_layers).
+ */
+MAMBA_API int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const void* dt,
+                           const void* z, const void* Bm, const void* Cm, int in_dtype,
+                           const float* A_log, const float* D, const float* dt_bias,
+                           float* ssm_state, int64_t layer, int64_t n_layers, int64_t B,
+                           int64_t Di, int64_t N, void* stream);
+
+/* Thread-local description of the last error returned on this thread
+ * (empty string after a successful call).  Never NULL; owned by the library. */
+MAMBA_API const char* mamba_last_error(void);
+
+/* Library version string, e.g. "0.1.0". */
+MAMBA_API const char* mamba_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SSM_H */

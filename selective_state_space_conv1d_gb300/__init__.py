@@ -1,1 +1,30 @@
-"""GB300-native Mamba-1 selective-SSM mixer core (placeholder until the binding lands)."""
+"""GB300-native (sm_103a) Mamba-1 selective-SSM mixer core.
+
+Four C-ABI entry points (include/mamba_ssm.h), each a hand-written CUDA kernel:
+  mamba_conv1d_silu_prefill     causal depthwise conv1d + SiLU over T tokens
+  mamba_conv1d_silu_step        T=1 conv step on a [n_layers][B*Di*K] state
+  mamba_selective_scan_prefill  selective scan + SiLU(z) gate, state in/out
+  mamba_ssm_step_batched        T=1 SSM step on a [n_layers][B*Di*N] state
+This package is the thin Python binding (argument marshalling over ctypes);
+`synth` holds the seeded synthetic inputs used by the tests and the benchmark.
+"""
+from ._binding import (  # noqa: F401
+    ABI_SYMBOLS,
+    LIB_PATH,
+    MAMBA_BF16,
+    MAMBA_ERR_CUDA,
+    MAMBA_ERR_INVALID_ARG,
+    MAMBA_ERR_UNSUPPORTED,
+    MAMBA_F32,
+    MAMBA_OK,
+    MambaError,
+    load,
+    mamba_conv1d_silu_prefill,
+    mamba_conv1d_silu_step,
+    mamba_last_error,
+    mamba_selective_scan_prefill,
+    mamba_ssm_step_batched,
+    mamba_version,
+)
+
+__version__ = "0.1.0"

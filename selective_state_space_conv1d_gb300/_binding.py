@@ -1,0 +1,234 @@
+"""ctypes binding of libmamba_ssm.so (the C ABI in include/mamba_ssm.h).
+
+Argument marshalling only: shapes and strides are read off torch tensors and
+passed as plain pointers and sizes; every step of the computation runs in the
+library's CUDA kernels on the caller's current torch stream.  There is no CPU
+or PyTorch fallback: if the library is missing or the device is not a GB300,
+the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+MAMBA_OK = 0
+MAMBA_ERR_INVALID_ARG = -1
+MAMBA_ERR_UNSUPPORTED = -2
+MAMBA_ERR_CUDA = -3
+MAMBA_F32 = 0
+MAMBA_BF16 = 1
+
+LIB_PATH = _build.LIB_PATH
+
+# every exported entry point of include/mamba_ssm.h
+ABI_SYMBOLS = (
+    "mamba_conv1d_silu_prefill",
+    "mamba_conv1d_silu_step",
+    "mamba_selective_scan_prefill",
+    "mamba_ssm_step_batched",
+    "mamba_last_error",
+    "mamba_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MambaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[{status}] {message}")
+        self.status = status
+
+
+def load(path: str | None = None):
+    """Load libmamba_ssm.so (built in-tree by build.py) and declare its ABI."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build the CUDA library first "
+                "(python -m selective_state_space_conv1d_gb300.build, or __graft_entry__.build())")
+        lib = ctypes.CDLL(p)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.mamba_conv1d_silu_prefill.argtypes = [vp, i64, vp, i64, i32, vp, vp, vp, vp, i64, i64, i64, i64, vp]
+        lib.mamba_conv1d_silu_step.argtypes = [vp, vp, i32, vp, i64, i64, vp, vp, i64, i64, i64, vp]
+        lib.mamba_selective_scan_prefill.argtypes = (
+            [vp, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32]
+            + [vp] * 5 + [i64, i64, i64, i64, vp])
+        lib.mamba_ssm_step_batched.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp]
+        for f in ("mamba_conv1d_silu_prefill", "mamba_conv1d_silu_step",
+                  "mamba_selective_scan_prefill", "mamba_ssm_step_batched"):
+            getattr(lib, f).restype = ctypes.c_int
+        lib.mamba_last_error.argtypes = []
+        lib.mamba_last_error.restype = ctypes.c_char_p
+        lib.mamba_version.argtypes = []
+        lib.mamba_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def mamba_last_error() -> str:
+    return load().mamba_last_error().decode()
+
+
+def mamba_version() -> str:
+    return load().mamba_version().decode()
+
+
+def _check(status: int):
+    if status != MAMBA_OK:
+        raise MambaError(status, mamba_last_error())
+
+
+# ------------------------------------------------------------------ helpers --
+
+def _dtype_code(t):
+    import torch
+
+    if t.dtype == torch.float32:
+        return MAMBA_F32
+    if t.dtype == torch.bfloat16:
+        return MAMBA_BF16
+    raise TypeError(f"unsupported storage dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream, like):
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream(like.device).cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _rows_ld(t, name):
+    """Row stride `ld` of a [B, T, C] tensor laid out as (b*T + t)*ld + c."""
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be 3-D [batch, T, channels], got {tuple(t.shape)}")
+    Bsz, T, C = t.shape
+    if C > 1 and t.stride(2) != 1:
+        raise ValueError(f"{name}: channels must be contiguous (stride {t.stride(2)})")
+    if T > 1:
+        ld = t.stride(1)
+        if Bsz > 1 and t.stride(0) != T * ld:
+            raise ValueError(f"{name}: batch stride {t.stride(0)} != T * row stride {T * ld}")
+    elif Bsz > 1:
+        ld = t.stride(0)
+    else:
+        ld = C
+    return ld
+
+
+def _f32_param(t, name, shape=None):
+    import torch
+
+    if t is None:
+        return None
+    if t.dtype != torch.float32 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous float32 tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+# ---------------------------------------------------------------- entry points --
+
+def mamba_conv1d_silu_prefill(u, x, w, bias=None, conv_state_in=None, conv_state_out=None,
+                              *, stream=None):
+    """Causal depthwise conv1d + SiLU over T tokens (u, x: [B, T, Di]; w: [Di, K])."""
+    Bsz, T, Di = x.shape
+    K = w.shape[1]
+    _f32_param(w, "w", (Di, K))
+    _f32_param(bias, "bias", (Di,))
+    _f32_param(conv_state_in, "conv_state_in", (Bsz, Di, K))
+    _f32_param(conv_state_out, "conv_state_out", (Bsz, Di, K))
+    if tuple(u.shape) != (Bsz, T, Di) or u.dtype != x.dtype:
+        raise ValueError("u must match x in shape and dtype")
+    _check(load().mamba_conv1d_silu_prefill(
+        _ptr(u), _rows_ld(u, "u"), _ptr(x), _rows_ld(x, "x"), _dtype_code(x),
+        _ptr(conv_state_in), _ptr(conv_state_out), _ptr(w), _ptr(bias),
+        Bsz, T, Di, K, _stream(stream, x)))
+
+
+def mamba_conv1d_silu_step(u, x, conv_state, layer, w, bias=None, *, stream=None):
+    """One T=1 conv step on slab `layer` of conv_state [L, B, Di, K] (u, x: [B, Di])."""
+    Bsz, Di = x.shape
+    K = w.shape[1]
+    if conv_state.dim() != 4 or tuple(conv_state.shape[1:]) != (Bsz, Di, K) or not conv_state.is_contiguous():
+        raise ValueError("conv_state must be a contiguous [n_layers, B, Di, K] tensor")
+    _f32_param(conv_state, "conv_state")
+    _f32_param(w, "w", (Di, K))
+    _f32_param(bias, "bias", (Di,))
+    if not (x.is_contiguous() and u.is_contiguous()) or tuple(u.shape) != (Bsz, Di) or u.dtype != x.dtype:
+        raise ValueError("u and x must be contiguous [B, Di] tensors of one dtype")
+    _check(load().mamba_conv1d_silu_step(
+        _ptr(u), _ptr(x), _dtype_code(x), _ptr(conv_state), int(layer), conv_state.shape[0],
+        _ptr(w), _ptr(bias), Bsz, Di, K, _stream(stream, x)))
+
+
+def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, z=None,
+                                 ssm_state_in=None, ssm_state_out=None, *, stream=None):
+    """Selective scan with SiLU(z) gate over T tokens, state in / state out.
+
+    y, u, dt, z: [B, T, Di] (row-strided views allowed); Bm, Cm: [B, T, N];
+    A_log: [Di, N]; D, dt_bias: [Di]; states: [B, Di, N] f32."""
+    Bsz, T, Di = u.shape
+    N = A_log.shape[1]
+    _f32_param(A_log, "A_log", (Di, N))
+    _f32_param(D, "D", (Di,))
+    _f32_param(dt_bias, "dt_bias", (Di,))
+    _f32_param(ssm_state_in, "ssm_state_in", (Bsz, Di, N))
+    _f32_param(ssm_state_out, "ssm_state_out", (Bsz, Di, N))
+    for t, nm in ((dt, "dt"), (z, "z"), (Bm, "Bm"), (Cm, "Cm")):
+        if t is not None and t.dtype != u.dtype:
+            raise ValueError(f"{nm} must have the dtype of u")
+    for t, nm in ((y, "y"), (dt, "dt"), (z, "z")):
+        if t is not None and tuple(t.shape) != (Bsz, T, Di):
+            raise ValueError(f"{nm} must be [B, T, Di]")
+    for t, nm in ((Bm, "Bm"), (Cm, "Cm")):
+        if tuple(t.shape) != (Bsz, T, N):
+            raise ValueError(f"{nm} must be [B, T, N]")
+    _check(load().mamba_selective_scan_prefill(
+        _ptr(y), _rows_ld(y, "y"), _dtype_code(y), _ptr(u), _rows_ld(u, "u"),
+        _ptr(dt), _rows_ld(dt, "dt"), _ptr(z), _rows_ld(z, "z") if z is not None else 0,
+        _ptr(Bm), _rows_ld(Bm, "Bm"), _ptr(Cm), _rows_ld(Cm, "Cm"), _dtype_code(u),
+        _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
+        Bsz, T, Di, N, _stream(stream, u)))
+
+
+def mamba_ssm_step_batched(y, u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt_bias=None,
+                           z=None, *, stream=None):
+    """One T=1 SSM step on slab `layer` of ssm_state [L, B, Di, N].
+
+    y, u, dt, z: contiguous [B, Di]; Bm, Cm: contiguous [B, N]."""
+    Bsz, Di = u.shape
+    N = A_log.shape[1]
+    if ssm_state.dim() != 4 or tuple(ssm_state.shape[1:]) != (Bsz, Di, N) or not ssm_state.is_contiguous():
+        raise ValueError("ssm_state must be a contiguous [n_layers, B, Di, N] tensor")
+    _f32_param(ssm_state, "ssm_state")
+    _f32_param(A_log, "A_log", (Di, N))
+    _f32_param(D, "D", (Di,))
+    _f32_param(dt_bias, "dt_bias", (Di,))
+    for t, nm, shp in ((y, "y", (Bsz, Di)), (dt, "dt", (Bsz, Di)), (z, "z", (Bsz, Di)),
+                       (Bm, "Bm", (Bsz, N)), (Cm, "Cm", (Bsz, N))):
+        if t is None:
+            continue
+        if tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous {shp} tensor")
+        if nm != "y" and t.dtype != u.dtype:
+            raise ValueError(f"{nm} must have the dtype of u")
+    _check(load().mamba_ssm_step_batched(
+        _ptr(y), _dtype_code(y), _ptr(u), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _dtype_code(u),
+        _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state), int(layer), ssm_state.shape[0],
+        Bsz, Di, N, _stream(stream, u)))

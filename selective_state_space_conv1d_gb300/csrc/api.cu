@@ -1,0 +1,342 @@
+// api.cu - the extern "C" entry points declared in include/mamba_ssm.h.
+//
+// Every entry point validates its arguments on the host (sizes, dtypes,
+// strides, 64-bit extents, pointer kinds, overlap), picks a kernel variant from
+// the shape, and enqueues it on the caller's stream.  Nothing is allocated,
+// freed or synchronised, so the calls are usable inside CUDA graph capture.
+// Errors follow the pages' Result<_, String> convention (mamba-rs prefill.rs
+// length checks before any work) as a status code plus a thread-local message.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include "../../include/mamba_ssm.h"
+#include "launch.h"
+
+namespace {
+
+thread_local char g_err[512] = {0};
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_err[0] = 0;
+  return MAMBA_OK;
+}
+
+// ---- device checks (cached per device ordinal) ------------------------------
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_state[kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
+mamba::DeviceInfo g_dev_info[kMaxDevices];
+int g_dev_cc[kMaxDevices];
+
+int current_device(mamba::DeviceInfo* info) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MAMBA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MAMBA_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  int st = g_dev_state[dev].load(std::memory_order_acquire);
+  if (st == 0) {
+    int major = 0, minor = 0, sms = 0, smem = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return fail(MAMBA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    g_dev_info[dev].sm_count = sms;
+    g_dev_info[dev].max_smem_optin = smem;
+    g_dev_cc[dev] = major * 10 + minor;
+    st = (major == 10 && minor == 3) ? 1 : 2;
+    g_dev_state[dev].store(st, std::memory_order_release);
+  }
+  if (st != 1)
+    return fail(MAMBA_ERR_UNSUPPORTED,
+                "this library is built for sm_103a (GB300); device %d is sm_%d", dev, g_dev_cc[dev]);
+  *info = g_dev_info[dev];
+  return MAMBA_OK;
+}
+
+// ---- argument checks --------------------------------------------------------
+constexpr int64_t kMaxExtent = int64_t(1) << 46;  // elements per dimension product
+
+struct Range {
+  const char* name;
+  uintptr_t lo, hi;  // [lo, hi) bytes; empty if lo == hi
+};
+
+// bytes spanned by rows*[cols] at stride ld (elements of es bytes)
+bool span_bytes(int64_t rows, int64_t cols, int64_t ld, int es, int64_t* out) {
+  if (rows <= 0 || cols <= 0) {
+    *out = 0;
+    return true;
+  }
+  if (rows > kMaxExtent || ld > kMaxExtent || cols > ld) return false;
+  const __int128 span = (__int128)(rows - 1) * ld + cols;
+  const __int128 bytes = span * es;
+  if (bytes > (__int128)(int64_t(1) << 60)) return false;
+  *out = (int64_t)bytes;
+  return true;
+}
+
+Range range_of(const char* name, const void* p, int64_t bytes) {
+  Range r{name, reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p)};
+  if (p && bytes > 0) r.hi = r.lo + (uintptr_t)bytes;
+  return r;
+}
+
+bool overlaps(const Range& a, const Range& b) {
+  if (a.lo == a.hi || b.lo == b.hi) return false;
+  return a.lo < b.hi && b.lo < a.hi;
+}
+
+// outputs must not overlap any other listed range
+int check_overlaps(const Range* outs, int n_out, const Range* ins, int n_in) {
+  for (int i = 0; i < n_out; ++i) {
+    for (int j = 0; j < n_in; ++j)
+      if (overlaps(outs[i], ins[j]))
+        return fail(MAMBA_ERR_INVALID_ARG, "%s overlaps %s", outs[i].name, ins[j].name);
+    for (int j = i + 1; j < n_out; ++j)
+      if (overlaps(outs[i], outs[j]))
+        return fail(MAMBA_ERR_INVALID_ARG, "%s overlaps %s", outs[i].name, outs[j].name);
+  }
+  return MAMBA_OK;
+}
+
+// the kernels dereference these: they must be memory this device can reach
+int check_pointer(const char* name, const void* p, int dev) {
+  if (!p) return MAMBA_OK;
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(MAMBA_ERR_INVALID_ARG, "%s: cudaPointerGetAttributes: %s", name, cudaGetErrorString(e));
+  }
+  if (at.type == cudaMemoryTypeUnregistered)
+    return fail(MAMBA_ERR_INVALID_ARG, "%s is not device-accessible memory (plain host pointer)", name);
+  if (at.type == cudaMemoryTypeDevice && at.device != dev)
+    return fail(MAMBA_ERR_INVALID_ARG, "%s lives on device %d, current device is %d", name, at.device, dev);
+  return MAMBA_OK;
+}
+
+int check_pointers(const Range* rs, int n, int dev) {
+  for (int i = 0; i < n; ++i) {
+    if (rs[i].lo == rs[i].hi) continue;
+    int rc = check_pointer(rs[i].name, reinterpret_cast<const void*>(rs[i].lo), dev);
+    if (rc) return rc;
+  }
+  return MAMBA_OK;
+}
+
+int check_dtype(const char* name, int dt) {
+  if (dt != MAMBA_F32 && dt != MAMBA_BF16)
+    return fail(MAMBA_ERR_INVALID_ARG, "%s: unknown dtype %d (expected MAMBA_F32=0 or MAMBA_BF16=1)", name, dt);
+  return MAMBA_OK;
+}
+
+int es_of(int dt) { return dt == MAMBA_BF16 ? 2 : 4; }
+
+// every size and every product of sizes used below stays under 2^46
+bool sizes_ok(int64_t a, int64_t b, int64_t c = 1) {
+  if (a > kMaxExtent || b > kMaxExtent || c > kMaxExtent) return false;
+  return (__int128)a * b * c <= (__int128)kMaxExtent;
+}
+
+bool valid_n(int64_t n) {
+  return n == 1 || n == 2 || n == 4 || n == 8 || n == 16 || n == 32 || n == 64;
+}
+
+int cuda_fail(const char* what, cudaError_t e) {
+  return fail(MAMBA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// T == 0: state_out <- state_in (or zeros)
+int copy_state(float* out, const float* in, int64_t count, cudaStream_t s) {
+  if (!out || count <= 0 || out == in) return ok();
+  cudaError_t e = in ? cudaMemcpyAsync(out, in, (size_t)count * 4, cudaMemcpyDeviceToDevice, s)
+                     : cudaMemsetAsync(out, 0, (size_t)count * 4, s);
+  if (e != cudaSuccess) return cuda_fail("state copy", e);
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mamba_last_error(void) { return g_err; }
+
+const char* mamba_version(void) { return "0.1.0"; }
+
+int mamba_conv1d_silu_prefill(void* u, int64_t ld_u, const void* x, int64_t ld_x, int act_dtype,
+                              const float* conv_state_in, float* conv_state_out, const float* w,
+                              const float* bias, int64_t B, int64_t T, int64_t Di, int64_t K,
+                              void* stream) {
+  int rc;
+  if ((rc = check_dtype("act_dtype", act_dtype))) return rc;
+  if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld T=%lld Di=%lld)", (long long)B, (long long)T, (long long)Di);
+  if (K < 1 || K > MAMBA_MAX_D_CONV) return fail(MAMBA_ERR_UNSUPPORTED, "d_conv=%lld not in 1..%d", (long long)K, MAMBA_MAX_D_CONV);
+  if (B == 0 || Di == 0) return ok();
+  if (!sizes_ok(B, T, Di) || !sizes_ok(B, Di, K)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!w) return fail(MAMBA_ERR_INVALID_ARG, "w is NULL");
+  if (T > 0 && (!u || !x)) return fail(MAMBA_ERR_INVALID_ARG, "u and x must not be NULL");
+  if (T > 0 && (ld_u < Di || ld_x < Di)) return fail(MAMBA_ERR_INVALID_ARG, "ld_u=%lld / ld_x=%lld smaller than Di=%lld", (long long)ld_u, (long long)ld_x, (long long)Di);
+  const int es = es_of(act_dtype);
+  int64_t bu = 0, bx = 0, bst = 0, bw = 0, bb = 0;
+  if (!span_bytes(B * T, Di, ld_u, es, &bu) || !span_bytes(B * T, Di, ld_x, es, &bx) ||
+      !span_bytes(B * Di, K, K, 4, &bst) || !span_bytes(Di, K, K, 4, &bw) || !span_bytes(1, Di, Di, 4, &bb))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (T == 0) bu = bx = 0;
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  Range ins[] = {range_of("x", x, bx), range_of("w", w, bw), range_of("bias", bias, bb),
+                 range_of("conv_state_in", conv_state_in, bst)};
+  const bool inplace = conv_state_out && conv_state_out == conv_state_in;
+  Range outs[] = {range_of("u", u, bu), range_of("conv_state_out", conv_state_out, bst)};
+  if ((rc = check_pointers(ins, 4, dev_id)) || (rc = check_pointers(outs, 2, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 2, ins, inplace ? 3 : 4))) return rc;
+  if (inplace && overlaps(outs[0], ins[3])) return fail(MAMBA_ERR_INVALID_ARG, "u overlaps conv_state_in");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) return copy_state(conv_state_out, conv_state_in, B * Di * K, s);
+  mamba::ConvPrefillArgs a{u, ld_u, x, ld_x, conv_state_in, conv_state_out, w, bias, B, T, Di, (int)K, act_dtype == MAMBA_BF16};
+  cudaError_t e = mamba::launch_conv1d_silu_prefill(a, dev, s);
+  if (e != cudaSuccess) return cuda_fail("conv1d_silu_prefill launch", e);
+  return ok();
+}
+
+int mamba_conv1d_silu_step(void* u, const void* x, int act_dtype, float* conv_state, int64_t layer,
+                           int64_t n_layers, const float* w, const float* bias, int64_t B, int64_t Di,
+                           int64_t K, void* stream) {
+  int rc;
+  if ((rc = check_dtype("act_dtype", act_dtype))) return rc;
+  if (B < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld Di=%lld)", (long long)B, (long long)Di);
+  if (K < 1 || K > MAMBA_MAX_D_CONV) return fail(MAMBA_ERR_UNSUPPORTED, "d_conv=%lld not in 1..%d", (long long)K, MAMBA_MAX_D_CONV);
+  if (n_layers < 1 || layer < 0 || layer >= n_layers) return fail(MAMBA_ERR_INVALID_ARG, "layer=%lld outside [0, n_layers=%lld)", (long long)layer, (long long)n_layers);
+  if (B == 0 || Di == 0) return ok();
+  if (!sizes_ok(B, Di, K) || !sizes_ok(n_layers, B * Di * K)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!u || !x || !conv_state || !w) return fail(MAMBA_ERR_INVALID_ARG, "u, x, conv_state and w must not be NULL");
+  const int es = es_of(act_dtype);
+  int64_t bact = 0, bst = 0, bw = 0, bb = 0, ball = 0;
+  if (!span_bytes(1, B * Di, B * Di, es, &bact) || !span_bytes(B * Di, K, K, 4, &bst) ||
+      !span_bytes(n_layers, B * Di * K, B * Di * K, 4, &ball) || !span_bytes(Di, K, K, 4, &bw) ||
+      !span_bytes(1, Di, Di, 4, &bb))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  float* slab = conv_state + layer * B * Di * K;
+  Range ins[] = {range_of("x", x, bact), range_of("w", w, bw), range_of("bias", bias, bb)};
+  Range outs[] = {range_of("u", u, bact), range_of("conv_state", slab, bst)};
+  if ((rc = check_pointers(ins, 3, dev_id)) || (rc = check_pointers(outs, 2, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 2, ins, 3))) return rc;
+  mamba::ConvStepArgs a{u, x, slab, w, bias, B, Di, (int)K, act_dtype == MAMBA_BF16};
+  cudaError_t e = mamba::launch_conv1d_silu_step(a, dev, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("conv1d_silu_step launch", e);
+  return ok();
+}
+
+int mamba_selective_scan_prefill(void* y, int64_t ld_y, int y_dtype, const void* u, int64_t ld_u,
+                                 const void* dt, int64_t ld_dt, const void* z, int64_t ld_z,
+                                 const void* Bm, int64_t ld_B, const void* Cm, int64_t ld_C,
+                                 int in_dtype, const float* A_log, const float* D,
+                                 const float* dt_bias, const float* ssm_state_in,
+                                 float* ssm_state_out, int64_t B, int64_t T, int64_t Di, int64_t N,
+                                 void* stream) {
+  int rc;
+  if ((rc = check_dtype("y_dtype", y_dtype)) || (rc = check_dtype("in_dtype", in_dtype))) return rc;
+  if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld T=%lld Di=%lld)", (long long)B, (long long)T, (long long)Di);
+  if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
+  if (B == 0 || Di == 0) return ok();
+  if (!sizes_ok(B, T, Di) || !sizes_ok(B, T, N) || !sizes_ok(B, Di, N)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!A_log) return fail(MAMBA_ERR_INVALID_ARG, "A_log is NULL");
+  if (T > 0) {
+    if (!y || !u || !dt || !Bm || !Cm) return fail(MAMBA_ERR_INVALID_ARG, "y, u, dt, Bm and Cm must not be NULL");
+    if (ld_y < Di || ld_u < Di || ld_dt < Di || (z && ld_z < Di))
+      return fail(MAMBA_ERR_INVALID_ARG, "an activation stride is smaller than Di=%lld", (long long)Di);
+    if (ld_B < N || ld_C < N) return fail(MAMBA_ERR_INVALID_ARG, "ld_B / ld_C smaller than d_state=%lld", (long long)N);
+  }
+  const int es = es_of(in_dtype), esy = es_of(y_dtype);
+  int64_t by = 0, bu = 0, bdt = 0, bz = 0, bB = 0, bC = 0, bA = 0, bv = 0, bst = 0;
+  if (!span_bytes(B * Di, N, N, 4, &bst) || !span_bytes(Di, N, N, 4, &bA) || !span_bytes(1, Di, Di, 4, &bv))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (T > 0 &&
+      (!span_bytes(B * T, Di, ld_y, esy, &by) || !span_bytes(B * T, Di, ld_u, es, &bu) ||
+       !span_bytes(B * T, Di, ld_dt, es, &bdt) || (z && !span_bytes(B * T, Di, ld_z, es, &bz)) ||
+       !span_bytes(B * T, N, ld_B, es, &bB) || !span_bytes(B * T, N, ld_C, es, &bC)))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  const bool inplace = ssm_state_out && ssm_state_out == ssm_state_in;
+  Range ins[] = {range_of("u", u, bu), range_of("dt", dt, bdt), range_of("z", z, bz),
+                 range_of("Bm", Bm, bB), range_of("Cm", Cm, bC), range_of("A_log", A_log, bA),
+                 range_of("D", D, bv), range_of("dt_bias", dt_bias, bv),
+                 range_of("ssm_state_in", ssm_state_in, bst)};
+  Range outs[] = {range_of("y", y, by), range_of("ssm_state_out", ssm_state_out, bst)};
+  if ((rc = check_pointers(ins, 9, dev_id)) || (rc = check_pointers(outs, 2, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 2, ins, inplace ? 8 : 9))) return rc;
+  if (inplace && overlaps(outs[0], ins[8])) return fail(MAMBA_ERR_INVALID_ARG, "y overlaps ssm_state_in");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) return copy_state(ssm_state_out, ssm_state_in, B * Di * N, s);
+  mamba::ScanArgs a{y, ld_y, y_dtype == MAMBA_BF16, u, ld_u, dt, ld_dt, z, ld_z, Bm, ld_B, Cm, ld_C,
+                    in_dtype == MAMBA_BF16, A_log, D, dt_bias, ssm_state_in, ssm_state_out,
+                    B, T, Di, (int)N};
+  const mamba::ScanPlan plan = mamba::plan_selective_scan(a, dev);
+  if (plan.smem_bytes > dev.max_smem_optin)
+    return fail(MAMBA_ERR_UNSUPPORTED, "scan plan needs %lld bytes of shared memory (device max %d)", (long long)plan.smem_bytes, dev.max_smem_optin);
+  cudaError_t e = mamba::launch_selective_scan_prefill(a, plan, dev, s);
+  if (e != cudaSuccess) return cuda_fail("selective_scan_prefill launch", e);
+  return ok();
+}
+
+int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const void* dt, const void* z,
+                           const void* Bm, const void* Cm, int in_dtype, const float* A_log,
+                           const float* D, const float* dt_bias, float* ssm_state, int64_t layer,
+                           int64_t n_layers, int64_t B, int64_t Di, int64_t N, void* stream) {
+  int rc;
+  if ((rc = check_dtype("y_dtype", y_dtype)) || (rc = check_dtype("in_dtype", in_dtype))) return rc;
+  if (B < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld Di=%lld)", (long long)B, (long long)Di);
+  if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
+  if (n_layers < 1 || layer < 0 || layer >= n_layers) return fail(MAMBA_ERR_INVALID_ARG, "layer=%lld outside [0, n_layers=%lld)", (long long)layer, (long long)n_layers);
+  if (B == 0 || Di == 0) return ok();
+  if (!sizes_ok(B, Di, N) || !sizes_ok(n_layers, B * Di * N)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!y || !u || !dt || !Bm || !Cm || !A_log || !ssm_state)
+    return fail(MAMBA_ERR_INVALID_ARG, "y, u, dt, Bm, Cm, A_log and ssm_state must not be NULL");
+  const int es = es_of(in_dtype), esy = es_of(y_dtype);
+  int64_t by = 0, bact = 0, bbc = 0, bA = 0, bv = 0, bst = 0, ball = 0;
+  if (!span_bytes(1, B * Di, B * Di, esy, &by) || !span_bytes(1, B * Di, B * Di, es, &bact) ||
+      !span_bytes(1, B * N, B * N, es, &bbc) || !span_bytes(Di, N, N, 4, &bA) ||
+      !span_bytes(1, Di, Di, 4, &bv) || !span_bytes(B * Di, N, N, 4, &bst) ||
+      !span_bytes(n_layers, B * Di * N, B * Di * N, 4, &ball))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  float* slab = ssm_state + layer * B * Di * N;
+  Range ins[] = {range_of("u", u, bact), range_of("dt", dt, bact), range_of("z", z, z ? bact : 0),
+                 range_of("Bm", Bm, bbc), range_of("Cm", Cm, bbc), range_of("A_log", A_log, bA),
+                 range_of("D", D, bv), range_of("dt_bias", dt_bias, bv)};
+  Range outs[] = {range_of("y", y, by), range_of("ssm_state", slab, bst)};
+  if ((rc = check_pointers(ins, 8, dev_id)) || (rc = check_pointers(outs, 2, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 2, ins, 8))) return rc;
+  mamba::SsmStepArgs a{y, y_dtype == MAMBA_BF16, u, dt, z, Bm, Cm, in_dtype == MAMBA_BF16,
+                       A_log, D, dt_bias, slab, B, Di, (int)N};
+  cudaError_t e = mamba::launch_ssm_step_batched(a, dev, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("ssm_step_batched launch", e);
+  return ok();
+}
+
+}  // extern "C"

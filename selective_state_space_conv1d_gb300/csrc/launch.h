@@ -1,0 +1,107 @@
+// launch.h - internal interface between the C-ABI layer (api.cu) and the
+// kernel translation units.  Arguments have already been validated; every
+// launcher only enqueues work on `stream` and returns cudaGetLastError().
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mamba {
+
+struct DeviceInfo {
+  int sm_count;
+  int max_smem_optin;  // bytes per block with opt-in
+};
+
+// ----------------------------------------------------------------- conv ----
+struct ConvPrefillArgs {
+  void* u;
+  int64_t ld_u;
+  const void* x;
+  int64_t ld_x;
+  const float* state_in;  // may be null
+  float* state_out;       // may be null, may equal state_in
+  const float* w;
+  const float* bias;      // may be null
+  int64_t B, T, Di;
+  int K;
+  int bf16;               // activation storage: 0 f32, 1 bf16
+};
+cudaError_t launch_conv1d_silu_prefill(const ConvPrefillArgs& a, const DeviceInfo& dev,
+                                       cudaStream_t stream);
+
+struct ConvStepArgs {
+  void* u;
+  const void* x;
+  float* state;  // slab of the layer: [B][Di][K]
+  const float* w;
+  const float* bias;
+  int64_t B, Di;
+  int K;
+  int bf16;
+};
+cudaError_t launch_conv1d_silu_step(const ConvStepArgs& a, const DeviceInfo& dev,
+                                    cudaStream_t stream);
+
+// ----------------------------------------------------------------- scan ----
+struct ScanArgs {
+  void* y;
+  int64_t ld_y;
+  int y_bf16;
+  const void* u;
+  int64_t ld_u;
+  const void* dt;
+  int64_t ld_dt;
+  const void* z;  // may be null
+  int64_t ld_z;
+  const void* Bm;
+  int64_t ld_B;
+  const void* Cm;
+  int64_t ld_C;
+  int in_bf16;
+  const float* A_log;
+  const float* D;        // may be null
+  const float* dt_bias;  // may be null
+  const float* state_in;  // may be null
+  float* state_out;       // may be null, may equal state_in
+  int64_t B, T, Di;
+  int N;
+};
+
+// How a prefill is cut into CTAs: each CTA owns `ct` channels of one batch
+// row for all T, with `g` thread groups that split every staged chunk of
+// tc = g * ls rows into g segments (g == 1: one sequential pass).
+struct ScanPlan {
+  int ct;      // channels per CTA
+  int g;       // segments per chunk
+  int ls;      // rows per segment
+  int stages;  // cp.async pipeline depth
+  int act_vec; // u/dt/z staged with 16-byte copies (else element loads)
+  int bc_vec;  // B/C staged with 16-byte copies
+  int bc_pad;  // B/C smem row stride in elements (>= N)
+  int64_t smem_bytes;
+};
+ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev);
+cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& plan,
+                                          const DeviceInfo& dev, cudaStream_t stream);
+
+struct SsmStepArgs {
+  void* y;
+  int y_bf16;
+  const void* u;
+  const void* dt;
+  const void* z;  // may be null
+  const void* Bm;
+  const void* Cm;
+  int in_bf16;
+  const float* A_log;
+  const float* D;
+  const float* dt_bias;
+  float* state;  // slab of the layer: [B][Di][N]
+  int64_t B, Di;
+  int N;
+};
+cudaError_t launch_ssm_step_batched(const SsmStepArgs& a, const DeviceInfo& dev,
+                                    cudaStream_t stream);
+
+}  // namespace mamba

@@ -1,0 +1,151 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must build for sm_103a, load, export every symbol include/*.h
+declares, and reject bad arguments on the host before touching a device.
+"""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+import selective_state_space_conv1d_gb300 as m
+from selective_state_space_conv1d_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = ctypes.c_void_p(0x100000)  # never dereferenced: the calls below fail before any device work
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return m.load()
+
+
+def header_symbols():
+    syms = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h).read()
+        syms |= set(re.findall(r"MAMBA_API\s+[\w\s\*]+?\b(mamba_\w+)\s*\(", txt))
+    return syms
+
+
+def test_header_declares_the_four_entry_points():
+    syms = header_symbols()
+    for s in ("mamba_conv1d_silu_prefill", "mamba_conv1d_silu_step",
+              "mamba_selective_scan_prefill", "mamba_ssm_step_batched", "mamba_last_error"):
+        assert s in syms
+    assert syms == set(m.ABI_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\bT\s+(mamba_\w+)", out))
+    assert header_symbols() <= exported
+    for s in header_symbols():
+        assert hasattr(lib, s)
+    # nothing but the ABI leaks out of the library
+    assert exported == header_symbols()
+
+
+def test_library_is_built_for_sm_103a_only(lib):
+    out = subprocess.run(["cuobjdump", "--list-elf", B.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    arches = set(re.findall(r"sm_(\d+a?)", out.stdout))
+    assert arches == {"103a"}, arches
+
+
+def test_version_and_error_string(lib):
+    assert m.mamba_version() == "0.1.0"
+    assert isinstance(m.mamba_last_error(), str)
+
+
+def _scan(lib, **kw):
+    a = dict(y=FAKE, ld_y=8, y_dtype=0, u=FAKE, ld_u=8, dt=FAKE, ld_dt=8, z=None, ld_z=0,
+             Bm=FAKE, ld_B=16, Cm=FAKE, ld_C=16, in_dtype=0, A_log=FAKE, D=None, dt_bias=None,
+             s_in=None, s_out=None, B=1, T=4, Di=8, N=16, stream=None)
+    a.update(kw)
+    return lib.mamba_selective_scan_prefill(
+        a["y"], a["ld_y"], a["y_dtype"], a["u"], a["ld_u"], a["dt"], a["ld_dt"], a["z"], a["ld_z"],
+        a["Bm"], a["ld_B"], a["Cm"], a["ld_C"], a["in_dtype"], a["A_log"], a["D"], a["dt_bias"],
+        a["s_in"], a["s_out"], a["B"], a["T"], a["Di"], a["N"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(y_dtype=7), m.MAMBA_ERR_INVALID_ARG),
+    (dict(in_dtype=-1), m.MAMBA_ERR_INVALID_ARG),
+    (dict(B=-1), m.MAMBA_ERR_INVALID_ARG),
+    (dict(T=-5), m.MAMBA_ERR_INVALID_ARG),
+    (dict(N=3), m.MAMBA_ERR_UNSUPPORTED),
+    (dict(N=65), m.MAMBA_ERR_UNSUPPORTED),
+    (dict(N=128), m.MAMBA_ERR_UNSUPPORTED),
+    (dict(u=None), m.MAMBA_ERR_INVALID_ARG),
+    (dict(y=None), m.MAMBA_ERR_INVALID_ARG),
+    (dict(A_log=None), m.MAMBA_ERR_INVALID_ARG),
+    (dict(ld_u=7), m.MAMBA_ERR_INVALID_ARG),
+    (dict(ld_z=4, z=FAKE), m.MAMBA_ERR_INVALID_ARG),
+    (dict(ld_B=15), m.MAMBA_ERR_INVALID_ARG),
+    (dict(B=1 << 40, T=1 << 40), m.MAMBA_ERR_INVALID_ARG),
+])
+def test_scan_rejects_bad_arguments_on_host(lib, kw, code):
+    assert _scan(lib, **kw) == code
+    assert m.mamba_last_error() != ""
+
+
+def test_zero_sized_calls_are_noops(lib):
+    assert _scan(lib, B=0) == m.MAMBA_OK
+    assert _scan(lib, Di=0) == m.MAMBA_OK
+    assert m.mamba_last_error() == ""
+    assert lib.mamba_conv1d_silu_prefill(None, 0, None, 0, 0, None, None, FAKE, None, 0, 5, 8, 4, None) == 0
+
+
+@pytest.mark.parametrize("K,code", [(0, m.MAMBA_ERR_UNSUPPORTED), (9, m.MAMBA_ERR_UNSUPPORTED)])
+def test_conv_rejects_unsupported_d_conv(lib, K, code):
+    assert lib.mamba_conv1d_silu_prefill(FAKE, 8, FAKE, 8, 0, None, None, FAKE, None, 1, 4, 8, K, None) == code
+    assert lib.mamba_conv1d_silu_step(FAKE, FAKE, 0, FAKE, 0, 1, FAKE, None, 1, 8, K, None) == code
+
+
+def test_conv_rejects_bad_arguments(lib):
+    E = m.MAMBA_ERR_INVALID_ARG
+    assert lib.mamba_conv1d_silu_prefill(FAKE, 4, FAKE, 8, 0, None, None, FAKE, None, 1, 4, 8, 4, None) == E
+    assert lib.mamba_conv1d_silu_prefill(None, 8, FAKE, 8, 0, None, None, FAKE, None, 1, 4, 8, 4, None) == E
+    assert lib.mamba_conv1d_silu_prefill(FAKE, 8, FAKE, 8, 0, None, None, None, None, 1, 4, 8, 4, None) == E
+    assert lib.mamba_conv1d_silu_prefill(FAKE, 8, FAKE, 8, 2, None, None, FAKE, None, 1, 4, 8, 4, None) == E
+    # layer outside [0, n_layers)
+    assert lib.mamba_conv1d_silu_step(FAKE, FAKE, 0, FAKE, 3, 3, FAKE, None, 1, 8, 4, None) == E
+    assert lib.mamba_conv1d_silu_step(FAKE, FAKE, 0, FAKE, -1, 3, FAKE, None, 1, 8, 4, None) == E
+
+
+def test_step_rejects_bad_arguments(lib):
+    E, U = m.MAMBA_ERR_INVALID_ARG, m.MAMBA_ERR_UNSUPPORTED
+    f = lib.mamba_ssm_step_batched
+    assert f(FAKE, 0, FAKE, FAKE, None, FAKE, FAKE, 0, FAKE, None, None, FAKE, 0, 1, 2, 8, 65, None) == U
+    assert f(FAKE, 0, FAKE, FAKE, None, FAKE, FAKE, 0, FAKE, None, None, FAKE, 1, 1, 2, 8, 16, None) == E
+    assert f(FAKE, 0, None, FAKE, None, FAKE, FAKE, 0, FAKE, None, None, FAKE, 0, 1, 2, 8, 16, None) == E
+    assert f(FAKE, 0, FAKE, FAKE, None, FAKE, FAKE, 0, FAKE, None, None, None, 0, 1, 2, 8, 16, None) == E
+
+
+def test_valid_call_without_a_gpu_fails_cleanly(lib):
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present; covered by the GPU tests")
+    rc = _scan(lib)
+    assert rc in (m.MAMBA_ERR_CUDA, m.MAMBA_ERR_UNSUPPORTED)
+    assert m.mamba_last_error()
+
+
+def test_python_binding_raises_when_library_missing(tmp_path):
+    from selective_state_space_conv1d_gb300 import _binding
+
+    saved = _binding._lib
+    _binding._lib = None
+    try:
+        with pytest.raises(RuntimeError, match="missing"):
+            _binding.load(str(tmp_path / "nope.so"))
+    finally:
+        _binding._lib = saved

@@ -1,0 +1,348 @@
+"""GPU parity: the CUDA path (through the C ABI) against the f64 CPU oracle.
+
+Element-by-element on seeded synthetic inputs, at sizes the oracle finishes in
+seconds that still span several chunks / tiles and a ragged tail, for both
+storage dtypes, strided (column-slice) inputs, every supported d_state and
+several d_conv, with and without gate / state, in place, and on the edge cases
+(T = 0, T = 1, delta -> 0, NaN containment, guard bands).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_conv1d_gb300 import synth
+from _helpers import Guarded, assert_within, strided_copy, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+SEED = 0x5EED1000
+
+
+def _params(seed, Di, N, K, layer=0, bias=True):
+    p = synth.mixer_params(seed, Di, N, K, layer)
+    if bias:
+        p["conv_b"] = synth.normal(seed, "conv_b", (Di,), 0.2, layer=layer)
+    return p
+
+
+# ------------------------------------------------------------------ conv ----
+
+CONV_CASES = [
+    # B, T, Di, K, dtype, state, strided
+    (1, 64, 128, 4, "f32", False, False),
+    (2, 257, 136, 4, "f32", True, False),
+    (3, 5, 130, 3, "f32", True, False),       # Di not a multiple of 4: scalar path
+    (2, 1000, 256, 2, "f32", True, True),     # x / u are column slices (ld = 2 Di)
+    (2, 300, 512, 4, "bf16", True, False),
+    (1, 77, 136, 4, "bf16", True, True),
+    (2, 33, 64, 1, "f32", True, False),
+    (1, 19, 64, 8, "bf16", True, False),
+    (4, 2, 96, 4, "f32", True, False),        # T < K: the new state mixes old state and x
+]
+
+
+@pytest.mark.parametrize("Bsz,T,Di,K,dtype,state,strided", CONV_CASES)
+def test_conv_prefill_matches_oracle(cuda_lib, Bsz, T, Di, K, dtype, state, strided):
+    m = cuda_lib
+    p = _params(SEED + K, Di, 16, K)
+    x = synth.normal(SEED, "x", (Bsz, T, Di), 1.0, dtype)
+    s0 = synth.normal(SEED, "conv_state", (Bsz, Di, K), 1.0) if state else None
+    if strided:
+        xd = strided_copy(x, dtype, 2 * Di, offset=Di)
+        ud = strided_copy(np.zeros_like(x), dtype, 2 * Di)
+    else:
+        xd = to_dev(x, dtype)
+        ud = torch.empty_like(xd)
+    sd_in = to_dev(s0) if state else None
+    sd_out = torch.empty((Bsz, Di, K), device="cuda")
+    m.mamba_conv1d_silu_prefill(ud, xd, to_dev(p["conv_w"]), to_dev(p["conv_b"]), sd_in, sd_out)
+    torch.cuda.synchronize()
+    u_ref, s_ref = oracle.conv1d_silu_prefill(x, p["conv_w"], p["conv_b"], s0)
+    assert_within(to_host(ud), u_ref, "u", bf16_out=dtype == "bf16")
+    assert np.array_equal(to_host(sd_out), s_ref), "conv state is a copy of inputs: must be exact"
+
+
+def test_conv_prefill_in_place_state_and_guard_bands(cuda_lib):
+    m = cuda_lib
+    Bsz, T, Di, K = 2, 123, 264, 4
+    p = _params(SEED, Di, 16, K)
+    x = synth.normal(SEED, "x", (Bsz, T, Di))
+    s0 = synth.normal(SEED, "conv_state", (Bsz, Di, K))
+    st = to_dev(s0)
+    u = Guarded((Bsz, T, Di))
+    m.mamba_conv1d_silu_prefill(u.view, to_dev(x), to_dev(p["conv_w"]), to_dev(p["conv_b"]), st, st)
+    torch.cuda.synchronize()
+    u.check()
+    u_ref, s_ref = oracle.conv1d_silu_prefill(x, p["conv_w"], p["conv_b"], s0)
+    assert_within(to_host(u.view), u_ref, "u")
+    assert np.array_equal(to_host(st), s_ref)
+
+
+def test_conv_T0_copies_state(cuda_lib):
+    m = cuda_lib
+    Bsz, Di, K = 2, 64, 4
+    s0 = synth.normal(SEED, "conv_state", (Bsz, Di, K))
+    out = torch.full((Bsz, Di, K), 3.0, device="cuda")
+    x = torch.empty((Bsz, 0, Di), device="cuda")
+    m.mamba_conv1d_silu_prefill(torch.empty_like(x), x, torch.zeros(Di, K, device="cuda"), None,
+                                to_dev(s0), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(out), s0)
+
+
+@pytest.mark.parametrize("dtype,K", [("f32", 4), ("bf16", 4), ("f32", 3), ("f32", 2)])
+def test_conv_step_matches_oracle_and_prefill_bitwise(cuda_lib, dtype, K):
+    m = cuda_lib
+    L, Bsz, Di = 3, 5, 200
+    p = _params(SEED + 1, Di, 16, K)
+    conv = synth.normal(SEED, "conv_state", (L, Bsz, Di, K), 0.5)
+    st = to_dev(conv)
+    ref_state = conv.astype(np.float64).copy()
+    w, b = to_dev(p["conv_w"]), to_dev(p["conv_b"])
+    for step in range(4):
+        x = synth.normal(SEED, "x", (Bsz, Di), 1.0, dtype, layer=1, step=step)
+        xd = to_dev(x, dtype)
+        # T=1 prefill on the same slab, for the bitwise comparison
+        u_pf = torch.empty((Bsz, 1, Di), device="cuda", dtype=xd.dtype)
+        s_pf = torch.empty((Bsz, Di, K), device="cuda")
+        m.mamba_conv1d_silu_prefill(u_pf, xd.view(Bsz, 1, Di), w, b, st[1].clone(), s_pf)
+        u = torch.empty_like(xd)
+        m.mamba_conv1d_silu_step(u, xd, st, 1, w, b)
+        torch.cuda.synchronize()
+        u_ref = oracle.conv1d_silu_step(x, ref_state, 1, p["conv_w"], p["conv_b"])
+        assert_within(to_host(u), u_ref, f"u step {step}", bf16_out=dtype == "bf16")
+        assert torch.equal(u, u_pf[:, 0]), "conv step != T=1 conv prefill"
+        assert torch.equal(st[1], s_pf)
+    assert np.array_equal(to_host(st), ref_state)
+
+
+# ------------------------------------------------------------------ scan ----
+
+SCAN_CASES = [
+    # B, T, Di, N, in, y, gate, state, strided
+    (1, 64, 128, 16, "f32", "f32", True, False, False),     # tiny-mixer shape
+    (1, 300, 128, 16, "f32", "f32", True, True, False),     # T split inside the CTA
+    (1, 1000, 136, 16, "f32", "f32", True, True, True),     # T split, strided, ragged tail
+    (2, 777, 130, 16, "f32", "f32", True, True, False),     # Di % 4 != 0: element staging
+    (24, 70, 1024, 16, "f32", "f32", True, True, False),    # wide: one sequential pass
+    (2, 513, 256, 16, "bf16", "f32", True, True, False),
+    (3, 129, 136, 16, "bf16", "bf16", True, True, True),
+    (1, 200, 64, 1, "f32", "f32", True, True, False),
+    (1, 200, 64, 2, "f32", "f32", False, True, False),
+    (1, 200, 64, 4, "bf16", "f32", True, True, False),
+    (1, 200, 64, 8, "f32", "bf16", True, False, False),
+    (2, 150, 64, 32, "f32", "f32", True, True, False),
+    (2, 150, 64, 64, "f32", "f32", True, True, False),
+    (1, 90, 64, 64, "bf16", "f32", True, True, True),
+    (2, 1, 96, 16, "f32", "f32", True, True, False),        # T = 1
+    (1, 2, 64, 16, "bf16", "f32", True, True, False),
+]
+
+
+def _scan_inputs(Bsz, T, Di, N, dtype, seed=SEED):
+    a = synth.prefill_inputs(seed, Bsz, T, Di, N, dtype, names=("u", "dt", "z", "B", "C"))
+    p = synth.mixer_params(seed, Di, N, 4)
+    return a, p
+
+
+def _run_scan(m, a, p, dtype, y_dtype, gate, state_in, strided, inplace=False):
+    Bsz, T, Di = a["u"].shape
+    N = a["B"].shape[2]
+    if strided:
+        # u / z as the two halves of one buffer, B / C as columns of an x_proj-like row
+        u = strided_copy(a["u"], dtype, 2 * Di)
+        z = strided_copy(a["z"], dtype, 2 * Di, offset=Di) if gate else None
+        dt = strided_copy(a["dt"], dtype, Di + 8, offset=8)
+        xdbl = Di // 4 + 2 * N  # dt_rank + 2 N
+        Bm = strided_copy(a["B"], dtype, xdbl, offset=Di // 4)
+        Cm = strided_copy(a["C"], dtype, xdbl, offset=Di // 4 + N)
+        y = strided_copy(np.zeros((Bsz, T, Di), np.float32), y_dtype, Di + 4)
+    else:
+        u, dt = to_dev(a["u"], dtype), to_dev(a["dt"], dtype)
+        z = to_dev(a["z"], dtype) if gate else None
+        Bm, Cm = to_dev(a["B"], dtype), to_dev(a["C"], dtype)
+        y = to_dev(np.zeros((Bsz, T, Di), np.float32), y_dtype)
+    s_in = to_dev(state_in) if state_in is not None else None
+    s_out = s_in if (inplace and s_in is not None) else torch.empty((Bsz, Di, N), device="cuda")
+    m.mamba_selective_scan_prefill(y, u, dt, Bm, Cm, to_dev(p["A_log"]), to_dev(p["D"]),
+                                   to_dev(p["dt_bias"]), z, s_in, s_out)
+    torch.cuda.synchronize()
+    return to_host(y), to_host(s_out)
+
+
+@pytest.mark.parametrize("Bsz,T,Di,N,dtype,y_dtype,gate,state,strided", SCAN_CASES)
+def test_scan_prefill_matches_oracle(cuda_lib, Bsz, T, Di, N, dtype, y_dtype, gate, state, strided):
+    m = cuda_lib
+    a, p = _scan_inputs(Bsz, T, Di, N, dtype)
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5) if state else None
+    y, s = _run_scan(m, a, p, dtype, y_dtype, gate, s0, strided)
+    y_ref, s_ref = oracle.selective_scan_prefill(a["u"], a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                 p["dt_bias"], a["z"] if gate else None, s0)
+    assert_within(y, y_ref, "y", bf16_out=y_dtype == "bf16")
+    assert_within(s, s_ref, "state")
+
+
+@pytest.mark.parametrize("Bsz,T,Di", [(1, 2000, 128), (8, 64, 512)])
+def test_scan_ssm_part_without_D_and_gate(cuda_lib, Bsz, T, Di):
+    """Tighter diagnostic: y - D u (the pure SSM part, ~1e-2) at the same bound."""
+    m = cuda_lib
+    a, p = _scan_inputs(Bsz, T, Di, 16, "f32", seed=SEED + 5)
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, 16), 0.5)
+    p = dict(p, D=np.zeros(Di, np.float32))
+    y, s = _run_scan(m, a, p, "f32", "f32", False, s0, False)
+    y_ref, s_ref = oracle.selective_scan_prefill(a["u"], a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                 p["dt_bias"], None, s0)
+    assert_within(y, y_ref, "C.h")
+    assert_within(s, s_ref, "state")
+
+
+def test_scan_in_place_state_and_guard_bands(cuda_lib):
+    m = cuda_lib
+    Bsz, T, Di, N = 1, 700, 192, 16
+    a, p = _scan_inputs(Bsz, T, Di, N, "f32")
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5)
+    st = to_dev(s0)
+    y = Guarded((Bsz, T, Di))
+    m.mamba_selective_scan_prefill(y.view, to_dev(a["u"]), to_dev(a["dt"]), to_dev(a["B"]), to_dev(a["C"]),
+                                   to_dev(p["A_log"]), to_dev(p["D"]), to_dev(p["dt_bias"]),
+                                   to_dev(a["z"]), st, st)
+    torch.cuda.synchronize()
+    y.check()
+    y_ref, s_ref = oracle.selective_scan_prefill(a["u"], a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                 p["dt_bias"], a["z"], s0)
+    assert_within(to_host(y.view), y_ref, "y")
+    assert_within(to_host(st), s_ref, "state")
+
+
+def test_scan_strided_y_leaves_gap_columns_untouched(cuda_lib):
+    m = cuda_lib
+    Bsz, T, Di, N = 2, 300, 64, 16
+    a, p = _scan_inputs(Bsz, T, Di, N, "f32")
+    ybuf = torch.full((Bsz, T, Di + 16), -3.5, device="cuda")
+    y = ybuf[:, :, 8:8 + Di]
+    m.mamba_selective_scan_prefill(y, to_dev(a["u"]), to_dev(a["dt"]), to_dev(a["B"]), to_dev(a["C"]),
+                                   to_dev(p["A_log"]), to_dev(p["D"]), to_dev(p["dt_bias"]), to_dev(a["z"]))
+    torch.cuda.synchronize()
+    assert bool((ybuf[:, :, :8] == -3.5).all()) and bool((ybuf[:, :, 8 + Di:] == -3.5).all())
+
+
+@pytest.mark.parametrize("T1,T2,Di", [(100, 157, 128), (1, 63, 256), (2048, 333, 128)])
+def test_scan_continuation(cuda_lib, T1, T2, Di):
+    """prefill(T1) then prefill(T2) from the returned state == prefill(T1 + T2)."""
+    m = cuda_lib
+    Bsz, N = 2, 16
+    a, p = _scan_inputs(Bsz, T1 + T2, Di, N, "f32")
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5)
+    y, s = _run_scan(m, a, p, "f32", "f32", True, s0, False)
+    a1 = {k: v[:, :T1].copy() for k, v in a.items()}
+    a2 = {k: v[:, T1:].copy() for k, v in a.items()}
+    y1, s1 = _run_scan(m, a1, p, "f32", "f32", True, s0, False)
+    y2, s2 = _run_scan(m, a2, p, "f32", "f32", True, s1.astype(np.float32), False)
+    y_ref, s_ref = oracle.selective_scan_prefill(a["u"], a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                 p["dt_bias"], a["z"], s0)
+    assert_within(np.concatenate([y1, y2], 1), y_ref, "y (two calls)")
+    assert_within(s2, s_ref, "state (two calls)")
+    assert_within(y, y_ref, "y (one call)")
+    assert_within(s, s_ref, "state (one call)")
+
+
+def test_scan_T0_copies_or_zeroes_state(cuda_lib):
+    m = cuda_lib
+    Bsz, Di, N = 2, 64, 16
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5)
+    e = torch.empty((Bsz, 0, Di), device="cuda")
+    eb = torch.empty((Bsz, 0, N), device="cuda")
+    A = torch.zeros(Di, N, device="cuda")
+    out = torch.full((Bsz, Di, N), 9.0, device="cuda")
+    m.mamba_selective_scan_prefill(e, e, e, eb, eb, A, None, None, None, to_dev(s0), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(out), s0)
+    m.mamba_selective_scan_prefill(e, e, e, eb, eb, A, None, None, None, None, out)
+    torch.cuda.synchronize()
+    assert not bool(out.any())
+
+
+@pytest.mark.parametrize("T,Di", [(40, 128), (500, 128)])
+def test_scan_delta_to_zero_keeps_state(cuda_lib, T, Di):
+    """dt + dt_bias = -200: delta underflows to 0, the state is unchanged bit for bit
+    and y = C . h0 + D u (gate off)."""
+    m = cuda_lib
+    Bsz, N = 1, 16
+    a, p = _scan_inputs(Bsz, T, Di, N, "f32")
+    a["dt"] = np.zeros_like(a["dt"])
+    p = dict(p, dt_bias=np.full(Di, -200.0, np.float32))
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5)
+    y, s = _run_scan(m, a, p, "f32", "f32", False, s0, False)
+    assert np.array_equal(s, s0.astype(np.float64))
+    expect = np.einsum("btn,bcn->btc", a["C"].astype(np.float64), s0.astype(np.float64)) + a["u"]
+    assert_within(y, expect, "y = C.h0 + D u")
+
+
+def test_scan_nan_stays_in_its_channel(cuda_lib):
+    m = cuda_lib
+    Bsz, T, Di, N = 2, 600, 128, 16
+    a, p = _scan_inputs(Bsz, T, Di, N, "f32")
+    t0, c0 = 250, 37
+    a["u"][1, t0, c0] = np.nan
+    y, s = _run_scan(m, a, p, "f32", "f32", True, None, False)
+    nan = np.isnan(y)
+    assert not nan[:, :t0].any() and not nan[0].any()
+    assert nan[1, t0:, c0].all()
+    other = np.ones(Di, bool)
+    other[c0] = False
+    assert not nan[1][:, other].any()
+    assert np.isnan(s[1, c0]).all() and not np.isnan(s[1, other]).any() and not np.isnan(s[0]).any()
+
+
+def test_scan_is_deterministic_and_batch_rows_are_independent(cuda_lib):
+    m = cuda_lib
+    Bsz, T, Di, N = 4, 48, 256, 16  # T <= 64: one sequential pass for any batch
+    a, p = _scan_inputs(Bsz, T, Di, N, "f32")
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5)
+    y, s = _run_scan(m, a, p, "f32", "f32", True, s0, False)
+    y2, s2 = _run_scan(m, a, p, "f32", "f32", True, s0, False)
+    assert np.array_equal(y, y2) and np.array_equal(s, s2)
+    a2 = {k: v[2:3].copy() for k, v in a.items()}
+    y1, s1 = _run_scan(m, a2, p, "f32", "f32", True, s0[2:3].copy(), False)
+    assert np.array_equal(y1[0], y[2]) and np.array_equal(s1[0], s[2])
+
+
+# ------------------------------------------------------------------ step ----
+
+@pytest.mark.parametrize("N,dtype,y_dtype,gate", [
+    (16, "f32", "f32", True), (16, "bf16", "f32", True), (16, "bf16", "bf16", True),
+    (1, "f32", "f32", True), (2, "f32", "f32", False), (4, "f32", "f32", True),
+    (8, "f32", "f32", True), (32, "f32", "f32", True), (64, "f32", "f32", True),
+    (64, "bf16", "f32", False),
+])
+def test_ssm_step_matches_oracle_and_T1_prefill_bitwise(cuda_lib, N, dtype, y_dtype, gate):
+    m = cuda_lib
+    L, Bsz, Di = 3, 9, 160
+    p = synth.mixer_params(SEED + N, Di, N, 4, layer=2)
+    st_h = synth.normal(SEED, "ssm_state", (L, Bsz, Di, N), 0.5)
+    st = to_dev(st_h)
+    ref_state = st_h.astype(np.float64).copy()
+    A, D, dtb = to_dev(p["A_log"]), to_dev(p["D"]), to_dev(p["dt_bias"])
+    for step in range(3):
+        inp = synth.decode_step_inputs(SEED, 2, step, Bsz, Di, N, dtype)
+        u_h = synth.normal(SEED, "u", (Bsz, Di), 1.0, dtype, layer=2, step=step)
+        u, dt = to_dev(u_h, dtype), to_dev(inp["dt"], dtype)
+        z = to_dev(inp["z"], dtype) if gate else None
+        Bm, Cm = to_dev(inp["B"], dtype), to_dev(inp["C"], dtype)
+        # T=1 prefill of the same slab (one sequential pass)
+        y_pf = torch.empty((Bsz, 1, Di), device="cuda", dtype=torch.bfloat16 if y_dtype == "bf16" else torch.float32)
+        s_pf = torch.empty((Bsz, Di, N), device="cuda")
+        m.mamba_selective_scan_prefill(y_pf, u.view(Bsz, 1, Di), dt.view(Bsz, 1, Di), Bm.view(Bsz, 1, N),
+                                       Cm.view(Bsz, 1, N), A, D, dtb,
+                                       z.view(Bsz, 1, Di) if gate else None, st[2].clone(), s_pf)
+        y = torch.empty((Bsz, Di), device="cuda", dtype=y_pf.dtype)
+        m.mamba_ssm_step_batched(y, u, dt, Bm, Cm, st, 2, A, D, dtb, z)
+        torch.cuda.synchronize()
+        y_ref = oracle.ssm_step(u_h, inp["dt"], inp["B"], inp["C"], ref_state, 2, p["A_log"], p["D"],
+                                p["dt_bias"], inp["z"] if gate else None)
+        assert_within(to_host(y), y_ref, f"y step {step}", bf16_out=y_dtype == "bf16")
+        assert_within(to_host(st[2]), ref_state[2], f"state step {step}")
+        assert torch.equal(y, y_pf[:, 0]), "ssm step != T=1 prefill"
+        assert torch.equal(st[2], s_pf), "ssm step state != T=1 prefill state"
+    assert np.array_equal(to_host(st[0]), st_h[0]) and np.array_equal(to_host(st[1]), st_h[1])
