@@ -131,21 +131,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def make_events(torch, n, external):
-    kw = {"enable_timing": True}
-    if external:
-        kw["external"] = True
-    return [torch.cuda.Event(**kw) for _ in range(n)]
-
-
-def external_events_supported(torch):
-    try:
-        torch.cuda.Event(enable_timing=True, external=True)
-        return True
-    except TypeError:
-        return False
-
-
 def capture(torch, fn):
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
@@ -219,29 +204,21 @@ class PrefillSet:
         return conv, scan
 
 
-def timed_graph_run(torch, m, sets, n_steps, per_graph, ext, clocks=None, dist=None):
-    """Run n_steps prefill steps as replays of captured graphs; returns timings."""
+def timed_graph_run(torch, m, sets, n_steps, per_graph, clocks=None, dist=None):
+    """Time n_steps prefill steps (conv then scan) as replays of captured graphs."""
     per_graph = max(1, min(per_graph, n_steps))
 
-    def build(nsteps, offset):
-        evs = make_events(torch, 2 * nsteps + 1, ext) if ext else None
-
+    def build(nsteps):
         def body():
             for i in range(nsteps):
-                s = sets[(offset + i) % len(sets)]
-                if evs:
-                    evs[2 * i].record()
+                s = sets[i % len(sets)]
                 s.conv(m)
-                if evs:
-                    evs[2 * i + 1].record()
                 s.scan(m)
-            if evs:
-                evs[2 * nsteps].record()
-        return capture(torch, body), evs
+        return capture(torch, body)
 
-    g_main, ev_main = build(per_graph, 0)
+    g_main = build(per_graph)
     reps, tail = divmod(n_steps, per_graph)
-    g_tail, ev_tail = build(tail, 0) if tail else (None, None)
+    g_tail = build(tail) if tail else None
     g_main.replay()
     if g_tail:
         g_tail.replay()
@@ -263,29 +240,25 @@ def timed_graph_run(torch, m, sets, n_steps, per_graph, ext, clocks=None, dist=N
     ck = clocks.stop() if clocks else None
     if dist is not None:
         dist.barrier()
-    total_ms = start.elapsed_time(end)
-    conv_ms, scan_ms = [], []
-    if ev_main:
-        for i in range(per_graph):
-            conv_ms.append(ev_main[2 * i].elapsed_time(ev_main[2 * i + 1]))
-            scan_ms.append(ev_main[2 * i + 1].elapsed_time(ev_main[2 * i + 2]))
-    return total_ms, conv_ms, scan_ms, ck
+    return start.elapsed_time(end), ck
 
 
-def kernel_only_times(torch, m, sets, n, which):
-    """Fallback when graphs cannot hold timing events: time graphs of one kernel kind."""
+def kernel_time(torch, calls, n, reps=3):
+    """Average duration of one call: a captured graph of n back-to-back calls
+    (calls[i % len]) replayed `reps` times between CUDA events on its stream."""
     def body():
         for i in range(n):
-            getattr(sets[i % len(sets)], which)(m)
+            calls[i % len(calls)]()
     g = capture(torch, body)
     g.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
-    g.replay()
+    for _ in range(reps):
+        g.replay()
     b.record()
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) / n] * n
+    return a.elapsed_time(b) / (n * reps)
 
 
 def roofline(bytes_per_launch, ms, peak, peak_src, traffic):
@@ -295,7 +268,7 @@ def roofline(bytes_per_launch, ms, peak, peak_src, traffic):
             "algorithmic_bytes_per_launch": int(bytes_per_launch), "avg_launch_ms": round(ms, 6)}
 
 
-def run_prefill(torch, m, synth, wl_index, steps, warmup, ext, device, dist, clocks, host_inputs=True):
+def run_prefill(torch, m, synth, wl_index, steps, warmup, device, dist, clocks, host_inputs=True):
     wl = synth.WORKLOADS[wl_index]
     Bsz, T, Di, N, K = wl.batch, wl.seqlen, wl.d_inner, wl.d_state, wl.d_conv
     params = synth.mixer_params(wl.seed, Di, N, K)
@@ -321,17 +294,18 @@ def run_prefill(torch, m, synth, wl_index, steps, warmup, ext, device, dist, clo
         sets[i % n_sets].conv(m)
         sets[i % n_sets].scan(m)
     torch.cuda.synchronize()
-    total_ms, conv_ms, scan_ms, ck = timed_graph_run(torch, m, sets, steps, 100, ext, clocks, dist)
-    if not scan_ms:
-        conv_ms = kernel_only_times(torch, m, sets, 100, "conv")
-        scan_ms = kernel_only_times(torch, m, sets, 100, "scan")
+    total_ms, ck = timed_graph_run(torch, m, sets, steps, 100, clocks, dist)
+    n_k = 40 if set_bytes < 1e9 else 10
+    conv_ms = kernel_time(torch, [lambda s=s: s.conv(m) for s in sets], n_k)
+    scan_ms = kernel_time(torch, [lambda s=s: s.scan(m) for s in sets], n_k)
+    scan_launches = 2 if m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) > 0 else 1
     l2_note = (f"inputs > 3x L2 ({set_bytes / 1e6:.0f} MB per step)" if n_sets == 1 else
                f"rotating {n_sets} resident buffer sets ({n_sets * set_bytes / 1e6:.0f} MB > 3x the "
                f"{l2 / 1e6:.0f} MB L2)")
     return {
         "wl": wl, "sets": sets, "host": host, "params": params, "total_ms": total_ms,
-        "ms_per_step": total_ms / steps, "conv_ms": float(np.mean(conv_ms)),
-        "scan_ms": float(np.mean(scan_ms)), "conv_bytes": conv_b, "scan_bytes": scan_b,
+        "ms_per_step": total_ms / steps, "conv_ms": conv_ms, "scan_ms": scan_ms,
+        "scan_launches": scan_launches, "conv_bytes": conv_b, "scan_bytes": scan_b,
         "tokens_per_step": Bsz * T, "clocks": ck, "l2_note": l2_note,
     }
 
@@ -375,7 +349,7 @@ def run_e2e(torch, m, res, steps, device):
             "ms_per_step": round(ms, 5), "api": "C ABI via the Python binding, pinned host buffers"}
 
 
-def run_decode(torch, m, synth, device, peak, peak_src, ext, n_steps=256):
+def run_decode(torch, m, synth, device, peak, peak_src, n_steps=256):
     """24-layer T=1 decode at batch 128 over a persistent state, graph-replayed."""
     wl = synth.WORKLOADS[2]
     L, Bsz, Di, N, K = wl.n_layers, wl.batch, wl.d_inner, wl.d_state, wl.d_conv
@@ -394,17 +368,11 @@ def run_decode(torch, m, synth, device, peak, peak_src, ext, n_steps=256):
     u = torch.empty((L, Bsz, Di), device=device)
     y = torch.empty((L, Bsz, Di), device=device)
 
-    def layer_step(s, l, evs=None, base=0):
+    def layer_step(s, l):
         p = params[l]
-        if evs:
-            evs[base].record()
         m.mamba_conv1d_silu_step(u[l], x[s, l], conv, l, p["conv_w"], p["conv_b"])
-        if evs:
-            evs[base + 1].record()
         m.mamba_ssm_step_batched(y[l], u[l], dt[s, l], Bm[s, l], Cm[s, l], ssm, l, p["A_log"],
                                  p["D"], p["dt_bias"], z[s, l])
-        if evs:
-            evs[base + 2].record()
 
     for s in range(3):  # warm-up steps
         for l in range(L):
@@ -421,17 +389,16 @@ def run_decode(torch, m, synth, device, peak, peak_src, ext, n_steps=256):
     b.record()
     torch.cuda.synchronize()
     ms_step = a.elapsed_time(b) / (reps * n_steps)
-    # per-kernel durations from an instrumented replay of 8 steps
-    conv_ms, step_ms = [], []
-    if ext:
-        ns = 8
-        evs = make_events(torch, 3 * ns * L, ext)
-        gi = capture(torch, lambda: [layer_step(s, l, evs, 3 * (s * L + l)) for s in range(ns) for l in range(L)])
-        gi.replay()
-        torch.cuda.synchronize()
-        for i in range(ns * L):
-            conv_ms.append(evs[3 * i].elapsed_time(evs[3 * i + 1]))
-            step_ms.append(evs[3 * i + 1].elapsed_time(evs[3 * i + 2]))
+    # per-kernel durations: graphs of one kernel kind over 4 steps x 24 layers
+    conv_calls = [lambda s=s, l=l: m.mamba_conv1d_silu_step(u[l], x[s, l], conv, l, params[l]["conv_w"],
+                                                             params[l]["conv_b"])
+                  for s in range(4) for l in range(L)]
+    step_calls = [lambda s=s, l=l: m.mamba_ssm_step_batched(y[l], u[l], dt[s, l], Bm[s, l], Cm[s, l], ssm, l,
+                                                             params[l]["A_log"], params[l]["D"],
+                                                             params[l]["dt_bias"], z[s, l])
+                  for s in range(4) for l in range(L)]
+    conv_ms = kernel_time(torch, conv_calls, len(conv_calls))
+    step_ms = kernel_time(torch, step_calls, len(step_calls))
     rows = Bsz * Di
     step_bytes = rows * (2 * 4 * N + 5 * 4) + Bsz * N * 2 * 4 + Di * (N + 2) * 4
     conv_bytes = rows * (2 * 4 * K + 2 * 4) + Di * (K + 1) * 4
@@ -447,11 +414,9 @@ def run_decode(torch, m, synth, device, peak, peak_src, ext, n_steps=256):
         "gpu_launches": 2 * L * n_steps * reps,
     }
     out["frac_of_hbm_peak"] = round(out["hbm_gbs_per_step"] / peak, 4)
-    if step_ms:
-        out["roofline"] = roofline(step_bytes, float(np.mean(step_ms)), peak, peak_src,
-                                   ncu_traffic("step", wl.name))
-        out["conv_step_roofline"] = roofline(conv_bytes, float(np.mean(conv_ms)), peak, peak_src,
-                                             ncu_traffic("conv", wl.name + "-step"))
+    out["roofline"] = roofline(step_bytes, step_ms, peak, peak_src, ncu_traffic("step", wl.name))
+    out["conv_step_roofline"] = roofline(conv_bytes, conv_ms, peak, peak_src,
+                                         ncu_traffic("conv", wl.name + "-step"))
     return out
 
 
@@ -571,11 +536,10 @@ def main():
         td.init_process_group("nccl", device_id=device)
         dist = td
     m.load()
-    ext = external_events_supported(torch)
     peak, peak_src = hbm_peak()
     clocks = ClockSampler(local_rank)
 
-    res = run_prefill(torch, m, synth, 1, args.steps, args.warmup, ext, device, dist, clocks)
+    res = run_prefill(torch, m, synth, 1, args.steps, args.warmup, device, dist, clocks)
     total_ms = res["total_ms"]
     if dist is not None:
         t = torch.tensor([total_ms], device=device)
@@ -591,8 +555,8 @@ def main():
 
     extra = {}
     if not args.no_extra:
-        extra["decode_130m_b128_l24"] = run_decode(torch, m, synth, device, peak, peak_src, ext)
-        r3 = run_prefill(torch, m, synth, 3, 50, 3, ext, device, None, None, host_inputs=False)
+        extra["decode_130m_b128_l24"] = run_decode(torch, m, synth, device, peak, peak_src)
+        r3 = run_prefill(torch, m, synth, 3, 50, 3, device, None, None, host_inputs=False)
         extra["prefill_2p8b_bf16"] = {
             "workload": r3["wl"].name, "value": round(r3["tokens_per_step"] / (r3["ms_per_step"] * 1e-3), 1),
             "unit": "tokens/s", "ms_per_step": round(r3["ms_per_step"], 5),
@@ -627,6 +591,8 @@ def main():
                        "launch": "CUDA graph replays of 100 steps"},
             "hbm_gbs_per_step": round(step_gbs, 1),
             "roofline": scan_roof,
+            "roofline_kernel": ("selective-scan prefill call (" + ("T-split: state-only pass + full pass, 2 launches"
+                                 if res["scan_launches"] == 2 else "one sequential launch") + ")"),
             "conv_roofline": conv_roof,
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -132,8 +132,15 @@ MAMBA_API int mamba_conv1d_silu_step(void* u, const void* x, int act_dtype, floa
  *   A_log  [Di][N] f32;  D, dt_bias [Di] f32 or NULL
  *   ssm_state_in  [B][Di][N] f32 or NULL (zeros)
  *   ssm_state_out [B][Di][N] f32 or NULL; may equal ssm_state_in
- * T == 0 copies the state.  Long, narrow shapes (few batch*channel rows) are
- * split along T inside each CTA; the split changes rounding only.
+ *   workspace     device scratch of workspace_bytes bytes (16-byte aligned),
+ *                 or NULL / 0.  Narrow shapes (few batch x channel rows, e.g.
+ *                 batch 1) are split along T into parts scanned in parallel,
+ *                 which needs mamba_selective_scan_workspace_bytes() bytes;
+ *                 with less, the call runs as one sequential pass (same
+ *                 result up to rounding, slower).  Contents on entry are
+ *                 ignored; calls that share a workspace must not overlap in
+ *                 time (same stream, or ordered by events).
+ * T == 0 copies the state.
  * Errors: MAMBA_ERR_INVALID_ARG for NULL required pointers, ld < row width,
  * y overlapping an input; MAMBA_ERR_UNSUPPORTED for N not in {1,2,4,...,64}.
  */
@@ -143,7 +150,16 @@ MAMBA_API int mamba_selective_scan_prefill(void* y, int64_t ld_y, int y_dtype, c
                                  const void* Cm, int64_t ld_C, int in_dtype,
                                  const float* A_log, const float* D, const float* dt_bias,
                                  const float* ssm_state_in, float* ssm_state_out, int64_t B,
-                                 int64_t T, int64_t Di, int64_t N, void* stream);
+                                 int64_t T, int64_t Di, int64_t N, void* workspace,
+                                 int64_t workspace_bytes, void* stream);
+
+/*
+ * Workspace (bytes) that mamba_selective_scan_prefill uses to split T across
+ * CTAs for a [B, T, Di] x d_state N prefill on the CURRENT device (the split
+ * depends on its SM count).  0 means the call runs as one sequential pass and
+ * needs no workspace.  Negative MAMBA_ERR_* on bad sizes or no usable device.
+ */
+MAMBA_API int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N);
 
 /*
  * Batched T=1 SSM step with fused gate, in place on the `layer` slab of a

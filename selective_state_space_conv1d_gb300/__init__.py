@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     mamba_conv1d_silu_step,
     mamba_last_error,
     mamba_selective_scan_prefill,
+    mamba_selective_scan_workspace_bytes,
     mamba_ssm_step_batched,
     mamba_version,
 )

@@ -28,6 +28,7 @@ ABI_SYMBOLS = (
     "mamba_conv1d_silu_prefill",
     "mamba_conv1d_silu_step",
     "mamba_selective_scan_prefill",
+    "mamba_selective_scan_workspace_bytes",
     "mamba_ssm_step_batched",
     "mamba_last_error",
     "mamba_version",
@@ -60,7 +61,9 @@ def load(path: str | None = None):
         lib.mamba_conv1d_silu_step.argtypes = [vp, vp, i32, vp, i64, i64, vp, vp, i64, i64, i64, vp]
         lib.mamba_selective_scan_prefill.argtypes = (
             [vp, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32]
-            + [vp] * 5 + [i64, i64, i64, i64, vp])
+            + [vp] * 5 + [i64, i64, i64, i64, vp, i64, vp])
+        lib.mamba_selective_scan_workspace_bytes.argtypes = [i64, i64, i64, i64]
+        lib.mamba_selective_scan_workspace_bytes.restype = i64
         lib.mamba_ssm_step_batched.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp]
         for f in ("mamba_conv1d_silu_prefill", "mamba_conv1d_silu_step",
                   "mamba_selective_scan_prefill", "mamba_ssm_step_batched"):
@@ -177,12 +180,40 @@ def mamba_conv1d_silu_step(u, x, conv_state, layer, w, bias=None, *, stream=None
         _ptr(w), _ptr(bias), Bsz, Di, K, _stream(stream, x)))
 
 
+def mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) -> int:
+    """Workspace bytes the T-split route needs on the current device (0: none)."""
+    v = load().mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
+    if v < 0:
+        raise MambaError(int(v), mamba_last_error())
+    return int(v)
+
+
+_ws_cache = {}
+
+
+def _workspace(device, nbytes):
+    """A per-device scratch buffer reused across calls (grown on demand)."""
+    import torch
+
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
 def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, z=None,
-                                 ssm_state_in=None, ssm_state_out=None, *, stream=None):
+                                 ssm_state_in=None, ssm_state_out=None, *, workspace=None,
+                                 stream=None):
     """Selective scan with SiLU(z) gate over T tokens, state in / state out.
 
     y, u, dt, z: [B, T, Di] (row-strided views allowed); Bm, Cm: [B, T, N];
-    A_log: [Di, N]; D, dt_bias: [Di]; states: [B, Di, N] f32."""
+    A_log: [Di, N]; D, dt_bias: [Di]; states: [B, Di, N] f32.
+    workspace: None = a cached per-device buffer sized by
+    mamba_selective_scan_workspace_bytes (shared: calls on concurrent streams
+    should pass their own); False = none (one sequential pass); or a uint8
+    cuda tensor."""
     Bsz, T, Di = u.shape
     N = A_log.shape[1]
     _f32_param(A_log, "A_log", (Di, N))
@@ -199,12 +230,21 @@ def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, 
     for t, nm in ((Bm, "Bm"), (Cm, "Cm")):
         if tuple(t.shape) != (Bsz, T, N):
             raise ValueError(f"{nm} must be [B, T, N]")
+    if workspace is None:
+        need = mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
+        ws = _workspace(u.device, need) if need > 0 else None
+    elif workspace is False:
+        ws = None
+    else:
+        ws = workspace
+    ws_ptr = ws.data_ptr() if ws is not None else None
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
     _check(load().mamba_selective_scan_prefill(
         _ptr(y), _rows_ld(y, "y"), _dtype_code(y), _ptr(u), _rows_ld(u, "u"),
         _ptr(dt), _rows_ld(dt, "dt"), _ptr(z), _rows_ld(z, "z") if z is not None else 0,
         _ptr(Bm), _rows_ld(Bm, "Bm"), _ptr(Cm), _rows_ld(Cm, "Cm"), _dtype_code(u),
         _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
-        Bsz, T, Di, N, _stream(stream, u)))
+        Bsz, T, Di, N, ws_ptr, ws_bytes, _stream(stream, u)))
 
 
 def mamba_ssm_step_batched(y, u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt_bias=None,

@@ -252,11 +252,15 @@ int mamba_selective_scan_prefill(void* y, int64_t ld_y, int y_dtype, const void*
                                  int in_dtype, const float* A_log, const float* D,
                                  const float* dt_bias, const float* ssm_state_in,
                                  float* ssm_state_out, int64_t B, int64_t T, int64_t Di, int64_t N,
-                                 void* stream) {
+                                 void* workspace, int64_t workspace_bytes, void* stream) {
   int rc;
   if ((rc = check_dtype("y_dtype", y_dtype)) || (rc = check_dtype("in_dtype", in_dtype))) return rc;
   if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld T=%lld Di=%lld)", (long long)B, (long long)T, (long long)Di);
   if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
+  if (workspace_bytes < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative workspace_bytes");
+  if (!workspace) workspace_bytes = 0;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15))
+    return fail(MAMBA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   if (B == 0 || Di == 0) return ok();
   if (!sizes_ok(B, T, Di) || !sizes_ok(B, T, N) || !sizes_ok(B, Di, N)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
   if (!A_log) return fail(MAMBA_ERR_INVALID_ARG, "A_log is NULL");
@@ -284,21 +288,36 @@ int mamba_selective_scan_prefill(void* y, int64_t ld_y, int y_dtype, const void*
                  range_of("Bm", Bm, bB), range_of("Cm", Cm, bC), range_of("A_log", A_log, bA),
                  range_of("D", D, bv), range_of("dt_bias", dt_bias, bv),
                  range_of("ssm_state_in", ssm_state_in, bst)};
-  Range outs[] = {range_of("y", y, by), range_of("ssm_state_out", ssm_state_out, bst)};
-  if ((rc = check_pointers(ins, 9, dev_id)) || (rc = check_pointers(outs, 2, dev_id))) return rc;
-  if ((rc = check_overlaps(outs, 2, ins, inplace ? 8 : 9))) return rc;
-  if (inplace && overlaps(outs[0], ins[8])) return fail(MAMBA_ERR_INVALID_ARG, "y overlaps ssm_state_in");
+  Range outs[] = {range_of("y", y, by), range_of("ssm_state_out", ssm_state_out, bst),
+                  range_of("workspace", workspace, workspace_bytes)};
+  if ((rc = check_pointers(ins, 9, dev_id)) || (rc = check_pointers(outs, 3, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 3, ins, inplace ? 8 : 9))) return rc;
+  if (inplace && (overlaps(outs[0], ins[8]) || overlaps(outs[2], ins[8])))
+    return fail(MAMBA_ERR_INVALID_ARG, "y or workspace overlaps ssm_state_in");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (T == 0) return copy_state(ssm_state_out, ssm_state_in, B * Di * N, s);
   mamba::ScanArgs a{y, ld_y, y_dtype == MAMBA_BF16, u, ld_u, dt, ld_dt, z, ld_z, Bm, ld_B, Cm, ld_C,
                     in_dtype == MAMBA_BF16, A_log, D, dt_bias, ssm_state_in, ssm_state_out,
                     B, T, Di, (int)N};
-  const mamba::ScanPlan plan = mamba::plan_selective_scan(a, dev);
-  if (plan.smem_bytes > dev.max_smem_optin)
-    return fail(MAMBA_ERR_UNSUPPORTED, "scan plan needs %lld bytes of shared memory (device max %d)", (long long)plan.smem_bytes, dev.max_smem_optin);
-  cudaError_t e = mamba::launch_selective_scan_prefill(a, plan, dev, s);
+  const mamba::ScanPlan plan = mamba::plan_selective_scan(a, dev, workspace_bytes);
+  cudaError_t e = mamba::launch_selective_scan_prefill(a, plan, static_cast<float*>(workspace), dev, s);
   if (e != cudaSuccess) return cuda_fail("selective_scan_prefill launch", e);
   return ok();
+}
+
+int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N) {
+  if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size");
+  if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
+  if (!sizes_ok(B, T, Di) || !sizes_ok(B, Di, N)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (B == 0 || Di == 0 || T == 0) {
+    ok();
+    return 0;
+  }
+  mamba::DeviceInfo dev;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  ok();
+  return mamba::scan_workspace_bytes(B, Di, N, mamba::scan_parts(B, T, Di, dev));
 }
 
 int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const void* dt, const void* z,

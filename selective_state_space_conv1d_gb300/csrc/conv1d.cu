@@ -1,12 +1,13 @@
 // conv1d.cu - causal depthwise conv1d + SiLU: T-tiled prefill and T=1 step.
 //
 // Prefill (mamba-rs prefill.rs `prefill_body` F4a, the T-tiled conv burn-in
-// with fused SiLU): each thread owns a vector of V channels (one 16-byte load:
-// 4 f32 or 8 bf16) and a tile of `tt` tokens.  It rebuilds the K-1 previous
-// inputs (the halo) from x, or from the conv state for the first tile, then
-// streams its tile keeping the window in registers.  Loads and stores are
-// 16-byte and coalesced along the contiguous channel axis; a warp moves
-// 32 x 16 B = 512 contiguous bytes per row.  The thread of tile 0 also writes
+// with fused SiLU): each thread owns 4 consecutive channels (one 16-byte f32 or
+// 8-byte bf16 access) and a tile of `tt` tokens.  It rebuilds the K-1 previous
+// inputs (the halo) from x, or from the conv state for the first tile, in the
+// same round trip as its first batch of rows, then streams the tile in batches
+// of 4 rows, loading batch i+1 while batch i computes, with the window in
+// registers.  Accesses are coalesced along the contiguous channel axis (a warp
+// moves 512 or 256 contiguous bytes per row).  The thread of tile 0 also writes
 // the new state: the last K entries of [state, x_0..x_{T-1}].  Tile 0 is the only
 // tile that reads the old state (tt >= K), so in-place state update is safe.
 //
@@ -14,59 +15,68 @@
 // epilogue SiLU"): one thread per (batch, channel) shifts its K-slot window
 // (slot 0 oldest), appends x, applies the taps and SiLU, and writes the
 // window back; K = 4 moves the window as one 16-byte load / store.
+#include <type_traits>
+
 #include "device_math.cuh"
 #include "launch.h"
 
 namespace mamba {
 namespace {
 
-template <typename T, int V>
-struct Vec;  // V elements of T in one 16-byte (or scalar) access
-
+// Four consecutive channels as one vector access: 16 bytes of f32 or 8 bytes
+// of bf16, held raw in registers until used (keeps the register count, and so
+// the number of rows in flight per SM, high).
+template <typename T>
+struct Raw4;
 template <>
-struct Vec<float, 4> {
-  static __device__ __forceinline__ void load(const float* p, float (&o)[4]) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+struct Raw4<float> {
+  float4 v;
+  __device__ __forceinline__ void load(const float* p) { v = *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ float get(int i) const {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
   }
   static __device__ __forceinline__ void store(float* p, const float (&o)[4]) {
     *reinterpret_cast<float4*>(p) = make_float4(o[0], o[1], o[2], o[3]);
   }
 };
 template <>
-struct Vec<__nv_bfloat16, 8> {
-  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&o)[8]) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      o[2 * i] = __uint_as_float(w[i] << 16);
-      o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
+struct Raw4<__nv_bfloat16> {
+  uint2 v;
+  __device__ __forceinline__ void load(const __nv_bfloat16* p) { v = *reinterpret_cast<const uint2*>(p); }
+  __device__ __forceinline__ float get(int i) const {
+    const uint32_t w = i < 2 ? v.x : v.y;
+    return __uint_as_float((i & 1) ? (w & 0xFFFF0000u) : (w << 16));
   }
-  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&o)[8]) {
-    uint32_t w[4];
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&o)[4]) {
+    uint32_t w[2];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 2; ++i) {
       const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(o[2 * i]));
       const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(o[2 * i + 1]));
       w[i] = lo | (hi << 16);
     }
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint2*>(p) = make_uint2(w[0], w[1]);
   }
 };
+// One channel per access (misaligned or ragged layouts): same arithmetic.
 template <typename T>
-struct Vec<T, 1> {
-  static __device__ __forceinline__ void load(const T* p, float (&o)[1]) { o[0] = to_f32(*p); }
+struct Raw1 {
+  T v;
+  __device__ __forceinline__ void load(const T* p) { v = *p; }
+  __device__ __forceinline__ float get(int) const { return to_f32(v); }
   static __device__ __forceinline__ void store(T* p, const float (&o)[1]) { *p = from_f32<T>(o[0]); }
 };
 
+template <typename T, int V>
+using RawV = typename std::conditional<V == 4, Raw4<T>, Raw1<T>>::type;
+
 constexpr int kConvThreads = 128;
-constexpr int kConvUnroll = 4;
+constexpr int kConvRows = 4;  // rows per batch; the next batch loads while this one computes
 
 template <int K, typename T, int V>
 __global__ void __launch_bounds__(kConvThreads)
     conv1d_silu_prefill_kernel(ConvPrefillArgs a, int tt, int64_t n_cblk, int64_t n_tiles) {
+  using R = RawV<T, V>;
   // block -> (batch, tile, channel block); channel blocks fastest
   int64_t blk = blockIdx.x;
   const int64_t cblk = blk % n_cblk;
@@ -79,60 +89,64 @@ __global__ void __launch_bounds__(kConvThreads)
   const int64_t t1 = min(a.T, t0 + (int64_t)tt);
   const int64_t Di = a.Di;
 
-  const T* __restrict__ x = reinterpret_cast<const T*>(a.x);
-  T* __restrict__ u = reinterpret_cast<T*>(a.u);
-  const T* xb = x + b * a.T * a.ld_x + c0;
-  T* ub = u + b * a.T * a.ld_u + c0;
+  const T* __restrict__ xb = reinterpret_cast<const T*>(a.x) + b * a.T * a.ld_x + c0;
+  T* __restrict__ ub = reinterpret_cast<T*>(a.u) + b * a.T * a.ld_u + c0;
 
-  float w[V][K], bias[V];
+  // window slot k (k < K-1) holds entry t0+1+k of [state_0..state_{K-1}, x_0, ...];
+  // its x rows are loaded together with the first batch
+  constexpr int KW = K > 1 ? K - 1 : 1;
+  R halo[KW];
+  R cur[kConvRows], nxt[kConvRows];
+#pragma unroll
+  for (int k = 0; k < K - 1; ++k) {
+    const int64_t j = t0 + 1 + k;
+    if (j >= K) halo[k].load(xb + (j - K) * a.ld_x);
+  }
+#pragma unroll
+  for (int r = 0; r < kConvRows; ++r)
+    if (t0 + r < t1) cur[r].load(xb + (t0 + r) * a.ld_x);
+
+  float w[V][K], bias[V], win[V][KW];
 #pragma unroll
   for (int v = 0; v < V; ++v) {
 #pragma unroll
     for (int k = 0; k < K; ++k) w[v][k] = a.w[(c0 + v) * K + k];
     bias[v] = a.bias ? a.bias[c0 + v] : 0.0f;
   }
-
-  // window slot k (k < K-1) holds entry t0+1+k of [state_0..state_{K-1}, x_0, ...]
-  constexpr int KW = K > 1 ? K - 1 : 1;
-  float win[V][KW];
 #pragma unroll
   for (int k = 0; k < K - 1; ++k) {
     const int64_t j = t0 + 1 + k;
-    if (j < K) {
 #pragma unroll
-      for (int v = 0; v < V; ++v)
-        win[v][k] = a.state_in ? a.state_in[(b * Di + c0 + v) * K + j] : 0.0f;
-    } else {
-      float r[V];
-      Vec<T, V>::load(xb + (j - K) * a.ld_x, r);
-#pragma unroll
-      for (int v = 0; v < V; ++v) win[v][k] = r[v];
-    }
+    for (int v = 0; v < V; ++v)
+      win[v][k] = j < K ? (a.state_in ? a.state_in[(b * Di + c0 + v) * K + j] : 0.0f) : halo[k].get(v);
   }
 
-  for (int64_t t = t0; t < t1; t += kConvUnroll) {
-    float xr[kConvUnroll][V];
+#pragma unroll 1
+  for (int64_t t = t0; t < t1; t += kConvRows) {
 #pragma unroll
-    for (int r = 0; r < kConvUnroll; ++r)
-      if (t + r < t1) Vec<T, V>::load(xb + (t + r) * a.ld_x, xr[r]);
+    for (int r = 0; r < kConvRows; ++r)
+      if (t + kConvRows + r < t1) nxt[r].load(xb + (t + kConvRows + r) * a.ld_x);
 #pragma unroll
-    for (int r = 0; r < kConvUnroll; ++r) {
+    for (int r = 0; r < kConvRows; ++r) {
       if (t + r < t1) {
         float o[V];
 #pragma unroll
         for (int v = 0; v < V; ++v) {
+          const float xv = cur[r].get(v);
           float s[K];
 #pragma unroll
           for (int k = 0; k < K - 1; ++k) s[k] = win[v][k];
-          s[K - 1] = xr[r][v];
+          s[K - 1] = xv;
           o[v] = silu_f(conv_taps<K>(w[v], s, bias[v]));
 #pragma unroll
           for (int k = 0; k + 1 < K - 1; ++k) win[v][k] = win[v][k + 1];
-          if (K > 1) win[v][KW - 1] = xr[r][v];
+          if (K > 1) win[v][KW - 1] = xv;
         }
-        Vec<T, V>::store(ub + (t + r) * a.ld_u, o);
+        R::store(ub + (t + r) * a.ld_u, o);
       }
     }
+#pragma unroll
+    for (int r = 0; r < kConvRows; ++r) cur[r] = nxt[r];
   }
 
   if (tile == 0 && a.state_out) {
@@ -147,10 +161,10 @@ __global__ void __launch_bounds__(kConvThreads)
         for (int v = 0; v < V; ++v)
           fin[v][k] = a.state_in ? a.state_in[(b * Di + c0 + v) * K + j] : 0.0f;
       } else {
-        float r[V];
-        Vec<T, V>::load(xb + (j - K) * a.ld_x, r);
+        R r;
+        r.load(xb + (j - K) * a.ld_x);
 #pragma unroll
-        for (int v = 0; v < V; ++v) fin[v][k] = r[v];
+        for (int v = 0; v < V; ++v) fin[v][k] = r.get(v);
       }
     }
 #pragma unroll
@@ -194,15 +208,14 @@ template <int K, typename T>
 __global__ void __launch_bounds__(kStepThreads) conv1d_silu_step_kernel(ConvStepArgs a) {
   const int64_t i = (int64_t)blockIdx.x * kStepThreads + threadIdx.x;  // b * Di + c
   if (i >= a.B * a.Di) return;
-  const int64_t c = i % a.Di;
+  const int64_t c = (a.B * a.Di < (int64_t(1) << 31)) ? (int64_t)((uint32_t)i % (uint32_t)a.Di) : i % a.Di;
   float* st = a.state + i * K;
   float old[K], s[K], w[K];
   load_window<K>(st, old);
+  load_window<K>(a.w + c * K, w);
 #pragma unroll
   for (int k = 0; k + 1 < K; ++k) s[k] = old[k + 1];
   s[K - 1] = to_f32(reinterpret_cast<const T*>(a.x)[i]);
-#pragma unroll
-  for (int k = 0; k < K; ++k) w[k] = a.w[c * K + k];
   const float bias = a.bias ? a.bias[c] : 0.0f;
   reinterpret_cast<T*>(a.u)[i] = from_f32<T>(silu_f(conv_taps<K>(w, s, bias)));
   store_window<K>(st, s);
@@ -210,26 +223,26 @@ __global__ void __launch_bounds__(kStepThreads) conv1d_silu_step_kernel(ConvStep
 
 template <int K, typename T>
 cudaError_t prefill_launch(const ConvPrefillArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  constexpr int VV = 16 / sizeof(T);
   const int es = sizeof(T);
-  const bool vec = (reinterpret_cast<uintptr_t>(a.x) % 16 == 0) &&
-                   (reinterpret_cast<uintptr_t>(a.u) % 16 == 0) && ((a.ld_x * es) % 16 == 0) &&
-                   ((a.ld_u * es) % 16 == 0) && (a.Di % VV == 0);
-  const int V = vec ? VV : 1;
+  const int vb = 4 * es;  // bytes of a 4-channel access
+  const bool vec = (reinterpret_cast<uintptr_t>(a.x) % vb == 0) &&
+                   (reinterpret_cast<uintptr_t>(a.u) % vb == 0) && ((a.ld_x * es) % vb == 0) &&
+                   ((a.ld_u * es) % vb == 0) && (a.Di % 4 == 0);
+  const int V = vec ? 4 : 1;
   const int64_t ncv = (a.Di + V - 1) / V;
-  // tokens per thread: enough threads for ~2 full waves, at least K (tile 0
-  // must be the only reader of the old state), a multiple of the unroll
+  // tokens per thread: enough threads for ~2 waves at full occupancy, at least
+  // K (tile 0 must be the only reader of the old state), a multiple of the batch
   const int64_t want_threads = (int64_t)dev.sm_count * 2048 * 2;
   int64_t tt = (a.B * a.T * ncv + want_threads - 1) / want_threads;
-  tt = ((tt + kConvUnroll - 1) / kConvUnroll) * kConvUnroll;
+  tt = ((tt + kConvRows - 1) / kConvRows) * kConvRows;
   tt = tt < 8 ? 8 : (tt > 256 ? 256 : tt);
-  if (tt < K) tt = ((K + kConvUnroll - 1) / kConvUnroll) * kConvUnroll;
+  if (tt < K) tt = ((K + kConvRows - 1) / kConvRows) * kConvRows;
   const int64_t n_tiles = (a.T + tt - 1) / tt;
   const int64_t n_cblk = (ncv + kConvThreads - 1) / kConvThreads;
   const int64_t blocks = n_cblk * n_tiles * a.B;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   if (vec)
-    conv1d_silu_prefill_kernel<K, T, VV>
+    conv1d_silu_prefill_kernel<K, T, 4>
         <<<(unsigned)blocks, kConvThreads, 0, stream>>>(a, (int)tt, n_cblk, n_tiles);
   else
     conv1d_silu_prefill_kernel<K, T, 1>

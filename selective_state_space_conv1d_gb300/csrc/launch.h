@@ -68,21 +68,20 @@ struct ScanArgs {
   int N;
 };
 
-// How a prefill is cut into CTAs: each CTA owns `ct` channels of one batch
-// row for all T, with `g` thread groups that split every staged chunk of
-// tc = g * ls rows into g segments (g == 1: one sequential pass).
+// How a prefill is launched: one sequential pass per channel tile (parts == 1)
+// or a T split into `parts` parts of `part_len` rows (two launches, needs
+// workspace_bytes of caller workspace).
 struct ScanPlan {
-  int ct;      // channels per CTA
-  int g;       // segments per chunk
-  int ls;      // rows per segment
-  int stages;  // cp.async pipeline depth
-  int act_vec; // u/dt/z staged with 16-byte copies (else element loads)
-  int bc_vec;  // B/C staged with 16-byte copies
-  int bc_pad;  // B/C smem row stride in elements (>= N)
-  int64_t smem_bytes;
+  int parts;
+  int64_t part_len;
+  int act_vec;  // u/dt/z staged with 16-byte copies (else element loads)
+  int bc_vec;   // B/C staged with 16-byte copies
+  int64_t workspace_bytes;
 };
-ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev);
-cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& plan,
+int scan_parts(int64_t B, int64_t T, int64_t Di, const DeviceInfo& dev);
+int64_t scan_workspace_bytes(int64_t B, int64_t Di, int64_t N, int parts);
+ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t workspace_bytes);
+cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& plan, float* ws,
                                           const DeviceInfo& dev, cudaStream_t stream);
 
 struct SsmStepArgs {

@@ -1,5 +1,5 @@
-// scan_prefill.cu - chunked selective scan with fused softplus, D skip and
-// SiLU(z) gate, continuing from (and returning) the SSM state.
+// scan_prefill.cu - selective scan over T tokens with fused softplus, D skip
+// and SiLU(z) gate, continuing from (and returning) the SSM state.
 //
 // mamba-rs prefill.rs `prefill_body` F4c/F4d computes, per (batch, channel),
 //   delta_t = softplus(dt_t + dt_bias),  h_t = exp(delta_t A) h_{t-1} + delta_t B_t u_t,
@@ -7,26 +7,30 @@
 // ("do NOT zero, we build on top"), with A = -exp(A_log) (inference.rs
 // `GpuMambaInference::new`).  The reference routes short prompts to a
 // sequential kernel and long ones to a parallel one (`use_parallel(t, ds)`);
-// here one kernel covers both, picking its T split from the shape.
+// here the route is picked from the shape (batch x channels vs SM count).
 //
 // Design (GB300):
-//  * A CTA owns `ct` consecutive channels of one batch row for all T.  Lanes
-//    run along the contiguous channel axis, so every global access of u, dt, z
-//    and y is coalesced, and B_t / C_t (shared by all channels of a row) are
-//    staged once per CTA and read as shared-memory broadcasts.
-//  * u, dt, z, B, C arrive in chunks of tc rows through a 3-deep cp.async
-//    ring (16-byte copies, L2-only), so HBM traffic is one read of every
-//    input and one write of y; state stays in registers (f32) throughout.
-//  * A thread keeps all N states of its channel in registers and walks its
-//    rows sequentially.  The state math is packed f32x2 (FFMA2 / FMUL2) plus
+//  * One warp per CTA; lane = channel, 32 consecutive channels of one batch
+//    row, so every global access of u, dt, z and y is a coalesced row segment
+//    and B_t / C_t (shared by all channels) are shared-memory broadcasts.  All
+//    synchronisation is __syncwarp; 1-warp CTAs also give fine-grained load
+//    balance over the 152 SMs.
+//  * u, dt, z, B, C stream in chunks of TC rows through a 3-deep cp.async ring
+//    (16-byte copies, L2-only): HBM sees one read of every input and one write
+//    of y.  bf16 B/C rows are widened to f32 once per chunk in shared memory.
+//  * A lane keeps all N states of its channel in registers (f32) and walks the
+//    rows sequentially; two rows are issued together so the exps of the second
+//    overlap the state FMAs of the first.  The state math is packed f32x2 plus
 //    one MUFU ex2 per state and token; no tensor cores (no contraction).
-//  * Narrow shapes (few batch*channel rows, e.g. one 130m layer at batch 1)
-//    split each chunk into g segments handled by g thread groups:
-//      pass 1: every segment but the last scans from a zero state and keeps
-//              its end state and total decay exp(A * sum delta);
-//      fold:   one thread per (channel, state) chains the segments' carries;
-//      pass 2: every segment rescans from its true carry-in and writes y.
-//    The split costs a second exp per state and token but no extra HBM traffic.
+//  * Route "sequential" (wide shapes: enough batch x channel rows to fill the
+//    GPU): one launch, each CTA scans all T for its channels.
+//  * Route "T-split" (narrow shapes, e.g. one 130m layer at batch 1): T is cut
+//    into P parts.  Launch 1 scans parts 0..P-2 from a zero state and writes
+//    each part's end state and total decay exp(A sum delta) to a workspace
+//    (plus a snapshot of state_in).  Launch 2 folds the aggregates of the
+//    preceding parts into each part's carry-in, then rescans the part from it
+//    and writes y; the last part writes state_out.  Cost: the state-only
+//    rescan of P-1 parts; no cross-CTA waiting.
 #include "device_math.cuh"
 #include "launch.h"
 
@@ -34,18 +38,23 @@ namespace mamba {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kMaxThreads = 256;
+constexpr int kLanes = 32;  // channels per CTA (one warp)
 
-struct ScanLayout {
-  int tc, ct, es, npad, g, n;
-  __host__ __device__ int64_t act_tile() const { return (int64_t)tc * ct * es; }
-  __host__ __device__ int64_t bc_tile() const { return (int64_t)tc * npad * es; }
-  __host__ __device__ int64_t stage_bytes() const { return 3 * act_tile() + 2 * bc_tile(); }
-  __host__ __device__ int64_t fold_offset() const { return kStages * stage_bytes(); }
-  __host__ __device__ int64_t fold_bytes() const {
-    return g > 1 ? (int64_t)(2 * g + 1) * ct * n * 4 : 0;
-  }
-  __host__ __device__ int64_t total() const { return fold_offset() + fold_bytes(); }
+template <typename Tin>
+struct Tile {
+  static constexpr int TC = 16;                            // rows per staged chunk
+  static constexpr int LOG_TC = 4;
+  static constexpr int ES = sizeof(Tin);
+  static constexpr int GA = kLanes * ES / 16;              // 16-byte granules per act row
+  static constexpr int LOG_GA = GA == 8 ? 3 : (GA == 4 ? 2 : (GA == 2 ? 1 : 0));
+};
+
+template <int N, typename Tin>
+struct Smem {
+  Tin act[kStages][3][Tile<Tin>::TC][kLanes];  // u, dt, z
+  Tin bc[kStages][2][Tile<Tin>::TC][N];        // B, C as staged (storage dtype)
+  // bf16 only: this chunk's B, C widened to f32
+  float bcf[sizeof(Tin) == 4 ? 1 : 2][sizeof(Tin) == 4 ? 1 : Tile<Tin>::TC][sizeof(Tin) == 4 ? 4 : N];
 };
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
@@ -58,30 +67,21 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(Pending) : "memory");
 }
 
-// P consecutive elements of a staged row, widened to f32.
-template <int P, typename Tin>
-__device__ __forceinline__ void load_group(const Tin* p, float (&o)[P]) {
-  if constexpr (sizeof(Tin) == 4 && P % 4 == 0) {
+template <int P>
+__device__ __forceinline__ void lds_f32(const float* p, float (&o)[P]) {
+  if constexpr (P % 4 == 0) {
 #pragma unroll
     for (int j = 0; j < P; j += 4) {
       const float4 v = *reinterpret_cast<const float4*>(p + j);
       o[j] = v.x; o[j + 1] = v.y; o[j + 2] = v.z; o[j + 3] = v.w;
     }
-  } else if constexpr (sizeof(Tin) == 2 && P == 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      o[2 * i] = __uint_as_float(w[i] << 16);
-      o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
   } else {
 #pragma unroll
-    for (int j = 0; j < P; ++j) o[j] = to_f32(p[j]);
+    for (int j = 0; j < P; ++j) o[j] = p[j];
   }
 }
 
-// State-only update of a group (pass 1: no output needed).
+// State-only update (pass 1 of the T split).
 template <int P>
 __device__ __forceinline__ void ssm_state_group(float* h, const float* a2, float delta, float du,
                                                 const float* Bv) {
@@ -102,27 +102,42 @@ __device__ __forceinline__ void ssm_state_group(float* h, const float* a2, float
   }
 }
 
-template <int N, typename Tin>
-__global__ void __launch_bounds__(kMaxThreads)
-    selective_scan_prefill_kernel(ScanArgs a, ScanLayout L, int ls, int act_vec, int bc_vec,
-                                  int64_t n_cblk) {
+struct ScanWork {
+  float* ws;           // T-split workspace (null for the sequential route)
+  int parts;           // P
+  int64_t part_len;    // rows per part (the last part may be shorter)
+  int64_t n_tiles;     // channel tiles per batch row
+  int64_t grid_parts;  // parts covered by this launch's grid
+};
+
+enum Mode { kSequential = 0, kPass1 = 1, kPass2 = 2 };
+
+template <int N, typename Tin, int MODE>
+__global__ void __launch_bounds__(kLanes) selective_scan_kernel(ScanArgs a, ScanWork w, int act_vec,
+                                                                int bc_vec) {
+  using TL = Tile<Tin>;
+  constexpr int TC = TL::TC;
   constexpr int P = group_size(N);
   constexpr int NG = N / P;
-  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr bool kBf16 = sizeof(Tin) == 2;
+  __shared__ __align__(16) Smem<N, Tin> sm;
 
-  const int tid = threadIdx.x;
-  const int nthr = blockDim.x;
-  const int ct = L.ct, gcnt = L.g, tc = L.tc;
-  const int cl = tid % ct;
-  const int g = tid / ct;
-  const int64_t cblk = blockIdx.x % n_cblk;
-  const int64_t b = blockIdx.x / n_cblk;
-  const int64_t c0 = cblk * ct;
-  const int64_t c = c0 + cl;
+  const int lane = threadIdx.x;
+  int64_t blk = blockIdx.x;
+  const int64_t part = blk % w.grid_parts;
+  blk /= w.grid_parts;
+  const int64_t tile = blk % w.n_tiles;
+  const int64_t b = blk / w.n_tiles;
+  const int64_t c0 = tile * kLanes;
+  const int64_t c = c0 + lane;
   const int64_t Di = a.Di, T = a.T;
   const bool active = c < Di;
   const int64_t cc = active ? c : Di - 1;
-  const bool gate = a.z != nullptr;
+  const bool gate = (MODE != kPass1) && a.z != nullptr;
+  const int64_t t_begin = part * w.part_len;
+  const int64_t t_end = min(T, t_begin + w.part_len);
+  const int64_t BDN = a.B * Di * N;
+  const int64_t srow = (b * Di + cc) * N;  // this lane's state row
 
   float a2[N];
 #pragma unroll
@@ -130,250 +145,242 @@ __global__ void __launch_bounds__(kMaxThreads)
   const float dtb = a.dt_bias ? a.dt_bias[cc] : 0.0f;
   const float Dc = a.D ? a.D[cc] : 0.0f;
 
-  float* foldP = reinterpret_cast<float*>(smem + L.fold_offset());  // [g][ct][N]
-  float* foldH = foldP + (int64_t)gcnt * ct * N;                    // [g][ct][N]
-  float* carry = foldH + (int64_t)gcnt * ct * N;                    // [ct][N]
-
+  // ---- carry-in ----
   float h[N];
-  if (gcnt == 1) {
+  if (MODE == kSequential) {
 #pragma unroll
-    for (int n = 0; n < N; ++n)
-      h[n] = (active && a.state_in) ? a.state_in[(b * Di + c) * N + n] : 0.0f;
-  } else if (g == 0) {
+    for (int n = 0; n < N; ++n) h[n] = (active && a.state_in) ? a.state_in[srow + n] : 0.0f;
+  } else if (MODE == kPass1) {
 #pragma unroll
-    for (int n = 0; n < N; ++n)
-      carry[cl * N + n] = (active && a.state_in) ? a.state_in[(b * Di + c) * N + n] : 0.0f;
+    for (int n = 0; n < N; ++n) h[n] = 0.0f;
+    if (part == 0 && active) {  // snapshot of the initial state for launch 2
+#pragma unroll
+      for (int n = 0; n < N; ++n) w.ws[srow + n] = a.state_in ? a.state_in[srow + n] : 0.0f;
+    }
+  } else {
+    // fold the preceding parts, H <- P_j H + Hloc_j, starting from the snapshot
+#pragma unroll
+    for (int n = 0; n < N; ++n) h[n] = w.ws[srow + n];
+    for (int64_t j = 0; j < part; ++j) {
+      float pj[N], hj[N];
+      lds_f32<N>(w.ws + BDN * (1 + 2 * j) + srow, pj);
+      lds_f32<N>(w.ws + BDN * (2 + 2 * j) + srow, hj);
+#pragma unroll
+      for (int n = 0; n < N; ++n) h[n] = fmaf(pj[n], h[n], hj[n]);
+    }
   }
 
-  // ---- staging of chunk k (rows k*tc ..) into ring slot `stage` ----
-  // source tensor `tens` of the activation tiles (0 u, 1 dt, 2 z) and of B/C
+  // ---- staging of chunk k (rows t_begin + k*TC ..) into ring slot `stage` ----
+  const int ntens = gate ? 3 : 2;            // pass 1 needs u and dt only
+  const int nbc = MODE == kPass1 ? 1 : 2;    // pass 1 needs B only
   auto act_src = [&](int tens) {
     return reinterpret_cast<const Tin*>(tens == 0 ? a.u : (tens == 1 ? a.dt : a.z));
   };
   auto act_ld = [&](int tens) { return tens == 0 ? a.ld_u : (tens == 1 ? a.ld_dt : a.ld_z); };
-  auto bc_src = [&](int tens) { return reinterpret_cast<const Tin*>(tens == 0 ? a.Bm : a.Cm); };
-  auto bc_ld = [&](int tens) { return tens == 0 ? a.ld_B : a.ld_C; };
-  const int ntens = gate ? 3 : 2;
-  const int es = (int)sizeof(Tin);
 
   auto issue = [&](int64_t k, int stage) {
-    const int64_t row0 = k * tc;
-    const int rows = (int)min((int64_t)tc, T - row0);
-    unsigned char* sb = smem + stage * L.stage_bytes();
-    const int64_t grow0 = b * T + row0;  // global row of the chunk's first token
+    const int64_t row0 = t_begin + k * TC;
+    const int rows = (int)min((int64_t)TC, t_end - row0);
+    const int64_t grow0 = b * T + row0;
     if (act_vec) {
-      const int gA = ct * es / 16;  // 16-byte granules per tile row
-      const int total = ntens * rows * gA;
-      for (int i = tid; i < total; i += nthr) {
-        const int q = i % gA;
-        const int ra = i / gA;
-        const int tens = ra / rows;
-        const int r = ra - tens * rows;
-        const int64_t ch = c0 + (int64_t)q * (16 / es);
-        if (ch < Di) {
-          const Tin* src = act_src(tens) + (grow0 + r) * act_ld(tens) + ch;
-          Tin* dst = reinterpret_cast<Tin*>(sb + tens * L.act_tile()) + r * ct + q * (16 / es);
-          cp_async16(dst, src);
-        }
+      // granule i: tensor i / (TC*GA), row (i / GA) % TC, granule-in-row i % GA
+      const int total = ntens * TC * TL::GA;
+      for (int i = lane; i < total; i += kLanes) {
+        const int q = i & (TL::GA - 1);
+        const int r = (i >> TL::LOG_GA) & (TC - 1);
+        const int tens = i >> (TL::LOG_GA + TL::LOG_TC);
+        const int64_t ch = c0 + q * (16 / TL::ES);
+        if (r < rows && ch < Di)
+          cp_async16(&sm.act[stage][tens][r][q * (16 / TL::ES)],
+                     act_src(tens) + (grow0 + r) * act_ld(tens) + ch);
       }
     } else {
-      const int total = ntens * rows * ct;
-      for (int i = tid; i < total; i += nthr) {
-        const int e = i % ct;
-        const int ra = i / ct;
-        const int tens = ra / rows;
-        const int r = ra - tens * rows;
-        if (c0 + e < Di) {
-          Tin* dst = reinterpret_cast<Tin*>(sb + tens * L.act_tile()) + r * ct + e;
-          *dst = act_src(tens)[(grow0 + r) * act_ld(tens) + c0 + e];
-        }
-      }
+      for (int tens = 0; tens < ntens; ++tens)
+        for (int r = 0; r < rows; ++r)
+          if (active) sm.act[stage][tens][r][lane] = act_src(tens)[(grow0 + r) * act_ld(tens) + c];
     }
-    unsigned char* sbc = sb + 3 * L.act_tile();
-    // granules per B/C row; bc_vec is only ever set when a row is >= 16 bytes
-    constexpr int gB = (N * (int)sizeof(Tin)) / 16 > 0 ? (N * (int)sizeof(Tin)) / 16 : 1;
-    if (bc_vec && N * (int)sizeof(Tin) >= 16) {
-      const int total = 2 * rows * gB;
-      for (int i = tid; i < total; i += nthr) {
-        const int q = i % gB;
-        const int ra = i / gB;
-        const int tens = ra / rows;
-        const int r = ra - tens * rows;
-        const Tin* src = bc_src(tens) + (grow0 + r) * bc_ld(tens) + q * (16 / es);
-        Tin* dst = reinterpret_cast<Tin*>(sbc + tens * L.bc_tile()) + r * L.npad + q * (16 / es);
-        cp_async16(dst, src);
+    constexpr int GB = (N * TL::ES) / 16 > 0 ? (N * TL::ES) / 16 : 1;  // granules per B/C row
+    if (bc_vec && N * TL::ES >= 16) {
+      const int total = nbc * TC * GB;
+      for (int i = lane; i < total; i += kLanes) {
+        const int q = i % GB;
+        const int r = (i / GB) % TC;
+        const int tens = i / (GB * TC);
+        const Tin* src = reinterpret_cast<const Tin*>(tens == 0 ? a.Bm : a.Cm);
+        const int64_t ld = tens == 0 ? a.ld_B : a.ld_C;
+        if (r < rows)
+          cp_async16(&sm.bc[stage][tens][r][q * (16 / TL::ES)], src + (grow0 + r) * ld + q * (16 / TL::ES));
       }
     } else {
-      const int total = 2 * rows * N;
-      for (int i = tid; i < total; i += nthr) {
+      for (int i = lane; i < nbc * TC * N; i += kLanes) {
         const int n = i % N;
-        const int ra = i / N;
-        const int tens = ra / rows;
-        const int r = ra - tens * rows;
-        Tin* dst = reinterpret_cast<Tin*>(sbc + tens * L.bc_tile()) + r * L.npad + n;
-        *dst = bc_src(tens)[(grow0 + r) * bc_ld(tens) + n];
+        const int r = (i / N) % TC;
+        const int tens = i / (N * TC);
+        const Tin* src = reinterpret_cast<const Tin*>(tens == 0 ? a.Bm : a.Cm);
+        const int64_t ld = tens == 0 ? a.ld_B : a.ld_C;
+        if (r < rows) sm.bc[stage][tens][r][n] = src[(grow0 + r) * ld + n];
       }
     }
   };
 
-  const int64_t nchunks = (T + tc - 1) / tc;
+  const int64_t nrows = max((int64_t)0, t_end - t_begin);
+  const int64_t nchunks = (nrows + TC - 1) / TC;
 #pragma unroll 1
   for (int s = 0; s < kStages - 1; ++s) {
     if (s < nchunks) issue(s, s);
     cp_async_commit();
   }
 
+  float sdelta = 0.0f;  // pass 1: sum of delta over the part
 #pragma unroll 1
   for (int64_t k = 0; k < nchunks; ++k) {
     cp_async_wait<kStages - 2>();
-    __syncthreads();  // chunk k is visible; every thread is done with chunk k-1
+    __syncwarp();  // chunk k visible to every lane; every lane is done with chunk k-1
+    const int stage = (int)(k % kStages);
+    const int rows = (int)min((int64_t)TC, nrows - k * TC);
+    const float* sB;
+    const float* sC;
+    if constexpr (kBf16) {
+      // widen this chunk's B (and C) rows to f32 once, shared by all lanes
+      for (int i = lane; i < nbc * TC * N; i += kLanes) {
+        const int n = i % N;
+        const int r = (i / N) % TC;
+        const int tens = i / (N * TC);
+        if (r < rows) sm.bcf[tens][r][n] = to_f32(sm.bc[stage][tens][r][n]);
+      }
+      __syncwarp();
+      sB = &sm.bcf[0][0][0];
+      sC = &sm.bcf[nbc - 1][0][0];
+    } else {
+      sB = reinterpret_cast<const float*>(&sm.bc[stage][0][0][0]);
+      sC = reinterpret_cast<const float*>(&sm.bc[stage][1][0][0]);
+    }
     if (k + kStages - 1 < nchunks) issue(k + kStages - 1, (int)((k + kStages - 1) % kStages));
     cp_async_commit();
 
-    const unsigned char* sb = smem + (k % kStages) * L.stage_bytes();
-    const Tin* su = reinterpret_cast<const Tin*>(sb);
-    const Tin* sdt = reinterpret_cast<const Tin*>(sb + L.act_tile());
-    const Tin* sz = reinterpret_cast<const Tin*>(sb + 2 * L.act_tile());
-    const Tin* sB = reinterpret_cast<const Tin*>(sb + 3 * L.act_tile());
-    const Tin* sC = reinterpret_cast<const Tin*>(sb + 3 * L.act_tile() + L.bc_tile());
-    const int rows = (int)min((int64_t)tc, T - k * tc);
-    const int r0 = g * ls;
-    const int nr = max(0, min(ls, rows - r0));
+    const Tin* su = &sm.act[stage][0][0][0];
+    const Tin* sdt = &sm.act[stage][1][0][0];
+    const Tin* sz = &sm.act[stage][2][0][0];
 
-    if (gcnt > 1) {
-      // pass 1: end state and total decay of every segment but the last
-      if (g < gcnt - 1) {
-        float hl[N];
-#pragma unroll
-        for (int n = 0; n < N; ++n) hl[n] = 0.0f;
-        float sd = 0.0f;
-        const int nr1 = active ? nr : 0;
-#pragma unroll 1
-        for (int i = 0; i < nr1; ++i) {
-          const int row = r0 + i;
-          const float uv = to_f32(su[row * ct + cl]);
-          const float delta = softplus_f(to_f32(sdt[row * ct + cl]) + dtb);
-          sd += delta;
+    if (MODE == kPass1) {
+      if (active) {
+#pragma unroll 2
+        for (int r = 0; r < rows; ++r) {
+          const float uv = to_f32(su[r * kLanes + lane]);
+          const float delta = softplus_f(to_f32(sdt[r * kLanes + lane]) + dtb);
+          sdelta += delta;
           const float du = delta * uv;
 #pragma unroll
           for (int q = 0; q < NG; ++q) {
             float Bv[P];
-            load_group<P>(sB + row * L.npad + q * P, Bv);
-            ssm_state_group<P>(hl + q * P, a2 + q * P, delta, du, Bv);
+            lds_f32<P>(sB + r * N + q * P, Bv);
+            ssm_state_group<P>(h + q * P, a2 + q * P, delta, du, Bv);
           }
         }
-#pragma unroll
-        for (int n = 0; n < N; ++n) {
-          foldP[(g * ct + cl) * N + n] = ex2_approx(a2[n] * sd);
-          foldH[(g * ct + cl) * N + n] = hl[n];
-        }
       }
-      __syncthreads();
-      // fold: chain the carries through the segments, one (channel, state) per thread
-      for (int w = tid; w < ct * N; w += nthr) {
-        float H = carry[w];
-#pragma unroll 4
-        for (int gg = 0; gg < gcnt - 1; ++gg) {
-          const int idx = gg * ct * N + w;
-          const float hl = foldH[idx];
-          foldH[idx] = H;
-          H = fmaf(foldP[idx], H, hl);
-        }
-        foldH[(gcnt - 1) * ct * N + w] = H;
-      }
-      __syncthreads();
-#pragma unroll
-      for (int n = 0; n < N; ++n) h[n] = foldH[(g * ct + cl) * N + n];
-    }
-
-    // pass 2: scan the segment from its carry-in and write y
-    if (active) {
-      const int64_t grow = b * T + k * tc + r0;
-#pragma unroll 2
-      for (int i = 0; i < nr; ++i) {
-        const int row = r0 + i;
-        const float uv = to_f32(su[row * ct + cl]);
-        const float delta = softplus_f(to_f32(sdt[row * ct + cl]) + dtb);
-        const float du = delta * uv;
-        float part[NG];
+    } else if (active) {
+      const int64_t grow = b * T + t_begin + k * TC;
+      int r = 0;
+      // two rows per iteration: the second row's exps do not depend on the
+      // first row's state update and overlap it
+#pragma unroll 1
+      for (; r + 1 < rows; r += 2) {
+        const float u0 = to_f32(su[r * kLanes + lane]);
+        const float u1 = to_f32(su[(r + 1) * kLanes + lane]);
+        const float d0 = softplus_f(to_f32(sdt[r * kLanes + lane]) + dtb);
+        const float d1 = softplus_f(to_f32(sdt[(r + 1) * kLanes + lane]) + dtb);
+        const float z0 = gate ? to_f32(sz[r * kLanes + lane]) : 0.0f;
+        const float z1 = gate ? to_f32(sz[(r + 1) * kLanes + lane]) : 0.0f;
+        const float du0 = d0 * u0, du1 = d1 * u1;
+        float p0[NG], p1[NG];
 #pragma unroll
         for (int q = 0; q < NG; ++q) {
           float Bv[P], Cv[P];
-          load_group<P>(sB + row * L.npad + q * P, Bv);
-          load_group<P>(sC + row * L.npad + q * P, Cv);
-          part[q] = ssm_token_group<P>(h + q * P, a2 + q * P, delta, du, Bv, Cv);
+          lds_f32<P>(sB + r * N + q * P, Bv);
+          lds_f32<P>(sC + r * N + q * P, Cv);
+          p0[q] = ssm_token_group<P>(h + q * P, a2 + q * P, d0, du0, Bv, Cv);
         }
-        const float zv = gate ? to_f32(sz[row * ct + cl]) : 0.0f;
-        const float yv = ssm_output(tree_sum<NG>(part), Dc, uv, gate, zv);
-        store_out(a.y, (grow + i) * a.ld_y + c, a.y_bf16, yv);
-      }
-    }
-    if (gcnt > 1 && rows > 0 && g == (rows - 1) / ls) {
-      // the segment holding the chunk's last row hands its state to the next chunk
 #pragma unroll
-      for (int n = 0; n < N; ++n) carry[cl * N + n] = h[n];
+        for (int q = 0; q < NG; ++q) {
+          float Bv[P], Cv[P];
+          lds_f32<P>(sB + (r + 1) * N + q * P, Bv);
+          lds_f32<P>(sC + (r + 1) * N + q * P, Cv);
+          p1[q] = ssm_token_group<P>(h + q * P, a2 + q * P, d1, du1, Bv, Cv);
+        }
+        store_out(a.y, (grow + r) * a.ld_y + c, a.y_bf16, ssm_output(tree_sum<NG>(p0), Dc, u0, gate, z0));
+        store_out(a.y, (grow + r + 1) * a.ld_y + c, a.y_bf16, ssm_output(tree_sum<NG>(p1), Dc, u1, gate, z1));
+      }
+      if (r < rows) {
+        const float u0 = to_f32(su[r * kLanes + lane]);
+        const float d0 = softplus_f(to_f32(sdt[r * kLanes + lane]) + dtb);
+        const float z0 = gate ? to_f32(sz[r * kLanes + lane]) : 0.0f;
+        const float du0 = d0 * u0;
+        float p0[NG];
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+          float Bv[P], Cv[P];
+          lds_f32<P>(sB + r * N + q * P, Bv);
+          lds_f32<P>(sC + r * N + q * P, Cv);
+          p0[q] = ssm_token_group<P>(h + q * P, a2 + q * P, d0, du0, Bv, Cv);
+        }
+        store_out(a.y, (grow + r) * a.ld_y + c, a.y_bf16, ssm_output(tree_sum<NG>(p0), Dc, u0, gate, z0));
+      }
     }
   }
   cp_async_wait<0>();
 
-  if (gcnt == 1) {
-    if (active && a.state_out) {
+  if (!active) return;
+  if (MODE == kPass1) {
+    float* Pj = w.ws + BDN * (1 + 2 * part) + srow;
+    float* Hj = w.ws + BDN * (2 + 2 * part) + srow;
 #pragma unroll
-      for (int n = 0; n < N; ++n) a.state_out[(b * Di + c) * N + n] = h[n];
+    for (int n = 0; n < N; ++n) {
+      Pj[n] = ex2_approx(a2[n] * sdelta);
+      Hj[n] = h[n];
     }
-  } else {
-    __syncthreads();
-    if (g == 0 && active && a.state_out) {
+  } else if (a.state_out && (MODE == kSequential || part == w.parts - 1)) {
 #pragma unroll
-      for (int n = 0; n < N; ++n) a.state_out[(b * Di + c) * N + n] = carry[cl * N + n];
-    }
+    for (int n = 0; n < N; ++n) a.state_out[srow + n] = h[n];
   }
-}
-
-ScanLayout layout_of(const ScanArgs& a, const ScanPlan& p) {
-  ScanLayout L;
-  L.tc = p.g * p.ls;
-  L.ct = p.ct;
-  L.es = a.in_bf16 ? 2 : 4;
-  L.npad = p.bc_pad;
-  L.g = p.g;
-  L.n = a.N;
-  return L;
 }
 
 template <int N, typename Tin>
-cudaError_t launch_n(const ScanArgs& a, const ScanPlan& p, cudaStream_t stream) {
-  const ScanLayout L = layout_of(a, p);
-  const int64_t smem = L.total();
-  auto kern = selective_scan_prefill_kernel<N, Tin>;
-  static thread_local int opted_device = -1;
-  static thread_local int64_t opted_bytes = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (smem > 48 * 1024 && (opted_device != dev || opted_bytes < smem)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    opted_device = dev;
-    opted_bytes = smem;
+cudaError_t launch_n(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream_t stream) {
+  ScanWork w;
+  w.ws = ws;
+  w.parts = p.parts;
+  w.part_len = p.part_len;
+  w.n_tiles = (a.Di + kLanes - 1) / kLanes;
+  if (p.parts <= 1) {
+    w.grid_parts = 1;
+    const int64_t blocks = w.n_tiles * a.B;
+    if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+    selective_scan_kernel<N, Tin, kSequential>
+        <<<(unsigned)blocks, kLanes, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
+    return cudaGetLastError();
   }
-  const int64_t n_cblk = (a.Di + p.ct - 1) / p.ct;
-  const int64_t blocks = n_cblk * a.B;
-  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  kern<<<(unsigned)blocks, p.ct * p.g, (size_t)smem, stream>>>(a, L, p.ls, p.act_vec, p.bc_vec,
-                                                               n_cblk);
+  w.grid_parts = p.parts - 1;
+  int64_t blocks = w.n_tiles * a.B * w.grid_parts;
+  if (w.n_tiles * a.B * p.parts > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  selective_scan_kernel<N, Tin, kPass1><<<(unsigned)blocks, kLanes, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  w.grid_parts = p.parts;
+  blocks = w.n_tiles * a.B * w.grid_parts;
+  selective_scan_kernel<N, Tin, kPass2><<<(unsigned)blocks, kLanes, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
   return cudaGetLastError();
 }
 
 template <typename Tin>
-cudaError_t launch_t(const ScanArgs& a, const ScanPlan& p, cudaStream_t s) {
+cudaError_t launch_t(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream_t s) {
   switch (a.N) {
-    case 1: return launch_n<1, Tin>(a, p, s);
-    case 2: return launch_n<2, Tin>(a, p, s);
-    case 4: return launch_n<4, Tin>(a, p, s);
-    case 8: return launch_n<8, Tin>(a, p, s);
-    case 16: return launch_n<16, Tin>(a, p, s);
-    case 32: return launch_n<32, Tin>(a, p, s);
-    case 64: return launch_n<64, Tin>(a, p, s);
+    case 1: return launch_n<1, Tin>(a, p, ws, s);
+    case 2: return launch_n<2, Tin>(a, p, ws, s);
+    case 4: return launch_n<4, Tin>(a, p, ws, s);
+    case 8: return launch_n<8, Tin>(a, p, ws, s);
+    case 16: return launch_n<16, Tin>(a, p, ws, s);
+    case 32: return launch_n<32, Tin>(a, p, ws, s);
+    case 64: return launch_n<64, Tin>(a, p, ws, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -382,49 +389,55 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) =
 
 }  // namespace
 
-ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev) {
+int64_t scan_workspace_bytes(int64_t B, int64_t Di, int64_t N, int parts) {
+  if (parts <= 1) return 0;
+  return (int64_t)(1 + 2 * (parts - 1)) * B * Di * N * (int64_t)sizeof(float);
+}
+
+int scan_parts(int64_t B, int64_t T, int64_t Di, const DeviceInfo& dev) {
+  // Number of T parts P.  With w = ceil(tiles * P / SMs) one-warp CTAs per SM,
+  // an SM needs about kWarpsSat warps to keep its pipes busy, and every part but
+  // the last is scanned twice (the state-only pass costs ~3/4 of the full one),
+  // so the time is ~ ceil(T / P) * (1 + 0.75 (P-1)/P) * max(w, kWarpsSat).
+  constexpr double kWarpsSat = 6.0;
+  const int64_t tiles = B * ((Di + kLanes - 1) / kLanes);
+  double best = 0.0;
+  int best_p = 1;
+  for (int P = 1; P <= 64; ++P) {
+    if (P > 1 && T / P < 64) break;  // parts of at least 64 rows
+    const double len = (double)((T + P - 1) / P);
+    const double wv = (double)((tiles * P + dev.sm_count - 1) / dev.sm_count);
+    const double cost = len * (1.0 + 0.75 * (P - 1) / P) * (wv > kWarpsSat ? wv : kWarpsSat);
+    if (P == 1 || cost < best * 0.97) {
+      best = cost;
+      best_p = P;
+    }
+  }
+  return best_p;
+}
+
+ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t workspace_bytes) {
   ScanPlan p;
   const int es = a.in_bf16 ? 2 : 4;
   const int vw = 16 / es;
-  p.stages = kStages;
   p.act_vec = al16(a.u) && al16(a.dt) && (!a.z || al16(a.z)) && (a.ld_u * es) % 16 == 0 &&
               (a.ld_dt * es) % 16 == 0 && (!a.z || (a.ld_z * es) % 16 == 0) && a.Di % vw == 0;
   p.bc_vec = al16(a.Bm) && al16(a.Cm) && (a.ld_B * es) % 16 == 0 && (a.ld_C * es) % 16 == 0 &&
              (a.N * es) % 16 == 0;
-
-  const int64_t chans = a.B * a.Di;
-  const int64_t want_warps = 8LL * dev.sm_count;  // two resident warps per scheduler
-  int g = 1;
-  if (a.T > 64) {
-    while (g < 32 && chans * g < want_warps * 32) g *= 2;
+  p.parts = scan_parts(a.B, a.T, a.Di, dev);
+  p.workspace_bytes = scan_workspace_bytes(a.B, a.Di, a.N, p.parts);
+  if (p.workspace_bytes > workspace_bytes) {  // not enough workspace: one sequential pass
+    p.parts = 1;
+    p.workspace_bytes = 0;
   }
-  if (g == 1) {
-    p.ct = 32;
-    p.g = 1;
-    p.ls = es == 2 ? 32 : 16;
-  } else {
-    p.ct = 8;
-    if (g < 4) g = 4;  // 8 channels x g segments >= one warp
-    p.g = g;
-    p.ls = 3;          // odd: segment rows of a warp fall in distinct banks
-  }
-  // B/C row stride in smem: whole 16-byte granules; with a T split (a warp
-  // reads 32/ct different rows) an odd granule count keeps them conflict-free
-  for (;;) {
-    int gran = (a.N * es + 15) / 16;
-    if (p.g > 1 && gran % 2 == 0) gran += 1;
-    p.bc_pad = gran * 16 / es;
-    p.smem_bytes = layout_of(a, p).total();
-    if (p.smem_bytes <= dev.max_smem_optin || p.g <= 4) break;
-    p.g /= 2;  // large d_state: fewer segments per chunk until the ring + fold fit
-  }
+  p.part_len = p.parts > 1 ? (a.T + p.parts - 1) / p.parts : a.T;
   return p;
 }
 
-cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& p,
+cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& p, float* ws,
                                           const DeviceInfo& dev, cudaStream_t stream) {
   (void)dev;
-  return a.in_bf16 ? launch_t<__nv_bfloat16>(a, p, stream) : launch_t<float>(a, p, stream);
+  return a.in_bf16 ? launch_t<__nv_bfloat16>(a, p, ws, stream) : launch_t<float>(a, p, ws, stream);
 }
 
 }  // namespace mamba

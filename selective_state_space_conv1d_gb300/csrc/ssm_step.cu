@@ -7,25 +7,29 @@
 //
 // Design (GB300): the step is pure streaming of the f32 state (read once,
 // written once: 2 * 4 * N bytes per (batch, channel)).  Each lane owns one
-// group of P = min(N, 8) consecutive states of one (batch, channel) row and
-// moves them with 16-byte loads / stores; the N/P lanes of a row are adjacent,
-// so a warp touches one contiguous span of the state.  A CTA covers 32
-// channels x bt batch rows: A2 = -exp(A_log) log2(e) for its channels is
-// computed once into shared memory instead of once per batch row.  The lanes'
-// partial C . h are combined with an xor butterfly, the same pairwise tree the
-// prefill kernel uses, so one step equals a T=1 prefill bit for bit.
+// group of P = min(N, 8) consecutive states of one channel and moves them with
+// 16-byte loads / stores; the N/P lanes of a row are adjacent, so a warp
+// touches one contiguous span of the state.  A lane serves 4 batch rows of its
+// channel: A2 = -exp(A_log) log2(e) is computed once for them, and the loads of
+// all 4 rows are issued before any arithmetic (one memory round trip with
+// 4 x 32 B of state in flight per lane); B / C rows are 16-byte loads shared
+// through L1.  The lanes' partial C . h are combined with an xor butterfly,
+// the same pairwise tree the prefill kernel uses, so one step equals a T=1
+// prefill bit for bit.
 #include "device_math.cuh"
 #include "launch.h"
 
 namespace mamba {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kMaxThreads = 256;
 constexpr int kChannels = 32;  // channels per CTA
+constexpr int kRows = 4;       // batch rows per thread (loads of all rows issued together)
 
-template <int P>
-__device__ __forceinline__ void load_f32_group(const float* p, float (&o)[P], bool vec) {
-  if constexpr (P % 4 == 0) {
+// P consecutive values at p (16-byte vector loads when `vec`), widened to f32.
+template <int P, typename T>
+__device__ __forceinline__ void load_group(const T* p, float (&o)[P], bool vec) {
+  if constexpr (sizeof(T) == 4 && P % 4 == 0) {
     if (vec) {
 #pragma unroll
       for (int j = 0; j < P; j += 4) {
@@ -34,12 +38,24 @@ __device__ __forceinline__ void load_f32_group(const float* p, float (&o)[P], bo
       }
       return;
     }
+  } else if constexpr (sizeof(T) == 2 && P == 8) {
+    if (vec) {
+      const uint4 v = *reinterpret_cast<const uint4*>(p);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        o[2 * i] = __uint_as_float(w[i] << 16);
+        o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      }
+      return;
+    }
   }
 #pragma unroll
-  for (int j = 0; j < P; ++j) o[j] = p[j];
+  for (int j = 0; j < P; ++j) o[j] = to_f32(p[j]);
 }
+
 template <int P>
-__device__ __forceinline__ void store_f32_group(float* p, const float (&o)[P], bool vec) {
+__device__ __forceinline__ void store_group(float* p, const float (&o)[P], bool vec) {
   if constexpr (P % 4 == 0) {
     if (vec) {
 #pragma unroll
@@ -52,66 +68,66 @@ __device__ __forceinline__ void store_f32_group(float* p, const float (&o)[P], b
   for (int j = 0; j < P; ++j) p[j] = o[j];
 }
 
+// grid: (channel block, batch block); a CTA covers 32 channels x (bt * kRows)
+// batch rows; lane -> (batch sub-row, channel, state group), groups fastest.
 template <int N, typename Tin>
-__global__ void __launch_bounds__(kThreads) ssm_step_kernel(SsmStepArgs a, int bt, int64_t n_cblk,
-                                                            int state_vec) {
+__global__ void __launch_bounds__(kMaxThreads) ssm_step_kernel(SsmStepArgs a, int bt, int64_t n_cblk,
+                                                            int state_vec, int bc_vec) {
   constexpr int P = group_size(N);
   constexpr int NG = N / P;
-  __shared__ float s_a2[kChannels * N];
-
   const int64_t cblk = blockIdx.x % n_cblk;
   const int64_t bblk = blockIdx.x / n_cblk;
-  const int64_t c0 = cblk * kChannels;
-  const int64_t Di = a.Di;
-
-  // A2 for this CTA's channels, once
-  for (int i = threadIdx.x; i < kChannels * N; i += kThreads) {
-    const int64_t ch = c0 + i / N;
-    s_a2[i] = ch < Di ? a2_from_alog(a.A_log[ch * N + (i % N)]) : 0.0f;
-  }
-  __syncthreads();
-
-  // lane -> (batch row, channel, state group); groups fastest, then channels
   const int q = threadIdx.x % NG;
   const int cl = (threadIdx.x / NG) % kChannels;
   const int bl = threadIdx.x / (NG * kChannels);
-  const int64_t b = bblk * bt + bl;
-  const int64_t c = c0 + cl;
-  const bool valid = (bl < bt) && (b < a.B) && (c < Di);
-  // invalid lanes still join the butterfly (full-warp shuffles); they read row 0
-  const int64_t row = valid ? b * Di + c : 0;
-  const int64_t bb = valid ? b : 0;
-  const int64_t ccl = valid ? c : 0;
+  const int64_t Di = a.Di;
+  const int64_t c = cblk * kChannels + cl;
+  const bool cvalid = (bl < bt) && (c < Di);
+  const int64_t cc = cvalid ? c : 0;
 
-  float* st = a.state + row * N + q * P;
-  float h[P], a2[P], Bv[P], Cv[P];
-  load_f32_group<P>(st, h, state_vec != 0);
+  float a2[P];
 #pragma unroll
-  for (int j = 0; j < P; ++j) a2[j] = s_a2[cl * N + q * P + j];
-  const Tin* Bm = reinterpret_cast<const Tin*>(a.Bm) + bb * N + q * P;
-  const Tin* Cm = reinterpret_cast<const Tin*>(a.Cm) + bb * N + q * P;
+  for (int j = 0; j < P; ++j) a2[j] = a2_from_alog(a.A_log[cc * N + q * P + j]);
+  const float dtb = a.dt_bias ? a.dt_bias[cc] : 0.0f;
+  const float Dc = a.D ? a.D[cc] : 0.0f;
+  const bool gate = a.z != nullptr;
+  const Tin* U = reinterpret_cast<const Tin*>(a.u);
+  const Tin* DT = reinterpret_cast<const Tin*>(a.dt);
+  const Tin* Z = reinterpret_cast<const Tin*>(a.z);
+  const Tin* Bm = reinterpret_cast<const Tin*>(a.Bm);
+  const Tin* Cm = reinterpret_cast<const Tin*>(a.Cm);
+
+  // the state (the HBM traffic) of all kRows rows is requested first, in one
+  // round trip; B / C rows, shared by every channel of a batch row, are L1/L2
+  // hits and are loaded per row just before use
+  float h[kRows][P], uv[kRows], dtv[kRows], zv[kRows];
+  int64_t row[kRows], brow[kRows];
+  bool valid[kRows];
 #pragma unroll
-  for (int j = 0; j < P; ++j) {
-    Bv[j] = to_f32(Bm[j]);
-    Cv[j] = to_f32(Cm[j]);
+  for (int i = 0; i < kRows; ++i) {
+    const int64_t b = (bblk * bt + bl) * kRows + i;
+    valid[i] = cvalid && b < a.B;
+    // invalid lanes still join the butterfly (full-warp shuffles); they read row 0
+    brow[i] = valid[i] ? b : 0;
+    row[i] = brow[i] * Di + cc;
+    load_group<P>(a.state + row[i] * N + q * P, h[i], state_vec);
+    uv[i] = to_f32(U[row[i]]);
+    dtv[i] = to_f32(DT[row[i]]);
+    zv[i] = gate ? to_f32(Z[row[i]]) : 0.0f;
   }
-  const float uv = to_f32(reinterpret_cast<const Tin*>(a.u)[row]);
-  const float dtv = to_f32(reinterpret_cast<const Tin*>(a.dt)[row]);
-  const float dtb = a.dt_bias ? a.dt_bias[ccl] : 0.0f;
-  const float Dc = a.D ? a.D[ccl] : 0.0f;
-
-  const float delta = softplus_f(dtv + dtb);
-  const float du = delta * uv;
-  float part = ssm_token_group<P>(h, a2, delta, du, Bv, Cv);
 #pragma unroll
-  for (int s = 1; s < NG; s *= 2) part = part + __shfl_xor_sync(0xffffffffu, part, s);
-
-  if (valid) {
-    store_f32_group<P>(st, h, state_vec != 0);
-    if (q == 0) {
-      const bool gate = a.z != nullptr;
-      const float zv = gate ? to_f32(reinterpret_cast<const Tin*>(a.z)[row]) : 0.0f;
-      store_out(a.y, row, a.y_bf16, ssm_output(part, Dc, uv, gate, zv));
+  for (int i = 0; i < kRows; ++i) {
+    float Bv[P], Cv[P];
+    load_group<P>(Bm + brow[i] * N + q * P, Bv, bc_vec);
+    load_group<P>(Cm + brow[i] * N + q * P, Cv, bc_vec);
+    const float delta = softplus_f(dtv[i] + dtb);
+    const float du = delta * uv[i];
+    float part = ssm_token_group<P>(h[i], a2, delta, du, Bv, Cv);
+#pragma unroll
+    for (int s = 1; s < NG; s *= 2) part = part + __shfl_xor_sync(0xffffffffu, part, s);
+    if (valid[i]) {
+      store_group<P>(a.state + row[i] * N + q * P, h[i], state_vec);
+      if (q == 0) store_out(a.y, row[i], a.y_bf16, ssm_output(part, Dc, uv[i], gate, zv[i]));
     }
   }
 }
@@ -119,14 +135,20 @@ __global__ void __launch_bounds__(kThreads) ssm_step_kernel(SsmStepArgs a, int b
 template <int N, typename Tin>
 cudaError_t launch_n(const SsmStepArgs& a, cudaStream_t stream) {
   constexpr int NG = N / group_size(N);
+  // 128-thread CTAs (256 when a channel needs 8 lanes): ~5 resident per SM
   const int per_b = NG * kChannels;
-  const int bt = kThreads / per_b;
+  const int bt = per_b >= 128 ? 1 : 128 / per_b;
+  const int threads = per_b * bt;
   const int64_t n_cblk = (a.Di + kChannels - 1) / kChannels;
-  const int64_t n_bblk = (a.B + bt - 1) / bt;
+  const int64_t rows_per_cta = (int64_t)bt * kRows;
+  const int64_t n_bblk = (a.B + rows_per_cta - 1) / rows_per_cta;
   const int64_t blocks = n_cblk * n_bblk;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  const int es = sizeof(Tin);
   const int state_vec = (reinterpret_cast<uintptr_t>(a.state) & 15) == 0;
-  ssm_step_kernel<N, Tin><<<(unsigned)blocks, kThreads, 0, stream>>>(a, bt, n_cblk, state_vec);
+  const int bc_vec = ((reinterpret_cast<uintptr_t>(a.Bm) | reinterpret_cast<uintptr_t>(a.Cm)) & 15) == 0 &&
+                     (N * es) % 16 == 0;
+  ssm_step_kernel<N, Tin><<<(unsigned)blocks, threads, 0, stream>>>(a, bt, n_cblk, state_vec, bc_vec);
   return cudaGetLastError();
 }
 

@@ -67,12 +67,12 @@ def test_version_and_error_string(lib):
 def _scan(lib, **kw):
     a = dict(y=FAKE, ld_y=8, y_dtype=0, u=FAKE, ld_u=8, dt=FAKE, ld_dt=8, z=None, ld_z=0,
              Bm=FAKE, ld_B=16, Cm=FAKE, ld_C=16, in_dtype=0, A_log=FAKE, D=None, dt_bias=None,
-             s_in=None, s_out=None, B=1, T=4, Di=8, N=16, stream=None)
+             s_in=None, s_out=None, B=1, T=4, Di=8, N=16, ws=None, ws_bytes=0, stream=None)
     a.update(kw)
     return lib.mamba_selective_scan_prefill(
         a["y"], a["ld_y"], a["y_dtype"], a["u"], a["ld_u"], a["dt"], a["ld_dt"], a["z"], a["ld_z"],
         a["Bm"], a["ld_B"], a["Cm"], a["ld_C"], a["in_dtype"], a["A_log"], a["D"], a["dt_bias"],
-        a["s_in"], a["s_out"], a["B"], a["T"], a["Di"], a["N"], a["stream"])
+        a["s_in"], a["s_out"], a["B"], a["T"], a["Di"], a["N"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -90,6 +90,7 @@ def _scan(lib, **kw):
     (dict(ld_z=4, z=FAKE), m.MAMBA_ERR_INVALID_ARG),
     (dict(ld_B=15), m.MAMBA_ERR_INVALID_ARG),
     (dict(B=1 << 40, T=1 << 40), m.MAMBA_ERR_INVALID_ARG),
+    (dict(ws=FAKE, ws_bytes=-1), m.MAMBA_ERR_INVALID_ARG),
 ])
 def test_scan_rejects_bad_arguments_on_host(lib, kw, code):
     assert _scan(lib, **kw) == code
@@ -101,6 +102,13 @@ def test_zero_sized_calls_are_noops(lib):
     assert _scan(lib, Di=0) == m.MAMBA_OK
     assert m.mamba_last_error() == ""
     assert lib.mamba_conv1d_silu_prefill(None, 0, None, 0, 0, None, None, FAKE, None, 0, 5, 8, 4, None) == 0
+
+
+def test_workspace_query_rejects_bad_sizes(lib):
+    assert lib.mamba_selective_scan_workspace_bytes(1, 10, 8, 3) == m.MAMBA_ERR_UNSUPPORTED
+    assert lib.mamba_selective_scan_workspace_bytes(-1, 10, 8, 16) == m.MAMBA_ERR_INVALID_ARG
+    assert lib.mamba_selective_scan_workspace_bytes(0, 10, 8, 16) == 0
+    assert lib.mamba_selective_scan_workspace_bytes(2, 0, 8, 16) == 0
 
 
 @pytest.mark.parametrize("K,code", [(0, m.MAMBA_ERR_UNSUPPORTED), (9, m.MAMBA_ERR_UNSUPPORTED)])

@@ -146,7 +146,7 @@ def _scan_inputs(Bsz, T, Di, N, dtype, seed=SEED):
     return a, p
 
 
-def _run_scan(m, a, p, dtype, y_dtype, gate, state_in, strided, inplace=False):
+def _run_scan(m, a, p, dtype, y_dtype, gate, state_in, strided, inplace=False, workspace=None):
     Bsz, T, Di = a["u"].shape
     N = a["B"].shape[2]
     if strided:
@@ -166,7 +166,7 @@ def _run_scan(m, a, p, dtype, y_dtype, gate, state_in, strided, inplace=False):
     s_in = to_dev(state_in) if state_in is not None else None
     s_out = s_in if (inplace and s_in is not None) else torch.empty((Bsz, Di, N), device="cuda")
     m.mamba_selective_scan_prefill(y, u, dt, Bm, Cm, to_dev(p["A_log"]), to_dev(p["D"]),
-                                   to_dev(p["dt_bias"]), z, s_in, s_out)
+                                   to_dev(p["dt_bias"]), z, s_in, s_out, workspace=workspace)
     torch.cuda.synchronize()
     return to_host(y), to_host(s_out)
 
@@ -181,6 +181,43 @@ def test_scan_prefill_matches_oracle(cuda_lib, Bsz, T, Di, N, dtype, y_dtype, ga
                                                  p["dt_bias"], a["z"] if gate else None, s0)
     assert_within(y, y_ref, "y", bf16_out=y_dtype == "bf16")
     assert_within(s, s_ref, "state")
+
+
+SPLIT_CASES = [
+    # narrow shapes that the plan splits along T; checked on both routes
+    (1, 2048, 256, 16, "f32", "f32", True, True, False),
+    (1, 3001, 96, 16, "bf16", "f32", True, True, False),
+    (2, 999, 64, 64, "f32", "f32", True, True, False),
+    (1, 1500, 64, 1, "f32", "f32", False, True, False),
+    (1, 700, 160, 8, "bf16", "bf16", True, False, True),
+]
+
+
+@pytest.mark.parametrize("route", ["auto", "sequential"])
+@pytest.mark.parametrize("Bsz,T,Di,N,dtype,y_dtype,gate,state,strided", SPLIT_CASES)
+def test_scan_routes_match_oracle(cuda_lib, route, Bsz, T, Di, N, dtype, y_dtype, gate, state, strided):
+    m = cuda_lib
+    need = m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
+    assert need > 0, "expected a T-split plan for this narrow shape"
+    a, p = _scan_inputs(Bsz, T, Di, N, dtype)
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5) if state else None
+    ws = None if route == "auto" else False
+    y, s = _run_scan(m, a, p, dtype, y_dtype, gate, s0, strided, workspace=ws)
+    y_ref, s_ref = oracle.selective_scan_prefill(a["u"], a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                 p["dt_bias"], a["z"] if gate else None, s0)
+    assert_within(y, y_ref, "y", bf16_out=y_dtype == "bf16")
+    assert_within(s, s_ref, "state")
+
+
+def test_scan_workspace_too_small_falls_back_to_one_pass(cuda_lib):
+    m = cuda_lib
+    Bsz, T, Di, N = 1, 1024, 128, 16
+    a, p = _scan_inputs(Bsz, T, Di, N, "f32")
+    need = m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
+    small = torch.empty(need // 2, dtype=torch.uint8, device="cuda")
+    y1, s1 = _run_scan(m, a, p, "f32", "f32", True, None, False, workspace=small)
+    y2, s2 = _run_scan(m, a, p, "f32", "f32", True, None, False, workspace=False)
+    assert np.array_equal(y1, y2) and np.array_equal(s1, s2)
 
 
 @pytest.mark.parametrize("Bsz,T,Di", [(1, 2000, 128), (8, 64, 512)])
