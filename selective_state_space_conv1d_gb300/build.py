@@ -18,8 +18,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libmamba_ssm.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["api.cu", "conv1d.cu", "scan_prefill.cu", "ssm_step.cu"]
-HEADERS = [os.path.join(CSRC, h) for h in ("device_math.cuh", "launch.h")] + [
+SOURCES = ["api.cu", "conv1d.cu", "scan_prefill.cu", "scan_f32.cu", "scan_bf16.cu", "ssm_step.cu"]
+HEADERS = [os.path.join(CSRC, h) for h in ("device_math.cuh", "launch.h", "scan_kernel.cuh")] + [
     os.path.join(INCLUDE, "mamba_ssm.h")
 ]
 

@@ -1,0 +1,405 @@
+// scan_kernel.cuh - kernels of the selective-scan prefill (see scan_prefill.cu
+// for the design).  Included by the per-dtype instantiation units so that the
+// template set (d_state x gate x output dtype x mode) compiles in parallel.
+#pragma once
+
+#include <type_traits>
+
+#include "device_math.cuh"
+#include "launch.h"
+
+namespace mamba {
+namespace scan {
+namespace {  // internal linkage: each instantiation unit keeps its own copies
+
+constexpr int kStages = 3;
+constexpr int kLanes = 32;  // channels per CTA (one warp)
+constexpr int kTC = 16;     // rows per staged chunk
+constexpr int kLogTC = 4;
+
+template <typename Tin>
+struct Tile {
+  static constexpr int ES = sizeof(Tin);
+  static constexpr int GA = kLanes * ES / 16;  // 16-byte granules per activation row
+  static constexpr int LOG_GA = GA == 8 ? 3 : (GA == 4 ? 2 : (GA == 2 ? 1 : 0));
+};
+
+template <int N, typename Tin>
+struct Smem {
+  Tin act[kStages][3][kTC][kLanes];  // u, dt, z
+  Tin bc[kStages][2][kTC][N];        // B, C as staged (storage dtype)
+  // bf16 only: this chunk's B, C widened to f32
+  float bcf[sizeof(Tin) == 4 ? 1 : 2][sizeof(Tin) == 4 ? 1 : kTC][sizeof(Tin) == 4 ? 4 : N];
+};
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int Pending>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(Pending) : "memory");
+}
+
+template <int P>
+__device__ __forceinline__ void ld_f32(const float* p, float (&o)[P]) {
+  if constexpr (P % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < P; j += 4) {
+      const float4 v = *reinterpret_cast<const float4*>(p + j);
+      o[j] = v.x; o[j + 1] = v.y; o[j + 2] = v.z; o[j + 3] = v.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < P; ++j) o[j] = p[j];
+  }
+}
+
+// State-only token update (pass 1 of the T split).
+template <int P>
+__device__ __forceinline__ void ssm_state_group(float* h, const float* a2, float delta, float du,
+                                                const float* Bv) {
+  if constexpr (P == 1) {
+    h[0] = fmaf(ex2_approx(delta * a2[0]), h[0], du * Bv[0]);
+  } else {
+    const float2 d2 = make_float2(delta, delta);
+    const float2 u2 = make_float2(du, du);
+#pragma unroll
+    for (int j = 0; j < P; j += 2) {
+      const float2 arg = __fmul2_rn(d2, make_float2(a2[j], a2[j + 1]));
+      const float2 dA = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+      const float2 x = __fmul2_rn(u2, make_float2(Bv[j], Bv[j + 1]));
+      const float2 hn = __ffma2_rn(dA, make_float2(h[j], h[j + 1]), x);
+      h[j] = hn.x;
+      h[j + 1] = hn.y;
+    }
+  }
+}
+
+struct Work {
+  float* ws;           // T-split workspace (null for the sequential route)
+  int parts;           // P
+  int64_t part_len;    // rows per part (the last part may be shorter)
+  int64_t n_tiles;     // channel tiles per batch row
+  int64_t grid_parts;  // parts covered by this launch's grid
+};
+
+enum Mode { kSequential = 0, kPass1 = 1, kPass2 = 2 };
+
+// Workspace layout (f32, each slot B*Di*N): slot 0 = state snapshot; slot
+// 1 + 2j = total decay of part j; slot 2 + 2j = end state of part j from zero,
+// replaced by the fold with the carry-in of part j + 1.
+__device__ __forceinline__ int64_t carry_slot(int64_t part) { return part == 0 ? 0 : 2 * part; }
+
+// per-row scalars, computed one row pair ahead of the state update
+struct RowS {
+  float u, delta, du, g;
+};
+
+template <int N, typename Tin, int MODE, bool GATE, bool YBF16>
+__global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int act_vec, int bc_vec) {
+  using TL = Tile<Tin>;
+  using Tout = typename std::conditional<YBF16, __nv_bfloat16, float>::type;
+  constexpr int P = group_size(N);
+  constexpr int NG = N / P;
+  constexpr bool kBf16 = sizeof(Tin) == 2;
+  constexpr int NTENS = MODE == kPass1 ? 2 : (GATE ? 3 : 2);  // u, dt (, z)
+  constexpr int NBC = MODE == kPass1 ? 1 : 2;                 // B (, C)
+  __shared__ __align__(16) Smem<N, Tin> sm;
+
+  const int lane = threadIdx.x;
+  int64_t blk = blockIdx.x;
+  const int64_t part = blk % w.grid_parts;
+  blk /= w.grid_parts;
+  const int64_t tile = blk % w.n_tiles;
+  const int64_t b = blk / w.n_tiles;
+  const int64_t c0 = tile * kLanes;
+  const int64_t c = c0 + lane;
+  const int64_t Di = a.Di, T = a.T;
+  const bool active = c < Di;
+  const int64_t cc = active ? c : Di - 1;
+  const int64_t t_begin = part * w.part_len;
+  const int64_t t_end = min(T, t_begin + w.part_len);
+  const int64_t BDN = a.B * Di * N;
+  const int64_t srow = (b * Di + cc) * N;  // this lane's state row
+
+  float a2[N];
+#pragma unroll
+  for (int n = 0; n < N; ++n) a2[n] = a2_from_alog(a.A_log[cc * N + n]);
+  const float dtb = a.dt_bias ? a.dt_bias[cc] : 0.0f;
+  const float Dc = a.D ? a.D[cc] : 0.0f;
+
+  // ---- carry-in ----
+  float h[N];
+  if (MODE == kSequential) {
+    if (a.state_in) {
+      ld_f32<N>(a.state_in + srow, h);
+    } else {
+#pragma unroll
+      for (int n = 0; n < N; ++n) h[n] = 0.0f;
+    }
+  } else if (MODE == kPass1) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) h[n] = 0.0f;
+    if (part == 0 && active) {  // snapshot of the initial state for the fold / pass 2
+#pragma unroll
+      for (int n = 0; n < N; ++n) w.ws[srow + n] = a.state_in ? a.state_in[srow + n] : 0.0f;
+    }
+  } else {
+    ld_f32<N>(w.ws + BDN * carry_slot(part) + srow, h);
+  }
+
+  // ---- staging of chunk k (rows t_begin + k*kTC ..) into ring slot `stage` ----
+  auto act_src = [&](int tens) {
+    return reinterpret_cast<const Tin*>(tens == 0 ? a.u : (tens == 1 ? a.dt : a.z));
+  };
+  auto act_ld = [&](int tens) { return tens == 0 ? a.ld_u : (tens == 1 ? a.ld_dt : a.ld_z); };
+  auto issue = [&](int64_t k, int stage) {
+    const int64_t row0 = t_begin + k * kTC;
+    const int rows = (int)min((int64_t)kTC, t_end - row0);
+    const int64_t grow0 = b * T + row0;
+    if (act_vec) {
+      // granule i: tensor i / (kTC*GA), row (i / GA) % kTC, granule-in-row i % GA
+      constexpr int total = NTENS * kTC * TL::GA;
+#pragma unroll
+      for (int i = lane; i < total; i += kLanes) {
+        const int q = i & (TL::GA - 1);
+        const int r = (i >> TL::LOG_GA) & (kTC - 1);
+        const int tens = i >> (TL::LOG_GA + kLogTC);
+        const int64_t ch = c0 + q * (16 / TL::ES);
+        if (r < rows && ch < Di)
+          cp_async16(&sm.act[stage][tens][r][q * (16 / TL::ES)],
+                     act_src(tens) + (grow0 + r) * act_ld(tens) + ch);
+      }
+    } else {
+      for (int tens = 0; tens < NTENS; ++tens)
+        for (int r = 0; r < rows; ++r)
+          if (active) sm.act[stage][tens][r][lane] = act_src(tens)[(grow0 + r) * act_ld(tens) + c];
+    }
+    constexpr int GB = (N * TL::ES) / 16 > 0 ? (N * TL::ES) / 16 : 1;  // granules per B/C row
+    if (bc_vec && N * TL::ES >= 16) {
+      constexpr int total = NBC * kTC * GB;
+#pragma unroll
+      for (int i = lane; i < total; i += kLanes) {
+        const int q = i % GB;
+        const int r = (i / GB) % kTC;
+        const int tens = i / (GB * kTC);
+        const Tin* src = reinterpret_cast<const Tin*>(tens == 0 ? a.Bm : a.Cm);
+        const int64_t ld = tens == 0 ? a.ld_B : a.ld_C;
+        if (r < rows)
+          cp_async16(&sm.bc[stage][tens][r][q * (16 / TL::ES)], src + (grow0 + r) * ld + q * (16 / TL::ES));
+      }
+    } else {
+      for (int i = lane; i < NBC * kTC * N; i += kLanes) {
+        const int n = i % N;
+        const int r = (i / N) % kTC;
+        const int tens = i / (N * kTC);
+        const Tin* src = reinterpret_cast<const Tin*>(tens == 0 ? a.Bm : a.Cm);
+        const int64_t ld = tens == 0 ? a.ld_B : a.ld_C;
+        if (r < rows) sm.bc[stage][tens][r][n] = src[(grow0 + r) * ld + n];
+      }
+    }
+  };
+
+  const int64_t nrows = max((int64_t)0, t_end - t_begin);
+  const int64_t nchunks = (nrows + kTC - 1) / kTC;
+#pragma unroll 1
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (s < nchunks) issue(s, s);
+    cp_async_commit();
+  }
+
+  Tout* ybase = reinterpret_cast<Tout*>(a.y) + (b * T + t_begin) * a.ld_y + c;
+  float sdelta = 0.0f;  // pass 1: sum of delta over the part
+#pragma unroll 1
+  for (int64_t k = 0; k < nchunks; ++k) {
+    cp_async_wait<kStages - 2>();
+    __syncwarp();  // chunk k visible to every lane; every lane is done with chunk k-1
+    const int stage = (int)(k % kStages);
+    const int rows = (int)min((int64_t)kTC, nrows - k * kTC);
+    const float* sB;
+    const float* sC;
+    if constexpr (kBf16) {
+      // widen this chunk's B (and C) rows to f32 once, shared by all lanes
+#pragma unroll
+      for (int i = lane; i < NBC * kTC * N; i += kLanes) {
+        const int n = i % N;
+        const int r = (i / N) % kTC;
+        const int tens = i / (N * kTC);
+        sm.bcf[tens][r][n] = to_f32(sm.bc[stage][tens][r][n]);
+      }
+      __syncwarp();
+      sB = &sm.bcf[0][0][0];
+      sC = &sm.bcf[NBC - 1][0][0];
+    } else {
+      sB = reinterpret_cast<const float*>(&sm.bc[stage][0][0][0]);
+      sC = reinterpret_cast<const float*>(&sm.bc[stage][NBC - 1][0][0]);
+    }
+    if (k + kStages - 1 < nchunks) issue(k + kStages - 1, (int)((k + kStages - 1) % kStages));
+    cp_async_commit();
+
+    const Tin* su = &sm.act[stage][0][0][0];
+    const Tin* sdt = &sm.act[stage][1][0][0];
+    const Tin* sz = &sm.act[stage][GATE ? 2 : 0][0][0];
+    auto prep = [&](int r) {
+      RowS s;
+      s.u = to_f32(su[r * kLanes + lane]);
+      s.delta = softplus_f(to_f32(sdt[r * kLanes + lane]) + dtb);
+      s.du = s.delta * s.u;
+      s.g = (MODE != kPass1 && GATE) ? silu_f(to_f32(sz[r * kLanes + lane])) : 1.0f;
+      return s;
+    };
+    if (!active) continue;
+
+    if (MODE == kPass1) {
+      RowS cur = prep(0);
+#pragma unroll 1
+      for (int r = 0; r < rows; ++r) {
+        RowS nxt = cur;
+        if (r + 1 < rows) nxt = prep(r + 1);
+        sdelta += cur.delta;
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+          float Bv[P];
+          ld_f32<P>(sB + r * N + q * P, Bv);
+          ssm_state_group<P>(h + q * P, a2 + q * P, cur.delta, cur.du, Bv);
+        }
+        cur = nxt;
+      }
+    } else {
+      Tout* yp = ybase + k * kTC * a.ld_y;
+      auto row_out = [&](int r, const RowS& s) {
+        float part_[NG];
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+          float Bv[P], Cv[P];
+          ld_f32<P>(sB + r * N + q * P, Bv);
+          ld_f32<P>(sC + r * N + q * P, Cv);
+          part_[q] = ssm_token_group<P>(h + q * P, a2 + q * P, s.delta, s.du, Bv, Cv);
+        }
+        float y = fmaf(Dc, s.u, tree_sum<NG>(part_));
+        if (GATE) y *= s.g;
+        yp[r * a.ld_y] = from_f32<Tout>(y);
+      };
+      // the scalars of rows r+2, r+3 are computed while rows r, r+1 update the state
+      RowS c0s = prep(0);
+      RowS c1s = rows > 1 ? prep(1) : c0s;
+#pragma unroll 1
+      for (int r = 0; r < rows; r += 2) {
+        RowS n0 = c0s, n1 = c1s;
+        if (r + 2 < rows) n0 = prep(r + 2);
+        if (r + 3 < rows) n1 = prep(r + 3);
+        row_out(r, c0s);
+        if (r + 1 < rows) row_out(r + 1, c1s);
+        c0s = n0;
+        c1s = n1;
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  if (!active) return;
+  if (MODE == kPass1) {
+    float* Pj = w.ws + BDN * (1 + 2 * part) + srow;
+    float* Hj = w.ws + BDN * (2 + 2 * part) + srow;
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+      Pj[n] = ex2_approx(a2[n] * sdelta);
+      Hj[n] = h[n];
+    }
+  } else if (a.state_out && (MODE == kSequential || part == w.parts - 1)) {
+#pragma unroll
+    for (int n = 0; n < N; ++n) a.state_out[srow + n] = h[n];
+  }
+}
+
+// Chains the parts' aggregates: carry_{j+1} = decay_j * carry_j + end_j, with
+// carry_0 = the state snapshot; carry_{j+1} overwrites end_j.  One thread per
+// 4 consecutive floats of the [B][Di][N] state.
+__global__ void __launch_bounds__(128) scan_fold_kernel(float* ws, int64_t BDN, int parts) {
+  const int64_t i = (int64_t)blockIdx.x * 128 + threadIdx.x;
+  if (i * 4 >= BDN) return;
+  float4 acc = reinterpret_cast<const float4*>(ws)[i];
+  const int64_t q4 = BDN / 4;
+#pragma unroll 4
+  for (int j = 0; j < parts - 1; ++j) {
+    const float4 p = reinterpret_cast<const float4*>(ws)[q4 * (1 + 2 * j) + i];
+    float4* hp = reinterpret_cast<float4*>(ws) + q4 * (2 + 2 * j) + i;
+    const float4 e = *hp;
+    acc = make_float4(fmaf(p.x, acc.x, e.x), fmaf(p.y, acc.y, e.y), fmaf(p.z, acc.z, e.z),
+                      fmaf(p.w, acc.w, e.w));
+    *hp = acc;
+  }
+}
+// Same with one float per thread (B*Di*N not a multiple of 4).
+__global__ void __launch_bounds__(128) scan_fold1_kernel(float* ws, int64_t BDN, int parts) {
+  const int64_t i = (int64_t)blockIdx.x * 128 + threadIdx.x;
+  if (i >= BDN) return;
+  float acc = ws[i];
+#pragma unroll 4
+  for (int j = 0; j < parts - 1; ++j) {
+    acc = fmaf(ws[BDN * (1 + 2 * j) + i], acc, ws[BDN * (2 + 2 * j) + i]);
+    ws[BDN * (2 + 2 * j) + i] = acc;
+  }
+}
+
+template <int N, typename Tin, int MODE, bool GATE, bool YBF16>
+cudaError_t launch_mode(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
+  const int64_t blocks = w.n_tiles * a.B * w.grid_parts;
+  if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  scan_kernel<N, Tin, MODE, GATE, YBF16><<<(unsigned)blocks, kLanes, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
+  return cudaGetLastError();
+}
+
+template <int N, typename Tin, int MODE>
+cudaError_t launch_out(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t s) {
+  const bool gate = a.z != nullptr;
+  if (gate)
+    return a.y_bf16 ? launch_mode<N, Tin, MODE, true, true>(a, w, p, s)
+                    : launch_mode<N, Tin, MODE, true, false>(a, w, p, s);
+  return a.y_bf16 ? launch_mode<N, Tin, MODE, false, true>(a, w, p, s)
+                  : launch_mode<N, Tin, MODE, false, false>(a, w, p, s);
+}
+
+template <int N, typename Tin>
+cudaError_t launch_n(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream_t stream) {
+  Work w;
+  w.ws = ws;
+  w.parts = p.parts;
+  w.part_len = p.part_len;
+  w.n_tiles = (a.Di + kLanes - 1) / kLanes;
+  if (p.parts <= 1) {
+    w.grid_parts = 1;
+    return launch_out<N, Tin, kSequential>(a, w, p, stream);
+  }
+  w.grid_parts = p.parts - 1;
+  cudaError_t e = launch_mode<N, Tin, kPass1, false, false>(a, w, p, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t BDN = a.B * a.Di * N;
+  if (BDN % 4 == 0)
+    scan_fold_kernel<<<(unsigned)((BDN / 4 + 127) / 128), 128, 0, stream>>>(ws, BDN, p.parts);
+  else
+    scan_fold1_kernel<<<(unsigned)((BDN + 127) / 128), 128, 0, stream>>>(ws, BDN, p.parts);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  w.grid_parts = p.parts;
+  return launch_out<N, Tin, kPass2>(a, w, p, stream);
+}
+
+template <typename Tin>
+cudaError_t launch_dtype(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream_t s) {
+  switch (a.N) {
+    case 1: return launch_n<1, Tin>(a, p, ws, s);
+    case 2: return launch_n<2, Tin>(a, p, ws, s);
+    case 4: return launch_n<4, Tin>(a, p, ws, s);
+    case 8: return launch_n<8, Tin>(a, p, ws, s);
+    case 16: return launch_n<16, Tin>(a, p, ws, s);
+    case 32: return launch_n<32, Tin>(a, p, ws, s);
+    case 64: return launch_n<64, Tin>(a, p, ws, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+}  // namespace scan
+}  // namespace mamba

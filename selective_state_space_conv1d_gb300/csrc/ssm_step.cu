@@ -7,7 +7,7 @@
 //
 // Design (GB300): the step is pure streaming of the f32 state (read once,
 // written once: 2 * 4 * N bytes per (batch, channel)).  Each lane owns one
-// group of P = min(N, 8) consecutive states of one channel and moves them with
+// group of P = min(N, 16) consecutive states of one channel and moves them with
 // 16-byte loads / stores; the N/P lanes of a row are adjacent, so a warp
 // touches one contiguous span of the state.  A lane serves 4 batch rows of its
 // channel: A2 = -exp(A_log) log2(e) is computed once for them, and the loads of
@@ -38,14 +38,17 @@ __device__ __forceinline__ void load_group(const T* p, float (&o)[P], bool vec) 
       }
       return;
     }
-  } else if constexpr (sizeof(T) == 2 && P == 8) {
+  } else if constexpr (sizeof(T) == 2 && P % 8 == 0) {
     if (vec) {
-      const uint4 v = *reinterpret_cast<const uint4*>(p);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        o[2 * i] = __uint_as_float(w[i] << 16);
-        o[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+      for (int g = 0; g < P; g += 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p + g);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          o[g + 2 * i] = __uint_as_float(w[i] << 16);
+          o[g + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+        }
       }
       return;
     }
