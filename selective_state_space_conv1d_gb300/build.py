@@ -18,7 +18,9 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libmamba_ssm.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["api.cu", "conv1d.cu", "scan_prefill.cu", "scan_f32.cu", "scan_bf16.cu", "ssm_step.cu"]
+SOURCES = ["api.cu", "conv1d.cu", "scan_prefill.cu", "ssm_step.cu"]
+# scan_inst.cu is compiled once per (storage dtype, d_state): small parallel units
+SCAN_INST = [(bf16, n) for n in (1, 2, 4, 8, 16, 32, 64) for bf16 in (0, 1)]
 HEADERS = [os.path.join(CSRC, h) for h in ("device_math.cuh", "launch.h", "scan_kernel.cuh")] + [
     os.path.join(INCLUDE, "mamba_ssm.h")
 ]
@@ -41,7 +43,8 @@ def _stale() -> bool:
     if not os.path.exists(LIB_PATH):
         return True
     t = os.path.getmtime(LIB_PATH)
-    deps = [os.path.join(CSRC, s) for s in SOURCES] + HEADERS + [os.path.abspath(__file__)]
+    deps = ([os.path.join(CSRC, s) for s in SOURCES + ["scan_inst.cu"]] + HEADERS
+            + [os.path.abspath(__file__)])
     return any(os.path.getmtime(d) > t for d in deps)
 
 
@@ -53,18 +56,24 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     cc = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
 
-    def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+    def compile_one(job) -> str:
+        src, obj_name, defines = job
+        obj = os.path.join(BUILD_DIR, obj_name)
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra, *defines, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+            raise RuntimeError(f"nvcc failed on {src} {defines}:\n{r.stdout}\n{r.stderr}")
         if verbose or ptxas_info:
             print(r.stdout + r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
+    jobs = [(f"scan_inst.cu", f"scan_{'bf16' if b else 'f32'}_{n}.o", [f"-DSCAN_BF16={b}", f"-DSCAN_N={n}"])
+            for b, n in SCAN_INST]
+    jobs.sort(key=lambda j: -int(j[2][1].split("=")[1]))  # largest d_state first
+    jobs += [(src, os.path.splitext(src)[0] + ".o", []) for src in SOURCES]
+    workers = max(1, min(len(jobs), os.cpu_count() or 4))
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        objs = list(ex.map(compile_one, jobs))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -1,6 +1,6 @@
 // scan_kernel.cuh - kernels of the selective-scan prefill (see scan_prefill.cu
-// for the design).  Included by the per-dtype instantiation units so that the
-// template set (d_state x gate x output dtype x mode) compiles in parallel.
+// for the design).  Included by scan_inst.cu, which the build compiles once per
+// (storage dtype, d_state) so that the template set compiles in parallel.
 #pragma once
 
 #include <type_traits>
@@ -97,15 +97,17 @@ struct RowS {
   float u, delta, du, g;
 };
 
-template <int N, typename Tin, int MODE, bool GATE, bool YBF16>
+template <int N, typename Tin, int MODE, bool GATE>
 __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int act_vec, int bc_vec) {
   using TL = Tile<Tin>;
-  using Tout = typename std::conditional<YBF16, __nv_bfloat16, float>::type;
   constexpr int P = group_size(N);
   constexpr int NG = N / P;
   constexpr bool kBf16 = sizeof(Tin) == 2;
   constexpr int NTENS = MODE == kPass1 ? 2 : (GATE ? 3 : 2);  // u, dt (, z)
   constexpr int NBC = MODE == kPass1 ? 1 : 2;                 // B (, C)
+  // rows unrolled together in a full chunk: all 16 for small states; large
+  // states carry enough independent work per row with 4
+  constexpr int kU = N <= 16 ? kTC : 4;
   __shared__ __align__(16) Smem<N, Tin> sm;
 
   const int lane = threadIdx.x;
@@ -210,7 +212,7 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
     cp_async_commit();
   }
 
-  Tout* ybase = reinterpret_cast<Tout*>(a.y) + (b * T + t_begin) * a.ld_y + c;
+  const int64_t yoff = (b * T + t_begin) * a.ld_y + c;  // this lane's first y element
   float sdelta = 0.0f;  // pass 1: sum of delta over the part
 #pragma unroll 1
   for (int64_t k = 0; k < nchunks; ++k) {
@@ -253,47 +255,57 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
     if (!active) continue;
 
     if (MODE == kPass1) {
-      RowS cur = prep(0);
-#pragma unroll 1
-      for (int r = 0; r < rows; ++r) {
-        RowS nxt = cur;
-        if (r + 1 < rows) nxt = prep(r + 1);
-        sdelta += cur.delta;
+      auto row_state = [&](int r, const RowS& rs) {
+        sdelta += rs.delta;
 #pragma unroll
         for (int q = 0; q < NG; ++q) {
           float Bv[P];
           ld_f32<P>(sB + r * N + q * P, Bv);
-          ssm_state_group<P>(h + q * P, a2 + q * P, cur.delta, cur.du, Bv);
+          ssm_state_group<P>(h + q * P, a2 + q * P, rs.delta, rs.du, Bv);
         }
-        cur = nxt;
+      };
+      if (rows == kTC) {
+        // full chunk: unrolled by kU rows, every row's scalars first, so the
+        // only serial chain left is the state update
+#pragma unroll 1
+        for (int r0 = 0; r0 < kTC; r0 += kU) {
+          RowS rs[kU];
+#pragma unroll
+          for (int r = 0; r < kU; ++r) rs[r] = prep(r0 + r);
+#pragma unroll
+          for (int r = 0; r < kU; ++r) row_state(r0 + r, rs[r]);
+        }
+      } else {
+#pragma unroll 1
+        for (int r = 0; r < rows; ++r) row_state(r, prep(r));
       }
     } else {
-      Tout* yp = ybase + k * kTC * a.ld_y;
-      auto row_out = [&](int r, const RowS& s) {
+      const int64_t yk = yoff + k * kTC * a.ld_y;
+      auto row_out = [&](int r, const RowS& rs) {
         float part_[NG];
 #pragma unroll
         for (int q = 0; q < NG; ++q) {
           float Bv[P], Cv[P];
           ld_f32<P>(sB + r * N + q * P, Bv);
           ld_f32<P>(sC + r * N + q * P, Cv);
-          part_[q] = ssm_token_group<P>(h + q * P, a2 + q * P, s.delta, s.du, Bv, Cv);
+          part_[q] = ssm_token_group<P>(h + q * P, a2 + q * P, rs.delta, rs.du, Bv, Cv);
         }
-        float y = fmaf(Dc, s.u, tree_sum<NG>(part_));
-        if (GATE) y *= s.g;
-        yp[r * a.ld_y] = from_f32<Tout>(y);
+        float y = fmaf(Dc, rs.u, tree_sum<NG>(part_));
+        if (GATE) y *= rs.g;
+        store_out(a.y, yk + r * a.ld_y, a.y_bf16, y);
       };
-      // the scalars of rows r+2, r+3 are computed while rows r, r+1 update the state
-      RowS c0s = prep(0);
-      RowS c1s = rows > 1 ? prep(1) : c0s;
+      if (rows == kTC) {
 #pragma unroll 1
-      for (int r = 0; r < rows; r += 2) {
-        RowS n0 = c0s, n1 = c1s;
-        if (r + 2 < rows) n0 = prep(r + 2);
-        if (r + 3 < rows) n1 = prep(r + 3);
-        row_out(r, c0s);
-        if (r + 1 < rows) row_out(r + 1, c1s);
-        c0s = n0;
-        c1s = n1;
+        for (int r0 = 0; r0 < kTC; r0 += kU) {
+          RowS rs[kU];
+#pragma unroll
+          for (int r = 0; r < kU; ++r) rs[r] = prep(r0 + r);
+#pragma unroll
+          for (int r = 0; r < kU; ++r) row_out(r0 + r, rs[r]);
+        }
+      } else {
+#pragma unroll 1
+        for (int r = 0; r < rows; ++r) row_out(r, prep(r));
       }
     }
   }
@@ -316,20 +328,32 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
 
 // Chains the parts' aggregates: carry_{j+1} = decay_j * carry_j + end_j, with
 // carry_0 = the state snapshot; carry_{j+1} overwrites end_j.  One thread per
-// 4 consecutive floats of the [B][Di][N] state.
+// 4 consecutive floats of the [B][Di][N] state; the loads of 4 parts are in
+// flight together.
 __global__ void __launch_bounds__(128) scan_fold_kernel(float* ws, int64_t BDN, int parts) {
   const int64_t i = (int64_t)blockIdx.x * 128 + threadIdx.x;
   if (i * 4 >= BDN) return;
-  float4 acc = reinterpret_cast<const float4*>(ws)[i];
   const int64_t q4 = BDN / 4;
-#pragma unroll 4
-  for (int j = 0; j < parts - 1; ++j) {
-    const float4 p = reinterpret_cast<const float4*>(ws)[q4 * (1 + 2 * j) + i];
-    float4* hp = reinterpret_cast<float4*>(ws) + q4 * (2 + 2 * j) + i;
-    const float4 e = *hp;
-    acc = make_float4(fmaf(p.x, acc.x, e.x), fmaf(p.y, acc.y, e.y), fmaf(p.z, acc.z, e.z),
-                      fmaf(p.w, acc.w, e.w));
-    *hp = acc;
+  float4* w4 = reinterpret_cast<float4*>(ws);
+  float4 acc = w4[i];
+  constexpr int kU = 4;  // parts whose loads are issued before any store
+  for (int j0 = 0; j0 < parts - 1; j0 += kU) {
+    float4 p[kU], e[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (j0 + u < parts - 1) {
+        p[u] = w4[q4 * (1 + 2 * (j0 + u)) + i];
+        e[u] = w4[q4 * (2 + 2 * (j0 + u)) + i];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (j0 + u < parts - 1) {
+        acc = make_float4(fmaf(p[u].x, acc.x, e[u].x), fmaf(p[u].y, acc.y, e[u].y),
+                          fmaf(p[u].z, acc.z, e[u].z), fmaf(p[u].w, acc.w, e[u].w));
+        w4[q4 * (2 + 2 * (j0 + u)) + i] = acc;
+      }
+    }
   }
 }
 // Same with one float per thread (B*Di*N not a multiple of 4).
@@ -344,22 +368,18 @@ __global__ void __launch_bounds__(128) scan_fold1_kernel(float* ws, int64_t BDN,
   }
 }
 
-template <int N, typename Tin, int MODE, bool GATE, bool YBF16>
+template <int N, typename Tin, int MODE, bool GATE>
 cudaError_t launch_mode(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
   const int64_t blocks = w.n_tiles * a.B * w.grid_parts;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  scan_kernel<N, Tin, MODE, GATE, YBF16><<<(unsigned)blocks, kLanes, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
+  scan_kernel<N, Tin, MODE, GATE><<<(unsigned)blocks, kLanes, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
   return cudaGetLastError();
 }
 
 template <int N, typename Tin, int MODE>
 cudaError_t launch_out(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t s) {
-  const bool gate = a.z != nullptr;
-  if (gate)
-    return a.y_bf16 ? launch_mode<N, Tin, MODE, true, true>(a, w, p, s)
-                    : launch_mode<N, Tin, MODE, true, false>(a, w, p, s);
-  return a.y_bf16 ? launch_mode<N, Tin, MODE, false, true>(a, w, p, s)
-                  : launch_mode<N, Tin, MODE, false, false>(a, w, p, s);
+  return a.z != nullptr ? launch_mode<N, Tin, MODE, true>(a, w, p, s)
+                        : launch_mode<N, Tin, MODE, false>(a, w, p, s);
 }
 
 template <int N, typename Tin>
@@ -374,7 +394,7 @@ cudaError_t launch_n(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream
     return launch_out<N, Tin, kSequential>(a, w, p, stream);
   }
   w.grid_parts = p.parts - 1;
-  cudaError_t e = launch_mode<N, Tin, kPass1, false, false>(a, w, p, stream);
+  cudaError_t e = launch_mode<N, Tin, kPass1, false>(a, w, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t BDN = a.B * a.Di * N;
   if (BDN % 4 == 0)
@@ -384,20 +404,6 @@ cudaError_t launch_n(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   w.grid_parts = p.parts;
   return launch_out<N, Tin, kPass2>(a, w, p, stream);
-}
-
-template <typename Tin>
-cudaError_t launch_dtype(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream_t s) {
-  switch (a.N) {
-    case 1: return launch_n<1, Tin>(a, p, ws, s);
-    case 2: return launch_n<2, Tin>(a, p, ws, s);
-    case 4: return launch_n<4, Tin>(a, p, ws, s);
-    case 8: return launch_n<8, Tin>(a, p, ws, s);
-    case 16: return launch_n<16, Tin>(a, p, ws, s);
-    case 32: return launch_n<32, Tin>(a, p, ws, s);
-    case 64: return launch_n<64, Tin>(a, p, ws, s);
-  }
-  return cudaErrorInvalidValue;
 }
 
 }  // namespace

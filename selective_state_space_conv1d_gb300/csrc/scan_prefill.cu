@@ -32,14 +32,24 @@
 //    and writes y; the last part writes state_out.  A small fold kernel
 //    between them chains the aggregates into each part's carry-in.  Cost: the
 //    state-only rescan of P-1 parts; no cross-CTA waiting.
-//  * The kernels live in scan_kernel.cuh, instantiated per storage dtype in
-//    scan_f32.cu / scan_bf16.cu; this file holds the route planner.
+//  * The kernels live in scan_kernel.cuh, instantiated per (storage dtype,
+//    d_state) from scan_inst.cu; this file holds the route planner.
 #include "launch.h"
 
 namespace mamba {
 
-cudaError_t launch_scan_f32(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream_t s);
-cudaError_t launch_scan_bf16(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream_t s);
+// one per (storage dtype, d_state), compiled from scan_inst.cu
+#define SCAN_DECL(n)                                                                          \
+  cudaError_t launch_scan_f32_##n(const ScanArgs&, const ScanPlan&, float*, cudaStream_t);  \
+  cudaError_t launch_scan_bf16_##n(const ScanArgs&, const ScanPlan&, float*, cudaStream_t);
+SCAN_DECL(1)
+SCAN_DECL(2)
+SCAN_DECL(4)
+SCAN_DECL(8)
+SCAN_DECL(16)
+SCAN_DECL(32)
+SCAN_DECL(64)
+#undef SCAN_DECL
 
 namespace {
 inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
@@ -94,7 +104,20 @@ ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t w
 cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& p, float* ws,
                                           const DeviceInfo& dev, cudaStream_t stream) {
   (void)dev;
-  return a.in_bf16 ? launch_scan_bf16(a, p, ws, stream) : launch_scan_f32(a, p, ws, stream);
+#define SCAN_CASE(n) \
+  case n:            \
+    return a.in_bf16 ? launch_scan_bf16_##n(a, p, ws, stream) : launch_scan_f32_##n(a, p, ws, stream);
+  switch (a.N) {
+    SCAN_CASE(1)
+    SCAN_CASE(2)
+    SCAN_CASE(4)
+    SCAN_CASE(8)
+    SCAN_CASE(16)
+    SCAN_CASE(32)
+    SCAN_CASE(64)
+  }
+#undef SCAN_CASE
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace mamba
