@@ -317,7 +317,7 @@ int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, i
   int rc = current_device(&dev);
   if (rc) return rc;
   ok();
-  return mamba::scan_workspace_bytes(B, Di, N, mamba::scan_parts(B, T, Di, dev));
+  return mamba::scan_workspace_bytes(B, Di, N, mamba::scan_parts(B, T, Di, N, dev));
 }
 
 int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const void* dt, const void* z,

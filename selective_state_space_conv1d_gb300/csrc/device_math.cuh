@@ -114,10 +114,10 @@ __device__ __forceinline__ float ssm_token_group(float* h, const float* a2, floa
   }
 }
 
-// States are handled in groups of group_size(N) = min(N, 16); the groups'
-// partials are summed by a pairwise tree (level s adds partial i and i + s),
-// which is the order an xor-shuffle butterfly over the groups produces.
-__host__ __device__ constexpr int group_size(int N) { return N < 16 ? N : 16; }
+// States are handled in groups of group_size(N) = min(N, 8), one group per
+// lane; the groups' partials are summed by a pairwise tree (level s adds
+// partial i and i + s), which is the order an xor-shuffle butterfly produces.
+__host__ __device__ constexpr int group_size(int N) { return N < 8 ? N : 8; }
 
 template <int NG>
 __device__ __forceinline__ float tree_sum(float (&part)[NG]) {

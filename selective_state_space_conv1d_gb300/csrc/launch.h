@@ -78,7 +78,7 @@ struct ScanPlan {
   int bc_vec;   // B/C staged with 16-byte copies
   int64_t workspace_bytes;
 };
-int scan_parts(int64_t B, int64_t T, int64_t Di, const DeviceInfo& dev);
+int scan_parts(int64_t B, int64_t T, int64_t Di, int64_t N, const DeviceInfo& dev);
 int64_t scan_workspace_bytes(int64_t B, int64_t Di, int64_t N, int parts);
 ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t workspace_bytes);
 cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& plan, float* ws,

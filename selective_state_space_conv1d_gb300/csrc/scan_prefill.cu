@@ -10,17 +10,21 @@
 // here the route is picked from the shape (batch x channels vs SM count).
 //
 // Design (GB300):
-//  * One warp per CTA; lane = channel, 32 consecutive channels of one batch
-//    row, so every global access of u, dt, z and y is a coalesced row segment
-//    and B_t / C_t (shared by all channels) are shared-memory broadcasts.  All
-//    synchronisation is __syncwarp; 1-warp CTAs also give fine-grained load
-//    balance over the 152 SMs.
+//  * One warp per CTA covering consecutive channels of one batch row; each
+//    lane holds 8 states (N/8 lanes per channel: 16 channels per CTA at
+//    d_state 16), so every global access of u, dt, z and y is a coalesced row
+//    segment and B_t / C_t (shared by all channels) are shared-memory
+//    broadcasts.  All synchronisation is __syncwarp; small one-warp CTAs give
+//    many resident warps and fine-grained load balance over the 152 SMs.
 //  * u, dt, z, B, C stream in chunks of TC rows through a 3-deep cp.async ring
 //    (16-byte copies, L2-only): HBM sees one read of every input and one write
 //    of y.  bf16 B/C rows are widened to f32 once per chunk in shared memory.
-//  * A lane keeps all N states of its channel in registers (f32) and walks the
-//    rows sequentially.  The per-row scalars (softplus, SiLU(z)) are computed
-//    one row pair ahead, so only the state FMAs form a serial chain.  The state math is packed f32x2 plus
+//  * A lane keeps its 8 states in registers (f32) and walks the rows
+//    sequentially.  The per-row scalars (softplus, SiLU(z)) are split over the
+//    lanes of a channel by row (lane j of a channel evaluates row r0 + j of each
+//    group of N/8 rows and shuffles delta to the others), the partial C . h
+//    are summed by an xor butterfly, and full 16-row chunks are unrolled so the
+//    only serial chain is the state FMA.  The state math is packed f32x2 plus
 //    one MUFU ex2 per state and token; no tensor cores (no contraction).
 //  * Route "sequential" (wide shapes: enough batch x channel rows to fill the
 //    GPU): one launch, each CTA scans all T for its channels.
@@ -52,8 +56,9 @@ SCAN_DECL(64)
 #undef SCAN_DECL
 
 namespace {
-inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
-constexpr int kLanes = 32;
+inline bool aligned(const void* p, int n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+// channels per one-warp CTA: 8 states per lane, N/8 lanes per channel
+inline int64_t channels_per_cta(int64_t N) { return N <= 8 ? 32 : 32 / (N / 8); }
 }  // namespace
 
 int64_t scan_workspace_bytes(int64_t B, int64_t Di, int64_t N, int parts) {
@@ -61,13 +66,14 @@ int64_t scan_workspace_bytes(int64_t B, int64_t Di, int64_t N, int parts) {
   return (int64_t)(1 + 2 * (parts - 1)) * B * Di * N * (int64_t)sizeof(float);
 }
 
-int scan_parts(int64_t B, int64_t T, int64_t Di, const DeviceInfo& dev) {
+int scan_parts(int64_t B, int64_t T, int64_t Di, int64_t N, const DeviceInfo& dev) {
   // Number of T parts P.  With w = ceil(tiles * P / SMs) one-warp CTAs per SM,
   // an SM needs about kWarpsSat warps to keep its pipes busy, and every part but
   // the last is scanned twice (the state-only pass costs ~3/4 of the full one),
   // so the time is ~ ceil(T / P) * (1 + 0.75 (P-1)/P) * max(w, kWarpsSat).
   constexpr double kWarpsSat = 8.0;
-  const int64_t tiles = B * ((Di + kLanes - 1) / kLanes);
+  const int64_t ct = channels_per_cta(N);
+  const int64_t tiles = B * ((Di + ct - 1) / ct);
   double best = 0.0;
   int best_p = 1;
   for (int P = 1; P <= 64; ++P) {
@@ -86,12 +92,14 @@ int scan_parts(int64_t B, int64_t T, int64_t Di, const DeviceInfo& dev) {
 ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t workspace_bytes) {
   ScanPlan p;
   const int es = a.in_bf16 ? 2 : 4;
-  const int vw = 16 / es;
-  p.act_vec = al16(a.u) && al16(a.dt) && (!a.z || al16(a.z)) && (a.ld_u * es) % 16 == 0 &&
-              (a.ld_dt * es) % 16 == 0 && (!a.z || (a.ld_z * es) % 16 == 0) && a.Di % vw == 0;
-  p.bc_vec = al16(a.Bm) && al16(a.Cm) && (a.ld_B * es) % 16 == 0 && (a.ld_C * es) % 16 == 0 &&
-             (a.N * es) % 16 == 0;
-  p.parts = scan_parts(a.B, a.T, a.Di, dev);
+  // activation tiles move in granules of min(16, channels_per_cta * es) bytes
+  const int64_t rowb = channels_per_cta(a.N) * es;
+  const int g = (int)(rowb < 16 ? rowb : 16);
+  p.act_vec = aligned(a.u, g) && aligned(a.dt, g) && (!a.z || aligned(a.z, g)) && (a.ld_u * es) % g == 0 &&
+              (a.ld_dt * es) % g == 0 && (!a.z || (a.ld_z * es) % g == 0) && a.Di % (g / es) == 0;
+  p.bc_vec = aligned(a.Bm, 16) && aligned(a.Cm, 16) && (a.ld_B * es) % 16 == 0 &&
+             (a.ld_C * es) % 16 == 0 && (a.N * es) % 16 == 0;
+  p.parts = scan_parts(a.B, a.T, a.Di, a.N, dev);
   p.workspace_bytes = scan_workspace_bytes(a.B, a.Di, a.N, p.parts);
   if (p.workspace_bytes > workspace_bytes) {  // not enough workspace: one sequential pass
     p.parts = 1;
