@@ -13,38 +13,28 @@ namespace scan {
 namespace {  // internal linkage: each instantiation unit keeps its own copies
 
 constexpr int kStages = 3;
-constexpr int kTC = 16;  // rows per staged chunk
+constexpr int kLanes = 32;  // channels per CTA (one warp)
+constexpr int kTC = 16;     // rows per staged chunk
 constexpr int kLogTC = 4;
 
-// Lane layout: a warp (= CTA) covers CT channels of one batch row with LPC
-// lanes per channel, each lane holding P = min(N, 8) consecutive states.
-template <int N, typename Tin>
-struct Geo {
-  static constexpr int P = group_size(N);
-  static constexpr int LPC = N / P;                   // lanes per channel: 1, 2, 4, 8
-  static constexpr int CT = 32 / LPC;                 // channels per CTA
+template <typename Tin>
+struct Tile {
   static constexpr int ES = sizeof(Tin);
-  static constexpr int ROWB = CT * ES;                // bytes of one activation tile row
-  static constexpr int G = ROWB < 16 ? ROWB : 16;     // cp.async granule (4, 8 or 16 bytes)
-  static constexpr int GA = ROWB / G;                 // granules per activation row
+  static constexpr int GA = kLanes * ES / 16;  // 16-byte granules per activation row
   static constexpr int LOG_GA = GA == 8 ? 3 : (GA == 4 ? 2 : (GA == 2 ? 1 : 0));
 };
 
 template <int N, typename Tin>
 struct Smem {
-  Tin act[kStages][3][kTC][Geo<N, Tin>::CT];  // u, dt, z
-  Tin bc[kStages][2][kTC][N];                 // B, C as staged (storage dtype)
+  Tin act[kStages][3][kTC][kLanes];  // u, dt, z
+  Tin bc[kStages][2][kTC][N];        // B, C as staged (storage dtype)
   // bf16 only: this chunk's B, C widened to f32
   float bcf[sizeof(Tin) == 4 ? 1 : 2][sizeof(Tin) == 4 ? 1 : kTC][sizeof(Tin) == 4 ? 4 : N];
 };
 
-template <int G>
-__device__ __forceinline__ void cp_async(void* smem_dst, const void* gmem_src) {
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-  if constexpr (G == 16)
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem_src) : "memory");
-  else
-    asm volatile("cp.async.ca.shared.global [%0], [%1], %2;\n" ::"r"(s), "l"(gmem_src), "n"(G) : "memory");
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem_src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 template <int Pending>
@@ -63,17 +53,6 @@ __device__ __forceinline__ void ld_f32(const float* p, float (&o)[P]) {
   } else {
 #pragma unroll
     for (int j = 0; j < P; ++j) o[j] = p[j];
-  }
-}
-template <int P>
-__device__ __forceinline__ void st_f32(float* p, const float (&o)[P]) {
-  if constexpr (P % 4 == 0) {
-#pragma unroll
-    for (int j = 0; j < P; j += 4)
-      *reinterpret_cast<float4*>(p + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-  } else {
-#pragma unroll
-    for (int j = 0; j < P; ++j) p[j] = o[j];
   }
 }
 
@@ -113,64 +92,64 @@ enum Mode { kSequential = 0, kPass1 = 1, kPass2 = 2 };
 // replaced by the fold with the carry-in of part j + 1.
 __device__ __forceinline__ int64_t carry_slot(int64_t part) { return part == 0 ? 0 : 2 * part; }
 
+// per-row scalars, computed one row pair ahead of the state update
+struct RowS {
+  float u, delta, du, g;
+};
+
 template <int N, typename Tin, int MODE, bool GATE>
-__global__ void __launch_bounds__(32) scan_kernel(ScanArgs a, Work w, int act_vec, int bc_vec) {
-  using GE = Geo<N, Tin>;
-  constexpr int P = GE::P, LPC = GE::LPC, CT = GE::CT;
+__global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int act_vec, int bc_vec) {
+  using TL = Tile<Tin>;
+  constexpr int P = group_size(N);
+  constexpr int NG = N / P;
   constexpr bool kBf16 = sizeof(Tin) == 2;
   constexpr int NTENS = MODE == kPass1 ? 2 : (GATE ? 3 : 2);  // u, dt (, z)
   constexpr int NBC = MODE == kPass1 ? 1 : 2;                 // B (, C)
+  // rows unrolled together in a full chunk: all 16 for small states; large
+  // states carry enough independent work per row with 4
+  constexpr int kU = N <= 16 ? kTC : 4;
   __shared__ __align__(16) Smem<N, Tin> sm;
 
   const int lane = threadIdx.x;
-  const int q = lane % LPC;    // state group of this lane
-  const int cl = lane / LPC;   // channel within the tile
-  const int lbase = lane - q;  // first lane of this channel
   int64_t blk = blockIdx.x;
   const int64_t part = blk % w.grid_parts;
   blk /= w.grid_parts;
   const int64_t tile = blk % w.n_tiles;
   const int64_t b = blk / w.n_tiles;
-  const int64_t c0 = tile * CT;
-  const int64_t c = c0 + cl;
+  const int64_t c0 = tile * kLanes;
+  const int64_t c = c0 + lane;
   const int64_t Di = a.Di, T = a.T;
   const bool active = c < Di;
   const int64_t cc = active ? c : Di - 1;
   const int64_t t_begin = part * w.part_len;
   const int64_t t_end = min(T, t_begin + w.part_len);
   const int64_t BDN = a.B * Di * N;
-  const int64_t srow = (b * Di + cc) * N + q * P;  // this lane's slice of the state
+  const int64_t srow = (b * Di + cc) * N;  // this lane's state row
 
-  float a2[P];
+  float a2[N];
 #pragma unroll
-  for (int n = 0; n < P; ++n) a2[n] = a2_from_alog(a.A_log[cc * N + q * P + n]);
+  for (int n = 0; n < N; ++n) a2[n] = a2_from_alog(a.A_log[cc * N + n]);
   const float dtb = a.dt_bias ? a.dt_bias[cc] : 0.0f;
   const float Dc = a.D ? a.D[cc] : 0.0f;
 
   // ---- carry-in ----
-  float h[P];
+  float h[N];
   if (MODE == kSequential) {
     if (a.state_in) {
-      ld_f32<P>(a.state_in + srow, h);
+      ld_f32<N>(a.state_in + srow, h);
     } else {
 #pragma unroll
-      for (int n = 0; n < P; ++n) h[n] = 0.0f;
+      for (int n = 0; n < N; ++n) h[n] = 0.0f;
     }
   } else if (MODE == kPass1) {
 #pragma unroll
-    for (int n = 0; n < P; ++n) h[n] = 0.0f;
+    for (int n = 0; n < N; ++n) h[n] = 0.0f;
     if (part == 0 && active) {  // snapshot of the initial state for the fold / pass 2
-      float s0[P];
-      if (a.state_in) {
-        ld_f32<P>(a.state_in + srow, s0);
-      } else {
 #pragma unroll
-        for (int n = 0; n < P; ++n) s0[n] = 0.0f;
-      }
-      st_f32<P>(w.ws + srow, s0);
+      for (int n = 0; n < N; ++n) w.ws[srow + n] = a.state_in ? a.state_in[srow + n] : 0.0f;
     }
   } else {
-    ld_f32<P>(w.ws + BDN * carry_slot(part) + srow, h);
+    ld_f32<N>(w.ws + BDN * carry_slot(part) + srow, h);
   }
 
   // ---- staging of chunk k (rows t_begin + k*kTC ..) into ring slot `stage` ----
@@ -184,39 +163,37 @@ __global__ void __launch_bounds__(32) scan_kernel(ScanArgs a, Work w, int act_ve
     const int64_t grow0 = b * T + row0;
     if (act_vec) {
       // granule i: tensor i / (kTC*GA), row (i / GA) % kTC, granule-in-row i % GA
-      constexpr int total = NTENS * kTC * GE::GA;
-      constexpr int EPG = GE::G / GE::ES;  // elements per granule
+      constexpr int total = NTENS * kTC * TL::GA;
 #pragma unroll
-      for (int i = lane; i < total; i += 32) {
-        const int g = i & (GE::GA - 1);
-        const int r = (i >> GE::LOG_GA) & (kTC - 1);
-        const int tens = i >> (GE::LOG_GA + kLogTC);
-        const int64_t ch = c0 + g * EPG;
+      for (int i = lane; i < total; i += kLanes) {
+        const int q = i & (TL::GA - 1);
+        const int r = (i >> TL::LOG_GA) & (kTC - 1);
+        const int tens = i >> (TL::LOG_GA + kLogTC);
+        const int64_t ch = c0 + q * (16 / TL::ES);
         if (r < rows && ch < Di)
-          cp_async<GE::G>(&sm.act[stage][tens][r][g * EPG], act_src(tens) + (grow0 + r) * act_ld(tens) + ch);
+          cp_async16(&sm.act[stage][tens][r][q * (16 / TL::ES)],
+                     act_src(tens) + (grow0 + r) * act_ld(tens) + ch);
       }
     } else {
-      for (int i = lane; i < NTENS * kTC * CT; i += 32) {
-        const int e = i % CT;
-        const int r = (i / CT) % kTC;
-        const int tens = i / (CT * kTC);
-        if (r < rows && c0 + e < Di) sm.act[stage][tens][r][e] = act_src(tens)[(grow0 + r) * act_ld(tens) + c0 + e];
-      }
+      for (int tens = 0; tens < NTENS; ++tens)
+        for (int r = 0; r < rows; ++r)
+          if (active) sm.act[stage][tens][r][lane] = act_src(tens)[(grow0 + r) * act_ld(tens) + c];
     }
-    constexpr int GB = (N * GE::ES) / 16 > 0 ? (N * GE::ES) / 16 : 1;  // granules per B/C row
-    if (bc_vec && N * GE::ES >= 16) {
+    constexpr int GB = (N * TL::ES) / 16 > 0 ? (N * TL::ES) / 16 : 1;  // granules per B/C row
+    if (bc_vec && N * TL::ES >= 16) {
       constexpr int total = NBC * kTC * GB;
 #pragma unroll
-      for (int i = lane; i < total; i += 32) {
-        const int g = i % GB;
+      for (int i = lane; i < total; i += kLanes) {
+        const int q = i % GB;
         const int r = (i / GB) % kTC;
         const int tens = i / (GB * kTC);
         const Tin* src = reinterpret_cast<const Tin*>(tens == 0 ? a.Bm : a.Cm);
         const int64_t ld = tens == 0 ? a.ld_B : a.ld_C;
-        if (r < rows) cp_async<16>(&sm.bc[stage][tens][r][g * (16 / GE::ES)], src + (grow0 + r) * ld + g * (16 / GE::ES));
+        if (r < rows)
+          cp_async16(&sm.bc[stage][tens][r][q * (16 / TL::ES)], src + (grow0 + r) * ld + q * (16 / TL::ES));
       }
     } else {
-      for (int i = lane; i < NBC * kTC * N; i += 32) {
+      for (int i = lane; i < NBC * kTC * N; i += kLanes) {
         const int n = i % N;
         const int r = (i / N) % kTC;
         const int tens = i / (N * kTC);
@@ -235,7 +212,7 @@ __global__ void __launch_bounds__(32) scan_kernel(ScanArgs a, Work w, int act_ve
     cp_async_commit();
   }
 
-  const int64_t yoff = (b * T + t_begin) * a.ld_y + c;  // this channel's first y element
+  const int64_t yoff = (b * T + t_begin) * a.ld_y + c;  // this lane's first y element
   float sdelta = 0.0f;  // pass 1: sum of delta over the part
 #pragma unroll 1
   for (int64_t k = 0; k < nchunks; ++k) {
@@ -248,7 +225,7 @@ __global__ void __launch_bounds__(32) scan_kernel(ScanArgs a, Work w, int act_ve
     if constexpr (kBf16) {
       // widen this chunk's B (and C) rows to f32 once, shared by all lanes
 #pragma unroll
-      for (int i = lane; i < NBC * kTC * N; i += 32) {
+      for (int i = lane; i < NBC * kTC * N; i += kLanes) {
         const int n = i % N;
         const int r = (i / N) % kTC;
         const int tens = i / (N * kTC);
@@ -267,67 +244,85 @@ __global__ void __launch_bounds__(32) scan_kernel(ScanArgs a, Work w, int act_ve
     const Tin* su = &sm.act[stage][0][0][0];
     const Tin* sdt = &sm.act[stage][1][0][0];
     const Tin* sz = &sm.act[stage][GATE ? 2 : 0][0][0];
-    const int64_t yk = yoff + k * kTC * a.ld_y;
-
-    // One group of LPC rows: lane q evaluates the scalars (softplus, SiLU(z))
-    // of row r0 + q and passes delta to the other lanes of its channel; every
-    // lane then updates its P states for each row of the group in order.  The
-    // lanes' partial C . h are summed by an xor butterfly; lane j stores row r0 + j.
-    auto row_group = [&](int r0, int nvalid) {
-      const int rq = r0 + q;
-      float my_delta = 0.0f, my_u = 0.0f, my_g = 1.0f;
-      if (rq < r0 + nvalid) {
-        my_u = to_f32(su[rq * CT + cl]);
-        my_delta = softplus_f(to_f32(sdt[rq * CT + cl]) + dtb);
-        if (MODE != kPass1 && GATE) my_g = silu_f(to_f32(sz[rq * CT + cl]));
-      }
-#pragma unroll
-      for (int j = 0; j < LPC; ++j) {
-        if (j < nvalid) {  // warp-uniform
-          const int r = r0 + j;
-          const float delta = LPC == 1 ? my_delta : __shfl_sync(0xffffffffu, my_delta, lbase + j);
-          const float uj = LPC == 1 ? my_u : to_f32(su[r * CT + cl]);
-          const float du = delta * uj;
-          if (MODE == kPass1) {
-            sdelta += delta;
-            float Bv[P];
-            ld_f32<P>(sB + r * N + q * P, Bv);
-            ssm_state_group<P>(h, a2, delta, du, Bv);
-          } else {
-            float Bv[P], Cv[P];
-            ld_f32<P>(sB + r * N + q * P, Bv);
-            ld_f32<P>(sC + r * N + q * P, Cv);
-            float part_ = ssm_token_group<P>(h, a2, delta, du, Bv, Cv);
-#pragma unroll
-            for (int sft = 1; sft < LPC; sft *= 2) part_ = part_ + __shfl_xor_sync(0xffffffffu, part_, sft);
-            if (q == j && active) {
-              float y = fmaf(Dc, my_u, part_);
-              if (GATE) y *= my_g;
-              store_out(a.y, yk + r * a.ld_y, a.y_bf16, y);
-            }
-          }
-        }
-      }
+    auto prep = [&](int r) {
+      RowS s;
+      s.u = to_f32(su[r * kLanes + lane]);
+      s.delta = softplus_f(to_f32(sdt[r * kLanes + lane]) + dtb);
+      s.du = s.delta * s.u;
+      s.g = (MODE != kPass1 && GATE) ? silu_f(to_f32(sz[r * kLanes + lane])) : 1.0f;
+      return s;
     };
-    if (rows == kTC) {
+    if (!active) continue;
+
+    if (MODE == kPass1) {
+      auto row_state = [&](int r, const RowS& rs) {
+        sdelta += rs.delta;
 #pragma unroll
-      for (int r0 = 0; r0 < kTC; r0 += LPC) row_group(r0, LPC);
-    } else {
+        for (int q = 0; q < NG; ++q) {
+          float Bv[P];
+          ld_f32<P>(sB + r * N + q * P, Bv);
+          ssm_state_group<P>(h + q * P, a2 + q * P, rs.delta, rs.du, Bv);
+        }
+      };
+      if (rows == kTC) {
+        // full chunk: unrolled by kU rows, every row's scalars first, so the
+        // only serial chain left is the state update
 #pragma unroll 1
-      for (int r0 = 0; r0 < rows; r0 += LPC) row_group(r0, min(LPC, rows - r0));
+        for (int r0 = 0; r0 < kTC; r0 += kU) {
+          RowS rs[kU];
+#pragma unroll
+          for (int r = 0; r < kU; ++r) rs[r] = prep(r0 + r);
+#pragma unroll
+          for (int r = 0; r < kU; ++r) row_state(r0 + r, rs[r]);
+        }
+      } else {
+#pragma unroll 1
+        for (int r = 0; r < rows; ++r) row_state(r, prep(r));
+      }
+    } else {
+      const int64_t yk = yoff + k * kTC * a.ld_y;
+      auto row_out = [&](int r, const RowS& rs) {
+        float part_[NG];
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+          float Bv[P], Cv[P];
+          ld_f32<P>(sB + r * N + q * P, Bv);
+          ld_f32<P>(sC + r * N + q * P, Cv);
+          part_[q] = ssm_token_group<P>(h + q * P, a2 + q * P, rs.delta, rs.du, Bv, Cv);
+        }
+        float y = fmaf(Dc, rs.u, tree_sum<NG>(part_));
+        if (GATE) y *= rs.g;
+        store_out(a.y, yk + r * a.ld_y, a.y_bf16, y);
+      };
+      if (rows == kTC) {
+#pragma unroll 1
+        for (int r0 = 0; r0 < kTC; r0 += kU) {
+          RowS rs[kU];
+#pragma unroll
+          for (int r = 0; r < kU; ++r) rs[r] = prep(r0 + r);
+#pragma unroll
+          for (int r = 0; r < kU; ++r) row_out(r0 + r, rs[r]);
+        }
+      } else {
+#pragma unroll 1
+        for (int r = 0; r < rows; ++r) row_out(r, prep(r));
+      }
     }
   }
   cp_async_wait<0>();
 
   if (!active) return;
   if (MODE == kPass1) {
-    float pj[P];
+    float* Pj = w.ws + BDN * (1 + 2 * part) + srow;
+    float* Hj = w.ws + BDN * (2 + 2 * part) + srow;
 #pragma unroll
-    for (int n = 0; n < P; ++n) pj[n] = ex2_approx(a2[n] * sdelta);
-    st_f32<P>(w.ws + BDN * (1 + 2 * part) + srow, pj);
-    st_f32<P>(w.ws + BDN * (2 + 2 * part) + srow, h);
+    for (int n = 0; n < N; ++n) {
+      Pj[n] = ex2_approx(a2[n] * sdelta);
+      Hj[n] = h[n];
+    }
   } else if (a.state_out && (MODE == kSequential || part == w.parts - 1)) {
-    st_f32<P>(a.state_out + srow, h);
+#pragma unroll
+    for (int n = 0; n < N; ++n) a.state_out[srow + n] = h[n];
   }
 }
 
@@ -377,7 +372,7 @@ template <int N, typename Tin, int MODE, bool GATE>
 cudaError_t launch_mode(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
   const int64_t blocks = w.n_tiles * a.B * w.grid_parts;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  scan_kernel<N, Tin, MODE, GATE><<<(unsigned)blocks, 32, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
+  scan_kernel<N, Tin, MODE, GATE><<<(unsigned)blocks, kLanes, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
   return cudaGetLastError();
 }
 
@@ -393,7 +388,7 @@ cudaError_t launch_n(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream
   w.ws = ws;
   w.parts = p.parts;
   w.part_len = p.part_len;
-  w.n_tiles = (a.Di + Geo<N, Tin>::CT - 1) / Geo<N, Tin>::CT;
+  w.n_tiles = (a.Di + kLanes - 1) / kLanes;
   if (p.parts <= 1) {
     w.grid_parts = 1;
     return launch_out<N, Tin, kSequential>(a, w, p, stream);

@@ -10,21 +10,23 @@
 // here the route is picked from the shape (batch x channels vs SM count).
 //
 // Design (GB300):
-//  * One warp per CTA covering consecutive channels of one batch row; each
-//    lane holds 8 states (N/8 lanes per channel: 16 channels per CTA at
-//    d_state 16), so every global access of u, dt, z and y is a coalesced row
-//    segment and B_t / C_t (shared by all channels) are shared-memory
-//    broadcasts.  All synchronisation is __syncwarp; small one-warp CTAs give
-//    many resident warps and fine-grained load balance over the 152 SMs.
+//  * One warp per CTA; lane = channel, 32 consecutive channels of one batch
+//    row, so every global access of u, dt, z and y is a coalesced row segment
+//    and B_t / C_t (shared by all channels) are shared-memory broadcasts.  All
+//    synchronisation is __syncwarp; 1-warp CTAs also give fine-grained load
+//    balance over the 152 SMs.  (Splitting a channel's states over several
+//    lanes doubles the warps but costs more instructions per channel-row than
+//    the extra occupancy returns; narrow shapes get occupancy from the T split.)
 //  * u, dt, z, B, C stream in chunks of TC rows through a 3-deep cp.async ring
 //    (16-byte copies, L2-only): HBM sees one read of every input and one write
 //    of y.  bf16 B/C rows are widened to f32 once per chunk in shared memory.
-//  * A lane keeps its 8 states in registers (f32) and walks the rows
-//    sequentially.  The per-row scalars (softplus, SiLU(z)) are split over the
-//    lanes of a channel by row (lane j of a channel evaluates row r0 + j of each
-//    group of N/8 rows and shuffles delta to the others), the partial C . h
-//    are summed by an xor butterfly, and full 16-row chunks are unrolled so the
-//    only serial chain is the state FMA.  The state math is packed f32x2 plus
+//  * A lane keeps all N states of its channel in registers (f32) and walks the
+//    rows sequentially.  Full 16-row chunks are unrolled with every row's
+//    scalars (softplus, SiLU(z)) computed first, so the only serial chain is
+//    the state FMA.  The state math is packed f32x2 plus one MUFU ex2 per state
+//    and token: per token and channel at d_state 16 that is 16 ex2 + 64 FP32
+//    lane-ops on two pipes that both saturate, which, not HBM, bounds the
+//    prefill on GB300 (no tensor cores: there is no contraction).  The state math is packed f32x2 plus
 //    one MUFU ex2 per state and token; no tensor cores (no contraction).
 //  * Route "sequential" (wide shapes: enough batch x channel rows to fill the
 //    GPU): one launch, each CTA scans all T for its channels.
@@ -57,8 +59,8 @@ SCAN_DECL(64)
 
 namespace {
 inline bool aligned(const void* p, int n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
-// channels per one-warp CTA: 8 states per lane, N/8 lanes per channel
-inline int64_t channels_per_cta(int64_t N) { return N <= 8 ? 32 : 32 / (N / 8); }
+// channels per one-warp CTA (one lane per channel)
+inline int64_t channels_per_cta(int64_t) { return 32; }
 }  // namespace
 
 int64_t scan_workspace_bytes(int64_t B, int64_t Di, int64_t N, int parts) {
@@ -71,7 +73,10 @@ int scan_parts(int64_t B, int64_t T, int64_t Di, int64_t N, const DeviceInfo& de
   // an SM needs about kWarpsSat warps to keep its pipes busy, and every part but
   // the last is scanned twice (the state-only pass costs ~3/4 of the full one),
   // so the time is ~ ceil(T / P) * (1 + 0.75 (P-1)/P) * max(w, kWarpsSat).
-  constexpr double kWarpsSat = 8.0;
+#ifndef MAMBA_SCAN_WARPS_SAT
+#define MAMBA_SCAN_WARPS_SAT 8.0
+#endif
+  constexpr double kWarpsSat = MAMBA_SCAN_WARPS_SAT;
   const int64_t ct = channels_per_cta(N);
   const int64_t tiles = B * ((Di + ct - 1) / ct);
   double best = 0.0;
