@@ -182,6 +182,37 @@ MAMBA_API int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const 
                            float* ssm_state, int64_t layer, int64_t n_layers, int64_t B,
                            int64_t Di, int64_t N, void* stream);
 
+/*
+ * mamba_selective_scan_prefill_noalloc - the selective-scan prefill for callers
+ * that cannot allocate device memory.  (No counterpart in the mamba-rs pages:
+ * it is an addition of this library.)
+ *
+ * Some callers cannot call cudaMalloc or any allocating routine when they run
+ * the prefill -- an engine whose device memory is fixed at start-up, or a
+ * plugin inside a framework that owns the allocator -- so they cannot supply
+ * the workspace mamba_selective_scan_prefill uses to split narrow prefills
+ * along T.  This variant takes that scratch from a static device array of
+ * MAMBA_NOALLOC_SCRATCH_BYTES inside the library (held on every GPU that loads
+ * the library, until the process exits) and otherwise behaves exactly like
+ * mamba_selective_scan_prefill with enough workspace: same arguments minus the
+ * workspace, same result.  It allocates and frees nothing.
+ *   - Shapes whose split needs more scratch than the array holds are rejected
+ *     with MAMBA_ERR_UNSUPPORTED (see mamba_selective_scan_workspace_bytes).
+ *   - The first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents (none of
+ *     which is read before being rewritten); calls that overlap on the GPU,
+ *     from two streams or two threads, race on it and must be serialised by
+ *     the caller.
+ */
+#define MAMBA_NOALLOC_SCRATCH_BYTES (16LL * 1024 * 1024)
+MAMBA_API int mamba_selective_scan_prefill_noalloc(
+    void* y, int64_t ld_y, int y_dtype, const void* u, int64_t ld_u, const void* dt,
+    int64_t ld_dt, const void* z, int64_t ld_z, const void* Bm, int64_t ld_B, const void* Cm,
+    int64_t ld_C, int in_dtype, const float* A_log, const float* D, const float* dt_bias,
+    const float* ssm_state_in, float* ssm_state_out, int64_t B, int64_t T, int64_t Di, int64_t N,
+    void* stream);
+
 /* Thread-local description of the last error returned on this thread
  * (empty string after a successful call).  Never NULL; owned by the library. */
 MAMBA_API const char* mamba_last_error(void);

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     MAMBA_ERR_INVALID_ARG,
     MAMBA_ERR_UNSUPPORTED,
     MAMBA_F32,
+    MAMBA_NOALLOC_SCRATCH_BYTES,
     MAMBA_OK,
     MambaError,
     load,
@@ -23,6 +24,7 @@ from ._binding import (  # noqa: F401
     mamba_conv1d_silu_step,
     mamba_last_error,
     mamba_selective_scan_prefill,
+    mamba_selective_scan_prefill_noalloc,
     mamba_selective_scan_workspace_bytes,
     mamba_ssm_step_batched,
     mamba_version,

@@ -20,6 +20,7 @@ MAMBA_ERR_UNSUPPORTED = -2
 MAMBA_ERR_CUDA = -3
 MAMBA_F32 = 0
 MAMBA_BF16 = 1
+MAMBA_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 LIB_PATH = _build.LIB_PATH
 
@@ -29,6 +30,7 @@ ABI_SYMBOLS = (
     "mamba_conv1d_silu_step",
     "mamba_selective_scan_prefill",
     "mamba_selective_scan_workspace_bytes",
+    "mamba_selective_scan_prefill_noalloc",
     "mamba_ssm_step_batched",
     "mamba_last_error",
     "mamba_version",
@@ -62,6 +64,10 @@ def load(path: str | None = None):
         lib.mamba_selective_scan_prefill.argtypes = (
             [vp, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32]
             + [vp] * 5 + [i64, i64, i64, i64, vp, i64, vp])
+        lib.mamba_selective_scan_prefill_noalloc.argtypes = (
+            [vp, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32]
+            + [vp] * 5 + [i64, i64, i64, i64, vp])
+        lib.mamba_selective_scan_prefill_noalloc.restype = ctypes.c_int
         lib.mamba_selective_scan_workspace_bytes.argtypes = [i64, i64, i64, i64]
         lib.mamba_selective_scan_workspace_bytes.restype = i64
         lib.mamba_ssm_step_batched.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp]
@@ -272,3 +278,23 @@ def mamba_ssm_step_batched(y, u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt
         _ptr(y), _dtype_code(y), _ptr(u), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _dtype_code(u),
         _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state), int(layer), ssm_state.shape[0],
         Bsz, Di, N, _stream(stream, u)))
+
+
+def mamba_selective_scan_prefill_noalloc(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, z=None,
+                                         ssm_state_in=None, ssm_state_out=None, *, stream=None):
+    """The selective-scan prefill for callers that cannot allocate device memory:
+    its T-split scratch is a static array inside the library (see the C header).
+    Same arguments and result as mamba_selective_scan_prefill, minus the workspace."""
+    Bsz, T, Di = u.shape
+    N = A_log.shape[1]
+    _f32_param(A_log, "A_log", (Di, N))
+    _f32_param(D, "D", (Di,))
+    _f32_param(dt_bias, "dt_bias", (Di,))
+    _f32_param(ssm_state_in, "ssm_state_in", (Bsz, Di, N))
+    _f32_param(ssm_state_out, "ssm_state_out", (Bsz, Di, N))
+    _check(load().mamba_selective_scan_prefill_noalloc(
+        _ptr(y), _rows_ld(y, "y"), _dtype_code(y), _ptr(u), _rows_ld(u, "u"),
+        _ptr(dt), _rows_ld(dt, "dt"), _ptr(z), _rows_ld(z, "z") if z is not None else 0,
+        _ptr(Bm), _rows_ld(Bm, "Bm"), _ptr(Cm), _rows_ld(Cm, "Cm"), _dtype_code(u),
+        _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
+        Bsz, T, Di, N, _stream(stream, u)))

@@ -170,6 +170,11 @@ int copy_state(float* out, const float* in, int64_t count, cudaStream_t s) {
 
 }  // namespace
 
+int mamba::set_last_error(int code, const char* msg) {
+  snprintf(g_err, sizeof(g_err), "%s", msg ? msg : "");
+  return code;
+}
+
 extern "C" {
 
 const char* mamba_last_error(void) { return g_err; }

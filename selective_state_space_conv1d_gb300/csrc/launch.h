@@ -8,6 +8,9 @@
 
 namespace mamba {
 
+// Sets the thread-local message returned by mamba_last_error(); returns code.
+int set_last_error(int code, const char* msg);
+
 struct DeviceInfo {
   int sm_count;
   int max_smem_optin;  // bytes per block with opt-in
