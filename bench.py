@@ -268,6 +268,37 @@ def roofline(bytes_per_launch, ms, peak, peak_src, traffic):
             "algorithmic_bytes_per_launch": int(bytes_per_launch), "avg_launch_ms": round(ms, 6)}
 
 
+# MUFU peak of GB300: ex2 issues 32 lanes/clk/SM (lg2 and rcp 16, counted as 2
+# slots each), 152 SMs, 2070 MHz maximum SM clock.
+MUFU_SLOTS_PER_CLK_SM = 32
+GB300_SMS = 152
+GB300_MAX_SM_MHZ = 2070.0
+
+
+def mufu_peak_tops(sm_count=GB300_SMS):
+    return MUFU_SLOTS_PER_CLK_SM * sm_count * GB300_MAX_SM_MHZ * 1e6 / 1e12
+
+
+def scan_roofline(tc, N, gate, bytes_per_launch, ms, hbm_peak_gbs, peak_src, traffic, sm_count):
+    """The scan is bound by MUFU (and FMA) throughput, not HBM: per (token,
+    channel) it needs N ex2 for the states, ex2 + lg2 for softplus and, with a
+    gate, ex2 + rcp for SiLU (lg2/rcp at half rate count twice): N + 3 (+ 3)
+    ex2-equivalent MUFU slots.  Reported against the MUFU peak, with the HBM
+    view alongside."""
+    slots = tc * (N + 3 + (3 if gate else 0))
+    tops = slots / (ms * 1e-3) / 1e12
+    peak = mufu_peak_tops(sm_count)
+    gbs = bytes_per_launch / (ms * 1e-3) / 1e9
+    return {"bound": "alu", "achieved": round(tops, 3), "peak": round(peak, 3),
+            "unit": "T MUFU-slot/s", "frac": round(tops / peak, 4), "traffic": traffic,
+            "peak_source": f"derived: {MUFU_SLOTS_PER_CLK_SM} ex2/clk/SM x {sm_count} SMs x "
+                           f"{GB300_MAX_SM_MHZ:.0f} MHz",
+            "algorithmic_mufu_slots_per_launch": int(slots),
+            "algorithmic_bytes_per_launch": int(bytes_per_launch), "avg_launch_ms": round(ms, 6),
+            "hbm": {"achieved": round(gbs, 1), "peak": hbm_peak_gbs, "unit": "GB/s",
+                    "frac": round(gbs / hbm_peak_gbs, 4), "peak_source": peak_src}}
+
+
 def run_prefill(torch, m, synth, wl_index, steps, warmup, device, dist, clocks, host_inputs=True):
     wl = synth.WORKLOADS[wl_index]
     Bsz, T, Di, N, K = wl.batch, wl.seqlen, wl.d_inner, wl.d_state, wl.d_conv
@@ -374,21 +405,31 @@ def run_decode(torch, m, synth, device, peak, peak_src, n_steps=256):
         m.mamba_ssm_step_batched(y[l], u[l], dt[s, l], Bm[s, l], Cm[s, l], ssm, l, p["A_log"],
                                  p["D"], p["dt_bias"], z[s, l])
 
-    for s in range(3):  # warm-up steps
-        for l in range(L):
-            layer_step(s, l)
-    torch.cuda.synchronize()
-    g = capture(torch, lambda: [layer_step(s, l) for s in range(n_steps) for l in range(L)])
-    g.replay()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = 4
-    a.record()
-    for _ in range(reps):
+    def layer_step_fused(s, l):
+        p = params[l]
+        m.mamba_mixer_step_batched(y[l], x[s, l], dt[s, l], Bm[s, l], Cm[s, l], conv, ssm, l, p["conv_w"],
+                                   p["A_log"], p["conv_b"], p["D"], p["dt_bias"], z[s, l])
+
+    def time_decode(fn):
+        for s in range(3):  # warm-up steps
+            for l in range(L):
+                fn(s, l)
+        torch.cuda.synchronize()
+        g = capture(torch, lambda: [fn(s, l) for s in range(n_steps) for l in range(L)])
         g.replay()
-    b.record()
-    torch.cuda.synchronize()
-    ms_step = a.elapsed_time(b) / (reps * n_steps)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 4
+        a.record()
+        for _ in range(reps):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        del g
+        return a.elapsed_time(b) / (reps * n_steps)
+
+    ms_sep = time_decode(layer_step)
+    ms_fused = time_decode(layer_step_fused)
     # per-kernel durations: graphs of one kernel kind over 4 steps x 24 layers
     conv_calls = [lambda s=s, l=l: m.mamba_conv1d_silu_step(u[l], x[s, l], conv, l, params[l]["conv_w"],
                                                              params[l]["conv_b"])
@@ -397,26 +438,34 @@ def run_decode(torch, m, synth, device, peak, peak_src, n_steps=256):
                                                              params[l]["A_log"], params[l]["D"],
                                                              params[l]["dt_bias"], z[s, l])
                   for s in range(4) for l in range(L)]
+    fused_calls = [lambda s=s, l=l: layer_step_fused(s, l) for s in range(4) for l in range(L)]
     conv_ms = kernel_time(torch, conv_calls, len(conv_calls))
     step_ms = kernel_time(torch, step_calls, len(step_calls))
+    fused_ms = kernel_time(torch, fused_calls, len(fused_calls))
     rows = Bsz * Di
     step_bytes = rows * (2 * 4 * N + 5 * 4) + Bsz * N * 2 * 4 + Di * (N + 2) * 4
     conv_bytes = rows * (2 * 4 * K + 2 * 4) + Di * (K + 1) * 4
+    fused_bytes = rows * (2 * 4 * N + 2 * 4 * K + 4 * 4) + Bsz * N * 2 * 4 + Di * (N + K + 3) * 4
     out = {
-        "workload": wl.name, "value": round(1e3 / ms_step, 2), "unit": "steps/s",
-        "ms_per_step": round(ms_step, 5),
-        "layer_token_updates_per_s": round(1e3 / ms_step * L * Bsz, 1),
-        "algorithmic_bytes_per_step": int(L * (step_bytes + conv_bytes)),
-        "hbm_gbs_per_step": round(L * (step_bytes + conv_bytes) / (ms_step * 1e-3) / 1e9, 1),
+        "workload": wl.name, "value": round(1e3 / ms_fused, 2), "unit": "steps/s",
+        "ms_per_step": round(ms_fused, 5),
+        "layer_token_updates_per_s": round(1e3 / ms_fused * L * Bsz, 1),
+        "algorithmic_bytes_per_step": int(L * fused_bytes),
+        "hbm_gbs_per_step": round(L * fused_bytes / (ms_fused * 1e-3) / 1e9, 1),
+        "step": "fused mixer step (conv1d+SiLU step then SSM step, 1 launch per layer)",
+        "separate_calls": {"value": round(1e3 / ms_sep, 2), "unit": "steps/s", "ms_per_step": round(ms_sep, 5),
+                           "hbm_gbs_per_step": round(L * (step_bytes + conv_bytes) / (ms_sep * 1e-3) / 1e9, 1),
+                           "step": "conv1d step + SSM step, 2 launches per layer"},
         "config": {"n_layers": L, "batch": Bsz, "d_inner": Di, "d_state": N, "d_conv": K,
-                   "steps_per_replay": n_steps, "launch": "CUDA graph of 256 x 24 x 2 kernels",
+                   "steps_per_replay": n_steps, "launch": "CUDA graph of 256 steps x 24 layers",
                    "l2": f"state {L * rows * (N + K) * 4 / 1e6:.0f} MB > L2"},
-        "gpu_launches": 2 * L * n_steps * reps,
+        "gpu_launches_per_step": L, "separate_calls_launches_per_step": 2 * L,
     }
-    out["frac_of_hbm_peak"] = round(out["hbm_gbs_per_step"] / peak, 4)
-    out["roofline"] = roofline(step_bytes, step_ms, peak, peak_src, ncu_traffic("step", wl.name))
+    out["roofline"] = roofline(fused_bytes, fused_ms, peak, peak_src, ncu_traffic("mixer_step", wl.name))
+    out["ssm_step_roofline"] = roofline(step_bytes, step_ms, peak, peak_src, ncu_traffic("step", wl.name))
     out["conv_step_roofline"] = roofline(conv_bytes, conv_ms, peak, peak_src,
                                          ncu_traffic("conv", wl.name + "-step"))
+    out["frac_of_hbm_peak"] = round(out["hbm_gbs_per_step"] / peak, 4)
     return out
 
 
@@ -547,8 +596,10 @@ def main():
         total_ms = float(t.item())
     ms_step = total_ms / args.steps
     value = world * res["tokens_per_step"] * args.steps / (total_ms * 1e-3)
-    scan_roof = roofline(res["scan_bytes"], res["scan_ms"], peak, peak_src,
-                         ncu_traffic("scan", res["wl"].name))
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    wl1 = res["wl"]
+    scan_roof = scan_roofline(wl1.batch * wl1.seqlen * wl1.d_inner, wl1.d_state, True, res["scan_bytes"],
+                              res["scan_ms"], peak, peak_src, ncu_traffic("scan", wl1.name), sms)
     conv_roof = roofline(res["conv_bytes"], res["conv_ms"], peak, peak_src,
                          ncu_traffic("conv", res["wl"].name))
     step_gbs = (res["conv_bytes"] + res["scan_bytes"]) / (ms_step * 1e-3) / 1e9
@@ -561,8 +612,8 @@ def main():
             "workload": r3["wl"].name, "value": round(r3["tokens_per_step"] / (r3["ms_per_step"] * 1e-3), 1),
             "unit": "tokens/s", "ms_per_step": round(r3["ms_per_step"], 5),
             "hbm_gbs_per_step": round((r3["conv_bytes"] + r3["scan_bytes"]) / (r3["ms_per_step"] * 1e-3) / 1e9, 1),
-            "roofline": roofline(r3["scan_bytes"], r3["scan_ms"], peak, peak_src,
-                                 ncu_traffic("scan", r3["wl"].name)),
+            "roofline": scan_roofline(8 * 4096 * 5120, 16, True, r3["scan_bytes"], r3["scan_ms"], peak,
+                                      peak_src, ncu_traffic("scan", r3["wl"].name), sms),
             "conv_roofline": roofline(r3["conv_bytes"], r3["conv_ms"], peak, peak_src,
                                       ncu_traffic("conv", r3["wl"].name)),
             "config": {"batch": 8, "seq_len": 4096, "d_inner": 5120, "d_state": 16, "d_conv": 4,
@@ -591,12 +642,12 @@ def main():
                        "launch": "CUDA graph replays of 100 steps"},
             "hbm_gbs_per_step": round(step_gbs, 1),
             "roofline": scan_roof,
-            "roofline_kernel": ("selective-scan prefill call (" + ("T-split: state-only pass + full pass, 2 launches"
+            "roofline_kernel": ("selective-scan prefill call (" + ("T-split: state-only pass, fold, full pass: 3 launches"
                                  if res["scan_launches"] == 2 else "one sequential launch") + ")"),
             "conv_roofline": conv_roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": (1 + (3 if res["scan_launches"] == 2 else 1)) * args.steps,
             "clocks": res["clocks"],
             "extra": extra,
         }

@@ -183,6 +183,30 @@ MAMBA_API int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const 
                            int64_t Di, int64_t N, void* stream);
 
 /*
+ * Fused T=1 decode step of the whole mixer core: the conv1d + SiLU step on x
+ * followed by the SSM step on its output u, in one kernel, in place on the
+ * `layer` slabs of both persistent states ([n_layers][B][Di][K] and
+ * [n_layers][B][Di][N], f32).  (inference.rs: the mixed step already fuses the
+ * conv step with its SiLU and the gather + SSM step + gate; here both halves
+ * share one launch and u stays in registers.)
+ *
+ *   y          [B][Di] dense, dtype y_dtype (out)
+ *   x, dt      [B][Di] dense, dtype act_dtype; z [B][Di] or NULL
+ *   Bm, Cm     [B][N] dense, dtype act_dtype
+ *   conv_w [Di][K], conv_b [Di] or NULL, A_log [Di][N], D / dt_bias [Di] or NULL: f32
+ * The result equals mamba_conv1d_silu_step then mamba_ssm_step_batched bit for
+ * bit (u is rounded to act_dtype in between, as the separate calls store it).
+ * Errors: as for the two separate steps.
+ */
+MAMBA_API int mamba_mixer_step_batched(void* y, int y_dtype, const void* x, const void* dt,
+                                       const void* z, const void* Bm, const void* Cm,
+                                       int act_dtype, const float* conv_w, const float* conv_b,
+                                       const float* A_log, const float* D, const float* dt_bias,
+                                       float* conv_state, float* ssm_state, int64_t layer,
+                                       int64_t n_layers, int64_t B, int64_t Di, int64_t K,
+                                       int64_t N, void* stream);
+
+/*
  * mamba_selective_scan_prefill_noalloc - the selective-scan prefill for callers
  * that cannot allocate device memory.  (No counterpart in the mamba-rs pages:
  * it is an addition of this library.)

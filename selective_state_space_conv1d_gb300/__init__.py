@@ -5,6 +5,7 @@ Four C-ABI entry points (include/mamba_ssm.h), each a hand-written CUDA kernel:
   mamba_conv1d_silu_step        T=1 conv step on a [n_layers][B*Di*K] state
   mamba_selective_scan_prefill  selective scan + SiLU(z) gate, state in/out
   mamba_ssm_step_batched        T=1 SSM step on a [n_layers][B*Di*N] state
+  mamba_mixer_step_batched      both T=1 steps fused in one kernel
 This package is the thin Python binding (argument marshalling over ctypes);
 `synth` holds the seeded synthetic inputs used by the tests and the benchmark.
 """
@@ -23,6 +24,7 @@ from ._binding import (  # noqa: F401
     mamba_conv1d_silu_prefill,
     mamba_conv1d_silu_step,
     mamba_last_error,
+    mamba_mixer_step_batched,
     mamba_selective_scan_prefill,
     mamba_selective_scan_prefill_noalloc,
     mamba_selective_scan_workspace_bytes,

@@ -32,6 +32,7 @@ ABI_SYMBOLS = (
     "mamba_selective_scan_workspace_bytes",
     "mamba_selective_scan_prefill_noalloc",
     "mamba_ssm_step_batched",
+    "mamba_mixer_step_batched",
     "mamba_last_error",
     "mamba_version",
 )
@@ -71,7 +72,9 @@ def load(path: str | None = None):
         lib.mamba_selective_scan_workspace_bytes.argtypes = [i64, i64, i64, i64]
         lib.mamba_selective_scan_workspace_bytes.restype = i64
         lib.mamba_ssm_step_batched.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp]
-        for f in ("mamba_conv1d_silu_prefill", "mamba_conv1d_silu_step",
+        lib.mamba_mixer_step_batched.argtypes = ([vp, i32, vp, vp, vp, vp, vp, i32] + [vp] * 7
+                                                 + [i64, i64, i64, i64, i64, i64, vp])
+        for f in ("mamba_mixer_step_batched", "mamba_conv1d_silu_prefill", "mamba_conv1d_silu_step",
                   "mamba_selective_scan_prefill", "mamba_ssm_step_batched"):
             getattr(lib, f).restype = ctypes.c_int
         lib.mamba_last_error.argtypes = []
@@ -298,3 +301,37 @@ def mamba_selective_scan_prefill_noalloc(y, u, dt, Bm, Cm, A_log, D=None, dt_bia
         _ptr(Bm), _rows_ld(Bm, "Bm"), _ptr(Cm), _rows_ld(Cm, "Cm"), _dtype_code(u),
         _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
         Bsz, T, Di, N, _stream(stream, u)))
+
+
+def mamba_mixer_step_batched(y, x, dt, Bm, Cm, conv_state, ssm_state, layer, conv_w, A_log,
+                             conv_b=None, D=None, dt_bias=None, z=None, *, stream=None):
+    """Fused T=1 step: conv1d + SiLU step on x, then the SSM step, on slab `layer`
+    of conv_state [L, B, Di, K] and ssm_state [L, B, Di, N] (both updated in place).
+
+    y, x, dt, z: contiguous [B, Di]; Bm, Cm: contiguous [B, N]."""
+    Bsz, Di = x.shape
+    N = A_log.shape[1]
+    K = conv_w.shape[1]
+    for st, nm, last in ((conv_state, "conv_state", K), (ssm_state, "ssm_state", N)):
+        if st.dim() != 4 or tuple(st.shape[1:]) != (Bsz, Di, last) or not st.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous [n_layers, B, Di, {last}] tensor")
+        _f32_param(st, nm)
+    if conv_state.shape[0] != ssm_state.shape[0]:
+        raise ValueError("conv_state and ssm_state must have the same n_layers")
+    _f32_param(conv_w, "conv_w", (Di, K))
+    _f32_param(conv_b, "conv_b", (Di,))
+    _f32_param(A_log, "A_log", (Di, N))
+    _f32_param(D, "D", (Di,))
+    _f32_param(dt_bias, "dt_bias", (Di,))
+    for t, nm, shp in ((y, "y", (Bsz, Di)), (dt, "dt", (Bsz, Di)), (z, "z", (Bsz, Di)),
+                       (Bm, "Bm", (Bsz, N)), (Cm, "Cm", (Bsz, N))):
+        if t is None:
+            continue
+        if tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous {shp} tensor")
+        if nm != "y" and t.dtype != x.dtype:
+            raise ValueError(f"{nm} must have the dtype of x")
+    _check(load().mamba_mixer_step_batched(
+        _ptr(y), _dtype_code(y), _ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _dtype_code(x),
+        _ptr(conv_w), _ptr(conv_b), _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(conv_state),
+        _ptr(ssm_state), int(layer), ssm_state.shape[0], Bsz, Di, K, N, _stream(stream, x)))

@@ -363,4 +363,50 @@ int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const void* dt, 
   return ok();
 }
 
+int mamba_mixer_step_batched(void* y, int y_dtype, const void* x, const void* dt, const void* z,
+                             const void* Bm, const void* Cm, int act_dtype, const float* conv_w,
+                             const float* conv_b, const float* A_log, const float* D,
+                             const float* dt_bias, float* conv_state, float* ssm_state, int64_t layer,
+                             int64_t n_layers, int64_t B, int64_t Di, int64_t K, int64_t N,
+                             void* stream) {
+  int rc;
+  if ((rc = check_dtype("y_dtype", y_dtype)) || (rc = check_dtype("act_dtype", act_dtype))) return rc;
+  if (B < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld Di=%lld)", (long long)B, (long long)Di);
+  if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
+  if (K < 1 || K > MAMBA_MAX_D_CONV) return fail(MAMBA_ERR_UNSUPPORTED, "d_conv=%lld not in 1..%d", (long long)K, MAMBA_MAX_D_CONV);
+  if (n_layers < 1 || layer < 0 || layer >= n_layers) return fail(MAMBA_ERR_INVALID_ARG, "layer=%lld outside [0, n_layers=%lld)", (long long)layer, (long long)n_layers);
+  if (B == 0 || Di == 0) return ok();
+  if (!sizes_ok(B, Di, N) || !sizes_ok(B, Di, K) || !sizes_ok(n_layers, B * Di * N) || !sizes_ok(n_layers, B * Di * K))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!y || !x || !dt || !Bm || !Cm || !A_log || !conv_w || !conv_state || !ssm_state)
+    return fail(MAMBA_ERR_INVALID_ARG, "y, x, dt, Bm, Cm, A_log, conv_w, conv_state and ssm_state must not be NULL");
+  const int es = es_of(act_dtype), esy = es_of(y_dtype);
+  int64_t by = 0, bact = 0, bbc = 0, bA = 0, bv = 0, bss = 0, bcs = 0, bw = 0;
+  if (!span_bytes(1, B * Di, B * Di, esy, &by) || !span_bytes(1, B * Di, B * Di, es, &bact) ||
+      !span_bytes(1, B * N, B * N, es, &bbc) || !span_bytes(Di, N, N, 4, &bA) ||
+      !span_bytes(1, Di, Di, 4, &bv) || !span_bytes(B * Di, N, N, 4, &bss) ||
+      !span_bytes(B * Di, K, K, 4, &bcs) || !span_bytes(Di, K, K, 4, &bw))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  float* sslab = ssm_state + layer * B * Di * N;
+  float* cslab = conv_state + layer * B * Di * K;
+  Range ins[] = {range_of("x", x, bact), range_of("dt", dt, bact), range_of("z", z, z ? bact : 0),
+                 range_of("Bm", Bm, bbc), range_of("Cm", Cm, bbc), range_of("A_log", A_log, bA),
+                 range_of("D", D, bv), range_of("dt_bias", dt_bias, bv), range_of("conv_w", conv_w, bw),
+                 range_of("conv_b", conv_b, bv)};
+  Range outs[] = {range_of("y", y, by), range_of("ssm_state", sslab, bss),
+                  range_of("conv_state", cslab, bcs)};
+  if ((rc = check_pointers(ins, 10, dev_id)) || (rc = check_pointers(outs, 3, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 3, ins, 10))) return rc;
+  mamba::MixerStepArgs a{{y, y_dtype == MAMBA_BF16, nullptr, dt, z, Bm, Cm, act_dtype == MAMBA_BF16, A_log,
+                          D, dt_bias, sslab, B, Di, (int)N},
+                         x, cslab, conv_w, conv_b, (int)K};
+  cudaError_t e = mamba::launch_mixer_step_batched(a, dev, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("mixer_step_batched launch", e);
+  return ok();
+}
+
 }  // extern "C"

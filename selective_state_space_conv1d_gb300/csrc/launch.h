@@ -106,4 +106,16 @@ struct SsmStepArgs {
 cudaError_t launch_ssm_step_batched(const SsmStepArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream);
 
+// Fused decode step: conv1d + SiLU step on x, then the SSM step on its u.
+struct MixerStepArgs {
+  SsmStepArgs ssm;         // ssm.u unused (u is produced in registers)
+  const void* x;           // [B][Di], storage dtype ssm.in_bf16
+  float* conv_state;       // slab of the layer: [B][Di][K]
+  const float* conv_w;     // [Di][K]
+  const float* conv_b;     // [Di] or null
+  int K;
+};
+cudaError_t launch_mixer_step_batched(const MixerStepArgs& a, const DeviceInfo& dev,
+                                      cudaStream_t stream);
+
 }  // namespace mamba
