@@ -237,6 +237,23 @@ MAMBA_API int mamba_selective_scan_prefill_noalloc(
     const float* ssm_state_in, float* ssm_state_out, int64_t B, int64_t T, int64_t Di, int64_t N,
     void* stream);
 
+/*
+ * mamba_device_faults - device-side watchdog events since the last clear.
+ * (No counterpart in the mamba-rs pages: an addition of this library.)
+ *
+ * The decode-step kernels stream their tiles through a ring of shared-memory
+ * stages filled by bulk asynchronous copies and handed over with mbarriers.
+ * Every wait on such a barrier is bounded (about a second of SM clock); a wait
+ * that runs out sets MAMBA_FAULT_RING_WAIT here and the kernel leaves its loop
+ * instead of hanging, so that launch's outputs are incomplete.  In correct
+ * operation no wait runs out and the value stays 0.
+ *   - Synchronises the current device (so it cannot be called during stream
+ *     capture), then returns the fault bits (>= 0) of that device, or
+ *     MAMBA_ERR_CUDA.  `clear` != 0 resets the bits after reading them.
+ */
+#define MAMBA_FAULT_RING_WAIT 1
+MAMBA_API int mamba_device_faults(int clear);
+
 /* Thread-local description of the last error returned on this thread
  * (empty string after a successful call).  Never NULL; owned by the library. */
 MAMBA_API const char* mamba_last_error(void);

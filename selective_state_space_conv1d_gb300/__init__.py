@@ -17,12 +17,14 @@ from ._binding import (  # noqa: F401
     MAMBA_ERR_INVALID_ARG,
     MAMBA_ERR_UNSUPPORTED,
     MAMBA_F32,
+    MAMBA_FAULT_RING_WAIT,
     MAMBA_NOALLOC_SCRATCH_BYTES,
     MAMBA_OK,
     MambaError,
     load,
     mamba_conv1d_silu_prefill,
     mamba_conv1d_silu_step,
+    mamba_device_faults,
     mamba_last_error,
     mamba_mixer_step_batched,
     mamba_selective_scan_prefill,

@@ -33,6 +33,7 @@ ABI_SYMBOLS = (
     "mamba_selective_scan_prefill_noalloc",
     "mamba_ssm_step_batched",
     "mamba_mixer_step_batched",
+    "mamba_device_faults",
     "mamba_last_error",
     "mamba_version",
 )
@@ -77,6 +78,8 @@ def load(path: str | None = None):
         for f in ("mamba_mixer_step_batched", "mamba_conv1d_silu_prefill", "mamba_conv1d_silu_step",
                   "mamba_selective_scan_prefill", "mamba_ssm_step_batched"):
             getattr(lib, f).restype = ctypes.c_int
+        lib.mamba_device_faults.argtypes = [i32]
+        lib.mamba_device_faults.restype = ctypes.c_int
         lib.mamba_last_error.argtypes = []
         lib.mamba_last_error.restype = ctypes.c_char_p
         lib.mamba_version.argtypes = []
@@ -91,6 +94,18 @@ def mamba_last_error() -> str:
 
 def mamba_version() -> str:
     return load().mamba_version().decode()
+
+
+MAMBA_FAULT_RING_WAIT = 1
+
+
+def mamba_device_faults(clear: bool = False) -> int:
+    """Watchdog bits of the current device (MAMBA_FAULT_RING_WAIT: a bounded
+    wait of the decode-step copy ring ran out); synchronises the device."""
+    v = load().mamba_device_faults(1 if clear else 0)
+    if v < 0:
+        raise MambaError(int(v), mamba_last_error())
+    return int(v)
 
 
 def _check(status: int):

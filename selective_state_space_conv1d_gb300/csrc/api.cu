@@ -181,6 +181,13 @@ const char* mamba_last_error(void) { return g_err; }
 
 const char* mamba_version(void) { return "0.1.0"; }
 
+int mamba_device_faults(int clear) {
+  cudaError_t e = cudaSuccess;
+  const int v = mamba::read_device_faults(clear != 0, &e);
+  if (v < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: %s", cudaGetErrorString(e));
+  return ok(), v;
+}
+
 int mamba_conv1d_silu_prefill(void* u, int64_t ld_u, const void* x, int64_t ld_x, int act_dtype,
                               const float* conv_state_in, float* conv_state_out, const float* w,
                               const float* bias, int64_t B, int64_t T, int64_t Di, int64_t K,

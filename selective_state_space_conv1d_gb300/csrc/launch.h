@@ -11,6 +11,10 @@ namespace mamba {
 // Sets the thread-local message returned by mamba_last_error(); returns code.
 int set_last_error(int code, const char* msg);
 
+// Synchronises the current device and returns its watchdog fault bits
+// (MAMBA_FAULT_*), clearing them if asked; -1 and *err on a CUDA error.
+int read_device_faults(bool clear, cudaError_t* err);
+
 struct DeviceInfo {
   int sm_count;
   int max_smem_optin;  // bytes per block with opt-in

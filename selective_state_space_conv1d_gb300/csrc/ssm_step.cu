@@ -11,15 +11,26 @@
 //
 // Design (GB300): the step streams the f32 state once in and once out
 // (2 * 4 * N bytes per (batch, channel), plus 2 * 4 * K for the conv window when
-// fused).  Each lane owns a group of P = min(N, 8) consecutive states of one
-// channel (N/P lanes per channel, adjacent) and serves kRows batch rows of it.
-// All HBM traffic of those rows -- state groups, conv windows, u/x, dt, z -- is
-// requested before any arithmetic (one memory round trip, ~200 B in flight per
-// lane); B / C rows, shared by every channel of a batch row, are L1/L2 hits
-// fetched one row ahead.  The lanes' partial C . h are summed with an xor
-// butterfly in the prefill's order, so one step equals a T=1 prefill bit for
-// bit, and the fused step equals conv step + SSM step bit for bit (u is
-// rounded to the storage dtype exactly as the separate conv step stores it).
+// fused).  A thread owns a group of P = min(N, 8) consecutive states of one
+// channel (N/P adjacent threads per channel).  Two kernels share that mapping
+// and the arithmetic:
+//  * ring_step_kernel (the main path): a persistent grid of SMs x resident CTAs;
+//    each CTA walks a contiguous range of (channel block, batch row) tiles.  One
+//    producer thread streams every tile's state, conv window, x/u, dt, z and
+//    B/C rows into a ring of shared-memory stages with bulk asynchronous copies
+//    (cp.async.bulk, completion on an mbarrier per stage); four consumer warps
+//    take each stage into registers, release it, compute and store.  Bytes in
+//    flight are set by the ring size, not by registers or by waves of CTAs.
+//  * step_kernel (any alignment / shape): each thread serves kRows batch rows
+//    and issues all their loads before any arithmetic (one memory round trip).
+// The threads' partial C . h are summed with an xor butterfly in the prefill's
+// order, so one step equals a T=1 prefill bit for bit, and the fused step equals
+// conv step + SSM step bit for bit (u is rounded to the storage dtype exactly as
+// the separate conv step stores it).
+#include <atomic>
+
+#include "../../include/mamba_ssm.h"
+#include "async_copy.cuh"
 #include "device_math.cuh"
 #include "launch.h"
 
@@ -180,6 +191,228 @@ __global__ void __launch_bounds__(kMaxThreads) step_kernel(StepArgs args, int bt
   }
 }
 
+// ------------------------------------------------------------ ring path --
+namespace ring {
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;  // + one producer warp (lane 0 issues)
+constexpr int kMaxStages = 16;
+constexpr int kBarBytes = 2 * kMaxStages * 8;  // full[kMaxStages], empty[kMaxStages]
+constexpr long long kWaitLimit = 1ll << 31;    // SM cycles (about a second)
+#ifndef MAMBA_STEP_RING_BYTES
+#define MAMBA_STEP_RING_BYTES (64 * 1024)
+#endif
+constexpr int kRingBytes = MAMBA_STEP_RING_BYTES;  // shared memory per CTA for the stages
+}  // namespace ring
+
+__host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
+
+// One stage = one (channel block, batch row) tile: byte offsets of its parts.
+template <int N, int K, typename Tin, bool FUSE>
+struct RingTile {
+  static constexpr int P = group_size(N);
+  static constexpr int NG = N / P;
+  static constexpr int CB = ring::kConsumers / NG;  // channels per tile
+  static constexpr int es = sizeof(Tin);
+  static constexpr int kState = 0;                               // [CB][N] f32
+  static constexpr int kConv = kState + CB * N * 4;              // [CB][K] f32 (fused)
+  static constexpr int kUX = kConv + (FUSE ? CB * K * 4 : 0);    // x (fused) or u: [CB]
+  static constexpr int kDT = kUX + align16(CB * es);
+  static constexpr int kZ = kDT + align16(CB * es);
+  static constexpr int kB = kZ + align16(CB * es);               // B row: [N]
+  static constexpr int kC = kB + align16(N * es);                // C row: [N]
+  static constexpr int kBytes = (kC + align16(N * es) + 127) & ~127;
+};
+
+__device__ int g_device_faults = 0;  // MAMBA_FAULT_* bits, set by bounded waits that gave up
+
+__device__ __forceinline__ void flag_fault(int bit) { atomicOr(&g_device_faults, bit); }
+
+template <int P>
+__device__ __forceinline__ void store_group_cs(float* p, const float (&o)[P]) {
+  if constexpr (P % 4 == 0) {
+#pragma unroll
+    for (int j = 0; j < P; j += 4)
+      __stcs(reinterpret_cast<float4*>(p + j), make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < P; ++j) __stcs(p + j, o[j]);
+  }
+}
+
+// Tiles are numbered cblk * B + b; CTA i takes the contiguous range
+// [n_tiles * i / grid, n_tiles * (i + 1) / grid), so consecutive tiles of a CTA
+// share a channel block and its parameters stay in registers.
+template <int N, int K, typename Tin, bool FUSE>
+__global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args, int stages, int64_t n_tiles) {
+  using L = RingTile<N, K, Tin, FUSE>;
+  constexpr int P = L::P, NG = L::NG, CB = L::CB, es = L::es;
+  constexpr int KK = FUSE ? K : 1;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const SsmStepArgs& a = args.s;
+  const uint32_t bars = smem_u32(smem);
+  const auto full = [&](int s) { return bars + 8u * s; };
+  const auto empty = [&](int s) { return bars + 8u * (ring::kMaxStages + s); };
+  const int64_t t_begin = n_tiles * blockIdx.x / gridDim.x;
+  const int n_my = (int)(n_tiles * (blockIdx.x + 1) / gridDim.x - t_begin);
+  const int64_t Bsz = a.B, Di = a.Di;
+  const bool gate = a.z != nullptr;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), ring::kConsumerWarps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == ring::kConsumerWarps) {
+    // ---- producer: one thread streams the tiles into the ring ----
+    if (lane != 0) return;
+    const char* UX = reinterpret_cast<const char*>(FUSE ? args.x : a.u);
+    const char* DT = reinterpret_cast<const char*>(a.dt);
+    const char* Z = reinterpret_cast<const char*>(a.z);
+    const char* BM = reinterpret_cast<const char*>(a.Bm);
+    const char* CM = reinterpret_cast<const char*>(a.Cm);
+    const uint32_t ring0 = bars + ring::kBarBytes;
+    int issued = 0;
+    for (int i = 0; i < n_my; ++i) {
+      const int s = i % stages;
+      if (i >= stages && !mbar_wait(empty(s), ((i / stages) - 1) & 1, ring::kWaitLimit)) {
+        flag_fault(MAMBA_FAULT_RING_WAIT);
+        break;
+      }
+      const int64_t tile = t_begin + i, cblk = tile / Bsz, b = tile - cblk * Bsz;
+      const int64_t c0 = cblk * CB;
+      const uint32_t nch = (uint32_t)(Di - c0 < CB ? Di - c0 : CB);
+      const int64_t row = b * Di + c0;
+      const uint32_t st = ring0 + (uint32_t)(s * L::kBytes), fb = full(s);
+      const uint32_t act = nch * es;
+      const uint32_t bytes = nch * N * 4 + (FUSE ? nch * K * 4 : 0) + (gate ? 3 : 2) * act + 2 * N * es;
+      mbar_arrive_expect_tx(fb, bytes);
+      bulk_g2s(st + L::kState, a.state + row * N, nch * N * 4, fb);
+      if constexpr (FUSE) bulk_g2s(st + L::kConv, args.conv_state + row * K, nch * K * 4, fb);
+      bulk_g2s(st + L::kUX, UX + row * es, act, fb);
+      bulk_g2s(st + L::kDT, DT + row * es, act, fb);
+      if (gate) bulk_g2s(st + L::kZ, Z + row * es, act, fb);
+      bulk_g2s(st + L::kB, BM + b * N * es, N * es, fb);
+      bulk_g2s(st + L::kC, CM + b * N * es, N * es, fb);
+      issued = i + 1;
+    }
+    // every issued copy lands before this thread leaves
+    for (int i = issued > stages ? issued - stages : 0; i < issued; ++i)
+      if (!mbar_wait(full(i % stages), (i / stages) & 1, ring::kWaitLimit)) flag_fault(MAMBA_FAULT_RING_WAIT);
+    return;
+  }
+
+  // ---- consumers: 128 threads, thread -> (channel cl, state group q) ----
+  const int q = threadIdx.x % NG;
+  const int cl = threadIdx.x / NG;
+  int64_t cur_cblk = -1;
+  float a2[P], w[KK], dtb = 0.0f, Dc = 0.0f, cb = 0.0f;
+  for (int i = 0; i < n_my; ++i) {
+    const int64_t tile = t_begin + i, cblk = tile / Bsz, b = tile - cblk * Bsz;
+    const int64_t c = cblk * CB + cl;
+    const bool valid = c < Di;
+    if (cblk != cur_cblk) {  // per-channel parameters (L2), loaded while the stage lands
+      cur_cblk = cblk;
+      const int64_t cc = valid ? c : Di - 1;
+      const float* al = a.A_log + cc * N + q * P;
+#pragma unroll
+      for (int j = 0; j < P; ++j) a2[j] = a2_from_alog(al[j]);
+      dtb = a.dt_bias ? a.dt_bias[cc] : 0.0f;
+      Dc = a.D ? a.D[cc] : 0.0f;
+      if constexpr (FUSE) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) w[k] = args.conv_w[cc * K + k];
+        cb = args.conv_b ? args.conv_b[cc] : 0.0f;
+      }
+    }
+    const int s = i % stages;
+    if (!__all_sync(0xffffffffu, mbar_wait(full(s), (i / stages) & 1, ring::kWaitLimit))) {
+      if (lane == 0) flag_fault(MAMBA_FAULT_RING_WAIT);
+      break;
+    }
+    const unsigned char* sp = smem + ring::kBarBytes + s * L::kBytes;
+    float h[P], win[KK], Bv[P], Cv[P];
+    load_group<P>(reinterpret_cast<const float*>(sp + L::kState) + cl * N + q * P, h, true);
+    if constexpr (FUSE) load_group<KK>(reinterpret_cast<const float*>(sp + L::kConv) + cl * K, win, K % 4 == 0);
+    const float uxv = to_f32(reinterpret_cast<const Tin*>(sp + L::kUX)[cl]);
+    const float dtv = to_f32(reinterpret_cast<const Tin*>(sp + L::kDT)[cl]);
+    const float zv = gate ? to_f32(reinterpret_cast<const Tin*>(sp + L::kZ)[cl]) : 0.0f;
+    load_group<P>(reinterpret_cast<const Tin*>(sp + L::kB) + q * P, Bv, true);
+    load_group<P>(reinterpret_cast<const Tin*>(sp + L::kC) + q * P, Cv, true);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty(s));  // the stage is in registers: hand it back
+
+    const int64_t row = b * Di + c;
+    float uv = uxv;
+    if constexpr (FUSE) {
+      float sw[KK];
+#pragma unroll
+      for (int k = 0; k + 1 < K; ++k) sw[k] = win[k + 1];
+      sw[K - 1] = uxv;
+      uv = to_f32(from_f32<Tin>(silu_f(conv_taps<KK>(w, sw, cb))));
+      if (valid && q == 0) store_group<KK>(args.conv_state + row * K, sw, K % 4 == 0);
+    }
+    const float delta = softplus_f(dtv + dtb);
+    const float du = delta * uv;
+    float part = ssm_token_group<P>(h, a2, delta, du, Bv, Cv);
+#pragma unroll
+    for (int sft = 1; sft < NG; sft *= 2) part = part + __shfl_xor_sync(0xffffffffu, part, sft);
+    if (valid) {
+      store_group_cs<P>(a.state + row * N + q * P, h);
+      if (q == 0) store_out(a.y, row, a.y_bf16, ssm_output(part, Dc, uv, gate, zv));
+    }
+  }
+}
+
+// The ring path needs every bulk copy 16-byte aligned and a multiple of 16
+// bytes: Di % 8 == 0 (tile offsets and lengths are multiples of 8 channels),
+// N * es % 16 == 0 (B / C rows), and 16-byte aligned base pointers.
+bool ring_eligible(const StepArgs& a, bool fuse) {
+  const int es = a.s.in_bf16 ? 2 : 4;
+  const auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
+  if (a.s.Di % 8 != 0 || (a.s.N * es) % 16 != 0) return false;
+  if (!al(a.s.state) || !al(a.s.dt) || !al(a.s.Bm) || !al(a.s.Cm)) return false;
+  if (a.s.z && !al(a.s.z)) return false;
+  return fuse ? (al(a.x) && al(a.conv_state)) : al(a.s.u);
+}
+
+template <int N, int K, typename Tin, bool FUSE>
+cudaError_t launch_ring(const StepArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
+  using L = RingTile<N, K, Tin, FUSE>;
+  constexpr int kStages =
+      ring::kRingBytes / L::kBytes < 2 ? 2
+      : (ring::kRingBytes / L::kBytes > ring::kMaxStages ? ring::kMaxStages : ring::kRingBytes / L::kBytes);
+  constexpr int kSmem = ring::kBarBytes + kStages * L::kBytes;
+  static std::atomic<int> occ_cache[64];
+  int dev_id = 0;
+  cudaError_t e = cudaGetDevice(&dev_id);
+  if (e != cudaSuccess) return e;
+  if (dev_id < 0 || dev_id >= 64) return cudaErrorInvalidDevice;
+  int occ = occ_cache[dev_id].load(std::memory_order_relaxed);
+  if (occ == 0) {
+    if (kSmem > 48 * 1024 &&
+        (e = cudaFuncSetAttribute(ring_step_kernel<N, K, Tin, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  kSmem)) != cudaSuccess)
+      return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, ring_step_kernel<N, K, Tin, FUSE>, ring::kThreads,
+                                                           kSmem)) != cudaSuccess)
+      return e;
+    occ = occ < 1 ? 1 : occ;
+    occ_cache[dev_id].store(occ, std::memory_order_relaxed);
+  }
+  const int64_t n_cblk = (a.s.Di + L::CB - 1) / L::CB;
+  const int64_t n_tiles = n_cblk * a.s.B;
+  const int64_t resident = (int64_t)dev.sm_count * occ;
+  const int64_t grid = n_tiles < resident ? n_tiles : resident;
+  ring_step_kernel<N, K, Tin, FUSE><<<(unsigned)grid, ring::kThreads, kSmem, stream>>>(a, kStages, n_tiles);
+  return cudaGetLastError();
+}
+
 template <int N, int K, typename Tin, bool FUSE>
 cudaError_t launch_nk(const StepArgs& a, cudaStream_t stream) {
   constexpr int NG = N / group_size(N);
@@ -201,36 +434,45 @@ cudaError_t launch_nk(const StepArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+template <int N, int K, typename Tin, bool FUSE>
+cudaError_t launch_nk_any(const StepArgs& a, const DeviceInfo& dev, bool use_ring, cudaStream_t s) {
+  if constexpr ((N * sizeof(Tin)) % 16 == 0) {
+    if (use_ring) return launch_ring<N, K, Tin, FUSE>(a, dev, s);
+  }
+  return launch_nk<N, K, Tin, FUSE>(a, s);
+}
+
 template <int N, typename Tin, bool FUSE>
-cudaError_t launch_k(const StepArgs& a, int K, cudaStream_t s) {
+cudaError_t launch_k(const StepArgs& a, const DeviceInfo& dev, int K, bool r, cudaStream_t s) {
   if constexpr (!FUSE) {
     (void)K;
-    return launch_nk<N, 1, Tin, false>(a, s);
+    return launch_nk_any<N, 1, Tin, false>(a, dev, r, s);
   } else {
     switch (K) {
-      case 1: return launch_nk<N, 1, Tin, true>(a, s);
-      case 2: return launch_nk<N, 2, Tin, true>(a, s);
-      case 3: return launch_nk<N, 3, Tin, true>(a, s);
-      case 4: return launch_nk<N, 4, Tin, true>(a, s);
-      case 5: return launch_nk<N, 5, Tin, true>(a, s);
-      case 6: return launch_nk<N, 6, Tin, true>(a, s);
-      case 7: return launch_nk<N, 7, Tin, true>(a, s);
-      case 8: return launch_nk<N, 8, Tin, true>(a, s);
+      case 1: return launch_nk_any<N, 1, Tin, true>(a, dev, r, s);
+      case 2: return launch_nk_any<N, 2, Tin, true>(a, dev, r, s);
+      case 3: return launch_nk_any<N, 3, Tin, true>(a, dev, r, s);
+      case 4: return launch_nk_any<N, 4, Tin, true>(a, dev, r, s);
+      case 5: return launch_nk_any<N, 5, Tin, true>(a, dev, r, s);
+      case 6: return launch_nk_any<N, 6, Tin, true>(a, dev, r, s);
+      case 7: return launch_nk_any<N, 7, Tin, true>(a, dev, r, s);
+      case 8: return launch_nk_any<N, 8, Tin, true>(a, dev, r, s);
     }
     return cudaErrorInvalidValue;
   }
 }
 
 template <typename Tin, bool FUSE>
-cudaError_t launch_t(const StepArgs& a, int K, cudaStream_t s) {
+cudaError_t launch_t(const StepArgs& a, const DeviceInfo& dev, int K, cudaStream_t s) {
+  const bool r = ring_eligible(a, FUSE);
   switch (a.s.N) {
-    case 1: return launch_k<1, Tin, FUSE>(a, K, s);
-    case 2: return launch_k<2, Tin, FUSE>(a, K, s);
-    case 4: return launch_k<4, Tin, FUSE>(a, K, s);
-    case 8: return launch_k<8, Tin, FUSE>(a, K, s);
-    case 16: return launch_k<16, Tin, FUSE>(a, K, s);
-    case 32: return launch_k<32, Tin, FUSE>(a, K, s);
-    case 64: return launch_k<64, Tin, FUSE>(a, K, s);
+    case 1: return launch_k<1, Tin, FUSE>(a, dev, K, r, s);
+    case 2: return launch_k<2, Tin, FUSE>(a, dev, K, r, s);
+    case 4: return launch_k<4, Tin, FUSE>(a, dev, K, r, s);
+    case 8: return launch_k<8, Tin, FUSE>(a, dev, K, r, s);
+    case 16: return launch_k<16, Tin, FUSE>(a, dev, K, r, s);
+    case 32: return launch_k<32, Tin, FUSE>(a, dev, K, r, s);
+    case 64: return launch_k<64, Tin, FUSE>(a, dev, K, r, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -239,17 +481,28 @@ cudaError_t launch_t(const StepArgs& a, int K, cudaStream_t s) {
 
 cudaError_t launch_ssm_step_batched(const SsmStepArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream) {
-  (void)dev;
   StepArgs s{a, nullptr, nullptr, nullptr, nullptr};
-  return a.in_bf16 ? launch_t<__nv_bfloat16, false>(s, 1, stream) : launch_t<float, false>(s, 1, stream);
+  return a.in_bf16 ? launch_t<__nv_bfloat16, false>(s, dev, 1, stream)
+                   : launch_t<float, false>(s, dev, 1, stream);
 }
 
 cudaError_t launch_mixer_step_batched(const MixerStepArgs& m, const DeviceInfo& dev,
                                       cudaStream_t stream) {
-  (void)dev;
   StepArgs s{m.ssm, m.x, m.conv_state, m.conv_w, m.conv_b};
-  return m.ssm.in_bf16 ? launch_t<__nv_bfloat16, true>(s, m.K, stream)
-                       : launch_t<float, true>(s, m.K, stream);
+  return m.ssm.in_bf16 ? launch_t<__nv_bfloat16, true>(s, dev, m.K, stream)
+                       : launch_t<float, true>(s, dev, m.K, stream);
+}
+
+int read_device_faults(bool clear, cudaError_t* err) {
+  int v = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(&v, g_device_faults, sizeof(int));
+  if (e == cudaSuccess && clear && v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_device_faults, &zero, sizeof(int));
+  }
+  *err = e;
+  return e == cudaSuccess ? v : -1;
 }
 
 }  // namespace mamba

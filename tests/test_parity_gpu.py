@@ -424,3 +424,46 @@ def test_mixer_step_equals_conv_step_then_ssm_step_bitwise(cuda_lib, N, K, dtype
     assert np.array_equal(to_host(c2), conv_ref)
     if dtype == "f32":
         assert_within(to_host(s2), ssm_ref, "ssm state")
+
+
+# ------------------------------------------------- ring vs direct step path ----
+
+def _offset_like(t, elems=1):
+    """A copy of t whose data starts `elems` elements past a 16-byte boundary
+    (so the decode steps take their any-alignment kernel)."""
+    flat = torch.empty(t.numel() + elems, device=t.device, dtype=t.dtype)
+    v = flat[elems:].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("N,K,dtype,fused", [(16, 4, "f32", True), (16, 4, "bf16", False), (64, 4, "f32", True),
+                                             (8, 3, "bf16", True), (4, 4, "f32", False), (32, 2, "f32", True)])
+def test_step_ring_and_direct_paths_agree_bitwise(cuda_lib, N, K, dtype, fused):
+    """The copy-ring kernel (aligned buffers, d_inner % 8 == 0) and the
+    any-alignment kernel give identical y and states."""
+    m = cuda_lib
+    L, Bsz, Di = 2, 37, 264
+    p = _params(SEED + 5, Di, N, K, layer=0)
+    pd = {k: to_dev(v) for k, v in p.items()}
+    conv_a = to_dev(synth.normal(SEED, "conv_state", (L, Bsz, Di, K), 0.5))
+    ssm_a = to_dev(synth.normal(SEED, "ssm_state", (L, Bsz, Di, N), 0.5))
+    conv_b, ssm_b = _offset_like(conv_a), _offset_like(ssm_a)
+    for step in range(4):
+        inp = synth.decode_step_inputs(SEED, 0, step, Bsz, Di, N, dtype)
+        x, dt, z = (to_dev(inp[k], dtype) for k in ("x", "dt", "z"))
+        Bm, Cm = to_dev(inp["B"], dtype), to_dev(inp["C"], dtype)
+        ya = torch.empty((Bsz, Di), device="cuda")
+        yb = torch.empty((Bsz, Di), device="cuda")
+        if fused:
+            m.mamba_mixer_step_batched(ya, x, dt, Bm, Cm, conv_a, ssm_a, 1, pd["conv_w"], pd["A_log"],
+                                       pd["conv_b"], pd["D"], pd["dt_bias"], z)
+            m.mamba_mixer_step_batched(yb, x, dt, Bm, Cm, conv_b, ssm_b, 1, pd["conv_w"], pd["A_log"],
+                                       pd["conv_b"], pd["D"], pd["dt_bias"], z)
+        else:
+            m.mamba_ssm_step_batched(ya, x, dt, Bm, Cm, ssm_a, 1, pd["A_log"], pd["D"], pd["dt_bias"], z)
+            m.mamba_ssm_step_batched(yb, x, dt, Bm, Cm, ssm_b, 1, pd["A_log"], pd["D"], pd["dt_bias"], z)
+        torch.cuda.synchronize()
+        assert torch.equal(ya, yb), f"y differs at step {step}"
+        assert torch.equal(ssm_a, ssm_b) and torch.equal(conv_a, conv_b)
+    assert m.mamba_device_faults(clear=True) == 0
