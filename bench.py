@@ -34,12 +34,16 @@ METRIC = "prefill tokens/s and decode steps/s (batch×layers) at 1 GB300; HBM GB
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = {
     "scan": ["selective_state_space_conv1d_gb300/csrc/scan_prefill.cu",
+             "selective_state_space_conv1d_gb300/csrc/scan_kernel.cuh",
+             "selective_state_space_conv1d_gb300/csrc/scan_inst.cu",
              "selective_state_space_conv1d_gb300/csrc/device_math.cuh"],
     "conv": ["selective_state_space_conv1d_gb300/csrc/conv1d.cu",
              "selective_state_space_conv1d_gb300/csrc/device_math.cuh"],
     "step": ["selective_state_space_conv1d_gb300/csrc/ssm_step.cu",
+             "selective_state_space_conv1d_gb300/csrc/async_copy.cuh",
              "selective_state_space_conv1d_gb300/csrc/device_math.cuh"],
 }
+KERNEL_SOURCES["mixer_step"] = KERNEL_SOURCES["step"]
 
 
 # ---------------------------------------------------------------- utilities --

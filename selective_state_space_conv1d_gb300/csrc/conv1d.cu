@@ -76,6 +76,7 @@ constexpr int kConvRows = 4;  // rows per batch; the next batch loads while this
 template <int K, typename T, int V>
 __global__ void __launch_bounds__(kConvThreads)
     conv1d_silu_prefill_kernel(ConvPrefillArgs a, int tt, int64_t n_cblk, int64_t n_tiles) {
+  grid_dependency_wait();
   using R = RawV<T, V>;
   // block -> (batch, tile, channel block); channel blocks fastest
   int64_t blk = blockIdx.x;
@@ -148,6 +149,8 @@ __global__ void __launch_bounds__(kConvThreads)
 #pragma unroll
     for (int r = 0; r < kConvRows; ++r) cur[r] = nxt[r];
   }
+  // signal late: a long scan that follows should find the SMs evenly free
+  grid_dependents_launch();
 
   if (tile == 0 && a.state_out) {
     // new state = entries T..T+K-1 of [state_0..state_{K-1}, x_0..x_{T-1}];
@@ -206,6 +209,7 @@ constexpr int kStepThreads = 256;
 
 template <int K, typename T>
 __global__ void __launch_bounds__(kStepThreads) conv1d_silu_step_kernel(ConvStepArgs a) {
+  grid_dependency_begin();
   const int64_t i = (int64_t)blockIdx.x * kStepThreads + threadIdx.x;  // b * Di + c
   if (i >= a.B * a.Di) return;
   const int64_t c = (a.B * a.Di < (int64_t(1) << 31)) ? (int64_t)((uint32_t)i % (uint32_t)a.Di) : i % a.Di;
@@ -242,12 +246,10 @@ cudaError_t prefill_launch(const ConvPrefillArgs& a, const DeviceInfo& dev, cuda
   const int64_t blocks = n_cblk * n_tiles * a.B;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   if (vec)
-    conv1d_silu_prefill_kernel<K, T, 4>
-        <<<(unsigned)blocks, kConvThreads, 0, stream>>>(a, (int)tt, n_cblk, n_tiles);
-  else
-    conv1d_silu_prefill_kernel<K, T, 1>
-        <<<(unsigned)blocks, kConvThreads, 0, stream>>>(a, (int)tt, n_cblk, n_tiles);
-  return cudaGetLastError();
+    return launch_pdl(false, conv1d_silu_prefill_kernel<K, T, 4>, dim3((unsigned)blocks), dim3(kConvThreads), 0,
+                      stream, a, (int)tt, n_cblk, n_tiles);
+  return launch_pdl(false, conv1d_silu_prefill_kernel<K, T, 1>, dim3((unsigned)blocks), dim3(kConvThreads), 0,
+                    stream, a, (int)tt, n_cblk, n_tiles);
 }
 
 template <int K, typename T>
@@ -255,8 +257,7 @@ cudaError_t step_launch(const ConvStepArgs& a, cudaStream_t stream) {
   const int64_t n = a.B * a.Di;
   const int64_t blocks = (n + kStepThreads - 1) / kStepThreads;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  conv1d_silu_step_kernel<K, T><<<(unsigned)blocks, kStepThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(true, conv1d_silu_step_kernel<K, T>, dim3((unsigned)blocks), dim3(kStepThreads), 0, stream, a);
 }
 
 template <typename T>

@@ -20,6 +20,29 @@ namespace mamba {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// --- programmatic dependent launch --------------------------------------------
+// The decode-step kernels are launched with programmatic stream serialisation
+// (the prefill kernels plainly; there both calls below are no-ops).  Every
+// kernel calls grid_dependency_wait() before its first global memory access:
+// that waits until the previous grid on the stream has completed and its
+// memory is visible, so the stream order of the library's calls is kept
+// exactly.  grid_dependents_launch() lets the next kernel on the
+// stream be scheduled once every CTA of this grid has called it (or exited);
+// its CTAs then sit in their own wait while this grid finishes, placed on
+// whichever SMs have room.  The decode-step kernels signal at entry (the next
+// layer's grid has the same shape, and its launch and CTA set-up overlap this
+// grid's tail).  The prefill kernels signal after their main loop: a long
+// one-wave scan launched early would be placed unevenly over SMs still busy
+// with the previous grid and keep that imbalance for its whole run.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_begin() {
+  grid_dependents_launch();
+  grid_dependency_wait();
+}
+
 // --- single MUFU instructions (PTX), flush-to-zero ---------------------------
 __device__ __forceinline__ float ex2_approx(float x) {
   float r;

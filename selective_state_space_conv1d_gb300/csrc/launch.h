@@ -8,6 +8,27 @@
 
 namespace mamba {
 
+// Launches `kernel` on `stream`; with `pdl`, under programmatic stream
+// serialisation: the kernel may be scheduled while the previous kernel on the
+// stream finishes (every kernel here waits for it with griddepcontrol.wait
+// before touching global memory).  The decode steps use it; the prefill
+// kernels measured slower with it and launch plainly.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Sets the thread-local message returned by mamba_last_error(); returns code.
 int set_last_error(int code, const char* msg);
 

@@ -99,6 +99,7 @@ struct RowS {
 
 template <int N, typename Tin, int MODE, bool GATE>
 __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int act_vec, int bc_vec) {
+  grid_dependency_wait();
   using TL = Tile<Tin>;
   constexpr int P = group_size(N);
   constexpr int NG = N / P;
@@ -310,6 +311,7 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
     }
   }
   cp_async_wait<0>();
+  grid_dependents_launch();  // main loop done: the next grid may be scheduled
 
   if (!active) return;
   if (MODE == kPass1) {
@@ -328,43 +330,31 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
 
 // Chains the parts' aggregates: carry_{j+1} = decay_j * carry_j + end_j, with
 // carry_0 = the state snapshot; carry_{j+1} overwrites end_j.  One thread per
-// 4 consecutive floats of the [B][Di][N] state; the loads of 4 parts are in
-// flight together.
+// state element; the loads of up to kFoldBatch parts are issued before the
+// batch's stores (the stores could alias later loads for the compiler, so
+// without the batching every part would cost an L2 round trip).
+constexpr int kFoldBatch = 16;
 __global__ void __launch_bounds__(128) scan_fold_kernel(float* ws, int64_t BDN, int parts) {
-  const int64_t i = (int64_t)blockIdx.x * 128 + threadIdx.x;
-  if (i * 4 >= BDN) return;
-  const int64_t q4 = BDN / 4;
-  float4* w4 = reinterpret_cast<float4*>(ws);
-  float4 acc = w4[i];
-  constexpr int kU = 4;  // parts whose loads are issued before any store
-  for (int j0 = 0; j0 < parts - 1; j0 += kU) {
-    float4 p[kU], e[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (j0 + u < parts - 1) {
-        p[u] = w4[q4 * (1 + 2 * (j0 + u)) + i];
-        e[u] = w4[q4 * (2 + 2 * (j0 + u)) + i];
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (j0 + u < parts - 1) {
-        acc = make_float4(fmaf(p[u].x, acc.x, e[u].x), fmaf(p[u].y, acc.y, e[u].y),
-                          fmaf(p[u].z, acc.z, e[u].z), fmaf(p[u].w, acc.w, e[u].w));
-        w4[q4 * (2 + 2 * (j0 + u)) + i] = acc;
-      }
-    }
-  }
-}
-// Same with one float per thread (B*Di*N not a multiple of 4).
-__global__ void __launch_bounds__(128) scan_fold1_kernel(float* ws, int64_t BDN, int parts) {
+  grid_dependency_begin();
   const int64_t i = (int64_t)blockIdx.x * 128 + threadIdx.x;
   if (i >= BDN) return;
   float acc = ws[i];
-#pragma unroll 4
-  for (int j = 0; j < parts - 1; ++j) {
-    acc = fmaf(ws[BDN * (1 + 2 * j) + i], acc, ws[BDN * (2 + 2 * j) + i]);
-    ws[BDN * (2 + 2 * j) + i] = acc;
+  for (int j0 = 0; j0 < parts - 1; j0 += kFoldBatch) {
+    float p[kFoldBatch], e[kFoldBatch];
+#pragma unroll
+    for (int u = 0; u < kFoldBatch; ++u) {
+      if (j0 + u < parts - 1) {
+        p[u] = ws[BDN * (1 + 2 * (j0 + u)) + i];
+        e[u] = ws[BDN * (2 + 2 * (j0 + u)) + i];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kFoldBatch; ++u) {
+      if (j0 + u < parts - 1) {
+        acc = fmaf(p[u], acc, e[u]);
+        ws[BDN * (2 + 2 * (j0 + u)) + i] = acc;
+      }
+    }
   }
 }
 
@@ -372,8 +362,8 @@ template <int N, typename Tin, int MODE, bool GATE>
 cudaError_t launch_mode(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
   const int64_t blocks = w.n_tiles * a.B * w.grid_parts;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  scan_kernel<N, Tin, MODE, GATE><<<(unsigned)blocks, kLanes, 0, stream>>>(a, w, p.act_vec, p.bc_vec);
-  return cudaGetLastError();
+  return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE>, dim3((unsigned)blocks), dim3(kLanes), 0, stream, a, w,
+                    p.act_vec, p.bc_vec);
 }
 
 template <int N, typename Tin, int MODE>
@@ -397,11 +387,10 @@ cudaError_t launch_n(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream
   cudaError_t e = launch_mode<N, Tin, kPass1, false>(a, w, p, stream);
   if (e != cudaSuccess) return e;
   const int64_t BDN = a.B * a.Di * N;
-  if (BDN % 4 == 0)
-    scan_fold_kernel<<<(unsigned)((BDN / 4 + 127) / 128), 128, 0, stream>>>(ws, BDN, p.parts);
-  else
-    scan_fold1_kernel<<<(unsigned)((BDN + 127) / 128), 128, 0, stream>>>(ws, BDN, p.parts);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((BDN + 127) / 128 > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  e = launch_pdl(false, scan_fold_kernel, dim3((unsigned)((BDN + 127) / 128)), dim3(128), 0, stream, ws, BDN,
+                 p.parts);
+  if (e != cudaSuccess) return e;
   w.grid_parts = p.parts;
   return launch_out<N, Tin, kPass2>(a, w, p, stream);
 }

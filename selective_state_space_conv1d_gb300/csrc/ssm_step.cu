@@ -100,6 +100,7 @@ struct StepArgs {
 template <int N, int K, typename Tin, bool FUSE>
 __global__ void __launch_bounds__(kMaxThreads) step_kernel(StepArgs args, int bt, int64_t n_cblk,
                                                            int state_vec, int bc_vec) {
+  grid_dependency_begin();
   constexpr int P = group_size(N);
   constexpr int NG = N / P;
   constexpr int KK = FUSE ? K : 1;
@@ -222,6 +223,11 @@ struct RingTile {
   static constexpr int kB = kZ + align16(CB * es);               // B row: [N]
   static constexpr int kC = kB + align16(N * es);                // C row: [N]
   static constexpr int kBytes = (kC + align16(N * es) + 127) & ~127;
+  // stages in the ring: as many as fit ring::kRingBytes, 2..kMaxStages
+  static constexpr int kStages = ring::kRingBytes / kBytes < 2 ? 2
+                                 : (ring::kRingBytes / kBytes > ring::kMaxStages ? ring::kMaxStages
+                                                                                 : ring::kRingBytes / kBytes);
+  static constexpr int kSmem = ring::kBarBytes + kStages * kBytes;
 };
 
 __device__ int g_device_faults = 0;  // MAMBA_FAULT_* bits, set by bounded waits that gave up
@@ -244,8 +250,9 @@ __device__ __forceinline__ void store_group_cs(float* p, const float (&o)[P]) {
 // [n_tiles * i / grid, n_tiles * (i + 1) / grid), so consecutive tiles of a CTA
 // share a channel block and its parameters stay in registers.
 template <int N, int K, typename Tin, bool FUSE>
-__global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args, int stages, int64_t n_tiles) {
+__global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args, int64_t n_tiles) {
   using L = RingTile<N, K, Tin, FUSE>;
+  constexpr int stages = L::kStages;
   constexpr int P = L::P, NG = L::NG, CB = L::CB, es = L::es;
   constexpr int KK = FUSE ? K : 1;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -266,6 +273,7 @@ __global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args
     }
     mbar_fence_init();
   }
+  grid_dependency_begin();
   __syncthreads();
 
   if (warp == ring::kConsumerWarps) {
@@ -278,13 +286,14 @@ __global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args
     const char* CM = reinterpret_cast<const char*>(a.Cm);
     const uint32_t ring0 = bars + ring::kBarBytes;
     int issued = 0;
-    for (int i = 0; i < n_my; ++i) {
-      const int s = i % stages;
-      if (i >= stages && !mbar_wait(empty(s), ((i / stages) - 1) & 1, ring::kWaitLimit)) {
+    int64_t cblk = t_begin / Bsz, b = t_begin - cblk * Bsz;  // walked, not divided, per tile
+    int s = 0;
+    uint32_t phase = 0;  // parity of this pass over the ring
+    for (int i = 0; i < n_my; ++i, b = (b + 1 == Bsz) ? (++cblk, 0) : b + 1) {
+      if (i >= stages && !mbar_wait(empty(s), phase ^ 1u, ring::kWaitLimit)) {
         flag_fault(MAMBA_FAULT_RING_WAIT);
         break;
       }
-      const int64_t tile = t_begin + i, cblk = tile / Bsz, b = tile - cblk * Bsz;
       const int64_t c0 = cblk * CB;
       const uint32_t nch = (uint32_t)(Di - c0 < CB ? Di - c0 : CB);
       const int64_t row = b * Di + c0;
@@ -300,6 +309,10 @@ __global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args
       bulk_g2s(st + L::kB, BM + b * N * es, N * es, fb);
       bulk_g2s(st + L::kC, CM + b * N * es, N * es, fb);
       issued = i + 1;
+      if (++s == stages) {
+        s = 0;
+        phase ^= 1u;
+      }
     }
     // every issued copy lands before this thread leaves
     for (int i = issued > stages ? issued - stages : 0; i < issued; ++i)
@@ -312,8 +325,10 @@ __global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args
   const int cl = threadIdx.x / NG;
   int64_t cur_cblk = -1;
   float a2[P], w[KK], dtb = 0.0f, Dc = 0.0f, cb = 0.0f;
-  for (int i = 0; i < n_my; ++i) {
-    const int64_t tile = t_begin + i, cblk = tile / Bsz, b = tile - cblk * Bsz;
+  int64_t cblk = t_begin / Bsz, b = t_begin - cblk * Bsz;  // walked, not divided, per tile
+  int s = 0;
+  uint32_t phase = 0;
+  for (int i = 0; i < n_my; ++i, b = (b + 1 == Bsz) ? (++cblk, 0) : b + 1, s = (s + 1 == stages) ? (phase ^= 1u, 0) : s + 1) {
     const int64_t c = cblk * CB + cl;
     const bool valid = c < Di;
     if (cblk != cur_cblk) {  // per-channel parameters (L2), loaded while the stage lands
@@ -330,8 +345,7 @@ __global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args
         cb = args.conv_b ? args.conv_b[cc] : 0.0f;
       }
     }
-    const int s = i % stages;
-    if (!__all_sync(0xffffffffu, mbar_wait(full(s), (i / stages) & 1, ring::kWaitLimit))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(full(s), phase, ring::kWaitLimit))) {
       if (lane == 0) flag_fault(MAMBA_FAULT_RING_WAIT);
       break;
     }
@@ -384,10 +398,7 @@ bool ring_eligible(const StepArgs& a, bool fuse) {
 template <int N, int K, typename Tin, bool FUSE>
 cudaError_t launch_ring(const StepArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   using L = RingTile<N, K, Tin, FUSE>;
-  constexpr int kStages =
-      ring::kRingBytes / L::kBytes < 2 ? 2
-      : (ring::kRingBytes / L::kBytes > ring::kMaxStages ? ring::kMaxStages : ring::kRingBytes / L::kBytes);
-  constexpr int kSmem = ring::kBarBytes + kStages * L::kBytes;
+  constexpr int kSmem = L::kSmem;
   static std::atomic<int> occ_cache[64];
   int dev_id = 0;
   cudaError_t e = cudaGetDevice(&dev_id);
@@ -409,8 +420,8 @@ cudaError_t launch_ring(const StepArgs& a, const DeviceInfo& dev, cudaStream_t s
   const int64_t n_tiles = n_cblk * a.s.B;
   const int64_t resident = (int64_t)dev.sm_count * occ;
   const int64_t grid = n_tiles < resident ? n_tiles : resident;
-  ring_step_kernel<N, K, Tin, FUSE><<<(unsigned)grid, ring::kThreads, kSmem, stream>>>(a, kStages, n_tiles);
-  return cudaGetLastError();
+  return launch_pdl(true, ring_step_kernel<N, K, Tin, FUSE>, dim3((unsigned)grid), dim3(ring::kThreads), kSmem,
+                    stream, a, n_tiles);
 }
 
 template <int N, int K, typename Tin, bool FUSE>
@@ -430,8 +441,8 @@ cudaError_t launch_nk(const StepArgs& a, cudaStream_t stream) {
   if (FUSE) state_vec = state_vec && (reinterpret_cast<uintptr_t>(a.conv_state) & 15) == 0;
   const int bc_vec = ((reinterpret_cast<uintptr_t>(a.s.Bm) | reinterpret_cast<uintptr_t>(a.s.Cm)) & 15) == 0 &&
                      (N * es) % 16 == 0;
-  step_kernel<N, K, Tin, FUSE><<<(unsigned)blocks, threads, 0, stream>>>(a, bt, n_cblk, state_vec, bc_vec);
-  return cudaGetLastError();
+  return launch_pdl(true, step_kernel<N, K, Tin, FUSE>, dim3((unsigned)blocks), dim3(threads), 0, stream, a, bt,
+                    n_cblk, state_vec, bc_vec);
 }
 
 template <int N, int K, typename Tin, bool FUSE>

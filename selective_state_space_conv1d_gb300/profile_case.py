@@ -1,0 +1,77 @@
+"""Run one kernel of the mixer core on one synthetic shape, a few times.
+
+A small, self-contained target for a profiler (for example
+`ncu -k regex:scan_kernel -s 1 -c 1 python -m selective_state_space_conv1d_gb300.profile_case --what scan ...`):
+it builds its inputs on the device with torch's RNG, calls the C ABI `--reps`
+times, then times one more call with CUDA events and prints it.
+
+  --what scan      selective-scan prefill  [B, T, Di] inputs, d_state N
+  --what conv      conv1d + SiLU prefill    [B, T, Di], d_conv 4
+  --what step      T=1 SSM step on layer 1 of an [L][B][Di][N] state
+  --what mixer     fused conv step + SSM step on layer 1
+  --what convstep  T=1 conv step on layer 1 of an [L][B][Di][4] state
+"""
+import argparse
+
+import torch
+
+from . import _binding as m
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--what", default="scan", choices=("scan", "conv", "step", "mixer", "convstep"))
+    ap.add_argument("--B", type=int, default=1)
+    ap.add_argument("--T", type=int, default=2048)
+    ap.add_argument("--Di", type=int, default=1536)
+    ap.add_argument("--N", type=int, default=16)
+    ap.add_argument("--L", type=int, default=24)
+    ap.add_argument("--dtype", default="f32", choices=("f32", "bf16"))
+    ap.add_argument("--reps", type=int, default=3)
+    a = ap.parse_args(argv)
+    td = torch.float32 if a.dtype == "f32" else torch.bfloat16
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1)
+    r = lambda s, std=1.0: (torch.randn(s, generator=g, device="cuda") * std).to(td)
+    A = torch.log(torch.arange(1, a.N + 1, device="cuda", dtype=torch.float32)).repeat(a.Di, 1).contiguous()
+    D = torch.ones(a.Di, device="cuda")
+    dtb = torch.full((a.Di,), -4.0, device="cuda")
+    w = torch.rand((a.Di, 4), generator=g, device="cuda") - 0.5
+    m.load()
+    if a.what in ("scan", "conv"):
+        sh = (a.B, a.T, a.Di)
+        x, u, dt, z = r(sh), r(sh), r(sh, 0.1), r(sh)
+        Bm, Cm = r((a.B, a.T, a.N)), r((a.B, a.T, a.N))
+        y = torch.empty(sh, device="cuda")
+        uo = torch.empty_like(x)
+        so = torch.empty((a.B, a.Di, a.N), device="cuda")
+        co = torch.empty((a.B, a.Di, 4), device="cuda")
+        if a.what == "conv":
+            f = lambda: m.mamba_conv1d_silu_prefill(uo, x, w, None, None, co)
+        else:
+            f = lambda: m.mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A, D, dtb, z, None, so)
+    else:
+        st = torch.randn((a.L, a.B, a.Di, a.N if a.what in ("step", "mixer") else 4), generator=g, device="cuda")
+        x, u, dt, z = r((a.B, a.Di)), r((a.B, a.Di)), r((a.B, a.Di), 0.1), r((a.B, a.Di))
+        Bm, Cm = r((a.B, a.N)), r((a.B, a.N))
+        y = torch.empty((a.B, a.Di), device="cuda", dtype=td)
+        if a.what == "step":
+            f = lambda: m.mamba_ssm_step_batched(y, u, dt, Bm, Cm, st, 1, A, D, dtb, z)
+        elif a.what == "mixer":
+            cs = torch.randn((a.L, a.B, a.Di, 4), generator=g, device="cuda")
+            f = lambda: m.mamba_mixer_step_batched(y, x, dt, Bm, Cm, cs, st, 1, w, A, None, D, dtb, z)
+        else:
+            f = lambda: m.mamba_conv1d_silu_step(y, x, st, 1, w, None)
+    for _ in range(a.reps):
+        f()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    f()
+    e1.record()
+    torch.cuda.synchronize()
+    print(f"{a.what} B={a.B} T={a.T} Di={a.Di} N={a.N} {a.dtype}: {e0.elapsed_time(e1) * 1e3:.1f} us", flush=True)
+
+
+if __name__ == "__main__":
+    main()
