@@ -432,8 +432,30 @@ def run_decode(torch, m, synth, device, peak, peak_src, n_steps=256):
         del g
         return a.elapsed_time(b) / (reps * n_steps)
 
+    def time_decode_driver():
+        # the library's graph-captured decode driver: 256 steps x 24 layers of
+        # fused mixer steps recorded once, replayed with one call
+        io = [[{"y": y[l], "x": x[s, l], "dt": dt[s, l], "z": z[s, l], "Bm": Bm[s, l], "Cm": Cm[s, l]}
+               for l in range(L)] for s in range(n_steps)]
+        for s in range(3):  # warm-up steps
+            for l in range(L):
+                layer_step_fused(s, l)
+        torch.cuda.synchronize()
+        with m.DecodeGraph(params, io, conv, ssm) as g:
+            g.launch()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            reps = 4
+            a.record()
+            for _ in range(reps):
+                g.launch()
+            b.record()
+            torch.cuda.synchronize()
+            kernels = g.kernels
+        return a.elapsed_time(b) / (reps * n_steps), kernels
+
     ms_sep = time_decode(layer_step)
-    ms_fused = time_decode(layer_step_fused)
+    ms_fused, driver_kernels = time_decode_driver()
     # per-kernel durations: graphs of one kernel kind over 4 steps x 24 layers
     conv_calls = [lambda s=s, l=l: m.mamba_conv1d_silu_step(u[l], x[s, l], conv, l, params[l]["conv_w"],
                                                              params[l]["conv_b"])
@@ -457,11 +479,14 @@ def run_decode(torch, m, synth, device, peak, peak_src, n_steps=256):
         "algorithmic_bytes_per_step": int(L * fused_bytes),
         "hbm_gbs_per_step": round(L * fused_bytes / (ms_fused * 1e-3) / 1e9, 1),
         "step": "fused mixer step (conv1d+SiLU step then SSM step, 1 launch per layer)",
+        "driver": f"mamba_decode_graph: {n_steps} steps x {L} layers recorded once ({driver_kernels} kernels), "
+                  "replayed per call",
         "separate_calls": {"value": round(1e3 / ms_sep, 2), "unit": "steps/s", "ms_per_step": round(ms_sep, 5),
                            "hbm_gbs_per_step": round(L * (step_bytes + conv_bytes) / (ms_sep * 1e-3) / 1e9, 1),
                            "step": "conv1d step + SSM step, 2 launches per layer"},
         "config": {"n_layers": L, "batch": Bsz, "d_inner": Di, "d_state": N, "d_conv": K,
-                   "steps_per_replay": n_steps, "launch": "CUDA graph of 256 steps x 24 layers",
+                   "steps_per_replay": n_steps,
+                   "launch": "library decode graph (fused); CUDA graph of 256 steps x 24 layers (separate calls)",
                    "l2": f"state {L * rows * (N + K) * 4 / 1e6:.0f} MB > L2"},
         "gpu_launches_per_step": L, "separate_calls_launches_per_step": 2 * L,
     }

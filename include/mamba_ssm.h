@@ -207,6 +207,59 @@ MAMBA_API int mamba_mixer_step_batched(void* y, int y_dtype, const void* x, cons
                                        int64_t N, void* stream);
 
 /*
+ * Graph-captured decode driver.  (inference.rs `capture_graph` / `step`: after
+ * a warm-up step the engine records its whole T=1 step chain into a CUDA graph
+ * once and replays it every token, cutting the launch overhead from ~50 us to
+ * ~5 us per step; the device pointers are fixed at capture, and the state and
+ * scratch buffers must be the ones the graph was captured with.)
+ *
+ * mamba_decode_graph_create records n_steps x n_layers fused mixer steps
+ * (mamba_mixer_step_batched), step-major: entry io[s * n_layers + l] is step s
+ * of layer l, with the parameters params[l] and slab l of both states.  Every
+ * step is validated exactly as mamba_mixer_step_batched validates it, before
+ * the graph is instantiated; on an error nothing is created and *out is NULL.
+ * mamba_decode_graph_launch replays the whole recording on `stream`: it reads
+ * and writes the buffers named at creation (write new inputs into the same
+ * buffers between launches), and the states advance by n_steps tokens.
+ *
+ *   params  [n_layers] per-layer parameters (shapes as mamba_mixer_step_batched)
+ *   io      [n_steps * n_layers] per-step buffers: y (out), x, dt, z (or NULL), Bm, Cm
+ *   conv_state [n_layers][B][Di][K] f32, ssm_state [n_layers][B][Di][N] f32
+ * Ownership: the graph objects are the library's (host side and driver
+ * resources; no device memory is allocated) until mamba_decode_graph_destroy;
+ * every buffer stays the caller's and must outlive the graph.  Launches of one
+ * graph on two streams at once race on the states.
+ */
+typedef struct MambaMixerLayerParams {
+  const float* conv_w;  /* [Di][K] */
+  const float* conv_b;  /* [Di] or NULL */
+  const float* A_log;   /* [Di][N] */
+  const float* D;       /* [Di] or NULL */
+  const float* dt_bias; /* [Di] or NULL */
+} MambaMixerLayerParams;
+
+typedef struct MambaMixerStepIO {
+  void* y;        /* [B][Di], y_dtype (out) */
+  const void* x;  /* [B][Di], act_dtype */
+  const void* dt; /* [B][Di], act_dtype */
+  const void* z;  /* [B][Di], act_dtype, or NULL (no gate) */
+  const void* Bm; /* [B][N], act_dtype */
+  const void* Cm; /* [B][N], act_dtype */
+} MambaMixerStepIO;
+
+typedef struct MambaDecodeGraph MambaDecodeGraph;
+
+MAMBA_API int mamba_decode_graph_create(MambaDecodeGraph** out, const MambaMixerLayerParams* params,
+                                        const MambaMixerStepIO* io, int64_t n_steps, int64_t n_layers,
+                                        int y_dtype, int act_dtype, float* conv_state, float* ssm_state,
+                                        int64_t B, int64_t Di, int64_t K, int64_t N);
+MAMBA_API int mamba_decode_graph_launch(MambaDecodeGraph* graph, void* stream);
+/* Kernel launches one replay makes (n_steps * n_layers), or a negative error code. */
+MAMBA_API int64_t mamba_decode_graph_kernels(const MambaDecodeGraph* graph);
+/* Releases the graph; NULL is accepted.  Not while a launch of it is still running. */
+MAMBA_API int mamba_decode_graph_destroy(MambaDecodeGraph* graph);
+
+/*
  * mamba_selective_scan_prefill_noalloc - the selective-scan prefill for callers
  * that cannot allocate device memory.  (No counterpart in the mamba-rs pages:
  * it is an addition of this library.)

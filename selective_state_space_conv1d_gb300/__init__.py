@@ -6,11 +6,13 @@ Four C-ABI entry points (include/mamba_ssm.h), each a hand-written CUDA kernel:
   mamba_selective_scan_prefill  selective scan + SiLU(z) gate, state in/out
   mamba_ssm_step_batched        T=1 SSM step on a [n_layers][B*Di*N] state
   mamba_mixer_step_batched      both T=1 steps fused in one kernel
+  mamba_decode_graph_*          n_steps x n_layers fused steps recorded as one CUDA graph
 This package is the thin Python binding (argument marshalling over ctypes);
 `synth` holds the seeded synthetic inputs used by the tests and the benchmark.
 """
 from ._binding import (  # noqa: F401
     ABI_SYMBOLS,
+    DecodeGraph,
     LIB_PATH,
     MAMBA_BF16,
     MAMBA_ERR_CUDA,

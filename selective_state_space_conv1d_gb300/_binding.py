@@ -33,6 +33,10 @@ ABI_SYMBOLS = (
     "mamba_selective_scan_prefill_noalloc",
     "mamba_ssm_step_batched",
     "mamba_mixer_step_batched",
+    "mamba_decode_graph_create",
+    "mamba_decode_graph_launch",
+    "mamba_decode_graph_kernels",
+    "mamba_decode_graph_destroy",
     "mamba_device_faults",
     "mamba_last_error",
     "mamba_version",
@@ -78,6 +82,15 @@ def load(path: str | None = None):
         for f in ("mamba_mixer_step_batched", "mamba_conv1d_silu_prefill", "mamba_conv1d_silu_step",
                   "mamba_selective_scan_prefill", "mamba_ssm_step_batched"):
             getattr(lib, f).restype = ctypes.c_int
+        lib.mamba_decode_graph_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i64, i32, i32, vp, vp,
+                                                  i64, i64, i64, i64]
+        lib.mamba_decode_graph_create.restype = ctypes.c_int
+        lib.mamba_decode_graph_launch.argtypes = [vp, vp]
+        lib.mamba_decode_graph_launch.restype = ctypes.c_int
+        lib.mamba_decode_graph_kernels.argtypes = [vp]
+        lib.mamba_decode_graph_kernels.restype = i64
+        lib.mamba_decode_graph_destroy.argtypes = [vp]
+        lib.mamba_decode_graph_destroy.restype = ctypes.c_int
         lib.mamba_device_faults.argtypes = [i32]
         lib.mamba_device_faults.restype = ctypes.c_int
         lib.mamba_last_error.argtypes = []
@@ -350,3 +363,104 @@ def mamba_mixer_step_batched(y, x, dt, Bm, Cm, conv_state, ssm_state, layer, con
         _ptr(y), _dtype_code(y), _ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _dtype_code(x),
         _ptr(conv_w), _ptr(conv_b), _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(conv_state),
         _ptr(ssm_state), int(layer), ssm_state.shape[0], Bsz, Di, K, N, _stream(stream, x)))
+
+
+class _LayerParams(ctypes.Structure):
+    _fields_ = [("conv_w", ctypes.c_void_p), ("conv_b", ctypes.c_void_p), ("A_log", ctypes.c_void_p),
+                ("D", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p)]
+
+
+class _StepIO(ctypes.Structure):
+    _fields_ = [("y", ctypes.c_void_p), ("x", ctypes.c_void_p), ("dt", ctypes.c_void_p),
+                ("z", ctypes.c_void_p), ("Bm", ctypes.c_void_p), ("Cm", ctypes.c_void_p)]
+
+
+class DecodeGraph:
+    """Graph-captured decode driver over the C ABI (mamba_decode_graph_*).
+
+    params: n_layers dicts with conv_w, A_log and optional conv_b, D, dt_bias.
+    io: n_steps lists of n_layers dicts with y, x, dt, Bm, Cm and optional z
+    (contiguous [B, Di] / [B, N] tensors).  One launch() replays all
+    n_steps x n_layers fused mixer steps on the given (or current) stream,
+    reading and writing exactly these tensors; keep them alive, and write new
+    inputs into them between launches.  Call close() (or use `with`) to free
+    the graph."""
+
+    def __init__(self, params, io, conv_state, ssm_state):
+        lib = load()
+        n_layers, n_steps = len(params), len(io)
+        if n_layers == 0 or n_steps == 0 or any(len(row) != n_layers for row in io):
+            raise ValueError("io must be n_steps lists of n_layers entries, params n_layers entries")
+        x0 = io[0][0]["x"]
+        Bsz, Di = x0.shape
+        N = params[0]["A_log"].shape[1]
+        K = params[0]["conv_w"].shape[1]
+        for st, nm, last in ((conv_state, "conv_state", K), (ssm_state, "ssm_state", N)):
+            if st.dim() != 4 or tuple(st.shape) != (n_layers, Bsz, Di, last) or not st.is_contiguous():
+                raise ValueError(f"{nm} must be a contiguous [{n_layers}, B, Di, {last}] tensor")
+            _f32_param(st, nm)
+        P = (_LayerParams * n_layers)()
+        for l, p in enumerate(params):
+            _f32_param(p["conv_w"], "conv_w", (Di, K))
+            _f32_param(p["A_log"], "A_log", (Di, N))
+            for k in ("conv_b", "D", "dt_bias"):
+                _f32_param(p.get(k), k, (Di,))
+            P[l] = _LayerParams(_ptr(p["conv_w"]), _ptr(p.get("conv_b")), _ptr(p["A_log"]), _ptr(p.get("D")),
+                                _ptr(p.get("dt_bias")))
+        Q = (_StepIO * (n_steps * n_layers))()
+        y_code = _dtype_code(io[0][0]["y"])
+        for s_, row in enumerate(io):
+            for l, q in enumerate(row):
+                for k, shp in (("y", (Bsz, Di)), ("x", (Bsz, Di)), ("dt", (Bsz, Di)), ("z", (Bsz, Di)),
+                               ("Bm", (Bsz, N)), ("Cm", (Bsz, N))):
+                    t = q.get(k)
+                    if t is None:
+                        continue
+                    if tuple(t.shape) != shp or not t.is_contiguous():
+                        raise ValueError(f"io[{s_}][{l}]['{k}'] must be a contiguous {shp} tensor")
+                    if k == "y" and _dtype_code(t) != y_code:
+                        raise ValueError("every y must have the same dtype")
+                    if k != "y" and t.dtype != x0.dtype:
+                        raise ValueError(f"io[{s_}][{l}]['{k}'] must have the dtype of x")
+                Q[s_ * n_layers + l] = _StepIO(_ptr(q["y"]), _ptr(q["x"]), _ptr(q["dt"]), _ptr(q.get("z")),
+                                               _ptr(q["Bm"]), _ptr(q["Cm"]))
+        h = ctypes.c_void_p()
+        _check(lib.mamba_decode_graph_create(ctypes.byref(h), P, Q, n_steps, n_layers, y_code, _dtype_code(x0),
+                                             _ptr(conv_state), _ptr(ssm_state), Bsz, Di, K, N))
+        self._h = h
+        self._device = x0.device
+        self.n_steps, self.n_layers = n_steps, n_layers
+
+    @property
+    def kernels(self) -> int:
+        """Kernel launches one replay makes."""
+        v = load().mamba_decode_graph_kernels(self._h)
+        if v < 0:
+            raise MambaError(int(v), mamba_last_error())
+        return int(v)
+
+    def launch(self, stream=None):
+        if self._h is None:
+            raise ValueError("graph is closed")
+        import torch
+
+        s = torch.cuda.current_stream(self._device).cuda_stream if stream is None else (
+            stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        _check(load().mamba_decode_graph_launch(self._h, s))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            _check(load().mamba_decode_graph_destroy(self._h))
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

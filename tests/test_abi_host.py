@@ -157,3 +157,19 @@ def test_python_binding_raises_when_library_missing(tmp_path):
             _binding.load(str(tmp_path / "nope.so"))
     finally:
         _binding._lib = saved
+
+
+def test_decode_graph_rejects_bad_arguments_on_host(lib):
+    h = ctypes.c_void_p()
+    # out NULL, params / io NULL, no steps or layers: refused before any device call
+    assert lib.mamba_decode_graph_create(None, FAKE, FAKE, 1, 1, 0, 0, FAKE, FAKE, 1, 8, 4, 16) == m.MAMBA_ERR_INVALID_ARG
+    assert lib.mamba_decode_graph_create(ctypes.byref(h), None, FAKE, 1, 1, 0, 0, FAKE, FAKE, 1, 8, 4, 16) \
+        == m.MAMBA_ERR_INVALID_ARG
+    assert h.value is None
+    for n_steps, n_layers in ((0, 1), (1, 0), (-1, 4), (1 << 21, 1)):
+        assert lib.mamba_decode_graph_create(ctypes.byref(h), FAKE, FAKE, n_steps, n_layers, 0, 0, FAKE, FAKE,
+                                             1, 8, 4, 16) == m.MAMBA_ERR_INVALID_ARG
+        assert "n_steps" in m.mamba_last_error()
+    assert lib.mamba_decode_graph_launch(None, None) == m.MAMBA_ERR_INVALID_ARG
+    assert lib.mamba_decode_graph_kernels(None) == m.MAMBA_ERR_INVALID_ARG
+    assert lib.mamba_decode_graph_destroy(None) == m.MAMBA_OK

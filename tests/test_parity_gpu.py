@@ -467,3 +467,60 @@ def test_step_ring_and_direct_paths_agree_bitwise(cuda_lib, N, K, dtype, fused):
         assert torch.equal(ya, yb), f"y differs at step {step}"
         assert torch.equal(ssm_a, ssm_b) and torch.equal(conv_a, conv_b)
     assert m.mamba_device_faults(clear=True) == 0
+
+
+# ------------------------------------------------------ decode graph driver ----
+
+@pytest.mark.parametrize("dtype,gate,Di", [("f32", True, 200), ("bf16", True, 160), ("f32", False, 100)])
+def test_decode_graph_replays_the_direct_calls_bitwise(cuda_lib, dtype, gate, Di):
+    """A recorded n_steps x n_layers decode graph, launched twice, gives the same
+    y and states, bit for bit, as the same fused mixer steps called directly."""
+    m = cuda_lib
+    L, S, Bsz, N, K = 3, 2, 9, 16, 4
+    ps = [_params(SEED + 7, Di, N, K, layer=l) for l in range(L)]
+    pd = [{k: to_dev(v) for k, v in p.items()} for p in ps]
+    conv_h = synth.normal(SEED, "conv_state", (L, Bsz, Di, K), 0.5)
+    ssm_h = synth.normal(SEED, "ssm_state", (L, Bsz, Di, N), 0.5)
+    cg, sg, cd, sd = to_dev(conv_h), to_dev(ssm_h), to_dev(conv_h), to_dev(ssm_h)
+    io = []
+    for s in range(S):
+        row = []
+        for l in range(L):
+            inp = synth.decode_step_inputs(SEED, l, s, Bsz, Di, N, dtype)
+            q = {k: to_dev(inp[k], dtype) for k in ("x", "dt", "B", "C")}
+            row.append({"y": torch.empty((Bsz, Di), device="cuda"), "x": q["x"], "dt": q["dt"],
+                        "z": to_dev(inp["z"], dtype) if gate else None, "Bm": q["B"], "Cm": q["C"]})
+        io.append(row)
+    with m.DecodeGraph(pd, io, cg, sg) as g:
+        assert g.kernels == S * L
+        for rep in range(2):
+            g.launch()
+            torch.cuda.synchronize()
+            ys = {}
+            for s in range(S):
+                for l in range(L):
+                    q = io[s][l]
+                    ys[s, l] = torch.empty((Bsz, Di), device="cuda")
+                    m.mamba_mixer_step_batched(ys[s, l], q["x"], q["dt"], q["Bm"], q["Cm"], cd, sd, l,
+                                               pd[l]["conv_w"], pd[l]["A_log"], pd[l]["conv_b"], pd[l]["D"],
+                                               pd[l]["dt_bias"], q["z"])
+            torch.cuda.synchronize()
+            for (s, l), y in ys.items():
+                assert torch.equal(y, io[s][l]["y"]), f"y differs (launch {rep}, step {s}, layer {l})"
+            assert torch.equal(cg, cd) and torch.equal(sg, sd), f"states differ after launch {rep}"
+    assert m.mamba_device_faults(clear=True) == 0
+
+
+def test_decode_graph_reports_the_failing_step(cuda_lib):
+    m = cuda_lib
+    L, Bsz, Di, N, K = 2, 4, 64, 16, 4
+    pd = [{k: to_dev(v) for k, v in _params(SEED, Di, N, K, layer=l).items()} for l in range(L)]
+    conv, ssm = torch.zeros((L, Bsz, Di, K), device="cuda"), torch.zeros((L, Bsz, Di, N), device="cuda")
+    mk = lambda: {"y": torch.empty((Bsz, Di), device="cuda"), "x": torch.zeros((Bsz, Di), device="cuda"),
+                  "dt": torch.zeros((Bsz, Di), device="cuda"), "Bm": torch.zeros((Bsz, N), device="cuda"),
+                  "Cm": torch.zeros((Bsz, N), device="cuda")}
+    io = [[mk(), mk()]]
+    io[0][1]["y"] = io[0][1]["x"]  # output overlapping an input: refused by the step's host checks
+    with pytest.raises(m.MambaError) as ei:
+        m.DecodeGraph(pd, io, conv, ssm)
+    assert ei.value.status == m.MAMBA_ERR_INVALID_ARG and "layer 1" in str(ei.value)
