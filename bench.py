@@ -44,6 +44,7 @@ KERNEL_SOURCES = {
              "selective_state_space_conv1d_gb300/csrc/device_math.cuh"],
 }
 KERNEL_SOURCES["mixer_step"] = KERNEL_SOURCES["step"]
+KERNEL_SOURCES["fused"] = KERNEL_SOURCES["scan"]
 
 
 # ---------------------------------------------------------------- utilities --
@@ -196,6 +197,11 @@ class PrefillSet:
         m.mamba_selective_scan_prefill(self.y, self.u, self.dt, self.B, self.C, self.p["A_log"],
                                        self.p["D"], self.p["dt_bias"], self.z, None, self.ssm_out)
 
+    def fused(self, m):
+        m.mamba_mixer_prefill(self.y, self.x, self.dt, self.B, self.C, self.p["conv_w"], self.p["A_log"],
+                              self.p["conv_b"], self.p["D"], self.p["dt_bias"], self.z, None, self.conv_out,
+                              None, self.ssm_out)
+
     def bytes_per_step(self):
         """Algorithmic HBM bytes of (conv, scan): every input read once, every output written once."""
         es = self.x.element_size()
@@ -208,16 +214,20 @@ class PrefillSet:
         return conv, scan
 
 
-def timed_graph_run(torch, m, sets, n_steps, per_graph, clocks=None, dist=None):
-    """Time n_steps prefill steps (conv then scan) as replays of captured graphs."""
+def timed_graph_run(torch, m, sets, n_steps, per_graph, clocks=None, dist=None, fused=False):
+    """Time n_steps prefill steps (conv then scan, or the fused call) as replays
+    of captured graphs."""
     per_graph = max(1, min(per_graph, n_steps))
 
     def build(nsteps):
         def body():
             for i in range(nsteps):
                 s = sets[i % len(sets)]
-                s.conv(m)
-                s.scan(m)
+                if fused:
+                    s.fused(m)
+                else:
+                    s.conv(m)
+                    s.scan(m)
         return capture(torch, body)
 
     g_main = build(per_graph)
@@ -283,13 +293,13 @@ def mufu_peak_tops(sm_count=GB300_SMS):
     return MUFU_SLOTS_PER_CLK_SM * sm_count * GB300_MAX_SM_MHZ * 1e6 / 1e12
 
 
-def scan_roofline(tc, N, gate, bytes_per_launch, ms, hbm_peak_gbs, peak_src, traffic, sm_count):
+def scan_roofline(tc, N, gate, bytes_per_launch, ms, hbm_peak_gbs, peak_src, traffic, sm_count, conv=False):
     """The scan is bound by MUFU (and FMA) throughput, not HBM: per (token,
     channel) it needs N ex2 for the states, ex2 + lg2 for softplus and, with a
     gate, ex2 + rcp for SiLU (lg2/rcp at half rate count twice): N + 3 (+ 3)
-    ex2-equivalent MUFU slots.  Reported against the MUFU peak, with the HBM
-    view alongside."""
-    slots = tc * (N + 3 + (3 if gate else 0))
+    ex2-equivalent MUFU slots; the fused prefill adds the conv's SiLU (+ 3).
+    Reported against the MUFU peak, with the HBM view alongside."""
+    slots = tc * (N + 3 + (3 if gate else 0) + (3 if conv else 0))
     tops = slots / (ms * 1e-3) / 1e12
     peak = mufu_peak_tops(sm_count)
     gbs = bytes_per_launch / (ms * 1e-3) / 1e9
@@ -329,20 +339,62 @@ def run_prefill(torch, m, synth, wl_index, steps, warmup, device, dist, clocks, 
         sets[i % n_sets].conv(m)
         sets[i % n_sets].scan(m)
     torch.cuda.synchronize()
-    total_ms, ck = timed_graph_run(torch, m, sets, steps, 100, clocks, dist)
     n_k = 40 if set_bytes < 1e9 else 10
     conv_ms = kernel_time(torch, [lambda s=s: s.conv(m) for s in sets], n_k)
     scan_ms = kernel_time(torch, [lambda s=s: s.scan(m) for s in sets], n_k)
+    fused_ms = kernel_time(torch, [lambda s=s: s.fused(m) for s in sets], n_k)
+    # both forms compute the same result bit for bit: the step is the faster one
+    use_fused = fused_ms < conv_ms + scan_ms
+    total_ms, ck = timed_graph_run(torch, m, sets, steps, 100, clocks, dist, fused=use_fused)
+    u_bytes = 2 * first.u.numel() * first.u.element_size()  # the u write + read the fusion drops
     scan_launches = 2 if m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) > 0 else 1
     l2_note = (f"inputs > 3x L2 ({set_bytes / 1e6:.0f} MB per step)" if n_sets == 1 else
                f"rotating {n_sets} resident buffer sets ({n_sets * set_bytes / 1e6:.0f} MB > 3x the "
                f"{l2 / 1e6:.0f} MB L2)")
     return {
         "wl": wl, "sets": sets, "host": host, "params": params, "total_ms": total_ms,
-        "ms_per_step": total_ms / steps, "conv_ms": conv_ms, "scan_ms": scan_ms,
+        "ms_per_step": total_ms / steps, "conv_ms": conv_ms, "scan_ms": scan_ms, "fused_ms": fused_ms,
+        "use_fused": use_fused,
+        "fused_bytes": conv_b + scan_b - u_bytes,
         "scan_launches": scan_launches, "conv_bytes": conv_b, "scan_bytes": scan_b,
         "tokens_per_step": Bsz * T, "clocks": ck, "l2_note": l2_note,
     }
+
+
+def step_desc(res, fused):
+    split = res["scan_launches"] == 2
+    if fused:
+        return ("mamba_mixer_prefill: conv1d+SiLU fused into the selective scan ("
+                + ("T-split: state-only pass, fold, full pass: 3 launches" if split else "1 launch") + ")")
+    return ("mamba_conv1d_silu_prefill then mamba_selective_scan_prefill ("
+            + ("4 launches: conv, state-only pass, fold, full pass" if split else "2 launches") + ")")
+
+
+def launches_per_step(res, fused):
+    return (0 if fused else 1) + (3 if res["scan_launches"] == 2 else 1)
+
+
+def other_form_line(res):
+    """The step in the form the line's value did not use (same result, bit for bit)."""
+    fused = not res["use_fused"]
+    ms = res["fused_ms"] if fused else res["conv_ms"] + res["scan_ms"]
+    b = res["fused_bytes"] if fused else res["conv_bytes"] + res["scan_bytes"]
+    return {"step": step_desc(res, fused), "value": round(res["tokens_per_step"] / (ms * 1e-3), 1),
+            "unit": "tokens/s", "ms_per_step": round(ms, 5), "algorithmic_bytes_per_step": int(b),
+            "hbm_gbs": round(b / (ms * 1e-3) / 1e9, 1), "launches_per_step": launches_per_step(res, fused),
+            "timing": "graphs of back-to-back calls per kernel kind, rotating buffer sets"}
+
+
+def prefill_roofline(res, peak, peak_src, sms):
+    """Roofline of the dominant call of the step the line times: the fused
+    prefill call, or the selective-scan call of the two-call form."""
+    wl = res["wl"]
+    tc = wl.batch * wl.seqlen * wl.d_inner
+    if res["use_fused"]:
+        return scan_roofline(tc, wl.d_state, True, res["fused_bytes"], res["fused_ms"], peak, peak_src,
+                             ncu_traffic("fused", wl.name), sms, conv=True)
+    return scan_roofline(tc, wl.d_state, True, res["scan_bytes"], res["scan_ms"], peak, peak_src,
+                         ncu_traffic("scan", wl.name), sms)
 
 
 def run_e2e(torch, m, res, steps, device):
@@ -361,8 +413,11 @@ def run_e2e(torch, m, res, steps, device):
     def step():
         for k, t in hin.items():
             getattr(s, k).copy_(t, non_blocking=True)
-        s.conv(m)
-        s.scan(m)
+        if res["use_fused"]:
+            s.fused(m)
+        else:
+            s.conv(m)
+            s.scan(m)
         hy.copy_(s.y, non_blocking=True)
         hc.copy_(s.conv_out, non_blocking=True)
         hs.copy_(s.ssm_out, non_blocking=True)
@@ -627,8 +682,7 @@ def main():
     value = world * res["tokens_per_step"] * args.steps / (total_ms * 1e-3)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     wl1 = res["wl"]
-    scan_roof = scan_roofline(wl1.batch * wl1.seqlen * wl1.d_inner, wl1.d_state, True, res["scan_bytes"],
-                              res["scan_ms"], peak, peak_src, ncu_traffic("scan", wl1.name), sms)
+    scan_roof = prefill_roofline(res, peak, peak_src, sms)
     conv_roof = roofline(res["conv_bytes"], res["conv_ms"], peak, peak_src,
                          ncu_traffic("conv", res["wl"].name))
     step_gbs = (res["conv_bytes"] + res["scan_bytes"]) / (ms_step * 1e-3) / 1e9
@@ -641,10 +695,11 @@ def main():
             "workload": r3["wl"].name, "value": round(r3["tokens_per_step"] / (r3["ms_per_step"] * 1e-3), 1),
             "unit": "tokens/s", "ms_per_step": round(r3["ms_per_step"], 5),
             "hbm_gbs_per_step": round((r3["conv_bytes"] + r3["scan_bytes"]) / (r3["ms_per_step"] * 1e-3) / 1e9, 1),
-            "roofline": scan_roofline(8 * 4096 * 5120, 16, True, r3["scan_bytes"], r3["scan_ms"], peak,
-                                      peak_src, ncu_traffic("scan", r3["wl"].name), sms),
+            "step": step_desc(r3, r3["use_fused"]),
+            "roofline": prefill_roofline(r3, peak, peak_src, sms),
             "conv_roofline": roofline(r3["conv_bytes"], r3["conv_ms"], peak, peak_src,
                                       ncu_traffic("conv", r3["wl"].name)),
+            "other_form": other_form_line(r3),
             "config": {"batch": 8, "seq_len": 4096, "d_inner": 5120, "d_state": 16, "d_conv": 4,
                        "storage": "bf16 x/u/dt/z/B/C, f32 y/params/state", "l2": r3["l2_note"],
                        "inputs": "torch device RNG, same distributions"},
@@ -666,17 +721,19 @@ def main():
             "data": "synthetic (seeded Philox inputs with the tiny-mixer distributions)",
             "config": {"workload": wl.name, "batch": wl.batch, "seq_len": wl.seqlen,
                        "d_inner": wl.d_inner, "d_state": wl.d_state, "d_conv": wl.d_conv,
-                       "step": "conv1d+SiLU prefill then selective-scan prefill (2 launches)",
+                       "step": step_desc(res, res["use_fused"]),
                        "parallelism": f"replicas x{world}", "l2": res["l2_note"],
                        "launch": "CUDA graph replays of 100 steps"},
             "hbm_gbs_per_step": round(step_gbs, 1),
             "roofline": scan_roof,
-            "roofline_kernel": ("selective-scan prefill call (" + ("T-split: state-only pass, fold, full pass: 3 launches"
-                                 if res["scan_launches"] == 2 else "one sequential launch") + ")"),
+            "roofline_kernel": ("fused conv+scan prefill call" if res["use_fused"] else "selective-scan prefill call")
+                               + (" (T-split: state-only pass, fold, full pass)" if res["scan_launches"] == 2
+                                  else " (one sequential launch)"),
             "conv_roofline": conv_roof,
+            "other_form": other_form_line(res),
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": (1 + (3 if res["scan_launches"] == 2 else 1)) * args.steps,
+            "gpu_launches": launches_per_step(res, res["use_fused"]) * args.steps,
             "clocks": res["clocks"],
             "extra": extra,
         }

@@ -207,6 +207,37 @@ MAMBA_API int mamba_mixer_step_batched(void* y, int y_dtype, const void* x, cons
                                        int64_t N, void* stream);
 
 /*
+ * Fused prefill of the whole mixer core: the conv1d + SiLU prefill and the
+ * selective-scan prefill in one pass, so u is never stored.  (prefill.rs
+ * `prefill_body` runs F4a, conv over all T with fused SiLU, and then F4c/F4d,
+ * softplus and the scan with the gate fused into the y store; here the scan
+ * computes each token's u from x itself.)  The result equals
+ * mamba_conv1d_silu_prefill followed by mamba_selective_scan_prefill on its u
+ * bit for bit: u is rounded to act_dtype in between, as the separate conv
+ * stores it.
+ *
+ *   y [B][T] rows of ld_y, dtype y_dtype (out)
+ *   x, dt, z (or NULL): [B][T] rows of ld_x / ld_dt / ld_z, dtype act_dtype
+ *   Bm, Cm [B][T][N] rows of ld_B / ld_C, dtype act_dtype
+ *   conv_w [Di][K], conv_b [Di] or NULL, A_log [Di][N], D / dt_bias [Di] or NULL: f32
+ *   conv_state_in / _out [B][Di][K], ssm_state_in / _out [B][Di][N]: f32; an _in
+ *   may be NULL (zero state), an _out NULL (discarded), and each _out may equal
+ *   its _in (in place).
+ *   workspace: as for mamba_selective_scan_prefill (same size query).
+ * d_conv must be 4 (MAMBA_ERR_UNSUPPORTED otherwise: use the two calls).
+ * Errors: as for the two separate prefills.
+ */
+MAMBA_API int mamba_mixer_prefill(void* y, int64_t ld_y, int y_dtype, const void* x, int64_t ld_x,
+                                  const void* dt, int64_t ld_dt, const void* z, int64_t ld_z,
+                                  const void* Bm, int64_t ld_B, const void* Cm, int64_t ld_C,
+                                  int act_dtype, const float* conv_w, const float* conv_b,
+                                  const float* conv_state_in, float* conv_state_out,
+                                  const float* A_log, const float* D, const float* dt_bias,
+                                  const float* ssm_state_in, float* ssm_state_out, int64_t B,
+                                  int64_t T, int64_t Di, int64_t K, int64_t N, void* workspace,
+                                  int64_t workspace_bytes, void* stream);
+
+/*
  * Graph-captured decode driver.  (inference.rs `capture_graph` / `step`: after
  * a warm-up step the engine records its whole T=1 step chain into a CUDA graph
  * once and replays it every token, cutting the launch overhead from ~50 us to

@@ -6,6 +6,7 @@ Four C-ABI entry points (include/mamba_ssm.h), each a hand-written CUDA kernel:
   mamba_selective_scan_prefill  selective scan + SiLU(z) gate, state in/out
   mamba_ssm_step_batched        T=1 SSM step on a [n_layers][B*Di*N] state
   mamba_mixer_step_batched      both T=1 steps fused in one kernel
+  mamba_mixer_prefill           conv1d + SiLU and the selective scan in one pass
   mamba_decode_graph_*          n_steps x n_layers fused steps recorded as one CUDA graph
 This package is the thin Python binding (argument marshalling over ctypes);
 `synth` holds the seeded synthetic inputs used by the tests and the benchmark.
@@ -28,6 +29,7 @@ from ._binding import (  # noqa: F401
     mamba_conv1d_silu_step,
     mamba_device_faults,
     mamba_last_error,
+    mamba_mixer_prefill,
     mamba_mixer_step_batched,
     mamba_selective_scan_prefill,
     mamba_selective_scan_prefill_noalloc,

@@ -33,6 +33,7 @@ ABI_SYMBOLS = (
     "mamba_selective_scan_prefill_noalloc",
     "mamba_ssm_step_batched",
     "mamba_mixer_step_batched",
+    "mamba_mixer_prefill",
     "mamba_decode_graph_create",
     "mamba_decode_graph_launch",
     "mamba_decode_graph_kernels",
@@ -82,6 +83,9 @@ def load(path: str | None = None):
         for f in ("mamba_mixer_step_batched", "mamba_conv1d_silu_prefill", "mamba_conv1d_silu_step",
                   "mamba_selective_scan_prefill", "mamba_ssm_step_batched"):
             getattr(lib, f).restype = ctypes.c_int
+        lib.mamba_mixer_prefill.argtypes = ([vp, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32]
+                                            + [vp] * 9 + [i64, i64, i64, i64, i64, vp, i64, vp])
+        lib.mamba_mixer_prefill.restype = ctypes.c_int
         lib.mamba_decode_graph_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i64, i32, i32, vp, vp,
                                                   i64, i64, i64, i64]
         lib.mamba_decode_graph_create.restype = ctypes.c_int
@@ -282,6 +286,55 @@ def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, 
         _ptr(Bm), _rows_ld(Bm, "Bm"), _ptr(Cm), _rows_ld(Cm, "Cm"), _dtype_code(u),
         _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
         Bsz, T, Di, N, ws_ptr, ws_bytes, _stream(stream, u)))
+
+
+def mamba_mixer_prefill(y, x, dt, Bm, Cm, conv_w, A_log, conv_b=None, D=None, dt_bias=None, z=None,
+                        conv_state_in=None, conv_state_out=None, ssm_state_in=None, ssm_state_out=None, *,
+                        workspace=None, stream=None):
+    """Fused conv1d + SiLU and selective-scan prefill (u never stored).
+
+    y, x, dt, z: [B, T, Di] (row-strided views allowed); Bm, Cm: [B, T, N];
+    conv_w: [Di, 4]; A_log: [Di, N]; conv_b, D, dt_bias: [Di]; conv states
+    [B, Di, 4] and ssm states [B, Di, N], f32.  workspace: as for
+    mamba_selective_scan_prefill.  Equals mamba_conv1d_silu_prefill followed by
+    mamba_selective_scan_prefill, bit for bit."""
+    Bsz, T, Di = x.shape
+    N = A_log.shape[1]
+    K = conv_w.shape[1]
+    _f32_param(conv_w, "conv_w", (Di, K))
+    _f32_param(conv_b, "conv_b", (Di,))
+    _f32_param(A_log, "A_log", (Di, N))
+    _f32_param(D, "D", (Di,))
+    _f32_param(dt_bias, "dt_bias", (Di,))
+    for t, nm in ((conv_state_in, "conv_state_in"), (conv_state_out, "conv_state_out")):
+        _f32_param(t, nm, (Bsz, Di, K))
+    for t, nm in ((ssm_state_in, "ssm_state_in"), (ssm_state_out, "ssm_state_out")):
+        _f32_param(t, nm, (Bsz, Di, N))
+    for t, nm in ((dt, "dt"), (z, "z"), (Bm, "Bm"), (Cm, "Cm")):
+        if t is not None and t.dtype != x.dtype:
+            raise ValueError(f"{nm} must have the dtype of x")
+    for t, nm in ((y, "y"), (dt, "dt"), (z, "z")):
+        if t is not None and tuple(t.shape) != (Bsz, T, Di):
+            raise ValueError(f"{nm} must be [B, T, Di]")
+    for t, nm in ((Bm, "Bm"), (Cm, "Cm")):
+        if tuple(t.shape) != (Bsz, T, N):
+            raise ValueError(f"{nm} must be [B, T, N]")
+    if workspace is None:
+        need = mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
+        ws = _workspace(x.device, need) if need > 0 else None
+    elif workspace is False:
+        ws = None
+    else:
+        ws = workspace
+    ws_ptr = ws.data_ptr() if ws is not None else None
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().mamba_mixer_prefill(
+        _ptr(y), _rows_ld(y, "y"), _dtype_code(y), _ptr(x), _rows_ld(x, "x"),
+        _ptr(dt), _rows_ld(dt, "dt"), _ptr(z), _rows_ld(z, "z") if z is not None else 0,
+        _ptr(Bm), _rows_ld(Bm, "Bm"), _ptr(Cm), _rows_ld(Cm, "Cm"), _dtype_code(x),
+        _ptr(conv_w), _ptr(conv_b), _ptr(conv_state_in), _ptr(conv_state_out),
+        _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
+        Bsz, T, Di, K, N, ws_ptr, ws_bytes, _stream(stream, x)))
 
 
 def mamba_ssm_step_batched(y, u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt_bias=None,

@@ -317,6 +317,89 @@ int mamba_selective_scan_prefill(void* y, int64_t ld_y, int y_dtype, const void*
   return ok();
 }
 
+int mamba_mixer_prefill(void* y, int64_t ld_y, int y_dtype, const void* x, int64_t ld_x, const void* dt,
+                        int64_t ld_dt, const void* z, int64_t ld_z, const void* Bm, int64_t ld_B, const void* Cm,
+                        int64_t ld_C, int act_dtype, const float* conv_w, const float* conv_b,
+                        const float* conv_state_in, float* conv_state_out, const float* A_log, const float* D,
+                        const float* dt_bias, const float* ssm_state_in, float* ssm_state_out, int64_t B,
+                        int64_t T, int64_t Di, int64_t K, int64_t N, void* workspace, int64_t workspace_bytes,
+                        void* stream) {
+  int rc;
+  if ((rc = check_dtype("y_dtype", y_dtype)) || (rc = check_dtype("act_dtype", act_dtype))) return rc;
+  if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld T=%lld Di=%lld)", (long long)B, (long long)T, (long long)Di);
+  if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
+  if (K != 4)
+    return fail(MAMBA_ERR_UNSUPPORTED, "the fused prefill supports d_conv=4 (got %lld); call "
+                "mamba_conv1d_silu_prefill and mamba_selective_scan_prefill instead", (long long)K);
+  if (workspace_bytes < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative workspace_bytes");
+  if (!workspace) workspace_bytes = 0;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15))
+    return fail(MAMBA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (B == 0 || Di == 0) return ok();
+  if (!sizes_ok(B, T, Di) || !sizes_ok(B, T, N) || !sizes_ok(B, Di, N) || !sizes_ok(B, Di, K))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!A_log || !conv_w) return fail(MAMBA_ERR_INVALID_ARG, "A_log and conv_w must not be NULL");
+  if (T > 0) {
+    if (!y || !x || !dt || !Bm || !Cm) return fail(MAMBA_ERR_INVALID_ARG, "y, x, dt, Bm and Cm must not be NULL");
+    if (ld_y < Di || ld_x < Di || ld_dt < Di || (z && ld_z < Di))
+      return fail(MAMBA_ERR_INVALID_ARG, "an activation stride is smaller than Di=%lld", (long long)Di);
+    if (ld_B < N || ld_C < N) return fail(MAMBA_ERR_INVALID_ARG, "ld_B / ld_C smaller than d_state=%lld", (long long)N);
+  }
+  const int es = es_of(act_dtype), esy = es_of(y_dtype);
+  int64_t by = 0, bx = 0, bdt = 0, bz = 0, bB = 0, bC = 0, bA = 0, bv = 0, bst = 0, bcs = 0, bw = 0;
+  if (!span_bytes(B * Di, N, N, 4, &bst) || !span_bytes(Di, N, N, 4, &bA) || !span_bytes(1, Di, Di, 4, &bv) ||
+      !span_bytes(B * Di, K, K, 4, &bcs) || !span_bytes(Di, K, K, 4, &bw))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (T > 0 &&
+      (!span_bytes(B * T, Di, ld_y, esy, &by) || !span_bytes(B * T, Di, ld_x, es, &bx) ||
+       !span_bytes(B * T, Di, ld_dt, es, &bdt) || (z && !span_bytes(B * T, Di, ld_z, es, &bz)) ||
+       !span_bytes(B * T, N, ld_B, es, &bB) || !span_bytes(B * T, N, ld_C, es, &bC)))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  const bool ssm_inplace = ssm_state_out && ssm_state_out == ssm_state_in;
+  const bool conv_inplace = conv_state_out && conv_state_out == conv_state_in;
+  const Range sin = range_of("ssm_state_in", ssm_state_in, bst);
+  const Range cin = range_of("conv_state_in", conv_state_in, bcs);
+  const Range none = range_of("", nullptr, 0);
+  Range ins[] = {range_of("x", x, bx), range_of("dt", dt, bdt), range_of("z", z, bz),
+                 range_of("Bm", Bm, bB), range_of("Cm", Cm, bC), range_of("A_log", A_log, bA),
+                 range_of("D", D, bv), range_of("dt_bias", dt_bias, bv), range_of("conv_w", conv_w, bw),
+                 range_of("conv_b", conv_b, bv), sin, cin};
+  Range outs[] = {range_of("y", y, by), range_of("ssm_state_out", ssm_state_out, bst),
+                  range_of("conv_state_out", conv_state_out, bcs), range_of("workspace", workspace, workspace_bytes)};
+  if ((rc = check_pointers(ins, 12, dev_id)) || (rc = check_pointers(outs, 4, dev_id))) return rc;
+  // a state may be updated in place; nothing else may touch it
+  if (ssm_inplace) ins[10] = none;
+  if (conv_inplace) ins[11] = none;
+  if ((rc = check_overlaps(outs, 4, ins, 12))) return rc;
+  for (int o = 0; o < 4; ++o) {
+    if (ssm_inplace && o != 1 && overlaps(outs[o], sin))
+      return fail(MAMBA_ERR_INVALID_ARG, "%s overlaps ssm_state_in", outs[o].name);
+    if (conv_inplace && o != 2 && overlaps(outs[o], cin))
+      return fail(MAMBA_ERR_INVALID_ARG, "%s overlaps conv_state_in", outs[o].name);
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if ((rc = copy_state(ssm_state_out, ssm_state_in, B * Di * N, s))) return rc;
+    return copy_state(conv_state_out, conv_state_in, B * Di * K, s);
+  }
+  mamba::ScanArgs a{y, ld_y, y_dtype == MAMBA_BF16, x, ld_x, dt, ld_dt, z, ld_z, Bm, ld_B, Cm, ld_C,
+                    act_dtype == MAMBA_BF16, A_log, D, dt_bias, ssm_state_in, ssm_state_out,
+                    B, T, Di, (int)N};
+  a.K = (int)K;
+  a.conv_w = conv_w;
+  a.conv_b = conv_b;
+  a.conv_state_in = conv_state_in;
+  a.conv_state_out = conv_state_out;
+  const mamba::ScanPlan plan = mamba::plan_selective_scan(a, dev, workspace_bytes);
+  cudaError_t e = mamba::launch_selective_scan_prefill(a, plan, static_cast<float*>(workspace), dev, s);
+  if (e != cudaSuccess) return cuda_fail("mixer_prefill launch", e);
+  return ok();
+}
+
 int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N) {
   if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size");
   if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);

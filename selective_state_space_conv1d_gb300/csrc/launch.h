@@ -94,6 +94,13 @@ struct ScanArgs {
   float* state_out;       // may be null, may equal state_in
   int64_t B, T, Di;
   int N;
+  // fused conv1d + SiLU (K > 0): u / ld_u then hold x, and u = SiLU(conv(x)) is
+  // computed in the scan, rounded to the storage dtype as the conv kernel stores it
+  int K = 0;
+  const float* conv_w = nullptr;          // [Di][K]
+  const float* conv_b = nullptr;          // [Di] or null
+  const float* conv_state_in = nullptr;   // [B][Di][K] or null (zero)
+  float* conv_state_out = nullptr;        // [B][Di][K] or null; may equal conv_state_in
 };
 
 // How a prefill is launched: one sequential pass per channel tile (parts == 1)

@@ -97,7 +97,9 @@ struct RowS {
   float u, delta, du, g;
 };
 
-template <int N, typename Tin, int MODE, bool GATE>
+// KC > 0: the conv1d + SiLU of width KC is fused in; the staged "u" is x, and
+// each lane carries the last KC-1 inputs of its channel from row to row.
+template <int N, typename Tin, int MODE, bool GATE, int KC>
 __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int act_vec, int bc_vec) {
   grid_dependency_wait();
   using TL = Tile<Tin>;
@@ -132,6 +134,25 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
   for (int n = 0; n < N; ++n) a2[n] = a2_from_alog(a.A_log[cc * N + n]);
   const float dtb = a.dt_bias ? a.dt_bias[cc] : 0.0f;
   const float Dc = a.D ? a.D[cc] : 0.0f;
+
+  // ---- fused conv: taps, bias and the window of the KC-1 inputs before t_begin.
+  // Input j of the extended sequence [conv_state_0..conv_state_{KC-1}, x_0, ...]
+  // is conv state slot j for j < KC, else x_{j-KC}; token t sees j = t+1..t+KC.
+  constexpr int KW = KC > 1 ? KC - 1 : 1;
+  float cw[KC > 0 ? KC : 1], cwin[KW];
+  float cbias = 0.0f;
+  const Tin* xin = reinterpret_cast<const Tin*>(a.u);
+  auto conv_input = [&](int64_t j) -> float {
+    if (j < KC) return a.conv_state_in ? a.conv_state_in[(b * Di + cc) * KC + j] : 0.0f;
+    return to_f32(xin[(b * T + j - KC) * a.ld_u + cc]);
+  };
+  if constexpr (KC > 0) {
+#pragma unroll
+    for (int k = 0; k < KC; ++k) cw[k] = a.conv_w[cc * KC + k];
+    cbias = a.conv_b ? a.conv_b[cc] : 0.0f;
+#pragma unroll
+    for (int k = 0; k < KC - 1; ++k) cwin[k] = conv_input(t_begin + 1 + k);
+  }
 
   // ---- carry-in ----
   float h[N];
@@ -248,6 +269,16 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
     auto prep = [&](int r) {
       RowS s;
       s.u = to_f32(su[r * kLanes + lane]);
+      if constexpr (KC > 0) {  // rows are prepped in order: slide the window
+        float sw[KC];
+#pragma unroll
+        for (int k = 0; k < KC - 1; ++k) sw[k] = cwin[k];
+        sw[KC - 1] = s.u;
+#pragma unroll
+        for (int k = 0; k + 1 < KC - 1; ++k) cwin[k] = cwin[k + 1];
+        if (KC > 1) cwin[KW - 1] = s.u;
+        s.u = to_f32(from_f32<Tin>(silu_f(conv_taps<KC>(cw, sw, cbias))));
+      }
       s.delta = softplus_f(to_f32(sdt[r * kLanes + lane]) + dtb);
       s.du = s.delta * s.u;
       s.g = (MODE != kPass1 && GATE) ? silu_f(to_f32(sz[r * kLanes + lane])) : 1.0f;
@@ -326,6 +357,18 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
 #pragma unroll
     for (int n = 0; n < N; ++n) a.state_out[srow + n] = h[n];
   }
+  if constexpr (KC > 0) {
+    // new conv state = inputs T..T+KC-1 of the extended sequence; written by
+    // part 0 of the final pass, the only reader of conv_state_in in that pass
+    // (every read before any write: in-place safe)
+    if (MODE != kPass1 && part == 0 && a.conv_state_out) {
+      float fin[KC];
+#pragma unroll
+      for (int k = 0; k < KC; ++k) fin[k] = conv_input(T + k);
+#pragma unroll
+      for (int k = 0; k < KC; ++k) a.conv_state_out[(b * Di + cc) * KC + k] = fin[k];
+    }
+  }
 }
 
 // Chains the parts' aggregates: carry_{j+1} = decay_j * carry_j + end_j, with
@@ -362,7 +405,11 @@ template <int N, typename Tin, int MODE, bool GATE>
 cudaError_t launch_mode(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
   const int64_t blocks = w.n_tiles * a.B * w.grid_parts;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE>, dim3((unsigned)blocks), dim3(kLanes), 0, stream, a, w,
+  if (a.K == 4)
+    return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 4>, dim3((unsigned)blocks), dim3(kLanes), 0, stream, a,
+                      w, p.act_vec, p.bc_vec);
+  if (a.K != 0) return cudaErrorInvalidValue;
+  return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 0>, dim3((unsigned)blocks), dim3(kLanes), 0, stream, a, w,
                     p.act_vec, p.bc_vec);
 }
 

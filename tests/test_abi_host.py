@@ -173,3 +173,14 @@ def test_decode_graph_rejects_bad_arguments_on_host(lib):
     assert lib.mamba_decode_graph_launch(None, None) == m.MAMBA_ERR_INVALID_ARG
     assert lib.mamba_decode_graph_kernels(None) == m.MAMBA_ERR_INVALID_ARG
     assert lib.mamba_decode_graph_destroy(None) == m.MAMBA_OK
+
+
+def test_mixer_prefill_refuses_other_d_conv_on_host(lib):
+    for K, code in ((3, m.MAMBA_ERR_UNSUPPORTED), (8, m.MAMBA_ERR_UNSUPPORTED)):
+        rc = lib.mamba_mixer_prefill(FAKE, 64, 0, FAKE, 64, FAKE, 64, None, 0, FAKE, 16, FAKE, 16, 0,
+                                     FAKE, None, None, None, FAKE, None, None, None, None,
+                                     1, 8, 64, K, 16, None, 0, None)
+        assert rc == code and "d_conv=4" in m.mamba_last_error()
+    rc = lib.mamba_mixer_prefill(FAKE, 64, 0, FAKE, 64, FAKE, 64, None, 0, FAKE, 16, FAKE, 16, 7,
+                                 FAKE, None, None, None, FAKE, None, None, None, None, 1, 8, 64, 4, 16, None, 0, None)
+    assert rc == m.MAMBA_ERR_INVALID_ARG

@@ -524,3 +524,80 @@ def test_decode_graph_reports_the_failing_step(cuda_lib):
     with pytest.raises(m.MambaError) as ei:
         m.DecodeGraph(pd, io, conv, ssm)
     assert ei.value.status == m.MAMBA_ERR_INVALID_ARG and "layer 1" in str(ei.value)
+
+
+# ------------------------------------------------------- fused mixer prefill ----
+
+MIXER_PREFILL_CASES = [
+    # (B, T, Di, N, dtype, y_dtype, gate, states, strided x) -- T-split and sequential shapes
+    (1, 2048, 256, 16, "f32", "f32", True, True, False),
+    (1, 1500, 96, 16, "bf16", "f32", True, True, True),
+    (6, 333, 200, 16, "f32", "bf16", False, True, False),
+    (3, 77, 64, 64, "bf16", "f32", True, False, False),
+    (2, 2, 40, 8, "f32", "f32", True, True, False),  # T < K: the new conv state mixes state and x
+    (1, 999, 130, 4, "f32", "f32", True, True, True),
+]
+
+
+@pytest.mark.parametrize("inplace", [False, True])
+@pytest.mark.parametrize("Bsz,T,Di,N,dtype,y_dtype,gate,states,strided", MIXER_PREFILL_CASES)
+def test_mixer_prefill_equals_conv_then_scan_bitwise(cuda_lib, inplace, Bsz, T, Di, N, dtype, y_dtype, gate,
+                                                      states, strided):
+    m = cuda_lib
+    K = 4
+    p = _params(SEED + 11, Di, N, K)
+    pd = {k: to_dev(v) for k, v in p.items()}
+    a = synth.prefill_inputs(SEED + 11, Bsz, T, Di, N, dtype, names=("x", "dt", "z", "B", "C"))
+    if strided:  # x as the first half of an in_proj-like row, z as the second
+        x = strided_copy(a["x"], dtype, 2 * Di)
+        z = strided_copy(a["z"], dtype, 2 * Di, offset=Di) if gate else None
+    else:
+        x = to_dev(a["x"], dtype)
+        z = to_dev(a["z"], dtype) if gate else None
+    dt, Bm, Cm = (to_dev(a[k], dtype) for k in ("dt", "B", "C"))
+    c0 = to_dev(synth.normal(SEED, "conv_state", (Bsz, Di, K), 0.5)) if states else None
+    s0 = to_dev(synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5)) if states else None
+    ytd = torch.bfloat16 if y_dtype == "bf16" else torch.float32
+    # separate calls
+    u = torch.empty((Bsz, T, Di), device="cuda", dtype=x.dtype)
+    c1, s1 = torch.empty((Bsz, Di, K), device="cuda"), torch.empty((Bsz, Di, N), device="cuda")
+    y1 = torch.empty((Bsz, T, Di), device="cuda", dtype=ytd)
+    m.mamba_conv1d_silu_prefill(u, x, pd["conv_w"], pd["conv_b"], c0, c1)
+    m.mamba_selective_scan_prefill(y1, u, dt, Bm, Cm, pd["A_log"], pd["D"], pd["dt_bias"], z, s0, s1)
+    # fused
+    y2 = torch.empty((Bsz, T, Di), device="cuda", dtype=ytd)
+    if inplace and states:
+        c2, s2 = c0.clone(), s0.clone()
+        m.mamba_mixer_prefill(y2, x, dt, Bm, Cm, pd["conv_w"], pd["A_log"], pd["conv_b"], pd["D"], pd["dt_bias"],
+                              z, c2, c2, s2, s2)
+    else:
+        c2, s2 = torch.empty_like(c1), torch.empty_like(s1)
+        m.mamba_mixer_prefill(y2, x, dt, Bm, Cm, pd["conv_w"], pd["A_log"], pd["conv_b"], pd["D"], pd["dt_bias"],
+                              z, c0, c2, s0, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2), "fused prefill y != conv prefill + scan prefill"
+    assert torch.equal(c1, c2) and torch.equal(s1, s2), "fused prefill states differ"
+    if dtype == "f32" and y_dtype == "f32" and not inplace:
+        # (bf16: u is rounded to bf16 between the halves; the separate calls are oracle-checked)
+        ch = synth.normal(SEED, "conv_state", (Bsz, Di, K), 0.5) if states else None
+        sh = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5) if states else None
+        u_ref, c_ref = oracle.conv1d_silu_prefill(a["x"], p["conv_w"], p["conv_b"], ch)
+        y_ref, s_ref = oracle.selective_scan_prefill(u_ref, a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                     p["dt_bias"], a["z"] if gate else None, sh)
+        assert_within(to_host(y2), y_ref, "fused y vs oracle")
+        assert_within(to_host(s2), s_ref, "fused ssm state vs oracle")
+        assert np.array_equal(to_host(c2), c_ref)
+
+
+def test_mixer_prefill_T0_copies_both_states(cuda_lib):
+    m = cuda_lib
+    Bsz, Di, N, K = 2, 32, 16, 4
+    p = {k: to_dev(v) for k, v in _params(SEED, Di, N, K).items()}
+    e = torch.empty((Bsz, 0, Di), device="cuda")
+    eb = torch.empty((Bsz, 0, N), device="cuda")
+    c0, s0 = torch.randn((Bsz, Di, K), device="cuda"), torch.randn((Bsz, Di, N), device="cuda")
+    c1, s1 = torch.full_like(c0, 7.0), torch.full_like(s0, 7.0)
+    m.mamba_mixer_prefill(e, e, e, eb, eb, p["conv_w"], p["A_log"], conv_state_in=c0, conv_state_out=c1,
+                          ssm_state_in=s0, ssm_state_out=s1)
+    torch.cuda.synchronize()
+    assert torch.equal(c0, c1) and torch.equal(s0, s1)
