@@ -60,6 +60,7 @@ def _load():
             lib.oracle_conv1d_silu_step.argtypes = [dp, dp, L, dp, dp, dp, L, L, L, ctypes.c_int]
             lib.oracle_conv1d_silu_step.restype = ctypes.c_int
             lib.oracle_ssm_step.argtypes = [dp, dp, L] + [dp] * 8 + [L, L, L, ctypes.c_int]
+            lib.oracle_m3_step.argtypes = [dp, dp, dp, dp, L] + [dp] * 7 + [L, L, L, L]
             lib.oracle_ssm_step.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -169,4 +170,26 @@ def ssm_step(u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt_bias=None, z=Non
         _ptr(A_log), _ptr(D), _ptr(dt_bias), Bsz, Di, N, nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle_ssm_step rejected its arguments")
+    return y
+
+
+def m3_step(x, k, q, alpha, beta, gamma, ssm_state, k_state, v_state, layer, D=None):
+    """One Mamba-3 SISO T=1 step on the `layer` slabs (states updated in place).
+
+    x: [B, H, P]; k, q: [B, H, N]; alpha, beta, gamma: [B, H]; D: [H];
+    ssm_state [L, B, H, P, N], k_state [L, B, H, N], v_state [L, B, H, P] (f64,
+    C-contiguous).  Returns y [B, H, P]."""
+    for s_ in (ssm_state, k_state, v_state):
+        assert s_.dtype == np.float64 and s_.flags.c_contiguous
+    x, k, q = _f64(x), _f64(k), _f64(q)
+    alpha, beta, gamma, D = _f64(alpha), _f64(beta), _f64(gamma), _f64(D)
+    Bsz, H, P = x.shape
+    N = k.shape[2]
+    assert ssm_state.shape[1:] == (Bsz, H, P, N) and k_state.shape[1:] == (Bsz, H, N)
+    assert v_state.shape[1:] == (Bsz, H, P)
+    y = np.empty((Bsz, H, P))
+    rc = _load().oracle_m3_step(_ptr(y), _ptr(ssm_state), _ptr(k_state), _ptr(v_state), layer, _ptr(x), _ptr(k),
+                                _ptr(q), _ptr(alpha), _ptr(beta), _ptr(gamma), _ptr(D), Bsz, H, P, N)
+    if rc != 0:
+        raise ValueError("oracle_m3_step rejected its arguments")
     return y

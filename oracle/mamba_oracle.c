@@ -239,3 +239,50 @@ int oracle_ssm_step(double* y, double* ssm_state, long layer, const double* u,
     return oracle_selective_scan_prefill(y, slab, u, dt, z, Bm, Cm, A_log, D, dt_bias, slab,
                                          B, 1, Di, N, nthreads);
 }
+
+/*
+ * Mamba-3 SISO T=1 step (docs.rs source view of mamba-rs 0.2.1
+ * src/mamba3_siso/gpu/inference.rs: `Mamba3GpuInferenceState` and the F6
+ * `m3_step_fwd` launch in `step_layer_kernels`).  The page shows the state
+ * buffers -- ssm [n_layers][batch*nh*hd*ds], k (the previous B after RoPE)
+ * [n_layers][batch*nh*ds], v (the previous x) [n_layers][batch*nh*hd] -- and
+ * the step's arguments (state, k state, v state, y, x, current k and q,
+ * alpha, beta, gamma per (batch, head), D), but not the kernel body.  Read
+ * plainly, the trapezoidal update mixes the previous token's input (k_prev,
+ * v_prev) with weight beta and the current one with weight gamma:
+ *   h[p][n] = alpha h[p][n] + beta k_prev[n] v_prev[p] + gamma k[n] x[p]
+ *   y[p]    = sum_n q[n] h[p][n] + D x[p]
+ * after which the k state holds k and the v state holds x.
+ */
+int oracle_m3_step(double* y, double* ssm_state, double* k_state, double* v_state, long layer,
+                   const double* x, const double* k, const double* q, const double* alpha,
+                   const double* beta, const double* gamma, const double* D, long B, long H,
+                   long P, long N)
+{
+    if (layer < 0 || !ssm_state || !k_state || !v_state || B < 0 || H < 0 || P < 0 || N < 0)
+        return -1;
+    double* hs = ssm_state + layer * B * H * P * N;
+    double* ks = k_state + layer * B * H * N;
+    double* vs = v_state + layer * B * H * P;
+    for (long b = 0; b < B; ++b) {
+        for (long hd = 0; hd < H; ++hd) {
+            const long bh = b * H + hd;
+            const double a = alpha[bh], be = beta[bh], g = gamma[bh];
+            for (long p = 0; p < P; ++p) {
+                double* hrow = hs + (bh * P + p) * N;
+                const double xp = x[bh * P + p];
+                const double vp = vs[bh * P + p];
+                double acc = 0.0;
+                for (long n = 0; n < N; ++n) {
+                    const double kp = ks[bh * N + n];
+                    hrow[n] = a * hrow[n] + be * kp * vp + g * k[bh * N + n] * xp;
+                    acc += q[bh * N + n] * hrow[n];
+                }
+                y[bh * P + p] = acc + (D ? D[hd] : 0.0) * xp;
+            }
+            for (long n = 0; n < N; ++n) ks[bh * N + n] = k[bh * N + n];
+            for (long p = 0; p < P; ++p) vs[bh * P + p] = x[bh * P + p];
+        }
+    }
+    return 0;
+}

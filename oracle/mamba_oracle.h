@@ -42,6 +42,15 @@ int oracle_ssm_step(double* y, double* ssm_state, long layer, const double* u,
                     const double* A_log, const double* D, const double* dt_bias, long B,
                     long Di, long N, int nthreads);
 
+/* Mamba-3 SISO step on the `layer` slabs (in place): x [B][H][P]; k, q
+ * [B][H][N]; alpha, beta, gamma [B][H]; D [H] or NULL; ssm state
+ * [n_layers][B][H][P][N], k state [n_layers][B][H][N], v state
+ * [n_layers][B][H][P]; y [B][H][P]. */
+int oracle_m3_step(double* y, double* ssm_state, double* k_state, double* v_state, long layer,
+                   const double* x, const double* k, const double* q, const double* alpha,
+                   const double* beta, const double* gamma, const double* D, long B, long H,
+                   long P, long N);
+
 #ifdef __cplusplus
 }
 #endif

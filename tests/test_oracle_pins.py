@@ -288,3 +288,111 @@ def test_tiny_workload_runs_and_is_finite():
     # delta lies in the log-uniform range widened by dt ~ N(0, 0.1^2)
     delta = np.logaddexp(0.0, a["dt"].astype(np.float64) + p["dt_bias"])
     assert 1e-4 < delta.min() and delta.max() < 0.3
+
+
+# ---------------------------------------------------------------- Mamba-3 step ----
+# Pins of oracle.m3_step (Mamba-3 SISO trapezoidal step, mamba-rs 0.2.1
+# mamba3_siso/gpu/inference.rs: state buffers and the F6 m3_step_fwd launch).
+
+def _m3_case(rng, B=2, H=3, P=4, N=5, L=2):
+    st = np.ascontiguousarray(rng.normal(size=(L, B, H, P, N)))
+    ks = np.ascontiguousarray(rng.normal(size=(L, B, H, N)))
+    vs = np.ascontiguousarray(rng.normal(size=(L, B, H, P)))
+    return st, ks, vs
+
+
+def test_m3_constant_inputs_follow_the_geometric_series():
+    """Constant k, x (and the states' previous k, v equal to them): after T steps
+    h_T = a^T h0 + (b + g) k x (1 - a^T) / (1 - a), y_T = q . h_T + D x."""
+    rng = np.random.default_rng(31)
+    B, H, P, N, T = 2, 3, 4, 5, 37
+    k, q, x = rng.normal(size=(B, H, N)), rng.normal(size=(B, H, N)), rng.normal(size=(B, H, P))
+    a = rng.uniform(0.5, 0.99, size=(B, H))
+    be, g = rng.uniform(0.0, 0.3, size=(B, H)), rng.uniform(0.0, 0.3, size=(B, H))
+    D = rng.normal(size=H)
+    h0 = rng.normal(size=(1, B, H, P, N))
+    st = h0.copy()
+    ks, vs = k[None].copy(), x[None].copy()
+    for _ in range(T):
+        y = oracle.m3_step(x, k, q, a, be, g, st, ks, vs, 0, D)
+    aT = a[..., None, None] ** T
+    outer = k[:, :, None, :] * x[:, :, :, None]
+    h_ref = aT * h0[0] + (be + g)[..., None, None] * outer * (1 - aT) / (1 - a)[..., None, None]
+    np.testing.assert_allclose(st[0], h_ref, rtol=1e-12, atol=1e-12)
+    y_ref = np.einsum("bhn,bhpn->bhp", q, h_ref) + D[None, :, None] * x
+    np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_m3_hands_the_current_k_and_x_to_the_next_step_and_keeps_other_layers():
+    rng = np.random.default_rng(32)
+    st, ks, vs = _m3_case(rng)
+    st0, ks0, vs0 = st.copy(), ks.copy(), vs.copy()
+    B, H, P, N = 2, 3, 4, 5
+    x, k, q = rng.normal(size=(B, H, P)), rng.normal(size=(B, H, N)), rng.normal(size=(B, H, N))
+    ones = np.ones((B, H))
+    oracle.m3_step(x, k, q, ones, ones, ones, st, ks, vs, 1)
+    assert np.array_equal(ks[1], k) and np.array_equal(vs[1], x)
+    assert np.array_equal(st[0], st0[0]) and np.array_equal(ks[0], ks0[0]) and np.array_equal(vs[0], vs0[0])
+    # the previous (k, v) enter with weight beta, the current (k, x) with gamma
+    zero = np.zeros((B, H))
+    st2, ks2, vs2 = st0.copy(), ks0.copy(), vs0.copy()
+    oracle.m3_step(x, k, q, zero, ones, zero, st2, ks2, vs2, 1)
+    np.testing.assert_allclose(st2[1], ks0[1][:, :, None, :] * vs0[1][:, :, :, None], rtol=1e-15)
+    st3, ks3, vs3 = st0.copy(), ks0.copy(), vs0.copy()
+    y3 = oracle.m3_step(x, k, q, zero, zero, ones, st3, ks3, vs3, 1)
+    np.testing.assert_allclose(st3[1], k[:, :, None, :] * x[:, :, :, None], rtol=1e-15)
+    np.testing.assert_allclose(y3, np.einsum("bhn,bhn,bhp->bhp", q, k, x), rtol=1e-12)
+
+
+def test_m3_pure_decay_and_skip():
+    rng = np.random.default_rng(33)
+    st, ks, vs = _m3_case(rng)
+    B, H, P, N = 2, 3, 4, 5
+    x, k, q = rng.normal(size=(B, H, P)), rng.normal(size=(B, H, N)), rng.normal(size=(B, H, N))
+    a = rng.uniform(0.1, 1.0, size=(B, H))
+    zero = np.zeros((B, H))
+    D = rng.normal(size=H)
+    h0 = st[0].copy()
+    y = oracle.m3_step(x, k, q, a, zero, zero, st, ks, vs, 0, D)
+    np.testing.assert_allclose(st[0], a[..., None, None] * h0, rtol=1e-15)
+    np.testing.assert_allclose(y, np.einsum("bhn,bhpn->bhp", q, st[0]) + D[None, :, None] * x, rtol=1e-12)
+
+
+def test_m3_is_jointly_linear_in_state_previous_v_and_x():
+    rng = np.random.default_rng(34)
+    B, H, P, N = 2, 3, 4, 5
+    k, q = rng.normal(size=(B, H, N)), rng.normal(size=(B, H, N))
+    kprev = rng.normal(size=(1, B, H, N))
+    a, be, g = (rng.uniform(0.2, 0.9, size=(B, H)) for _ in range(3))
+    D = rng.normal(size=H)
+
+    def run(h0, v0, x):
+        st, ks, vs = h0[None].copy(), kprev.copy(), v0[None].copy()
+        y = oracle.m3_step(x, k, q, a, be, g, st, ks, vs, 0, D)
+        return st[0], y
+
+    s1 = (rng.normal(size=(B, H, P, N)), rng.normal(size=(B, H, P)), rng.normal(size=(B, H, P)))
+    s2 = (rng.normal(size=(B, H, P, N)), rng.normal(size=(B, H, P)), rng.normal(size=(B, H, P)))
+    c1, c2 = 0.7, -1.3
+    h1, y1 = run(*s1)
+    h2, y2 = run(*s2)
+    h12, y12 = run(*(c1 * u + c2 * v for u, v in zip(s1, s2)))
+    np.testing.assert_allclose(h12, c1 * h1 + c2 * h2, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y12, c1 * y1 + c2 * y2, rtol=1e-12, atol=1e-12)
+
+
+def test_m3_batch_and_head_independence():
+    rng = np.random.default_rng(35)
+    B, H, P, N = 3, 4, 2, 3
+    st, ks, vs = _m3_case(rng, B, H, P, N, L=1)
+    x, k, q = rng.normal(size=(B, H, P)), rng.normal(size=(B, H, N)), rng.normal(size=(B, H, N))
+    a, be, g = (rng.uniform(0.2, 0.9, size=(B, H)) for _ in range(3))
+    D = rng.normal(size=H)
+    pb, ph = np.array([2, 0, 1]), np.array([3, 1, 0, 2])
+    sA, kA, vA = st.copy(), ks.copy(), vs.copy()
+    y = oracle.m3_step(x, k, q, a, be, g, sA, kA, vA, 0, D)
+    perm = lambda t: np.ascontiguousarray(t[pb][:, ph])
+    sB, kB, vB = (np.ascontiguousarray(s_[:, pb][:, :, ph]) for s_ in (st, ks, vs))
+    yB = oracle.m3_step(perm(x), perm(k), perm(q), perm(a), perm(be), perm(g), sB, kB, vB, 0, D[ph])
+    np.testing.assert_array_equal(yB, perm(y))
+    np.testing.assert_array_equal(sB[0], perm(sA[0]))
