@@ -45,6 +45,8 @@ KERNEL_SOURCES = {
 }
 KERNEL_SOURCES["mixer_step"] = KERNEL_SOURCES["step"]
 KERNEL_SOURCES["fused"] = KERNEL_SOURCES["scan"]
+KERNEL_SOURCES["m3_step"] = ["selective_state_space_conv1d_gb300/csrc/m3_step.cu",
+                             "selective_state_space_conv1d_gb300/csrc/device_math.cuh"]
 
 
 # ---------------------------------------------------------------- utilities --
@@ -553,6 +555,57 @@ def run_decode(torch, m, synth, device, peak, peak_src, n_steps=256):
     return out
 
 
+def run_m3_decode(torch, m, device, peak, peak_src, n_steps=16, L=24, Bsz=128, H=24, P=64, N=64):
+    """Mamba-3 SISO T=1 decode: L layers x batch B, H heads of headdim P and
+    d_state N (a synthetic shape: the pages give none), graph-replayed."""
+    g = torch.Generator(device=device)
+    g.manual_seed(0x5EED0005)
+    rn = lambda *shape: torch.randn(shape, generator=g, device=device)
+    st = rn(L, Bsz, H, P, N) * 0.5
+    ks, vs = rn(L, Bsz, H, N), rn(L, Bsz, H, P)
+    x, k, q = rn(n_steps, L, Bsz, H, P), rn(n_steps, L, Bsz, H, N), rn(n_steps, L, Bsz, H, N)
+    al = torch.exp(-torch.rand((n_steps, L, Bsz, H), generator=g, device=device) * 0.2)
+    be = torch.rand((n_steps, L, Bsz, H), generator=g, device=device) * 0.1
+    ga = torch.rand((n_steps, L, Bsz, H), generator=g, device=device) * 0.1
+    D = rn(L, H)
+    y = torch.empty((L, Bsz, H, P), device=device)
+
+    def step(s_, l):
+        m.mamba3_siso_step_batched(y[l], x[s_, l], k[s_, l], q[s_, l], al[s_, l], be[s_, l], ga[s_, l], st, ks, vs,
+                                   l, D[l])
+
+    for s_ in range(3):
+        for l in range(L):
+            step(s_, l)
+    torch.cuda.synchronize()
+    gr = capture(torch, lambda: [step(s_, l) for s_ in range(n_steps) for l in range(L)])
+    gr.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 4
+    a.record()
+    for _ in range(reps):
+        gr.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (reps * n_steps)
+    del gr
+    kms = kernel_time(torch, [lambda s_=s_, l=l: step(s_, l) for s_ in range(4) for l in range(L)], 4 * L)
+    BH = Bsz * H
+    per_launch = BH * P * N * 8 + BH * P * 16 + BH * N * 16 + BH * 12 + H * 4
+    out = {
+        "workload": f"mamba3-siso-decode-b{Bsz}-l{L}-h{H}-p{P}-n{N}", "value": round(1e3 / ms, 2),
+        "unit": "steps/s", "ms_per_step": round(ms, 5),
+        "config": {"n_layers": L, "batch": Bsz, "nheads": H, "headdim": P, "d_state": N,
+                   "shape": "synthetic (the pages give no Mamba-3 shapes)",
+                   "launch": f"CUDA graph of {n_steps} steps x {L} layers",
+                   "l2": f"state {L * BH * P * N * 4 / 1e9:.2f} GB > L2"},
+        "gpu_launches_per_step": L,
+    }
+    out["roofline"] = roofline(per_launch, kms, peak, peak_src, ncu_traffic("m3_step", out["workload"]))
+    return out
+
+
 # ----------------------------------------------------------- CPU oracle arm --
 
 def oracle_prefill_sample(synth, wl_index, n_channels, nthreads):
@@ -690,6 +743,7 @@ def main():
     extra = {}
     if not args.no_extra:
         extra["decode_130m_b128_l24"] = run_decode(torch, m, synth, device, peak, peak_src)
+        extra["decode_mamba3_siso"] = run_m3_decode(torch, m, device, peak, peak_src)
         r3 = run_prefill(torch, m, synth, 3, 50, 3, device, None, None, host_inputs=False)
         extra["prefill_2p8b_bf16"] = {
             "workload": r3["wl"].name, "value": round(r3["tokens_per_step"] / (r3["ms_per_step"] * 1e-3), 1),

@@ -238,6 +238,34 @@ MAMBA_API int mamba_mixer_prefill(void* y, int64_t ld_y, int y_dtype, const void
                                   int64_t workspace_bytes, void* stream);
 
 /*
+ * mamba3_siso_step_batched - batched T=1 step of the Mamba-3 SISO mixer (the
+ * trapezoidal SSM recurrence), in place on the `layer` slabs of its three
+ * persistent states.  (mamba-rs 0.2.1 mamba3_siso/gpu/inference.rs:
+ * `Mamba3GpuInferenceState` -- SSM [n_layers][batch*nh*hd*ds], k = previous B
+ * after RoPE [n_layers][batch*nh*ds], v = previous x [n_layers][batch*nh*hd] --
+ * and step F6 `m3_step_fwd` on the current x, k, q and the alpha / beta /
+ * gamma of F5.  The page prints the launch, not the kernel; the update read off
+ * its arguments is, per (batch b, head h, row p, state n):
+ *   h = alpha h + beta k_prev[n] v_prev[p] + gamma k[n] x[p]
+ *   y[p] = sum_n q[n] h[p][n] + D[h] x[p]
+ * after which the k state holds k and the v state holds x.)
+ *
+ *   y          [B][H][P] dense, dtype y_dtype (out)
+ *   x          [B][H][P] dense, dtype act_dtype
+ *   k, q       [B][H][N] dense, dtype act_dtype (B and C after norm, bias, RoPE)
+ *   alpha, beta, gamma [B][H] f32; D [H] f32 or NULL
+ *   ssm_state  base of [n_layers][B][H][P][N] f32 (16-byte aligned)
+ *   k_state    base of [n_layers][B][H][N] f32; v_state base of [n_layers][B][H][P] f32
+ * N (d_state) in {16, 32, 64, 128}; P * N / 8 <= 2048.
+ * Errors: as for mamba_ssm_step_batched.
+ */
+MAMBA_API int mamba3_siso_step_batched(void* y, int y_dtype, const void* x, const void* k, const void* q,
+                                       int act_dtype, const float* alpha, const float* beta,
+                                       const float* gamma, const float* D, float* ssm_state, float* k_state,
+                                       float* v_state, int64_t layer, int64_t n_layers, int64_t B, int64_t H,
+                                       int64_t P, int64_t N, void* stream);
+
+/*
  * Graph-captured decode driver.  (inference.rs `capture_graph` / `step`: after
  * a warm-up step the engine records its whole T=1 step chain into a CUDA graph
  * once and replays it every token, cutting the launch overhead from ~50 us to

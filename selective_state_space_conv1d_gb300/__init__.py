@@ -8,6 +8,7 @@ Four C-ABI entry points (include/mamba_ssm.h), each a hand-written CUDA kernel:
   mamba_mixer_step_batched      both T=1 steps fused in one kernel
   mamba_mixer_prefill           conv1d + SiLU and the selective scan in one pass
   mamba_decode_graph_*          n_steps x n_layers fused steps recorded as one CUDA graph
+  mamba3_siso_step_batched      T=1 step of the Mamba-3 SISO (trapezoidal) recurrence
 This package is the thin Python binding (argument marshalling over ctypes);
 `synth` holds the seeded synthetic inputs used by the tests and the benchmark.
 """
@@ -25,6 +26,7 @@ from ._binding import (  # noqa: F401
     MAMBA_OK,
     MambaError,
     load,
+    mamba3_siso_step_batched,
     mamba_conv1d_silu_prefill,
     mamba_conv1d_silu_step,
     mamba_device_faults,

@@ -34,6 +34,7 @@ ABI_SYMBOLS = (
     "mamba_ssm_step_batched",
     "mamba_mixer_step_batched",
     "mamba_mixer_prefill",
+    "mamba3_siso_step_batched",
     "mamba_decode_graph_create",
     "mamba_decode_graph_launch",
     "mamba_decode_graph_kernels",
@@ -86,6 +87,8 @@ def load(path: str | None = None):
         lib.mamba_mixer_prefill.argtypes = ([vp, i64, i32, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i32]
                                             + [vp] * 9 + [i64, i64, i64, i64, i64, vp, i64, vp])
         lib.mamba_mixer_prefill.restype = ctypes.c_int
+        lib.mamba3_siso_step_batched.argtypes = [vp, i32, vp, vp, vp, i32] + [vp] * 7 + [i64] * 6 + [vp]
+        lib.mamba3_siso_step_batched.restype = ctypes.c_int
         lib.mamba_decode_graph_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i64, i32, i32, vp, vp,
                                                   i64, i64, i64, i64]
         lib.mamba_decode_graph_create.restype = ctypes.c_int
@@ -335,6 +338,32 @@ def mamba_mixer_prefill(y, x, dt, Bm, Cm, conv_w, A_log, conv_b=None, D=None, dt
         _ptr(conv_w), _ptr(conv_b), _ptr(conv_state_in), _ptr(conv_state_out),
         _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
         Bsz, T, Di, K, N, ws_ptr, ws_bytes, _stream(stream, x)))
+
+
+def mamba3_siso_step_batched(y, x, k, q, alpha, beta, gamma, ssm_state, k_state, v_state, layer, D=None, *,
+                             stream=None):
+    """Mamba-3 SISO T=1 step on slab `layer` of ssm_state [L, B, H, P, N],
+    k_state [L, B, H, N] and v_state [L, B, H, P] (all updated in place).
+
+    y, x: contiguous [B, H, P]; k, q: contiguous [B, H, N]; alpha, beta, gamma:
+    f32 [B, H]; D: f32 [H]."""
+    Bsz, H, P = x.shape
+    N = k.shape[2]
+    L = ssm_state.shape[0]
+    for st, nm, shp in ((ssm_state, "ssm_state", (L, Bsz, H, P, N)), (k_state, "k_state", (L, Bsz, H, N)),
+                        (v_state, "v_state", (L, Bsz, H, P))):
+        _f32_param(st, nm, shp)
+    for t, nm in ((alpha, "alpha"), (beta, "beta"), (gamma, "gamma")):
+        _f32_param(t, nm, (Bsz, H))
+    _f32_param(D, "D", (H,))
+    for t, nm, shp in ((y, "y", (Bsz, H, P)), (x, "x", (Bsz, H, P)), (k, "k", (Bsz, H, N)), (q, "q", (Bsz, H, N))):
+        if tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous {shp} tensor")
+        if nm in ("k", "q") and t.dtype != x.dtype:
+            raise ValueError(f"{nm} must have the dtype of x")
+    _check(load().mamba3_siso_step_batched(
+        _ptr(y), _dtype_code(y), _ptr(x), _ptr(k), _ptr(q), _dtype_code(x), _ptr(alpha), _ptr(beta), _ptr(gamma),
+        _ptr(D), _ptr(ssm_state), _ptr(k_state), _ptr(v_state), int(layer), L, Bsz, H, P, N, _stream(stream, x)))
 
 
 def mamba_ssm_step_batched(y, u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt_bias=None,

@@ -400,6 +400,52 @@ int mamba_mixer_prefill(void* y, int64_t ld_y, int y_dtype, const void* x, int64
   return ok();
 }
 
+int mamba3_siso_step_batched(void* y, int y_dtype, const void* x, const void* k, const void* q, int act_dtype,
+                             const float* alpha, const float* beta, const float* gamma, const float* D,
+                             float* ssm_state, float* k_state, float* v_state, int64_t layer, int64_t n_layers,
+                             int64_t B, int64_t H, int64_t P, int64_t N, void* stream) {
+  int rc;
+  if ((rc = check_dtype("y_dtype", y_dtype)) || (rc = check_dtype("act_dtype", act_dtype))) return rc;
+  if (B < 0 || H < 0 || P < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld H=%lld P=%lld)", (long long)B, (long long)H, (long long)P);
+  if (N != 16 && N != 32 && N != 64 && N != 128)
+    return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {16,32,64,128}", (long long)N);
+  if (P * (N / 8) > mamba::m3_max_items())
+    return fail(MAMBA_ERR_UNSUPPORTED, "headdim * d_state / 8 = %lld exceeds %d", (long long)(P * (N / 8)),
+                mamba::m3_max_items());
+  if (n_layers < 1 || layer < 0 || layer >= n_layers) return fail(MAMBA_ERR_INVALID_ARG, "layer=%lld outside [0, n_layers=%lld)", (long long)layer, (long long)n_layers);
+  if (B == 0 || H == 0 || P == 0) return ok();
+  if (!sizes_ok(B, H, P * N) || !sizes_ok(n_layers, B * H, P * N)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!y || !x || !k || !q || !alpha || !beta || !gamma || !ssm_state || !k_state || !v_state)
+    return fail(MAMBA_ERR_INVALID_ARG, "y, x, k, q, alpha, beta, gamma and the three states must not be NULL");
+  if (reinterpret_cast<uintptr_t>(ssm_state) & 15) return fail(MAMBA_ERR_INVALID_ARG, "ssm_state must be 16-byte aligned");
+  const int es = es_of(act_dtype), esy = es_of(y_dtype);
+  const int64_t BH = B * H;
+  int64_t by = 0, bx = 0, bk = 0, bs = 0, bh = 0, bss = 0, bks = 0, bvs = 0;
+  if (!span_bytes(1, BH * P, BH * P, esy, &by) || !span_bytes(1, BH * P, BH * P, es, &bx) ||
+      !span_bytes(1, BH * N, BH * N, es, &bk) || !span_bytes(1, BH, BH, 4, &bs) || !span_bytes(1, H, H, 4, &bh) ||
+      !span_bytes(BH * P, N, N, 4, &bss) || !span_bytes(1, BH * N, BH * N, 4, &bks) ||
+      !span_bytes(1, BH * P, BH * P, 4, &bvs))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  float* sslab = ssm_state + layer * BH * P * N;
+  float* kslab = k_state + layer * BH * N;
+  float* vslab = v_state + layer * BH * P;
+  Range ins[] = {range_of("x", x, bx), range_of("k", k, bk), range_of("q", q, bk), range_of("alpha", alpha, bs),
+                 range_of("beta", beta, bs), range_of("gamma", gamma, bs), range_of("D", D, bh)};
+  Range outs[] = {range_of("y", y, by), range_of("ssm_state", sslab, bss), range_of("k_state", kslab, bks),
+                  range_of("v_state", vslab, bvs)};
+  if ((rc = check_pointers(ins, 7, dev_id)) || (rc = check_pointers(outs, 4, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 4, ins, 7))) return rc;
+  mamba::M3StepArgs a{y, y_dtype == MAMBA_BF16, x, k, q, act_dtype == MAMBA_BF16, alpha, beta, gamma, D,
+                      sslab, kslab, vslab, B, H, (int)P, (int)N};
+  cudaError_t e = mamba::launch_m3_step_batched(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("mamba3_siso_step_batched launch", e);
+  return ok();
+}
+
 int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N) {
   if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size");
   if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);

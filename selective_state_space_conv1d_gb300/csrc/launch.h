@@ -138,6 +138,28 @@ struct SsmStepArgs {
 cudaError_t launch_ssm_step_batched(const SsmStepArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream);
 
+// Mamba-3 SISO T=1 step on one layer's slabs (pointers already offset).
+struct M3StepArgs {
+  void* y;              // [B][H][P], y_bf16 ? bf16 : f32
+  int y_bf16;
+  const void* x;        // [B][H][P]
+  const void* k;        // [B][H][N] (B after RoPE)
+  const void* q;        // [B][H][N] (C after RoPE)
+  int in_bf16;
+  const float* alpha;   // [B][H]
+  const float* beta;    // [B][H]
+  const float* gamma;   // [B][H]
+  const float* D;       // [H] or null
+  float* ssm_state;     // [B][H][P][N]
+  float* k_state;       // [B][H][N]
+  float* v_state;       // [B][H][P]
+  int64_t B, H;
+  int P, N;
+};
+// hd * ds / 8 must not exceed this
+int m3_max_items();
+cudaError_t launch_m3_step_batched(const M3StepArgs& a, cudaStream_t stream);
+
 // Fused decode step: conv1d + SiLU step on x, then the SSM step on its u.
 struct MixerStepArgs {
   SsmStepArgs ssm;         // ssm.u unused (u is produced in registers)

@@ -34,6 +34,9 @@ _TENSOR_IDS = {
     "x": 1, "z": 2, "dt": 3, "u": 4, "B": 5, "C": 6,
     "conv_w": 10, "conv_b": 11, "dt_bias": 12, "D": 13, "A_log": 14,
     "conv_state": 20, "ssm_state": 21,
+    # Mamba-3 SISO step
+    "m3_x": 30, "m3_k": 31, "m3_q": 32, "m3_alpha": 33, "m3_beta": 34, "m3_gamma": 35, "m3_D": 36,
+    "m3_ssm_state": 37, "m3_k_state": 38, "m3_v_state": 39,
 }
 
 
@@ -169,6 +172,31 @@ def decode_step_inputs(seed: int, layer: int, step: int, batch: int, d_inner: in
         "B": normal(seed, "B", bc, 1.0, dtype, layer, step),
         "C": normal(seed, "C", bc, 1.0, dtype, layer, step),
     }
+
+
+def m3_step_inputs(seed: int, layer: int, step: int, batch: int, nheads: int, headdim: int,
+                   d_state: int, dtype: str = "f32") -> dict:
+    """Per-(layer, step) inputs of one Mamba-3 SISO step: x [B, H, P]; k, q
+    [B, H, N] (standing for B and C after norm, bias and RoPE); alpha, beta,
+    gamma [B, H] f32 in the ranges exp(dt A), (1 - lambda) dt alpha and
+    lambda dt take for dt ~ 1e-3..0.1 and A of order -1."""
+    bh = (batch, nheads)
+    g = generator(seed, "m3_alpha", layer, step)
+    return {
+        "x": normal(seed, "m3_x", (batch, nheads, headdim), 1.0, dtype, layer, step),
+        "k": normal(seed, "m3_k", (batch, nheads, d_state), 1.0, dtype, layer, step),
+        "q": normal(seed, "m3_q", (batch, nheads, d_state), 1.0, dtype, layer, step),
+        "alpha": np.exp(-g.uniform(1e-3, 0.2, size=bh)).astype(np.float32),
+        "beta": generator(seed, "m3_beta", layer, step).uniform(0.0, 0.1, size=bh).astype(np.float32),
+        "gamma": generator(seed, "m3_gamma", layer, step).uniform(0.0, 0.1, size=bh).astype(np.float32),
+    }
+
+
+def m3_states(seed: int, n_layers: int, batch: int, nheads: int, headdim: int, d_state: int, std: float = 0.5):
+    """f32 Mamba-3 states: ssm [L, B, H, P, N], k [L, B, H, N], v [L, B, H, P]."""
+    return (normal(seed, "m3_ssm_state", (n_layers, batch, nheads, headdim, d_state), std),
+            normal(seed, "m3_k_state", (n_layers, batch, nheads, d_state), 1.0),
+            normal(seed, "m3_v_state", (n_layers, batch, nheads, headdim), 1.0))
 
 
 def torch_normal(shape, std, seed, device, dtype=None):

@@ -28,7 +28,7 @@ def header_symbols():
     syms = set()
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         txt = open(h).read()
-        syms |= set(re.findall(r"MAMBA_API\s+[\w\s\*]+?\b(mamba_\w+)\s*\(", txt))
+        syms |= set(re.findall(r"MAMBA_API\s+[\w\s\*]+?\b(mamba\w+)\s*\(", txt))
     return syms
 
 
@@ -43,7 +43,7 @@ def test_header_declares_the_four_entry_points():
 def test_library_exports_every_declared_symbol(lib):
     out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True,
                          check=True).stdout
-    exported = set(re.findall(r"\bT\s+(mamba_\w+)", out))
+    exported = set(re.findall(r"\bT\s+(mamba\w+)", out))
     assert header_symbols() <= exported
     for s in header_symbols():
         assert hasattr(lib, s)
@@ -184,3 +184,12 @@ def test_mixer_prefill_refuses_other_d_conv_on_host(lib):
     rc = lib.mamba_mixer_prefill(FAKE, 64, 0, FAKE, 64, FAKE, 64, None, 0, FAKE, 16, FAKE, 16, 7,
                                  FAKE, None, None, None, FAKE, None, None, None, None, 1, 8, 64, 4, 16, None, 0, None)
     assert rc == m.MAMBA_ERR_INVALID_ARG
+
+
+def test_m3_step_rejects_bad_arguments_on_host(lib):
+    args = lambda P=64, N=64, layer=0, L=1: (FAKE, 0, FAKE, FAKE, FAKE, 0, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE,
+                                            layer, L, 2, 3, P, N, None)
+    assert lib.mamba3_siso_step_batched(*args(N=8)) == m.MAMBA_ERR_UNSUPPORTED
+    assert lib.mamba3_siso_step_batched(*args(P=1024, N=128)) == m.MAMBA_ERR_UNSUPPORTED
+    assert lib.mamba3_siso_step_batched(*args(layer=1, L=1)) == m.MAMBA_ERR_INVALID_ARG
+    assert lib.mamba3_siso_step_batched(*args(P=-1)) == m.MAMBA_ERR_INVALID_ARG

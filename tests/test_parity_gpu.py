@@ -601,3 +601,38 @@ def test_mixer_prefill_T0_copies_both_states(cuda_lib):
                           ssm_state_in=s0, ssm_state_out=s1)
     torch.cuda.synchronize()
     assert torch.equal(c0, c1) and torch.equal(s0, s1)
+
+
+# ------------------------------------------------------------ Mamba-3 step ----
+
+@pytest.mark.parametrize("Bsz,H,P,N,dtype,y_dtype,with_D", [
+    (3, 5, 64, 64, "f32", "f32", True), (2, 3, 32, 128, "bf16", "f32", True), (4, 2, 100, 16, "f32", "bf16", False),
+    (1, 1, 256, 64, "f32", "f32", True), (2, 4, 48, 32, "bf16", "bf16", True),
+])
+def test_m3_step_matches_oracle(cuda_lib, Bsz, H, P, N, dtype, y_dtype, with_D):
+    """Three Mamba-3 SISO steps on the middle layer of a 3-layer state: y and
+    all three states against the oracle; the other layers untouched."""
+    m = cuda_lib
+    L, layer = 3, 1
+    st_h, ks_h, vs_h = synth.m3_states(SEED, L, Bsz, H, P, N)
+    st, ks, vs = to_dev(st_h), to_dev(ks_h), to_dev(vs_h)
+    ref = [a.astype(np.float64).copy() for a in (st_h, ks_h, vs_h)]
+    D_h = synth.normal(SEED, "m3_D", (H,), 1.0) if with_D else None
+    D = to_dev(D_h) if with_D else None
+    ytd = torch.bfloat16 if y_dtype == "bf16" else torch.float32
+    for step in range(3):
+        inp = synth.m3_step_inputs(SEED, layer, step, Bsz, H, P, N, dtype)
+        x, k, q = (to_dev(inp[n], dtype) for n in ("x", "k", "q"))
+        al, be, ga = (to_dev(inp[n]) for n in ("alpha", "beta", "gamma"))
+        y = torch.empty((Bsz, H, P), device="cuda", dtype=ytd)
+        m.mamba3_siso_step_batched(y, x, k, q, al, be, ga, st, ks, vs, layer, D)
+        torch.cuda.synchronize()
+        y_ref = oracle.m3_step(inp["x"], inp["k"], inp["q"], inp["alpha"], inp["beta"], inp["gamma"],
+                               ref[0], ref[1], ref[2], layer, D_h)
+        assert_within(to_host(y), y_ref, f"m3 y step {step}", bf16_out=y_dtype == "bf16")
+        assert_within(to_host(st[layer]), ref[0][layer], f"m3 ssm state step {step}")
+        assert np.array_equal(to_host(ks[layer]), ref[1][layer]) and np.array_equal(to_host(vs[layer]), ref[2][layer])
+    for s_dev, s_h in ((st, st_h), (ks, ks_h), (vs, vs_h)):
+        for l in (0, 2):
+            assert np.array_equal(to_host(s_dev[l]), s_h[l])
+    assert m.mamba_device_faults(clear=True) == 0
