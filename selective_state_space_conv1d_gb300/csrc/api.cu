@@ -185,7 +185,9 @@ int mamba_device_faults(int clear) {
   cudaError_t e = cudaSuccess;
   const int v = mamba::read_device_faults(clear != 0, &e);
   if (v < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: %s", cudaGetErrorString(e));
-  return ok(), v;
+  const int v3 = mamba::read_m3_faults(clear != 0);
+  if (v3 < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the Mamba-3 watchdog failed");
+  return ok(), v | v3;
 }
 
 int mamba_conv1d_silu_prefill(void* u, int64_t ld_u, const void* x, int64_t ld_x, int act_dtype,
@@ -441,7 +443,7 @@ int mamba3_siso_step_batched(void* y, int y_dtype, const void* x, const void* k,
   if ((rc = check_overlaps(outs, 4, ins, 7))) return rc;
   mamba::M3StepArgs a{y, y_dtype == MAMBA_BF16, x, k, q, act_dtype == MAMBA_BF16, alpha, beta, gamma, D,
                       sslab, kslab, vslab, B, H, (int)P, (int)N};
-  cudaError_t e = mamba::launch_m3_step_batched(a, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = mamba::launch_m3_step_batched(a, dev, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail("mamba3_siso_step_batched launch", e);
   return ok();
 }

@@ -158,7 +158,9 @@ struct M3StepArgs {
 };
 // hd * ds / 8 must not exceed this
 int m3_max_items();
-cudaError_t launch_m3_step_batched(const M3StepArgs& a, cudaStream_t stream);
+cudaError_t launch_m3_step_batched(const M3StepArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+// watchdog bits of the Mamba-3 ring kernel (the device must be synchronised)
+int read_m3_faults(bool clear);
 
 // Fused decode step: conv1d + SiLU step on x, then the SSM step on its u.
 struct MixerStepArgs {

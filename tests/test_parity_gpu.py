@@ -636,3 +636,27 @@ def test_m3_step_matches_oracle(cuda_lib, Bsz, H, P, N, dtype, y_dtype, with_D):
         for l in (0, 2):
             assert np.array_equal(to_host(s_dev[l]), s_h[l])
     assert m.mamba_device_faults(clear=True) == 0
+
+
+@pytest.mark.parametrize("P,N,dtype", [(64, 64, "f32"), (32, 128, "bf16"), (100, 16, "f32")])
+def test_m3_ring_and_direct_paths_agree_bitwise(cuda_lib, P, N, dtype):
+    """The copy-ring Mamba-3 kernel (aligned buffers) and the per-(batch, head)
+    kernel (k_state 4 bytes off a 16-byte boundary) give identical results."""
+    m = cuda_lib
+    L, Bsz, H, layer = 2, 5, 3, 1
+    st_h, ks_h, vs_h = synth.m3_states(SEED + 1, L, Bsz, H, P, N)
+    sa, ka, va = to_dev(st_h), to_dev(ks_h), to_dev(vs_h)
+    sb, kb, vb = to_dev(st_h), _offset_like(to_dev(ks_h)), to_dev(vs_h)
+    D = to_dev(synth.normal(SEED, "m3_D", (H,), 1.0))
+    for step in range(3):
+        inp = synth.m3_step_inputs(SEED + 1, layer, step, Bsz, H, P, N, dtype)
+        x, k, q = (to_dev(inp[n], dtype) for n in ("x", "k", "q"))
+        al, be, ga = (to_dev(inp[n]) for n in ("alpha", "beta", "gamma"))
+        ya = torch.empty((Bsz, H, P), device="cuda")
+        yb = torch.empty((Bsz, H, P), device="cuda")
+        m.mamba3_siso_step_batched(ya, x, k, q, al, be, ga, sa, ka, va, layer, D)
+        m.mamba3_siso_step_batched(yb, x, k, q, al, be, ga, sb, kb, vb, layer, D)
+        torch.cuda.synchronize()
+        assert torch.equal(ya, yb), f"y differs at step {step}"
+        assert torch.equal(sa, sb) and torch.equal(ka, kb) and torch.equal(va, vb)
+    assert m.mamba_device_faults(clear=True) == 0
