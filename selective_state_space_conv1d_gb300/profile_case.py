@@ -10,6 +10,8 @@ times, then times one more call with CUDA events and prints it.
   --what step      T=1 SSM step on layer 1 of an [L][B][Di][N] state
   --what mixer     fused conv step + SSM step on layer 1
   --what convstep  T=1 conv step on layer 1 of an [L][B][Di][4] state
+  --what fused     fused conv1d + SiLU and selective-scan prefill  [B, T, Di]
+  --what m3        Mamba-3 SISO step on layer 1: --B batch, --H heads, --P headdim, --N d_state
 """
 import argparse
 
@@ -20,7 +22,9 @@ from . import _binding as m
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--what", default="scan", choices=("scan", "conv", "step", "mixer", "convstep"))
+    ap.add_argument("--what", default="scan", choices=("scan", "conv", "step", "mixer", "convstep", "fused", "m3"))
+    ap.add_argument("--H", type=int, default=24)
+    ap.add_argument("--P", type=int, default=64)
     ap.add_argument("--B", type=int, default=1)
     ap.add_argument("--T", type=int, default=2048)
     ap.add_argument("--Di", type=int, default=1536)
@@ -38,7 +42,19 @@ def main(argv=None):
     dtb = torch.full((a.Di,), -4.0, device="cuda")
     w = torch.rand((a.Di, 4), generator=g, device="cuda") - 0.5
     m.load()
-    if a.what in ("scan", "conv"):
+    if a.what == "m3":
+        BH = (a.B, a.H)
+        st = torch.randn((a.L, a.B, a.H, a.P, a.N), generator=g, device="cuda")
+        ks = torch.randn((a.L, a.B, a.H, a.N), generator=g, device="cuda")
+        vs = torch.randn((a.L, a.B, a.H, a.P), generator=g, device="cuda")
+        x, k, q = r((a.B, a.H, a.P)), r((a.B, a.H, a.N)), r((a.B, a.H, a.N))
+        al = torch.exp(-torch.rand(BH, generator=g, device="cuda") * 0.2)
+        be = torch.rand(BH, generator=g, device="cuda") * 0.1
+        ga = torch.rand(BH, generator=g, device="cuda") * 0.1
+        Dh = torch.ones(a.H, device="cuda")
+        y = torch.empty((a.B, a.H, a.P), device="cuda")
+        f = lambda: m.mamba3_siso_step_batched(y, x, k, q, al, be, ga, st, ks, vs, 1, Dh)
+    elif a.what in ("scan", "conv", "fused"):
         sh = (a.B, a.T, a.Di)
         x, u, dt, z = r(sh), r(sh), r(sh, 0.1), r(sh)
         Bm, Cm = r((a.B, a.T, a.N)), r((a.B, a.T, a.N))
@@ -48,6 +64,8 @@ def main(argv=None):
         co = torch.empty((a.B, a.Di, 4), device="cuda")
         if a.what == "conv":
             f = lambda: m.mamba_conv1d_silu_prefill(uo, x, w, None, None, co)
+        elif a.what == "fused":
+            f = lambda: m.mamba_mixer_prefill(y, x, dt, Bm, Cm, w, A, None, D, dtb, z, None, co, None, so)
         else:
             f = lambda: m.mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A, D, dtb, z, None, so)
     else:
