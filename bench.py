@@ -699,6 +699,18 @@ def cpu_baseline(synth, budget_s=10.0):
                       f"f64 conv+scan, {total_s:.1f} s of wall time on {nthreads} threads"}
 
 
+def replica_throughput(torch, local_ms, tokens_per_step, steps, world, dist=None, device=None):
+    """Whole-job throughput of `world` independent replicas: every rank ran
+    `steps` steps of `tokens_per_step` tokens in local_ms; the job took the
+    slowest rank's time.  Returns (max_ms, tokens/s over all ranks)."""
+    total_ms = local_ms
+    if dist is not None:
+        t = torch.tensor([float(local_ms)], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, world * tokens_per_step * steps / (total_ms * 1e-3)
+
+
 def run_reference(args, rank, world):
     """The oracle as the reference arm: the f64 CPU oracle on this host's cores."""
     from selective_state_space_conv1d_gb300 import synth
@@ -779,13 +791,9 @@ def main():
     clocks = ClockSampler(local_rank)
 
     res = run_prefill(torch, m, synth, 1, args.steps, args.warmup, device, dist, clocks)
-    total_ms = res["total_ms"]
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = replica_throughput(torch, res["total_ms"], res["tokens_per_step"], args.steps, world, dist,
+                                         device)
     ms_step = total_ms / args.steps
-    value = world * res["tokens_per_step"] * args.steps / (total_ms * 1e-3)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     wl1 = res["wl"]
     scan_roof = prefill_roofline(res, peak, peak_src, sms)
