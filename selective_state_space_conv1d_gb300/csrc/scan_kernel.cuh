@@ -99,8 +99,13 @@ struct RowS {
 
 // KC > 0: the conv1d + SiLU of width KC is fused in; the staged "u" is x, and
 // each lane carries the last KC-1 inputs of its channel from row to row.
-template <int N, typename Tin, int MODE, bool GATE, int KC>
-__global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int act_vec, int bc_vec) {
+// YB: the y dtype is bf16; VEC: u/dt/z and B/C stage as 16-byte copies.  Both
+// are compile-time choices: a runtime flag in the unrolled row loop costs the
+// scheduler's freedom across rows (measured 5-17% on GB300).
+template <int N, typename Tin, int MODE, bool GATE, int KC, bool YB = false, bool VEC = false>
+__global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int act_vec_rt, int bc_vec_rt) {
+  const bool act_vec = VEC || act_vec_rt;
+  const bool bc_vec = VEC || bc_vec_rt;
   grid_dependency_wait();
   using TL = Tile<Tin>;
   constexpr int P = group_size(N);
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
         }
         float y = fmaf(Dc, rs.u, tree_sum<NG>(part_));
         if (GATE) y *= rs.g;
-        store_out(a.y, yk + r * a.ld_y, a.y_bf16, y);
+        store_out(a.y, yk + r * a.ld_y, YB, y);
       };
       if (rows == kTC) {
 #pragma unroll 1
@@ -401,16 +406,33 @@ __global__ void __launch_bounds__(128) scan_fold_kernel(float* ws, int64_t BDN, 
   }
 }
 
-template <int N, typename Tin, int MODE, bool GATE>
-cudaError_t launch_mode(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
+template <int N, typename Tin, int MODE, bool GATE, bool YB, bool VEC>
+cudaError_t launch_mode_v(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
   const int64_t blocks = w.n_tiles * a.B * w.grid_parts;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   if (a.K == 4)
-    return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 4>, dim3((unsigned)blocks), dim3(kLanes), 0, stream, a,
-                      w, p.act_vec, p.bc_vec);
+    return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 4, YB, VEC>, dim3((unsigned)blocks), dim3(kLanes), 0,
+                      stream, a, w, p.act_vec, p.bc_vec);
   if (a.K != 0) return cudaErrorInvalidValue;
-  return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 0>, dim3((unsigned)blocks), dim3(kLanes), 0, stream, a, w,
-                    p.act_vec, p.bc_vec);
+  return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 0, YB, VEC>, dim3((unsigned)blocks), dim3(kLanes), 0,
+                    stream, a, w, p.act_vec, p.bc_vec);
+}
+
+template <int N, typename Tin, int MODE, bool GATE, bool YB>
+cudaError_t launch_mode_y(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
+  // the 16-byte staging path exists only where every row can take it
+  constexpr bool kCanVec = N * sizeof(Tin) >= 16;
+  if constexpr (kCanVec) {
+    if (p.act_vec && p.bc_vec) return launch_mode_v<N, Tin, MODE, GATE, YB, true>(a, w, p, stream);
+  }
+  return launch_mode_v<N, Tin, MODE, GATE, YB, false>(a, w, p, stream);
+}
+
+template <int N, typename Tin, int MODE, bool GATE>
+cudaError_t launch_mode(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
+  if constexpr (MODE == kPass1) return launch_mode_y<N, Tin, MODE, GATE, false>(a, w, p, stream);  // no y
+  return a.y_bf16 ? launch_mode_y<N, Tin, MODE, GATE, true>(a, w, p, stream)
+                  : launch_mode_y<N, Tin, MODE, GATE, false>(a, w, p, stream);
 }
 
 template <int N, typename Tin, int MODE>
