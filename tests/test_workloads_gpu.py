@@ -234,3 +234,45 @@ def test_long_context_continuation(cuda_lib):
     assert_within(Y2[:, :, sel], y_ref, "y vs oracle (sampled channels, 16448 tokens)")
     assert_within(to_host(ssm[0][:, sel]), s_ref, "ssm state vs oracle")
     assert np.array_equal(to_host(conv[0][:, sel]), c_ref)
+
+
+def test_prefill_beyond_2pow31_activation_elements(cuda_lib):
+    """B*T*Di = 2.2e9 > 2^31 activation elements (every index 64-bit): the fused
+    prefill equals conv prefill + scan prefill bit for bit at full size, and
+    both match the oracle on 4 channels (first, last, two in between) over all
+    2.1M tokens, with the final states."""
+    m = cuda_lib
+    Bsz, T, Di, N, K = 1, (1 << 21) + 17, 1056, 16, 4
+    assert Bsz * T * Di > 2 ** 31
+    SEED = 0x5EED0B16
+    p = synth.mixer_params(SEED, Di, N, K)
+    pd = {k: to_dev(v) for k, v in p.items()}
+    x = synth.torch_normal((Bsz, T, Di), 1.0, SEED + 901, "cuda")
+    dt = synth.torch_normal((Bsz, T, Di), 0.1, SEED + 902, "cuda")
+    z = synth.torch_normal((Bsz, T, Di), 1.0, SEED + 903, "cuda")
+    Bm = synth.torch_normal((Bsz, T, N), 1.0, SEED + 904, "cuda")
+    Cm = synth.torch_normal((Bsz, T, N), 1.0, SEED + 905, "cuda")
+    y = torch.empty((Bsz, T, Di), device="cuda")
+    c1, s1 = torch.empty((Bsz, Di, K), device="cuda"), torch.empty((Bsz, Di, N), device="cuda")
+    m.mamba_mixer_prefill(y, x, dt, Bm, Cm, pd["conv_w"], pd["A_log"], pd["conv_b"], pd["D"], pd["dt_bias"], z,
+                          None, c1, None, s1)
+    u = torch.empty_like(x)
+    c2, s2 = torch.empty_like(c1), torch.empty_like(s1)
+    m.mamba_conv1d_silu_prefill(u, x, pd["conv_w"], pd["conv_b"], None, c2)
+    y2 = torch.empty_like(y)
+    m.mamba_selective_scan_prefill(y2, u, dt, Bm, Cm, pd["A_log"], pd["D"], pd["dt_bias"], z, None, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(y, y2), "fused prefill != conv prefill + scan prefill at > 2^31 elements"
+    assert torch.equal(c1, c2) and torch.equal(s1, s2)
+    del u, y2
+    sel = np.array([0, 517, 1030, Di - 1])
+    idx = torch.as_tensor(sel, device="cuda")
+    col = lambda t: np.ascontiguousarray(t.index_select(2, idx).cpu().numpy().astype(np.float64))
+    ps = {k: np.ascontiguousarray(v[sel]) for k, v in p.items()}
+    u_ref, c_ref = oracle.conv1d_silu_prefill(col(x), ps["conv_w"], ps["conv_b"], None)
+    y_ref, s_ref = oracle.selective_scan_prefill(u_ref, col(dt), to_host(Bm).astype(np.float64),
+                                                 to_host(Cm).astype(np.float64), ps["A_log"], ps["D"],
+                                                 ps["dt_bias"], col(z), None)
+    assert_within(col(y), y_ref, "y (4 channels, all tokens)")
+    assert_within(to_host(s1[:, sel]), s_ref, "ssm state")
+    assert np.array_equal(to_host(c1[:, sel]), c_ref)
