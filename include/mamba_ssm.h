@@ -48,6 +48,9 @@
  *     (final state discarded).  state_out may equal state_in (in place); no
  *     other output may overlap any input or output.
  *   - The device must be compute capability 10.3 (GB300, sm_103a).
+ *   - The first call of a kernel variant on a device configures it (shared
+ *     memory opt-in, occupancy query); make that first call outside stream
+ *     capture, or capture in relaxed mode (cudaStreamCaptureModeRelaxed).
  */
 #ifndef MAMBA_SSM_H
 #define MAMBA_SSM_H
