@@ -381,7 +381,7 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
 // state element; the loads of up to kFoldBatch parts are issued before the
 // batch's stores (the stores could alias later loads for the compiler, so
 // without the batching every part would cost an L2 round trip).
-constexpr int kFoldBatch = 16;
+constexpr int kFoldBatch = 32;
 __global__ void __launch_bounds__(128) scan_fold_kernel(float* ws, int64_t BDN, int parts) {
   grid_dependency_begin();
   const int64_t i = (int64_t)blockIdx.x * 128 + threadIdx.x;
