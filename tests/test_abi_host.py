@@ -193,3 +193,43 @@ def test_m3_step_rejects_bad_arguments_on_host(lib):
     assert lib.mamba3_siso_step_batched(*args(P=1024, N=128)) == m.MAMBA_ERR_UNSUPPORTED
     assert lib.mamba3_siso_step_batched(*args(layer=1, L=1)) == m.MAMBA_ERR_INVALID_ARG
     assert lib.mamba3_siso_step_batched(*args(P=-1)) == m.MAMBA_ERR_INVALID_ARG
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "mamba_ssm.h"
+
+int main(void) {
+    int fails = 0;
+    if (strlen(mamba_version()) == 0) { puts("empty version"); ++fails; }
+    /* refused on the host, before any device work */
+    if (mamba_selective_scan_prefill(NULL, 0, MAMBA_F32, NULL, 0, NULL, 0, NULL, 0, NULL, 0, NULL, 0, MAMBA_F32,
+                                     NULL, NULL, NULL, NULL, NULL, 1, 8, 32, 3, NULL, 0, NULL) != MAMBA_ERR_UNSUPPORTED)
+        { puts("d_state 3 accepted"); ++fails; }
+    if (strstr(mamba_last_error(), "d_state") == NULL) { puts("no message"); ++fails; }
+    if (mamba_conv1d_silu_step(NULL, NULL, 7, NULL, 0, 1, NULL, NULL, 1, 8, 4, NULL) != MAMBA_ERR_INVALID_ARG)
+        { puts("bad dtype accepted"); ++fails; }
+    if (mamba_decode_graph_destroy(NULL) != MAMBA_OK) { puts("destroy(NULL)"); ++fails; }
+    if (mamba_selective_scan_prefill(NULL, 0, MAMBA_F32, NULL, 0, NULL, 0, NULL, 0, NULL, 0, NULL, 0, MAMBA_F32,
+                                     NULL, NULL, NULL, NULL, NULL, 0, 8, 32, 16, NULL, 0, NULL) != MAMBA_OK)
+        { puts("empty batch not a no-op"); ++fails; }
+    printf("%s\n", fails ? "FAIL" : "OK");
+    return fails;
+}
+"""
+
+
+def test_header_compiles_as_c99_and_library_links(lib, tmp_path):
+    """The ABI is plain C: a C99 program built with gcc against include/ and
+    linked to the library runs the host-side paths."""
+    src = tmp_path / "abi_check.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi_check"
+    pkg = os.path.dirname(B.LIB_PATH)
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                        "-o", str(exe), "-L", pkg, "-lmamba_ssm", f"-Wl,-rpath,{pkg}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0 and run.stdout.strip().endswith("OK"), run.stdout + run.stderr
