@@ -603,6 +603,51 @@ def test_mixer_prefill_T0_copies_both_states(cuda_lib):
     assert torch.equal(c0, c1) and torch.equal(s0, s1)
 
 
+@pytest.mark.parametrize("route", ["auto", "sequential"])
+@pytest.mark.parametrize("Bsz,T,Di,N", [(1, 1200, 96, 16), (2, 300, 64, 4), (1, 500, 40, 64)])
+def test_prefill_states_at_a_4_byte_offset_match_aligned_states(cuda_lib, route, Bsz, T, Di, N):
+    """States passed as views one float past a 16-byte boundary (in, out and in
+    place) give the same bits as aligned ones, for the scan and the fused
+    prefill, on the T-split and the one-pass route."""
+    m = cuda_lib
+    K = 4
+    assert m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) > 0
+    ws = None if route == "auto" else False
+    p = {k: to_dev(v) for k, v in _params(SEED + 5, Di, N, K).items()}
+    a = synth.prefill_inputs(SEED + 5, Bsz, T, Di, N, "f32", names=("x", "dt", "z", "B", "C"))
+    x, dt, z, Bm, Cm = (to_dev(a[k]) for k in ("x", "dt", "z", "B", "C"))
+    c0 = to_dev(synth.normal(SEED, "conv_state", (Bsz, Di, K), 0.5))
+    s0 = to_dev(synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5))
+
+    def scan(s_in, s_out):
+        y = torch.empty((Bsz, T, Di), device="cuda")
+        m.mamba_selective_scan_prefill(y, x, dt, Bm, Cm, p["A_log"], p["D"], p["dt_bias"], z, s_in, s_out,
+                                       workspace=ws)
+        return y
+
+    def fused(c_in, c_out, s_in, s_out):
+        y = torch.empty((Bsz, T, Di), device="cuda")
+        m.mamba_mixer_prefill(y, x, dt, Bm, Cm, p["conv_w"], p["A_log"], p["conv_b"], p["D"], p["dt_bias"], z,
+                              c_in, c_out, s_in, s_out, workspace=ws)
+        return y
+
+    s_ref = torch.empty_like(s0)
+    y_ref = scan(s0, s_ref)
+    s_off = _offset_like(torch.zeros_like(s0))
+    y_off = scan(_offset_like(s0), s_off)
+    s_inp = _offset_like(s0)
+    y_inp = scan(s_inp, s_inp)
+    c_ref, s_fref = torch.empty_like(c0), torch.empty_like(s0)
+    yf_ref = fused(c0, c_ref, s0, s_fref)
+    c_off, s_foff = _offset_like(torch.zeros_like(c0)), _offset_like(torch.zeros_like(s0))
+    yf_off = fused(_offset_like(c0), c_off, _offset_like(s0), s_foff)
+    torch.cuda.synchronize()
+    assert s_off.data_ptr() % 16 == 4 and c_off.data_ptr() % 16 == 4
+    assert torch.equal(y_ref, y_off) and torch.equal(s_ref, s_off)
+    assert torch.equal(y_ref, y_inp) and torch.equal(s_ref, s_inp)
+    assert torch.equal(yf_ref, yf_off) and torch.equal(c_ref, c_off) and torch.equal(s_fref, s_foff)
+
+
 # ------------------------------------------------------------ Mamba-3 step ----
 
 @pytest.mark.parametrize("Bsz,H,P,N,dtype,y_dtype,with_D", [
