@@ -316,6 +316,43 @@ def test_scan_delta_to_zero_keeps_state(cuda_lib, T, Di):
     assert_within(y, expect, "y = C.h0 + D u")
 
 
+@pytest.mark.parametrize("case", ["memoryless", "wide_dt", "mixed"])
+@pytest.mark.parametrize("route", ["auto", "sequential"])
+def test_scan_extreme_parameters_match_oracle(cuda_lib, case, route):
+    """Parameters at the edges of the recurrence, against the oracle:
+    - memoryless: A_log = 80 makes exp(delta A) = 0, so h_t = delta_t B_t u_t;
+    - wide_dt: dt + dt_bias spread over about -60..60, across the softplus
+      threshold, so delta runs from ~0 to ~60 and the decay from 1 to 0;
+    - mixed: half the channels memoryless, the other half with delta ~ 0."""
+    m = cuda_lib
+    Bsz, T, Di, N = 2, 700, 96, 16
+    a, p = _scan_inputs(Bsz, T, Di, N, "f32", seed=SEED + 21)
+    p = dict(p)
+    if case == "memoryless":
+        p["A_log"] = np.full((Di, N), 80.0, np.float32)
+    elif case == "wide_dt":
+        a["dt"] = synth.normal(SEED + 21, "dt", a["dt"].shape, 20.0, part=7)
+        p["dt_bias"] = np.zeros(Di, np.float32)
+    else:
+        p["A_log"] = p["A_log"].copy()
+        p["A_log"][::2] = 80.0
+        p["dt_bias"] = p["dt_bias"].copy()
+        p["dt_bias"][1::2] = -200.0
+    s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5)
+    ws = None if route == "auto" else False
+    y, s = _run_scan(m, a, p, "f32", "f32", True, s0, False, workspace=ws)
+    y_ref, s_ref = oracle.selective_scan_prefill(a["u"], a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                 p["dt_bias"], a["z"], s0)
+    assert_within(y, y_ref, f"{case} y")
+    assert_within(s, s_ref, f"{case} state")
+    if case == "memoryless":
+        # h_T = delta_{T-1} B_{T-1} u_{T-1}, with delta = softplus(dt + dt_bias)
+        v = a["dt"][:, -1, :].astype(np.float64) + p["dt_bias"].astype(np.float64)
+        delta = np.maximum(v, 0) + np.log1p(np.exp(-np.abs(v)))
+        h_last = (delta * a["u"][:, -1, :])[:, :, None] * a["B"][:, -1, None, :].astype(np.float64)
+        assert_within(s, h_last, "memoryless state")
+
+
 def test_scan_nan_stays_in_its_channel(cuda_lib):
     m = cuda_lib
     Bsz, T, Di, N = 2, 600, 128, 16
