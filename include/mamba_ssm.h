@@ -47,6 +47,12 @@
  *     NULL (no gate); state_in may be NULL (zero state); state_out may be NULL
  *     (final state discarded).  state_out may equal state_in (in place); no
  *     other output may overlap any input or output.
+ *   - Alignment: pointers need only their element's alignment (4 bytes for
+ *     f32, 2 for bf16).  Bases and row strides that are multiples of 16
+ *     bytes take the 16-byte vector and bulk-copy paths; any other layout
+ *     runs an element-wise path with the same arithmetic and the same bits.
+ *     Two buffers must be 16-byte aligned: a prefill workspace and the
+ *     Mamba-3 step's ssm_state (both refused with MAMBA_ERR_INVALID_ARG).
  *   - The device must be compute capability 10.3 (GB300, sm_103a).
  *   - The first call of a kernel variant on a device configures it (shared
  *     memory opt-in, occupancy query); make that first call outside stream
