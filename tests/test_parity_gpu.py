@@ -685,6 +685,46 @@ def test_prefill_states_at_a_4_byte_offset_match_aligned_states(cuda_lib, route,
     assert torch.equal(yf_ref, yf_off) and torch.equal(c_ref, c_off) and torch.equal(s_fref, s_foff)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("route", ["auto", "sequential"])
+def test_prefill_activations_one_element_off_alignment_match_aligned(cuda_lib, dtype, route):
+    """Every activation (x / u, dt, z, B, C and y) one element past a 16-byte
+    boundary takes the element-wise staging; the conv prefill, the scan and the
+    fused prefill give the same bits as with aligned buffers."""
+    m = cuda_lib
+    Bsz, T, Di, N, K = 2, 900, 128, 16, 4
+    assert m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) > 0
+    ws = None if route == "auto" else False
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    p = {k: to_dev(v) for k, v in _params(SEED + 6, Di, N, K).items()}
+    a = synth.prefill_inputs(SEED + 6, Bsz, T, Di, N, dtype, names=("x", "dt", "z", "B", "C"))
+    al = {k: to_dev(a[k], dtype) for k in ("x", "dt", "z", "B", "C")}
+    off = {k: _offset_like(v) for k, v in al.items()}
+    c0 = to_dev(synth.normal(SEED, "conv_state", (Bsz, Di, K), 0.5))
+    s0 = to_dev(synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5))
+
+    def run(t, shift):
+        mk = (lambda shape, dt_: _offset_like(torch.zeros(shape, device="cuda", dtype=dt_))) if shift else \
+             (lambda shape, dt_: torch.zeros(shape, device="cuda", dtype=dt_))
+        u, c1 = mk((Bsz, T, Di), td), torch.empty_like(c0)
+        m.mamba_conv1d_silu_prefill(u, t["x"], p["conv_w"], p["conv_b"], c0, c1)
+        y1, s1 = mk((Bsz, T, Di), torch.float32), torch.empty_like(s0)
+        m.mamba_selective_scan_prefill(y1, u, t["dt"], t["B"], t["C"], p["A_log"], p["D"], p["dt_bias"], t["z"],
+                                       s0, s1, workspace=ws)
+        y2, c2, s2 = mk((Bsz, T, Di), torch.float32), torch.empty_like(c0), torch.empty_like(s0)
+        m.mamba_mixer_prefill(y2, t["x"], t["dt"], t["B"], t["C"], p["conv_w"], p["A_log"], p["conv_b"], p["D"],
+                              p["dt_bias"], t["z"], c0, c2, s0, s2, workspace=ws)
+        return u, c1, y1, s1, y2, c2, s2
+
+    ref = run(al, False)
+    got = run(off, True)
+    torch.cuda.synchronize()
+    assert off["x"].data_ptr() % 16 != 0 and got[2].data_ptr() % 16 != 0
+    for name, r, g in zip(("u", "conv state", "y", "ssm state", "fused y", "fused conv state", "fused ssm state"),
+                          ref, got):
+        assert torch.equal(r, g), name
+
+
 # ------------------------------------------------------------ Mamba-3 step ----
 
 @pytest.mark.parametrize("Bsz,H,P,N,dtype,y_dtype,with_D", [
