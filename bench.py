@@ -608,6 +608,90 @@ def run_decode(torch, m, synth, device, peak, peak_src, n_steps=256):
     return out
 
 
+def run_prefill_vs_steps(torch, m, synth, device, lengths=(128, 512, 2048), prompt=5, n_layers=24):
+    """Parallel prefill against step-by-step prefill on the 130m layer shape
+    (batch 1, d_inner 1536, d_state 16, d_conv 4, f32): one mamba_mixer_prefill
+    call over T tokens against T fused T=1 steps replayed by the library's
+    decode graph; and a `prompt`-token prompt through `n_layers` layers both
+    ways.  Both paths start from the same seeded state; their final states and
+    y agree within 2e-4 (1 + |ref|), checked here before timing."""
+    wl = synth.WORKLOADS[1]
+    Di, N, K = wl.d_inner, wl.d_state, wl.d_conv
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(device)
+
+    def time_fn(fn, reps=5):
+        fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def setup(T, L):
+        params = [{k: dev(v) for k, v in synth.mixer_params(wl.seed, Di, N, K, layer=l).items()} for l in range(L)]
+        x = synth.torch_normal((L, T, 1, Di), 1.0, wl.seed + 31, device)
+        z = synth.torch_normal((L, T, 1, Di), 1.0, wl.seed + 32, device)
+        dt = synth.torch_normal((L, T, 1, Di), 0.1, wl.seed + 33, device)
+        Bm = synth.torch_normal((L, T, 1, N), 1.0, wl.seed + 34, device)
+        Cm = synth.torch_normal((L, T, 1, N), 1.0, wl.seed + 35, device)
+        c0 = synth.torch_normal((L, 1, Di, K), 0.5, wl.seed + 36, device)
+        s0 = synth.torch_normal((L, 1, Di, N), 0.5, wl.seed + 37, device)
+        return params, x, z, dt, Bm, Cm, c0, s0
+
+    def both(T, L):
+        params, x, z, dt, Bm, Cm, c0, s0 = setup(T, L)
+        yp = torch.empty((L, T, 1, Di), device=device)
+        cp, sp = torch.empty_like(c0), torch.empty_like(s0)
+
+        def prefill():
+            for l in range(L):
+                p = params[l]
+                m.mamba_mixer_prefill(yp[l].view(1, T, Di), x[l].view(1, T, Di), dt[l].view(1, T, Di),
+                                      Bm[l].view(1, T, N), Cm[l].view(1, T, N), p["conv_w"], p["A_log"],
+                                      p["conv_b"], p["D"], p["dt_bias"], z[l].view(1, T, Di), c0[l], cp[l],
+                                      s0[l], sp[l])
+        ys = torch.empty_like(yp)
+        cs, ss = c0.clone(), s0.clone()
+        io = [[{"y": ys[l, t], "x": x[l, t], "dt": dt[l, t], "z": z[l, t], "Bm": Bm[l, t], "Cm": Cm[l, t]}
+               for l in range(L)] for t in range(T)]
+        with m.DecodeGraph(params, io, cs, ss) as g:
+            g.launch()
+            torch.cuda.synchronize()
+            prefill()
+            torch.cuda.synchronize()
+            for got, ref, nm in ((ys, yp, "y"), (cs, cp, "conv state"), (ss, sp, "ssm state")):
+                err = ((got - ref).abs() / (1.0 + ref.abs())).max().item()
+                if not err <= 2e-4:
+                    raise RuntimeError(f"step-by-step and parallel prefill disagree on {nm}: {err:.3g}")
+
+            def steps():
+                cs.copy_(c0)
+                ss.copy_(s0)
+                g.launch()
+            reset_ms = time_fn(lambda: (cs.copy_(c0), ss.copy_(s0)))
+            step_ms = time_fn(steps) - reset_ms
+        pre_g = capture(torch, prefill)  # both paths replay graphs: no host launch cost in either
+        pre_ms = time_fn(pre_g.replay)
+        del pre_g
+        return pre_ms, step_ms
+
+    out = {"workload": "mamba130m-layer, batch 1", "unit": "ms",
+           "method": "parallel: mamba_mixer_prefill per layer; step-by-step: T x layers fused T=1 steps replayed "
+                     "by mamba_decode_graph (state reset excluded); both as CUDA graphs, L2-resident inputs",
+           "single_layer": {}}
+    for T in lengths:
+        pre_ms, step_ms = both(T, 1)
+        out["single_layer"][f"T{T}"] = {"prefill_ms": round(pre_ms, 5), "steps_ms": round(step_ms, 5),
+                                        "speedup": round(step_ms / pre_ms, 1)}
+    pre_ms, step_ms = both(prompt, n_layers)
+    out[f"prompt{prompt}_layers{n_layers}"] = {"prefill_ms": round(pre_ms, 5), "steps_ms": round(step_ms, 5),
+                                               "extra_ms_step_path": round(step_ms - pre_ms, 5)}
+    return out
+
+
 def run_m3_decode(torch, m, device, peak, peak_src, n_steps=16, L=24, Bsz=128, H=24, P=64, N=64):
     """Mamba-3 SISO T=1 decode: L layers x batch B, H heads of headdim P and
     d_state N (a synthetic shape: the pages give none), graph-replayed."""
@@ -805,6 +889,7 @@ def main():
     if not args.no_extra:
         extra["decode_130m_b128_l24"] = run_decode(torch, m, synth, device, peak, peak_src)
         extra["decode_mamba3_siso"] = run_m3_decode(torch, m, device, peak, peak_src)
+        extra["prefill_vs_steps"] = run_prefill_vs_steps(torch, m, synth, device)
         r3 = run_prefill(torch, m, synth, 3, 50, 3, device, None, None, host_inputs=False)
         extra["prefill_2p8b_bf16"] = {
             "workload": r3["wl"].name, "value": round(r3["tokens_per_step"] / (r3["ms_per_step"] * 1e-3), 1),
