@@ -232,18 +232,27 @@ def mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) -> int:
     return int(v)
 
 
-_ws_cache = {}
+_ws_cache = {}    # (device index, stream handle) -> uint8 scratch tensor
+_ws_retired = []  # outgrown scratch tensors, kept alive (see _workspace)
 
 
-def _workspace(device, nbytes):
-    """A per-device scratch buffer reused across calls (grown on demand)."""
+def _workspace(device, nbytes, stream_handle):
+    """A scratch buffer per (device, stream), reused across calls and grown on
+    demand (at least doubling).  Calls on different streams never share one, so
+    concurrent streams cannot overwrite each other's carries.  An outgrown
+    buffer is kept alive rather than freed: a CUDA graph captured earlier may
+    still hold its address."""
     import torch
 
-    key = device.index if device.index is not None else torch.cuda.current_device()
+    dev = device.index if device.index is not None else torch.cuda.current_device()
+    key = (dev, int(stream_handle))
     with _lock:
         buf = _ws_cache.get(key)
         if buf is None or buf.numel() < nbytes:
-            buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+            size = max(nbytes, 1 << 20, 2 * buf.numel() if buf is not None else 0)
+            if buf is not None:
+                _ws_retired.append(buf)
+            buf = torch.empty(size, dtype=torch.uint8, device=torch.device("cuda", dev))
             _ws_cache[key] = buf
     return buf
 
@@ -255,10 +264,10 @@ def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, 
 
     y, u, dt, z: [B, T, Di] (row-strided views allowed); Bm, Cm: [B, T, N];
     A_log: [Di, N]; D, dt_bias: [Di]; states: [B, Di, N] f32.
-    workspace: None = a cached per-device buffer sized by
-    mamba_selective_scan_workspace_bytes (shared: calls on concurrent streams
-    should pass their own); False = none (one sequential pass); or a uint8
-    cuda tensor."""
+    workspace: None = a cached buffer per (device, stream) sized by
+    mamba_selective_scan_workspace_bytes; False = none (one sequential pass);
+    or a uint8 cuda tensor (16-byte aligned), which the caller must not reuse
+    on another stream while this call may still be running."""
     Bsz, T, Di = u.shape
     N = A_log.shape[1]
     _f32_param(A_log, "A_log", (Di, N))
@@ -275,9 +284,10 @@ def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, 
     for t, nm in ((Bm, "Bm"), (Cm, "Cm")):
         if tuple(t.shape) != (Bsz, T, N):
             raise ValueError(f"{nm} must be [B, T, N]")
+    st = _stream(stream, u)
     if workspace is None:
         need = mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
-        ws = _workspace(u.device, need) if need > 0 else None
+        ws = _workspace(u.device, need, st) if need > 0 else None
     elif workspace is False:
         ws = None
     else:
@@ -289,7 +299,7 @@ def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, 
         _ptr(dt), _rows_ld(dt, "dt"), _ptr(z), _rows_ld(z, "z") if z is not None else 0,
         _ptr(Bm), _rows_ld(Bm, "Bm"), _ptr(Cm), _rows_ld(Cm, "Cm"), _dtype_code(u),
         _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
-        Bsz, T, Di, N, ws_ptr, ws_bytes, _stream(stream, u)))
+        Bsz, T, Di, N, ws_ptr, ws_bytes, st))
 
 
 def mamba_mixer_prefill(y, x, dt, Bm, Cm, conv_w, A_log, conv_b=None, D=None, dt_bias=None, z=None,
@@ -323,9 +333,10 @@ def mamba_mixer_prefill(y, x, dt, Bm, Cm, conv_w, A_log, conv_b=None, D=None, dt
     for t, nm in ((Bm, "Bm"), (Cm, "Cm")):
         if tuple(t.shape) != (Bsz, T, N):
             raise ValueError(f"{nm} must be [B, T, N]")
+    st = _stream(stream, x)
     if workspace is None:
         need = mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
-        ws = _workspace(x.device, need) if need > 0 else None
+        ws = _workspace(x.device, need, st) if need > 0 else None
     elif workspace is False:
         ws = None
     else:
@@ -338,7 +349,7 @@ def mamba_mixer_prefill(y, x, dt, Bm, Cm, conv_w, A_log, conv_b=None, D=None, dt
         _ptr(Bm), _rows_ld(Bm, "Bm"), _ptr(Cm), _rows_ld(Cm, "Cm"), _dtype_code(x),
         _ptr(conv_w), _ptr(conv_b), _ptr(conv_state_in), _ptr(conv_state_out),
         _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state_in), _ptr(ssm_state_out),
-        Bsz, T, Di, K, N, ws_ptr, ws_bytes, _stream(stream, x)))
+        Bsz, T, Di, K, N, ws_ptr, ws_bytes, st))
 
 
 def mamba3_siso_step_batched(y, x, k, q, alpha, beta, gamma, ssm_state, k_state, v_state, layer, D=None, *,

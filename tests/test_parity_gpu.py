@@ -725,6 +725,44 @@ def test_prefill_activations_one_element_off_alignment_match_aligned(cuda_lib, d
         assert torch.equal(r, g), name
 
 
+def test_prefills_on_two_streams_with_the_cached_workspace_match_serial(cuda_lib):
+    """T-split prefills enqueued on two streams at once, each with the
+    binding's cached workspace, give the same bits as the same calls run one
+    after the other: the cache keeps one workspace per stream."""
+    m = cuda_lib
+    Bsz, T, Di, N = 1, 2048, 256, 16
+    assert m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) > 0
+    p = {k: to_dev(v) for k, v in _params(SEED + 7, Di, N, 4).items()}
+    cases = []
+    for i in range(2):
+        a = synth.prefill_inputs(SEED + 70 + i, Bsz, T, Di, N, "f32", names=("x", "dt", "z", "B", "C"))
+        cases.append({k: to_dev(a[k]) for k in ("x", "dt", "z", "B", "C")})
+
+    def call(t, y, s_out, stream=None):
+        m.mamba_mixer_prefill(y, t["x"], t["dt"], t["B"], t["C"], p["conv_w"], p["A_log"], p["conv_b"], p["D"],
+                              p["dt_bias"], t["z"], None, None, None, s_out, stream=stream)
+
+    ref = []
+    for t in cases:
+        y, so = torch.empty((Bsz, T, Di), device="cuda"), torch.empty((Bsz, Di, N), device="cuda")
+        call(t, y, so)
+        torch.cuda.synchronize()
+        ref.append((y, so))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [[(torch.empty((Bsz, T, Di), device="cuda"), torch.empty((Bsz, Di, N), device="cuda"))
+             for _ in range(6)] for _ in range(2)]
+    for st in streams:
+        st.wait_stream(torch.cuda.current_stream())
+    for r in range(6):  # interleaved, so that the two streams' calls overlap on the GPU
+        for i in range(2):
+            with torch.cuda.stream(streams[i]):
+                call(cases[i], *outs[i][r])
+    torch.cuda.synchronize()
+    for i in range(2):
+        for y, so in outs[i]:
+            assert torch.equal(y, ref[i][0]) and torch.equal(so, ref[i][1])
+
+
 # ------------------------------------------------------------ Mamba-3 step ----
 
 @pytest.mark.parametrize("Bsz,H,P,N,dtype,y_dtype,with_D", [
