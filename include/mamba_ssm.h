@@ -232,13 +232,7 @@ MAMBA_API int mamba_mixer_step_batched(void* y, int y_dtype, const void* x, cons
  *   conv_state_in / _out [B][Di][K], ssm_state_in / _out [B][Di][N]: f32; an _in
  *   may be NULL (zero state), an _out NULL (discarded), and each _out may equal
  *   its _in (in place).
- *   workspace: device scratch (16-byte aligned) of workspace_bytes bytes, or
- *   NULL / 0.  mamba_mixer_prefill_workspace_bytes() gives the size of the
- *   fastest plan.  With at least mamba_selective_scan_workspace_bytes() the
- *   call still splits T, but its second pass recomputes the conv and softplus;
- *   with less it runs one sequential pass.  All three give the same bits.
- *   Contents on entry are ignored; calls that share a workspace must not
- *   overlap in time.
+ *   workspace: as for mamba_selective_scan_prefill (same size query).
  * d_conv must be 4 (MAMBA_ERR_UNSUPPORTED otherwise: use the two calls).
  * Errors: as for the two separate prefills.
  */
@@ -251,19 +245,6 @@ MAMBA_API int mamba_mixer_prefill(void* y, int64_t ld_y, int y_dtype, const void
                                   const float* ssm_state_in, float* ssm_state_out, int64_t B,
                                   int64_t T, int64_t Di, int64_t K, int64_t N, void* workspace,
                                   int64_t workspace_bytes, void* stream);
-
-/*
- * Workspace bytes for the fastest plan of mamba_mixer_prefill at this shape on
- * the current device (d_conv 4; act_dtype MAMBA_F32 or MAMBA_BF16).  This
- * library's addition, like the scan's query.  It returns 0 for shapes that run
- * as one pass.  For narrow shapes split along T, it covers the carries between
- * the parts.  With f32 activations and when both fit in 48 MiB, it adds two
- * [B][T][Di] f32 buffers: the first pass stores each token's u and delta
- * there, and the second pass reads them instead of recomputing the conv and
- * softplus.  Negative MAMBA_ERR_* on bad sizes or no usable device.
- */
-MAMBA_API int64_t mamba_mixer_prefill_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N,
-                                                      int act_dtype);
 
 /*
  * mamba3_siso_step_batched - batched T=1 step of the Mamba-3 SISO mixer (the

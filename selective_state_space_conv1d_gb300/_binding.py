@@ -30,7 +30,6 @@ ABI_SYMBOLS = (
     "mamba_conv1d_silu_step",
     "mamba_selective_scan_prefill",
     "mamba_selective_scan_workspace_bytes",
-    "mamba_mixer_prefill_workspace_bytes",
     "mamba_selective_scan_prefill_noalloc",
     "mamba_ssm_step_batched",
     "mamba_mixer_step_batched",
@@ -79,8 +78,6 @@ def load(path: str | None = None):
         lib.mamba_selective_scan_prefill_noalloc.restype = ctypes.c_int
         lib.mamba_selective_scan_workspace_bytes.argtypes = [i64, i64, i64, i64]
         lib.mamba_selective_scan_workspace_bytes.restype = i64
-        lib.mamba_mixer_prefill_workspace_bytes.argtypes = [i64, i64, i64, i64, ctypes.c_int]
-        lib.mamba_mixer_prefill_workspace_bytes.restype = i64
         lib.mamba_ssm_step_batched.argtypes = [vp, i32, vp, vp, vp, vp, vp, i32, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp]
         lib.mamba_mixer_step_batched.argtypes = ([vp, i32, vp, vp, vp, vp, vp, i32] + [vp] * 7
                                                  + [i64, i64, i64, i64, i64, i64, vp])
@@ -235,18 +232,6 @@ def mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) -> int:
     return int(v)
 
 
-def mamba_mixer_prefill_workspace_bytes(Bsz, T, Di, N, act_dtype=None) -> int:
-    """Workspace bytes of mamba_mixer_prefill's fastest plan on the current
-    device (0: none); act_dtype a torch dtype (float32 or bfloat16)."""
-    import torch
-
-    code = MAMBA_BF16 if act_dtype == torch.bfloat16 else MAMBA_F32
-    v = load().mamba_mixer_prefill_workspace_bytes(Bsz, T, Di, N, code)
-    if v < 0:
-        raise MambaError(int(v), mamba_last_error())
-    return int(v)
-
-
 _ws_cache = {}    # (device index, stream handle) -> uint8 scratch tensor
 _ws_retired = []  # outgrown scratch tensors, kept alive (see _workspace)
 
@@ -324,11 +309,8 @@ def mamba_mixer_prefill(y, x, dt, Bm, Cm, conv_w, A_log, conv_b=None, D=None, dt
 
     y, x, dt, z: [B, T, Di] (row-strided views allowed); Bm, Cm: [B, T, N];
     conv_w: [Di, 4]; A_log: [Di, N]; conv_b, D, dt_bias: [Di]; conv states
-    [B, Di, 4] and ssm states [B, Di, N], f32.  workspace: None = a cached
-    buffer per (device, stream) sized by mamba_mixer_prefill_workspace_bytes;
-    False = none (one sequential pass); or a uint8 cuda tensor (16-byte
-    aligned; with less than the fastest plan's size the call takes a slower
-    plan, with the same bits).  Equals mamba_conv1d_silu_prefill followed by
+    [B, Di, 4] and ssm states [B, Di, N], f32.  workspace: as for
+    mamba_selective_scan_prefill.  Equals mamba_conv1d_silu_prefill followed by
     mamba_selective_scan_prefill, bit for bit."""
     Bsz, T, Di = x.shape
     N = A_log.shape[1]
@@ -353,7 +335,7 @@ def mamba_mixer_prefill(y, x, dt, Bm, Cm, conv_w, A_log, conv_b=None, D=None, dt
             raise ValueError(f"{nm} must be [B, T, N]")
     st = _stream(stream, x)
     if workspace is None:
-        need = mamba_mixer_prefill_workspace_bytes(Bsz, T, Di, N, x.dtype)
+        need = mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
         ws = _workspace(x.device, need, st) if need > 0 else None
     elif workspace is False:
         ws = None

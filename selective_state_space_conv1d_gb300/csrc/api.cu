@@ -463,22 +463,6 @@ int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, i
   return mamba::scan_workspace_bytes(B, Di, N, mamba::scan_parts(B, T, Di, N, dev));
 }
 
-int64_t mamba_mixer_prefill_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N, int act_dtype) {
-  if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size");
-  if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
-  if (act_dtype != MAMBA_F32 && act_dtype != MAMBA_BF16) return fail(MAMBA_ERR_INVALID_ARG, "act_dtype %d", act_dtype);
-  if (!sizes_ok(B, T, Di) || !sizes_ok(B, Di, N)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
-  if (B == 0 || Di == 0 || T == 0) {
-    ok();
-    return 0;
-  }
-  mamba::DeviceInfo dev;
-  int rc = current_device(&dev);
-  if (rc) return rc;
-  ok();
-  return mamba::mixer_workspace_bytes(B, T, Di, N, act_dtype == MAMBA_BF16, dev);
-}
-
 int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const void* dt, const void* z,
                            const void* Bm, const void* Cm, int in_dtype, const float* A_log,
                            const float* D, const float* dt_bias, float* ssm_state, int64_t layer,

@@ -112,18 +112,9 @@ struct ScanPlan {
   int act_vec;  // u/dt/z staged with 16-byte copies (else element loads)
   int bc_vec;   // B/C staged with 16-byte copies
   int64_t workspace_bytes;
-  // fused conv, f32 storage, T split: the state-only pass hands u and delta to
-  // the full pass through the workspace (byte offsets of the two [B][T][Di] f32
-  // buffers), and the full pass stages them (16-byte copies if act_vec_handoff)
-  int handoff = 0;
-  int64_t hand_u_offset = 0, hand_d_offset = 0;
-  int act_vec_handoff = 0;
 };
 int scan_parts(int64_t B, int64_t T, int64_t Di, int64_t N, const DeviceInfo& dev);
 int64_t scan_workspace_bytes(int64_t B, int64_t Di, int64_t N, int parts);
-// workspace of the fused prefill's fastest plan: the T-split carries plus,
-// where the plan hands u and delta over, the two hand-off buffers
-int64_t mixer_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N, bool act_bf16, const DeviceInfo& dev);
 ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t workspace_bytes);
 cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& plan, float* ws,
                                           const DeviceInfo& dev, cudaStream_t stream);

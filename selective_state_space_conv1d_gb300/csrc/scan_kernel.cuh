@@ -83,8 +83,6 @@ struct Work {
   int64_t part_len;    // rows per part (the last part may be shorter)
   int64_t n_tiles;     // channel tiles per batch row
   int64_t grid_parts;  // parts covered by this launch's grid
-  float* hand_u = nullptr;  // hand-off: u and delta of every (b, t, c), [B][T][Di] f32,
-  float* hand_d = nullptr;  // written by the state-only pass, read by the full pass
 };
 
 enum Mode { kSequential = 0, kPass1 = 1, kPass2 = 2 };
@@ -101,13 +99,10 @@ struct RowS {
 
 // KC > 0: the conv1d + SiLU of width KC is fused in; the staged "u" is x, and
 // each lane carries the last KC-1 inputs of its channel from row to row.
-// YB: the y dtype is bf16; VEC: u/dt/z and B/C stage as 16-byte copies.
-// HO (hand-off, f32 storage): the state-only pass also stores each row's u and
-// delta, covers every part and writes the new conv state; the full pass then
-// stages u and delta from those buffers (KC = 0, no softplus).  All are
-// compile-time choices: a runtime flag in the unrolled row loop costs the
+// YB: the y dtype is bf16; VEC: u/dt/z and B/C stage as 16-byte copies.  Both
+// are compile-time choices: a runtime flag in the unrolled row loop costs the
 // scheduler's freedom across rows (measured 5-17% on GB300).
-template <int N, typename Tin, int MODE, bool GATE, int KC, bool YB = false, bool VEC = false, bool HO = false>
+template <int N, typename Tin, int MODE, bool GATE, int KC, bool YB = false, bool VEC = false>
 __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int act_vec_rt, int bc_vec_rt) {
   const bool act_vec = VEC || act_vec_rt;
   const bool bc_vec = VEC || bc_vec_rt;
@@ -287,7 +282,6 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
     if (k + kStages - 1 < nchunks) issue(k + kStages - 1, (int)((k + kStages - 1) % kStages));
     cp_async_commit();
 
-    const int64_t hand_row = (b * T + t_begin + k * kTC) * Di + c;  // hand-off: this lane, row 0 of chunk k
     const Tin* su = &sm.act[stage][0][0][0];
     const Tin* sdt = &sm.act[stage][1][0][0];
     const Tin* sz = &sm.act[stage][GATE ? 2 : 0][0][0];
@@ -304,15 +298,7 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
         if (KC > 1) cwin[KW - 1] = s.u;
         s.u = to_f32(from_f32<Tin>(silu_f(conv_taps<KC>(cw, sw, cbias))));
       }
-      if constexpr (HO && MODE == kPass2) {
-        s.delta = to_f32(sdt[r * kLanes + lane]);  // handed over by the state-only pass
-      } else {
-        s.delta = softplus_f(to_f32(sdt[r * kLanes + lane]) + dtb);
-      }
-      if constexpr (HO && MODE == kPass1) {
-        w.hand_u[hand_row + r * Di] = s.u;
-        w.hand_d[hand_row + r * Di] = s.delta;
-      }
+      s.delta = softplus_f(to_f32(sdt[r * kLanes + lane]) + dtb);
       s.du = s.delta * s.u;
       s.g = (MODE != kPass1 && GATE) ? silu_f(to_f32(sz[r * kLanes + lane])) : 1.0f;
       return s;
@@ -378,7 +364,7 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
   grid_dependents_launch();  // main loop done: the next grid may be scheduled
 
   if (!active) return;
-  if (MODE == kPass1 && (!HO || part < w.parts - 1)) {  // (the hand-off pass also scans the last part)
+  if (MODE == kPass1) {
     float* Pj = w.ws + BDN * (1 + 2 * part) + srow;
     float* Hj = w.ws + BDN * (2 + 2 * part) + srow;
 #pragma unroll
@@ -392,10 +378,9 @@ __global__ void __launch_bounds__(kLanes) scan_kernel(ScanArgs a, Work w, int ac
   }
   if constexpr (KC > 0) {
     // new conv state = inputs T..T+KC-1 of the extended sequence; written by
-    // part 0 of the last pass that has the conv fused in (the final pass, or
-    // the hand-off pass), the only reader of conv_state_in in that pass
+    // part 0 of the final pass, the only reader of conv_state_in in that pass
     // (every read before any write: in-place safe)
-    if ((MODE != kPass1 || HO) && part == 0 && a.conv_state_out) {
+    if (MODE != kPass1 && part == 0 && a.conv_state_out) {
       float fin[KC];
 #pragma unroll
       for (int k = 0; k < KC; ++k) fin[k] = conv_input(T + k);
@@ -435,82 +420,39 @@ __global__ void __launch_bounds__(128) scan_fold_kernel(float* ws, int64_t BDN, 
   }
 }
 
-template <int N, typename Tin, int MODE, bool GATE, bool YB, bool VEC, bool HO>
+template <int N, typename Tin, int MODE, bool GATE, bool YB, bool VEC>
 cudaError_t launch_mode_v(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
   const int64_t blocks = w.n_tiles * a.B * w.grid_parts;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  const dim3 grid((unsigned)blocks), block(kLanes);
-  if constexpr (HO && MODE == kPass2) {  // stages the handed-over u and delta: no conv, no softplus
-    return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 0, YB, VEC, true>, grid, block, 0, stream, a, w,
-                      p.act_vec, p.bc_vec);
-  } else if constexpr (HO) {  // the state-only pass that computes and hands over u and delta
-    if (a.K != 4) return cudaErrorInvalidValue;
-    return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 4, YB, VEC, true>, grid, block, 0, stream, a, w,
-                      p.act_vec, p.bc_vec);
-  } else {
-    if (a.K == 4)
-      return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 4, YB, VEC>, grid, block, 0, stream, a, w,
-                        p.act_vec, p.bc_vec);
-    if (a.K != 0) return cudaErrorInvalidValue;
-    return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 0, YB, VEC>, grid, block, 0, stream, a, w,
-                      p.act_vec, p.bc_vec);
-  }
+  if (a.K == 4)
+    return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 4, YB, VEC>, dim3((unsigned)blocks), dim3(kLanes), 0,
+                      stream, a, w, p.act_vec, p.bc_vec);
+  if (a.K != 0) return cudaErrorInvalidValue;
+  return launch_pdl(false, scan_kernel<N, Tin, MODE, GATE, 0, YB, VEC>, dim3((unsigned)blocks), dim3(kLanes), 0,
+                    stream, a, w, p.act_vec, p.bc_vec);
 }
 
-template <int N, typename Tin, int MODE, bool GATE, bool YB, bool HO>
+template <int N, typename Tin, int MODE, bool GATE, bool YB>
 cudaError_t launch_mode_y(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
   // the 16-byte staging path exists only where every row can take it
   constexpr bool kCanVec = N * sizeof(Tin) >= 16;
   if constexpr (kCanVec) {
-    if (p.act_vec && p.bc_vec) return launch_mode_v<N, Tin, MODE, GATE, YB, true, HO>(a, w, p, stream);
+    if (p.act_vec && p.bc_vec) return launch_mode_v<N, Tin, MODE, GATE, YB, true>(a, w, p, stream);
   }
-  return launch_mode_v<N, Tin, MODE, GATE, YB, false, HO>(a, w, p, stream);
+  return launch_mode_v<N, Tin, MODE, GATE, YB, false>(a, w, p, stream);
 }
 
-template <int N, typename Tin, int MODE, bool GATE, bool HO>
+template <int N, typename Tin, int MODE, bool GATE>
 cudaError_t launch_mode(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t stream) {
-  if constexpr (MODE == kPass1) return launch_mode_y<N, Tin, MODE, GATE, false, HO>(a, w, p, stream);  // no y
-  return a.y_bf16 ? launch_mode_y<N, Tin, MODE, GATE, true, HO>(a, w, p, stream)
-                  : launch_mode_y<N, Tin, MODE, GATE, false, HO>(a, w, p, stream);
+  if constexpr (MODE == kPass1) return launch_mode_y<N, Tin, MODE, GATE, false>(a, w, p, stream);  // no y
+  return a.y_bf16 ? launch_mode_y<N, Tin, MODE, GATE, true>(a, w, p, stream)
+                  : launch_mode_y<N, Tin, MODE, GATE, false>(a, w, p, stream);
 }
 
-template <int N, typename Tin, int MODE, bool HO>
+template <int N, typename Tin, int MODE>
 cudaError_t launch_out(const ScanArgs& a, const Work& w, const ScanPlan& p, cudaStream_t s) {
-  return a.z != nullptr ? launch_mode<N, Tin, MODE, true, HO>(a, w, p, s)
-                        : launch_mode<N, Tin, MODE, false, HO>(a, w, p, s);
-}
-
-// The T split: state-only pass, fold, full pass.  With the hand-off the
-// state-only pass covers every part and stores u and delta, and the full pass
-// stages them instead of x and dt.
-template <int N, typename Tin, bool HO>
-cudaError_t launch_split(const ScanArgs& a, const ScanPlan& p, Work w, cudaStream_t stream) {
-  if (HO) {
-    char* base = reinterpret_cast<char*>(w.ws);
-    w.hand_u = reinterpret_cast<float*>(base + p.hand_u_offset);
-    w.hand_d = reinterpret_cast<float*>(base + p.hand_d_offset);
-  }
-  w.grid_parts = HO ? p.parts : p.parts - 1;
-  cudaError_t e = launch_mode<N, Tin, kPass1, false, HO>(a, w, p, stream);
-  if (e != cudaSuccess) return e;
-  const int64_t BDN = a.B * a.Di * N;
-  if ((BDN + 127) / 128 > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
-  e = launch_pdl(false, scan_fold_kernel, dim3((unsigned)((BDN + 127) / 128)), dim3(128), 0, stream, w.ws, BDN,
-                 p.parts);
-  if (e != cudaSuccess) return e;
-  w.grid_parts = p.parts;
-  if constexpr (HO) {
-    ScanArgs a2 = a;
-    a2.u = w.hand_u;
-    a2.ld_u = a.Di;
-    a2.dt = w.hand_d;
-    a2.ld_dt = a.Di;
-    a2.K = 0;
-    ScanPlan p2 = p;
-    p2.act_vec = p.act_vec_handoff;
-    return launch_out<N, Tin, kPass2, true>(a2, w, p2, stream);
-  }
-  return launch_out<N, Tin, kPass2, false>(a, w, p, stream);
+  return a.z != nullptr ? launch_mode<N, Tin, MODE, true>(a, w, p, s)
+                        : launch_mode<N, Tin, MODE, false>(a, w, p, s);
 }
 
 template <int N, typename Tin>
@@ -522,12 +464,18 @@ cudaError_t launch_n(const ScanArgs& a, const ScanPlan& p, float* ws, cudaStream
   w.n_tiles = (a.Di + kLanes - 1) / kLanes;
   if (p.parts <= 1) {
     w.grid_parts = 1;
-    return launch_out<N, Tin, kSequential, false>(a, w, p, stream);
+    return launch_out<N, Tin, kSequential>(a, w, p, stream);
   }
-  if constexpr (std::is_same<Tin, float>::value) {
-    if (p.handoff) return launch_split<N, Tin, true>(a, p, w, stream);
-  }
-  return launch_split<N, Tin, false>(a, p, w, stream);
+  w.grid_parts = p.parts - 1;
+  cudaError_t e = launch_mode<N, Tin, kPass1, false>(a, w, p, stream);
+  if (e != cudaSuccess) return e;
+  const int64_t BDN = a.B * a.Di * N;
+  if ((BDN + 127) / 128 > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
+  e = launch_pdl(false, scan_fold_kernel, dim3((unsigned)((BDN + 127) / 128)), dim3(128), 0, stream, ws, BDN,
+                 p.parts);
+  if (e != cudaSuccess) return e;
+  w.grid_parts = p.parts;
+  return launch_out<N, Tin, kPass2>(a, w, p, stream);
 }
 
 }  // namespace

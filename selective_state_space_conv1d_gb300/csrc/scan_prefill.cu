@@ -103,26 +103,6 @@ int scan_parts(int64_t B, int64_t T, int64_t Di, int64_t N, const DeviceInfo& de
   return best_p;
 }
 
-namespace {
-// The hand-off keeps u and delta (8 bytes per (t, c)) for the full pass.  It is
-// used only while the two buffers are small enough to stay in L2 between the
-// passes, where writing and re-reading them costs less than recomputing the
-// conv and softplus (measured on the 130m layer); larger shapes recompute.
-constexpr int64_t kHandoffMaxBytes = 48ll << 20;
-inline int64_t round256(int64_t x) { return (x + 255) & ~int64_t(255); }
-inline int64_t handoff_buffer_bytes(int64_t B, int64_t T, int64_t Di) { return round256(B * T * Di * 4); }
-inline bool handoff_fits(int64_t B, int64_t T, int64_t Di) {
-  return 2 * handoff_buffer_bytes(B, T, Di) <= kHandoffMaxBytes;
-}
-}  // namespace
-
-int64_t mixer_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N, bool act_bf16, const DeviceInfo& dev) {
-  const int parts = scan_parts(B, T, Di, N, dev);
-  const int64_t carries = scan_workspace_bytes(B, Di, N, parts);
-  if (parts <= 1 || act_bf16 || !handoff_fits(B, T, Di)) return carries;
-  return round256(carries) + 2 * handoff_buffer_bytes(B, T, Di);
-}
-
 ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t workspace_bytes) {
   ScanPlan p;
   const int es = a.in_bf16 ? 2 : 4;
@@ -140,18 +120,6 @@ ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t w
     p.workspace_bytes = 0;
   }
   p.part_len = p.parts > 1 ? (a.T + p.parts - 1) / p.parts : a.T;
-  if (p.parts > 1 && a.K == 4 && !a.in_bf16 && handoff_fits(a.B, a.T, a.Di)) {
-    const int64_t hb = handoff_buffer_bytes(a.B, a.T, a.Di);
-    const int64_t need = round256(p.workspace_bytes) + 2 * hb;
-    if (need <= workspace_bytes) {  // with only the carries' room, the full pass recomputes
-      p.handoff = 1;
-      p.hand_u_offset = round256(p.workspace_bytes);
-      p.hand_d_offset = p.hand_u_offset + hb;
-      p.workspace_bytes = need;
-      // the buffers start 16-byte aligned with rows of Di floats; z keeps its layout
-      p.act_vec_handoff = a.Di % 4 == 0 && (!a.z || (aligned(a.z, 16) && (a.ld_z * 4) % 16 == 0));
-    }
-  }
   return p;
 }
 

@@ -626,51 +626,6 @@ def test_mixer_prefill_equals_conv_then_scan_bitwise(cuda_lib, inplace, Bsz, T, 
         assert np.array_equal(to_host(c2), c_ref)
 
 
-@pytest.mark.parametrize("Bsz,T,Di,N,gate,strided", [
-    (1, 2048, 256, 16, True, False),
-    (1, 999, 130, 4, True, True),    # d_inner % 4 != 0: the handed-over rows stage element by element
-    (2, 1500, 96, 16, False, False),
-    (1, 3001, 64, 64, True, True),
-])
-def test_mixer_prefill_handoff_matches_recompute_and_two_calls(cuda_lib, Bsz, T, Di, N, gate, strided):
-    """f32 T-split prefill: with the fastest plan's workspace the state-only
-    pass hands u and delta to the full pass; with only the carries' room the
-    full pass recomputes them.  Both equal the two separate calls bit for bit,
-    in place and not."""
-    m = cuda_lib
-    K = 4
-    scan_ws = m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
-    mix_ws = m.mamba_mixer_prefill_workspace_bytes(Bsz, T, Di, N, torch.float32)
-    assert scan_ws > 0 and mix_ws >= scan_ws + 2 * Bsz * T * Di * 4
-    assert m.mamba_mixer_prefill_workspace_bytes(Bsz, T, Di, N, torch.bfloat16) == scan_ws
-    p = {k: to_dev(v) for k, v in _params(SEED + 9, Di, N, K).items()}
-    a = synth.prefill_inputs(SEED + 9, Bsz, T, Di, N, "f32", names=("x", "dt", "z", "B", "C"))
-    if strided:
-        x = strided_copy(a["x"], "f32", 2 * Di)
-        z = strided_copy(a["z"], "f32", 2 * Di, offset=Di) if gate else None
-    else:
-        x = to_dev(a["x"])
-        z = to_dev(a["z"]) if gate else None
-    dt, Bm, Cm = (to_dev(a[k]) for k in ("dt", "B", "C"))
-    c0 = to_dev(synth.normal(SEED, "conv_state", (Bsz, Di, K), 0.5))
-    s0 = to_dev(synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5))
-    u = torch.empty((Bsz, T, Di), device="cuda")
-    c1, s1, y1 = torch.empty_like(c0), torch.empty_like(s0), torch.empty((Bsz, T, Di), device="cuda")
-    m.mamba_conv1d_silu_prefill(u, x, p["conv_w"], p["conv_b"], c0, c1)
-    m.mamba_selective_scan_prefill(y1, u, dt, Bm, Cm, p["A_log"], p["D"], p["dt_bias"], z, s0, s1)
-    for ws_bytes in (mix_ws, scan_ws):
-        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
-        y2, c2, s2 = torch.empty_like(y1), torch.empty_like(c0), torch.empty_like(s0)
-        m.mamba_mixer_prefill(y2, x, dt, Bm, Cm, p["conv_w"], p["A_log"], p["conv_b"], p["D"], p["dt_bias"], z,
-                              c0, c2, s0, s2, workspace=ws)
-        y3, c3, s3 = torch.empty_like(y1), c0.clone(), s0.clone()
-        m.mamba_mixer_prefill(y3, x, dt, Bm, Cm, p["conv_w"], p["A_log"], p["conv_b"], p["D"], p["dt_bias"], z,
-                              c3, c3, s3, s3, workspace=ws)
-        torch.cuda.synchronize()
-        for got in ((y2, c2, s2), (y3, c3, s3)):
-            assert torch.equal(got[0], y1) and torch.equal(got[1], c1) and torch.equal(got[2], s1), ws_bytes
-
-
 def test_mixer_prefill_T0_copies_both_states(cuda_lib):
     m = cuda_lib
     Bsz, Di, N, K = 2, 32, 16, 4
