@@ -1,6 +1,6 @@
 """GB300-native (sm_103a) Mamba-1 selective-SSM mixer core.
 
-Four C-ABI entry points (include/mamba_ssm.h), each a hand-written CUDA kernel:
+C-ABI entry points (include/mamba_ssm.h), each backed by hand-written CUDA kernels:
   mamba_conv1d_silu_prefill     causal depthwise conv1d + SiLU over T tokens
   mamba_conv1d_silu_step        T=1 conv step on a [n_layers][B*Di*K] state
   mamba_selective_scan_prefill  selective scan + SiLU(z) gate, state in/out
@@ -9,6 +9,8 @@ Four C-ABI entry points (include/mamba_ssm.h), each a hand-written CUDA kernel:
   mamba_mixer_prefill           conv1d + SiLU and the selective scan in one pass
   mamba_decode_graph_*          n_steps x n_layers fused steps recorded as one CUDA graph
   mamba3_siso_step_batched      T=1 step of the Mamba-3 SISO (trapezoidal) recurrence
+  mamba_selective_scan_prefill_noalloc  the scan prefill with a static scratch
+  mamba_selective_scan_workspace_bytes  scratch size of the prefill's T split
 This package is the thin Python binding (argument marshalling over ctypes);
 `synth` holds the seeded synthetic inputs used by the tests and the benchmark.
 """
