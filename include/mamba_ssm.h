@@ -367,13 +367,28 @@ MAMBA_API int mamba_selective_scan_prefill_noalloc(
  * Every wait on such a barrier is bounded (about a second of SM clock); a wait
  * that runs out sets MAMBA_FAULT_RING_WAIT here and the kernel leaves its loop
  * instead of hanging, so that launch's outputs are incomplete.  In correct
- * operation no wait runs out and the value stays 0.
+ * operation no wait runs out and the value stays 0 (mamba_selftest_bounded_wait
+ * sets the bit on purpose, through the same bounded wait).
  *   - Synchronises the current device (so it cannot be called during stream
  *     capture), then returns the fault bits (>= 0) of that device, or
  *     MAMBA_ERR_CUDA.  `clear` != 0 resets the bits after reading them.
  */
 #define MAMBA_FAULT_RING_WAIT 1
 MAMBA_API int mamba_device_faults(int clear);
+
+/*
+ * mamba_selftest_bounded_wait - exercises the watchdog path of
+ * mamba_device_faults without a fault.  (No counterpart in the mamba-rs pages:
+ * an addition of this library.)  It enqueues on `stream` one CTA that waits,
+ * with the same bounded wait as the decode kernels' copy rings, on a fresh
+ * mbarrier that needs one arrival.  With complete != 0 the CTA arrives first
+ * and the wait succeeds at once.  With complete == 0 nothing arrives: after
+ * limit_cycles SM clock cycles (1 .. 2^31; 2e6 is about 1 ms at 2 GHz) the wait
+ * gives up, sets MAMBA_FAULT_RING_WAIT, and the kernel returns.  The device
+ * stays usable.  Errors: MAMBA_ERR_INVALID_ARG for a limit out of range,
+ * MAMBA_ERR_UNSUPPORTED / MAMBA_ERR_CUDA as for the other calls.
+ */
+MAMBA_API int mamba_selftest_bounded_wait(int64_t limit_cycles, int complete, void* stream);
 
 /* Thread-local description of the last error returned on this thread
  * (empty string after a successful call).  Never NULL; owned by the library. */

@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     mamba_selective_scan_prefill,
     mamba_selective_scan_prefill_noalloc,
     mamba_selective_scan_workspace_bytes,
+    mamba_selftest_bounded_wait,
     mamba_ssm_step_batched,
     mamba_version,
 )

@@ -40,6 +40,7 @@ ABI_SYMBOLS = (
     "mamba_decode_graph_kernels",
     "mamba_decode_graph_destroy",
     "mamba_device_faults",
+    "mamba_selftest_bounded_wait",
     "mamba_last_error",
     "mamba_version",
 )
@@ -100,6 +101,8 @@ def load(path: str | None = None):
         lib.mamba_decode_graph_destroy.restype = ctypes.c_int
         lib.mamba_device_faults.argtypes = [i32]
         lib.mamba_device_faults.restype = ctypes.c_int
+        lib.mamba_selftest_bounded_wait.argtypes = [i64, i32, vp]
+        lib.mamba_selftest_bounded_wait.restype = ctypes.c_int
         lib.mamba_last_error.argtypes = []
         lib.mamba_last_error.restype = ctypes.c_char_p
         lib.mamba_version.argtypes = []
@@ -126,6 +129,18 @@ def mamba_device_faults(clear: bool = False) -> int:
     if v < 0:
         raise MambaError(int(v), mamba_last_error())
     return int(v)
+
+
+def mamba_selftest_bounded_wait(limit_cycles: int, complete: bool, stream=None):
+    """One CTA waits, with the decode rings' bounded wait, on an mbarrier that is
+    completed first (complete=True) or never (False: the wait runs out after
+    limit_cycles and sets MAMBA_FAULT_RING_WAIT).  Enqueued on `stream` (default:
+    the current stream)."""
+    import torch
+
+    st = torch.cuda.current_stream().cuda_stream if stream is None else (
+        stream if isinstance(stream, int) else stream.cuda_stream)
+    _check(load().mamba_selftest_bounded_wait(int(limit_cycles), 1 if complete else 0, st))
 
 
 def _check(status: int):

@@ -187,7 +187,20 @@ int mamba_device_faults(int clear) {
   if (v < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: %s", cudaGetErrorString(e));
   const int v3 = mamba::read_m3_faults(clear != 0);
   if (v3 < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the Mamba-3 watchdog failed");
-  return ok(), v | v3;
+  const int vs = mamba::read_selftest_faults(clear != 0);
+  if (vs < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the self-test watchdog failed");
+  return ok(), v | v3 | vs;
+}
+
+int mamba_selftest_bounded_wait(int64_t limit_cycles, int complete, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 31))
+    return fail(MAMBA_ERR_INVALID_ARG, "limit_cycles=%lld not in 1..2^31", (long long)limit_cycles);
+  mamba::DeviceInfo dev;
+  int rc;
+  if ((rc = current_device(&dev))) return rc;
+  cudaError_t e = mamba::launch_selftest_wait(limit_cycles, complete != 0, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("mamba_selftest_bounded_wait launch", e);
+  return ok();
 }
 
 int mamba_conv1d_silu_prefill(void* u, int64_t ld_u, const void* x, int64_t ld_x, int act_dtype,

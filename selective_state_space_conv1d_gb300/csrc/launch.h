@@ -34,6 +34,10 @@ int set_last_error(int code, const char* msg);
 
 // Synchronises the current device and returns its watchdog fault bits
 // (MAMBA_FAULT_*), clearing them if asked; -1 and *err on a CUDA error.
+// one CTA whose bounded mbarrier wait runs out unless `complete`, and its fault
+// word (selftest.cu; read like the other watchdog words, -1 on a CUDA error)
+cudaError_t launch_selftest_wait(long long limit, int complete, cudaStream_t stream);
+int read_selftest_faults(bool clear);
 int read_device_faults(bool clear, cudaError_t* err);
 
 struct DeviceInfo {

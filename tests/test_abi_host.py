@@ -211,6 +211,7 @@ int main(void) {
     if (mamba_conv1d_silu_step(NULL, NULL, 7, NULL, 0, 1, NULL, NULL, 1, 8, 4, NULL) != MAMBA_ERR_INVALID_ARG)
         { puts("bad dtype accepted"); ++fails; }
     if (mamba_decode_graph_destroy(NULL) != MAMBA_OK) { puts("destroy(NULL)"); ++fails; }
+    if (mamba_selftest_bounded_wait(0, 0, NULL) != MAMBA_ERR_INVALID_ARG) { puts("limit 0 accepted"); ++fails; }
     if (mamba_selective_scan_prefill(NULL, 0, MAMBA_F32, NULL, 0, NULL, 0, NULL, 0, NULL, 0, NULL, 0, MAMBA_F32,
                                      NULL, NULL, NULL, NULL, NULL, 0, 8, 32, 16, NULL, 0, NULL) != MAMBA_OK)
         { puts("empty batch not a no-op"); ++fails; }

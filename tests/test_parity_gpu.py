@@ -506,6 +506,48 @@ def test_step_ring_and_direct_paths_agree_bitwise(cuda_lib, N, K, dtype, fused):
     assert m.mamba_device_faults(clear=True) == 0
 
 
+def test_a_bounded_wait_that_runs_out_sets_the_fault_bit_and_the_device_stays_usable(cuda_lib):
+    """The watchdog path without a fault: a CTA waits, with the copy rings'
+    bounded wait, on an mbarrier that nothing completes.  The wait gives up
+    after its limit (about 1 ms here), the kernel returns, the host reads
+    MAMBA_FAULT_RING_WAIT, and a ring-kernel decode step run afterwards still
+    matches the oracle.  With the barrier completed first, no bit is set."""
+    m = cuda_lib
+    assert m.mamba_device_faults(clear=True) == 0
+    try:
+        m.mamba_selftest_bounded_wait(2_000_000, complete=True)
+        assert m.mamba_device_faults() == 0
+        m.mamba_selftest_bounded_wait(2_000_000, complete=False)
+        assert m.mamba_device_faults() & m.MAMBA_FAULT_RING_WAIT
+    finally:
+        m.mamba_device_faults(clear=True)
+    assert m.mamba_device_faults() == 0
+    with pytest.raises(m.MambaError) as ei:
+        m.mamba_selftest_bounded_wait(0, complete=False)
+    assert ei.value.status == m.MAMBA_ERR_INVALID_ARG
+    # the context is intact: a ring-path mixer step against the oracle
+    L, Bsz, Di, N, K = 1, 8, 256, 16, 4
+    p = _params(SEED + 13, Di, N, K)
+    conv0 = synth.normal(SEED, "conv_state", (L, Bsz, Di, K), 0.5)
+    ssm0 = synth.normal(SEED, "ssm_state", (L, Bsz, Di, N), 0.5)
+    inp = synth.decode_step_inputs(SEED, 0, 0, Bsz, Di, N, "f32")
+    conv, ssm = to_dev(conv0), to_dev(ssm0)
+    y = torch.empty((Bsz, Di), device="cuda")
+    pd = {k: to_dev(v) for k, v in p.items()}
+    m.mamba_mixer_step_batched(y, to_dev(inp["x"]), to_dev(inp["dt"]), to_dev(inp["B"]), to_dev(inp["C"]), conv,
+                               ssm, 0, pd["conv_w"], pd["A_log"], pd["conv_b"], pd["D"], pd["dt_bias"],
+                               to_dev(inp["z"]))
+    torch.cuda.synchronize()
+    cs, ss = conv0.astype(np.float64), ssm0.astype(np.float64)
+    u = oracle.conv1d_silu_step(inp["x"], cs, 0, p["conv_w"], p["conv_b"])
+    y_ref = oracle.ssm_step(u, inp["dt"], inp["B"], inp["C"], ss, 0, p["A_log"], D=p["D"], dt_bias=p["dt_bias"],
+                            z=inp["z"])
+    assert_within(to_host(y), y_ref, "y after the watchdog self-test")
+    assert_within(to_host(ssm), ss, "ssm state after the watchdog self-test")
+    assert np.array_equal(to_host(conv), cs)
+    assert m.mamba_device_faults(clear=True) == 0
+
+
 # ------------------------------------------------------ decode graph driver ----
 
 @pytest.mark.parametrize("dtype,gate,Di", [("f32", True, 200), ("bf16", True, 160), ("f32", False, 100)])
