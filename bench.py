@@ -295,16 +295,30 @@ def mufu_peak_tops(sm_count=GB300_SMS):
     return MUFU_SLOTS_PER_CLK_SM * sm_count * GB300_MAX_SM_MHZ * 1e6 / 1e12
 
 
+# FP32 pipe of GB300: 128 lanes/clk/SM (an FMA counts as one operation)
+FP32_LANES_PER_CLK_SM = 128
+
+
+def fp32_peak_tops(sm_count=GB300_SMS):
+    return FP32_LANES_PER_CLK_SM * sm_count * GB300_MAX_SM_MHZ * 1e6 / 1e12
+
+
 def scan_roofline(tc, N, gate, bytes_per_launch, ms, hbm_peak_gbs, peak_src, traffic, sm_count, conv=False):
     """The scan is bound by MUFU (and FMA) throughput, not HBM: per (token,
     channel) it needs N ex2 for the states, ex2 + lg2 for softplus and, with a
     gate, ex2 + rcp for SiLU (lg2/rcp at half rate count twice): N + 3 (+ 3)
     ex2-equivalent MUFU slots; the fused prefill adds the conv's SiLU (+ 3).
-    Reported against the MUFU peak, with the HBM view alongside."""
+    Reported against the MUFU peak, with the HBM and FP32-pipe views alongside."""
     slots = tc * (N + 3 + (3 if gate else 0) + (3 if conv else 0))
     tops = slots / (ms * 1e-3) / 1e12
     peak = mufu_peak_tops(sm_count)
     gbs = bytes_per_launch / (ms * 1e-3) / 1e9
+    # FP32 operations per (token, channel): 4 per state (delta*A, delta*u*B, the
+    # h update and the C.h term), 8 scalars (softplus 5, delta*u, the D term,
+    # the gate product), the gate's SiLU 3, the conv's taps and SiLU 7
+    ops = tc * (4 * N + 8 + (3 if gate else 0) + (7 if conv else 0))
+    fops = ops / (ms * 1e-3) / 1e12
+    fpeak = fp32_peak_tops(sm_count)
     return {"bound": "alu", "achieved": round(tops, 3), "peak": round(peak, 3),
             "unit": "T MUFU-slot/s", "frac": round(tops / peak, 4), "traffic": traffic,
             "peak_source": f"derived: {MUFU_SLOTS_PER_CLK_SM} ex2/clk/SM x {sm_count} SMs x "
@@ -312,7 +326,11 @@ def scan_roofline(tc, N, gate, bytes_per_launch, ms, hbm_peak_gbs, peak_src, tra
             "algorithmic_mufu_slots_per_launch": int(slots),
             "algorithmic_bytes_per_launch": int(bytes_per_launch), "avg_launch_ms": round(ms, 6),
             "hbm": {"achieved": round(gbs, 1), "peak": hbm_peak_gbs, "unit": "GB/s",
-                    "frac": round(gbs / hbm_peak_gbs, 4), "peak_source": peak_src}}
+                    "frac": round(gbs / hbm_peak_gbs, 4), "peak_source": peak_src},
+            "fp32": {"achieved": round(fops, 3), "peak": round(fpeak, 3), "unit": "T FP32-op/s",
+                     "frac": round(fops / fpeak, 4), "algorithmic_fp32_ops_per_launch": int(ops),
+                     "peak_source": f"derived: {FP32_LANES_PER_CLK_SM} lanes/clk/SM x {sm_count} SMs x "
+                                    f"{GB300_MAX_SM_MHZ:.0f} MHz"}}
 
 
 def run_prefill(torch, m, synth, wl_index, steps, warmup, device, dist, clocks, host_inputs=True):
