@@ -47,6 +47,43 @@ def test_f32_prefill_workloads_full(cuda_lib, wl_index):
     assert_within(to_host(y), y_ref, "y")
     assert np.array_equal(to_host(cst), c_ref)
     assert_within(to_host(sst), s_ref, "ssm state")
+    # the fused prefill, as the benchmark's step runs it (default workspace)
+    y2 = torch.empty_like(y)
+    c2, s2 = torch.empty_like(cst), torch.empty_like(sst)
+    m.mamba_mixer_prefill(y2, to_dev(a["x"]), to_dev(a["dt"]), to_dev(a["B"]), to_dev(a["C"]), to_dev(p["conv_w"]),
+                          to_dev(p["A_log"]), to_dev(p["conv_b"]), to_dev(p["D"]), to_dev(p["dt_bias"]),
+                          to_dev(a["z"]), None, c2, None, s2)
+    torch.cuda.synchronize()
+    assert_within(to_host(y2), y_ref, "fused y")
+    assert np.array_equal(to_host(c2), c_ref)
+    assert_within(to_host(s2), s_ref, "fused ssm state")
+    assert torch.equal(y2, y) and torch.equal(s2, sst), "fused prefill != conv + scan"
+
+
+def test_2p8b_bf16_fused_prefill_equals_the_two_calls(cuda_lib):
+    """mamba-2.8b layer at full size, as the benchmark's step runs it: the
+    fused prefill equals the conv prefill followed by the scan on its bf16 u,
+    bit for bit (the two calls are checked against the oracle in the test
+    below, and u's bf16 rounding is shared by both forms)."""
+    m = cuda_lib
+    wl = synth.WORKLOADS[3]
+    Bsz, T, Di, N, K = wl.batch, wl.seqlen, wl.d_inner, wl.d_state, wl.d_conv
+    p = {k: to_dev(v) for k, v in synth.mixer_params(wl.seed, Di, N, K).items()}
+    a = synth.prefill_inputs(wl.seed, Bsz, T, Di, N, "bf16", names=("x", "dt", "z", "B", "C"))
+    x, dt, z, Bm, Cm = (to_dev(a[k], "bf16") for k in ("x", "dt", "z", "B", "C"))
+    u = torch.empty_like(x)
+    c1 = torch.empty((Bsz, Di, K), device="cuda")
+    m.mamba_conv1d_silu_prefill(u, x, p["conv_w"], p["conv_b"], None, c1)
+    y1 = torch.empty((Bsz, T, Di), device="cuda")
+    s1 = torch.empty((Bsz, Di, N), device="cuda")
+    m.mamba_selective_scan_prefill(y1, u, dt, Bm, Cm, p["A_log"], p["D"], p["dt_bias"], z, None, s1)
+    del u
+    y2 = torch.empty_like(y1)
+    c2, s2 = torch.empty_like(c1), torch.empty_like(s1)
+    m.mamba_mixer_prefill(y2, x, dt, Bm, Cm, p["conv_w"], p["A_log"], p["conv_b"], p["D"], p["dt_bias"], z,
+                          None, c2, None, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2) and torch.equal(c1, c2) and torch.equal(s1, s2)
 
 
 def test_2p8b_bf16_prefill_sampled(cuda_lib):
