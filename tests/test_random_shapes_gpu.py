@@ -1,0 +1,96 @@
+"""A seeded sweep of random shapes and layouts (GPU).
+
+Each case draws batch, T, d_inner, d_state, d_conv, the storage dtype, the gate,
+the initial states and a row stride for the activations, then checks:
+  - the conv prefill against the oracle (u within the bound, the new conv state
+    exactly);
+  - the scan prefill, on the conv's own stored u, against the oracle (y and the
+    final state within the bound);
+  - for d_conv 4, the fused prefill against the two calls, bit for bit;
+  - for T = 1, one fused decode step against the T=1 prefill, bit for bit.
+The shapes cover ragged channel tails, both prefill routes and every d_state.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_conv1d_gb300 import synth
+from _helpers import assert_within, strided_copy, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 24
+
+
+def _draw(i):
+    r = np.random.default_rng(0x5EED_2000 + i)
+    case = dict(
+        Bsz=int(r.integers(1, 5)),
+        T=int(r.choice([1, 2, 3, int(r.integers(4, 200)), int(r.integers(200, 1400))])),
+        Di=int(r.integers(1, 300)),
+        N=int(r.choice([1, 2, 4, 8, 16, 32, 64])),
+        K=int(r.choice([2, 3, 4, 4])),
+        dtype=str(r.choice(["f32", "bf16"])),
+        gate=bool(r.integers(0, 2)),
+        states=bool(r.integers(0, 2)),
+        pad=int(r.choice([0, 0, 1, 8])),  # extra row stride, in elements
+    )
+    return case
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_shape_matches_oracle(cuda_lib, i):
+    m = cuda_lib
+    c = _draw(i)
+    Bsz, T, Di, N, K, dtype = c["Bsz"], c["T"], c["Di"], c["N"], c["K"], c["dtype"]
+    seed = 0x5EED_2100 + i
+    p = synth.mixer_params(seed, Di, N, K)
+    pd = {k: to_dev(v) for k, v in p.items()}
+    a = synth.prefill_inputs(seed, Bsz, T, Di, N, dtype, names=("x", "dt", "z", "B", "C"))
+    ld = Di + c["pad"]
+    x = strided_copy(a["x"], dtype, ld)
+    dt = strided_copy(a["dt"], dtype, ld)
+    z = strided_copy(a["z"], dtype, ld) if c["gate"] else None
+    Bm, Cm = to_dev(a["B"], dtype), to_dev(a["C"], dtype)
+    c0 = synth.normal(seed, "conv_state", (Bsz, Di, K), 0.5) if c["states"] else None
+    s0 = synth.normal(seed, "ssm_state", (Bsz, Di, N), 0.5) if c["states"] else None
+    c0d = to_dev(c0) if c0 is not None else None
+    s0d = to_dev(s0) if s0 is not None else None
+
+    u = torch.empty((Bsz, T, Di), device="cuda", dtype=x.dtype)
+    c1 = torch.empty((Bsz, Di, K), device="cuda")
+    m.mamba_conv1d_silu_prefill(u, x, pd["conv_w"], pd["conv_b"], c0d, c1)
+    y1 = torch.empty((Bsz, T, Di), device="cuda")
+    s1 = torch.empty((Bsz, Di, N), device="cuda")
+    m.mamba_selective_scan_prefill(y1, u, dt, Bm, Cm, pd["A_log"], pd["D"], pd["dt_bias"], z, s0d, s1)
+    torch.cuda.synchronize()
+
+    u_ref, c_ref = oracle.conv1d_silu_prefill(a["x"], p["conv_w"], p["conv_b"], c0)
+    assert_within(to_host(u), u_ref, f"case {i} {c}: u", bf16_out=dtype == "bf16")
+    assert np.array_equal(to_host(c1), c_ref), f"case {i} {c}: conv state"
+    u_stored = to_host(u)  # the scan's input as stored (bf16 values are exact in f64)
+    y_ref, s_ref = oracle.selective_scan_prefill(u_stored, a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                 p["dt_bias"], a["z"] if c["gate"] else None, s0)
+    assert_within(to_host(y1), y_ref, f"case {i} {c}: y")
+    assert_within(to_host(s1), s_ref, f"case {i} {c}: ssm state")
+
+    if K == 4:
+        y2 = torch.empty_like(y1)
+        c2, s2 = torch.empty_like(c1), torch.empty_like(s1)
+        m.mamba_mixer_prefill(y2, x, dt, Bm, Cm, pd["conv_w"], pd["A_log"], pd["conv_b"], pd["D"], pd["dt_bias"],
+                              z, c0d, c2, s0d, s2)
+        torch.cuda.synchronize()
+        assert torch.equal(y2, y1) and torch.equal(c2, c1) and torch.equal(s2, s1), f"case {i} {c}: fused"
+
+    if T == 1:
+        # one layer of a [1][B][Di][K|N] state, continuing from the same states
+        conv = (c0d.clone() if c0d is not None else torch.zeros((Bsz, Di, K), device="cuda")).unsqueeze(0)
+        ssm = (s0d.clone() if s0d is not None else torch.zeros((Bsz, Di, N), device="cuda")).unsqueeze(0)
+        ys = torch.empty((Bsz, Di), device="cuda")
+        m.mamba_mixer_step_batched(ys, x[:, 0].contiguous(), dt[:, 0].contiguous(), Bm[:, 0].contiguous(),
+                                   Cm[:, 0].contiguous(), conv, ssm, 0, pd["conv_w"], pd["A_log"], pd["conv_b"],
+                                   pd["D"], pd["dt_bias"], z[:, 0].contiguous() if z is not None else None)
+        torch.cuda.synchronize()
+        assert torch.equal(ys, y1[:, 0]), f"case {i} {c}: step y"
+        assert torch.equal(conv[0], c1) and torch.equal(ssm[0], s1), f"case {i} {c}: step states"
