@@ -94,3 +94,45 @@ def test_random_shape_matches_oracle(cuda_lib, i):
         torch.cuda.synchronize()
         assert torch.equal(ys, y1[:, 0]), f"case {i} {c}: step y"
         assert torch.equal(conv[0], c1) and torch.equal(ssm[0], s1), f"case {i} {c}: step states"
+
+
+def _draw_m3(i):
+    r = np.random.default_rng(0x5EED_3000 + i)
+    N = int(r.choice([16, 32, 64, 128]))
+    P = int(r.choice([1, 3, 8, 17, 32, 64, 100, 2048 * 8 // N]))  # up to the P*N/8 <= 2048 limit
+    return dict(Bsz=int(r.integers(1, 4)), H=int(r.integers(1, 6)), P=P, N=N, L=int(r.integers(1, 4)),
+                dtype=str(r.choice(["f32", "bf16"])), y_dtype=str(r.choice(["f32", "bf16"])),
+                with_D=bool(r.integers(0, 2)))
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_m3_shape_matches_oracle(cuda_lib, i):
+    """Random Mamba-3 SISO shapes (both kernels: headdim * 4 % 16 picks the
+    copy ring or the any-alignment one): two steps on the last layer against
+    the oracle, the other layers untouched."""
+    m = cuda_lib
+    c = _draw_m3(i)
+    Bsz, H, P, N, L, dtype, y_dtype = c["Bsz"], c["H"], c["P"], c["N"], c["L"], c["dtype"], c["y_dtype"]
+    seed, layer = 0x5EED_3100 + i, c["L"] - 1
+    st_h, ks_h, vs_h = synth.m3_states(seed, L, Bsz, H, P, N)
+    st, ks, vs = to_dev(st_h), to_dev(ks_h), to_dev(vs_h)
+    ref = [a.astype(np.float64).copy() for a in (st_h, ks_h, vs_h)]
+    D_h = synth.normal(seed, "m3_D", (H,), 1.0) if c["with_D"] else None
+    D = to_dev(D_h) if D_h is not None else None
+    ytd = torch.bfloat16 if y_dtype == "bf16" else torch.float32
+    for step in range(2):
+        inp = synth.m3_step_inputs(seed, layer, step, Bsz, H, P, N, dtype)
+        x, k, q = (to_dev(inp[n], dtype) for n in ("x", "k", "q"))
+        al, be, ga = (to_dev(inp[n]) for n in ("alpha", "beta", "gamma"))
+        y = torch.empty((Bsz, H, P), device="cuda", dtype=ytd)
+        m.mamba3_siso_step_batched(y, x, k, q, al, be, ga, st, ks, vs, layer, D)
+        torch.cuda.synchronize()
+        y_ref = oracle.m3_step(inp["x"], inp["k"], inp["q"], inp["alpha"], inp["beta"], inp["gamma"],
+                               ref[0], ref[1], ref[2], layer, D_h)
+        assert_within(to_host(y), y_ref, f"case {i} {c}: y step {step}", bf16_out=y_dtype == "bf16")
+        assert_within(to_host(st[layer]), ref[0][layer], f"case {i} {c}: ssm state step {step}")
+        assert np.array_equal(to_host(ks[layer]), ref[1][layer]) and np.array_equal(to_host(vs[layer]), ref[2][layer])
+    for s_dev, s_h in ((st, st_h), (ks, ks_h), (vs, vs_h)):
+        for l in range(L - 1):
+            assert np.array_equal(to_host(s_dev[l]), s_h[l])
+    assert m.mamba_device_faults(clear=True) == 0
