@@ -136,6 +136,34 @@ def test_scan_continuation_is_bitwise(T1):
     assert np.array_equal(h2, hT)
 
 
+@pytest.mark.parametrize("parts", [2, 3, 5])
+def test_scan_split_along_T_and_folded_equals_the_whole_scan(parts):
+    """The decomposition the T-split route rests on, in exact arithmetic: scan
+    each part from a zero state, take each part's total decay exp(A * sum of
+    its deltas), fold carry_{j+1} = decay_j * carry_j + end_j from carry_0 =
+    h0, and rescan each part from its carry.  That reproduces the whole scan's
+    y and final state (f64, to rounding)."""
+    c = _rand_scan_case(Bsz=2, T=37, Di=3, N=5, seed=21)
+    y_all, h_all = _scan(c)
+    T = c["u"].shape[1]
+    bounds = np.linspace(0, T, parts + 1).astype(int)
+    A = -np.exp(c["A_log"])
+    carry = c["state_in"].copy()
+    ys = []
+    for j in range(parts):
+        sl = slice(bounds[j], bounds[j + 1])
+        part = {k: (v[:, sl] if k in ("u", "dt", "Bm", "Cm", "z") else v) for k, v in c.items()}
+        _, end = _scan(part, state_in=None)                       # this part from a zero state
+        delta = np.logaddexp(0.0, part["dt"] + c["dt_bias"])      # [B, t, Di]
+        decay = np.exp(A[None] * delta.sum(axis=1)[:, :, None])    # [B, Di, N]
+        y_j, h_j = _scan(part, state_in=carry)                    # the rescan from the carry-in
+        ys.append(y_j)
+        np.testing.assert_allclose(h_j, decay * carry + end, rtol=1e-12, atol=1e-13)
+        carry = decay * carry + end
+    np.testing.assert_allclose(np.concatenate(ys, axis=1), y_all, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(carry, h_all, rtol=1e-12, atol=1e-13)
+
+
 def test_scan_T1_prefill_equals_step_bitwise():
     c = _rand_scan_case(Bsz=3, T=1, Di=6, N=16, seed=11)
     y, hT = _scan(c)
