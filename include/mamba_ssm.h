@@ -83,6 +83,7 @@ extern "C" {
 #define MAMBA_BF16 1
 
 #define MAMBA_MAX_D_CONV 8 /* d_conv in 1..8 */
+#define MAMBA_MAX_FUSED_D_CONV 4 /* d_conv of the fused prefill: 1..4 */
 /* d_state in {1, 2, 4, 8, 16, 32, 64} (mirrors the d_state <= 64 register
  * contract of the fused step kernel in inference.rs, mixed step F8+F9+F10). */
 #define MAMBA_MAX_D_STATE 64
@@ -142,13 +143,18 @@ MAMBA_API int mamba_conv1d_silu_step(void* u, const void* x, int act_dtype, floa
  *   ssm_state_in  [B][Di][N] f32 or NULL (zeros)
  *   ssm_state_out [B][Di][N] f32 or NULL; may equal ssm_state_in
  *   workspace     device scratch of workspace_bytes bytes (16-byte aligned),
- *                 or NULL / 0.  Narrow shapes (few batch x channel rows, e.g.
- *                 batch 1) are split along T into parts scanned in parallel,
- *                 which needs mamba_selective_scan_workspace_bytes() bytes;
- *                 with less, the call runs as one sequential pass (same
- *                 result up to rounding, slower).  Contents on entry are
- *                 ignored; calls that share a workspace must not overlap in
- *                 time (same stream, or ordered by events).
+ *                 or NULL / 0.  With mamba_selective_scan_workspace_bytes()
+ *                 bytes the call balances the scan over all SMs: wide shapes
+ *                 hand each tile's state from one stretch of rows to the next
+ *                 through the workspace, and narrow shapes (few batch x channel
+ *                 rows, e.g. batch 1) are split along T into parts scanned in
+ *                 parallel and joined by their carries.  With less, a narrow
+ *                 shape is split into as many parts as the workspace holds, and
+ *                 anything else runs as one sequential pass per 32 channels
+ *                 (same result up to rounding, slower).  Contents on entry are
+ *                 ignored (the call clears what it needs); calls that share a
+ *                 workspace must not overlap in time (same stream, or ordered
+ *                 by events).
  * T == 0 copies the state.
  * Errors: MAMBA_ERR_INVALID_ARG for NULL required pointers, ld < row width,
  * y overlapping an input; MAMBA_ERR_UNSUPPORTED for N not in {1,2,4,...,64}.
@@ -163,10 +169,11 @@ MAMBA_API int mamba_selective_scan_prefill(void* y, int64_t ld_y, int y_dtype, c
                                  int64_t workspace_bytes, void* stream);
 
 /*
- * Workspace (bytes) that mamba_selective_scan_prefill uses to split T across
- * CTAs for a [B, T, Di] x d_state N prefill on the CURRENT device (the split
- * depends on its SM count).  0 means the call runs as one sequential pass and
- * needs no workspace.  Negative MAMBA_ERR_* on bad sizes or no usable device.
+ * Workspace (bytes) that mamba_selective_scan_prefill (and mamba_mixer_prefill)
+ * uses to balance a [B, T, Di] x d_state N prefill over the SMs of the CURRENT
+ * device (the plan depends on its SM count).  0 means the call runs as one
+ * sequential pass per 32 channels and needs no workspace.  Negative MAMBA_ERR_*
+ * on bad sizes or no usable device.
  */
 MAMBA_API int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N);
 
@@ -233,7 +240,8 @@ MAMBA_API int mamba_mixer_step_batched(void* y, int y_dtype, const void* x, cons
  *   may be NULL (zero state), an _out NULL (discarded), and each _out may equal
  *   its _in (in place).
  *   workspace: as for mamba_selective_scan_prefill (same size query).
- * d_conv must be 4 (MAMBA_ERR_UNSUPPORTED otherwise: use the two calls).
+ * d_conv must be in 1..MAMBA_MAX_FUSED_D_CONV (MAMBA_ERR_UNSUPPORTED otherwise:
+ * use the two calls).
  * Errors: as for the two separate prefills.
  */
 MAMBA_API int mamba_mixer_prefill(void* y, int64_t ld_y, int y_dtype, const void* x, int64_t ld_x,
@@ -339,10 +347,16 @@ MAMBA_API int mamba_decode_graph_destroy(MambaDecodeGraph* graph);
  * along T.  This variant takes that scratch from a static device array of
  * MAMBA_NOALLOC_SCRATCH_BYTES inside the library (held on every GPU that loads
  * the library, until the process exits) and otherwise behaves exactly like
- * mamba_selective_scan_prefill with enough workspace: same arguments minus the
- * workspace, same result.  It allocates and frees nothing.
- *   - Shapes whose split needs more scratch than the array holds are rejected
- *     with MAMBA_ERR_UNSUPPORTED (see mamba_selective_scan_workspace_bytes).
+ * mamba_selective_scan_prefill given a workspace of the smaller of the size
+ * mamba_selective_scan_workspace_bytes reports and the array: same arguments
+ * minus the workspace, same plan, same result bit for bit.  It allocates and
+ * frees nothing.
+ *   - A shape whose plan needs more scratch than the array holds runs as the
+ *     regular entry point runs it with a workspace of MAMBA_NOALLOC_SCRATCH_BYTES
+ *     (a narrow shape split into as many parts as the array holds).  A narrow
+ *     shape for which not even two parts fit is rejected with
+ *     MAMBA_ERR_UNSUPPORTED before anything is launched: run as one sequential
+ *     pass it would be many times slower than its split.
  *   - The first call on each device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *   - All calls share the array and it keeps the last call's contents (none of
@@ -374,6 +388,7 @@ MAMBA_API int mamba_selective_scan_prefill_noalloc(
  *     MAMBA_ERR_CUDA.  `clear` != 0 resets the bits after reading them.
  */
 #define MAMBA_FAULT_RING_WAIT 1
+#define MAMBA_FAULT_SCAN_WAIT 2 /* a prefill unit waited too long for the state it continues */
 MAMBA_API int mamba_device_faults(int clear);
 
 /*

@@ -10,7 +10,7 @@ C-ABI entry points (include/mamba_ssm.h), each backed by hand-written CUDA kerne
   mamba_decode_graph_*          n_steps x n_layers fused steps recorded as one CUDA graph
   mamba3_siso_step_batched      T=1 step of the Mamba-3 SISO (trapezoidal) recurrence
   mamba_selective_scan_prefill_noalloc  the scan prefill with a static scratch
-  mamba_selective_scan_workspace_bytes  scratch size of the prefill's T split
+  mamba_selective_scan_workspace_bytes  scratch size of the prefill's balanced routes
 This package is the thin Python binding (argument marshalling over ctypes);
 `synth` holds the seeded synthetic inputs used by the tests and the benchmark.
 """
@@ -24,6 +24,8 @@ from ._binding import (  # noqa: F401
     MAMBA_ERR_UNSUPPORTED,
     MAMBA_F32,
     MAMBA_FAULT_RING_WAIT,
+    MAMBA_FAULT_SCAN_WAIT,
+    MAMBA_MAX_FUSED_D_CONV,
     MAMBA_NOALLOC_SCRATCH_BYTES,
     MAMBA_OK,
     MambaError,

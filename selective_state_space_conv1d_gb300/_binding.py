@@ -21,6 +21,8 @@ MAMBA_ERR_CUDA = -3
 MAMBA_F32 = 0
 MAMBA_BF16 = 1
 MAMBA_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+MAMBA_MAX_FUSED_D_CONV = 4
+MAMBA_FAULT_SCAN_WAIT = 2
 
 LIB_PATH = _build.LIB_PATH
 
@@ -272,6 +274,37 @@ def _workspace(device, nbytes, stream_handle):
     return buf
 
 
+def _check_scan_args(y, u, dt, Bm, Cm, A_log, D, dt_bias, z, ssm_state_in, ssm_state_out):
+    """Shapes and dtypes of a selective-scan prefill call, checked before any
+    launch: the C ABI sees only pointers and sizes, so a tensor that is shorter
+    than the sizes say, or holds another dtype, must be refused here.
+    Returns (B, T, Di, N)."""
+    if u.dim() != 3:
+        raise ValueError(f"u must be 3-D [B, T, Di], got {tuple(u.shape)}")
+    if A_log.dim() != 2:
+        raise ValueError(f"A_log must be 2-D [Di, N], got {tuple(A_log.shape)}")
+    Bsz, T, Di = u.shape
+    N = A_log.shape[1]
+    _f32_param(A_log, "A_log", (Di, N))
+    _f32_param(D, "D", (Di,))
+    _f32_param(dt_bias, "dt_bias", (Di,))
+    _f32_param(ssm_state_in, "ssm_state_in", (Bsz, Di, N))
+    _f32_param(ssm_state_out, "ssm_state_out", (Bsz, Di, N))
+    for t, nm in ((y, "y"), (dt, "dt"), (Bm, "Bm"), (Cm, "Cm")):
+        if t is None:
+            raise ValueError(f"{nm} must not be None")
+    for t, nm in ((dt, "dt"), (z, "z"), (Bm, "Bm"), (Cm, "Cm")):
+        if t is not None and t.dtype != u.dtype:
+            raise ValueError(f"{nm} must have the dtype of u")
+    for t, nm in ((y, "y"), (dt, "dt"), (z, "z")):
+        if t is not None and tuple(t.shape) != (Bsz, T, Di):
+            raise ValueError(f"{nm} must be [B, T, Di] = {(Bsz, T, Di)}, got {tuple(t.shape)}")
+    for t, nm in ((Bm, "Bm"), (Cm, "Cm")):
+        if tuple(t.shape) != (Bsz, T, N):
+            raise ValueError(f"{nm} must be [B, T, N] = {(Bsz, T, N)}, got {tuple(t.shape)}")
+    return Bsz, T, Di, N
+
+
 def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, z=None,
                                  ssm_state_in=None, ssm_state_out=None, *, workspace=None,
                                  stream=None):
@@ -283,22 +316,7 @@ def mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, 
     mamba_selective_scan_workspace_bytes; False = none (one sequential pass);
     or a uint8 cuda tensor (16-byte aligned), which the caller must not reuse
     on another stream while this call may still be running."""
-    Bsz, T, Di = u.shape
-    N = A_log.shape[1]
-    _f32_param(A_log, "A_log", (Di, N))
-    _f32_param(D, "D", (Di,))
-    _f32_param(dt_bias, "dt_bias", (Di,))
-    _f32_param(ssm_state_in, "ssm_state_in", (Bsz, Di, N))
-    _f32_param(ssm_state_out, "ssm_state_out", (Bsz, Di, N))
-    for t, nm in ((dt, "dt"), (z, "z"), (Bm, "Bm"), (Cm, "Cm")):
-        if t is not None and t.dtype != u.dtype:
-            raise ValueError(f"{nm} must have the dtype of u")
-    for t, nm in ((y, "y"), (dt, "dt"), (z, "z")):
-        if t is not None and tuple(t.shape) != (Bsz, T, Di):
-            raise ValueError(f"{nm} must be [B, T, Di]")
-    for t, nm in ((Bm, "Bm"), (Cm, "Cm")):
-        if tuple(t.shape) != (Bsz, T, N):
-            raise ValueError(f"{nm} must be [B, T, N]")
+    Bsz, T, Di, N = _check_scan_args(y, u, dt, Bm, Cm, A_log, D, dt_bias, z, ssm_state_in, ssm_state_out)
     st = _stream(stream, u)
     if workspace is None:
         need = mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
@@ -323,8 +341,8 @@ def mamba_mixer_prefill(y, x, dt, Bm, Cm, conv_w, A_log, conv_b=None, D=None, dt
     """Fused conv1d + SiLU and selective-scan prefill (u never stored).
 
     y, x, dt, z: [B, T, Di] (row-strided views allowed); Bm, Cm: [B, T, N];
-    conv_w: [Di, 4]; A_log: [Di, N]; conv_b, D, dt_bias: [Di]; conv states
-    [B, Di, 4] and ssm states [B, Di, N], f32.  workspace: as for
+    conv_w: [Di, K] with K in 1..4; A_log: [Di, N]; conv_b, D, dt_bias: [Di];
+    conv states [B, Di, K] and ssm states [B, Di, N], f32.  workspace: as for
     mamba_selective_scan_prefill.  Equals mamba_conv1d_silu_prefill followed by
     mamba_selective_scan_prefill, bit for bit."""
     Bsz, T, Di = x.shape
@@ -425,13 +443,7 @@ def mamba_selective_scan_prefill_noalloc(y, u, dt, Bm, Cm, A_log, D=None, dt_bia
     """The selective-scan prefill for callers that cannot allocate device memory:
     its T-split scratch is a static array inside the library (see the C header).
     Same arguments and result as mamba_selective_scan_prefill, minus the workspace."""
-    Bsz, T, Di = u.shape
-    N = A_log.shape[1]
-    _f32_param(A_log, "A_log", (Di, N))
-    _f32_param(D, "D", (Di,))
-    _f32_param(dt_bias, "dt_bias", (Di,))
-    _f32_param(ssm_state_in, "ssm_state_in", (Bsz, Di, N))
-    _f32_param(ssm_state_out, "ssm_state_out", (Bsz, Di, N))
+    Bsz, T, Di, N = _check_scan_args(y, u, dt, Bm, Cm, A_log, D, dt_bias, z, ssm_state_in, ssm_state_out)
     _check(load().mamba_selective_scan_prefill_noalloc(
         _ptr(y), _rows_ld(y, "y"), _dtype_code(y), _ptr(u), _rows_ld(u, "u"),
         _ptr(dt), _rows_ld(dt, "dt"), _ptr(z), _rows_ld(z, "z") if z is not None else 0,

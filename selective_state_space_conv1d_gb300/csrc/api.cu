@@ -170,6 +170,15 @@ int copy_state(float* out, const float* in, int64_t count, cudaStream_t s) {
 
 }  // namespace
 
+int mamba::plan_scan_for_current_device(int64_t B, int64_t T, int64_t Di, int64_t N, int64_t workspace_bytes,
+                                        ScanShapePlan* out) {
+  mamba::DeviceInfo dev;
+  const int rc = current_device(&dev);
+  if (rc) return rc;
+  *out = mamba::plan_scan_shape(B, T, Di, N, dev, workspace_bytes);
+  return MAMBA_OK;
+}
+
 int mamba::set_last_error(int code, const char* msg) {
   snprintf(g_err, sizeof(g_err), "%s", msg ? msg : "");
   return code;
@@ -186,10 +195,12 @@ int mamba_device_faults(int clear) {
   const int v = mamba::read_device_faults(clear != 0, &e);
   if (v < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: %s", cudaGetErrorString(e));
   const int v3 = mamba::read_m3_faults(clear != 0);
+  const int v2 = mamba::read_scan_faults(clear != 0);
+  if (v2 < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the scan watchdog failed");
   if (v3 < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the Mamba-3 watchdog failed");
   const int vs = mamba::read_selftest_faults(clear != 0);
   if (vs < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the self-test watchdog failed");
-  return ok(), v | v3 | vs;
+  return ok(), v | v2 | v3 | vs;
 }
 
 int mamba_selftest_bounded_wait(int64_t limit_cycles, int complete, void* stream) {
@@ -343,9 +354,10 @@ int mamba_mixer_prefill(void* y, int64_t ld_y, int y_dtype, const void* x, int64
   if ((rc = check_dtype("y_dtype", y_dtype)) || (rc = check_dtype("act_dtype", act_dtype))) return rc;
   if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld T=%lld Di=%lld)", (long long)B, (long long)T, (long long)Di);
   if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
-  if (K != 4)
-    return fail(MAMBA_ERR_UNSUPPORTED, "the fused prefill supports d_conv=4 (got %lld); call "
-                "mamba_conv1d_silu_prefill and mamba_selective_scan_prefill instead", (long long)K);
+  if (K < 1 || K > MAMBA_MAX_FUSED_D_CONV)
+    return fail(MAMBA_ERR_UNSUPPORTED, "the fused prefill supports d_conv 1..%d (got %lld); call "
+                "mamba_conv1d_silu_prefill and mamba_selective_scan_prefill instead", MAMBA_MAX_FUSED_D_CONV,
+                (long long)K);
   if (workspace_bytes < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative workspace_bytes");
   if (!workspace) workspace_bytes = 0;
   if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 15))
@@ -469,11 +481,11 @@ int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, i
     ok();
     return 0;
   }
-  mamba::DeviceInfo dev;
-  int rc = current_device(&dev);
+  mamba::ScanShapePlan p;
+  const int rc = mamba::plan_scan_for_current_device(B, T, Di, N, INT64_MAX, &p);
   if (rc) return rc;
   ok();
-  return mamba::scan_workspace_bytes(B, Di, N, mamba::scan_parts(B, T, Di, N, dev));
+  return p.workspace_bytes;
 }
 
 int mamba_ssm_step_batched(void* y, int y_dtype, const void* u, const void* dt, const void* z,

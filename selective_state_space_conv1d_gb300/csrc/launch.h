@@ -107,21 +107,47 @@ struct ScanArgs {
   float* conv_state_out = nullptr;        // [B][Di][K] or null; may equal conv_state_in
 };
 
-// How a prefill is launched: one sequential pass per channel tile (parts == 1)
-// or a T split into `parts` parts of `part_len` rows (two launches, needs
-// workspace_bytes of caller workspace).
-struct ScanPlan {
-  int parts;
-  int64_t part_len;
-  int act_vec;  // u/dt/z staged with 16-byte copies (else element loads)
-  int bc_vec;   // B/C staged with 16-byte copies
+// How a prefill is launched.  Every route is one launch of the scan kernel; its
+// warps scan "segments": a 32-channel tile of one batch row over a range of rows.
+//  * plain:   one warp per tile scans all T rows (no workspace)
+//  * chained: one CTA per SM; its warps take "roles" from a queue in order, role
+//             r being tile-rows [r*span, (r+1)*span) of the tiles laid end to
+//             end, span >= T, so every warp gets the same share and a tile cut
+//             between two roles is handed from one to the other through the
+//             workspace: no row is scanned twice
+//  * split:   T cut into `parts` parts of `seg` rows: a state-only pass per part
+//             from a zero state, fold units that chain the parts' (decay, end
+//             state) into carries, then a full pass per part from its carry
+enum ScanMode { kScanPlain = 0, kScanChained = 1, kScanSplit = 2 };
+struct ScanShapePlan {
+  int mode;
+  int parts;  // chained: levels; split: parts; plain: 1
+  int64_t seg;  // rows per level / part
   int64_t workspace_bytes;
 };
-int scan_parts(int64_t B, int64_t T, int64_t Di, int64_t N, const DeviceInfo& dev);
-int64_t scan_workspace_bytes(int64_t B, int64_t Di, int64_t N, int parts);
+struct ScanPlan {
+  ScanShapePlan shape;
+  int act_vec;  // u/dt/z staged with 16-byte copies (else element loads)
+  int bc_vec;   // B/C staged with 16-byte copies
+};
+// The route for a [B, T, Di] x N prefill given `workspace_bytes` of caller
+// workspace (INT64_MAX: as much as the best route wants); it does not depend on
+// the dtypes, strides or the fused conv, so the workspace query needs only sizes.
+ScanShapePlan plan_scan_shape(int64_t B, int64_t T, int64_t Di, int64_t N, const DeviceInfo& dev,
+                              int64_t workspace_bytes);
 ScanPlan plan_selective_scan(const ScanArgs& a, const DeviceInfo& dev, int64_t workspace_bytes);
+// Bytes of a chained / split workspace's header: 32-bit words (a 64-bit queue
+// head, an abort flag, a counter and a flag per tile), rounded up to 256 bytes.
+inline int64_t scan_header_bytes(int64_t tiles) { return ((4 * (4 + 2 * tiles)) + 255) / 256 * 256; }
+// plan_scan_shape on the current device (api.cu); MAMBA_OK or an error status
+int plan_scan_for_current_device(int64_t B, int64_t T, int64_t Di, int64_t N, int64_t workspace_bytes,
+                                 ScanShapePlan* out);
 cudaError_t launch_selective_scan_prefill(const ScanArgs& a, const ScanPlan& plan, float* ws,
                                           const DeviceInfo& dev, cudaStream_t stream);
+// watchdog bits of the scan kernels' bounded waits (the device must be synchronised)
+int read_scan_faults(bool clear);
+// device address of the scan kernels' fault word on the current device (null on error)
+int* scan_fault_word();
 
 struct SsmStepArgs {
   void* y;

@@ -15,9 +15,10 @@
 // address is looked up once per device (cudaGetSymbolAddress, with that device
 // current) on the first call made on that device, so that first call should
 // happen before any stream capture.  All calls share the one array and it
-// keeps the last call's contents; the scan overwrites every byte it later
-// reads, so nothing needs clearing, but calls that overlap on the GPU (two
-// streams, or two threads) race on it and must be ordered by the caller.
+// keeps the last call's contents; each call clears the few header words it
+// needs (an in-stream memset, no allocation) and overwrites every other byte
+// before reading it, but calls that overlap on the GPU (two streams, or two
+// threads) race on it and must be ordered by the caller.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -73,15 +74,26 @@ extern "C" int mamba_selective_scan_prefill_noalloc(
     int in_dtype, const float* A_log, const float* D, const float* dt_bias,
     const float* ssm_state_in, float* ssm_state_out, int64_t B, int64_t T, int64_t Di, int64_t N,
     void* stream) {
-  const int64_t need = mamba_selective_scan_workspace_bytes(B, T, Di, N);
+  int64_t need = mamba_selective_scan_workspace_bytes(B, T, Di, N);
   if (need < 0) return (int)need;  // bad sizes or no usable device; message already set
   if (need > kNoallocScratchBytes) {
-    char msg[160];
-    snprintf(msg, sizeof(msg),
-             "mamba_selective_scan_prefill_noalloc: this shape needs %lld bytes of scratch, the "
-             "static array holds %lld",
-             (long long)need, (long long)kNoallocScratchBytes);
-    return mamba::set_last_error(MAMBA_ERR_UNSUPPORTED, msg);
+    // The plan does not fit: the regular entry point, given the array as its
+    // workspace, splits a narrow shape into as many parts as the array holds.
+    // A narrow shape that does not split at all within the array is refused:
+    // run as one sequential pass it would be many times slower than its split.
+    mamba::ScanShapePlan full, lim;
+    int rc = mamba::plan_scan_for_current_device(B, T, Di, N, INT64_MAX, &full);
+    if (rc == MAMBA_OK) rc = mamba::plan_scan_for_current_device(B, T, Di, N, kNoallocScratchBytes, &lim);
+    if (rc != MAMBA_OK) return rc;
+    if (full.mode == mamba::kScanSplit && lim.mode != mamba::kScanSplit) {
+      char msg[200];
+      snprintf(msg, sizeof(msg),
+               "mamba_selective_scan_prefill_noalloc: splitting this shape along T needs more than the "
+               "%lld bytes of scratch the static array holds (the full split needs %lld)",
+               (long long)kNoallocScratchBytes, (long long)need);
+      return mamba::set_last_error(MAMBA_ERR_UNSUPPORTED, msg);
+    }
+    need = kNoallocScratchBytes;
   }
   void* scratch = nullptr;
   if (need > 0) {

@@ -12,6 +12,7 @@ times, then times one more call with CUDA events and prints it.
   --what convstep  T=1 conv step on layer 1 of an [L][B][Di][4] state
   --what fused     fused conv1d + SiLU and selective-scan prefill  [B, T, Di]
   --what m3        Mamba-3 SISO step on layer 1: --B batch, --H heads, --P headdim, --N d_state
+  --route plain    prefills without a workspace (one warp per 32-channel tile)
 """
 import argparse
 
@@ -32,6 +33,8 @@ def main(argv=None):
     ap.add_argument("--L", type=int, default=24)
     ap.add_argument("--dtype", default="f32", choices=("f32", "bf16"))
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--route", default="auto", choices=("auto", "plain"),
+                    help="prefills: the planned route, or one warp per tile with no workspace")
     a = ap.parse_args(argv)
     td = torch.float32 if a.dtype == "f32" else torch.bfloat16
     g = torch.Generator(device="cuda")
@@ -62,12 +65,14 @@ def main(argv=None):
         uo = torch.empty_like(x)
         so = torch.empty((a.B, a.Di, a.N), device="cuda")
         co = torch.empty((a.B, a.Di, 4), device="cuda")
+        ws = False if a.route == "plain" else None
         if a.what == "conv":
             f = lambda: m.mamba_conv1d_silu_prefill(uo, x, w, None, None, co)
         elif a.what == "fused":
-            f = lambda: m.mamba_mixer_prefill(y, x, dt, Bm, Cm, w, A, None, D, dtb, z, None, co, None, so)
+            f = lambda: m.mamba_mixer_prefill(y, x, dt, Bm, Cm, w, A, None, D, dtb, z, None, co, None, so,
+                                              workspace=ws)
         else:
-            f = lambda: m.mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A, D, dtb, z, None, so)
+            f = lambda: m.mamba_selective_scan_prefill(y, u, dt, Bm, Cm, A, D, dtb, z, None, so, workspace=ws)
     else:
         st = torch.randn((a.L, a.B, a.Di, a.N if a.what in ("step", "mixer") else 4), generator=g, device="cuda")
         x, u, dt, z = r((a.B, a.Di)), r((a.B, a.Di)), r((a.B, a.Di), 0.1), r((a.B, a.Di))

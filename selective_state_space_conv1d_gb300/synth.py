@@ -133,6 +133,21 @@ def mixer_params(seed: int, d_inner: int, d_state: int, d_conv: int, layer: int 
     }
 
 
+def parity_params(seed: int, d_inner: int, d_state: int, d_conv: int, layer: int = 0) -> dict:
+    """Per-layer parameters for parity cases, varied per channel and per state
+    so that a kernel reading a parameter at the wrong channel or state fails:
+      A_log[c, n] = log(U(0.5, 16))  (A from -0.5 to -16, independent per (c, n))
+      D[c] ~ N(1, 0.5^2),  conv_b[c] ~ N(0, 0.2^2),  dt_bias and conv_w as in
+      the workload recipe.  The workloads keep mixer_params."""
+    g = generator(seed, "A_log", layer)
+    A_log = np.log(g.uniform(0.5, 16.0, size=(d_inner, d_state)))
+    p = mixer_params(seed, d_inner, d_state, d_conv, layer)
+    p["A_log"] = A_log.astype(np.float32)
+    p["D"] = (1.0 + 0.5 * generator(seed, "D", layer).standard_normal(d_inner)).astype(np.float32)
+    p["conv_b"] = normal(seed, "conv_b", (d_inner,), 0.2, layer=layer)
+    return p
+
+
 def prefill_inputs(seed: int, batch: int, seqlen: int, d_inner: int, d_state: int,
                    dtype: str = "f32", names=("x", "u", "dt", "z", "B", "C"),
                    t_offset_part: int = 0) -> dict:

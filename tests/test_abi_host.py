@@ -176,11 +176,11 @@ def test_decode_graph_rejects_bad_arguments_on_host(lib):
 
 
 def test_mixer_prefill_refuses_other_d_conv_on_host(lib):
-    for K, code in ((3, m.MAMBA_ERR_UNSUPPORTED), (8, m.MAMBA_ERR_UNSUPPORTED)):
+    for K, code in ((0, m.MAMBA_ERR_UNSUPPORTED), (5, m.MAMBA_ERR_UNSUPPORTED), (8, m.MAMBA_ERR_UNSUPPORTED)):
         rc = lib.mamba_mixer_prefill(FAKE, 64, 0, FAKE, 64, FAKE, 64, None, 0, FAKE, 16, FAKE, 16, 0,
                                      FAKE, None, None, None, FAKE, None, None, None, None,
                                      1, 8, 64, K, 16, None, 0, None)
-        assert rc == code and "d_conv=4" in m.mamba_last_error()
+        assert rc == code and "d_conv 1..4" in m.mamba_last_error()
     rc = lib.mamba_mixer_prefill(FAKE, 64, 0, FAKE, 64, FAKE, 64, None, 0, FAKE, 16, FAKE, 16, 7,
                                  FAKE, None, None, None, FAKE, None, None, None, None, 1, 8, 64, 4, 16, None, 0, None)
     assert rc == m.MAMBA_ERR_INVALID_ARG
@@ -234,3 +234,47 @@ def test_header_compiles_as_c99_and_library_links(lib, tmp_path):
     assert r.returncode == 0, r.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0 and run.stdout.strip().endswith("OK"), run.stdout + run.stderr
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    """The binding's copy of MAMBA_NOALLOC_SCRATCH_BYTES is the header's value."""
+    txt = open(os.path.join(ROOT, "include", "mamba_ssm.h")).read()
+    mm = re.search(r"#define\s+MAMBA_NOALLOC_SCRATCH_BYTES\s+\(([0-9L\s\*]+)\)", txt)
+    assert mm, "MAMBA_NOALLOC_SCRATCH_BYTES not found in the header"
+    value = 1
+    for factor in mm.group(1).split("*"):
+        value *= int(factor.strip().rstrip("L"))
+    assert value == m.MAMBA_NOALLOC_SCRATCH_BYTES
+
+
+@pytest.mark.parametrize("fn", ["mamba_selective_scan_prefill", "mamba_selective_scan_prefill_noalloc"])
+@pytest.mark.parametrize("bad", ["dt_dtype", "B_dtype", "short_B", "short_C", "short_z", "short_y", "short_dt",
+                                 "state_shape"])
+def test_scan_wrappers_refuse_mismatched_tensors_before_any_call(fn, bad):
+    """The C ABI cannot see allocation sizes, so both scan wrappers refuse a
+    tensor of another dtype or of fewer rows than the sizes say (host tensors:
+    nothing is loaded or launched)."""
+    import torch
+
+    Bsz, T, Di, N = 2, 8, 32, 16
+    f = lambda *s, dtype=torch.float32: torch.zeros(*s, dtype=dtype)
+    args = dict(y=f(Bsz, T, Di), u=f(Bsz, T, Di), dt=f(Bsz, T, Di), Bm=f(Bsz, T, N), Cm=f(Bsz, T, N),
+                A_log=f(Di, N), z=f(Bsz, T, Di), ssm_state_out=f(Bsz, Di, N))
+    if bad == "dt_dtype":
+        args["dt"] = f(Bsz, T, Di, dtype=torch.bfloat16)
+    elif bad == "B_dtype":
+        args["Bm"] = f(Bsz, T, N, dtype=torch.bfloat16)
+    elif bad == "short_B":
+        args["Bm"] = f(Bsz, T - 1, N)
+    elif bad == "short_C":
+        args["Cm"] = f(Bsz, T, N - 1)
+    elif bad == "short_z":
+        args["z"] = f(Bsz, T - 1, Di)
+    elif bad == "short_y":
+        args["y"] = f(Bsz, T - 1, Di)
+    elif bad == "short_dt":
+        args["dt"] = f(Bsz, T, Di - 1)
+    elif bad == "state_shape":
+        args["ssm_state_out"] = f(Bsz, Di, N - 1)
+    with pytest.raises(ValueError):
+        getattr(m, fn)(**args)

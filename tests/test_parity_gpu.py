@@ -20,9 +20,11 @@ SEED = 0x5EED1000
 
 
 def _params(seed, Di, N, K, layer=0, bias=True):
-    p = synth.mixer_params(seed, Di, N, K, layer)
-    if bias:
-        p["conv_b"] = synth.normal(seed, "conv_b", (Di,), 0.2, layer=layer)
+    """Parameters drawn per channel (and per state for A_log), so that a kernel
+    that reads one at the wrong channel or state cannot pass."""
+    p = synth.parity_params(seed, Di, N, K, layer)
+    if not bias:
+        p["conv_b"] = np.zeros(Di, np.float32)
     return p
 
 
@@ -142,7 +144,7 @@ SCAN_CASES = [
 
 def _scan_inputs(Bsz, T, Di, N, dtype, seed=SEED):
     a = synth.prefill_inputs(seed, Bsz, T, Di, N, dtype, names=("u", "dt", "z", "B", "C"))
-    p = synth.mixer_params(seed, Di, N, 4)
+    p = _params(seed, Di, N, 4)
     return a, p
 
 
@@ -209,15 +211,25 @@ def test_scan_routes_match_oracle(cuda_lib, route, Bsz, T, Di, N, dtype, y_dtype
     assert_within(s, s_ref, "state")
 
 
-def test_scan_workspace_too_small_falls_back_to_one_pass(cuda_lib):
+def test_scan_workspace_smaller_than_asked_splits_less_or_runs_one_pass(cuda_lib):
+    """With half the workspace the narrow shape is split into fewer parts (still
+    within the bound of the oracle); with less than two parts' worth it runs as
+    one sequential pass, bit for bit the no-workspace result."""
     m = cuda_lib
     Bsz, T, Di, N = 1, 1024, 128, 16
     a, p = _scan_inputs(Bsz, T, Di, N, "f32")
     need = m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
-    small = torch.empty(need // 2, dtype=torch.uint8, device="cuda")
-    y1, s1 = _run_scan(m, a, p, "f32", "f32", True, None, False, workspace=small)
-    y2, s2 = _run_scan(m, a, p, "f32", "f32", True, None, False, workspace=False)
-    assert np.array_equal(y1, y2) and np.array_equal(s1, s2)
+    y_ref, s_ref = oracle.selective_scan_prefill(a["u"], a["dt"], a["B"], a["C"], p["A_log"], p["D"],
+                                                 p["dt_bias"], a["z"], None)
+    half = torch.empty(need // 2, dtype=torch.uint8, device="cuda")
+    y1, s1 = _run_scan(m, a, p, "f32", "f32", True, None, False, workspace=half)
+    assert_within(y1, y_ref, "y (half workspace)")
+    assert_within(s1, s_ref, "state (half workspace)")
+    tiny = torch.empty(4096, dtype=torch.uint8, device="cuda")
+    y2, s2 = _run_scan(m, a, p, "f32", "f32", True, None, False, workspace=tiny)
+    y3, s3 = _run_scan(m, a, p, "f32", "f32", True, None, False, workspace=False)
+    assert np.array_equal(y2, y3) and np.array_equal(s2, s3)
+    assert_within(y3, y_ref, "y (one pass)")
 
 
 @pytest.mark.parametrize("Bsz,T,Di", [(1, 2000, 128), (8, 64, 512)])
@@ -312,7 +324,8 @@ def test_scan_delta_to_zero_keeps_state(cuda_lib, T, Di):
     s0 = synth.normal(SEED, "ssm_state", (Bsz, Di, N), 0.5)
     y, s = _run_scan(m, a, p, "f32", "f32", False, s0, False)
     assert np.array_equal(s, s0.astype(np.float64))
-    expect = np.einsum("btn,bcn->btc", a["C"].astype(np.float64), s0.astype(np.float64)) + a["u"]
+    expect = (np.einsum("btn,bcn->btc", a["C"].astype(np.float64), s0.astype(np.float64))
+              + p["D"].astype(np.float64) * a["u"])
     assert_within(y, expect, "y = C.h0 + D u")
 
 
@@ -393,7 +406,7 @@ def test_scan_is_deterministic_and_batch_rows_are_independent(cuda_lib):
 def test_ssm_step_matches_oracle_and_T1_prefill_bitwise(cuda_lib, N, dtype, y_dtype, gate):
     m = cuda_lib
     L, Bsz, Di = 3, 9, 160
-    p = synth.mixer_params(SEED + N, Di, N, 4, layer=2)
+    p = _params(SEED + N, Di, N, 4, layer=2)
     st_h = synth.normal(SEED, "ssm_state", (L, Bsz, Di, N), 0.5)
     st = to_dev(st_h)
     ref_state = st_h.astype(np.float64).copy()
@@ -506,6 +519,43 @@ def test_step_ring_and_direct_paths_agree_bitwise(cuda_lib, N, K, dtype, fused):
     assert m.mamba_device_faults(clear=True) == 0
 
 
+@pytest.mark.parametrize("fused", [True, False])
+def test_ring_step_with_per_channel_parameters_across_channel_blocks_matches_oracle(cuda_lib, fused):
+    """The copy-ring decode kernel keeps a channel block's parameters in
+    registers while its CTA walks consecutive (channel block, batch row)
+    tiles.  With batch 3 and 200 channel blocks every CTA crosses block
+    boundaries, and per-channel A_log, D, dt_bias and conv weights make a
+    stale or shifted parameter fail against the oracle."""
+    m = cuda_lib
+    L, Bsz, Di, N, K = 2, 3, 64 * 200, 16, 4
+    p = _params(SEED + 21, Di, N, K, layer=1)
+    pd = {k: to_dev(v) for k, v in p.items()}
+    conv_h = synth.normal(SEED, "conv_state", (L, Bsz, Di, K), 0.5)
+    ssm_h = synth.normal(SEED, "ssm_state", (L, Bsz, Di, N), 0.5)
+    conv, ssm = to_dev(conv_h), to_dev(ssm_h)
+    conv_ref, ssm_ref = conv_h.astype(np.float64), ssm_h.astype(np.float64)
+    for step in range(2):
+        inp = synth.decode_step_inputs(SEED + 21, 1, step, Bsz, Di, N, "f32")
+        x, dt, z, Bm, Cm = (to_dev(inp[k]) for k in ("x", "dt", "z", "B", "C"))
+        y = torch.empty((Bsz, Di), device="cuda")
+        if fused:
+            m.mamba_mixer_step_batched(y, x, dt, Bm, Cm, conv, ssm, 1, pd["conv_w"], pd["A_log"], pd["conv_b"],
+                                       pd["D"], pd["dt_bias"], z)
+            u_ref = oracle.conv1d_silu_step(inp["x"], conv_ref, 1, p["conv_w"], p["conv_b"])
+        else:
+            u_ref = inp["x"]
+            m.mamba_ssm_step_batched(y, x, dt, Bm, Cm, ssm, 1, pd["A_log"], pd["D"], pd["dt_bias"], z)
+        torch.cuda.synchronize()
+        y_ref = oracle.ssm_step(u_ref, inp["dt"], inp["B"], inp["C"], ssm_ref, 1, p["A_log"], p["D"],
+                                p["dt_bias"], inp["z"])
+        assert_within(to_host(y), y_ref, f"y step {step}")
+        assert_within(to_host(ssm[1]), ssm_ref[1], f"ssm state step {step}")
+        if fused:
+            assert np.array_equal(to_host(conv[1]), conv_ref[1])
+    assert np.array_equal(to_host(ssm[0]), ssm_h[0])
+    assert m.mamba_device_faults(clear=True) == 0
+
+
 def test_a_bounded_wait_that_runs_out_sets_the_fault_bit_and_the_device_stays_usable(cuda_lib):
     """The watchdog path without a fault: a CTA waits, with the copy rings'
     bounded wait, on an mbarrier that nothing completes.  The wait gives up
@@ -608,22 +658,29 @@ def test_decode_graph_reports_the_failing_step(cuda_lib):
 # ------------------------------------------------------- fused mixer prefill ----
 
 MIXER_PREFILL_CASES = [
-    # (B, T, Di, N, dtype, y_dtype, gate, states, strided x) -- T-split and sequential shapes
-    (1, 2048, 256, 16, "f32", "f32", True, True, False),
-    (1, 1500, 96, 16, "bf16", "f32", True, True, True),
-    (6, 333, 200, 16, "f32", "bf16", False, True, False),
-    (3, 77, 64, 64, "bf16", "f32", True, False, False),
-    (2, 2, 40, 8, "f32", "f32", True, True, False),  # T < K: the new conv state mixes state and x
-    (1, 999, 130, 4, "f32", "f32", True, True, True),
+    # (B, T, Di, N, K, dtype, y_dtype, gate, states, strided x) -- T-split and sequential shapes
+    (1, 2048, 256, 16, 4, "f32", "f32", True, True, False),
+    (1, 1500, 96, 16, 4, "bf16", "f32", True, True, True),
+    (6, 333, 200, 16, 4, "f32", "bf16", False, True, False),
+    (3, 77, 64, 64, 4, "bf16", "f32", True, False, False),
+    (2, 2, 40, 8, 4, "f32", "f32", True, True, False),  # T < K: the new conv state mixes state and x
+    (1, 999, 130, 4, 4, "f32", "f32", True, True, True),
+    # every fused d_conv below 4, on both routes and both dtypes
+    (1, 1700, 96, 16, 3, "f32", "f32", True, True, False),
+    (2, 300, 72, 16, 3, "bf16", "f32", True, True, True),
+    (1, 1300, 64, 8, 2, "bf16", "bf16", False, True, False),
+    (3, 200, 136, 16, 2, "f32", "f32", True, True, False),
+    (1, 900, 64, 32, 1, "f32", "f32", True, True, False),
+    (2, 1, 48, 16, 1, "bf16", "f32", True, True, False),
+    (2, 1, 48, 16, 3, "f32", "f32", True, True, False),   # T < K - 1
 ]
 
 
 @pytest.mark.parametrize("inplace", [False, True])
-@pytest.mark.parametrize("Bsz,T,Di,N,dtype,y_dtype,gate,states,strided", MIXER_PREFILL_CASES)
-def test_mixer_prefill_equals_conv_then_scan_bitwise(cuda_lib, inplace, Bsz, T, Di, N, dtype, y_dtype, gate,
+@pytest.mark.parametrize("Bsz,T,Di,N,K,dtype,y_dtype,gate,states,strided", MIXER_PREFILL_CASES)
+def test_mixer_prefill_equals_conv_then_scan_bitwise(cuda_lib, inplace, Bsz, T, Di, N, K, dtype, y_dtype, gate,
                                                       states, strided):
     m = cuda_lib
-    K = 4
     p = _params(SEED + 11, Di, N, K)
     pd = {k: to_dev(v) for k, v in p.items()}
     a = synth.prefill_inputs(SEED + 11, Bsz, T, Di, N, dtype, names=("x", "dt", "z", "B", "C"))

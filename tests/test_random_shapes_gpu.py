@@ -45,7 +45,7 @@ def test_random_shape_matches_oracle(cuda_lib, i):
     c = _draw(i)
     Bsz, T, Di, N, K, dtype = c["Bsz"], c["T"], c["Di"], c["N"], c["K"], c["dtype"]
     seed = 0x5EED_2100 + i
-    p = synth.mixer_params(seed, Di, N, K)
+    p = synth.parity_params(seed, Di, N, K)
     pd = {k: to_dev(v) for k, v in p.items()}
     a = synth.prefill_inputs(seed, Bsz, T, Di, N, dtype, names=("x", "dt", "z", "B", "C"))
     ld = Di + c["pad"]
@@ -75,7 +75,7 @@ def test_random_shape_matches_oracle(cuda_lib, i):
     assert_within(to_host(y1), y_ref, f"case {i} {c}: y")
     assert_within(to_host(s1), s_ref, f"case {i} {c}: ssm state")
 
-    if K == 4:
+    if K <= m.MAMBA_MAX_FUSED_D_CONV:
         y2 = torch.empty_like(y1)
         c2, s2 = torch.empty_like(c1), torch.empty_like(s1)
         m.mamba_mixer_prefill(y2, x, dt, Bm, Cm, pd["conv_w"], pd["A_log"], pd["conv_b"], pd["D"], pd["dt_bias"],
