@@ -1,14 +1,17 @@
 #!/usr/bin/env python3
 """Benchmark of the GB300 Mamba-1 mixer core.
 
-Headline (one JSON line on rank 0): prefill tokens/s of one mamba-130m-shaped
-layer (batch 1, T 2048, d_inner 1536, d_state 16, d_conv 4, f32) -- one step is
-the conv1d+SiLU prefill followed by the selective-scan prefill, through the C
-ABI, on seeded synthetic inputs already resident in HBM.  The same line carries
-the decode workload (24 layers x batch 128 T=1 steps; decode steps/s) and the
-mamba-2.8b-shaped bf16 prefill under "extra", the HBM roofline of the dominant
-kernel, the end-to-end figure (host buffers, copies inside the timed region),
-the f64 CPU oracle timed on the host cores, and the SM clocks seen.
+Headline (one JSON line on rank 0): prefill tokens/s of one mamba-2.8b-shaped
+layer (batch 8, T 4096, d_inner 5120, d_state 16, d_conv 4; x/dt/z/B/C stored
+in bf16, f32 arithmetic, f32 y) -- one step is the whole mixer-core prefill
+(conv1d+SiLU and the selective scan with its gate, fused or as two calls,
+whichever is faster: the two give the same bits), through the C ABI, on seeded
+synthetic inputs already resident in HBM.  The same line carries the roofline
+of the dominant call, the end-to-end figure (host buffers, copies inside the
+timed region), the f64 CPU oracle timed on the host cores for every workload,
+the SM clocks seen, and under "extra" the other workloads: the mamba-130m
+layer prefill (f32), the long-context continuation, the 24-layer batch-128
+decode, the Mamba-3 SISO decode and the prefill-versus-steps comparison.
 
 Launch: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 N > 1 runs under torch.distributed.run: every rank runs an independent replica
@@ -284,19 +287,107 @@ def roofline(bytes_per_launch, ms, peak, peak_src, traffic):
             "algorithmic_bytes_per_launch": int(bytes_per_launch), "avg_launch_ms": round(ms, 6)}
 
 
-# MUFU peak of GB300: ex2 issues 32 lanes/clk/SM (lg2 and rcp 16, counted as 2
-# slots each), 152 SMs, 2070 MHz maximum SM clock.
-MUFU_SLOTS_PER_CLK_SM = 32
 GB300_SMS = 152
 GB300_MAX_SM_MHZ = 2070.0
+# FP32 pipe of GB300: 128 lanes/clk/SM (an FMA counts as one operation)
+FP32_LANES_PER_CLK_SM = 128
+
+# MUFU throughput probe: every thread runs 8 independent chains of
+# ex2.approx.ftz.f32 (or fma.rn.f32), and each CTA times itself with clock64;
+# lanes per clock per SM = operations / (cycles of the slowest CTA on an SM).
+_PROBE_SRC = r"""
+#include <cuda_runtime.h>
+template <int OP>
+__global__ void probe(float* out, long long* cyc, int iters) {
+  float v[8];
+  for (int j = 0; j < 8; ++j) v[j] = -1e-3f * (threadIdx.x + j);
+  const long long t0 = clock64();
+  for (int i = 0; i < iters; ++i) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (OP == 0) asm volatile("ex2.approx.ftz.f32 %0, %0;" : "+f"(v[j]));
+      else asm volatile("fma.rn.f32 %0, %0, 0f3F7FFFF0, 0f3A83126F;" : "+f"(v[j]));
+    }
+  }
+  const long long t1 = clock64();
+  float s = 0.f;
+  for (int j = 0; j < 8; ++j) s += v[j];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+extern "C" int run_probe(int op, int blocks, int threads, int iters, double* lanes_per_clk_sm) {
+  float* out; long long* cyc;
+  if (cudaMalloc(&out, sizeof(float) * blocks * threads) != cudaSuccess) return 1;
+  if (cudaMalloc(&cyc, sizeof(long long) * blocks) != cudaSuccess) return 1;
+  for (int rep = 0; rep < 2; ++rep) {
+    if (op == 0) probe<0><<<blocks, threads>>>(out, cyc, iters);
+    else probe<1><<<blocks, threads>>>(out, cyc, iters);
+  }
+  if (cudaDeviceSynchronize() != cudaSuccess) return 2;
+  long long* h = new long long[blocks];
+  cudaMemcpy(h, cyc, sizeof(long long) * blocks, cudaMemcpyDeviceToHost);
+  long long mx = 0;
+  for (int i = 0; i < blocks; ++i) mx = h[i] > mx ? h[i] : mx;
+  delete[] h;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const double ops_per_sm = (double)blocks / sms * threads * iters * 8.0;
+  *lanes_per_clk_sm = ops_per_sm / (double)mx;
+  cudaFree(out); cudaFree(cyc);
+  return 0;
+}
+"""
+
+
+def alu_probe():
+    """ex2 and FP32-FMA lanes per SM clock, measured on this GPU (None if nvcc
+    or the run fails).  Eight CTAs of 256 threads per SM, chains long enough to
+    run for milliseconds."""
+    import ctypes
+
+    try:
+        d = tempfile.mkdtemp(prefix="mamba_probe_")
+        src, lib = os.path.join(d, "probe.cu"), os.path.join(d, "probe.so")
+        with open(src, "w") as f:
+            f.write(_PROBE_SRC)
+        nvcc = "nvcc" if subprocess.run(["which", "nvcc"], capture_output=True).returncode == 0 \
+            else "/usr/local/cuda/bin/nvcc"
+        r = subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-shared", "-Xcompiler",
+                            "-fPIC", "-o", lib, src], capture_output=True, text=True)
+        if r.returncode != 0:
+            return None
+        so = ctypes.CDLL(lib)
+        so.run_probe.argtypes = (ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 ctypes.POINTER(ctypes.c_double))
+        import torch
+
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        res = {}
+        for name, op, iters in (("ex2", 0, 20000), ("ffma", 1, 40000)):
+            v = ctypes.c_double(0.0)
+            if so.run_probe(op, 8 * sms, 256, iters, ctypes.byref(v)) != 0:
+                return None
+            res[name] = round(v.value, 2)
+        return res
+    except Exception:
+        return None
+
+
+_ALU = {"probe": None}
+
+
+def mufu_lanes_per_clk():
+    """Measured ex2 lanes per clock per SM (the probe), else the unit count 32."""
+    p = _ALU["probe"]
+    if p and p.get("ex2"):
+        return p["ex2"], "measured: ex2.approx.ftz.f32 throughput probe (8 independent chains per thread)"
+    return 32.0, "derived: 32 ex2 lanes/clk/SM (unit count; the probe did not run)"
 
 
 def mufu_peak_tops(sm_count=GB300_SMS):
-    return MUFU_SLOTS_PER_CLK_SM * sm_count * GB300_MAX_SM_MHZ * 1e6 / 1e12
-
-
-# FP32 pipe of GB300: 128 lanes/clk/SM (an FMA counts as one operation)
-FP32_LANES_PER_CLK_SM = 128
+    lanes, _ = mufu_lanes_per_clk()
+    return lanes * sm_count * GB300_MAX_SM_MHZ * 1e6 / 1e12
 
 
 def fp32_peak_tops(sm_count=GB300_SMS):
@@ -321,8 +412,8 @@ def scan_roofline(tc, N, gate, bytes_per_launch, ms, hbm_peak_gbs, peak_src, tra
     fpeak = fp32_peak_tops(sm_count)
     return {"bound": "alu", "achieved": round(tops, 3), "peak": round(peak, 3),
             "unit": "T MUFU-slot/s", "frac": round(tops / peak, 4), "traffic": traffic,
-            "peak_source": f"derived: {MUFU_SLOTS_PER_CLK_SM} ex2/clk/SM x {sm_count} SMs x "
-                           f"{GB300_MAX_SM_MHZ:.0f} MHz",
+            "peak_source": f"{mufu_lanes_per_clk()[1]}: {mufu_lanes_per_clk()[0]} ex2 lanes/clk/SM x "
+                           f"{sm_count} SMs x {GB300_MAX_SM_MHZ:.0f} MHz",
             "algorithmic_mufu_slots_per_launch": int(slots),
             "algorithmic_bytes_per_launch": int(bytes_per_launch), "avg_launch_ms": round(ms, 6),
             "hbm": {"achieved": round(gbs, 1), "peak": hbm_peak_gbs, "unit": "GB/s",
@@ -354,6 +445,10 @@ def run_prefill(torch, m, synth, wl_index, steps, warmup, device, dist, clocks, 
         s.__dict__.update({k: (v.clone() if hasattr(v, "clone") else v) for k, v in first.__dict__.items()})
         s.p = first.p
         sets.append(s)
+    # the clock record spans the warm-up, the per-kernel timings and the timed
+    # steps, so that it holds samples even when the timed steps last milliseconds
+    if clocks:
+        clocks.start()
     # warm-up steps (eager), then graphs
     for i in range(max(warmup, 3)):
         sets[i % n_sets].conv(m)
@@ -365,9 +460,12 @@ def run_prefill(torch, m, synth, wl_index, steps, warmup, device, dist, clocks, 
     fused_ms = kernel_time(torch, [lambda s=s: s.fused(m) for s in sets], n_k)
     # both forms compute the same result bit for bit: the step is the faster one
     use_fused = fused_ms < conv_ms + scan_ms
-    total_ms, ck = timed_graph_run(torch, m, sets, steps, 100, clocks, dist, fused=use_fused)
+    total_ms, _ = timed_graph_run(torch, m, sets, steps, 100, None, dist, fused=use_fused)
+    ck = clocks.stop() if clocks else None
+    if ck is not None:
+        ck["window"] = "this workload's warm-up, per-kernel timing graphs and timed steps"
     u_bytes = 2 * first.u.numel() * first.u.element_size()  # the u write + read the fusion drops
-    scan_launches = 2 if m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N) > 0 else 1
+    route = scan_route(m, Bsz, T, Di, N, props.multi_processor_count)
     l2_note = (f"inputs > 3x L2 ({set_bytes / 1e6:.0f} MB per step)" if n_sets == 1 else
                f"rotating {n_sets} resident buffer sets ({n_sets * set_bytes / 1e6:.0f} MB > 3x the "
                f"{l2 / 1e6:.0f} MB L2)")
@@ -376,22 +474,39 @@ def run_prefill(torch, m, synth, wl_index, steps, warmup, device, dist, clocks, 
         "ms_per_step": total_ms / steps, "conv_ms": conv_ms, "scan_ms": scan_ms, "fused_ms": fused_ms,
         "use_fused": use_fused,
         "fused_bytes": conv_b + scan_b - u_bytes,
-        "scan_launches": scan_launches, "conv_bytes": conv_b, "scan_bytes": scan_b,
+        "route": route, "conv_bytes": conv_b, "scan_bytes": scan_b,
         "tokens_per_step": Bsz * T, "clocks": ck, "l2_note": l2_note,
     }
 
 
+def scan_route(m, Bsz, T, Di, N, sms):
+    """The route the library plans for a prefill with its default workspace:
+    chained (one launch of persistent CTAs) for at least eight 32-channel tiles
+    per SM, the T split (state-only pass, fold, full pass: three launches) for
+    narrower shapes that get a workspace, else one warp per tile (one launch)."""
+    ws = m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N)
+    tiles = Bsz * ((Di + 31) // 32)
+    if ws > 0:
+        return "chained" if tiles >= 8 * sms else "split"
+    return "plain"
+
+
+ROUTE_DESC = {
+    "chained": "one launch: persistent CTAs, rows cut into equal roles, tiles handed between roles",
+    "split": "T-split: state-only pass, fold, full pass: 3 launches",
+    "plain": "one launch: one warp per 32-channel tile",
+}
+
+
 def step_desc(res, fused):
-    split = res["scan_launches"] == 2
+    r = ROUTE_DESC[res["route"]]
     if fused:
-        return ("mamba_mixer_prefill: conv1d+SiLU fused into the selective scan ("
-                + ("T-split: state-only pass, fold, full pass: 3 launches" if split else "1 launch") + ")")
-    return ("mamba_conv1d_silu_prefill then mamba_selective_scan_prefill ("
-            + ("4 launches: conv, state-only pass, fold, full pass" if split else "2 launches") + ")")
+        return "mamba_mixer_prefill: conv1d+SiLU fused into the selective scan (" + r + ")"
+    return "mamba_conv1d_silu_prefill (1 launch) then mamba_selective_scan_prefill (" + r + ")"
 
 
 def launches_per_step(res, fused):
-    return (0 if fused else 1) + (3 if res["scan_launches"] == 2 else 1)
+    return (0 if fused else 1) + (3 if res["route"] == "split" else 1)
 
 
 def other_form_line(res):
@@ -422,8 +537,11 @@ def run_e2e(torch, m, res, steps, device):
     copies its inputs host->device and reads y and both final states back."""
     wl, host = res["wl"], res["host"]
     s = res["sets"][0]
-    pin = lambda a, like: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(like.dtype).pin_memory()
-    hin = {k: pin(host[k], getattr(s, k)) for k in ("x", "dt", "z", "B", "C")}
+    if host is not None:
+        pin = lambda a, like: torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(like.dtype).pin_memory()
+        hin = {k: pin(host[k], getattr(s, k)) for k in ("x", "dt", "z", "B", "C")}
+    else:  # inputs drawn on the device: their pinned host copies are the step's inputs
+        hin = {k: getattr(s, k).cpu().pin_memory() for k in ("x", "dt", "z", "B", "C")}
     hy = torch.empty(s.y.shape, dtype=s.y.dtype).pin_memory()
     hc = torch.empty(s.conv_out.shape).pin_memory()
     hs = torch.empty(s.ssm_out.shape).pin_memory()
@@ -464,7 +582,13 @@ def run_e2e(torch, m, res, steps, device):
     # stream and step i's outputs come down on another, so the copies of
     # neighbouring steps overlap step i's kernels (every step still moves
     # all of its bytes inside the timed region)
-    sets2 = res["sets"][:2] if len(res["sets"]) >= 2 else [s, s]
+    if len(res["sets"]) >= 2:
+        sets2 = res["sets"][:2]
+    else:  # a second buffer set, so that neighbouring steps never share buffers
+        s2 = PrefillSet.__new__(PrefillSet)
+        s2.__dict__.update({k: (v.clone() if hasattr(v, "clone") else v) for k, v in s.__dict__.items()})
+        s2.p = s.p
+        sets2 = [s, s2]
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def pipelined():
@@ -626,6 +750,75 @@ def run_decode(torch, m, synth, device, peak, peak_src, n_steps=256):
     return out
 
 
+def run_long_context(torch, m, synth, device, peak, peak_src, sms):
+    """Long-context continuation (batch 4, d_inner 2048, d_state 16, d_conv 4,
+    f32): one mamba_mixer_prefill of 16384 tokens from a seeded state, then 64
+    fused T=1 steps replayed by the library's decode graph.  tokens/s counts
+    all 4 x 16448 tokens over the time of both."""
+    wl = synth.WORKLOADS[4]
+    Bsz, T, Di, N, K, S = wl.batch, wl.seqlen, wl.d_inner, wl.d_state, wl.d_conv, wl.steps
+    params = synth.mixer_params(wl.seed, Di, N, K)
+    pre = PrefillSet.from_device(torch, (Bsz, T, Di), N, params, "f32", device, wl.seed)
+    c0 = synth.torch_normal((Bsz, Di, K), 1.0, wl.seed + 41, device)
+    s0 = synth.torch_normal((Bsz, Di, N), 0.5, wl.seed + 42, device)
+    conv = torch.empty((1, Bsz, Di, K), device=device)
+    ssm = torch.empty((1, Bsz, Di, N), device=device)
+    xs = synth.torch_normal((S, Bsz, Di), 1.0, wl.seed + 43, device)
+    zs = synth.torch_normal((S, Bsz, Di), 1.0, wl.seed + 44, device)
+    dts = synth.torch_normal((S, Bsz, Di), 0.1, wl.seed + 45, device)
+    Bs = synth.torch_normal((S, Bsz, N), 1.0, wl.seed + 46, device)
+    Cs = synth.torch_normal((S, Bsz, N), 1.0, wl.seed + 47, device)
+    ys = torch.empty((S, Bsz, Di), device=device)
+    p = pre.p
+
+    def prefill():
+        m.mamba_mixer_prefill(pre.y, pre.x, pre.dt, pre.B, pre.C, p["conv_w"], p["A_log"], p["conv_b"], p["D"],
+                              p["dt_bias"], pre.z, c0, conv[0], s0, ssm[0])
+
+    io = [[{"y": ys[t], "x": xs[t], "dt": dts[t], "z": zs[t], "Bm": Bs[t], "Cm": Cs[t]}] for t in range(S)]
+    prefill()
+    torch.cuda.synchronize()
+    with m.DecodeGraph([p], io, conv, ssm) as g:
+        def step():
+            prefill()
+            g.launch()
+        step()
+        torch.cuda.synchronize()
+        pre_g = capture(torch, prefill)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 5
+        a.record()
+        for _ in range(reps):
+            pre_g.replay()
+            g.launch()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        pre_ms = kernel_time(torch, [prefill], 5)
+        decode_kernels = g.kernels
+        del pre_g
+    route = scan_route(m, Bsz, T, Di, N, sms)
+    _, scan_b = pre.bytes_per_step()
+    conv_b, _ = pre.bytes_per_step()
+    fused_bytes = conv_b + scan_b - 2 * pre.x.numel() * pre.x.element_size()
+    tokens = Bsz * (T + S)
+    out = {
+        "workload": wl.name, "value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+        "step": f"mamba_mixer_prefill over {T} tokens ({ROUTE_DESC[route]}) then {S} fused T=1 steps "
+                f"(mamba_decode_graph, {decode_kernels} kernels)",
+        "prefill_ms": round(pre_ms, 5), "decode_ms": round(ms - pre_ms, 5),
+        "config": {"batch": Bsz, "seq_len": T, "decode_steps": S, "d_inner": Di, "d_state": N, "d_conv": K,
+                   "state": "seeded (ssm N(0, 0.5^2), conv N(0, 1))",
+                   "inputs": "torch device RNG, the tiny-mixer distributions",
+                   "l2": f"{fused_bytes / 1e9:.2f} GB per prefill > L2"},
+        "gpu_launches_per_step": (3 if route == "split" else 1) + decode_kernels,
+    }
+    tc = Bsz * T * Di
+    out["roofline"] = scan_roofline(tc, N, True, fused_bytes, pre_ms, peak, peak_src,
+                                    ncu_traffic("fused", wl.name), sms, conv=True)
+    return out
+
+
 def run_prefill_vs_steps(torch, m, synth, device, lengths=(128, 512, 2048), prompt=5, n_layers=24):
     """Parallel prefill against step-by-step prefill on the 130m layer shape
     (batch 1, d_inner 1536, d_state 16, d_conv 4, f32): one mamba_mixer_prefill
@@ -763,50 +956,107 @@ def run_m3_decode(torch, m, device, peak, peak_src, n_steps=16, L=24, Bsz=128, H
 
 # ----------------------------------------------------------- CPU oracle arm --
 
-def oracle_prefill_sample(synth, wl_index, n_channels, nthreads):
-    """Run the f64 oracle (conv then scan) on the first n_channels channels of
-    the workload; returns (seconds, tokens-equivalent processed)."""
+def oracle_prefill_sample(synth, wl_index, n_channels, nthreads, stride=1):
+    """Run the f64 oracle (conv then scan, from the workload's initial state) on
+    n_channels channels of the workload (every `stride`-th); returns (seconds,
+    tokens-equivalent processed = B*T*n_channels/Di).  Channels are independent
+    recurrences, so a sample is a full-fidelity run of those channels."""
     import oracle
 
     wl = synth.WORKLOADS[wl_index]
     Bsz, T, Di, N, K = wl.batch, wl.seqlen, wl.d_inner, wl.d_state, wl.d_conv
+    sel = np.arange(0, Di, stride)[:n_channels]
+    g = np.random.default_rng(wl.seed)
+    # the sample's inputs, drawn from the workload's distributions (only the
+    # sampled channels: drawing a whole 2.8b layer on the host takes longer than
+    # the oracle's sample)
+    x = g.standard_normal((Bsz, T, len(sel)))
+    dt = 0.1 * g.standard_normal((Bsz, T, len(sel)))
+    z = g.standard_normal((Bsz, T, len(sel)))
+    if wl.dtype == "bf16":
+        x, dt, z = (synth.round_to_bf16(v.astype(np.float32)).astype(np.float64) for v in (x, dt, z))
+    Bm = g.standard_normal((Bsz, T, N))
+    Cm = g.standard_normal((Bsz, T, N))
     params = synth.mixer_params(wl.seed, Di, N, K)
-    host = synth.prefill_inputs(wl.seed, Bsz, T, Di, N, wl.dtype, names=("x", "dt", "z", "B", "C"))
-    sel = slice(0, n_channels)
-    x, dt, z = (np.ascontiguousarray(host[k][:, :, sel], np.float64) for k in ("x", "dt", "z"))
-    Bm, Cm = host["B"].astype(np.float64), host["C"].astype(np.float64)
     p = {k: np.ascontiguousarray(v[sel], np.float64) for k, v in params.items()}
+    s0 = 0.5 * g.standard_normal((Bsz, len(sel), N)) if wl.state == "seeded" else None
+    c0 = g.standard_normal((Bsz, len(sel), K)) if wl.state == "seeded" else None
     t0 = time.perf_counter()
-    u, _ = oracle.conv1d_silu_prefill(x, p["conv_w"], p["conv_b"], None, nthreads=nthreads)
-    oracle.selective_scan_prefill(u, dt, Bm, Cm, p["A_log"], p["D"], p["dt_bias"], z, None,
-                                  nthreads=nthreads)
+    u, _ = oracle.conv1d_silu_prefill(x, p["conv_w"], p["conv_b"], c0, nthreads=nthreads)
+    oracle.selective_scan_prefill(u, dt, Bm, Cm, p["A_log"], p["D"], p["dt_bias"], z, s0, nthreads=nthreads)
     dtm = time.perf_counter() - t0
-    return dtm, Bsz * T * n_channels / Di
+    return dtm, Bsz * T * len(sel) / Di
 
 
-def cpu_baseline(synth, budget_s=10.0):
+def oracle_decode_sample(synth, n_rows, n_layers, n_steps, nthreads):
+    """The oracle's fused T=1 step (conv step then SSM step) over n_rows batch
+    rows x channels of the 24-layer decode state, n_steps steps of n_layers
+    layers; returns (seconds, full 24-layer batch-128 steps equivalent)."""
+    import oracle
+
+    wl = synth.WORKLOADS[2]
+    L, Bsz, Di, N, K = wl.n_layers, wl.batch, wl.d_inner, wl.d_state, wl.d_conv
+    g = np.random.default_rng(wl.seed)
+    ch = max(1, n_rows // Bsz)
+    conv = 0.5 * g.standard_normal((n_layers, Bsz, ch, K))
+    ssm = 0.5 * g.standard_normal((n_layers, Bsz, ch, N))
+    params = [synth.mixer_params(wl.seed, Di, N, K, layer=l) for l in range(n_layers)]
+    ps = [{k: np.ascontiguousarray(v[:ch], np.float64) for k, v in pl.items()} for pl in params]
+    inp = [[(g.standard_normal((Bsz, ch)), 0.1 * g.standard_normal((Bsz, ch)), g.standard_normal((Bsz, ch)),
+             g.standard_normal((Bsz, N)), g.standard_normal((Bsz, N))) for _ in range(n_layers)]
+           for _ in range(n_steps)]
+    t0 = time.perf_counter()
+    for s_ in range(n_steps):
+        for l in range(n_layers):
+            x, dt, z, Bm, Cm = inp[s_][l]
+            u = oracle.conv1d_silu_step(x, conv, l, ps[l]["conv_w"], ps[l]["conv_b"], nthreads=nthreads)
+            oracle.ssm_step(u, dt, Bm, Cm, ssm, l, ps[l]["A_log"], ps[l]["D"], ps[l]["dt_bias"], z,
+                            nthreads=nthreads)
+    dtm = time.perf_counter() - t0
+    full = n_steps * (n_layers / L) * (Bsz * ch) / (Bsz * Di)
+    return dtm, full
+
+
+def cpu_baseline(synth, headline_wl=3):
+    """The f64 oracle as it stands, on all host cores, per workload: bounded
+    samples of independent channels (or rows), each about 2-10 s, with the
+    throughput scaled to the whole workload; plus one thread on the headline
+    workload."""
     import oracle
 
     nthreads = oracle.default_threads()
-    wl = synth.WORKLOADS[1]
-    total_s, total_tok, reps = 0.0, 0.0, 0
-    while total_s < budget_s:
-        s, tok = oracle_prefill_sample(synth, 1, wl.d_inner, nthreads)
-        total_s += s
-        total_tok += tok
-        reps += 1
-    # one thread on 192-channel slices (the channels are independent rows), for about a second
-    s1, tok1 = 0.0, 0.0
-    while s1 < 1.0:
-        s, tok = oracle_prefill_sample(synth, 1, 192, 1)
-        s1 += s
-        tok1 += tok
-    return {"value": round(total_tok / total_s, 1), "unit": "tokens/s", "cores": nthreads,
-            "kind": "oracle",
-            "sample": f"{reps} full passes of the 130m-layer prefill (1x2048x1536, d_state 16): "
-                      f"f64 conv+scan, {total_s:.1f} s of wall time on {nthreads} threads",
-            "single_core": {"value": round(tok1 / s1, 1), "unit": "tokens/s",
-                            "sample": f"channels 0..191 of the same prefill on 1 thread, repeated for {s1:.2f} s"}}
+    per = {}
+
+    def timed(fn, budget):
+        tot_s, tot_u, reps = 0.0, 0.0, 0
+        while tot_s < budget:
+            s_, u_ = fn()
+            tot_s += s_
+            tot_u += u_
+            reps += 1
+        return tot_s, tot_u, reps
+
+    for wl_index, n_ch, budget in ((1, 1536, 6.0), (3, 256, 6.0), (4, 128, 4.0)):
+        wl = synth.WORKLOADS[wl_index]
+        stride = max(1, wl.d_inner // n_ch)
+        sec, tok, reps = timed(lambda: oracle_prefill_sample(synth, wl_index, n_ch, nthreads, stride), budget)
+        per[wl.name] = {"value": round(tok / sec, 1), "unit": "tokens/s", "cores": nthreads,
+                        "sample": f"{reps} x {n_ch} of {wl.d_inner} channels (every {stride}-th), all "
+                                  f"{wl.batch} x {wl.seqlen} tokens, f64 conv+scan; {sec:.1f} s of wall time; "
+                                  f"tokens/s scaled by d_inner / channels"}
+    sec, steps, reps = timed(lambda: oracle_decode_sample(synth, 128 * 16, 24, 2, nthreads), 4.0)
+    per[synth.WORKLOADS[2].name] = {
+        "value": round(steps / sec, 3), "unit": "steps/s", "cores": nthreads,
+        "sample": f"{reps} x 2 steps x 24 layers on batch 128 x 16 of 1536 channels, f64 conv step + SSM step; "
+                  f"{sec:.1f} s; steps/s scaled to all 1536 channels"}
+    wl = synth.WORKLOADS[headline_wl]
+    s1, t1, _ = timed(lambda: oracle_prefill_sample(synth, headline_wl, 16, 1, wl.d_inner // 16), 1.5)
+    head = per[wl.name]
+    return {"value": head["value"], "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": head["sample"],
+            "single_core": {"value": round(t1 / s1, 1), "unit": "tokens/s",
+                            "sample": f"16 channels of the same workload on 1 thread, {s1:.2f} s"},
+            "per_workload": per}
 
 
 def replica_throughput(torch, local_ms, tokens_per_step, steps, world, dist=None, device=None):
@@ -822,29 +1072,33 @@ def replica_throughput(torch, local_ms, tokens_per_step, steps, world, dist=None
 
 
 def run_reference(args, rank, world):
-    """The oracle as the reference arm: the f64 CPU oracle on this host's cores."""
+    """The oracle as the reference arm: the f64 CPU oracle on this host's cores,
+    on the headline workload (the mamba-2.8b layer prefill), each step a
+    bounded sample of its channels."""
     from selective_state_space_conv1d_gb300 import synth
     import oracle
 
     if rank != 0:
         return
     nthreads = oracle.default_threads()
-    wl = synth.WORKLOADS[1]
+    wl = synth.WORKLOADS[HEADLINE_WL]
     n_steps = args.steps + args.warmup
-    # size the per-step sample so the whole run stays within ~2 minutes
-    one_s, _ = oracle_prefill_sample(synth, 1, 16, nthreads)
-    per_ch = one_s / 16
-    n_ch = int(max(1, min(wl.d_inner, (120.0 / max(n_steps, 1)) / max(per_ch, 1e-9))))
+    # size the per-step sample so the whole run stays within --ref-budget seconds
+    one_s, _ = oracle_prefill_sample(synth, HEADLINE_WL, 8, nthreads, wl.d_inner // 8)
+    per_ch = one_s / 8
+    n_ch = int(max(1, min(wl.d_inner, (args.ref_budget / max(n_steps, 1)) / max(per_ch, 1e-9))))
+    stride = max(1, wl.d_inner // n_ch)
     for _ in range(args.warmup):
-        oracle_prefill_sample(synth, 1, n_ch, nthreads)
+        oracle_prefill_sample(synth, HEADLINE_WL, n_ch, nthreads, stride)
     tot_s, tot_tok = 0.0, 0.0
     for _ in range(args.steps):
-        s, tok = oracle_prefill_sample(synth, 1, n_ch, nthreads)
-        tot_s += s
+        s_, tok = oracle_prefill_sample(synth, HEADLINE_WL, n_ch, nthreads, stride)
+        tot_s += s_
         tot_tok += tok
     value = tot_tok / tot_s
-    sample = (f"first {n_ch} of {wl.d_inner} channels of the 130m-layer prefill per step "
-              f"(1x2048, d_state 16), f64 conv+scan")
+    sample = (f"{n_ch} of {wl.d_inner} channels (every {stride}-th) of the 2.8b-layer prefill per step "
+              f"({wl.batch}x{wl.seqlen}, d_state 16, bf16-rounded inputs), f64 conv+scan; tokens/s scaled by "
+              f"d_inner / channels")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -862,14 +1116,38 @@ def run_reference(args, rank, world):
 
 # --------------------------------------------------------------------- main --
 
+HEADLINE_WL = 3  # the mamba-2.8b layer prefill: the largest single-GPU prefill workload
+
+
+def prefill_line(res, peak, peak_src, sms):
+    """One prefill workload as an extra line: value, dominant call's roofline, the other form."""
+    wl = res["wl"]
+    return {
+        "workload": wl.name, "value": round(res["tokens_per_step"] / (res["ms_per_step"] * 1e-3), 1),
+        "unit": "tokens/s", "ms_per_step": round(res["ms_per_step"], 5),
+        "hbm_gbs_per_step": round((res["fused_bytes"] if res["use_fused"] else res["conv_bytes"] + res["scan_bytes"])
+                                  / (res["ms_per_step"] * 1e-3) / 1e9, 1),
+        "step": step_desc(res, res["use_fused"]),
+        "gpu_launches_per_step": launches_per_step(res, res["use_fused"]),
+        "roofline": prefill_roofline(res, peak, peak_src, sms),
+        "conv_roofline": roofline(res["conv_bytes"], res["conv_ms"], peak, peak_src, ncu_traffic("conv", wl.name)),
+        "other_form": other_form_line(res),
+        "config": {"batch": wl.batch, "seq_len": wl.seqlen, "d_inner": wl.d_inner, "d_state": wl.d_state,
+                   "d_conv": wl.d_conv, "storage": wl.dtype + " activations, f32 y/params/state",
+                   "l2": res["l2_note"]},
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-extra", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=120.0,
+                    help="--impl reference: seconds of oracle work for the whole run")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -897,46 +1175,41 @@ def main():
         td.init_process_group("nccl", device_id=device)
         dist = td
     m.load()
+    _ALU["probe"] = alu_probe()
     peak, peak_src = hbm_peak()
     clocks = ClockSampler(local_rank)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
 
-    res = run_prefill(torch, m, synth, 1, args.steps, args.warmup, device, dist, clocks)
+    # headline: the mamba-2.8b layer prefill (inputs drawn on the device: too
+    # large to draw on the host quickly; > 3x L2, so every step reads HBM)
+    res = run_prefill(torch, m, synth, HEADLINE_WL, args.steps, args.warmup, device, dist, clocks,
+                      host_inputs=False)
     total_ms, value = replica_throughput(torch, res["total_ms"], res["tokens_per_step"], args.steps, world, dist,
                                          device)
     ms_step = total_ms / args.steps
-    sms = torch.cuda.get_device_properties(device).multi_processor_count
-    wl1 = res["wl"]
-    scan_roof = prefill_roofline(res, peak, peak_src, sms)
-    conv_roof = roofline(res["conv_bytes"], res["conv_ms"], peak, peak_src,
-                         ncu_traffic("conv", res["wl"].name))
-    step_gbs = (res["conv_bytes"] + res["scan_bytes"]) / (ms_step * 1e-3) / 1e9
+    head_roof = prefill_roofline(res, peak, peak_src, sms)
+    conv_roof = roofline(res["conv_bytes"], res["conv_ms"], peak, peak_src, ncu_traffic("conv", res["wl"].name))
+    step_bytes = res["fused_bytes"] if res["use_fused"] else res["conv_bytes"] + res["scan_bytes"]
+    step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
 
     extra = {}
     if not args.no_extra:
+        r1 = run_prefill(torch, m, synth, 1, 2000, 3, device, None, None)
+        extra["prefill_130m_f32"] = prefill_line(r1, peak, peak_src, sms)
+        extra["prefill_130m_f32"]["e2e"] = run_e2e(torch, m, r1, 400, device)
+        del r1
+        torch.cuda.empty_cache()
+        extra["long_context_b4_t16384"] = run_long_context(torch, m, synth, device, peak, peak_src, sms)
+        torch.cuda.empty_cache()
         extra["decode_130m_b128_l24"] = run_decode(torch, m, synth, device, peak, peak_src)
         extra["decode_mamba3_siso"] = run_m3_decode(torch, m, device, peak, peak_src)
         extra["prefill_vs_steps"] = run_prefill_vs_steps(torch, m, synth, device)
-        r3 = run_prefill(torch, m, synth, 3, 50, 3, device, None, None, host_inputs=False)
-        extra["prefill_2p8b_bf16"] = {
-            "workload": r3["wl"].name, "value": round(r3["tokens_per_step"] / (r3["ms_per_step"] * 1e-3), 1),
-            "unit": "tokens/s", "ms_per_step": round(r3["ms_per_step"], 5),
-            "hbm_gbs_per_step": round((r3["conv_bytes"] + r3["scan_bytes"]) / (r3["ms_per_step"] * 1e-3) / 1e9, 1),
-            "step": step_desc(r3, r3["use_fused"]),
-            "roofline": prefill_roofline(r3, peak, peak_src, sms),
-            "conv_roofline": roofline(r3["conv_bytes"], r3["conv_ms"], peak, peak_src,
-                                      ncu_traffic("conv", r3["wl"].name)),
-            "other_form": other_form_line(r3),
-            "config": {"batch": 8, "seq_len": 4096, "d_inner": 5120, "d_state": 16, "d_conv": 4,
-                       "storage": "bf16 x/u/dt/z/B/C, f32 y/params/state", "l2": r3["l2_note"],
-                       "inputs": "torch device RNG, same distributions"},
-        }
-        del r3
 
-    e2e = run_e2e(torch, m, res, min(args.steps, 400), device)
+    e2e = run_e2e(torch, m, res, min(args.steps, 100), device)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(synth)
+        cpu = cpu_baseline(synth, HEADLINE_WL)
 
     if rank == 0:
         wl = res["wl"]
@@ -944,23 +1217,24 @@ def main():
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 6),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded Philox inputs with the tiny-mixer distributions)",
+            "data": "synthetic (seeded, the tiny-mixer distributions; inputs drawn on the device)",
             "config": {"workload": wl.name, "batch": wl.batch, "seq_len": wl.seqlen,
                        "d_inner": wl.d_inner, "d_state": wl.d_state, "d_conv": wl.d_conv,
+                       "storage": "bf16 x/dt/z/B/C, f32 y/params/state; arithmetic f32",
                        "step": step_desc(res, res["use_fused"]),
                        "parallelism": f"replicas x{world}", "l2": res["l2_note"],
-                       "launch": "CUDA graph replays of 100 steps"},
+                       "launch": "CUDA graph replays of up to 100 steps"},
             "hbm_gbs_per_step": round(step_gbs, 1),
-            "roofline": scan_roof,
+            "roofline": head_roof,
             "roofline_kernel": ("fused conv+scan prefill call" if res["use_fused"] else "selective-scan prefill call")
-                               + (" (T-split: state-only pass, fold, full pass)" if res["scan_launches"] == 2
-                                  else " (one sequential launch)"),
+                               + f" ({ROUTE_DESC[res['route']]})",
             "conv_roofline": conv_roof,
             "other_form": other_form_line(res),
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": launches_per_step(res, res["use_fused"]) * args.steps,
             "clocks": res["clocks"],
+            "alu_probe": _ALU["probe"],
             "extra": extra,
         }
         print(json.dumps(line), flush=True)
