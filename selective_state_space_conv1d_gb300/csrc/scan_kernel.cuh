@@ -678,17 +678,22 @@ cudaError_t launch_k(const ScanArgs& a, Work w, const ScanPlan& p, cudaStream_t 
     w.wpc = 1;  // one warp per tile: one-warp CTAs spread evenly over the SMs
     grid = w.n_roles;
   } else {
-    w.wpc = wpc;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     if (w.mode == kScanChained) {
       // one role per resident warp, one CTA per SM (at most one role per tile,
       // so a role spans at least T tile-rows and no tile is cut twice)
-      int dev = 0, sms = 0;
-      if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-      if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
       const int64_t warps = (int64_t)wpc * sms;
       w.n_roles = w.n_tiles < warps ? w.n_tiles : warps;
       w.span = (w.n_tiles * a.T + w.n_roles - 1) / w.n_roles;
+    } else {
+      // a split pass with few roles spreads them over every SM rather than
+      // packing 8 to an SM (a short prefill is latency-bound)
+      const int64_t per_sm = (w.n_roles + sms - 1) / sms;
+      if (per_sm < wpc) wpc = (int)(per_sm > 0 ? per_sm : 1);
     }
+    w.wpc = wpc;
     grid = (w.n_roles + wpc - 1) / wpc;
   }
   if (grid > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
