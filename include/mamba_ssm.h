@@ -336,6 +336,114 @@ MAMBA_API int64_t mamba_decode_graph_kernels(const MambaDecodeGraph* graph);
 MAMBA_API int mamba_decode_graph_destroy(MambaDecodeGraph* graph);
 
 /*
+ * One linear layer of the Mamba-1 block on the tensor cores (bf16 operands,
+ * f32 accumulation):  C[M][N] = A[M][K] . W[N][K]^T (+ R[M][N]).
+ * (inference.rs step chain F2 in_proj, F5 x_proj, F6 dt_proj and F11
+ *  out_proj with the residual add; prefill.rs `prefill_body` runs the same
+ *  projections over all T rows.)
+ *
+ *   c         [M] rows of N at ld_c, dtype c_dtype (MAMBA_F32 or MAMBA_BF16)
+ *   a         [M] rows of K bf16 at ld_a (activations)
+ *   w         [N] rows of K bf16 at ld_w (the weight, [out_features][in_features])
+ *   residual  [M] rows of N f32 at ld_r, added before the store, or NULL; it
+ *             may be c itself (f32, same stride) for an in-place residual add
+ * a and w must be 16-byte aligned with ld_a, ld_w multiples of 8 (the tiles
+ * are moved by the tensor memory accelerator); K >= 1 of any size (the tiles
+ * past K read as zero).  M, N, K below 2^31.
+ * Errors: MAMBA_ERR_INVALID_ARG for NULL pointers, strides smaller than a row,
+ * misaligned a / w, overlap of c with an input (other than the residual as
+ * above), extent overflow.
+ */
+MAMBA_API int mamba_linear_bf16(void* c, int64_t ld_c, int c_dtype, const void* a, int64_t ld_a, const void* w,
+                                int64_t ld_w, const float* residual, int64_t ld_r, int64_t M, int64_t N, int64_t K,
+                                void* stream);
+
+/*
+ * RMSNorm of the residual stream, row by row:
+ *     out[m][j] = x[m][j] / sqrt(mean_j x[m][j]^2 + eps) * weight[j]
+ * (inference.rs step chain F1 "Save residual + RmsNorm" with rms_norm_eps;
+ *  the mixed-precision chain and prefill.rs `prefill_body` F1 read the f32
+ *  residual and write bf16 activations.)
+ *
+ *   out     [M] rows of D at ld_out, dtype out_dtype (rounded once)     (out)
+ *   x       [M] rows of D f32 at ld_x                                   (in)
+ *   weight  [D] f32                                                     (in)
+ * Errors: MAMBA_ERR_INVALID_ARG for NULL pointers, eps outside [0, 1],
+ * strides smaller than D, out overlapping x or weight.
+ */
+MAMBA_API int mamba_rmsnorm(void* out, int64_t ld_out, int out_dtype, const float* x, int64_t ld_x,
+                            const float* weight, float eps, int64_t M, int64_t D, void* stream);
+
+/*
+ * One whole Mamba-1 block (residual block around the mixer), as the mamba-rs
+ * engine runs a layer (inference.rs step chain F1-F12; prefill.rs
+ * `prefill_body`, mixed-precision path with the residual stream in f32):
+ *
+ *   h  = RMSNorm(x) * norm_w                       -> bf16
+ *   xz = h in_proj^T                               -> bf16 [2 d_inner]: x | z
+ *   u  = SiLU(conv1d(x half) + conv_b)             -> bf16   (conv state in / out)
+ *   xd = u x_proj^T                                -> bf16 [dt_rank | B | C]
+ *   dt = xd[:, :dt_rank] dt_proj^T                 -> bf16   (pre-bias)
+ *   y  = scan(u, softplus(dt + dt_proj_b), B, C, A_log, D) * SiLU(z)  -> bf16
+ *   x  = x + y out_proj^T                          (f32, in place)
+ *
+ * The projections are mamba_linear_bf16 calls, the norm mamba_rmsnorm, the
+ * conv and scan mamba_conv1d_silu_prefill and mamba_selective_scan_prefill
+ * on strided views of the workspace (x and z at row stride 2 d_inner, B and C
+ * at the x_proj output's stride): the block is exactly that sequence of calls.
+ * Weights are [out_features][in_features], bf16 for the projections, f32
+ * otherwise.  d_model, d_inner and dt_rank must be multiples of 8 (the
+ * projections' rows are moved in 16-byte granules) and the bf16 weights
+ * 16-byte aligned.
+ */
+typedef struct MambaLayer {
+  int64_t d_model, d_inner, d_state, d_conv, dt_rank;
+  float eps;              /* RMSNorm epsilon (1e-5 in the mamba-rs configs) */
+  const float* norm_w;    /* [d_model] */
+  const void* in_proj_w;  /* [2 d_inner][d_model] bf16 */
+  const float* conv_w;    /* [d_inner][d_conv] */
+  const float* conv_b;    /* [d_inner] or NULL */
+  const void* x_proj_w;   /* [dt_rank + 2 d_state][d_inner] bf16 */
+  const void* dt_proj_w;  /* [d_inner][dt_rank] bf16 */
+  const float* dt_proj_b; /* [d_inner] or NULL (the scan's dt_bias) */
+  const float* A_log;     /* [d_inner][d_state] */
+  const float* D;         /* [d_inner] or NULL */
+  const void* out_proj_w; /* [d_model][d_inner] bf16 */
+} MambaLayer;
+
+/* Workspace bytes a block over B x T tokens uses: the bf16 activations
+ * (h, xz, u, xd, dt, y) plus, for a prefill, what the scan's fastest route
+ * wants.  A step (T = 1) needs no more than mamba_layer_workspace_bytes(l, B, 1).
+ * Negative MAMBA_ERR_* on invalid dims. */
+MAMBA_API int64_t mamba_layer_workspace_bytes(const MambaLayer* layer, int64_t B, int64_t T);
+
+/*
+ *   hidden           [B][T][d_model] f32 residual stream, updated in place
+ *   conv_state_in/out, ssm_state_in/out  as for mamba_mixer_prefill ([B][d_inner][d_conv]
+ *                    and [B][d_inner][d_state] f32; in may equal out; NULL in = zeros)
+ *   workspace        16-byte aligned device scratch of workspace_bytes (contents
+ *                    on entry ignored); a smaller scan share than the query's
+ *                    picks a slower scan route with the same results
+ * Errors: MAMBA_ERR_INVALID_ARG (NULL, misaligned, overlap, workspace smaller
+ * than the activations), MAMBA_ERR_UNSUPPORTED (dims); everything is checked
+ * before the first launch.
+ */
+MAMBA_API int mamba_layer_prefill(float* hidden, const MambaLayer* layer, const float* conv_state_in,
+                                  float* conv_state_out, const float* ssm_state_in, float* ssm_state_out, int64_t B,
+                                  int64_t T, void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * One T = 1 block step for B sequences on slab `layer_index` of the
+ * persistent layer-major states (conv [n_layers][B][d_inner][d_conv], ssm
+ * [n_layers][B][d_inner][d_state], both updated in place): the prefill's
+ * sequence with T = 1 (inference.rs `step_kernels`).  hidden [B][d_model] f32
+ * in place; workspace as for mamba_layer_prefill with T = 1.
+ */
+MAMBA_API int mamba_layer_step(float* hidden, const MambaLayer* layer, float* conv_state, float* ssm_state,
+                               int64_t layer_index, int64_t n_layers, int64_t B, void* workspace,
+                               int64_t workspace_bytes, void* stream);
+
+/*
  * mamba_selective_scan_prefill_noalloc - the selective-scan prefill for callers
  * that cannot allocate device memory.  (No counterpart in the mamba-rs pages:
  * it is an addition of this library.)
@@ -389,6 +497,7 @@ MAMBA_API int mamba_selective_scan_prefill_noalloc(
  */
 #define MAMBA_FAULT_RING_WAIT 1
 #define MAMBA_FAULT_SCAN_WAIT 2 /* a prefill unit waited too long for the state it continues */
+#define MAMBA_FAULT_GEMM_WAIT 4 /* a projection GEMM waited too long for a tile or its MMAs */
 MAMBA_API int mamba_device_faults(int clear);
 
 /*

@@ -9,6 +9,9 @@ C-ABI entry points (include/mamba_ssm.h), each backed by hand-written CUDA kerne
   mamba_mixer_prefill           conv1d + SiLU and the selective scan in one pass
   mamba_decode_graph_*          n_steps x n_layers fused steps recorded as one CUDA graph
   mamba3_siso_step_batched      T=1 step of the Mamba-3 SISO (trapezoidal) recurrence
+  mamba_linear_bf16             a projection of the layer on the tensor cores (tcgen05)
+  mamba_rmsnorm                 RMSNorm of the f32 residual stream
+  mamba_layer_prefill / _step   the whole Mamba-1 block (norm, projections, mixer, residual)
   mamba_selective_scan_prefill_noalloc  the scan prefill with a static scratch
   mamba_selective_scan_workspace_bytes  scratch size of the prefill's balanced routes
 This package is the thin Python binding (argument marshalling over ctypes);
@@ -25,6 +28,7 @@ from ._binding import (  # noqa: F401
     MAMBA_F32,
     MAMBA_FAULT_RING_WAIT,
     MAMBA_FAULT_SCAN_WAIT,
+    MAMBA_FAULT_GEMM_WAIT,
     MAMBA_MAX_FUSED_D_CONV,
     MAMBA_NOALLOC_SCRATCH_BYTES,
     MAMBA_OK,
@@ -35,6 +39,13 @@ from ._binding import (  # noqa: F401
     mamba_conv1d_silu_step,
     mamba_device_faults,
     mamba_last_error,
+    mamba_layer_prefill,
+    mamba_layer_step,
+    mamba_layer_workspace_bytes,
+    mamba_linear_bf16,
+    mamba_rmsnorm,
+    layer_struct,
+    LAYER_WEIGHTS,
     mamba_mixer_prefill,
     mamba_mixer_step_batched,
     mamba_selective_scan_prefill,

@@ -23,6 +23,7 @@ MAMBA_BF16 = 1
 MAMBA_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 MAMBA_MAX_FUSED_D_CONV = 4
 MAMBA_FAULT_SCAN_WAIT = 2
+MAMBA_FAULT_GEMM_WAIT = 4
 
 LIB_PATH = _build.LIB_PATH
 
@@ -37,6 +38,11 @@ ABI_SYMBOLS = (
     "mamba_mixer_step_batched",
     "mamba_mixer_prefill",
     "mamba3_siso_step_batched",
+    "mamba_linear_bf16",
+    "mamba_rmsnorm",
+    "mamba_layer_workspace_bytes",
+    "mamba_layer_prefill",
+    "mamba_layer_step",
     "mamba_decode_graph_create",
     "mamba_decode_graph_launch",
     "mamba_decode_graph_kernels",
@@ -55,6 +61,16 @@ class MambaError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"[{status}] {message}")
         self.status = status
+
+
+class _MambaLayer(ctypes.Structure):
+    """struct MambaLayer of the C ABI (dims, RMSNorm eps, weight pointers)."""
+    _fields_ = [("d_model", ctypes.c_int64), ("d_inner", ctypes.c_int64), ("d_state", ctypes.c_int64),
+                ("d_conv", ctypes.c_int64), ("dt_rank", ctypes.c_int64), ("eps", ctypes.c_float),
+                ("norm_w", ctypes.c_void_p), ("in_proj_w", ctypes.c_void_p), ("conv_w", ctypes.c_void_p),
+                ("conv_b", ctypes.c_void_p), ("x_proj_w", ctypes.c_void_p), ("dt_proj_w", ctypes.c_void_p),
+                ("dt_proj_b", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("D", ctypes.c_void_p),
+                ("out_proj_w", ctypes.c_void_p)]
 
 
 def load(path: str | None = None):
@@ -92,6 +108,17 @@ def load(path: str | None = None):
         lib.mamba_mixer_prefill.restype = ctypes.c_int
         lib.mamba3_siso_step_batched.argtypes = [vp, i32, vp, vp, vp, i32] + [vp] * 7 + [i64] * 6 + [vp]
         lib.mamba3_siso_step_batched.restype = ctypes.c_int
+        lib.mamba_linear_bf16.argtypes = [vp, i64, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]
+        lib.mamba_linear_bf16.restype = ctypes.c_int
+        lib.mamba_rmsnorm.argtypes = [vp, i64, i32, vp, i64, vp, ctypes.c_float, i64, i64, vp]
+        lib.mamba_rmsnorm.restype = ctypes.c_int
+        lp = ctypes.POINTER(_MambaLayer)
+        lib.mamba_layer_workspace_bytes.argtypes = [lp, i64, i64]
+        lib.mamba_layer_workspace_bytes.restype = i64
+        lib.mamba_layer_prefill.argtypes = [vp, lp, vp, vp, vp, vp, i64, i64, vp, i64, vp]
+        lib.mamba_layer_prefill.restype = ctypes.c_int
+        lib.mamba_layer_step.argtypes = [vp, lp, vp, vp, i64, i64, i64, vp, i64, vp]
+        lib.mamba_layer_step.restype = ctypes.c_int
         lib.mamba_decode_graph_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i64, i32, i32, vp, vp,
                                                   i64, i64, i64, i64]
         lib.mamba_decode_graph_create.restype = ctypes.c_int
@@ -436,6 +463,149 @@ def mamba_ssm_step_batched(y, u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt
         _ptr(y), _dtype_code(y), _ptr(u), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _dtype_code(u),
         _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(ssm_state), int(layer), ssm_state.shape[0],
         Bsz, Di, N, _stream(stream, u)))
+
+
+def _rows2d(t, name):
+    """Row stride of a 2-D [rows, cols] tensor with contiguous columns."""
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D [rows, cols], got {tuple(t.shape)}")
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name}: columns must be contiguous (stride {t.stride(1)})")
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1]
+
+
+def mamba_linear_bf16(c, a, w, residual=None, *, stream=None):
+    """c[M, N] = a[M, K] @ w[N, K]^T (+ residual[M, N]) on the tensor cores.
+
+    a, w: bf16 (row-strided views allowed, rows 16-byte aligned); c: f32 or
+    bf16 [M, N]; residual: f32 [M, N], may be c itself."""
+    import torch
+
+    M, K = a.shape
+    N = w.shape[0]
+    if a.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise ValueError("a and w must be bfloat16")
+    if w.dim() != 2 or w.shape[1] != K:
+        raise ValueError(f"w must be [N, K={K}], got {tuple(w.shape)}")
+    if tuple(c.shape) != (M, N):
+        raise ValueError(f"c must be [M, N] = {(M, N)}, got {tuple(c.shape)}")
+    if residual is not None and (residual.dtype != torch.float32 or tuple(residual.shape) != (M, N)):
+        raise ValueError("residual must be a float32 [M, N] tensor")
+    _check(load().mamba_linear_bf16(
+        _ptr(c), _rows2d(c, "c"), _dtype_code(c), _ptr(a), _rows2d(a, "a"), _ptr(w), _rows2d(w, "w"),
+        _ptr(residual), _rows2d(residual, "residual") if residual is not None else 0, M, N, K,
+        _stream(stream, a)))
+
+
+def mamba_rmsnorm(out, x, weight, eps=1e-5, *, stream=None):
+    """out[m] = x[m] / sqrt(mean(x[m]^2) + eps) * weight; x f32 [M, D], out f32
+    or bf16 [M, D] (row-strided views allowed), weight f32 [D]."""
+    import torch
+
+    if x.dtype != torch.float32 or x.dim() != 2:
+        raise ValueError("x must be a 2-D float32 tensor [M, D]")
+    M, Dm = x.shape
+    _f32_param(weight, "weight", (Dm,))
+    if tuple(out.shape) != (M, Dm):
+        raise ValueError(f"out must be [M, D] = {(M, Dm)}, got {tuple(out.shape)}")
+    _check(load().mamba_rmsnorm(_ptr(out), _rows2d(out, "out"), _dtype_code(out), _ptr(x), _rows2d(x, "x"),
+                                _ptr(weight), float(eps), M, Dm, _stream(stream, x)))
+
+
+LAYER_WEIGHTS = ("norm_w", "in_proj_w", "conv_w", "conv_b", "x_proj_w", "dt_proj_w", "dt_bias", "A_log", "D",
+                 "out_proj_w")
+
+
+def layer_struct(w, eps=1e-5):
+    """The C struct MambaLayer for a dict of block weights: norm_w [dm],
+    in_proj_w [2 Di, dm] bf16, conv_w [Di, K], conv_b [Di] or None, x_proj_w
+    [R + 2N, Di] bf16, dt_proj_w [Di, R] bf16, dt_bias (dt_proj's bias) [Di] or
+    None, A_log [Di, N], D [Di] or None, out_proj_w [dm, Di] bf16.  Shapes and
+    dtypes are checked here; the tensors must outlive every call that uses
+    the struct."""
+    import torch
+
+    for k in ("norm_w", "in_proj_w", "conv_w", "x_proj_w", "dt_proj_w", "A_log", "out_proj_w"):
+        if w.get(k) is None:
+            raise ValueError(f"layer weight {k} is missing")
+    Di, K = w["conv_w"].shape
+    N = w["A_log"].shape[1]
+    dm = w["norm_w"].shape[0]
+    R = w["dt_proj_w"].shape[1]
+    for k, shp in (("in_proj_w", (2 * Di, dm)), ("x_proj_w", (R + 2 * N, Di)), ("dt_proj_w", (Di, R)),
+                   ("out_proj_w", (dm, Di))):
+        t = w[k]
+        if t.dtype != torch.bfloat16 or tuple(t.shape) != shp or not t.is_contiguous():
+            raise ValueError(f"{k} must be a contiguous bfloat16 {shp} tensor")
+    _f32_param(w["norm_w"], "norm_w", (dm,))
+    _f32_param(w["conv_w"], "conv_w", (Di, K))
+    _f32_param(w["A_log"], "A_log", (Di, N))
+    for k in ("conv_b", "dt_bias", "D"):
+        _f32_param(w.get(k), k, (Di,))
+    return _MambaLayer(dm, Di, N, K, R, float(eps), _ptr(w["norm_w"]), _ptr(w["in_proj_w"]), _ptr(w["conv_w"]),
+                       _ptr(w.get("conv_b")), _ptr(w["x_proj_w"]), _ptr(w["dt_proj_w"]), _ptr(w.get("dt_bias")),
+                       _ptr(w["A_log"]), _ptr(w.get("D")), _ptr(w["out_proj_w"]))
+
+
+def mamba_layer_workspace_bytes(w, Bsz, T, eps=1e-5) -> int:
+    """Workspace bytes of a block over Bsz x T tokens (activations + the scan's share)."""
+    v = load().mamba_layer_workspace_bytes(ctypes.byref(layer_struct(w, eps)), Bsz, T)
+    if v < 0:
+        raise MambaError(int(v), mamba_last_error())
+    return int(v)
+
+
+def _layer_workspace(workspace, w, Bsz, T, eps, device, st):
+    if workspace is None:
+        return _workspace(device, mamba_layer_workspace_bytes(w, Bsz, T, eps), st)
+    return workspace
+
+
+def mamba_layer_prefill(hidden, w, conv_state_in=None, conv_state_out=None, ssm_state_in=None,
+                        ssm_state_out=None, *, eps=1e-5, workspace=None, stream=None):
+    """One Mamba-1 block over T tokens: hidden [B, T, d_model] f32 (contiguous)
+    is updated in place, hidden += out_proj(mixer(RMSNorm(hidden))).  States
+    [B, Di, K] / [B, Di, N] f32 (in may be out; None in = zeros).  workspace:
+    None = a cached buffer per (device, stream), or a uint8 cuda tensor."""
+    import torch
+
+    if hidden.dtype != torch.float32 or hidden.dim() != 3 or not hidden.is_contiguous():
+        raise ValueError("hidden must be a contiguous float32 [B, T, d_model] tensor")
+    Bsz, T, dm = hidden.shape
+    S = layer_struct(w, eps)
+    if dm != S.d_model:
+        raise ValueError(f"hidden has d_model {dm}, the weights {S.d_model}")
+    for t, nm, last in ((conv_state_in, "conv_state_in", S.d_conv), (conv_state_out, "conv_state_out", S.d_conv),
+                        (ssm_state_in, "ssm_state_in", S.d_state), (ssm_state_out, "ssm_state_out", S.d_state)):
+        _f32_param(t, nm, (Bsz, S.d_inner, last))
+    st = _stream(stream, hidden)
+    ws = _layer_workspace(workspace, w, Bsz, T, eps, hidden.device, st)
+    _check(load().mamba_layer_prefill(_ptr(hidden), ctypes.byref(S), _ptr(conv_state_in), _ptr(conv_state_out),
+                                      _ptr(ssm_state_in), _ptr(ssm_state_out), Bsz, T, _ptr(ws),
+                                      ws.numel() * ws.element_size(), st))
+
+
+def mamba_layer_step(hidden, w, conv_state, ssm_state, layer, *, eps=1e-5, workspace=None, stream=None):
+    """One T=1 block step: hidden [B, d_model] f32 (contiguous, in place) on slab
+    `layer` of conv_state [L, B, Di, K] and ssm_state [L, B, Di, N] (in place)."""
+    import torch
+
+    if hidden.dtype != torch.float32 or hidden.dim() != 2 or not hidden.is_contiguous():
+        raise ValueError("hidden must be a contiguous float32 [B, d_model] tensor")
+    Bsz, dm = hidden.shape
+    S = layer_struct(w, eps)
+    if dm != S.d_model:
+        raise ValueError(f"hidden has d_model {dm}, the weights {S.d_model}")
+    for t, nm, last in ((conv_state, "conv_state", S.d_conv), (ssm_state, "ssm_state", S.d_state)):
+        if t.dim() != 4 or tuple(t.shape[1:]) != (Bsz, S.d_inner, last):
+            raise ValueError(f"{nm} must be [n_layers, B, Di, {last}]")
+        _f32_param(t, nm)
+    if conv_state.shape[0] != ssm_state.shape[0]:
+        raise ValueError("conv_state and ssm_state must have the same number of layers")
+    st = _stream(stream, hidden)
+    ws = _layer_workspace(workspace, w, Bsz, 1, eps, hidden.device, st)
+    _check(load().mamba_layer_step(_ptr(hidden), ctypes.byref(S), _ptr(conv_state), _ptr(ssm_state), int(layer),
+                                   conv_state.shape[0], Bsz, _ptr(ws), ws.numel() * ws.element_size(), st))
 
 
 def mamba_selective_scan_prefill_noalloc(y, u, dt, Bm, Cm, A_log, D=None, dt_bias=None, z=None,

@@ -168,6 +168,132 @@ int copy_state(float* out, const float* in, int64_t count, cudaStream_t s) {
   return ok();
 }
 
+// ---- the whole Mamba-1 block ---------------------------------------------------
+// Workspace layout of a block over rows = B*T tokens: six bf16 activation
+// buffers, each starting on a 256-byte boundary, then the scan's share.
+struct LayerPlan {
+  int64_t rows, ldx;  // ldx: row stride of the x_proj output (dt_rank + 2 d_state, rounded up to 8)
+  int64_t off_h, off_xz, off_u, off_xd, off_dt, off_y, act_bytes;
+};
+
+int64_t round256(int64_t b) { return (b + 255) / 256 * 256; }
+
+int layer_plan(const MambaLayer* L, int64_t B, int64_t T, LayerPlan* p) {
+  if (!L) return fail(MAMBA_ERR_INVALID_ARG, "layer is NULL");
+  if (B < 0 || T < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld T=%lld)", (long long)B, (long long)T);
+  const int64_t dm = L->d_model, Di = L->d_inner, N = L->d_state, K = L->d_conv, R = L->dt_rank;
+  if (dm < 1 || Di < 1 || R < 1)
+    return fail(MAMBA_ERR_INVALID_ARG, "d_model, d_inner and dt_rank must be >= 1");
+  if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
+  if (K < 1 || K > MAMBA_MAX_D_CONV)
+    return fail(MAMBA_ERR_UNSUPPORTED, "d_conv=%lld not in 1..%d", (long long)K, MAMBA_MAX_D_CONV);
+  if (dm % 8 || Di % 8 || R % 8)
+    return fail(MAMBA_ERR_UNSUPPORTED, "d_model=%lld, d_inner=%lld and dt_rank=%lld must be multiples of 8",
+                (long long)dm, (long long)Di, (long long)R);
+  if (!(L->eps >= 0.0f) || L->eps > 1.0f) return fail(MAMBA_ERR_INVALID_ARG, "eps must be in [0, 1]");
+  if (dm > INT32_MAX || Di > INT32_MAX / 2 || R > INT32_MAX || !sizes_ok(B, T) || !sizes_ok(B * T, 2 * Di) ||
+      !sizes_ok(B * T, dm) || !sizes_ok(B * T, R + 2 * N + 8) || !sizes_ok(2 * Di, dm) || !sizes_ok(B, Di, N) ||
+      !sizes_ok(B, Di, K))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  p->rows = B * T;
+  p->ldx = (R + 2 * N + 7) / 8 * 8;
+  p->off_h = 0;
+  p->off_xz = p->off_h + round256(p->rows * dm * 2);
+  p->off_u = p->off_xz + round256(p->rows * 2 * Di * 2);
+  p->off_xd = p->off_u + round256(p->rows * Di * 2);
+  p->off_dt = p->off_xd + round256(p->rows * p->ldx * 2);
+  p->off_y = p->off_dt + round256(p->rows * Di * 2);
+  p->act_bytes = p->off_y + round256(p->rows * Di * 2);
+  return MAMBA_OK;
+}
+
+// the block over B x T tokens; the scan gets the workspace past the
+// activations when scan_share (prefill), none for a step (its plain route)
+int run_layer(float* hidden, const MambaLayer* L, const float* conv_in, float* conv_out, const float* ssm_in,
+              float* ssm_out, int64_t B, int64_t T, void* workspace, int64_t workspace_bytes, bool scan_share,
+              void* stream) {
+  int rc;
+  LayerPlan p;
+  if ((rc = layer_plan(L, B, T, &p))) return rc;
+  const int64_t dm = L->d_model, Di = L->d_inner, N = L->d_state, K = L->d_conv, R = L->dt_rank;
+  if (B == 0) return ok();
+  if (T == 0) {  // the states pass through
+    if ((rc = mamba_conv1d_silu_prefill(nullptr, Di, nullptr, Di, MAMBA_BF16, conv_in, conv_out, L->conv_w,
+                                        L->conv_b, B, 0, Di, K, stream)))
+      return rc;
+    return mamba_selective_scan_prefill(nullptr, Di, MAMBA_BF16, nullptr, Di, nullptr, Di, nullptr, Di, nullptr, N,
+                                        nullptr, N, MAMBA_BF16, L->A_log, L->D, L->dt_proj_b, ssm_in, ssm_out, B, 0,
+                                        Di, N, nullptr, 0, stream);
+  }
+  if (!hidden || !workspace) return fail(MAMBA_ERR_INVALID_ARG, "hidden and workspace must not be NULL");
+  if (!L->norm_w || !L->in_proj_w || !L->conv_w || !L->x_proj_w || !L->dt_proj_w || !L->A_log || !L->out_proj_w)
+    return fail(MAMBA_ERR_INVALID_ARG, "a required weight of the layer is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) & 15) return fail(MAMBA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+  if (workspace_bytes < p.act_bytes)
+    return fail(MAMBA_ERR_INVALID_ARG, "workspace_bytes=%lld below the %lld bytes of the block's activations",
+                (long long)workspace_bytes, (long long)p.act_bytes);
+  for (const void* w : {L->in_proj_w, L->x_proj_w, L->dt_proj_w, L->out_proj_w})
+    if (reinterpret_cast<uintptr_t>(w) & 15) return fail(MAMBA_ERR_INVALID_ARG, "the bf16 weights must be 16-byte aligned");
+  // every range the sequence touches, checked together before the first launch
+  const int64_t xdim = R + 2 * N;
+  Range ins[] = {range_of("norm_w", L->norm_w, dm * 4), range_of("in_proj_w", L->in_proj_w, 2 * Di * dm * 2),
+                 range_of("conv_w", L->conv_w, Di * K * 4), range_of("conv_b", L->conv_b, Di * 4),
+                 range_of("x_proj_w", L->x_proj_w, xdim * Di * 2), range_of("dt_proj_w", L->dt_proj_w, Di * R * 2),
+                 range_of("dt_proj_b", L->dt_proj_b, Di * 4), range_of("A_log", L->A_log, Di * N * 4),
+                 range_of("D", L->D, Di * 4), range_of("out_proj_w", L->out_proj_w, dm * Di * 2),
+                 range_of("conv_state_in", conv_in, B * Di * K * 4), range_of("ssm_state_in", ssm_in, B * Di * N * 4)};
+  Range outs[] = {range_of("hidden", hidden, p.rows * dm * 4), range_of("workspace", workspace, workspace_bytes),
+                  range_of("conv_state_out", conv_out, B * Di * K * 4),
+                  range_of("ssm_state_out", ssm_out, B * Di * N * 4)};
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  if ((rc = check_pointers(ins, 12, dev_id)) || (rc = check_pointers(outs, 4, dev_id))) return rc;
+  // a state may be updated in place: then its input range is its output range
+  Range ins_x[12];
+  int n_in = 0;
+  for (int i = 0; i < 12; ++i) {
+    if ((i == 10 && conv_in && conv_in == conv_out) || (i == 11 && ssm_in && ssm_in == ssm_out)) continue;
+    ins_x[n_in++] = ins[i];
+  }
+  if ((rc = check_overlaps(outs, 4, ins_x, n_in))) return rc;
+
+  char* ws = static_cast<char*>(workspace);
+  auto* h = ws + p.off_h;
+  auto* xz = ws + p.off_xz;
+  auto* u = ws + p.off_u;
+  auto* xd = ws + p.off_xd;
+  auto* dt = ws + p.off_dt;
+  auto* y = ws + p.off_y;
+  void* scan_ws = scan_share && workspace_bytes > p.act_bytes ? ws + p.act_bytes : nullptr;
+  const int64_t scan_bytes = scan_ws ? workspace_bytes - p.act_bytes : 0;
+  const int64_t rows = p.rows, ldx = p.ldx;
+  // F1 RMSNorm (f32 residual in, bf16 out); F2 in_proj
+  if ((rc = mamba_rmsnorm(h, dm, MAMBA_BF16, hidden, dm, L->norm_w, L->eps, rows, dm, stream))) return rc;
+  if ((rc = mamba_linear_bf16(xz, 2 * Di, MAMBA_BF16, h, dm, L->in_proj_w, dm, nullptr, 0, rows, 2 * Di, dm, stream)))
+    return rc;
+  // F3-F4: the conv reads the x half of xz in place (row stride 2 d_inner)
+  if ((rc = mamba_conv1d_silu_prefill(u, Di, xz, 2 * Di, MAMBA_BF16, conv_in, conv_out, L->conv_w, L->conv_b, B, T,
+                                      Di, K, stream)))
+    return rc;
+  // F5 x_proj -> [dt_rank | B | C]; F6 dt_proj on the first dt_rank columns
+  if ((rc = mamba_linear_bf16(xd, ldx, MAMBA_BF16, u, Di, L->x_proj_w, Di, nullptr, 0, rows, xdim, Di, stream)))
+    return rc;
+  if ((rc = mamba_linear_bf16(dt, Di, MAMBA_BF16, xd, ldx, L->dt_proj_w, R, nullptr, 0, rows, Di, R, stream)))
+    return rc;
+  // F7-F10: softplus(dt + dt_proj_b), the scan and the SiLU(z) gate in one call
+  char* xz_z = xz + Di * 2;
+  char* xd_b = xd + R * 2;
+  char* xd_c = xd + (R + N) * 2;
+  if ((rc = mamba_selective_scan_prefill(y, Di, MAMBA_BF16, u, Di, dt, Di, xz_z, 2 * Di, xd_b, ldx, xd_c, ldx,
+                                         MAMBA_BF16, L->A_log, L->D, L->dt_proj_b, ssm_in, ssm_out, B, T, Di, N,
+                                         scan_ws, scan_bytes, stream)))
+    return rc;
+  // F11-F12: out_proj with the residual added in its epilogue, in place
+  return mamba_linear_bf16(hidden, dm, MAMBA_F32, y, Di, L->out_proj_w, Di, hidden, dm, rows, dm, Di, stream);
+}
+
 }  // namespace
 
 int mamba::plan_scan_for_current_device(int64_t B, int64_t T, int64_t Di, int64_t N, int64_t workspace_bytes,
@@ -197,10 +323,12 @@ int mamba_device_faults(int clear) {
   const int v3 = mamba::read_m3_faults(clear != 0);
   const int v2 = mamba::read_scan_faults(clear != 0);
   if (v2 < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the scan watchdog failed");
+  const int vg = mamba::read_gemm_faults(clear != 0);
+  if (vg < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the GEMM watchdog failed");
   if (v3 < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the Mamba-3 watchdog failed");
   const int vs = mamba::read_selftest_faults(clear != 0);
   if (vs < 0) return fail(MAMBA_ERR_CUDA, "mamba_device_faults: reading the self-test watchdog failed");
-  return ok(), v | v2 | v3 | vs;
+  return ok(), v | v2 | v3 | vs | vg;
 }
 
 int mamba_selftest_bounded_wait(int64_t limit_cycles, int complete, void* stream) {
@@ -473,6 +601,70 @@ int mamba3_siso_step_batched(void* y, int y_dtype, const void* x, const void* k,
   return ok();
 }
 
+int mamba_linear_bf16(void* c, int64_t ld_c, int c_dtype, const void* a, int64_t ld_a, const void* w, int64_t ld_w,
+                      const float* residual, int64_t ld_r, int64_t M, int64_t N, int64_t K, void* stream) {
+  int rc;
+  if ((rc = check_dtype("c_dtype", c_dtype))) return rc;
+  if (M < 0 || N < 0 || K < 1) return fail(MAMBA_ERR_INVALID_ARG, "sizes must be M >= 0, N >= 0, K >= 1 (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
+  if (M == 0 || N == 0) return ok();
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || !sizes_ok(M, K) || !sizes_ok(N, K) || !sizes_ok(M, N))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!c || !a || !w) return fail(MAMBA_ERR_INVALID_ARG, "c, a and w must not be NULL");
+  if (ld_c < N || (residual && ld_r < N) || ld_a < K || ld_w < K)
+    return fail(MAMBA_ERR_INVALID_ARG, "a row stride is smaller than its row");
+  // the tensor-memory copies read whole 16-byte granules of A and W rows
+  if ((reinterpret_cast<uintptr_t>(a) & 15) || (reinterpret_cast<uintptr_t>(w) & 15) || (ld_a * 2) % 16 ||
+      (ld_w * 2) % 16)
+    return fail(MAMBA_ERR_INVALID_ARG, "a and w must be 16-byte aligned with row strides of a multiple of 8 elements");
+  const int esc = es_of(c_dtype);
+  int64_t bc = 0, ba = 0, bw = 0, br = 0;
+  if (!span_bytes(M, N, ld_c, esc, &bc) || !span_bytes(M, K, ld_a, 2, &ba) || !span_bytes(N, K, ld_w, 2, &bw) ||
+      (residual && !span_bytes(M, N, ld_r, 4, &br)))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  Range ins[] = {range_of("a", a, ba), range_of("w", w, bw), range_of("residual", residual, br)};
+  Range outs[] = {range_of("c", c, bc)};
+  if ((rc = check_pointers(ins, 3, dev_id)) || (rc = check_pointers(outs, 1, dev_id))) return rc;
+  // the residual may be the output itself (x += out_proj(y)); nothing else may overlap c
+  const bool inplace_r = residual && reinterpret_cast<const void*>(residual) == c && ld_r == ld_c && c_dtype == MAMBA_F32;
+  if ((rc = check_overlaps(outs, 1, ins, inplace_r ? 2 : 3))) return rc;
+  mamba::GemmArgs g{c, ld_c, c_dtype == MAMBA_BF16, a, ld_a, w, ld_w, residual, ld_r, M, N, K};
+  cudaError_t e = mamba::launch_gemm_bf16(g, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("linear_bf16 launch", e);
+  return ok();
+}
+
+int mamba_rmsnorm(void* out, int64_t ld_out, int out_dtype, const float* x, int64_t ld_x, const float* weight,
+                  float eps, int64_t M, int64_t D, void* stream) {
+  int rc;
+  if ((rc = check_dtype("out_dtype", out_dtype))) return rc;
+  if (M < 0 || D < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size (M=%lld D=%lld)", (long long)M, (long long)D);
+  if (!(eps >= 0.0f) || eps > 1.0f) return fail(MAMBA_ERR_INVALID_ARG, "eps must be in [0, 1]");
+  if (M == 0 || D == 0) return ok();
+  if (D > INT32_MAX || !sizes_ok(M, D)) return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!out || !x || !weight) return fail(MAMBA_ERR_INVALID_ARG, "out, x and weight must not be NULL");
+  if (ld_out < D || ld_x < D) return fail(MAMBA_ERR_INVALID_ARG, "a row stride is smaller than D=%lld", (long long)D);
+  int64_t bo = 0, bx = 0, bw = 0;
+  if (!span_bytes(M, D, ld_out, es_of(out_dtype), &bo) || !span_bytes(M, D, ld_x, 4, &bx) ||
+      !span_bytes(1, D, D, 4, &bw))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  Range ins[] = {range_of("x", x, bx), range_of("weight", weight, bw)};
+  Range outs[] = {range_of("out", out, bo)};
+  if ((rc = check_pointers(ins, 2, dev_id)) || (rc = check_pointers(outs, 1, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 1, ins, 2))) return rc;
+  mamba::RmsNormArgs a{out, ld_out, out_dtype == MAMBA_BF16, x, ld_x, weight, eps, M, D};
+  cudaError_t e = mamba::launch_rmsnorm(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("rmsnorm launch", e);
+  return ok();
+}
+
 int64_t mamba_selective_scan_workspace_bytes(int64_t B, int64_t T, int64_t Di, int64_t N) {
   if (B < 0 || T < 0 || Di < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative size");
   if (!valid_n(N)) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {1,2,4,8,16,32,64}", (long long)N);
@@ -570,6 +762,44 @@ int mamba_mixer_step_batched(void* y, int y_dtype, const void* x, const void* dt
   cudaError_t e = mamba::launch_mixer_step_batched(a, dev, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail("mixer_step_batched launch", e);
   return ok();
+}
+
+int64_t mamba_layer_workspace_bytes(const MambaLayer* layer, int64_t B, int64_t T) {
+  LayerPlan p;
+  int rc;
+  if ((rc = layer_plan(layer, B, T, &p))) return rc;
+  if (B == 0 || T == 0) return ok(), 0;
+  mamba::ScanShapePlan sp;
+  if ((rc = mamba::plan_scan_for_current_device(B, T, layer->d_inner, layer->d_state, INT64_MAX, &sp))) return rc;
+  ok();
+  return p.act_bytes + sp.workspace_bytes;
+}
+
+int mamba_layer_prefill(float* hidden, const MambaLayer* layer, const float* conv_state_in, float* conv_state_out,
+                        const float* ssm_state_in, float* ssm_state_out, int64_t B, int64_t T, void* workspace,
+                        int64_t workspace_bytes, void* stream) {
+  if (workspace_bytes < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative workspace_bytes");
+  return run_layer(hidden, layer, conv_state_in, conv_state_out, ssm_state_in, ssm_state_out, B, T, workspace,
+                   workspace_bytes, true, stream);
+}
+
+int mamba_layer_step(float* hidden, const MambaLayer* layer, float* conv_state, float* ssm_state,
+                     int64_t layer_index, int64_t n_layers, int64_t B, void* workspace, int64_t workspace_bytes,
+                     void* stream) {
+  if (workspace_bytes < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative workspace_bytes");
+  if (!layer) return fail(MAMBA_ERR_INVALID_ARG, "layer is NULL");
+  if (n_layers < 1 || layer_index < 0 || layer_index >= n_layers)
+    return fail(MAMBA_ERR_INVALID_ARG, "layer_index=%lld outside [0, n_layers=%lld)", (long long)layer_index,
+                (long long)n_layers);
+  if (B < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative B");
+  if (B == 0) return ok();
+  if (!conv_state || !ssm_state) return fail(MAMBA_ERR_INVALID_ARG, "conv_state and ssm_state must not be NULL");
+  const int64_t Di = layer->d_inner, N = layer->d_state, K = layer->d_conv;
+  if (Di < 1 || N < 1 || K < 1 || !sizes_ok(B, Di, N > K ? N : K) || !sizes_ok(n_layers, B * Di * (N > K ? N : K)))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow or invalid dims");
+  float* cslab = conv_state + layer_index * B * Di * K;
+  float* sslab = ssm_state + layer_index * B * Di * N;
+  return run_layer(hidden, layer, cslab, cslab, sslab, sslab, B, 1, workspace, workspace_bytes, false, stream);
 }
 
 }  // extern "C"

@@ -192,6 +192,37 @@ cudaError_t launch_m3_step_batched(const M3StepArgs& a, const DeviceInfo& dev, c
 // watchdog bits of the Mamba-3 ring kernel (the device must be synchronised)
 int read_m3_faults(bool clear);
 
+// ---------------------------------------------------------------- layer ----
+// C[M][N] = A[M][K] . W[N][K]^T (+ R), bf16 operands, f32 accumulation on the
+// tensor cores (gemm.cu).  ld_* in elements; A, W rows 16-byte aligned.
+struct GemmArgs {
+  void* c;
+  int64_t ld_c;
+  int c_bf16;
+  const void* a;
+  int64_t ld_a;
+  const void* w;
+  int64_t ld_w;
+  const float* r;  // residual [M][N] at ld_r, or null
+  int64_t ld_r;
+  int64_t M, N, K;
+};
+cudaError_t launch_gemm_bf16(const GemmArgs& g, cudaStream_t stream);
+int read_gemm_faults(bool clear);
+
+// out[m][j] = x[m][j] / sqrt(mean_j x[m][j]^2 + eps) * w[j]   (rmsnorm.cu)
+struct RmsNormArgs {
+  void* out;
+  int64_t ld_out;
+  int out_bf16;
+  const float* x;
+  int64_t ld_x;
+  const float* w;
+  float eps;
+  int64_t M, D;
+};
+cudaError_t launch_rmsnorm(const RmsNormArgs& a, cudaStream_t stream);
+
 // Fused decode step: conv1d + SiLU step on x, then the SSM step on its u.
 struct MixerStepArgs {
   SsmStepArgs ssm;         // ssm.u unused (u is produced in registers)

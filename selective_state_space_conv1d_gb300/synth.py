@@ -37,6 +37,8 @@ _TENSOR_IDS = {
     # Mamba-3 SISO step
     "m3_x": 30, "m3_k": 31, "m3_q": 32, "m3_alpha": 33, "m3_beta": 34, "m3_gamma": 35, "m3_D": 36,
     "m3_ssm_state": 37, "m3_k_state": 38, "m3_v_state": 39,
+    # the rest of the Mamba-1 block
+    "norm_w": 40, "in_proj_w": 41, "x_proj_w": 42, "dt_proj_w": 43, "out_proj_w": 44, "hidden": 45,
 }
 
 
@@ -145,6 +147,27 @@ def parity_params(seed: int, d_inner: int, d_state: int, d_conv: int, layer: int
     p["A_log"] = A_log.astype(np.float32)
     p["D"] = (1.0 + 0.5 * generator(seed, "D", layer).standard_normal(d_inner)).astype(np.float32)
     p["conv_b"] = normal(seed, "conv_b", (d_inner,), 0.2, layer=layer)
+    return p
+
+
+def layer_params(seed: int, d_model: int, d_inner: int, d_state: int, d_conv: int, dt_rank: int,
+                 layer: int = 0, parity: bool = False) -> dict:
+    """Weights of one Mamba-1 block (random init, no trained weights):
+      in_proj_w [2 Di, dm], x_proj_w [R + 2N, Di], out_proj_w [dm, Di]
+                ~ N(0, 1/fan_in), stored bf16
+      dt_proj_w [Di, R] ~ U(-R^-1/2, R^-1/2), stored bf16
+      norm_w [dm] = 1 (U(0.5, 1.5) for parity cases)
+      the mixer's conv_w, conv_b, A_log, D and dt_bias (dt_proj's bias) from
+      mixer_params, or parity_params for parity cases.
+    Every array is f32; the bf16 weights hold exactly their bf16 values."""
+    p = (parity_params if parity else mixer_params)(seed, d_inner, d_state, d_conv, layer)
+    p["in_proj_w"] = normal(seed, "in_proj_w", (2 * d_inner, d_model), d_model ** -0.5, "bf16", layer)
+    p["x_proj_w"] = normal(seed, "x_proj_w", (dt_rank + 2 * d_state, d_inner), d_inner ** -0.5, "bf16", layer)
+    p["out_proj_w"] = normal(seed, "out_proj_w", (d_model, d_inner), d_inner ** -0.5, "bf16", layer)
+    r = dt_rank ** -0.5
+    p["dt_proj_w"] = store(uniform(seed, "dt_proj_w", (d_inner, dt_rank), -r, r, layer), "bf16")
+    p["norm_w"] = (uniform(seed, "norm_w", (d_model,), 0.5, 1.5, layer) if parity
+                   else np.ones(d_model, np.float32))
     return p
 
 

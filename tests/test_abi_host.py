@@ -278,3 +278,92 @@ def test_scan_wrappers_refuse_mismatched_tensors_before_any_call(fn, bad):
         args["ssm_state_out"] = f(Bsz, Di, N - 1)
     with pytest.raises(ValueError):
         getattr(m, fn)(**args)
+
+
+def _layer(dm=64, Di=128, N=16, K=4, R=8, eps=1e-5, null=()):
+    S = m._binding._MambaLayer(dm, Di, N, K, R, eps, *([FAKE.value] * 10))
+    for f in null:
+        setattr(S, f, None)
+    return S
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dm=60), m.MAMBA_ERR_UNSUPPORTED),     # d_model not a multiple of 8
+    (dict(Di=100), m.MAMBA_ERR_UNSUPPORTED),    # d_inner not a multiple of 8
+    (dict(R=6), m.MAMBA_ERR_UNSUPPORTED),       # dt_rank not a multiple of 8
+    (dict(N=3), m.MAMBA_ERR_UNSUPPORTED),
+    (dict(K=9), m.MAMBA_ERR_UNSUPPORTED),
+    (dict(dm=0), m.MAMBA_ERR_INVALID_ARG),
+    (dict(eps=-1.0), m.MAMBA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), m.MAMBA_ERR_INVALID_ARG),
+])
+def test_layer_rejects_bad_dims_on_host(lib, kw, code):
+    S = _layer(**kw)
+    assert lib.mamba_layer_workspace_bytes(ctypes.byref(S), 2, 16) == code
+    assert lib.mamba_layer_prefill(FAKE, ctypes.byref(S), None, None, None, None, 2, 16, FAKE, 1 << 30, None) == code
+    assert lib.mamba_layer_step(FAKE, ctypes.byref(S), FAKE, FAKE, 0, 1, 2, FAKE, 1 << 30, None) == code
+    assert m.mamba_last_error()
+
+
+def test_layer_rejects_bad_arguments_on_host(lib):
+    E = m.MAMBA_ERR_INVALID_ARG
+    S = _layer()
+    assert lib.mamba_layer_workspace_bytes(None, 2, 16) == E
+    assert lib.mamba_layer_workspace_bytes(ctypes.byref(S), -1, 16) == E
+    assert lib.mamba_layer_prefill(FAKE, None, None, None, None, None, 2, 16, FAKE, 1 << 30, None) == E
+    assert lib.mamba_layer_prefill(FAKE, ctypes.byref(S), None, None, None, None, 2, 16, FAKE, -1, None) == E
+    # the block over B x T rows needs at least its activations' bytes
+    assert lib.mamba_layer_prefill(FAKE, ctypes.byref(S), None, None, None, None, 2, 16, FAKE, 1024, None) == E
+    # a misaligned workspace or bf16 weight, a missing weight
+    assert lib.mamba_layer_prefill(FAKE, ctypes.byref(S), None, None, None, None, 2, 16,
+                                   ctypes.c_void_p(FAKE.value + 8), 1 << 30, None) == E
+    S2 = _layer()
+    S2.in_proj_w = FAKE.value + 2
+    assert lib.mamba_layer_prefill(FAKE, ctypes.byref(S2), None, None, None, None, 2, 16, FAKE, 1 << 30, None) == E
+    for f in ("norm_w", "in_proj_w", "conv_w", "x_proj_w", "dt_proj_w", "A_log", "out_proj_w"):
+        assert lib.mamba_layer_prefill(FAKE, ctypes.byref(_layer(null=(f,))), None, None, None, None, 2, 16, FAKE,
+                                       1 << 30, None) == E, f
+    # step: layer index outside [0, n_layers), missing states
+    assert lib.mamba_layer_step(FAKE, ctypes.byref(S), FAKE, FAKE, 2, 2, 2, FAKE, 1 << 30, None) == E
+    assert lib.mamba_layer_step(FAKE, ctypes.byref(S), None, FAKE, 0, 2, 2, FAKE, 1 << 30, None) == E
+    # B == 0 is a no-op
+    assert lib.mamba_layer_prefill(None, ctypes.byref(S), None, None, None, None, 0, 16, None, 0, None) == 0
+
+
+def test_rmsnorm_and_linear_reject_bad_arguments_on_host(lib):
+    E = m.MAMBA_ERR_INVALID_ARG
+    f = lib.mamba_rmsnorm
+    assert f(FAKE, 32, 1, FAKE, 64, FAKE, 1e-5, 4, 64, None) == E         # ld_out < D
+    assert f(None, 64, 1, FAKE, 64, FAKE, 1e-5, 4, 64, None) == E
+    assert f(FAKE, 64, 1, FAKE, 64, None, 1e-5, 4, 64, None) == E
+    assert f(FAKE, 64, 7, FAKE, 64, FAKE, 1e-5, 4, 64, None) == E          # unknown dtype
+    assert f(FAKE, 64, 1, FAKE, 64, FAKE, -1.0, 4, 64, None) == E
+    assert f(None, 0, 1, None, 0, None, 1e-5, 0, 64, None) == 0           # M == 0
+    g = lib.mamba_linear_bf16
+    assert g(FAKE, 64, 0, ctypes.c_void_p(FAKE.value + 2), 64, FAKE, 64, None, 0, 8, 64, 64, None) == E
+    assert g(FAKE, 64, 0, FAKE, 60, FAKE, 64, None, 0, 8, 64, 60, None) == E   # ld_a not a multiple of 8
+    assert g(FAKE, 32, 0, FAKE, 64, FAKE, 64, None, 0, 8, 64, 64, None) == E   # ld_c < N
+    assert g(FAKE, 64, 0, FAKE, 64, FAKE, 64, None, 0, 8, 64, 0, None) == E    # K == 0
+
+
+def test_layer_wrappers_refuse_mismatched_tensors_before_any_call():
+    import torch
+
+    dm, Di, N, K, R = 64, 128, 16, 4, 8
+    bf = lambda *s: torch.zeros(*s, dtype=torch.bfloat16)
+    f = lambda *s: torch.zeros(*s)
+    w = dict(norm_w=f(dm), in_proj_w=bf(2 * Di, dm), conv_w=f(Di, K), x_proj_w=bf(R + 2 * N, Di),
+             dt_proj_w=bf(Di, R), A_log=f(Di, N), out_proj_w=bf(dm, Di))
+    m.layer_struct(w)  # consistent shapes pass
+    for k, bad in (("in_proj_w", f(2 * Di, dm)), ("x_proj_w", bf(R + 2 * N + 1, Di)), ("out_proj_w", bf(Di, dm)),
+                   ("norm_w", f(dm + 1)), ("D", f(Di - 1))):
+        with pytest.raises(ValueError):
+            m.layer_struct(dict(w, **{k: bad}))
+    with pytest.raises(ValueError):
+        m.mamba_layer_prefill(torch.zeros(2, 4, dm, dtype=torch.bfloat16), w)
+    with pytest.raises(ValueError):
+        m.mamba_layer_prefill(torch.zeros(2, 4, dm + 8), w)
+    with pytest.raises(ValueError):
+        m.mamba_layer_prefill(torch.zeros(2, 4, dm), w, conv_state_in=f(2, Di, K + 1))
+    with pytest.raises(ValueError):
+        m.mamba_layer_step(torch.zeros(2, dm), w, f(3, 2, Di, K), f(2, 2, Di, N), 0)
