@@ -49,6 +49,9 @@ KERNEL_SOURCES = {
 }
 KERNEL_SOURCES["mixer_step"] = KERNEL_SOURCES["step"]
 KERNEL_SOURCES["fused"] = KERNEL_SOURCES["scan"]
+KERNEL_SOURCES["gemm"] = ["selective_state_space_conv1d_gb300/csrc/gemm.cu",
+                          "selective_state_space_conv1d_gb300/csrc/async_copy.cuh"]
+KERNEL_SOURCES["rmsnorm"] = ["selective_state_space_conv1d_gb300/csrc/rmsnorm.cu"]
 KERNEL_SOURCES["m3_step"] = ["selective_state_space_conv1d_gb300/csrc/m3_step.cu",
                              "selective_state_space_conv1d_gb300/csrc/device_math.cuh"]
 
@@ -61,6 +64,17 @@ def source_hash(kind: str) -> str:
         with open(os.path.join(ROOT, p), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def bf16_peak():
+    """Dense bf16 tensor peak of the GB300s: (burst, sustained, source)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
 
 
 def hbm_peak():
@@ -903,6 +917,166 @@ def run_prefill_vs_steps(torch, m, synth, device, lengths=(128, 512, 2048), prom
     return out
 
 
+# ------------------------------------------------------------ the whole block ----
+
+BLOCK_SHAPES = {  # name: (d_model, d_inner, d_state, d_conv, dt_rank)
+    "mamba2.8b": (2560, 5120, 16, 4, 160),
+    "mamba130m": (768, 1536, 16, 4, 48),
+}
+
+
+def block_weights(torch, synth, seed, shape, device, layer=0):
+    dm, Di, N, K, R = shape
+    p = synth.layer_params(seed, dm, Di, N, K, R, layer=layer)
+    return {k: torch.from_numpy(np.ascontiguousarray(v, np.float32)).to(device).to(
+        torch.bfloat16 if k.endswith("proj_w") else torch.float32) for k, v in p.items()}
+
+
+def block_stage_calls(torch, m, wd, hidden, Bsz, T, conv_state, ssm_state):
+    """The block's seven calls on buffers of their own (the sequence the block
+    call makes), for per-stage timing: [(name, call, flops or None)]."""
+    dm = hidden.shape[-1]
+    Di, K = wd["conv_w"].shape
+    N = wd["A_log"].shape[1]
+    R = wd["dt_proj_w"].shape[1]
+    rows = Bsz * T
+    dev = hidden.device
+    bf = dict(device=dev, dtype=torch.bfloat16)
+    ldx = (R + 2 * N + 7) // 8 * 8
+    h = torch.empty(rows, dm, **bf)
+    xz = torch.empty(Bsz, T, 2 * Di, **bf)
+    u = torch.empty(Bsz, T, Di, **bf)
+    xd = torch.empty(Bsz, T, ldx, **bf)
+    dt = torch.empty(Bsz, T, Di, **bf)
+    y = torch.empty(Bsz, T, Di, **bf)
+    hid = hidden.view(rows, dm)
+    ws = torch.empty(max(m.mamba_selective_scan_workspace_bytes(Bsz, T, Di, N), 16), dtype=torch.uint8, device=dev)
+    return [
+        ("rmsnorm", lambda: m.mamba_rmsnorm(h, hid, wd["norm_w"]), None),
+        ("in_proj", lambda: m.mamba_linear_bf16(xz.view(rows, 2 * Di), h, wd["in_proj_w"]), 2 * rows * 2 * Di * dm),
+        ("conv", lambda: m.mamba_conv1d_silu_prefill(u, xz[:, :, :Di], wd["conv_w"], wd["conv_b"], conv_state,
+                                                     conv_state), None),
+        ("x_proj", lambda: m.mamba_linear_bf16(xd.view(rows, ldx)[:, :R + 2 * N], u.view(rows, Di), wd["x_proj_w"]),
+         2 * rows * (R + 2 * N) * Di),
+        ("dt_proj", lambda: m.mamba_linear_bf16(dt.view(rows, Di), xd.view(rows, ldx)[:, :R], wd["dt_proj_w"]),
+         2 * rows * Di * R),
+        ("scan", lambda: m.mamba_selective_scan_prefill(y, u, dt, xd[:, :, R:R + N], xd[:, :, R + N:R + 2 * N],
+                                                        wd["A_log"], wd["D"], wd["dt_bias"], xz[:, :, Di:],
+                                                        ssm_state, ssm_state, workspace=ws), None),
+        ("out_proj", lambda: m.mamba_linear_bf16(hid, y.view(rows, Di), wd["out_proj_w"], hid), 2 * rows * dm * Di),
+    ]
+
+
+def run_block_prefill(torch, m, synth, device, steps=20, warmup=3):
+    """One whole mamba-2.8b-shaped Mamba-1 block (RMSNorm, in_proj, conv,
+    x_proj, dt_proj, scan, out_proj + residual) over batch 8 x T 4096 through
+    mamba_layer_prefill, graph-replayed; tokens/s = 32768 / time per block.
+    The roofline is the tensor one of the dominant kernel, the in_proj GEMM."""
+    shape = BLOCK_SHAPES["mamba2.8b"]
+    dm, Di, N, K, R = shape
+    Bsz, T = 8, 4096
+    seed = synth.SEED_BASE + 3
+    wd = block_weights(torch, synth, seed, shape, device)
+    hidden = synth.torch_normal((Bsz, T, dm), 1.0, seed + 31, device)
+    conv = synth.torch_normal((Bsz, Di, K), 1.0, seed + 32, device)
+    ssm = synth.torch_normal((Bsz, Di, N), 0.5, seed + 33, device)
+    ws = torch.empty(m.mamba_layer_workspace_bytes(wd, Bsz, T), dtype=torch.uint8, device=device)
+
+    def block():
+        m.mamba_layer_prefill(hidden, wd, conv, conv, ssm, ssm, workspace=ws)
+
+    for _ in range(warmup):
+        block()
+    torch.cuda.synchronize()
+    ms = kernel_time(torch, [block], steps, reps=1)
+    stages = block_stage_calls(torch, m, wd, hidden, Bsz, T, conv, ssm)
+    stage_ms = {}
+    tflops = {}
+    for name, fn, flops in stages:
+        fn()
+        torch.cuda.synchronize()
+        stage_ms[name] = kernel_time(torch, [fn], 10 if flops else 5, reps=2)
+        if flops:
+            tflops[name] = round(flops / (stage_ms[name] * 1e-3) / 1e12, 1)
+    burst, sustained, src = bf16_peak()
+    in_flops = 2 * Bsz * T * 2 * Di * dm
+    ach = in_flops / (stage_ms["in_proj"] * 1e-3) / 1e12
+    gemm_flops = sum(f for _, _, f in stages if f)
+    gemm_ms = sum(stage_ms[n] for n, _, f in stages if f)
+    rows = Bsz * T
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    route = scan_route(m, Bsz, T, Di, N, sms)
+    del stages
+    return {
+        "workload": "mamba2.8b-block-prefill", "value": round(rows / (ms * 1e-3), 1), "unit": "tokens/s",
+        "ms_per_block": round(ms, 4),
+        "config": {"batch": Bsz, "seq_len": T, "d_model": dm, "d_inner": Di, "d_state": N, "d_conv": K,
+                   "dt_rank": R, "storage": "bf16 weights and activations, f32 residual stream/params/states; "
+                                            "f32 accumulation", "launch": f"CUDA graph of {steps} blocks",
+                   "weights": "random init (no trained weights)"},
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "gemm_tflops": tflops,
+        "gemm_share": round(gemm_ms / sum(stage_ms.values()), 3),
+        "gemm_tflops_all": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
+        "roofline": {"bound": "tensor", "achieved": round(ach, 1), "peak": burst, "unit": "TFLOP/s",
+                     "frac": round(ach / burst, 4), "traffic": ncu_traffic("gemm", "mamba2.8b-in_proj"),
+                     "peak_source": f"{src} cuBLAS bf16 burst (sustained {sustained})",
+                     "algorithmic_flops_per_launch": int(in_flops), "avg_launch_ms": round(stage_ms["in_proj"], 6)},
+        "roofline_kernel": "in_proj GEMM (tcgen05, 128 x 256 tiles)",
+        "scan_route": ROUTE_DESC[route],
+        "gpu_launches_per_block": 6 + (3 if route == "split" else 1),
+    }
+
+
+def run_block_decode(torch, m, synth, device, n_steps=32, L=24, Bsz=128):
+    """Whole-block T=1 decode on mamba-130m shapes: 24 layers x batch 128, each
+    layer the block step (RMSNorm, projections, conv and scan on the layer's
+    state slab, out_proj + residual), graph-replayed; steps/s."""
+    shape = BLOCK_SHAPES["mamba130m"]
+    dm, Di, N, K, R = shape
+    seed = synth.SEED_BASE + 2
+    wds = [block_weights(torch, synth, seed, shape, device, layer=l) for l in range(L)]
+    conv = synth.torch_normal((L, Bsz, Di, K), 0.5, seed + 41, device)
+    ssm = synth.torch_normal((L, Bsz, Di, N), 0.5, seed + 42, device)
+    emb = synth.torch_normal((n_steps, Bsz, dm), 1.0, seed + 43, device)
+    hidden = torch.empty(Bsz, dm, device=device)
+    ws = torch.empty(m.mamba_layer_workspace_bytes(wds[0], Bsz, 1), dtype=torch.uint8, device=device)
+
+    def step(s):
+        hidden.copy_(emb[s])
+        for l in range(L):
+            m.mamba_layer_step(hidden, wds[l], conv, ssm, l, workspace=ws)
+
+    for s in range(3):
+        step(s)
+    torch.cuda.synchronize()
+    g = capture(torch, lambda: [step(s) for s in range(n_steps)])
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 4
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / (reps * n_steps)
+    del g
+    w_bytes = 2 * (2 * Di * dm + (R + 2 * N) * Di + Di * R + dm * Di)
+    state_bytes = Bsz * Di * (N + K) * 4 * 2
+    return {
+        "workload": "mamba130m-block-decode-b128-l24", "value": round(1e3 / ms, 2), "unit": "steps/s",
+        "ms_per_step": round(ms, 5), "layer_token_updates_per_s": round(1e3 / ms * L * Bsz, 1),
+        "config": {"n_layers": L, "batch": Bsz, "d_model": dm, "d_inner": Di, "d_state": N, "d_conv": K,
+                   "dt_rank": R, "launch": f"CUDA graph of {n_steps} steps x {L} layers",
+                   "weights": "random init, distinct per layer"},
+        "bytes_per_step_weights_and_state": int(L * (w_bytes + state_bytes)),
+        "hbm_gbs_weights_and_state": round(L * (w_bytes + state_bytes) / (ms * 1e-3) / 1e9, 1),
+        "gpu_launches_per_step": L * 7,
+    }
+
+
+
 def run_m3_decode(torch, m, device, peak, peak_src, n_steps=16, L=24, Bsz=128, H=24, P=64, N=64):
     """Mamba-3 SISO T=1 decode: L layers x batch B, H heads of headdim P and
     d_state N (a synthetic shape: the pages give none), graph-replayed."""
@@ -1204,6 +1378,10 @@ def main():
         extra["decode_130m_b128_l24"] = run_decode(torch, m, synth, device, peak, peak_src)
         extra["decode_mamba3_siso"] = run_m3_decode(torch, m, device, peak, peak_src)
         extra["prefill_vs_steps"] = run_prefill_vs_steps(torch, m, synth, device)
+        torch.cuda.empty_cache()
+        extra["block_prefill_2p8b"] = run_block_prefill(torch, m, synth, device)
+        torch.cuda.empty_cache()
+        extra["block_decode_130m_b128_l24"] = run_block_decode(torch, m, synth, device)
 
     e2e = run_e2e(torch, m, res, min(args.steps, 100), device)
 

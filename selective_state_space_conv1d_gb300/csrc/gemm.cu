@@ -9,22 +9,26 @@
 // dt_proj, F11 out_proj + residual; prefill.rs `prefill_body` runs the same
 // projections over all T rows.)
 //
-// Design (one CTA per 128 x BN output tile, 4 warps):
+// Design (persistent: one CTA per SM, tiles of 128 x BN, BN 64 / 128 / 256):
 //  * TMA (cp.async.bulk.tensor.2d, 128-byte swizzle) brings 128 x 64 tiles of
-//    A and BN x 64 tiles of W into a 3-stage shared-memory ring; an mbarrier
-//    per stage says "landed" (transaction bytes) and another "consumed".
-//    Rows and columns past M, N or K are zero-filled by the TMA unit.
+//    A and BN x 64 tiles of W into a shared-memory ring of 4-8 stages; an
+//    mbarrier per stage says "landed" (transaction bytes) and another
+//    "consumed".  Rows and columns past M, N or K are zero-filled by TMA.
 //  * One thread issues tcgen05.mma (kind::f16, bf16 x bf16 -> f32, M 128,
-//    N BN, K 16 per instruction) from the shared-memory descriptors into a
-//    BN-column accumulator in tensor memory; tcgen05.commit frees a stage when
-//    its MMAs are done, and a last commit tells the epilogue.
-//  * The four warps read the accumulator back (tcgen05.ld, 32 lanes x 32 bit,
-//    warp w owning rows 32w..32w+31) into shared memory (the ring is free by
-//    then), and the CTA stores it row by row with 16-byte coalesced accesses,
-//    adding the residual and rounding on the way.
+//    N BN, K 16 per instruction) from the shared-memory descriptors into one
+//    of two BN-column accumulators in tensor memory; tcgen05.commit frees a
+//    stage when its MMAs are done, and marks the accumulator full at the end
+//    of a tile.
+//  * Four epilogue warps drain the other accumulator meanwhile (tcgen05.ld,
+//    32 lanes x 32 columns, warp w owning tile rows 32 (w % 4) ...), stage
+//    each 32 x 32 block in shared memory and store it with 16-byte coalesced
+//    accesses, adding the residual and rounding on the way.  A wide tile
+//    reads half the shared memory per MMA of a 128-wide one; the double
+//    accumulator hides the epilogue behind the next tile's MMAs.
 //  * Every mbarrier wait is bounded (about a second); one that runs out sets
-//    MAMBA_FAULT_GEMM_WAIT, and the CTA still waits (bounded) for its copies and
-//    MMAs in flight and frees its tensor memory before it returns.
+//    MAMBA_FAULT_GEMM_WAIT and an abort flag that ends every role's loop; the
+//    CTA still waits (bounded) for its copies and MMAs in flight and frees its
+//    tensor memory before it returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -43,8 +47,11 @@ namespace {
 
 constexpr int kBM = 128;        // rows per tile (the MMA's M)
 constexpr int kBK = 64;         // K per stage: one 128-byte swizzle row of bf16
-constexpr int kStages = 3;  // two CTAs per SM: one's epilogue overlaps the other's main loop
-constexpr int kThreads = 128;
+constexpr int kThreads = 192;   // warp 0 TMA, warp 1 MMA (and tensor-memory owner), warps 2-5 epilogue
+constexpr int kEpiWarps = 4;
+constexpr int kChunk = 32;      // epilogue columns per tensor-memory load
+constexpr int kStagePitch = kChunk + 4;  // floats per staged row (16-byte rows, conflict-free)
+constexpr int kSmemLimit = 232448;       // opt-in shared memory per block on sm_103a
 constexpr long long kWaitLimit = 1ll << 31;  // SM cycles (about a second)
 
 __device__ int g_gemm_faults = 0;
@@ -54,12 +61,17 @@ struct GemmSmem {
   static constexpr int kA = kBM * kBK * 2;  // bytes per stage
   static constexpr int kB = BN * kBK * 2;
   static constexpr int kStage = kA + kB;
+  static constexpr int kEpi = kEpiWarps * 32 * kStagePitch * 4;
+  static constexpr int kFixed = kEpi + 256 + 1024;  // staging, barriers, base alignment
+  static constexpr int kStages0 = (kSmemLimit - kFixed) / kStage;
+  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
   static constexpr int kRing = kStages * kStage;
-  static constexpr int kPitch = BN + 4;                  // epilogue staging row, floats (bank-conflict free)
-  static constexpr int kStaged = kBM * kPitch * 4;       // the staged accumulator reuses the ring
-  static constexpr int kBar = kRing > kStaged ? kRing : kStaged;  // mbarriers after both
-  static constexpr int kBytes = kBar + 8 * (2 * kStages + 1) + 16;
-  static constexpr int kAlloc = kBytes + 1024;           // room to align the base to 1024 bytes
+  static constexpr int kBar = kRing + kEpi;                 // barriers after the ring and the staging
+  static constexpr int kBytes = kBar + 8 * (2 * kStages + 5) + 16;
+  static constexpr int kAlloc = kBytes + 1024;              // room to align the base to 1024 bytes
+  static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+  static_assert(kStages >= 2, "shared memory too small for two stages");
+  static_assert(kAlloc <= kSmemLimit, "shared memory over the opt-in limit");
 };
 
 // Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
@@ -103,11 +115,134 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// 32 lanes x 32 columns of f32 from tensor memory, asynchronous: the registers
+// may be read only after tmem_wait on the same array.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Waits for this thread's tensor-memory loads; the registers are threaded
+// through so that no use of them is scheduled before the wait.
+__device__ __forceinline__ void tmem_wait(uint32_t (&v)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                 "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                 "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                 "+r"(v[29]), "+r"(v[30]), "+r"(v[31])
+               :
+               : "memory");
+}
+
+// One 32 x 32 block of the accumulator, held one row per lane in v, to C:
+// staged through this warp's shared memory and stored 4 rows x 32 columns per
+// step (8 lanes x 4 columns per row), the residual added and the value rounded
+// on the way.  full: the block is inside M and N and the vector accesses are
+// aligned -- then the 8 residual loads are issued together, branch-free.
+template <bool C_BF16>
+__device__ __forceinline__ void emit_block(const uint32_t (&v)[32], float* stage_f, int lane, int row0, int col0,
+                                           bool full, void* c, int64_t ld_c, const float* r, int64_t ld_r, int M,
+                                           int N) {
+  float4* dst = reinterpret_cast<float4*>(stage_f + lane * kStagePitch);
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
+                         __uint_as_float(v[4 * j + 3]));
+  __syncwarp();
+  const int cq = (lane & 7) * 4;
+  const int col = col0 + cq;
+  const int rsub = lane >> 3;
+  if (full) {
+    float4 rv[8];
+    if (r) {
+#pragma unroll
+      for (int it = 0; it < 8; ++it)
+        rv[it] = *reinterpret_cast<const float4*>(r + (int64_t)(row0 + it * 4 + rsub) * ld_r + col);
+    }
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int rr = it * 4 + rsub;
+      float4 x = *reinterpret_cast<const float4*>(stage_f + rr * kStagePitch + cq);
+      if (r) {
+        x.x += rv[it].x;
+        x.y += rv[it].y;
+        x.z += rv[it].z;
+        x.w += rv[it].w;
+      }
+      const int64_t off = (int64_t)(row0 + rr) * ld_c + col;
+      if (C_BF16) {
+        __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(c) + off) = pk;
+      } else {
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(c) + off) = x;
+      }
+    }
+  } else {
+    // an edge block: element by element, inside M and N only
+#pragma unroll 1
+    for (int it = 0; it < 8; ++it) {
+      const int rr = it * 4 + rsub;
+      const int row = row0 + rr;
+      if (row >= M) break;
+      const float* xs = stage_f + rr * kStagePitch + cq;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (col + j >= N) break;
+        float xv = xs[j];
+        if (r) xv += r[(int64_t)row * ld_r + col + j];
+        if (C_BF16)
+          reinterpret_cast<__nv_bfloat16*>(c)[(int64_t)row * ld_c + col + j] = __float2bfloat16_rn(xv);
+        else
+          reinterpret_cast<float*>(c)[(int64_t)row * ld_c + col + j] = xv;
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// The output tile of the persistent schedule's `t`-th tile: groups of kGroupM
+// row blocks sweep all column blocks, so the CTAs of one wave share a few
+// weight tiles and a few activation row blocks in L2.
+constexpr int kGroupM = 16;
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mb, int& nb) {
+  const int per_group = kGroupM * n_tiles;
+  const int g = t / per_group, r = t % per_group;
+  const int m0 = g * kGroupM;
+  const int rows = m_tiles - m0 < kGroupM ? m_tiles - m0 : kGroupM;
+  mb = m0 + r % rows;
+  nb = r / rows;
+}
+
+__device__ __forceinline__ void fail_gemm(volatile int* abort_flag) {
+  atomicOr(&g_gemm_faults, MAMBA_FAULT_GEMM_WAIT);
+  *abort_flag = 1;
+}
+
+// Persistent, warp-specialised: each CTA takes tiles blockIdx.x, +gridDim.x, ...
+//  * warp 0 (one lane) streams the A and W tiles of every K step of every
+//    tile into a kStages-deep ring (TMA; "full" / "empty" barriers per stage);
+//  * warp 1 (one lane) issues the MMAs of a tile into one of two
+//    tensor-memory accumulators and commits "accumulator full";
+//  * warps 2-5 drain the other accumulator meanwhile (tcgen05.ld, staged
+//    through shared memory for 16-byte coalesced stores, residual added and
+//    rounded on the way) and release it ("accumulator empty").
 template <int BN, bool C_BF16>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w, void* c,
                      int64_t ld_c, const float* r, int64_t ld_r, int M, int N, int K, int vec_ok) {
   using L = GemmSmem<BN>;
+  constexpr int S = L::kStages;
   extern __shared__ unsigned char smem_raw[];
   grid_dependency_wait();
   const uint32_t raw = smem_u32(smem_raw);
@@ -115,25 +250,34 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* gbase = smem_raw + (base - raw);
   const uint32_t bars = base + L::kBar;
   auto full = [&](int s) { return bars + 8 * s; };
-  auto empty = [&](int s) { return bars + 8 * (kStages + s); };
-  const uint32_t done = bars + 8 * (2 * kStages);
-  const uint32_t tmem_slot = done + 8;
-  uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(gbase + L::kBar + 8 * (2 * kStages + 1));
+  auto empty = [&](int s) { return bars + 8 * (S + s); };
+  auto acc_full = [&](int a) { return bars + 8 * (2 * S + a); };
+  auto acc_empty = [&](int a) { return bars + 8 * (2 * S + 2 + a); };
+  const uint32_t drain = bars + 8 * (2 * S + 4);
+  uint32_t* tmem_ptr = reinterpret_cast<uint32_t*>(gbase + L::kBar + 8 * (2 * S + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_ptr + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * BN;
+  const int m_tiles = (M + kBM - 1) / kBM, n_tiles = (N + BN - 1) / BN;
+  const int tiles = m_tiles * n_tiles;
   const int k_tiles = (K + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
-    mbar_init(done, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full(a), 1);
+      mbar_init(acc_empty(a), kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 0) {  // the accumulator: BN columns of tensor memory
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tmem_slot), "r"(BN)
+  if (warp == 1) {  // two accumulators of BN f32 columns each
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_ptr)),
+                 "r"(L::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -141,123 +285,116 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_ptr;
-  bool ok = true;
 
-  if (warp == 0 && lane == 0) {
-    // producer: TMA into the ring
-    int issued = 0;
-    for (int kt = 0; kt < k_tiles; ++kt) {
-      const int s = kt % kStages;
-      if (kt >= kStages && !mbar_wait(empty(s), ((kt / kStages) + 1) & 1, kWaitLimit)) {
-        atomicOr(&g_gemm_faults, MAMBA_FAULT_GEMM_WAIT);
-        break;
+  if (warp == 0) {
+    if (lane == 0) {
+      // producer: TMA into the ring, K steps of all this CTA's tiles in order
+      int g = 0;
+      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+        int mb, nb;
+        tile_coords(t, m_tiles, n_tiles, mb, nb);
+        for (int kt = 0; kt < k_tiles; ++kt, ++g) {
+          const int s = g % S;
+          if (g >= S && !mbar_wait(empty(s), ((g / S) + 1) & 1, kWaitLimit)) {
+            fail_gemm(abort_flag);
+            break;
+          }
+          const uint32_t sa = base + s * L::kStage, sb = sa + L::kA;
+          mbar_arrive_expect_tx(full(s), L::kStage);
+          tma_load_2d(sa, &map_a, kt * kBK, mb * kBM, full(s));
+          tma_load_2d(sb, &map_w, kt * kBK, nb * BN, full(s));
+        }
       }
-      const uint32_t sa = base + s * L::kStage, sb = sa + L::kA;
-      mbar_arrive_expect_tx(full(s), L::kStage);
-      tma_load_2d(sa, &map_a, kt * kBK, m0, full(s));
-      tma_load_2d(sb, &map_w, kt * kBK, n0, full(s));
-      issued = kt + 1;
+      // every copy issued lands before this thread moves on
+      for (int q = g > S ? g - S : 0; q < g; ++q)
+        if (!mbar_wait(full(q % S), (q / S) & 1, kWaitLimit)) fail_gemm(abort_flag);
     }
-    // every copy issued lands before this thread moves on
-    for (int kt = issued > kStages ? issued - kStages : 0; kt < issued; ++kt)
-      if (!mbar_wait(full(kt % kStages), (kt / kStages) & 1, kWaitLimit)) atomicOr(&g_gemm_faults, MAMBA_FAULT_GEMM_WAIT);
-  } else if (warp == 1 && lane == 0) {
-    // MMA issuer
-    constexpr uint32_t idesc = instr_desc<BN>();
-    for (int kt = 0; kt < k_tiles; ++kt) {
-      const int s = kt % kStages;
-      if (!mbar_wait(full(s), (kt / kStages) & 1, kWaitLimit)) {
-        atomicOr(&g_gemm_faults, MAMBA_FAULT_GEMM_WAIT);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // MMA issuer
+      constexpr uint32_t idesc = instr_desc<BN>();
+      int g = 0, i = 0;
+      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++i) {
+        const int a = i & 1;
+        if (i >= 2 && !mbar_wait(acc_empty(a), ((i >> 1) + 1) & 1, kWaitLimit)) {
+          fail_gemm(abort_flag);
+          break;
+        }
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint32_t d = tmem + (uint32_t)(a * BN);
+        bool ok = true;
+        for (int kt = 0; kt < k_tiles; ++kt, ++g) {
+          const int s = g % S;
+          if (!mbar_wait(full(s), (g / S) & 1, kWaitLimit)) {
+            fail_gemm(abort_flag);
+            ok = false;
+            break;
+          }
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t sa = base + s * L::kStage, sb = sa + L::kA;
+          const uint64_t da = smem_desc(sa), db = smem_desc(sb);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes = 2 descriptor units per step
+            mma_bf16(d, da + 2 * k, db + 2 * k, idesc, (kt > 0 || k > 0) ? 1u : 0u);
+          mma_commit(empty(s));
+        }
+        if (!ok) break;
+        mma_commit(acc_full(a));
+      }
+      // the MMAs in flight complete before the accumulators are freed
+      mma_commit(drain);
+      if (!mbar_wait(drain, 0, kWaitLimit)) fail_gemm(abort_flag);
+    }
+  } else {
+    // epilogue warps: warp w reads accumulator lanes (tile rows) 32 (w % 4) ...
+    const int quad = warp & 3;
+    float* stage_f = reinterpret_cast<float*>(gbase + L::kRing) + (warp - 2) * 32 * kStagePitch;
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+      const int a = i & 1;
+      if (*abort_flag || !mbar_wait(acc_full(a), (i >> 1) & 1, kWaitLimit)) {
+        if (lane == 0 && !*abort_flag) fail_gemm(abort_flag);
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const uint32_t sa = base + s * L::kStage, sb = sa + L::kA;
-      const uint64_t da = smem_desc(sa), db = smem_desc(sb);
-#pragma unroll
-      for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes = 2 descriptor units per step
-        mma_bf16(tmem, da + 2 * k, db + 2 * k, idesc, (kt > 0 || k > 0) ? 1u : 0u);
-      mma_commit(empty(s));
+      int mb, nb;
+      tile_coords(t, m_tiles, n_tiles, mb, nb);
+      const int row0 = mb * kBM + quad * 32;
+      const int col0 = nb * BN;
+      const int ncols = N - col0 < BN ? N - col0 : BN;  // columns of this tile inside N
+      const bool rows_full = vec_ok && row0 + 32 <= M;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * BN);
+      // two blocks in flight: the next block's tensor-memory load overlaps
+      // this block's stores
+      uint32_t va[32], vb[32];
+      tmem_ld32(taddr, va);
+      tmem_wait(va);
+#pragma unroll 1
+      for (int c0 = 0; c0 < ncols; c0 += 2 * kChunk) {
+        const bool has_b = c0 + kChunk < ncols;
+        if (has_b) tmem_ld32(taddr + (uint32_t)(c0 + kChunk), vb);
+        emit_block<C_BF16>(va, stage_f, lane, row0, col0 + c0, rows_full && c0 + kChunk <= ncols, c, ld_c, r, ld_r,
+                           M, N);
+        if (has_b) tmem_wait(vb);
+        const bool has_next = c0 + 2 * kChunk < ncols;
+        if (has_next) tmem_ld32(taddr + (uint32_t)(c0 + 2 * kChunk), va);
+        if (has_b)
+          emit_block<C_BF16>(vb, stage_f, lane, row0, col0 + c0 + kChunk, rows_full && c0 + 2 * kChunk <= ncols, c,
+                             ld_c, r, ld_r, M, N);
+        if (has_next) tmem_wait(va);
+      }
+      // this warp's share of the accumulator has been read: release it
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(a));
     }
-    mma_commit(done);  // also after a failed wait: the epilogue waits for the MMAs in flight
   }
   __syncwarp();
-
-  // epilogue: all four warps; warp w reads accumulator lanes (rows) 32w..32w+31
-  if (!mbar_wait(done, 0, kWaitLimit)) {
-    if (lane == 0) atomicOr(&g_gemm_faults, MAMBA_FAULT_GEMM_WAIT);
-    ok = false;
-  }
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-  float* stage_f = reinterpret_cast<float*>(gbase);  // [kBM][kPitch], over the (now idle) ring
-  if (ok) {
-#pragma unroll 1
-    for (int c0 = 0; c0 < BN; c0 += 16) {
-      uint32_t v[16];
-      const uint32_t taddr = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c0;
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-          "%15}, [%16];"
-          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-          : "r"(taddr)
-          : "memory");
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      float4* dst = reinterpret_cast<float4*>(stage_f + (warp * 32 + lane) * L::kPitch + c0);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        dst[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]), __uint_as_float(v[4 * j + 2]),
-                             __uint_as_float(v[4 * j + 3]));
-    }
-  }
-  __syncthreads();
-  if (ok) {
-    // row by row: 4 consecutive columns per thread, BN / 4 threads per row
-    constexpr int kTPR = BN / 4;
-    constexpr int kRowsPer = kThreads / kTPR;
-    const int cq = (threadIdx.x % kTPR) * 4;
-    const int col = n0 + cq;
-    // vec_ok: c (and r) aligned for 4-column vector accesses, strides multiples of 4
-    const bool vec = vec_ok && col + 3 < N;
-#pragma unroll 1
-    for (int rr = threadIdx.x / kTPR; rr < kBM; rr += kRowsPer) {
-      const int row = m0 + rr;
-      if (row >= M) break;
-      float4 x = *reinterpret_cast<const float4*>(stage_f + rr * L::kPitch + cq);
-      float xs[4] = {x.x, x.y, x.z, x.w};
-      if (vec) {
-        if (r) {
-          const float4 rv = *reinterpret_cast<const float4*>(r + (int64_t)row * ld_r + col);
-          xs[0] += rv.x; xs[1] += rv.y; xs[2] += rv.z; xs[3] += rv.w;
-        }
-        if (C_BF16) {
-          __nv_bfloat162 lo = __floats2bfloat162_rn(xs[0], xs[1]), hi = __floats2bfloat162_rn(xs[2], xs[3]);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&lo);
-          pk.y = *reinterpret_cast<uint32_t*>(&hi);
-          *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(c) + (int64_t)row * ld_c + col) = pk;
-        } else {
-          *reinterpret_cast<float4*>(reinterpret_cast<float*>(c) + (int64_t)row * ld_c + col) =
-              make_float4(xs[0], xs[1], xs[2], xs[3]);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (col + j >= N) break;
-          float xv = xs[j];
-          if (r) xv += r[(int64_t)row * ld_r + col + j];
-          if (C_BF16)
-            reinterpret_cast<__nv_bfloat16*>(c)[(int64_t)row * ld_c + col + j] = __float2bfloat16_rn(xv);
-          else
-            reinterpret_cast<float*>(c)[(int64_t)row * ld_c + col + j] = xv;
-        }
-      }
-    }
-  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   grid_dependents_launch();
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(BN) : "memory");
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::kTmemCols) : "memory");
 }
 
 // cuTensorMapEncodeTiled from the driver, looked up once
@@ -293,7 +430,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
 }
 
 template <int BN, bool C_BF16>
-cudaError_t launch_bn(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap& mw, cudaStream_t stream) {
+cudaError_t launch_bn(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap& mw, int sms, cudaStream_t stream) {
   auto kern = gemm_bf16_kernel<BN, C_BF16>;
   static int configured[64];
   int dev = 0;
@@ -306,25 +443,55 @@ cudaError_t launch_bn(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMa
       return e;
     __atomic_store_n(&configured[dev], 1, __ATOMIC_RELAXED);
   }
-  const dim3 grid((unsigned)((g.M + kBM - 1) / kBM), (unsigned)((g.N + BN - 1) / BN));
+  const int64_t tiles = ((g.M + kBM - 1) / kBM) * ((g.N + BN - 1) / BN);
+  const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
   const uintptr_t cp = reinterpret_cast<uintptr_t>(g.c), rp = reinterpret_cast<uintptr_t>(g.r);
   const int vec_ok = (cp % (C_BF16 ? 8 : 16)) == 0 && g.ld_c % 4 == 0 && (!g.r || (rp % 16 == 0 && g.ld_r % 4 == 0));
   return launch_pdl(false, kern, grid, dim3(kThreads), (size_t)GemmSmem<BN>::kAlloc, stream, ma, mw, g.c, g.ld_c, g.r,
                     g.ld_r, (int)g.M, (int)g.N, (int)g.K, vec_ok);
 }
 
+template <bool C_BF16>
+cudaError_t launch_typed(const GemmArgs& g, int bn, const CUtensorMap& ma, const CUtensorMap& mw, int sms,
+                         cudaStream_t stream) {
+  if (bn == 64) return launch_bn<64, C_BF16>(g, ma, mw, sms, stream);
+  if (bn == 128) return launch_bn<128, C_BF16>(g, ma, mw, sms, stream);
+  return launch_bn<256, C_BF16>(g, ma, mw, sms, stream);
+}
+
 }  // namespace
+
+// Tile width: the candidate with the least estimated time, (waves of tiles) x
+// (BN + 32) -- a tile costs about its width plus a fixed share (its A tile,
+// the epilogue's start) -- so small problems take narrower tiles that fill
+// more SMs and large ones the wide tiles that halve the shared-memory traffic
+// per MMA.
+int gemm_tile_n(int64_t M, int64_t N, int sms) {
+  int best = 256;
+  int64_t best_cost = INT64_MAX;
+  for (int bn : {256, 128, 64}) {
+    if (bn > 64 && N <= bn / 2) continue;  // no wider than needed
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+    const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 32);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
 
 cudaError_t launch_gemm_bf16(const GemmArgs& g, cudaStream_t stream) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
-  // output tiles of 128 x BN: narrow outputs (x_proj's dt_rank + 2 d_state)
-  // take BN = 64, the rest 128
-  const int bn = g.N <= 64 ? 64 : 128;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int bn = gemm_tile_n(g.M, g.N, sms);
   CUtensorMap ma, mw;
   if (!make_map(&ma, g.a, g.M, g.K, g.ld_a, kBM) || !make_map(&mw, g.w, g.N, g.K, g.ld_w, bn))
     return cudaErrorInvalidValue;
-  if (bn == 64) return g.c_bf16 ? launch_bn<64, true>(g, ma, mw, stream) : launch_bn<64, false>(g, ma, mw, stream);
-  return g.c_bf16 ? launch_bn<128, true>(g, ma, mw, stream) : launch_bn<128, false>(g, ma, mw, stream);
+  return g.c_bf16 ? launch_typed<true>(g, bn, ma, mw, sms, stream) : launch_typed<false>(g, bn, ma, mw, sms, stream);
 }
 
 int read_gemm_faults(bool clear) {

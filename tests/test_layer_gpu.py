@@ -37,6 +37,8 @@ def _bf16_dev(a):
     (2048, 768, 1536),     # 130m out_proj
     (1, 3072, 768),        # one row (a T=1 step at batch 1)
     (130, 200, 1000),
+    (2048, 4096, 256),     # 128 x 256 tiles, more tiles than SMs: both accumulators in turn
+    (640, 2560, 2560),     # 2.8b out_proj-shaped K and N
 ])
 @pytest.mark.parametrize("out", ["f32", "bf16", "f32+residual"])
 def test_linear_matches_oracle(cuda_lib, M, N, K, out):
@@ -333,3 +335,60 @@ def test_block_workspace_smaller_scan_share_same_result(cuda_lib):
     with pytest.raises(m.MambaError):
         ws = torch.empty(act - 256, dtype=torch.uint8, device="cuda")
         m.mamba_layer_prefill(to_dev(x).view(Bsz, T, dm), wd, workspace=ws)
+
+
+def test_block_prefill_2p8b_full_size_sampled(cuda_lib):
+    """The mamba-2.8b-shaped block over batch 8 x T 4096 (the launch shapes the
+    benchmark times): the block call equals its call sequence bit for bit, and
+    each stage matches the oracle on sampled rows (the norm and the
+    projections are row-independent) and on sampled channels of one batch row
+    (the conv and the scan are channel-independent)."""
+    m = cuda_lib
+    dm, Di, N, K, R = 2560, 5120, 16, 4, 160
+    Bsz, T = 8, 4096
+    rows = Bsz * T
+    seed = SEED + 2800
+    p = synth.layer_params(seed, dm, Di, N, K, R, parity=True)
+    wd = _dev_weights(p)
+    x = synth.torch_normal((Bsz, T, dm), 1.0, seed + 1, "cuda")
+    c0 = synth.torch_normal((Bsz, Di, K), 1.0, seed + 2, "cuda")
+    s0 = synth.torch_normal((Bsz, Di, N), 0.5, seed + 3, "cuda")
+    hidden = x.clone()
+    c_out, s_out = torch.empty_like(c0), torch.empty_like(s0)
+    st = _staged(m, wd, hidden, Bsz, T, c0, c_out, s0, s_out)
+    hidden2 = x.clone()
+    c2, s2 = torch.empty_like(c0), torch.empty_like(s0)
+    m.mamba_layer_prefill(hidden2, wd, c0, c2, s0, s2)
+    torch.cuda.synchronize()
+    assert m.mamba_device_faults(clear=True) == 0
+    assert torch.equal(hidden2, hidden) and torch.equal(c2, c_out) and torch.equal(s2, s_out)
+
+    r = np.random.default_rng(seed)
+    sel = np.unique(np.concatenate([r.choice(rows, 96, replace=False), [0, 127, 128, rows - 1]]))
+    idx = torch.as_tensor(sel, device="cuda")
+    pick = lambda t: to_host(t.reshape(rows, -1).index_select(0, idx))
+    xh = pick(x)
+    g = {k: pick(v) for k, v in st.items()}
+    assert_within(g["h"], OL.rmsnorm(xh, p["norm_w"]), "h (sampled rows)", bf16_out=True)
+    assert_within(g["xz"], OL.linear(g["h"], p["in_proj_w"]), "xz (sampled rows)", bf16_out=True)
+    assert_within(g["x_dbl"], OL.linear(g["u"], p["x_proj_w"]), "x_dbl (sampled rows)", bf16_out=True)
+    assert_within(g["dt"], OL.linear(g["x_dbl"][:, :R], p["dt_proj_w"]), "dt (sampled rows)", bf16_out=True)
+    assert_within(pick(hidden), OL.linear(g["y"], p["out_proj_w"], xh), "x + out_proj(y) (sampled rows)")
+
+    # one batch row, sampled channels, through the conv and the scan
+    import oracle
+
+    b = 5
+    ch = np.unique(np.concatenate([r.choice(Di, 40, replace=False), [0, 31, 32, Di - 1]]))
+    cidx = torch.as_tensor(ch, device="cuda")
+    col = lambda t, off=0: to_host(t.view(Bsz, T, -1)[b:b + 1].index_select(2, cidx + off))
+    ps = {k: np.ascontiguousarray(v[ch]) for k, v in p.items() if k in ("conv_w", "conv_b", "A_log", "D", "dt_bias")}
+    u_ref, c_ref = oracle.conv1d_silu_prefill(col(st["xz"]), ps["conv_w"], ps["conv_b"], to_host(c0[b:b + 1, ch]))
+    assert_within(col(st["u"]), u_ref, "u (one row, sampled channels)", bf16_out=True)
+    assert np.array_equal(to_host(c_out[b:b + 1, ch]), c_ref)
+    xdb = to_host(st["x_dbl"].view(Bsz, T, -1)[b:b + 1])
+    y_ref, s_ref = oracle.selective_scan_prefill(col(st["u"]), col(st["dt"]), xdb[:, :, R:R + N],
+                                                 xdb[:, :, R + N:R + 2 * N], ps["A_log"], ps["D"], ps["dt_bias"],
+                                                 col(st["xz"], Di), to_host(s0[b:b + 1, ch]))
+    assert_within(col(st["y"]), y_ref, "y (one row, sampled channels)", bf16_out=True)
+    assert_within(to_host(s_out[b:b + 1, ch]), s_ref, "ssm state (one row, sampled channels)")
