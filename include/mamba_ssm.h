@@ -349,7 +349,9 @@ MAMBA_API int mamba_decode_graph_destroy(MambaDecodeGraph* graph);
  *             may be c itself (f32, same stride) for an in-place residual add
  * a and w must be 16-byte aligned with ld_a, ld_w multiples of 8 (the tiles
  * are moved by the tensor memory accelerator); K >= 1 of any size (the tiles
- * past K read as zero).  M, N, K below 2^31.
+ * past K read as zero).  M, N, K below 2^31.  A shape with few output tiles
+ * and a long K splits K over a cluster of CTAs that sum their parts in a fixed
+ * order; the split depends on (M, N, K) only, so results are deterministic.
  * Errors: MAMBA_ERR_INVALID_ARG for NULL pointers, strides smaller than a row,
  * misaligned a / w, overlap of c with an input (other than the residual as
  * above), extent overflow.
@@ -436,8 +438,11 @@ MAMBA_API int mamba_layer_prefill(float* hidden, const MambaLayer* layer, const 
  * One T = 1 block step for B sequences on slab `layer_index` of the
  * persistent layer-major states (conv [n_layers][B][d_inner][d_conv], ssm
  * [n_layers][B][d_inner][d_state], both updated in place): the prefill's
- * sequence with T = 1 (inference.rs `step_kernels`).  hidden [B][d_model] f32
- * in place; workspace as for mamba_layer_prefill with T = 1.
+ * sequence with T = 1 (inference.rs `step_kernels`), the conv and the scan
+ * being the T = 1 step kernels of mamba_conv1d_silu_step and
+ * mamba_ssm_step_batched on the same strided views (equal to a T = 1 prefill
+ * bit for bit).  hidden [B][d_model] f32 in place; workspace as for
+ * mamba_layer_prefill with T = 1.
  */
 MAMBA_API int mamba_layer_step(float* hidden, const MambaLayer* layer, float* conv_state, float* ssm_state,
                                int64_t layer_index, int64_t n_layers, int64_t B, void* workspace,

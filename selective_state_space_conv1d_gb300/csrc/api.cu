@@ -207,10 +207,12 @@ int layer_plan(const MambaLayer* L, int64_t B, int64_t T, LayerPlan* p) {
   return MAMBA_OK;
 }
 
-// the block over B x T tokens; the scan gets the workspace past the
-// activations when scan_share (prefill), none for a step (its plain route)
+// the block over B x T tokens.  A prefill gives the scan the workspace past
+// the activations; a step (T = 1, states updated in place on their slab) runs
+// the conv and SSM step kernels on the same strided views instead of the
+// prefill kernels -- the same arithmetic, bit for bit
 int run_layer(float* hidden, const MambaLayer* L, const float* conv_in, float* conv_out, const float* ssm_in,
-              float* ssm_out, int64_t B, int64_t T, void* workspace, int64_t workspace_bytes, bool scan_share,
+              float* ssm_out, int64_t B, int64_t T, void* workspace, int64_t workspace_bytes, bool step,
               void* stream) {
   int rc;
   LayerPlan p;
@@ -266,7 +268,7 @@ int run_layer(float* hidden, const MambaLayer* L, const float* conv_in, float* c
   auto* xd = ws + p.off_xd;
   auto* dt = ws + p.off_dt;
   auto* y = ws + p.off_y;
-  void* scan_ws = scan_share && workspace_bytes > p.act_bytes ? ws + p.act_bytes : nullptr;
+  void* scan_ws = !step && workspace_bytes > p.act_bytes ? ws + p.act_bytes : nullptr;
   const int64_t scan_bytes = scan_ws ? workspace_bytes - p.act_bytes : 0;
   const int64_t rows = p.rows, ldx = p.ldx;
   // F1 RMSNorm (f32 residual in, bf16 out); F2 in_proj
@@ -274,9 +276,16 @@ int run_layer(float* hidden, const MambaLayer* L, const float* conv_in, float* c
   if ((rc = mamba_linear_bf16(xz, 2 * Di, MAMBA_BF16, h, dm, L->in_proj_w, dm, nullptr, 0, rows, 2 * Di, dm, stream)))
     return rc;
   // F3-F4: the conv reads the x half of xz in place (row stride 2 d_inner)
-  if ((rc = mamba_conv1d_silu_prefill(u, Di, xz, 2 * Di, MAMBA_BF16, conv_in, conv_out, L->conv_w, L->conv_b, B, T,
-                                      Di, K, stream)))
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (step) {
+    mamba::ConvStepArgs ca{u, xz, conv_out, L->conv_w, L->conv_b, B, Di, (int)K, 1};
+    ca.ld_x = 2 * Di;
+    const cudaError_t e = mamba::launch_conv1d_silu_step(ca, dev, cs);
+    if (e != cudaSuccess) return cuda_fail("layer step: conv1d_silu_step launch", e);
+  } else if ((rc = mamba_conv1d_silu_prefill(u, Di, xz, 2 * Di, MAMBA_BF16, conv_in, conv_out, L->conv_w, L->conv_b,
+                                             B, T, Di, K, stream))) {
     return rc;
+  }
   // F5 x_proj -> [dt_rank | B | C]; F6 dt_proj on the first dt_rank columns
   if ((rc = mamba_linear_bf16(xd, ldx, MAMBA_BF16, u, Di, L->x_proj_w, Di, nullptr, 0, rows, xdim, Di, stream)))
     return rc;
@@ -286,10 +295,20 @@ int run_layer(float* hidden, const MambaLayer* L, const float* conv_in, float* c
   char* xz_z = xz + Di * 2;
   char* xd_b = xd + R * 2;
   char* xd_c = xd + (R + N) * 2;
-  if ((rc = mamba_selective_scan_prefill(y, Di, MAMBA_BF16, u, Di, dt, Di, xz_z, 2 * Di, xd_b, ldx, xd_c, ldx,
-                                         MAMBA_BF16, L->A_log, L->D, L->dt_proj_b, ssm_in, ssm_out, B, T, Di, N,
-                                         scan_ws, scan_bytes, stream)))
+  if (step) {
+    mamba::SsmStepArgs sa{y, 1, u, dt, xz_z, xd_b, xd_c, 1, L->A_log, L->D, L->dt_proj_b, ssm_out, B, Di, (int)N};
+    sa.ld_ux = Di;
+    sa.ld_dt = Di;
+    sa.ld_z = 2 * Di;
+    sa.ld_B = ldx;
+    sa.ld_C = ldx;
+    const cudaError_t e = mamba::launch_ssm_step_batched(sa, dev, cs);
+    if (e != cudaSuccess) return cuda_fail("layer step: ssm_step_batched launch", e);
+  } else if ((rc = mamba_selective_scan_prefill(y, Di, MAMBA_BF16, u, Di, dt, Di, xz_z, 2 * Di, xd_b, ldx, xd_c,
+                                                ldx, MAMBA_BF16, L->A_log, L->D, L->dt_proj_b, ssm_in, ssm_out, B, T,
+                                                Di, N, scan_ws, scan_bytes, stream))) {
     return rc;
+  }
   // F11-F12: out_proj with the residual added in its epilogue, in place
   return mamba_linear_bf16(hidden, dm, MAMBA_F32, y, Di, L->out_proj_w, Di, hidden, dm, rows, dm, Di, stream);
 }
@@ -780,7 +799,7 @@ int mamba_layer_prefill(float* hidden, const MambaLayer* layer, const float* con
                         int64_t workspace_bytes, void* stream) {
   if (workspace_bytes < 0) return fail(MAMBA_ERR_INVALID_ARG, "negative workspace_bytes");
   return run_layer(hidden, layer, conv_state_in, conv_state_out, ssm_state_in, ssm_state_out, B, T, workspace,
-                   workspace_bytes, true, stream);
+                   workspace_bytes, false, stream);
 }
 
 int mamba_layer_step(float* hidden, const MambaLayer* layer, float* conv_state, float* ssm_state,
@@ -799,7 +818,7 @@ int mamba_layer_step(float* hidden, const MambaLayer* layer, float* conv_state, 
     return fail(MAMBA_ERR_INVALID_ARG, "extent overflow or invalid dims");
   float* cslab = conv_state + layer_index * B * Di * K;
   float* sslab = ssm_state + layer_index * B * Di * N;
-  return run_layer(hidden, layer, cslab, cslab, sslab, sslab, B, 1, workspace, workspace_bytes, false, stream);
+  return run_layer(hidden, layer, cslab, cslab, sslab, sslab, B, 1, workspace, workspace_bytes, true, stream);
 }
 
 }  // extern "C"

@@ -219,7 +219,7 @@ __global__ void __launch_bounds__(kStepThreads) conv1d_silu_step_kernel(ConvStep
   load_window<K>(a.w + c * K, w);
 #pragma unroll
   for (int k = 0; k + 1 < K; ++k) s[k] = old[k + 1];
-  s[K - 1] = to_f32(reinterpret_cast<const T*>(a.x)[i]);
+  s[K - 1] = to_f32(reinterpret_cast<const T*>(a.x)[a.ld_x == a.Di ? i : (i - c) / a.Di * a.ld_x + c]);
   const float bias = a.bias ? a.bias[c] : 0.0f;
   reinterpret_cast<T*>(a.u)[i] = from_f32<T>(silu_f(conv_taps<K>(w, s, bias)));
   store_window<K>(st, s);
@@ -301,7 +301,9 @@ cudaError_t launch_conv1d_silu_prefill(const ConvPrefillArgs& a, const DeviceInf
 cudaError_t launch_conv1d_silu_step(const ConvStepArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream) {
   (void)dev;
-  return a.bf16 ? step_dispatch_k<__nv_bfloat16>(a, stream) : step_dispatch_k<float>(a, stream);
+  ConvStepArgs d = a;
+  if (d.ld_x == 0) d.ld_x = d.Di;  // dense rows
+  return d.bf16 ? step_dispatch_k<__nv_bfloat16>(d, stream) : step_dispatch_k<float>(d, stream);
 }
 
 }  // namespace mamba

@@ -29,6 +29,7 @@
 //    MAMBA_FAULT_GEMM_WAIT and an abort flag that ends every role's loop; the
 //    CTA still waits (bounded) for its copies and MMAs in flight and frees its
 //    tensor memory before it returns.
+#include <cooperative_groups.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -56,7 +57,7 @@ constexpr long long kWaitLimit = 1ll << 31;  // SM cycles (about a second)
 
 __device__ int g_gemm_faults = 0;
 
-template <int BN>
+template <int BN, int MAX_STAGES = 8>
 struct GemmSmem {
   static constexpr int kA = kBM * kBK * 2;  // bytes per stage
   static constexpr int kB = BN * kBK * 2;
@@ -64,7 +65,7 @@ struct GemmSmem {
   static constexpr int kEpi = kEpiWarps * 32 * kStagePitch * 4;
   static constexpr int kFixed = kEpi + 256 + 1024;  // staging, barriers, base alignment
   static constexpr int kStages0 = (kSmemLimit - kFixed) / kStage;
-  static constexpr int kStages = kStages0 > 8 ? 8 : kStages0;
+  static constexpr int kStages = kStages0 > MAX_STAGES ? MAX_STAGES : kStages0;
   static constexpr int kRing = kStages * kStage;
   static constexpr int kBar = kRing + kEpi;                 // barriers after the ring and the staging
   static constexpr int kBytes = kBar + 8 * (2 * kStages + 5) + 16;
@@ -237,14 +238,23 @@ __device__ __forceinline__ void fail_gemm(volatile int* abort_flag) {
 //  * warps 2-5 drain the other accumulator meanwhile (tcgen05.ld, staged
 //    through shared memory for 16-byte coalesced stores, residual added and
 //    rounded on the way) and release it ("accumulator empty").
-template <int BN, bool C_BF16>
+//
+// SPLIT (few output tiles, long K): a cluster of `splits` CTAs shares one
+// tile, CTA rank q accumulating K steps [q k_tiles / splits, (q + 1) k_tiles /
+// splits).  Every rank leaves its partial sums in its shared memory; after a
+// cluster barrier rank q sums all ranks' partials, in rank order, for its
+// 128 / splits rows of the tile through distributed shared memory and stores
+// them -- a deterministic split with no global scratch and no second launch.
+template <int BN, bool C_BF16, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w, void* c,
-                     int64_t ld_c, const float* r, int64_t ld_r, int M, int N, int K, int vec_ok) {
-  using L = GemmSmem<BN>;
+                     int64_t ld_c, const float* r, int64_t ld_r, int M, int N, int K, int vec_ok, int splits) {
+  // a split CTA runs a few K steps of one tile: a short ring and half the
+  // shared memory, so two split CTAs fit on an SM
+  using L = GemmSmem<BN, SPLIT ? 3 : 8>;
   constexpr int S = L::kStages;
+  static_assert(!SPLIT || kBM * (BN + 4) * 4 <= L::kRing, "the partial sums must fit in the ring");
   extern __shared__ unsigned char smem_raw[];
-  grid_dependency_wait();
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023) & ~1023u;  // 1024-byte aligned for the 128-byte swizzle
   unsigned char* gbase = smem_raw + (base - raw);
@@ -261,6 +271,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int m_tiles = (M + kBM - 1) / kBM, n_tiles = (N + BN - 1) / BN;
   const int tiles = m_tiles * n_tiles;
   const int k_tiles = (K + kBK - 1) / kBK;
+  // this CTA's tiles (t_first, + t_step, ...) and K steps [kb, ke)
+  int rank = 0, t_first = blockIdx.x, t_step = gridDim.x, kb = 0, ke = k_tiles;
+  if constexpr (SPLIT) {
+    asm("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+    t_first = blockIdx.x / splits;
+    t_step = gridDim.x / splits;
+    kb = rank * k_tiles / splits;
+    ke = (rank + 1) * k_tiles / splits;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -285,15 +304,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_ptr;
+  // every CTA is resident (one wave): the next kernel may start its set-up;
+  // nothing below touches global memory before the previous kernel is done
+  grid_dependents_launch();
+  grid_dependency_wait();
 
+  bool have_acc = false;  // SPLIT: this epilogue warp saw its accumulator complete
   if (warp == 0) {
     if (lane == 0) {
       // producer: TMA into the ring, K steps of all this CTA's tiles in order
       int g = 0;
-      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x) {
+      for (int t = t_first; t < tiles && !*abort_flag; t += t_step) {
         int mb, nb;
         tile_coords(t, m_tiles, n_tiles, mb, nb);
-        for (int kt = 0; kt < k_tiles; ++kt, ++g) {
+        for (int kt = kb; kt < ke; ++kt, ++g) {
           const int s = g % S;
           if (g >= S && !mbar_wait(empty(s), ((g / S) + 1) & 1, kWaitLimit)) {
             fail_gemm(abort_flag);
@@ -314,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // MMA issuer
       constexpr uint32_t idesc = instr_desc<BN>();
       int g = 0, i = 0;
-      for (int t = blockIdx.x; t < tiles && !*abort_flag; t += gridDim.x, ++i) {
+      for (int t = t_first; t < tiles && !*abort_flag; t += t_step, ++i) {
         const int a = i & 1;
         if (i >= 2 && !mbar_wait(acc_empty(a), ((i >> 1) + 1) & 1, kWaitLimit)) {
           fail_gemm(abort_flag);
@@ -323,7 +347,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t d = tmem + (uint32_t)(a * BN);
         bool ok = true;
-        for (int kt = 0; kt < k_tiles; ++kt, ++g) {
+        for (int kt = kb; kt < ke; ++kt, ++g) {
           const int s = g % S;
           if (!mbar_wait(full(s), (g / S) & 1, kWaitLimit)) {
             fail_gemm(abort_flag);
@@ -335,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t da = smem_desc(sa), db = smem_desc(sb);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k)  // 16 bf16 = 32 bytes = 2 descriptor units per step
-            mma_bf16(d, da + 2 * k, db + 2 * k, idesc, (kt > 0 || k > 0) ? 1u : 0u);
+            mma_bf16(d, da + 2 * k, db + 2 * k, idesc, (kt > kb || k > 0) ? 1u : 0u);
           mma_commit(empty(s));
         }
         if (!ok) break;
@@ -350,13 +374,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     float* stage_f = reinterpret_cast<float*>(gbase + L::kRing) + (warp - 2) * 32 * kStagePitch;
     int i = 0;
-    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+    for (int t = t_first; t < tiles; t += t_step, ++i) {
       const int a = i & 1;
       if (*abort_flag || !mbar_wait(acc_full(a), (i >> 1) & 1, kWaitLimit)) {
         if (lane == 0 && !*abort_flag) fail_gemm(abort_flag);
         break;
       }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if constexpr (SPLIT) {
+        // one tile per CTA: every rank parks its partial sums (all BN
+        // columns) in its shared memory, over the idle ring
+        {
+          float* part = reinterpret_cast<float*>(gbase) + (quad * 32 + lane) * (BN + 4);
+#pragma unroll 1
+          for (int c0 = 0; c0 < BN; c0 += kChunk) {
+            uint32_t v[32];
+            tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)c0, v);
+            tmem_wait(v);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(part + c0 + 4 * j) =
+                  make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                              __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
+        }
+        have_acc = true;
+        continue;
+      }
       int mb, nb;
       tile_coords(t, m_tiles, n_tiles, mb, nb);
       const int row0 = mb * kBM + quad * 32;
@@ -390,9 +434,78 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncwarp();
+  if constexpr (SPLIT) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();  // the partial sums of every rank are in place
+    if (warp >= 2 && have_acc) {
+      // rank q finishes rows [q 128 / splits, (q + 1) 128 / splits) of the
+      // tile: each element is the sum of the ranks' partials in rank order
+      // (the same order whichever rank adds them), read through distributed
+      // shared memory a row segment of 4 columns per thread, coalesced
+      int mb, nb;
+      tile_coords(t_first, m_tiles, n_tiles, mb, nb);
+      const int col0 = nb * BN;
+      const int ncols = N - col0 < BN ? N - col0 : BN;
+      const int r_lo = rank * kBM / splits, r_hi = (rank + 1) * kBM / splits;
+      constexpr int kTPR = BN / 4;                   // threads per row
+      constexpr int kRowsPer = (kEpiWarps * 32) / kTPR;
+      const int e = threadIdx.x - 64;                // 0..127
+      const int cq = (e % kTPR) * 4;
+      const float* part0 = reinterpret_cast<const float*>(gbase);
+#pragma unroll 1
+      for (int rr = r_lo + e / kTPR; rr < r_hi; rr += kRowsPer) {
+        const int row = mb * kBM + rr;
+        if (row >= M || cq >= ncols) continue;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < splits; ++q) {
+          const float4 x =
+              *reinterpret_cast<const float4*>(cluster.map_shared_rank(part0, q) + rr * (BN + 4) + cq);
+          if (q == 0) {
+            acc = x;
+          } else {
+            acc.x += x.x;
+            acc.y += x.y;
+            acc.z += x.z;
+            acc.w += x.w;
+          }
+        }
+        const int col = col0 + cq;
+        float xs[4] = {acc.x, acc.y, acc.z, acc.w};
+        if (vec_ok && cq + 4 <= ncols) {
+          if (r) {
+            const float4 rv = *reinterpret_cast<const float4*>(r + (int64_t)row * ld_r + col);
+            xs[0] += rv.x;
+            xs[1] += rv.y;
+            xs[2] += rv.z;
+            xs[3] += rv.w;
+          }
+          if (C_BF16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(xs[0], xs[1]), hi = __floats2bfloat162_rn(xs[2], xs[3]);
+            uint2 pk;
+            pk.x = *reinterpret_cast<uint32_t*>(&lo);
+            pk.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(c) + (int64_t)row * ld_c + col) = pk;
+          } else {
+            *reinterpret_cast<float4*>(reinterpret_cast<float*>(c) + (int64_t)row * ld_c + col) =
+                make_float4(xs[0], xs[1], xs[2], xs[3]);
+          }
+        } else {
+          for (int j = 0; j < 4 && cq + j < ncols; ++j) {
+            float xv = xs[j];
+            if (r) xv += r[(int64_t)row * ld_r + col + j];
+            if (C_BF16)
+              reinterpret_cast<__nv_bfloat16*>(c)[(int64_t)row * ld_c + col + j] = __float2bfloat16_rn(xv);
+            else
+              reinterpret_cast<float*>(c)[(int64_t)row * ld_c + col + j] = xv;
+          }
+        }
+      }
+    }
+    cluster.sync();  // every rank has read its peers' shared memory
+  }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  grid_dependents_launch();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(L::kTmemCols) : "memory");
 }
@@ -429,34 +542,52 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, bool C_BF16>
-cudaError_t launch_bn(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap& mw, int sms, cudaStream_t stream) {
-  auto kern = gemm_bf16_kernel<BN, C_BF16>;
+template <int BN, bool C_BF16, bool SPLIT>
+cudaError_t launch_bn(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMap& mw, int sms, int splits,
+                      cudaStream_t stream) {
+  auto kern = gemm_bf16_kernel<BN, C_BF16, SPLIT>;
+  using Smem = GemmSmem<BN, SPLIT ? 3 : 8>;
   static int configured[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!__atomic_load_n(&configured[dev], __ATOMIC_RELAXED)) {
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmSmem<BN>::kAlloc)) !=
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem::kAlloc)) !=
         cudaSuccess)
       return e;
     __atomic_store_n(&configured[dev], 1, __ATOMIC_RELAXED);
   }
   const int64_t tiles = ((g.M + kBM - 1) / kBM) * ((g.N + BN - 1) / BN);
-  const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
   const uintptr_t cp = reinterpret_cast<uintptr_t>(g.c), rp = reinterpret_cast<uintptr_t>(g.r);
   const int vec_ok = (cp % (C_BF16 ? 8 : 16)) == 0 && g.ld_c % 4 == 0 && (!g.r || (rp % 16 == 0 && g.ld_r % 4 == 0));
-  return launch_pdl(false, kern, grid, dim3(kThreads), (size_t)GemmSmem<BN>::kAlloc, stream, ma, mw, g.c, g.ld_c, g.r,
-                    g.ld_r, (int)g.M, (int)g.N, (int)g.K, vec_ok);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(SPLIT ? tiles * splits : (tiles < sms ? tiles : sms)));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem::kAlloc;
+  cfg.stream = stream;
+  // programmatic dependent launch: this grid's set-up (barriers, tensor
+  // memory) overlaps the previous kernel's tail; its first global access waits
+  // for that kernel (griddepcontrol.wait)
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = SPLIT ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mw, g.c, g.ld_c, g.r, g.ld_r, (int)g.M, (int)g.N, (int)g.K, vec_ok,
+                            SPLIT ? splits : 1);
 }
 
-template <bool C_BF16>
-cudaError_t launch_typed(const GemmArgs& g, int bn, const CUtensorMap& ma, const CUtensorMap& mw, int sms,
+template <bool C_BF16, bool SPLIT>
+cudaError_t launch_typed(const GemmArgs& g, int bn, const CUtensorMap& ma, const CUtensorMap& mw, int sms, int splits,
                          cudaStream_t stream) {
-  if (bn == 64) return launch_bn<64, C_BF16>(g, ma, mw, sms, stream);
-  if (bn == 128) return launch_bn<128, C_BF16>(g, ma, mw, sms, stream);
-  return launch_bn<256, C_BF16>(g, ma, mw, sms, stream);
+  if (bn == 64) return launch_bn<64, C_BF16, SPLIT>(g, ma, mw, sms, splits, stream);
+  if (bn == 128) return launch_bn<128, C_BF16, SPLIT>(g, ma, mw, sms, splits, stream);
+  return launch_bn<256, C_BF16, SPLIT>(g, ma, mw, sms, splits, stream);
 }
 
 }  // namespace
@@ -481,6 +612,20 @@ int gemm_tile_n(int64_t M, int64_t N, int sms) {
   return best;
 }
 
+// K split: when the output has at most half an SM's worth of tiles and K has
+// at least 4 stages, clusters of up to 8 CTAs share a tile (at least two K
+// stages each, no more CTAs than SMs).  It depends on the shape only, so a
+// shape always sums its K in the same order.
+int gemm_k_splits(int64_t M, int64_t N, int64_t K, int bn, int sms) {
+  const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
+  const int64_t k_tiles = (K + kBK - 1) / kBK;
+  if (tiles * 2 > sms || k_tiles < 4) return 1;
+  int64_t sp = k_tiles / 2;
+  if (sp > 8) sp = 8;
+  if (sp > sms / tiles) sp = sms / tiles;
+  return sp >= 2 ? (int)sp : 1;
+}
+
 cudaError_t launch_gemm_bf16(const GemmArgs& g, cudaStream_t stream) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
   int dev = 0, sms = 0;
@@ -488,10 +633,15 @@ cudaError_t launch_gemm_bf16(const GemmArgs& g, cudaStream_t stream) {
   if (e != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int bn = gemm_tile_n(g.M, g.N, sms);
+  const int splits = gemm_k_splits(g.M, g.N, g.K, bn, sms);
   CUtensorMap ma, mw;
   if (!make_map(&ma, g.a, g.M, g.K, g.ld_a, kBM) || !make_map(&mw, g.w, g.N, g.K, g.ld_w, bn))
     return cudaErrorInvalidValue;
-  return g.c_bf16 ? launch_typed<true>(g, bn, ma, mw, sms, stream) : launch_typed<false>(g, bn, ma, mw, sms, stream);
+  if (splits > 1)
+    return g.c_bf16 ? launch_typed<true, true>(g, bn, ma, mw, sms, splits, stream)
+                    : launch_typed<false, true>(g, bn, ma, mw, sms, splits, stream);
+  return g.c_bf16 ? launch_typed<true, false>(g, bn, ma, mw, sms, 1, stream)
+                  : launch_typed<false, false>(g, bn, ma, mw, sms, 1, stream);
 }
 
 int read_gemm_faults(bool clear) {

@@ -71,6 +71,7 @@ struct ConvStepArgs {
   int64_t B, Di;
   int K;
   int bf16;
+  int64_t ld_x = 0;  // row stride of x (elements); 0: dense (Di)
 };
 cudaError_t launch_conv1d_silu_step(const ConvStepArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream);
@@ -164,6 +165,9 @@ struct SsmStepArgs {
   float* state;  // slab of the layer: [B][Di][N]
   int64_t B, Di;
   int N;
+  // row strides (elements) of u (x in the fused step), dt, z, B and C; 0: dense
+  // (Di for the activations, N for B and C).  y and the states are dense.
+  int64_t ld_ux = 0, ld_dt = 0, ld_z = 0, ld_B = 0, ld_C = 0;
 };
 cudaError_t launch_ssm_step_batched(const SsmStepArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream);

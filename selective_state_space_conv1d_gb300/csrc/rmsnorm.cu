@@ -72,6 +72,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta)
       }
     }
   }
+  // after the work: a many-wave grid must not let the next kernel take SMs early
   grid_dependents_launch();
 }
 
@@ -85,9 +86,9 @@ cudaError_t launch_typed(const RmsNormArgs& a, cudaStream_t stream) {
                    po % (OUT_BF16 ? 8 : 16) == 0;
   const dim3 grid((unsigned)((a.M + kRowsPerCta - 1) / kRowsPerCta)), block(32 * kRowsPerCta);
   if (vec)
-    return launch_pdl(false, rmsnorm_kernel<OUT_BF16, true>, grid, block, 0, stream, a.out, a.ld_out, a.x, a.ld_x,
+    return launch_pdl(true, rmsnorm_kernel<OUT_BF16, true>, grid, block, 0, stream, a.out, a.ld_out, a.x, a.ld_x,
                       a.w, a.eps, a.M, (int)a.D);
-  return launch_pdl(false, rmsnorm_kernel<OUT_BF16, false>, grid, block, 0, stream, a.out, a.ld_out, a.x, a.ld_x,
+  return launch_pdl(true, rmsnorm_kernel<OUT_BF16, false>, grid, block, 0, stream, a.out, a.ld_out, a.x, a.ld_x,
                     a.w, a.eps, a.M, (int)a.D);
 }
 

@@ -134,13 +134,13 @@ __global__ void __launch_bounds__(kMaxThreads) step_kernel(StepArgs args, int bt
     const int64_t row = brow[i] * Di + cc;
     load_group<P>(a.state + row * N + q * P, h[i], state_vec);
     if constexpr (FUSE) load_group<KK>(args.conv_state + row * K, win[i], (K % 4 == 0) && state_vec);
-    uxv[i] = to_f32(UX[row]);
-    dtv[i] = to_f32(DT[row]);
-    zv[i] = gate ? to_f32(Z[row]) : 0.0f;
+    uxv[i] = to_f32(UX[brow[i] * a.ld_ux + cc]);
+    dtv[i] = to_f32(DT[brow[i] * a.ld_dt + cc]);
+    zv[i] = gate ? to_f32(Z[brow[i] * a.ld_z + cc]) : 0.0f;
   }
   float Bn[P], Cn[P];  // B / C of the next row, fetched one row ahead
-  load_group<P>(Bm + brow[0] * N + q * P, Bn, bc_vec);
-  load_group<P>(Cm + brow[0] * N + q * P, Cn, bc_vec);
+  load_group<P>(Bm + brow[0] * a.ld_B + q * P, Bn, bc_vec);
+  load_group<P>(Cm + brow[0] * a.ld_C + q * P, Cn, bc_vec);
 
   // per-channel parameters (L2-resident), after the loads are in flight
   float a2[P], w[KK];
@@ -165,8 +165,8 @@ __global__ void __launch_bounds__(kMaxThreads) step_kernel(StepArgs args, int bt
       Cv[j] = Cn[j];
     }
     if (i + 1 < kRows) {
-      load_group<P>(Bm + brow[i + 1] * N + q * P, Bn, bc_vec);
-      load_group<P>(Cm + brow[i + 1] * N + q * P, Cn, bc_vec);
+      load_group<P>(Bm + brow[i + 1] * a.ld_B + q * P, Bn, bc_vec);
+      load_group<P>(Cm + brow[i + 1] * a.ld_C + q * P, Cn, bc_vec);
     }
     const int64_t row = brow[i] * Di + cc;
     float uv = uxv[i];
@@ -303,11 +303,11 @@ __global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args
       mbar_arrive_expect_tx(fb, bytes);
       bulk_g2s(st + L::kState, a.state + row * N, nch * N * 4, fb);
       if constexpr (FUSE) bulk_g2s(st + L::kConv, args.conv_state + row * K, nch * K * 4, fb);
-      bulk_g2s(st + L::kUX, UX + row * es, act, fb);
-      bulk_g2s(st + L::kDT, DT + row * es, act, fb);
-      if (gate) bulk_g2s(st + L::kZ, Z + row * es, act, fb);
-      bulk_g2s(st + L::kB, BM + b * N * es, N * es, fb);
-      bulk_g2s(st + L::kC, CM + b * N * es, N * es, fb);
+      bulk_g2s(st + L::kUX, UX + (b * a.ld_ux + c0) * es, act, fb);
+      bulk_g2s(st + L::kDT, DT + (b * a.ld_dt + c0) * es, act, fb);
+      if (gate) bulk_g2s(st + L::kZ, Z + (b * a.ld_z + c0) * es, act, fb);
+      bulk_g2s(st + L::kB, BM + b * a.ld_B * es, N * es, fb);
+      bulk_g2s(st + L::kC, CM + b * a.ld_C * es, N * es, fb);
       issued = i + 1;
       if (++s == stages) {
         s = 0;
@@ -385,11 +385,16 @@ __global__ void __launch_bounds__(ring::kThreads) ring_step_kernel(StepArgs args
 
 // The ring path needs every bulk copy 16-byte aligned and a multiple of 16
 // bytes: Di % 8 == 0 (tile offsets and lengths are multiples of 8 channels),
-// N * es % 16 == 0 (B / C rows), and 16-byte aligned base pointers.
+// N * es % 16 == 0 (B / C rows), 16-byte aligned base pointers and row
+// strides.
 bool ring_eligible(const StepArgs& a, bool fuse) {
   const int es = a.s.in_bf16 ? 2 : 4;
   const auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
   if (a.s.Di % 8 != 0 || (a.s.N * es) % 16 != 0) return false;
+  // every row of every input starts on a 16-byte boundary
+  for (int64_t ld : {a.s.ld_ux, a.s.ld_dt, a.s.ld_B, a.s.ld_C})
+    if ((ld * es) % 16 != 0) return false;
+  if (a.s.z && (a.s.ld_z * es) % 16 != 0) return false;
   if (!al(a.s.state) || !al(a.s.dt) || !al(a.s.Bm) || !al(a.s.Cm)) return false;
   if (a.s.z && !al(a.s.z)) return false;
   return fuse ? (al(a.x) && al(a.conv_state)) : al(a.s.u);
@@ -440,7 +445,7 @@ cudaError_t launch_nk(const StepArgs& a, cudaStream_t stream) {
   int state_vec = (reinterpret_cast<uintptr_t>(a.s.state) & 15) == 0;
   if (FUSE) state_vec = state_vec && (reinterpret_cast<uintptr_t>(a.conv_state) & 15) == 0;
   const int bc_vec = ((reinterpret_cast<uintptr_t>(a.s.Bm) | reinterpret_cast<uintptr_t>(a.s.Cm)) & 15) == 0 &&
-                     (N * es) % 16 == 0;
+                     (N * es) % 16 == 0 && (a.s.ld_B * es) % 16 == 0 && (a.s.ld_C * es) % 16 == 0;
   return launch_pdl(true, step_kernel<N, K, Tin, FUSE>, dim3((unsigned)blocks), dim3(threads), 0, stream, a, bt,
                     n_cblk, state_vec, bc_vec);
 }
@@ -488,18 +493,28 @@ cudaError_t launch_t(const StepArgs& a, const DeviceInfo& dev, int K, cudaStream
   return cudaErrorInvalidValue;
 }
 
+// zero strides mean dense rows
+SsmStepArgs with_strides(SsmStepArgs a) {
+  if (a.ld_ux == 0) a.ld_ux = a.Di;
+  if (a.ld_dt == 0) a.ld_dt = a.Di;
+  if (a.ld_z == 0) a.ld_z = a.Di;
+  if (a.ld_B == 0) a.ld_B = a.N;
+  if (a.ld_C == 0) a.ld_C = a.N;
+  return a;
+}
+
 }  // namespace
 
 cudaError_t launch_ssm_step_batched(const SsmStepArgs& a, const DeviceInfo& dev,
                                     cudaStream_t stream) {
-  StepArgs s{a, nullptr, nullptr, nullptr, nullptr};
+  StepArgs s{with_strides(a), nullptr, nullptr, nullptr, nullptr};
   return a.in_bf16 ? launch_t<__nv_bfloat16, false>(s, dev, 1, stream)
                    : launch_t<float, false>(s, dev, 1, stream);
 }
 
 cudaError_t launch_mixer_step_batched(const MixerStepArgs& m, const DeviceInfo& dev,
                                       cudaStream_t stream) {
-  StepArgs s{m.ssm, m.x, m.conv_state, m.conv_w, m.conv_b};
+  StepArgs s{with_strides(m.ssm), m.x, m.conv_state, m.conv_w, m.conv_b};
   return m.ssm.in_bf16 ? launch_t<__nv_bfloat16, true>(s, dev, m.K, stream)
                        : launch_t<float, true>(s, dev, m.K, stream);
 }

@@ -12,6 +12,10 @@ times, then times one more call with CUDA events and prints it.
   --what convstep  T=1 conv step on layer 1 of an [L][B][Di][4] state
   --what fused     fused conv1d + SiLU and selective-scan prefill  [B, T, Di]
   --what m3        Mamba-3 SISO step on layer 1: --B batch, --H heads, --P headdim, --N d_state
+  --what linear    projection GEMM: --M rows, --Nout outputs, --K inputs (--out f32|bf16, --residual)
+  --what rmsnorm   RMSNorm of --M rows of --dm (f32 in, bf16 out)
+  --what block     whole Mamba-1 block prefill: --B, --T, --dm, --Di, --N, --R (dt_rank), d_conv 4
+  --what blockstep whole-block T=1 step on layer 1 of --L layers: --B, --dm, --Di, --N, --R
   --route plain    prefills without a workspace (one warp per 32-channel tile)
 """
 import argparse
@@ -23,7 +27,15 @@ from . import _binding as m
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--what", default="scan", choices=("scan", "conv", "step", "mixer", "convstep", "fused", "m3"))
+    ap.add_argument("--what", default="scan", choices=("scan", "conv", "step", "mixer", "convstep", "fused", "m3", "linear",
+                                                           "rmsnorm", "block", "blockstep"))
+    ap.add_argument("--M", type=int, default=2048)
+    ap.add_argument("--Nout", type=int, default=3072)
+    ap.add_argument("--K", type=int, default=768)
+    ap.add_argument("--out", default="bf16", choices=("f32", "bf16"))
+    ap.add_argument("--residual", action="store_true")
+    ap.add_argument("--dm", type=int, default=768)
+    ap.add_argument("--R", type=int, default=48)
     ap.add_argument("--H", type=int, default=24)
     ap.add_argument("--P", type=int, default=64)
     ap.add_argument("--B", type=int, default=1)
@@ -45,7 +57,36 @@ def main(argv=None):
     dtb = torch.full((a.Di,), -4.0, device="cuda")
     w = torch.rand((a.Di, 4), generator=g, device="cuda") - 0.5
     m.load()
-    if a.what == "m3":
+    bf = torch.bfloat16
+    if a.what in ("block", "blockstep"):
+        wts = {"norm_w": torch.ones(a.dm, device="cuda"),
+               "in_proj_w": (torch.randn((2 * a.Di, a.dm), generator=g, device="cuda") * a.dm ** -0.5).to(bf),
+               "conv_w": w, "conv_b": torch.zeros(a.Di, device="cuda"),
+               "x_proj_w": (torch.randn((a.R + 2 * a.N, a.Di), generator=g, device="cuda") * a.Di ** -0.5).to(bf),
+               "dt_proj_w": (torch.randn((a.Di, a.R), generator=g, device="cuda") * a.R ** -0.5).to(bf),
+               "dt_bias": dtb, "A_log": A, "D": D,
+               "out_proj_w": (torch.randn((a.dm, a.Di), generator=g, device="cuda") * a.Di ** -0.5).to(bf)}
+    if a.what == "linear":
+        A_ = torch.randn((a.M, a.K), generator=g, device="cuda").to(bf)
+        W_ = (torch.randn((a.Nout, a.K), generator=g, device="cuda") * a.K ** -0.5).to(bf)
+        C_ = torch.zeros((a.M, a.Nout), device="cuda", dtype=bf if a.out == "bf16" else torch.float32)
+        f = lambda: m.mamba_linear_bf16(C_, A_, W_, C_ if a.residual else None)
+    elif a.what == "rmsnorm":
+        X_ = torch.randn((a.M, a.dm), generator=g, device="cuda")
+        O_ = torch.empty((a.M, a.dm), device="cuda", dtype=bf)
+        nw = torch.ones(a.dm, device="cuda")
+        f = lambda: m.mamba_rmsnorm(O_, X_, nw)
+    elif a.what == "block":
+        hid = torch.randn((a.B, a.T, a.dm), generator=g, device="cuda")
+        cs = torch.zeros((a.B, a.Di, 4), device="cuda")
+        ss = torch.zeros((a.B, a.Di, a.N), device="cuda")
+        f = lambda: m.mamba_layer_prefill(hid, wts, cs, cs, ss, ss)
+    elif a.what == "blockstep":
+        hid = torch.randn((a.B, a.dm), generator=g, device="cuda")
+        cs = torch.zeros((a.L, a.B, a.Di, 4), device="cuda")
+        ss = torch.zeros((a.L, a.B, a.Di, a.N), device="cuda")
+        f = lambda: m.mamba_layer_step(hid, wts, cs, ss, 1)
+    elif a.what == "m3":
         BH = (a.B, a.H)
         st = torch.randn((a.L, a.B, a.H, a.P, a.N), generator=g, device="cuda")
         ks = torch.randn((a.L, a.B, a.H, a.N), generator=g, device="cuda")
