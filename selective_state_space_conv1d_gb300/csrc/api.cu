@@ -626,7 +626,8 @@ int mamba_linear_bf16(void* c, int64_t ld_c, int c_dtype, const void* a, int64_t
   if ((rc = check_dtype("c_dtype", c_dtype))) return rc;
   if (M < 0 || N < 0 || K < 1) return fail(MAMBA_ERR_INVALID_ARG, "sizes must be M >= 0, N >= 0, K >= 1 (M=%lld N=%lld K=%lld)", (long long)M, (long long)N, (long long)K);
   if (M == 0 || N == 0) return ok();
-  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || !sizes_ok(M, K) || !sizes_ok(N, K) || !sizes_ok(M, N))
+  if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX || !sizes_ok(M, K) || !sizes_ok(N, K) || !sizes_ok(M, N) ||
+      ((M + 127) / 128) * ((N + 63) / 64) > INT32_MAX)  // output tiles are counted in 32 bits
     return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
   if (!c || !a || !w) return fail(MAMBA_ERR_INVALID_ARG, "c, a and w must not be NULL");
   if (ld_c < N || (residual && ld_r < N) || ld_a < K || ld_w < K)
