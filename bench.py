@@ -11,7 +11,9 @@ of the dominant call, the end-to-end figure (host buffers, copies inside the
 timed region), the f64 CPU oracle timed on the host cores for every workload,
 the SM clocks seen, and under "extra" the other workloads: the mamba-130m
 layer prefill (f32), the long-context continuation, the 24-layer batch-128
-decode, the Mamba-3 SISO decode and the prefill-versus-steps comparison.
+decode, the Mamba-3 SISO decode, the prefill-versus-steps comparison, and the
+whole Mamba-1 block (RMSNorm, projections on the tensor cores, mixer,
+residual): the mamba-2.8b block prefill and the 24-layer block decode.
 
 Launch: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 N > 1 runs under torch.distributed.run: every rank runs an independent replica
@@ -1191,6 +1193,44 @@ def oracle_decode_sample(synth, n_rows, n_layers, n_steps, nthreads):
     return dtm, full
 
 
+def oracle_block_samples(synth, nthreads):
+    """The f64 block oracle (oracle/layer.py: numpy matmuls, the C conv and
+    scan) on bounded samples of the two block workloads: the mamba-2.8b block
+    over 256 tokens of one sequence (every token costs the same, so tokens/s
+    carries over to batch 8 x 4096), and one whole-block decode step (24
+    layers, batch 128) on mamba-130m shapes."""
+    from oracle import layer as OL
+
+    out = {}
+    dm, Di, N, K, R = BLOCK_SHAPES["mamba2.8b"]
+    seed = synth.SEED_BASE + 3
+    p = {k: np.asarray(v, np.float64) for k, v in synth.layer_params(seed, dm, Di, N, K, R).items()}
+    x = synth.normal(seed, "hidden", (1024, dm), 1.0).astype(np.float64)
+    t0 = time.perf_counter()
+    OL.layer_prefill(x, p, 1, 1024)
+    sec = time.perf_counter() - t0
+    out["mamba2.8b-block-prefill"] = {
+        "value": round(1024 / sec, 1), "unit": "tokens/s", "cores": nthreads,
+        "sample": f"one sequence of 1024 tokens through the f64 block oracle, {sec:.2f} s; per-token work is the "
+                  f"workload's (batch 8 x 4096)"}
+    dm, Di, N, K, R = BLOCK_SHAPES["mamba130m"]
+    seed = synth.SEED_BASE + 2
+    L, Bsz = 24, 128
+    ps = [{k: np.asarray(v, np.float64) for k, v in synth.layer_params(seed, dm, Di, N, K, R, layer=l).items()}
+          for l in range(L)]
+    conv = np.ascontiguousarray(0.5 * np.random.default_rng(seed).standard_normal((L, Bsz, Di, K)))
+    ssm = np.ascontiguousarray(0.5 * np.random.default_rng(seed + 1).standard_normal((L, Bsz, Di, N)))
+    h = synth.normal(seed, "hidden", (Bsz, dm), 1.0).astype(np.float64)
+    t0 = time.perf_counter()
+    for l in range(L):
+        h, _ = OL.layer_step(h, ps[l], conv, ssm, l)
+    sec = time.perf_counter() - t0
+    out["mamba130m-block-decode-b128-l24"] = {
+        "value": round(1.0 / sec, 3), "unit": "steps/s", "cores": nthreads,
+        "sample": f"one whole-block decode step (24 layers, batch 128) through the f64 block oracle, {sec:.2f} s"}
+    return out
+
+
 def cpu_baseline(synth, headline_wl=3):
     """The f64 oracle as it stands, on all host cores, per workload: bounded
     samples of independent channels (or rows), each about 2-10 s, with the
@@ -1223,6 +1263,7 @@ def cpu_baseline(synth, headline_wl=3):
         "value": round(steps / sec, 3), "unit": "steps/s", "cores": nthreads,
         "sample": f"{reps} x 2 steps x 24 layers on batch 128 x 16 of 1536 channels, f64 conv step + SSM step; "
                   f"{sec:.1f} s; steps/s scaled to all 1536 channels"}
+    per.update(oracle_block_samples(synth, nthreads))
     wl = synth.WORKLOADS[headline_wl]
     s1, t1, _ = timed(lambda: oracle_prefill_sample(synth, headline_wl, 16, 1, wl.d_inner // 16), 1.5)
     head = per[wl.name]
@@ -1388,6 +1429,12 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(synth, HEADLINE_WL)
+
+    if cpu is not None:
+        for key, name in (("block_prefill_2p8b", "mamba2.8b-block-prefill"),
+                          ("block_decode_130m_b128_l24", "mamba130m-block-decode-b128-l24")):
+            if key in extra and name in cpu["per_workload"]:
+                extra[key]["cpu_baseline"] = dict(cpu["per_workload"][name], kind="oracle")
 
     if rank == 0:
         wl = res["wl"]
