@@ -9,7 +9,7 @@
 // dt_proj, F11 out_proj + residual; prefill.rs `prefill_body` runs the same
 // projections over all T rows.)
 //
-// Design (persistent: one CTA per SM, tiles of 128 x BN, BN 64 / 128 / 256):
+// Design (persistent: one CTA per SM, tiles of 128 x BN, BN 64 / 128 / 192 / 256):
 //  * TMA (cp.async.bulk.tensor.2d, 128-byte swizzle) brings 128 x 64 tiles of
 //    A and BN x 64 tiles of W into a shared-memory ring of 4-8 stages; an
 //    mbarrier per stage says "landed" (transaction bytes) and another
@@ -70,7 +70,10 @@ struct GemmSmem {
   static constexpr int kBar = kRing + kEpi;                 // barriers after the ring and the staging
   static constexpr int kBytes = kBar + 8 * (2 * kStages + 5) + 16;
   static constexpr int kAlloc = kBytes + 1024;              // room to align the base to 1024 bytes
-  static constexpr int kTmemCols = 2 * BN <= 32 ? 32 : 2 * BN <= 64 ? 64 : 2 * BN <= 128 ? 128 : 2 * BN <= 256 ? 256 : 512;
+  // accumulator a starts at column a * kAccCols: BN rounded up to a power of
+  // two, so each accumulator starts on a boundary of its own width
+  static constexpr int kAccCols = BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  static constexpr int kTmemCols = 2 * kAccCols;
   static_assert(kStages >= 2, "shared memory too small for two stages");
   static_assert(kAlloc <= kSmemLimit, "shared memory over the opt-in limit");
 };
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t d = tmem + (uint32_t)(a * BN);
+        const uint32_t d = tmem + (uint32_t)(a * L::kAccCols);
         bool ok = true;
         for (int kt = kb; kt < ke; ++kt, ++g) {
           const int s = g % S;
@@ -409,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int col0 = nb * BN;
       const int ncols = N - col0 < BN ? N - col0 : BN;  // columns of this tile inside N
       const bool rows_full = vec_ok && row0 + 32 <= M;
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * BN);
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * L::kAccCols);
       // two blocks in flight: the next block's tensor-memory load overlaps
       // this block's stores
       uint32_t va[32], vb[32];
@@ -595,6 +598,7 @@ cudaError_t launch_typed(const GemmArgs& g, int bn, const CUtensorMap& ma, const
                          cudaStream_t stream) {
   if (bn == 64) return launch_bn<64, C_BF16, SPLIT>(g, ma, mw, sms, splits, stream);
   if (bn == 128) return launch_bn<128, C_BF16, SPLIT>(g, ma, mw, sms, splits, stream);
+  if (bn == 192) return launch_bn<192, C_BF16, SPLIT>(g, ma, mw, sms, splits, stream);
   return launch_bn<256, C_BF16, SPLIT>(g, ma, mw, sms, splits, stream);
 }
 
@@ -608,7 +612,7 @@ cudaError_t launch_typed(const GemmArgs& g, int bn, const CUtensorMap& ma, const
 int gemm_tile_n(int64_t M, int64_t N, int sms) {
   int best = 256;
   int64_t best_cost = INT64_MAX;
-  for (int bn : {256, 128, 64}) {
+  for (int bn : {256, 192, 128, 64}) {
     if (bn > 64 && N <= bn / 2) continue;  // no wider than needed
     const int64_t tiles = ((M + kBM - 1) / kBM) * ((N + bn - 1) / bn);
     const int64_t cost = ((tiles + sms - 1) / sms) * (bn + 32);

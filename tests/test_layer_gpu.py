@@ -39,6 +39,7 @@ def _bf16_dev(a):
     (130, 200, 1000),
     (128, 768, 1536),      # decode out_proj: few tiles, K split over a cluster of 8
     (128, 80, 1536),       # decode x_proj
+    (300, 380, 256),       # 192-wide tiles, ragged second column block
     (2048, 4096, 256),     # 128 x 256 tiles, more tiles than SMs: both accumulators in turn
     (640, 2560, 2560),     # 2.8b out_proj-shaped K and N
 ])
