@@ -62,7 +62,11 @@ struct GemmSmem {
   static constexpr int kA = kBM * kBK * 2;  // bytes per stage
   static constexpr int kB = BN * kBK * 2;
   static constexpr int kStage = kA + kB;
-  static constexpr int kEpi = kEpiWarps * 32 * kStagePitch * 4;
+  // epilogue staging per warp: 32 rows of 32 f32 (padded), or two 4 KB bf16
+  // buffers for the tensor-memory-accelerator stores; 1024-byte aligned
+  static constexpr int kEpiF32 = kEpiWarps * 32 * kStagePitch * 4;
+  static constexpr int kEpiTma = kEpiWarps * 2 * 4096;
+  static constexpr int kEpi = kEpiF32 > kEpiTma ? kEpiF32 : kEpiTma;
   static constexpr int kFixed = kEpi + 256 + 1024;  // staging, barriers, base alignment
   static constexpr int kStages0 = (kSmemLimit - kFixed) / kStage;
   static constexpr int kStages = kStages0 > MAX_STAGES ? MAX_STAGES : kStages0;
@@ -113,6 +117,29 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b
       "}\n" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
+}
+
+// shared -> global tensor store of one box, in a bulk group
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(x),
+               "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most N of this thread's bulk groups still reading shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// generic-proxy shared-memory writes visible to the tensor memory accelerator
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(uint32_t lo, uint32_t hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<uint32_t*>(&v);
 }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -251,9 +278,9 @@ __device__ __forceinline__ void fail_gemm(volatile int* abort_flag) {
 // them -- a deterministic split with no global scratch and no second launch.
 template <int BN, bool C_BF16, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w, void* c,
-                     int64_t ld_c, const float* r, int64_t ld_r, int M, int N, int K, int vec_ok, int splits,
-                     int group_m) {
+    gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
+                     const __grid_constant__ CUtensorMap map_c, void* c, int64_t ld_c, const float* r, int64_t ld_r,
+                     int M, int N, int K, int vec_ok, int splits, int group_m, int c_tma) {
   // a split CTA runs a few K steps of one tile: a short ring and half the
   // shared memory, so two split CTAs fit on an SM
   using L = GemmSmem<BN, SPLIT ? 3 : 8>;
@@ -378,6 +405,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue warps: warp w reads accumulator lanes (tile rows) 32 (w % 4) ...
     const int quad = warp & 3;
     float* stage_f = reinterpret_cast<float*>(gbase + L::kRing) + (warp - 2) * 32 * kStagePitch;
+    const uint32_t tma_stage = base + L::kRing + (uint32_t)((warp - 2) * 8192);  // two 4 KB buffers
+    int tma_chunk = 0;
     int i = 0;
     for (int t = t_first; t < tiles; t += t_step, ++i) {
       const int a = i & 1;
@@ -413,6 +442,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ncols = N - col0 < BN ? N - col0 : BN;  // columns of this tile inside N
       const bool rows_full = vec_ok && row0 + 32 <= M;
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * L::kAccCols);
+      if constexpr (C_BF16) {
+        if (c_tma) {
+          // bf16 output through the tensor memory accelerator: 32 rows x 64
+          // columns per store, staged in one of this warp's two 4 KB buffers in
+          // the 128-byte swizzled layout of the box (16-byte granule j of row r
+          // at granule j ^ (r % 8): conflict-free writes); the unit clips rows
+          // and columns past M and N
+          // (a box wholly below M is not stored at all)
+#pragma unroll 1
+          for (int c0 = 0; c0 < (row0 < M ? ncols : 0); c0 += 2 * kChunk, ++tma_chunk) {
+            uint32_t va[32], vb[32];
+            tmem_ld32(taddr + (uint32_t)c0, va);
+            tmem_ld32(taddr + (uint32_t)(c0 + kChunk), vb);  // inside the accumulator even past N
+            tmem_wait(va);
+            tmem_wait(vb);
+            const uint32_t sb = tma_stage + (uint32_t)((tma_chunk & 1) * 4096);
+            if (lane == 0) bulk_wait_read<1>();  // the store two chunks back has read this buffer
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t* v = j < 4 ? va : vb;
+              const int q = (j & 3) * 8;
+              const uint32_t w0 = pack_bf16(v[q], v[q + 1]), w1 = pack_bf16(v[q + 2], v[q + 3]);
+              const uint32_t w2 = pack_bf16(v[q + 4], v[q + 5]), w3 = pack_bf16(v[q + 6], v[q + 7]);
+              const uint32_t dst = sb + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4));
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&map_c, col0 + c0, row0, sb);
+              bulk_commit();
+            }
+          }
+          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty(a));
+          continue;
+        }
+      }
       // two blocks in flight: the next block's tensor-memory load overlaps
       // this block's stores
       uint32_t va[32], vb[32];
@@ -437,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(acc_empty(a));
     }
+    if (lane == 0 && tma_chunk > 0) bulk_wait_all();  // the tensor stores have landed
   }
   __syncwarp();
   if constexpr (SPLIT) {
@@ -589,8 +660,13 @@ cudaError_t launch_bn(const GemmArgs& g, const CUtensorMap& ma, const CUtensorMa
   const int64_t m_tiles = (g.M + kBM - 1) / kBM;
   int64_t group_m = (int64_t)24e6 / ((int64_t)kBM * g.K * 2);
   group_m = group_m < 8 ? 8 : (group_m > m_tiles ? m_tiles : group_m);
-  return cudaLaunchKernelEx(&cfg, kern, ma, mw, g.c, g.ld_c, g.r, g.ld_r, (int)g.M, (int)g.N, (int)g.K, vec_ok,
-                            SPLIT ? splits : 1, (int)(group_m < 1 ? 1 : group_m));
+  // bf16 output without a residual goes out through tensor stores: C 16-byte
+  // aligned with 16-byte rows
+  CUtensorMap mc = ma;
+  const int c_tma = C_BF16 && !SPLIT && !g.r && (cp % 16) == 0 && (g.ld_c * 2) % 16 == 0 &&
+                    make_map(&mc, g.c, g.M, g.N, g.ld_c, 32);
+  return cudaLaunchKernelEx(&cfg, kern, ma, mw, mc, g.c, g.ld_c, g.r, g.ld_r, (int)g.M, (int)g.N, (int)g.K, vec_ok,
+                            SPLIT ? splits : 1, (int)(group_m < 1 ? 1 : group_m), c_tma);
 }
 
 template <bool C_BF16, bool SPLIT>
