@@ -108,6 +108,22 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// the same with an L2 eviction-priority hint (a createpolicy value)
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+      "%3}], [%4], %5;" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n"
@@ -345,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // producer: TMA into the ring, K steps of all this CTA's tiles in order
+      const uint64_t w_policy = l2_evict_last_policy();
       int g = 0;
       for (int t = t_first; t < tiles && !*abort_flag; t += t_step) {
         int mb, nb;
@@ -358,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = base + s * L::kStage, sb = sa + L::kA;
           mbar_arrive_expect_tx(full(s), L::kStage);
           tma_load_2d(sa, &map_a, kt * kBK, mb * kBM, full(s));
-          tma_load_2d(sb, &map_w, kt * kBK, nb * BN, full(s));
+          // the weight is re-read by every row-block group: keep it in L2
+          tma_load_2d_hint(sb, &map_w, kt * kBK, nb * BN, full(s), w_policy);
         }
       }
       // every copy issued lands before this thread moves on

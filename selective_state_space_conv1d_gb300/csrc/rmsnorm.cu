@@ -26,7 +26,10 @@ constexpr int kRowsPerCta = 8;
 template <bool OUT_BF16, bool VEC>
 __global__ void __launch_bounds__(32 * kRowsPerCta)
     rmsnorm_kernel(void* __restrict__ out, int64_t ld_out, const float* __restrict__ x, int64_t ld_x,
-                   const float* __restrict__ w, float eps, int64_t M, int D) {
+                   const float* __restrict__ w, float eps, int64_t M, int D, int early) {
+  // a grid that fits in one wave lets the next kernel start its set-up at
+  // once; a many-wave grid must not let it take SMs early
+  if (early) grid_dependents_launch();
   grid_dependency_wait();
   const int lane = threadIdx.x % 32;
   const int64_t row = (int64_t)blockIdx.x * kRowsPerCta + threadIdx.x / 32;
@@ -72,12 +75,11 @@ __global__ void __launch_bounds__(32 * kRowsPerCta)
       }
     }
   }
-  // after the work: a many-wave grid must not let the next kernel take SMs early
-  grid_dependents_launch();
+  if (!early) grid_dependents_launch();
 }
 
 template <bool OUT_BF16>
-cudaError_t launch_typed(const RmsNormArgs& a, cudaStream_t stream) {
+cudaError_t launch_typed(const RmsNormArgs& a, int sms, cudaStream_t stream) {
   const uintptr_t po = reinterpret_cast<uintptr_t>(a.out), px = reinterpret_cast<uintptr_t>(a.x),
                   pw = reinterpret_cast<uintptr_t>(a.w);
   // 4-column vectors: D, the strides and the bases must keep every row's
@@ -85,18 +87,23 @@ cudaError_t launch_typed(const RmsNormArgs& a, cudaStream_t stream) {
   const bool vec = a.D % 4 == 0 && a.ld_x % 4 == 0 && a.ld_out % 4 == 0 && px % 16 == 0 && pw % 16 == 0 &&
                    po % (OUT_BF16 ? 8 : 16) == 0;
   const dim3 grid((unsigned)((a.M + kRowsPerCta - 1) / kRowsPerCta)), block(32 * kRowsPerCta);
+  const int early = (int64_t)grid.x <= (int64_t)sms * 8;  // 8 CTAs of 256 threads per SM
   if (vec)
     return launch_pdl(true, rmsnorm_kernel<OUT_BF16, true>, grid, block, 0, stream, a.out, a.ld_out, a.x, a.ld_x,
-                      a.w, a.eps, a.M, (int)a.D);
+                      a.w, a.eps, a.M, (int)a.D, early);
   return launch_pdl(true, rmsnorm_kernel<OUT_BF16, false>, grid, block, 0, stream, a.out, a.ld_out, a.x, a.ld_x,
-                    a.w, a.eps, a.M, (int)a.D);
+                    a.w, a.eps, a.M, (int)a.D, early);
 }
 
 }  // namespace
 
 cudaError_t launch_rmsnorm(const RmsNormArgs& a, cudaStream_t stream) {
   if (a.M <= 0 || a.D <= 0) return cudaSuccess;
-  return a.out_bf16 ? launch_typed<true>(a, stream) : launch_typed<false>(a, stream);
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  return a.out_bf16 ? launch_typed<true>(a, sms, stream) : launch_typed<false>(a, sms, stream);
 }
 
 }  // namespace mamba
