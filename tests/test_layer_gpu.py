@@ -165,11 +165,16 @@ def _staged(m, wd, hidden, Bsz, T, c_in, c_out, s_in, s_out):
     return dict(h=h, xz=xz, u=u.view(rows, Di), x_dbl=xd, dt=dt, y=y.view(rows, Di))
 
 
-@pytest.mark.parametrize("name,Bsz,T", [("small", 2, 300), ("130m", 1, 256), ("n8_k3", 3, 70), ("small", 1, 1)])
-def test_block_prefill_stages_match_oracle(cuda_lib, name, Bsz, T):
-    m = cuda_lib
-    p, x, c0, s0 = _block(name, SEED + T, Bsz, T)
-    dm, Di, N, K, R = SHAPES[name]
+def _check_block(m, p, x, c0, s0, Bsz, T, end_to_end=True):
+    """Every stage against the oracle on its own GPU inputs; the block call
+    equal to its call sequence bit for bit; optionally end to end against the
+    storage-mirroring oracle."""
+    import oracle
+
+    Di, K = p["conv_w"].shape
+    N = p["A_log"].shape[1]
+    R = p["dt_proj_w"].shape[1]
+    dm = p["norm_w"].shape[0]
     wd = _dev_weights(p)
     hidden = to_dev(x).view(Bsz, T, dm)
     cs, ss = to_dev(c0), to_dev(s0)
@@ -181,8 +186,6 @@ def test_block_prefill_stages_match_oracle(cuda_lib, name, Bsz, T):
     # every stage against the oracle on the GPU's own (rounded) inputs
     assert_within(g["h"], OL.rmsnorm(x, p["norm_w"]), "h = RMSNorm(x)", bf16_out=True)
     assert_within(g["xz"], OL.linear(g["h"], p["in_proj_w"]), "xz = in_proj(h)", bf16_out=True)
-    import oracle
-
     u_ref, c_ref = oracle.conv1d_silu_prefill(g["xz"][:, :Di].reshape(Bsz, T, Di), p["conv_w"], p["conv_b"], c0)
     assert_within(g["u"], u_ref.reshape(-1, Di), "u = SiLU(conv(x))", bf16_out=True)
     assert np.array_equal(to_host(c_out), c_ref)
@@ -204,7 +207,8 @@ def test_block_prefill_stages_match_oracle(cuda_lib, name, Bsz, T):
     assert torch.equal(hidden2, hidden)
     assert torch.equal(c2, c_out) and torch.equal(s2, s_out)
     assert m.mamba_device_faults(clear=True) == 0
-
+    if not end_to_end:
+        return
     # end to end against the oracle that stores every activation in bf16 as
     # the GPU does: only rounding decisions taken on f32 vs f64 values differ,
     # each by one bf16 unit, so the block output stays within the bound of the
@@ -219,6 +223,53 @@ def test_block_prefill_stages_match_oracle(cuda_lib, name, Bsz, T):
     c_err = np.abs(to_host(c2) - c_e)
     assert np.all(c_err <= 2.0 ** -7 * np.abs(c_e) + 1e-30), np.max(c_err)
     assert np.mean(c_err > 0) < 1e-2
+
+
+@pytest.mark.parametrize("name,Bsz,T", [("small", 2, 300), ("130m", 1, 256), ("n8_k3", 3, 70), ("small", 1, 1)])
+def test_block_prefill_stages_match_oracle(cuda_lib, name, Bsz, T):
+    p, x, c0, s0 = _block(name, SEED + T, Bsz, T)
+    _check_block(cuda_lib, p, x, c0, s0, Bsz, T)
+
+
+@pytest.mark.parametrize("case", range(10))
+def test_block_random_shapes(cuda_lib, case):
+    """Seeded random block shapes: d_model, d_inner and dt_rank any multiples of
+    8, every supported d_state, d_conv 1..8, batch 1..4, T 1..400 (ragged GEMM
+    tiles and scan tiles, element and vector paths); stages against the
+    oracle, the block call against its call sequence, and the T = 1 block step
+    against the T = 1 block prefill, bit for bit."""
+    m = cuda_lib
+    r = np.random.default_rng(SEED + 900 + case)
+    dm = 8 * int(r.integers(1, 41))
+    Di = 8 * int(r.integers(1, 65))
+    N = int(r.choice([1, 2, 4, 8, 16, 32, 64]))
+    K = int(r.integers(1, 9))
+    R = 8 * int(r.integers(1, 7))
+    Bsz = int(r.integers(1, 5))
+    T = int(r.integers(1, 401))
+    seed = SEED + 1000 + case
+    p = synth.layer_params(seed, dm, Di, N, K, R, parity=True)
+    x = synth.normal(seed, "hidden", (Bsz * T, dm), 1.0)
+    c0 = synth.normal(seed, "conv_state", (Bsz, Di, K), 1.0)
+    s0 = synth.normal(seed, "ssm_state", (Bsz, Di, N), 0.5)
+    _check_block(m, p, x, c0, s0, Bsz, T, end_to_end=False)
+    # the step on slab 1 of 2 layers equals the T = 1 prefill
+    wd = _dev_weights(p)
+    x1 = to_dev(x[:Bsz])
+    cst = torch.stack([to_dev(c0), to_dev(c0) + 1.0]).contiguous()
+    sst = torch.stack([to_dev(s0), to_dev(s0) - 1.0]).contiguous()
+    h_step = x1.clone()
+    c_before = cst[0].clone()
+    s_before = sst[0].clone()
+    m.mamba_layer_step(h_step, wd, cst, sst, 1)
+    h_pre = x1.clone().view(Bsz, 1, dm)
+    c1, s1 = (to_dev(c0) + 1.0), (to_dev(s0) - 1.0)
+    m.mamba_layer_prefill(h_pre, wd, c1, c1, s1, s1)
+    torch.cuda.synchronize()
+    assert torch.equal(h_step, h_pre.view(Bsz, dm))
+    assert torch.equal(cst[1], c1) and torch.equal(sst[1], s1)
+    assert torch.equal(cst[0], c_before) and torch.equal(sst[0], s_before)
+    assert m.mamba_device_faults(clear=True) == 0
 
 
 def test_block_prefill_zero_state_defaults_and_in_place_states(cuda_lib):
