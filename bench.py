@@ -1066,7 +1066,7 @@ def run_block_decode(torch, m, synth, device, n_steps=32, L=24, Bsz=128):
     del g
     w_bytes = 2 * (2 * Di * dm + (R + 2 * N) * Di + Di * R + dm * Di)
     state_bytes = Bsz * Di * (N + K) * 4 * 2
-    return {
+    out = {
         "workload": "mamba130m-block-decode-b128-l24", "value": round(1e3 / ms, 2), "unit": "steps/s",
         "ms_per_step": round(ms, 5), "layer_token_updates_per_s": round(1e3 / ms * L * Bsz, 1),
         "config": {"n_layers": L, "batch": Bsz, "d_model": dm, "d_inner": Di, "d_state": N, "d_conv": K,
@@ -1076,6 +1076,11 @@ def run_block_decode(torch, m, synth, device, n_steps=32, L=24, Bsz=128):
         "hbm_gbs_weights_and_state": round(L * (w_bytes + state_bytes) / (ms * 1e-3) / 1e9, 1),
         "gpu_launches_per_step": L * 7,
     }
+    peak, peak_src = hbm_peak()
+    out["roofline"] = roofline(L * (w_bytes + state_bytes), ms, peak, peak_src, None)
+    out["roofline_kernel"] = ("whole 24-layer step (7 kernels per layer; each is latency-bound: the bytes are "
+                              "the layers' weights and the state read and written once)")
+    return out
 
 
 
