@@ -449,6 +449,23 @@ MAMBA_API int mamba_layer_step(float* hidden, const MambaLayer* layer, float* co
                                int64_t workspace_bytes, void* stream);
 
 /*
+ * One decode token through n_layers whole blocks, recorded once as a CUDA
+ * graph (inference.rs `capture_graph` / `step`: the full step chain F1-F12 of
+ * every layer captured after a warm-up and replayed per token): the graph
+ * holds mamba_layer_step(hidden, &layers[l], conv_state, ssm_state, l,
+ * n_layers, B, workspace, ...) for l = 0 .. n_layers-1, each validated as the
+ * direct call validates it; on an error nothing is created.  Every layer must
+ * have layer 0's dims.  Launch with mamba_decode_graph_launch (write the next
+ * token's f32 hidden state [B][d_model] into `hidden` before each launch; it
+ * holds the last block's output after it); mamba_decode_graph_kernels gives
+ * the graph's node count; mamba_decode_graph_destroy frees it.  The buffers
+ * and the weights stay the caller's and must outlive the graph.
+ */
+MAMBA_API int mamba_layer_decode_graph_create(MambaDecodeGraph** out, const MambaLayer* layers, int64_t n_layers,
+                                              float* hidden, float* conv_state, float* ssm_state, int64_t B,
+                                              void* workspace, int64_t workspace_bytes);
+
+/*
  * mamba_selective_scan_prefill_noalloc - the selective-scan prefill for callers
  * that cannot allocate device memory.  (No counterpart in the mamba-rs pages:
  * it is an addition of this library.)

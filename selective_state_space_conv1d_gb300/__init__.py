@@ -12,6 +12,7 @@ C-ABI entry points (include/mamba_ssm.h), each backed by hand-written CUDA kerne
   mamba_linear_bf16             a projection of the layer on the tensor cores (tcgen05)
   mamba_rmsnorm                 RMSNorm of the f32 residual stream
   mamba_layer_prefill / _step   the whole Mamba-1 block (norm, projections, mixer, residual)
+  mamba_layer_decode_graph_create  one decode token through n_layers blocks as one CUDA graph
   mamba_selective_scan_prefill_noalloc  the scan prefill with a static scratch
   mamba_selective_scan_workspace_bytes  scratch size of the prefill's balanced routes
 This package is the thin Python binding (argument marshalling over ctypes);
@@ -20,6 +21,7 @@ This package is the thin Python binding (argument marshalling over ctypes);
 from ._binding import (  # noqa: F401
     ABI_SYMBOLS,
     DecodeGraph,
+    LayerDecodeGraph,
     LIB_PATH,
     MAMBA_BF16,
     MAMBA_ERR_CUDA,

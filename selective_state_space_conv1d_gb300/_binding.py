@@ -43,6 +43,7 @@ ABI_SYMBOLS = (
     "mamba_layer_workspace_bytes",
     "mamba_layer_prefill",
     "mamba_layer_step",
+    "mamba_layer_decode_graph_create",
     "mamba_decode_graph_create",
     "mamba_decode_graph_launch",
     "mamba_decode_graph_kernels",
@@ -119,6 +120,8 @@ def load(path: str | None = None):
         lib.mamba_layer_prefill.restype = ctypes.c_int
         lib.mamba_layer_step.argtypes = [vp, lp, vp, vp, i64, i64, i64, vp, i64, vp]
         lib.mamba_layer_step.restype = ctypes.c_int
+        lib.mamba_layer_decode_graph_create.argtypes = [ctypes.POINTER(vp), lp, i64, vp, vp, vp, i64, vp, i64]
+        lib.mamba_layer_decode_graph_create.restype = ctypes.c_int
         lib.mamba_decode_graph_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i64, i32, i32, vp, vp,
                                                   i64, i64, i64, i64]
         lib.mamba_decode_graph_create.restype = ctypes.c_int
@@ -654,6 +657,81 @@ def mamba_mixer_step_batched(y, x, dt, Bm, Cm, conv_state, ssm_state, layer, con
         _ptr(y), _dtype_code(y), _ptr(x), _ptr(dt), _ptr(z), _ptr(Bm), _ptr(Cm), _dtype_code(x),
         _ptr(conv_w), _ptr(conv_b), _ptr(A_log), _ptr(D), _ptr(dt_bias), _ptr(conv_state),
         _ptr(ssm_state), int(layer), ssm_state.shape[0], Bsz, Di, K, N, _stream(stream, x)))
+
+
+class LayerDecodeGraph:
+    """One decode token through whole Mamba-1 blocks, recorded once as a CUDA
+    graph (mamba_layer_decode_graph_create): weights is a list of n_layers
+    block weight dicts (see layer_struct), hidden a contiguous f32 [B,
+    d_model] tensor updated in place by every launch (write the next token's
+    hidden state into it first), conv_state / ssm_state [n_layers, B, Di, K|N].
+    The tensors must outlive the graph; close() (or `with`) frees it."""
+
+    def __init__(self, weights, hidden, conv_state, ssm_state, *, eps=1e-5, workspace=None):
+        import torch
+
+        lib = load()
+        L = len(weights)
+        if L == 0:
+            raise ValueError("weights must hold at least one layer")
+        if hidden.dtype != torch.float32 or hidden.dim() != 2 or not hidden.is_contiguous():
+            raise ValueError("hidden must be a contiguous float32 [B, d_model] tensor")
+        Bsz, dm = hidden.shape
+        structs = (_MambaLayer * L)(*[layer_struct(w, eps) for w in weights])
+        S0 = structs[0]
+        if dm != S0.d_model:
+            raise ValueError(f"hidden has d_model {dm}, the weights {S0.d_model}")
+        for t, nm, last in ((conv_state, "conv_state", S0.d_conv), (ssm_state, "ssm_state", S0.d_state)):
+            if t.dim() != 4 or tuple(t.shape) != (L, Bsz, S0.d_inner, last):
+                raise ValueError(f"{nm} must be [{L}, B, Di, {last}]")
+            _f32_param(t, nm)
+        self._keep = (weights, hidden, conv_state, ssm_state, structs)
+        if workspace is None:
+            v = lib.mamba_layer_workspace_bytes(ctypes.byref(S0), Bsz, 1)
+            if v < 0:
+                raise MambaError(int(v), mamba_last_error())
+            workspace = torch.empty(max(int(v), 16), dtype=torch.uint8, device=hidden.device)
+        self._ws = workspace
+        h = ctypes.c_void_p()
+        _check(lib.mamba_layer_decode_graph_create(ctypes.byref(h), structs, L, _ptr(hidden), _ptr(conv_state),
+                                                   _ptr(ssm_state), Bsz, _ptr(workspace),
+                                                   workspace.numel() * workspace.element_size()))
+        self._h = h
+        self._device = hidden.device
+        self.n_layers = L
+
+    @property
+    def kernels(self) -> int:
+        v = load().mamba_decode_graph_kernels(self._h)
+        if v < 0:
+            raise MambaError(int(v), mamba_last_error())
+        return int(v)
+
+    def launch(self, stream=None):
+        if self._h is None:
+            raise ValueError("graph is closed")
+        import torch
+
+        s = torch.cuda.current_stream(self._device).cuda_stream if stream is None else (
+            stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        _check(load().mamba_decode_graph_launch(self._h, s))
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            _check(load().mamba_decode_graph_destroy(self._h))
+            self._h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class _LayerParams(ctypes.Structure):

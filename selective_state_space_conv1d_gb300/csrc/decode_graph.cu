@@ -8,6 +8,10 @@
 // recording validates every step with the same host checks and launches the
 // same kernels (with their programmatic-launch edges) as the direct calls.
 //
+// mamba_layer_decode_graph_create records the same way one token through whole
+// Mamba-1 blocks (the pages' full F1-F12 chain per layer): n_layers
+// mamba_layer_step calls; the graph handle is the same type.
+//
 // Capture runs on a private stream in relaxed mode: the first call of a kernel
 // instance configures it (shared-memory opt-in, occupancy query), which is not
 // a stream operation and must not be refused inside the capture.  Nothing runs
@@ -103,6 +107,78 @@ extern "C" int mamba_decode_graph_create(MambaDecodeGraph** out, const MambaMixe
   g->exec = exec;
   g->device = dev;
   g->kernels = kernels;
+  *out = g;
+  return mamba::set_last_error(MAMBA_OK, "");
+}
+
+// The whole-block form: one token through n_layers Mamba-1 blocks, each the
+// public mamba_layer_step call on slab l of the states, recorded once.
+extern "C" int mamba_layer_decode_graph_create(MambaDecodeGraph** out, const MambaLayer* layers, int64_t n_layers,
+                                               float* hidden, float* conv_state, float* ssm_state, int64_t B,
+                                               void* workspace, int64_t workspace_bytes) {
+  if (!out) return mamba::set_last_error(MAMBA_ERR_INVALID_ARG, "mamba_layer_decode_graph_create: out is NULL");
+  *out = nullptr;
+  if (!layers) return mamba::set_last_error(MAMBA_ERR_INVALID_ARG, "mamba_layer_decode_graph_create: layers is NULL");
+  if (n_layers < 1 || n_layers > (int64_t(1) << 16))
+    return mamba::set_last_error(MAMBA_ERR_INVALID_ARG, "mamba_layer_decode_graph_create: n_layers not in 1..2^16");
+  for (int64_t l = 1; l < n_layers; ++l) {
+    const MambaLayer& a = layers[0];
+    const MambaLayer& b = layers[l];
+    if (a.d_model != b.d_model || a.d_inner != b.d_inner || a.d_state != b.d_state || a.d_conv != b.d_conv ||
+        a.dt_rank != b.dt_rank)
+      return mamba::set_last_error(MAMBA_ERR_INVALID_ARG,
+                                   "mamba_layer_decode_graph_create: every layer must have the dims of layer 0 "
+                                   "(the states are one [n_layers][B][d_inner][.] slab array)");
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error("cudaGetDevice", e);
+  cudaStream_t s = nullptr;
+  if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess)
+    return cuda_error("cudaStreamCreateWithFlags", e);
+  if ((e = cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed)) != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return cuda_error("cudaStreamBeginCapture", e);
+  }
+  int rc = MAMBA_OK;
+  std::string msg;
+  for (int64_t l = 0; l < n_layers; ++l) {
+    rc = mamba_layer_step(hidden, &layers[l], conv_state, ssm_state, l, n_layers, B, workspace, workspace_bytes, s);
+    if (rc != MAMBA_OK) {
+      char head[80];
+      snprintf(head, sizeof(head), "mamba_layer_decode_graph_create: layer %lld: ", (long long)l);
+      msg = std::string(head) + mamba_last_error();
+      break;
+    }
+  }
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(s, &graph);  // ends the capture on every path
+  cudaStreamDestroy(s);
+  if (rc != MAMBA_OK || e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    if (rc != MAMBA_OK) return mamba::set_last_error(rc, msg.c_str());
+    return cuda_error("cudaStreamEndCapture", e);
+  }
+  size_t nodes = 0;
+  if ((e = cudaGraphGetNodes(graph, nullptr, &nodes)) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return cuda_error("cudaGraphGetNodes", e);
+  }
+  cudaGraphExec_t exec = nullptr;
+  if ((e = cudaGraphInstantiate(&exec, graph, 0)) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return cuda_error("cudaGraphInstantiate", e);
+  }
+  MambaDecodeGraph* g = new (std::nothrow) MambaDecodeGraph;
+  if (!g) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(graph);
+    return mamba::set_last_error(MAMBA_ERR_CUDA, "mamba_layer_decode_graph_create: out of host memory");
+  }
+  g->graph = graph;
+  g->exec = exec;
+  g->device = dev;
+  g->kernels = (int64_t)nodes;
   *out = g;
   return mamba::set_last_error(MAMBA_OK, "");
 }

@@ -367,3 +367,15 @@ def test_layer_wrappers_refuse_mismatched_tensors_before_any_call():
         m.mamba_layer_prefill(torch.zeros(2, 4, dm), w, conv_state_in=f(2, Di, K + 1))
     with pytest.raises(ValueError):
         m.mamba_layer_step(torch.zeros(2, dm), w, f(3, 2, Di, K), f(2, 2, Di, N), 0)
+
+
+def test_layer_decode_graph_rejects_bad_arguments_on_host(lib):
+    E = m.MAMBA_ERR_INVALID_ARG
+    h = ctypes.c_void_p()
+    two = (m._binding._MambaLayer * 2)(_layer(), _layer(dm=72))
+    assert lib.mamba_layer_decode_graph_create(ctypes.byref(h), two, 2, FAKE, FAKE, FAKE, 4, FAKE, 1 << 30) == E
+    assert "dims of layer 0" in m.mamba_last_error()
+    assert lib.mamba_layer_decode_graph_create(None, two, 2, FAKE, FAKE, FAKE, 4, FAKE, 1 << 30) == E
+    assert lib.mamba_layer_decode_graph_create(ctypes.byref(h), None, 2, FAKE, FAKE, FAKE, 4, FAKE, 1 << 30) == E
+    assert lib.mamba_layer_decode_graph_create(ctypes.byref(h), two, 0, FAKE, FAKE, FAKE, 4, FAKE, 1 << 30) == E
+    assert h.value is None

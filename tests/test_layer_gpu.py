@@ -446,3 +446,29 @@ def test_block_prefill_2p8b_full_size_sampled(cuda_lib):
                                                  col(st["xz"], Di), to_host(s0[b:b + 1, ch]))
     assert_within(col(st["y"]), y_ref, "y (one row, sampled channels)", bf16_out=True)
     assert_within(to_host(s_out[b:b + 1, ch]), s_ref, "ssm state (one row, sampled channels)")
+
+
+def test_layer_decode_graph_replays_the_block_steps_bitwise(cuda_lib):
+    """The whole-block decode graph (n_layers block steps recorded once) gives
+    the direct calls' bits, launch after launch, and records 7 kernels per layer."""
+    m = cuda_lib
+    L, Bsz, S = 3, 5, 3
+    dm, Di, N, K, R = SHAPES["130m"]
+    wds = [_dev_weights(synth.layer_params(SEED + 70 + l, dm, Di, N, K, R, parity=True)) for l in range(L)]
+    xs = [to_dev(synth.normal(SEED + 80 + s_, "hidden", (Bsz, dm), 1.0)) for s_ in range(S)]
+    c0 = to_dev(synth.normal(SEED + 90, "conv_state", (L, Bsz, Di, K), 1.0))
+    s0 = to_dev(synth.normal(SEED + 90, "ssm_state", (L, Bsz, Di, N), 0.5))
+    hg, cg, sg = torch.empty(Bsz, dm, device="cuda"), c0.clone(), s0.clone()
+    hd, cd, sd = torch.empty(Bsz, dm, device="cuda"), c0.clone(), s0.clone()
+    with m.LayerDecodeGraph(wds, hg, cg, sg) as g:
+        assert g.kernels == 7 * L
+        for s_ in range(S):
+            hg.copy_(xs[s_])
+            g.launch()
+            hd.copy_(xs[s_])
+            for l in range(L):
+                m.mamba_layer_step(hd, wds[l], cd, sd, l)
+            torch.cuda.synchronize()
+            assert torch.equal(hg, hd), f"step {s_}"
+            assert torch.equal(cg, cd) and torch.equal(sg, sd)
+    assert m.mamba_device_faults(clear=True) == 0
