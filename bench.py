@@ -969,6 +969,37 @@ def block_stage_calls(torch, m, wd, hidden, Bsz, T, conv_state, ssm_state):
     ]
 
 
+def run_block_prefill_small(torch, m, synth, device, steps=50, warmup=3):
+    """One mamba-130m-shaped block prefill (batch 1 x T 2048, d_model 768): the
+    narrow shape, where the scan takes its T split and the x_proj its K split;
+    tokens/s = 2048 / time per block."""
+    shape = BLOCK_SHAPES["mamba130m"]
+    dm, Di, N, K, R = shape
+    Bsz, T = 1, 2048
+    seed = synth.SEED_BASE + 1
+    wd = block_weights(torch, synth, seed, shape, device)
+    hidden = synth.torch_normal((Bsz, T, dm), 1.0, seed + 31, device)
+    conv = torch.zeros((Bsz, Di, K), device=device)
+    ssm = torch.zeros((Bsz, Di, N), device=device)
+    ws = torch.empty(m.mamba_layer_workspace_bytes(wd, Bsz, T), dtype=torch.uint8, device=device)
+
+    def block():
+        m.mamba_layer_prefill(hidden, wd, conv, conv, ssm, ssm, workspace=ws)
+
+    for _ in range(warmup):
+        block()
+    torch.cuda.synchronize()
+    ms = kernel_time(torch, [block], steps, reps=2)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    route = scan_route(m, Bsz, T, Di, N, sms)
+    return {"workload": "mamba130m-block-prefill", "value": round(Bsz * T / (ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_block": round(ms, 5),
+            "config": {"batch": Bsz, "seq_len": T, "d_model": dm, "d_inner": Di, "d_state": N, "d_conv": K,
+                       "dt_rank": R, "launch": f"CUDA graph of {steps} blocks", "weights": "random init",
+                       "l2": "the block's working set (~40 MB) fits the L2: an upper bound for a cold layer"},
+            "scan_route": ROUTE_DESC[route], "gpu_launches_per_block": 6 + (3 if route == "split" else 1)}
+
+
 def run_block_prefill(torch, m, synth, device, steps=20, warmup=3):
     """One whole mamba-2.8b-shaped Mamba-1 block (RMSNorm, in_proj, conv,
     x_proj, dt_proj, scan, out_proj + residual) over batch 8 x T 4096 through
@@ -1446,6 +1477,7 @@ def main():
         extra["block_prefill_2p8b"] = run_block_prefill(torch, m, synth, device)
         torch.cuda.empty_cache()
         extra["block_decode_130m_b128_l24"] = run_block_decode(torch, m, synth, device)
+        extra["block_prefill_130m"] = run_block_prefill_small(torch, m, synth, device)
 
     e2e = run_e2e(torch, m, res, min(args.steps, 100), device)
 

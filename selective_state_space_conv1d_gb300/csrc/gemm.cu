@@ -20,11 +20,16 @@
 //    stage when its MMAs are done, and marks the accumulator full at the end
 //    of a tile.
 //  * Four epilogue warps drain the other accumulator meanwhile (tcgen05.ld,
-//    32 lanes x 32 columns, warp w owning tile rows 32 (w % 4) ...), stage
-//    each 32 x 32 block in shared memory and store it with 16-byte coalesced
-//    accesses, adding the residual and rounding on the way.  A wide tile
-//    reads half the shared memory per MMA of a 128-wide one; the double
-//    accumulator hides the epilogue behind the next tile's MMAs.
+//    32 lanes x 32 columns, warp w owning tile rows 32 (w % 4) ...).  A bf16
+//    output is packed into 32 x 64 boxes in the 128-byte swizzled layout and
+//    leaves by tensor stores (cp.async.bulk.tensor, clipped at M and N); an
+//    f32 output stages 32 x 32 blocks and stores them with 16-byte coalesced
+//    accesses, adding the residual on the way.  A wide tile reads half the
+//    shared memory per MMA of a 128-wide one; the double accumulator hides
+//    the epilogue behind the next tile's MMAs.
+//  * Few output tiles and a long K (the decode projections): K is split over a
+//    thread-block cluster whose ranks reduce through distributed shared memory
+//    (see the kernel's comment).
 //  * Every mbarrier wait is bounded (about a second); one that runs out sets
 //    MAMBA_FAULT_GEMM_WAIT and an abort flag that ends every role's loop; the
 //    CTA still waits (bounded) for its copies and MMAs in flight and frees its
@@ -298,9 +303,10 @@ __device__ __forceinline__ void fail_gemm(volatile int* abort_flag) {
 //    tile into a kStages-deep ring (TMA; "full" / "empty" barriers per stage);
 //  * warp 1 (one lane) issues the MMAs of a tile into one of two
 //    tensor-memory accumulators and commits "accumulator full";
-//  * warps 2-5 drain the other accumulator meanwhile (tcgen05.ld, staged
-//    through shared memory for 16-byte coalesced stores, residual added and
-//    rounded on the way) and release it ("accumulator empty").
+//  * warps 2-5 drain the other accumulator meanwhile (tcgen05.ld; bf16 out
+//    through swizzled staging and tensor stores, f32 out with its residual
+//    through padded staging and 16-byte coalesced stores) and release it
+//    ("accumulator empty").
 //
 // SPLIT (few output tiles, long K): a cluster of `splits` CTAs shares one
 // tile, CTA rank q accumulating K steps [q k_tiles / splits, (q + 1) k_tiles /
@@ -313,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
                      const __grid_constant__ CUtensorMap map_c, void* c, int64_t ld_c, const float* r, int64_t ld_r,
                      int M, int N, int K, int vec_ok, int splits, int group_m, int c_tma) {
-  // a split CTA runs a few K steps of one tile: a short ring and half the
-  // shared memory, so two split CTAs fit on an SM
+  // a split CTA runs a few K steps of one tile: a short ring (two split CTAs
+  // of a 64- or 128-wide tile fit on an SM)
   using L = GemmSmem<BN, SPLIT ? 3 : 8>;
   constexpr int S = L::kStages;
   static_assert(!SPLIT || kBM * (BN + 4) * 4 <= L::kRing, "the partial sums must fit in the ring");
