@@ -17,6 +17,9 @@ times, then times one more call with CUDA events and prints it.
   --what block     whole Mamba-1 block prefill: --B, --T, --dm, --Di, --N, --R (dt_rank), d_conv 4
   --what blockstep whole-block T=1 step on layer 1 of --L layers: --B, --dm, --Di, --N, --R
   --route plain    prefills without a workspace (one warp per 32-channel tile)
+  --flush          write a 256 MB buffer before every call, so each call starts with a cold L2
+                   (for counters taken with ncu --cache-control none: the launches inside one call
+                   then see the cache state they see in a real run)
 """
 import argparse
 
@@ -45,6 +48,7 @@ def main(argv=None):
     ap.add_argument("--L", type=int, default=24)
     ap.add_argument("--dtype", default="f32", choices=("f32", "bf16"))
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--flush", action="store_true", help="cold L2 before every call")
     ap.add_argument("--route", default="auto", choices=("auto", "plain"),
                     help="prefills: the planned route, or one warp per tile with no workspace")
     a = ap.parse_args(argv)
@@ -126,6 +130,10 @@ def main(argv=None):
             f = lambda: m.mamba_mixer_step_batched(y, x, dt, Bm, Cm, cs, st, 1, w, A, None, D, dtb, z)
         else:
             f = lambda: m.mamba_conv1d_silu_step(y, x, st, 1, w, None)
+    if a.flush:
+        scratch = torch.empty(64 * 1024 * 1024, device="cuda")  # 256 MB, twice the L2
+        call = f
+        f = lambda: (scratch.zero_(), call())
     for _ in range(a.reps):
         f()
     torch.cuda.synchronize()
