@@ -1018,19 +1018,27 @@ def run_block_prefill(torch, m, synth, device, steps=20, warmup=3):
     def block():
         m.mamba_layer_prefill(hidden, wd, conv, conv, ssm, ssm, workspace=ws)
 
+    # the block's GEMMs run the GPU at its power cap: the clocks seen while the
+    # block and while its stages are timed go into the line
+    ck = ClockSampler(device.index if device.index is not None else 0)
+    ck.start()
     for _ in range(warmup):
         block()
     torch.cuda.synchronize()
     ms = kernel_time(torch, [block], steps, reps=1)
+    block_clocks = ck.stop()
     stages = block_stage_calls(torch, m, wd, hidden, Bsz, T, conv, ssm)
     stage_ms = {}
     tflops = {}
+    ck = ClockSampler(device.index if device.index is not None else 0)
+    ck.start()
     for name, fn, flops in stages:
         fn()
         torch.cuda.synchronize()
         stage_ms[name] = kernel_time(torch, [fn], 10 if flops else 5, reps=2)
         if flops:
             tflops[name] = round(flops / (stage_ms[name] * 1e-3) / 1e12, 1)
+    stage_clocks = ck.stop()
     burst, sustained, src = bf16_peak()
     in_flops = 2 * Bsz * T * 2 * Di * dm
     ach = in_flops / (stage_ms["in_proj"] * 1e-3) / 1e12
@@ -1058,6 +1066,7 @@ def run_block_prefill(torch, m, synth, device, steps=20, warmup=3):
         "roofline_kernel": "in_proj GEMM (tcgen05, 128 x 256 tiles)",
         "scan_route": ROUTE_DESC[route],
         "gpu_launches_per_block": 6 + (3 if route == "split" else 1),
+        "clocks": block_clocks, "stage_clocks": stage_clocks,
     }
 
 
