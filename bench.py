@@ -1000,7 +1000,7 @@ def run_block_prefill_small(torch, m, synth, device, steps=50, warmup=3):
             "scan_route": ROUTE_DESC[route], "gpu_launches_per_block": 6 + (3 if route == "split" else 1)}
 
 
-def run_block_prefill(torch, m, synth, device, steps=20, warmup=3):
+def run_block_prefill(torch, m, synth, device, steps=100, warmup=3):
     """One whole mamba-2.8b-shaped Mamba-1 block (RMSNorm, in_proj, conv,
     x_proj, dt_proj, scan, out_proj + residual) over batch 8 x T 4096 through
     mamba_layer_prefill, graph-replayed; tokens/s = 32768 / time per block.
