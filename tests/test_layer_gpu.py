@@ -77,6 +77,28 @@ def test_linear_strided_operands_and_output(cuda_lib):
     assert bool((cbuf[:, :16] == 5.5).all()) and bool((cbuf[:, 16 + N:] == 5.5).all())
 
 
+@pytest.mark.parametrize("out", ["bf16", "f32+residual"])
+def test_linear_misaligned_output_takes_the_element_path(cuda_lib, out):
+    """An output at an odd element offset with an odd row stride (no 16-byte
+    rows: neither tensor stores nor vector stores apply) gives the same values."""
+    m = cuda_lib
+    M, N, K, ld_c, off = 260, 136, 192, 151, 3
+    r = np.random.default_rng(SEED + 9)
+    a = synth.store(r.standard_normal((M, K)).astype(np.float32), "bf16")
+    w = synth.store((r.standard_normal((N, K)) * K ** -0.5).astype(np.float32), "bf16")
+    dt = torch.bfloat16 if out == "bf16" else torch.float32
+    cbuf = torch.full((M, ld_c), 9.0, device="cuda", dtype=dt)
+    c = cbuf[:, off:off + N]
+    res = None
+    if out != "bf16":
+        res = r.standard_normal((M, N)).astype(np.float32)
+        c.copy_(to_dev(res))
+    m.mamba_linear_bf16(c, _bf16_dev(a), _bf16_dev(w), c if res is not None else None)
+    torch.cuda.synchronize()
+    assert_within(to_host(c), OL.linear(a, w, res), f"misaligned {out}", bf16_out=out == "bf16")
+    assert bool((cbuf[:, :off] == 9.0).all()) and bool((cbuf[:, off + N:] == 9.0).all())
+
+
 def test_linear_is_row_independent_bitwise(cuda_lib):
     """A row's result does not depend on M or on the row's place in its tile:
     the K order of every output element is fixed."""
