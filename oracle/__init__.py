@@ -62,6 +62,8 @@ def _load():
             lib.oracle_ssm_step.argtypes = [dp, dp, L] + [dp] * 8 + [L, L, L, ctypes.c_int]
             lib.oracle_m3_step.argtypes = [dp, dp, dp, dp, L] + [dp] * 7 + [L, L, L, L]
             lib.oracle_ssm_step.restype = ctypes.c_int
+            lib.oracle_m3_prepare.argtypes = [dp] * 6 + [L] + [dp] * 6 + [L, L, L, L]
+            lib.oracle_m3_prepare.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -171,6 +173,35 @@ def ssm_step(u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt_bias=None, z=Non
     if rc != 0:
         raise ValueError("oracle_ssm_step rejected its arguments")
     return y
+
+
+def m3_prepare(k_in, q_in, dt, A, lam, angles, angle_state, layer):
+    """The Mamba-3 SISO step's inputs from one token's projections: the layer's
+    angle state advanced by dt * angles, k_in and q_in rotated in pairs by it,
+    and alpha / beta / gamma (the exponential-trapezoidal weights).
+
+    k_in, q_in: [B, H, N]; dt, A, lam: [B, H]; angles: [B, n_angles] (None or
+    n_angles = 0: no rotation); angle_state [L, B, H, n_angles] (f64,
+    C-contiguous, updated in place).  Returns (k, q, alpha, beta, gamma)."""
+    k_in, q_in, dt, A, lam = _f64(k_in), _f64(q_in), _f64(dt), _f64(A), _f64(lam)
+    Bsz, H, N = k_in.shape
+    assert q_in.shape == k_in.shape and dt.shape == (Bsz, H) and A.shape == (Bsz, H) and lam.shape == (Bsz, H)
+    na = 0 if angles is None else np.asarray(angles).shape[1]
+    if na:
+        angles = _f64(angles)
+        assert angles.shape == (Bsz, na)
+        assert angle_state.dtype == np.float64 and angle_state.flags.c_contiguous
+        assert angle_state.shape[1:] == (Bsz, H, na)
+    else:
+        angles, angle_state = None, None
+    k, q = np.empty_like(k_in), np.empty_like(q_in)
+    alpha, beta, gamma = np.empty((Bsz, H)), np.empty((Bsz, H)), np.empty((Bsz, H))
+    rc = _load().oracle_m3_prepare(_ptr(k), _ptr(q), _ptr(alpha), _ptr(beta), _ptr(gamma), _ptr(angle_state),
+                                   layer, _ptr(k_in), _ptr(q_in), _ptr(dt), _ptr(A), _ptr(lam), _ptr(angles),
+                                   Bsz, H, N, na)
+    if rc != 0:
+        raise ValueError("oracle_m3_prepare rejected its arguments")
+    return k, q, alpha, beta, gamma
 
 
 def m3_step(x, k, q, alpha, beta, gamma, ssm_state, k_state, v_state, layer, D=None):

@@ -286,3 +286,61 @@ int oracle_m3_step(double* y, double* ssm_state, double* k_state, double* v_stat
     }
     return 0;
 }
+
+/*
+ * Mamba-3 SISO step inputs from one token's projections (docs.rs source view
+ * of mamba-rs 0.2.1 src/mamba3_siso/gpu/inference.rs, `step_layer_kernels`:
+ * step F4c "Angle accumulation + RoPE" -- the `m3_angle_dt_fwd_batch` launch
+ * (angle_cumsum out, the layer's angle_state in/out, angles_raw
+ * [batch][n_angles], dt [batch][nh]) and the `rope_fwd` launch (B and C
+ * rotated in pairs by angle_cumsum into the step's k and q) -- and step F5
+ * `m3_compute_abg` (alpha, beta, gamma from dt, a_val and trap); the page
+ * header cites the Mamba-3 paper for the method).  The page prints the
+ * launches, not the kernel bodies.  Read plainly, with the paper's
+ * exponential-trapezoidal rule and its data-dependent rotation:
+ *   theta[b][h][i] += dt[b][h] * angles[b][i]                  (i < n_angles)
+ *   (k[2i], k[2i+1]) = R(theta[b][h][i]) (k_in[2i], k_in[2i+1]),
+ *       R(t) = [[cos t, -sin t], [sin t, cos t]]; q likewise from q_in;
+ *       the components from 2 n_angles on are copied
+ *   alpha = exp(dt A), beta = (1 - lam) dt alpha, gamma = lam dt
+ * (beta weighs the previous token's input, decayed over the step; gamma the
+ * current one).  Layouts: k_in, q_in, k, q [B][H][N]; dt, A, lam, alpha,
+ * beta, gamma [B][H]; angles [B][n_angles]; angle_state the base of
+ * [n_layers][B][H][n_angles] (NULL allowed when n_angles == 0).
+ */
+int oracle_m3_prepare(double* k, double* q, double* alpha, double* beta, double* gamma,
+                      double* angle_state, long layer, const double* k_in, const double* q_in,
+                      const double* dt, const double* A, const double* lam,
+                      const double* angles, long B, long H, long N, long n_angles)
+{
+    if (layer < 0 || B < 0 || H < 0 || N < 0 || n_angles < 0 || 2 * n_angles > N)
+        return -1;
+    if (n_angles > 0 && (!angle_state || !angles))
+        return -1;
+    double* th = n_angles > 0 ? angle_state + layer * B * H * n_angles : NULL;
+    for (long b = 0; b < B; ++b) {
+        for (long hd = 0; hd < H; ++hd) {
+            const long bh = b * H + hd;
+            const double d = dt[bh];
+            for (long n = 0; n < N; ++n) {
+                k[bh * N + n] = k_in[bh * N + n];
+                q[bh * N + n] = q_in[bh * N + n];
+            }
+            for (long i = 0; i < n_angles; ++i) {
+                th[bh * n_angles + i] += d * angles[b * n_angles + i];
+                const double t = th[bh * n_angles + i];
+                const double c = cos(t), s = sin(t);
+                const long e = bh * N + 2 * i, o = e + 1;
+                k[e] = c * k_in[e] - s * k_in[o];
+                k[o] = s * k_in[e] + c * k_in[o];
+                q[e] = c * q_in[e] - s * q_in[o];
+                q[o] = s * q_in[e] + c * q_in[o];
+            }
+            const double a = exp(d * A[bh]);
+            alpha[bh] = a;
+            beta[bh] = (1.0 - lam[bh]) * d * a;
+            gamma[bh] = lam[bh] * d;
+        }
+    }
+    return 0;
+}

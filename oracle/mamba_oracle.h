@@ -51,6 +51,15 @@ int oracle_m3_step(double* y, double* ssm_state, double* k_state, double* v_stat
                    const double* beta, const double* gamma, const double* D, long B, long H,
                    long P, long N);
 
+/* Mamba-3 SISO step inputs (angle accumulation, rotation of k and q in pairs,
+ * alpha / beta / gamma) on the `layer` slab of the angle state (in place):
+ * k_in, q_in, k, q [B][H][N]; dt, A, lam, alpha, beta, gamma [B][H]; angles
+ * [B][n_angles]; angle state [n_layers][B][H][n_angles]; 2 n_angles <= N. */
+int oracle_m3_prepare(double* k, double* q, double* alpha, double* beta, double* gamma,
+                      double* angle_state, long layer, const double* k_in, const double* q_in,
+                      const double* dt, const double* A, const double* lam,
+                      const double* angles, long B, long H, long N, long n_angles);
+
 #ifdef __cplusplus
 }
 #endif

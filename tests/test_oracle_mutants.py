@@ -51,6 +51,23 @@ MUTANTS = [
     ("m3 alpha per head", "const double a = alpha[bh],", "const double a = alpha[hd],"),
     ("m3 k state slab ignores batch", "double* ks = k_state + layer * B * H * N;",
      "double* ks = k_state + layer * H * N;"),
+    # Mamba-3 step inputs (angle state, rotation, trapezoid weights)
+    ("m3 rotation by the old angle", "const double t = th[bh * n_angles + i];",
+     "const double t = th[bh * n_angles + i] - d * angles[b * n_angles + i];"),
+    ("m3 rotation sin sign", "k[e] = c * k_in[e] - s * k_in[o];", "k[e] = c * k_in[e] + s * k_in[o];"),
+    ("m3 rotation pairs in halves", "const long e = bh * N + 2 * i, o = e + 1;",
+     "const long e = bh * N + i, o = e + N / 2;"),
+    ("m3 q not rotated", "q[e] = c * q_in[e] - s * q_in[o];\n                q[o] = s * q_in[e] + c * q_in[o];",
+     "q[e] = q_in[e];\n                q[o] = q_in[o];"),
+    ("m3 angle increment without dt", "th[bh * n_angles + i] += d * angles[b * n_angles + i];",
+     "th[bh * n_angles + i] += angles[b * n_angles + i];"),
+    ("m3 angles of batch row 0", "+= d * angles[b * n_angles + i];", "+= d * angles[i];"),
+    ("m3 angle state slab ignores batch", "angle_state + layer * B * H * n_angles",
+     "angle_state + layer * H * n_angles"),
+    ("m3 beta without alpha", "beta[bh] = (1.0 - lam[bh]) * d * a;", "beta[bh] = (1.0 - lam[bh]) * d;"),
+    ("m3 gamma decayed", "gamma[bh] = lam[bh] * d;", "gamma[bh] = lam[bh] * d * a;"),
+    ("m3 trapezoid weights swapped", "gamma[bh] = lam[bh] * d;", "gamma[bh] = (1.0 - lam[bh]) * d;"),
+    ("m3 alpha without dt", "const double a = exp(d * A[bh]);", "const double a = exp(A[bh]);"),
 ]
 
 

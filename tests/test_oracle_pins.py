@@ -424,3 +424,134 @@ def test_m3_batch_and_head_independence():
     yB = oracle.m3_step(perm(x), perm(k), perm(q), perm(a), perm(be), perm(g), sB, kB, vB, 0, D[ph])
     np.testing.assert_array_equal(yB, perm(y))
     np.testing.assert_array_equal(sB[0], perm(sA[0]))
+
+
+# ------------------------------------------------------- Mamba-3 step inputs ----
+# Pins of oracle.m3_prepare (mamba-rs 0.2.1 mamba3_siso/gpu/inference.rs: step
+# F4c, the angle accumulation into the layer's angle state and the rotation of
+# B and C in pairs, and step F5, alpha / beta / gamma of the
+# exponential-trapezoidal rule).
+
+def _m3p_inputs(rng, B=2, H=3, N=8):
+    k_in, q_in = rng.normal(size=(B, H, N)), rng.normal(size=(B, H, N))
+    dt = rng.uniform(0.01, 0.2, size=(B, H))
+    A = -rng.uniform(0.2, 3.0, size=(B, H))
+    lam = rng.uniform(0.0, 1.0, size=(B, H))
+    return k_in, q_in, dt, A, lam
+
+
+def test_m3_prepare_quarter_and_half_turns_move_each_pair_and_copy_the_rest():
+    """From a zero angle state, dt * angle = pi/2 turns each pair (x, y) into
+    (-y, x) and pi turns it into (-x, -y); the components past the rotated
+    pairs are copied.  Batch row 0 takes the quarter turn, row 1 the half."""
+    rng = np.random.default_rng(41)
+    B, H, N, na = 2, 3, 8, 3
+    k_in, q_in, _, A, lam = _m3p_inputs(rng, B, H, N)
+    dt = np.full((B, H), 0.5)
+    angles = np.empty((B, na))
+    angles[0], angles[1] = np.pi, 2 * np.pi
+    st = np.zeros((1, B, H, na))
+    k, q, *_ = oracle.m3_prepare(k_in, q_in, dt, A, lam, angles, st, 0)
+    for src, out in ((k_in, k), (q_in, q)):
+        exp_ = src.copy()
+        e, o = src[..., 0:2 * na:2], src[..., 1:2 * na:2]
+        exp_[0, :, 0:2 * na:2], exp_[0, :, 1:2 * na:2] = -o[0], e[0]
+        exp_[1, :, 0:2 * na:2], exp_[1, :, 1:2 * na:2] = -e[1], -o[1]
+        np.testing.assert_allclose(out, exp_, rtol=0, atol=1e-14)
+        assert np.array_equal(out[..., 2 * na:], src[..., 2 * na:])
+    np.testing.assert_allclose(st[0, 0], np.pi / 2, rtol=1e-15)
+    np.testing.assert_allclose(st[0, 1], np.pi, rtol=1e-15)
+
+
+def test_m3_prepare_angle_state_continues_over_tokens():
+    """Two tokens' increments add up in the angle state, and the rotation is a
+    function of the accumulated angle: the second token's k equals k_in turned
+    once by the total, from a zero state."""
+    rng = np.random.default_rng(42)
+    B, H, N, na = 2, 3, 8, 4
+    k_in, q_in, dt1, A, lam = _m3p_inputs(rng, B, H, N)
+    dt2 = rng.uniform(0.01, 0.2, size=(B, H))
+    a1, a2 = rng.normal(size=(B, na)), rng.normal(size=(B, na))
+    th0 = rng.normal(size=(1, B, H, na))
+    st = th0.copy()
+    oracle.m3_prepare(k_in, q_in, dt1, A, lam, a1, st, 0)
+    k2, q2, *_ = oracle.m3_prepare(k_in, q_in, dt2, A, lam, a2, st, 0)
+    # one token carrying both increments (the state is per (b, h), the angles per b)
+    total = th0[0] + dt1[..., None] * a1[:, None, :] + dt2[..., None] * a2[:, None, :]
+    np.testing.assert_allclose(st[0], total, rtol=1e-14, atol=1e-14)
+    for b in range(B):
+        for h in range(H):
+            z = np.zeros((1, 1, 1, na))
+            kk, qq, *_ = oracle.m3_prepare(k_in[b:b + 1, h:h + 1], q_in[b:b + 1, h:h + 1], np.ones((1, 1)),
+                                           A[b:b + 1, h:h + 1], lam[b:b + 1, h:h + 1], total[b:b + 1, h], z, 0)
+            np.testing.assert_allclose(k2[b, h], kk[0, 0], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(q2[b, h], qq[0, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_m3_prepare_rotation_keeps_pair_norms_and_the_q_k_product():
+    """A rotation keeps each pair's length, and turning k and q by the same
+    angles keeps q . k (only relative angles reach the read-out)."""
+    rng = np.random.default_rng(43)
+    B, H, N, na = 3, 2, 16, 8
+    k_in, q_in, dt, A, lam = _m3p_inputs(rng, B, H, N)
+    st = rng.normal(scale=50.0, size=(2, B, H, na))
+    k, q, *_ = oracle.m3_prepare(k_in, q_in, dt, A, lam, rng.normal(size=(B, na)), st, 1)
+    pn = lambda v: np.hypot(v[..., 0::2], v[..., 1::2])
+    np.testing.assert_allclose(pn(k), pn(k_in), rtol=1e-13)
+    np.testing.assert_allclose(pn(q), pn(q_in), rtol=1e-13)
+    np.testing.assert_allclose(np.einsum("bhn,bhn->bh", q, k), np.einsum("bhn,bhn->bh", q_in, k_in),
+                               rtol=1e-12, atol=1e-12)
+    assert not np.allclose(k, k_in)
+
+
+def test_m3_prepare_weights_are_the_trapezoid_rule_of_the_decay():
+    """Over one step the input weight is the integral of exp(A s) for s in
+    [0, dt], (exp(A dt) - 1) / A.  lam = 1/2 takes the trapezoid rule: beta +
+    gamma is within its error bound dt^3 A^2 / 12.  lam = 1 is the right
+    end-point rule (only the current input, undecayed: beta = 0, gamma = dt),
+    lam = 0 the left one (only the previous input, decayed over the step:
+    gamma = 0, beta = dt alpha).  alpha is the decay exp(A dt): a semigroup in
+    dt (alpha(d1) alpha(d2) = alpha(d1 + d2)) with alpha(0) = 1 and slope A at 0."""
+    rng = np.random.default_rng(44)
+    B, H, N = 2, 5, 4
+    k_in, q_in, dt, A, _ = _m3p_inputs(rng, B, H, N)
+    prep = lambda d, l: oracle.m3_prepare(k_in, q_in, d, A, np.full((B, H), l), None, None, 0)[2:]
+    al, be, ga = prep(dt, 0.5)
+    integral = np.expm1(A * dt) / A
+    assert np.all(np.abs(be + ga - integral) <= dt ** 3 * A ** 2 / 12 * (1 + 1e-9))
+    assert np.all(np.abs(be + ga - integral) > 0)
+    al1, be1, ga1 = prep(dt, 1.0)
+    assert np.array_equal(be1, np.zeros((B, H))) and np.array_equal(ga1, dt)
+    al0, be0, ga0 = prep(dt, 0.0)
+    assert np.array_equal(ga0, np.zeros((B, H)))
+    np.testing.assert_allclose(be0, dt * al0, rtol=1e-15)
+    # alpha: the decay semigroup with generator A
+    d2 = rng.uniform(0.01, 0.2, size=(B, H))
+    np.testing.assert_allclose(prep(dt, 0.5)[0] * prep(d2, 0.5)[0], prep(dt + d2, 0.5)[0], rtol=1e-14)
+    assert np.array_equal(prep(np.zeros((B, H)), 0.5)[0], np.ones((B, H)))
+    eps = 1e-7
+    np.testing.assert_allclose((prep(np.full((B, H), eps), 0.5)[0] - 1) / eps, A, rtol=1e-6)
+
+
+def test_m3_prepare_without_angles_copies_and_keeps_other_slabs():
+    """n_angles = 0 leaves k and q as they come; with angles, only the named
+    layer's slab of the angle state moves, and each (b, h) only sees its own
+    dt, its batch row's angles and its own slot."""
+    rng = np.random.default_rng(45)
+    B, H, N, na = 3, 4, 8, 2
+    k_in, q_in, dt, A, lam = _m3p_inputs(rng, B, H, N)
+    k, q, *_ = oracle.m3_prepare(k_in, q_in, dt, A, lam, None, None, 0)
+    assert np.array_equal(k, k_in) and np.array_equal(q, q_in)
+    st = rng.normal(size=(3, B, H, na))
+    st0 = st.copy()
+    angles = rng.normal(size=(B, na))
+    k, q, al, be, ga = oracle.m3_prepare(k_in, q_in, dt, A, lam, angles, st, 1)
+    assert np.array_equal(st[0], st0[0]) and np.array_equal(st[2], st0[2])
+    assert not np.allclose(st[1], st0[1])
+    pb, ph = np.array([2, 0, 1]), np.array([3, 1, 0, 2])
+    perm = lambda t: np.ascontiguousarray(t[pb][:, ph])
+    stP = np.ascontiguousarray(st0[:, pb][:, :, ph])
+    kP, qP, alP, beP, gaP = oracle.m3_prepare(perm(k_in), perm(q_in), perm(dt), perm(A), perm(lam),
+                                              np.ascontiguousarray(angles[pb]), stP, 1)
+    for u, v in ((kP, k), (qP, q), (alP, al), (beP, be), (gaP, ga), (stP[1], st[1])):
+        np.testing.assert_array_equal(u, perm(v))
