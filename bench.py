@@ -1190,6 +1190,54 @@ def run_m3_decode(torch, m, device, peak, peak_src, n_steps=16, L=24, Bsz=128, H
         "gpu_launches_per_step": L,
     }
     out["roofline"] = roofline(per_launch, kms, peak, peak_src, ncu_traffic("m3_step", out["workload"]))
+    del x, k, q, al, be, ga
+
+    # The same decode with each token's step inputs prepared on the GPU first
+    # (the fourth state, the angles, advanced by dt * angles; B and C rotated in
+    # pairs into k and q; alpha / beta / gamma): two launches per layer.
+    na = N // 2
+    th = (torch.rand((L, Bsz, H, na), generator=g, device=device) - 0.5) * 100.0
+    k_in, q_in = rn(n_steps, L, Bsz, H, N), rn(n_steps, L, Bsz, H, N)
+    x = rn(n_steps, L, Bsz, H, P)
+    u01 = lambda *shape: torch.rand(shape, generator=g, device=device)
+    dt = torch.exp(math.log(1e-3) + u01(n_steps, L, Bsz, H) * math.log(100.0))
+    A = -(0.05 + 3.95 * u01(n_steps, L, Bsz, H))
+    lam = u01(n_steps, L, Bsz, H)
+    ang = (u01(n_steps, L, Bsz, na) * 2.0 - 1.0) * math.pi
+    kc, qc = torch.empty((L, Bsz, H, N), device=device), torch.empty((L, Bsz, H, N), device=device)
+    alc, bec, gac = (torch.empty((L, Bsz, H), device=device) for _ in range(3))
+
+    def prep(s_, l):
+        m.mamba3_siso_step_prepare(kc[l], qc[l], alc[l], bec[l], gac[l], k_in[s_, l], q_in[s_, l], dt[s_, l],
+                                   A[s_, l], lam[s_, l], ang[s_, l], th, l)
+
+    def prep_step(s_, l):
+        prep(s_, l)
+        m.mamba3_siso_step_batched(y[l], x[s_, l], kc[l], qc[l], alc[l], bec[l], gac[l], st, ks, vs, l, D[l])
+
+    for s_ in range(3):
+        for l in range(L):
+            prep_step(s_, l)
+    torch.cuda.synchronize()
+    gr = capture(torch, lambda: [prep_step(s_, l) for s_ in range(n_steps) for l in range(L)])
+    gr.replay()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        gr.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms2 = a.elapsed_time(b) / (reps * n_steps)
+    del gr
+    pms = kernel_time(torch, [lambda s_=s_, l=l: prep(s_, l) for s_ in range(4) for l in range(L)], 4 * L)
+    out["with_prepare"] = {
+        "value": round(1e3 / ms2, 2), "unit": "steps/s", "ms_per_step": round(ms2, 5),
+        "n_angles": na, "gpu_launches_per_step": 2 * L,
+        "prepare_us_per_launch": round(pms * 1e3, 3),
+        "prepare_bytes_per_launch": int(BH * N * 4 * 4 + BH * na * 8 + BH * 6 * 4 + Bsz * na * 4),
+        "note": "each layer: mamba3_siso_step_prepare (angle state, rotated k and q, alpha/beta/gamma) then "
+                "mamba3_siso_step_batched",
+    }
     return out
 
 

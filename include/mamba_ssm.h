@@ -283,6 +283,42 @@ MAMBA_API int mamba3_siso_step_batched(void* y, int y_dtype, const void* x, cons
                                        int64_t P, int64_t N, void* stream);
 
 /*
+ * mamba3_siso_step_prepare - the inputs of one Mamba-3 SISO step from the
+ * token's projections, and the fourth persistent state advanced by one token.
+ * (mamba-rs 0.2.1 mamba3_siso/gpu/inference.rs: `Mamba3GpuInferenceState`
+ * keeps an angle state [n_layers][batch*nh*n_angles]; step F4c launches
+ * `m3_angle_dt_fwd_batch` (angle_cumsum out, angle_state in/out, angles_raw
+ * [batch][n_angles], dt [batch][nh]) and `rope_fwd` (B and C rotated in pairs
+ * by angle_cumsum into the step's k and q), and step F5 `m3_compute_abg`
+ * (alpha, beta, gamma from dt, a_val and trap).  The page prints the launches,
+ * not the kernel bodies; read plainly, with the exponential-trapezoidal rule
+ * of the Mamba-3 paper the page cites, per (batch b, head h):
+ *   theta[i] += dt angles[b][i]                        (i < n_angles)
+ *   (k[2i], k[2i+1]) = R(theta[i]) (k_in[2i], k_in[2i+1]), q likewise,
+ *       R(t) = [[cos t, -sin t], [sin t, cos t]]; components 2 n_angles.. copied
+ *   alpha = exp(dt A), beta = (1 - lam) dt alpha, gamma = lam dt
+ * One launch does F4c and F5; its k, q, alpha, beta and gamma are the inputs
+ * of mamba3_siso_step_batched.)
+ *
+ *   k, q         [B][H][N] dense, dtype kq_dtype (out)
+ *   alpha, beta, gamma [B][H] f32 (out)
+ *   k_in, q_in   [B][H][N] f32 (B and C after the norm and the bias)
+ *   dt, A, lam   [B][H] f32 (step size after softplus, the decay rate A < 0 as
+ *                the split produces it, the trapezoid weight in [0, 1])
+ *   angles       [B][n_angles] f32 (the token's raw angles; NULL when n_angles = 0)
+ *   angle_state  base of [n_layers][B][H][n_angles] f32, slab `layer` updated in
+ *                place (NULL when n_angles = 0; layer and n_layers are then
+ *                not used)
+ * N (d_state) even; 2 n_angles <= N.  The outputs may not overlap each other or
+ * the inputs.  Errors: as for mamba_ssm_step_batched.
+ */
+MAMBA_API int mamba3_siso_step_prepare(void* k, void* q, int kq_dtype, float* alpha, float* beta, float* gamma,
+                                       const float* k_in, const float* q_in, const float* dt, const float* A,
+                                       const float* lam, const float* angles, float* angle_state, int64_t layer,
+                                       int64_t n_layers, int64_t B, int64_t H, int64_t N, int64_t n_angles,
+                                       void* stream);
+
+/*
  * Graph-captured decode driver.  (inference.rs `capture_graph` / `step`: after
  * a warm-up step the engine records its whole T=1 step chain into a CUDA graph
  * once and replays it every token, cutting the launch overhead from ~50 us to

@@ -9,6 +9,7 @@ C-ABI entry points (include/mamba_ssm.h), each backed by hand-written CUDA kerne
   mamba_mixer_prefill           conv1d + SiLU and the selective scan in one pass
   mamba_decode_graph_*          n_steps x n_layers fused steps recorded as one CUDA graph
   mamba3_siso_step_batched      T=1 step of the Mamba-3 SISO (trapezoidal) recurrence
+  mamba3_siso_step_prepare      its inputs: angle state advanced, k and q rotated, alpha/beta/gamma
   mamba_linear_bf16             a projection of the layer on the tensor cores (tcgen05)
   mamba_rmsnorm                 RMSNorm of the f32 residual stream
   mamba_layer_prefill / _step   the whole Mamba-1 block (norm, projections, mixer, residual)
@@ -37,6 +38,7 @@ from ._binding import (  # noqa: F401
     MambaError,
     load,
     mamba3_siso_step_batched,
+    mamba3_siso_step_prepare,
     mamba_conv1d_silu_prefill,
     mamba_conv1d_silu_step,
     mamba_device_faults,

@@ -38,6 +38,7 @@ ABI_SYMBOLS = (
     "mamba_mixer_step_batched",
     "mamba_mixer_prefill",
     "mamba3_siso_step_batched",
+    "mamba3_siso_step_prepare",
     "mamba_linear_bf16",
     "mamba_rmsnorm",
     "mamba_layer_workspace_bytes",
@@ -109,6 +110,8 @@ def load(path: str | None = None):
         lib.mamba_mixer_prefill.restype = ctypes.c_int
         lib.mamba3_siso_step_batched.argtypes = [vp, i32, vp, vp, vp, i32] + [vp] * 7 + [i64] * 6 + [vp]
         lib.mamba3_siso_step_batched.restype = ctypes.c_int
+        lib.mamba3_siso_step_prepare.argtypes = [vp, vp, i32] + [vp] * 10 + [i64] * 6 + [vp]
+        lib.mamba3_siso_step_prepare.restype = ctypes.c_int
         lib.mamba_linear_bf16.argtypes = [vp, i64, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]
         lib.mamba_linear_bf16.restype = ctypes.c_int
         lib.mamba_rmsnorm.argtypes = [vp, i64, i32, vp, i64, vp, ctypes.c_float, i64, i64, vp]
@@ -439,6 +442,38 @@ def mamba3_siso_step_batched(y, x, k, q, alpha, beta, gamma, ssm_state, k_state,
     _check(load().mamba3_siso_step_batched(
         _ptr(y), _dtype_code(y), _ptr(x), _ptr(k), _ptr(q), _dtype_code(x), _ptr(alpha), _ptr(beta), _ptr(gamma),
         _ptr(D), _ptr(ssm_state), _ptr(k_state), _ptr(v_state), int(layer), L, Bsz, H, P, N, _stream(stream, x)))
+
+
+def mamba3_siso_step_prepare(k, q, alpha, beta, gamma, k_in, q_in, dt, A, lam, angles, angle_state, layer, *,
+                             stream=None):
+    """The Mamba-3 SISO step's inputs from one token's projections: slab
+    `layer` of angle_state [L, B, H, n_angles] advanced by dt * angles, k_in and
+    q_in rotated in pairs by it into k and q, and alpha / beta / gamma.
+
+    k, q: contiguous [B, H, N] (f32 or bf16, one dtype); alpha, beta, gamma,
+    dt, A, lam: f32 [B, H]; k_in, q_in: f32 [B, H, N]; angles: f32 [B,
+    n_angles], or None (with angle_state None) for no rotation."""
+    Bsz, H, N = k_in.shape
+    for t, nm in ((k_in, "k_in"), (q_in, "q_in")):
+        _f32_param(t, nm, (Bsz, H, N))
+    for t, nm in ((alpha, "alpha"), (beta, "beta"), (gamma, "gamma"), (dt, "dt"), (A, "A"), (lam, "lam")):
+        _f32_param(t, nm, (Bsz, H))
+    for t, nm in ((k, "k"), (q, "q")):
+        if tuple(t.shape) != (Bsz, H, N) or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous {(Bsz, H, N)} tensor")
+    if q.dtype != k.dtype:
+        raise ValueError("q must have the dtype of k")
+    if (angles is None) != (angle_state is None):
+        raise ValueError("angles and angle_state go together")
+    na, L = 0, 1
+    if angles is not None:
+        na = angles.shape[1] if angles.dim() == 2 else -1
+        _f32_param(angles, "angles", (Bsz, na))
+        L = angle_state.shape[0]
+        _f32_param(angle_state, "angle_state", (L, Bsz, H, na))
+    _check(load().mamba3_siso_step_prepare(
+        _ptr(k), _ptr(q), _dtype_code(k), _ptr(alpha), _ptr(beta), _ptr(gamma), _ptr(k_in), _ptr(q_in), _ptr(dt),
+        _ptr(A), _ptr(lam), _ptr(angles), _ptr(angle_state), int(layer), L, Bsz, H, N, na, _stream(stream, k_in)))
 
 
 def mamba_ssm_step_batched(y, u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt_bias=None,

@@ -620,6 +620,54 @@ int mamba3_siso_step_batched(void* y, int y_dtype, const void* x, const void* k,
   return ok();
 }
 
+int mamba3_siso_step_prepare(void* k, void* q, int kq_dtype, float* alpha, float* beta, float* gamma,
+                             const float* k_in, const float* q_in, const float* dt, const float* A, const float* lam,
+                             const float* angles, float* angle_state, int64_t layer, int64_t n_layers, int64_t B,
+                             int64_t H, int64_t N, int64_t n_angles, void* stream) {
+  int rc;
+  if ((rc = check_dtype("kq_dtype", kq_dtype))) return rc;
+  if (B < 0 || H < 0 || N < 0 || n_angles < 0)
+    return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld H=%lld N=%lld n_angles=%lld)", (long long)B,
+                (long long)H, (long long)N, (long long)n_angles);
+  if (N % 2 || N > INT32_MAX) return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld must be even", (long long)N);
+  if (2 * n_angles > N)
+    return fail(MAMBA_ERR_INVALID_ARG, "n_angles=%lld rotates more than the d_state=%lld components",
+                (long long)n_angles, (long long)N);
+  // layer selects the slab of the angle state, the only per-layer buffer here
+  if (n_angles > 0 && (n_layers < 1 || layer < 0 || layer >= n_layers))
+    return fail(MAMBA_ERR_INVALID_ARG, "layer=%lld outside [0, n_layers=%lld)", (long long)layer, (long long)n_layers);
+  if (B == 0 || H == 0 || N == 0) return ok();
+  if (!sizes_ok(B, H, N) || (n_angles > 0 && !sizes_ok(n_layers, B * H, n_angles)))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!k || !q || !alpha || !beta || !gamma || !k_in || !q_in || !dt || !A || !lam)
+    return fail(MAMBA_ERR_INVALID_ARG, "k, q, alpha, beta, gamma, k_in, q_in, dt, A and lam must not be NULL");
+  if (n_angles > 0 && (!angles || !angle_state))
+    return fail(MAMBA_ERR_INVALID_ARG, "angles and angle_state must not be NULL when n_angles > 0");
+  const int64_t BH = B * H;
+  int64_t bkq = 0, bkin = 0, bs = 0, ban = 0, bth = 0;
+  if (!span_bytes(1, BH * N, BH * N, es_of(kq_dtype), &bkq) || !span_bytes(1, BH * N, BH * N, 4, &bkin) ||
+      !span_bytes(1, BH, BH, 4, &bs) || !span_bytes(1, B * n_angles, B * n_angles, 4, &ban) ||
+      !span_bytes(1, BH * n_angles, BH * n_angles, 4, &bth))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  float* th = n_angles > 0 ? angle_state + layer * BH * n_angles : nullptr;
+  const float* an = n_angles > 0 ? angles : nullptr;
+  Range ins[] = {range_of("k_in", k_in, bkin), range_of("q_in", q_in, bkin), range_of("dt", dt, bs),
+                 range_of("A", A, bs), range_of("lam", lam, bs), range_of("angles", an, ban)};
+  Range outs[] = {range_of("k", k, bkq), range_of("q", q, bkq), range_of("alpha", alpha, bs),
+                  range_of("beta", beta, bs), range_of("gamma", gamma, bs), range_of("angle_state", th, bth)};
+  if ((rc = check_pointers(ins, 6, dev_id)) || (rc = check_pointers(outs, 6, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 6, ins, 6))) return rc;
+  mamba::M3PrepArgs a{k, q, kq_dtype == MAMBA_BF16, alpha, beta, gamma, k_in, q_in, dt, A, lam, an, th, B, H,
+                      (int)N, (int)n_angles};
+  cudaError_t e = mamba::launch_m3_prepare(a, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("mamba3_siso_step_prepare launch", e);
+  return ok();
+}
+
 int mamba_linear_bf16(void* c, int64_t ld_c, int c_dtype, const void* a, int64_t ld_a, const void* w, int64_t ld_w,
                       const float* residual, int64_t ld_r, int64_t M, int64_t N, int64_t K, void* stream) {
   int rc;

@@ -193,6 +193,27 @@ struct M3StepArgs {
 // hd * ds / 8 must not exceed this
 int m3_max_items();
 cudaError_t launch_m3_step_batched(const M3StepArgs& a, const DeviceInfo& dev, cudaStream_t stream);
+
+// The Mamba-3 step's inputs: angle state advanced, k and q rotated in pairs,
+// alpha / beta / gamma (m3_step.cu).
+struct M3PrepArgs {
+  void* k;              // [B][H][N] out, kq_bf16 ? bf16 : f32
+  void* q;              // [B][H][N] out
+  int kq_bf16;
+  float* alpha;         // [B][H] out
+  float* beta;
+  float* gamma;
+  const float* k_in;    // [B][H][N] (B after norm and bias)
+  const float* q_in;    // [B][H][N] (C after norm and bias)
+  const float* dt;      // [B][H]
+  const float* A;       // [B][H]
+  const float* lam;     // [B][H]
+  const float* angles;  // [B][na]
+  float* theta;         // this layer's angle state [B][H][na] (null when na == 0)
+  int64_t B, H;
+  int N, na;
+};
+cudaError_t launch_m3_prepare(const M3PrepArgs& a, cudaStream_t stream);
 // watchdog bits of the Mamba-3 ring kernel (the device must be synchronised)
 int read_m3_faults(bool clear);
 

@@ -39,6 +39,8 @@ _TENSOR_IDS = {
     "m3_ssm_state": 37, "m3_k_state": 38, "m3_v_state": 39,
     # the rest of the Mamba-1 block
     "norm_w": 40, "in_proj_w": 41, "x_proj_w": 42, "dt_proj_w": 43, "out_proj_w": 44, "hidden": 45,
+    # inputs of the Mamba-3 step's preparation (angle state, rotation, trapezoid weights)
+    "m3p_k": 50, "m3p_q": 51, "m3p_dt": 52, "m3p_A": 53, "m3p_lam": 54, "m3p_angles": 55, "m3_angle_state": 56,
 }
 
 
@@ -235,6 +237,33 @@ def m3_states(seed: int, n_layers: int, batch: int, nheads: int, headdim: int, d
     return (normal(seed, "m3_ssm_state", (n_layers, batch, nheads, headdim, d_state), std),
             normal(seed, "m3_k_state", (n_layers, batch, nheads, d_state), 1.0),
             normal(seed, "m3_v_state", (n_layers, batch, nheads, headdim), 1.0))
+
+
+def m3_prepare_inputs(seed: int, layer: int, step: int, batch: int, nheads: int, d_state: int,
+                      n_angles: int) -> dict:
+    """Per-(layer, step) inputs of the preparation of one Mamba-3 SISO step, all
+    f32: k_in, q_in [B, H, N] N(0, 1) (B and C after norm and bias); dt [B, H]
+    log-uniform in [1e-3, 0.1] (a softplus output); A [B, H] = -U(0.05, 4) (the
+    decay rate); lam [B, H] U(0, 1) (the trapezoid weight, a sigmoid output);
+    angles [B, n_angles] U(-pi, pi) (the token's raw angles)."""
+    bh = (batch, nheads)
+    dt = np.exp(generator(seed, "m3p_dt", layer, step).uniform(math.log(1e-3), math.log(0.1), size=bh))
+    return {
+        "k_in": normal(seed, "m3p_k", (batch, nheads, d_state), 1.0, "f32", layer, step),
+        "q_in": normal(seed, "m3p_q", (batch, nheads, d_state), 1.0, "f32", layer, step),
+        "dt": dt.astype(np.float32),
+        "A": (-generator(seed, "m3p_A", layer, step).uniform(0.05, 4.0, size=bh)).astype(np.float32),
+        "lam": generator(seed, "m3p_lam", layer, step).uniform(0.0, 1.0, size=bh).astype(np.float32),
+        "angles": generator(seed, "m3p_angles", layer, step).uniform(-math.pi, math.pi,
+                                                                     size=(batch, n_angles)).astype(np.float32),
+    }
+
+
+def m3_angle_state(seed: int, n_layers: int, batch: int, nheads: int, n_angles: int, span: float = 50.0):
+    """f32 angle state [L, B, H, n_angles], U(-span, span): the angles a stretch
+    of earlier tokens has accumulated."""
+    g = generator(seed, "m3_angle_state")
+    return g.uniform(-span, span, size=(n_layers, batch, nheads, n_angles)).astype(np.float32)
 
 
 def torch_normal(shape, std, seed, device, dtype=None):

@@ -195,6 +195,38 @@ def test_m3_step_rejects_bad_arguments_on_host(lib):
     assert lib.mamba3_siso_step_batched(*args(P=-1)) == m.MAMBA_ERR_INVALID_ARG
 
 
+def test_m3_prepare_rejects_bad_arguments_on_host(lib):
+    def call(N=64, na=32, layer=0, L=1, dtype=0, angles=FAKE, state=FAKE, k_in=FAKE, B=2):
+        return lib.mamba3_siso_step_prepare(FAKE, FAKE, dtype, FAKE, FAKE, FAKE, k_in, FAKE, FAKE, FAKE, FAKE,
+                                            angles, state, layer, L, B, 3, N, na, None)
+    assert call(N=15, na=4) == m.MAMBA_ERR_UNSUPPORTED          # odd d_state
+    assert call(N=16, na=9) == m.MAMBA_ERR_INVALID_ARG          # more angles than pairs
+    assert call(na=-1) == m.MAMBA_ERR_INVALID_ARG
+    assert call(layer=1, L=1) == m.MAMBA_ERR_INVALID_ARG
+    assert call(layer=1, L=1, na=0, angles=None, state=None, B=0) == m.MAMBA_OK  # no angle state: layer unused
+    assert call(dtype=7) == m.MAMBA_ERR_INVALID_ARG
+    assert call(angles=None) == m.MAMBA_ERR_INVALID_ARG         # angles needed when n_angles > 0
+    assert "angles" in m.mamba_last_error()
+    assert call(state=None) == m.MAMBA_ERR_INVALID_ARG
+    assert call(k_in=None) == m.MAMBA_ERR_INVALID_ARG
+    assert call(B=0, k_in=None) == m.MAMBA_OK                   # empty batch: nothing to do
+
+
+def test_m3_prepare_wrapper_refuses_mismatched_tensors_before_any_call():
+    import torch
+    B, H, N, na = 2, 3, 8, 2
+    f = lambda *s: torch.zeros(*s)
+    good = dict(k=f(B, H, N), q=f(B, H, N), alpha=f(B, H), beta=f(B, H), gamma=f(B, H), k_in=f(B, H, N),
+                q_in=f(B, H, N), dt=f(B, H), A=f(B, H), lam=f(B, H), angles=f(B, na), angle_state=f(1, B, H, na),
+                layer=0)
+    bad = [dict(q=f(B, H, N).to(torch.bfloat16)), dict(k_in=f(B, H, N + 2)), dict(dt=f(B, H + 1)),
+           dict(angles=None), dict(angle_state=f(1, B, H, na + 1)), dict(k=f(B, H, N // 2)),
+           dict(lam=f(B, H).double())]
+    for b in bad:
+        with pytest.raises(ValueError):
+            m.mamba3_siso_step_prepare(**{**good, **b})
+
+
 C_PROGRAM = r"""
 #include <stdio.h>
 #include <string.h>

@@ -919,3 +919,109 @@ def test_m3_ring_and_direct_paths_agree_bitwise(cuda_lib, P, N, dtype):
         assert torch.equal(ya, yb), f"y differs at step {step}"
         assert torch.equal(sa, sb) and torch.equal(ka, kb) and torch.equal(va, vb)
     assert m.mamba_device_faults(clear=True) == 0
+
+
+# ---------------------------------------------- Mamba-3 step preparation ----
+
+def _m3p_call(m, inp, na, th, layer, kq_dtype=torch.float32, k=None):
+    Bsz, H, N = inp["k_in"].shape
+    d = {n: to_dev(v) for n, v in inp.items()}
+    k = torch.empty((Bsz, H, N), device="cuda", dtype=kq_dtype) if k is None else k
+    q = torch.empty((Bsz, H, N), device="cuda", dtype=kq_dtype)
+    al, be, ga = (torch.empty((Bsz, H), device="cuda") for _ in range(3))
+    m.mamba3_siso_step_prepare(k, q, al, be, ga, d["k_in"], d["q_in"], d["dt"], d["A"], d["lam"],
+                               d["angles"] if na else None, th if na else None, layer)
+    return k, q, al, be, ga
+
+
+@pytest.mark.parametrize("Bsz,H,N,na,kq", [
+    (3, 5, 64, 32, "f32"), (2, 3, 128, 16, "bf16"), (4, 2, 16, 0, "f32"), (1, 7, 32, 1, "f32"),
+    (2, 4, 64, 32, "bf16"), (5, 3, 2, 1, "f32"),
+])
+def test_m3_prepare_matches_oracle(cuda_lib, Bsz, H, N, na, kq):
+    """Three tokens of the step's preparation on the middle layer of a 3-layer
+    angle state: k, q, alpha, beta, gamma and the angle state against the
+    oracle; the other layers untouched, nothing written past k."""
+    m = cuda_lib
+    L, layer = 3, 1
+    th_h = synth.m3_angle_state(SEED, L, Bsz, H, max(na, 1))
+    th = to_dev(th_h)
+    th_ref = th_h.astype(np.float64)
+    kqd = torch.bfloat16 if kq == "bf16" else torch.float32
+    for step in range(3):
+        inp = synth.m3_prepare_inputs(SEED, layer, step, Bsz, H, N, na)
+        kg = Guarded((Bsz, H, N), kq)
+        k, q, al, be, ga = _m3p_call(m, inp, na, th, layer, kqd, kg.view)
+        torch.cuda.synchronize()
+        kg.check()
+        rk, rq, ral, rbe, rga = oracle.m3_prepare(inp["k_in"], inp["q_in"], inp["dt"], inp["A"], inp["lam"],
+                                                  inp["angles"] if na else None, th_ref if na else None, layer)
+        assert_within(to_host(k), rk, f"m3 prepare k step {step}", bf16_out=kq == "bf16")
+        assert_within(to_host(q), rq, f"m3 prepare q step {step}", bf16_out=kq == "bf16")
+        for g, r, nm in ((al, ral, "alpha"), (be, rbe, "beta"), (ga, rga, "gamma")):
+            assert_within(to_host(g), r, f"m3 prepare {nm} step {step}")
+        if na:
+            assert_within(to_host(th[layer]), th_ref[layer], f"m3 angle state step {step}")
+    for l in (0, 2):
+        assert np.array_equal(to_host(th[l]), th_h[l])
+    if not na:
+        assert np.array_equal(to_host(th), th_h)
+
+
+def test_m3_prepare_rotates_by_the_stored_angle_at_any_size(cuda_lib):
+    """Angles of order 1e4 (a long stream of tokens): the stored f32 angle is
+    the oracle's sum rounded once, and k and q are turned by exactly that
+    stored angle (the rotation reduces any argument accurately)."""
+    m = cuda_lib
+    Bsz, H, N, na = 4, 6, 64, 32
+    th_h = synth.m3_angle_state(SEED + 3, 1, Bsz, H, na, span=2e4)
+    th = to_dev(th_h)
+    inp = synth.m3_prepare_inputs(SEED + 3, 0, 0, Bsz, H, N, na)
+    k, q, *_ = _m3p_call(m, inp, na, th, 0)
+    torch.cuda.synchronize()
+    th_sum = th_h.astype(np.float64).copy()
+    oracle.m3_prepare(inp["k_in"], inp["q_in"], inp["dt"], inp["A"], inp["lam"], inp["angles"], th_sum, 0)
+    got = to_host(th)
+    assert np.all(np.abs(got - th_sum) <= np.spacing(np.abs(th_sum).astype(np.float32)).astype(np.float64))
+    # the rotation by the stored angle: the oracle from the stored state with no increment
+    stored = got.copy()
+    rk, rq, *_ = oracle.m3_prepare(inp["k_in"], inp["q_in"], np.zeros((Bsz, H)), inp["A"], inp["lam"],
+                                   inp["angles"], stored, 0)
+    assert_within(to_host(k), rk, "m3 prepare k at large angles")
+    assert_within(to_host(q), rq, "m3 prepare q at large angles")
+
+
+@pytest.mark.parametrize("P,N,na,dtype", [(64, 64, 32, "f32"), (32, 128, 8, "bf16"), (48, 16, 8, "f32")])
+def test_m3_prepare_then_step_decodes_like_the_oracle(cuda_lib, P, N, na, dtype):
+    """Six tokens of the Mamba-3 SISO decode on layer 1 of 2, each token the
+    preparation (angle state, rotated k and q, alpha / beta / gamma) and then
+    the step, against the same chain of oracle calls: y and all four states."""
+    m = cuda_lib
+    L, layer, Bsz, H = 2, 1, 3, 4
+    st_h, ks_h, vs_h = synth.m3_states(SEED + 5, L, Bsz, H, P, N)
+    th_h = synth.m3_angle_state(SEED + 5, L, Bsz, H, na)
+    st, ks, vs, th = to_dev(st_h), to_dev(ks_h), to_dev(vs_h), to_dev(th_h)
+    ref = [a.astype(np.float64).copy() for a in (st_h, ks_h, vs_h, th_h)]
+    D_h = synth.normal(SEED + 5, "m3_D", (H,), 1.0)
+    D = to_dev(D_h)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    for step in range(6):
+        inp = synth.m3_prepare_inputs(SEED + 5, layer, step, Bsz, H, N, na)
+        x_h = synth.normal(SEED + 5, "m3_x", (Bsz, H, P), 1.0, dtype, layer, step)
+        k, q, al, be, ga = _m3p_call(m, inp, na, th, layer, tdt)
+        y = torch.empty((Bsz, H, P), device="cuda")
+        m.mamba3_siso_step_batched(y, to_dev(x_h, dtype), k, q, al, be, ga, st, ks, vs, layer, D)
+        torch.cuda.synchronize()
+        rk, rq, ral, rbe, rga = oracle.m3_prepare(inp["k_in"], inp["q_in"], inp["dt"], inp["A"], inp["lam"],
+                                                  inp["angles"], ref[3], layer)
+        if dtype == "bf16":  # the step reads k and q as stored; the oracle takes the same values
+            rk, rq = to_host(k), to_host(q)
+        y_ref = oracle.m3_step(x_h, rk, rq, ral, rbe, rga, ref[0], ref[1], ref[2], layer, D_h)
+        assert_within(to_host(y), y_ref, f"m3 decode y token {step}")
+        assert_within(to_host(st[layer]), ref[0][layer], f"m3 decode ssm state token {step}")
+        assert_within(to_host(ks[layer]), ref[1][layer], f"m3 decode k state token {step}")
+        assert_within(to_host(th[layer]), ref[3][layer], f"m3 decode angle state token {step}")
+        assert np.array_equal(to_host(vs[layer]), ref[2][layer])
+    for s_dev, s_h in ((st, st_h), (ks, ks_h), (vs, vs_h), (th, th_h)):
+        assert np.array_equal(to_host(s_dev[0]), s_h[0])
+    assert m.mamba_device_faults(clear=True) == 0

@@ -136,3 +136,42 @@ def test_random_m3_shape_matches_oracle(cuda_lib, i):
         for l in range(L - 1):
             assert np.array_equal(to_host(s_dev[l]), s_h[l])
     assert m.mamba_device_faults(clear=True) == 0
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_random_m3_prepare_shape_matches_oracle(cuda_lib, i):
+    """Random shapes of the Mamba-3 step's preparation (any even d_state, any
+    number of rotated pairs up to all of them, f32 or bf16 k and q): two tokens
+    on the last layer against the oracle, the other layers' angle state
+    untouched."""
+    m = cuda_lib
+    r = np.random.default_rng(0x5EED_3200 + i)
+    N = 2 * int(r.integers(1, 65))
+    na = int(r.integers(0, N // 2 + 1))
+    Bsz, H, L = int(r.integers(1, 9)), int(r.integers(1, 33)), int(r.integers(1, 4))
+    kq = str(r.choice(["f32", "bf16"]))
+    seed, layer = 0x5EED_3300 + i, L - 1
+    th_h = synth.m3_angle_state(seed, L, Bsz, H, max(na, 1))
+    th = to_dev(th_h)
+    th_ref = th_h.astype(np.float64)
+    kqd = torch.bfloat16 if kq == "bf16" else torch.float32
+    what = f"case {i} (B={Bsz} H={H} N={N} n_angles={na} {kq})"
+    for step in range(2):
+        inp = synth.m3_prepare_inputs(seed, layer, step, Bsz, H, N, na)
+        d = {n: to_dev(v) for n, v in inp.items()}
+        k = torch.empty((Bsz, H, N), device="cuda", dtype=kqd)
+        q = torch.empty_like(k)
+        al, be, ga = (torch.empty((Bsz, H), device="cuda") for _ in range(3))
+        m.mamba3_siso_step_prepare(k, q, al, be, ga, d["k_in"], d["q_in"], d["dt"], d["A"], d["lam"],
+                                   d["angles"] if na else None, th if na else None, layer)
+        torch.cuda.synchronize()
+        rk, rq, ral, rbe, rga = oracle.m3_prepare(inp["k_in"], inp["q_in"], inp["dt"], inp["A"], inp["lam"],
+                                                  inp["angles"] if na else None, th_ref if na else None, layer)
+        assert_within(to_host(k), rk, f"{what}: k step {step}", bf16_out=kq == "bf16")
+        assert_within(to_host(q), rq, f"{what}: q step {step}", bf16_out=kq == "bf16")
+        for g, rr, nm in ((al, ral, "alpha"), (be, rbe, "beta"), (ga, rga, "gamma")):
+            assert_within(to_host(g), rr, f"{what}: {nm} step {step}")
+        if na:
+            assert_within(to_host(th[layer]), th_ref[layer], f"{what}: angle state step {step}")
+    for l in range(L - 1):
+        assert np.array_equal(to_host(th[l]), th_h[l])
