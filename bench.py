@@ -55,6 +55,7 @@ KERNEL_SOURCES["gemm"] = ["selective_state_space_conv1d_gb300/csrc/gemm.cu",
                           "selective_state_space_conv1d_gb300/csrc/async_copy.cuh"]
 KERNEL_SOURCES["rmsnorm"] = ["selective_state_space_conv1d_gb300/csrc/rmsnorm.cu"]
 KERNEL_SOURCES["m3_step"] = ["selective_state_space_conv1d_gb300/csrc/m3_step.cu",
+                             "selective_state_space_conv1d_gb300/csrc/m3_math.cuh",
                              "selective_state_space_conv1d_gb300/csrc/device_math.cuh"]
 
 
@@ -1230,6 +1231,34 @@ def run_m3_decode(torch, m, device, peak, peak_src, n_steps=16, L=24, Bsz=128, H
     ms2 = a.elapsed_time(b) / (reps * n_steps)
     del gr
     pms = kernel_time(torch, [lambda s_=s_, l=l: prep(s_, l) for s_ in range(4) for l in range(L)], 4 * L)
+
+    # the same tokens with the preparation inside the step (one launch per layer)
+    def fused(s_, l):
+        m.mamba3_siso_step_fused_batched(y[l], x[s_, l], k_in[s_, l], q_in[s_, l], dt[s_, l], A[s_, l], lam[s_, l],
+                                         ang[s_, l], st, ks, vs, th, l, D[l])
+
+    for s_ in range(3):
+        for l in range(L):
+            fused(s_, l)
+    torch.cuda.synchronize()
+    gr = capture(torch, lambda: [fused(s_, l) for s_ in range(n_steps) for l in range(L)])
+    gr.replay()
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(reps):
+        gr.replay()
+    b.record()
+    torch.cuda.synchronize()
+    ms3 = a.elapsed_time(b) / (reps * n_steps)
+    del gr
+    fms = kernel_time(torch, [lambda s_=s_, l=l: fused(s_, l) for s_ in range(4) for l in range(L)], 4 * L)
+    # k_in, q_in replace k, q and dt, A, lam replace alpha, beta, gamma (same bytes); plus the angles
+    fused_bytes = per_launch + BH * na * 8 + Bsz * na * 4
+    out["fused"] = {
+        "value": round(1e3 / ms3, 2), "unit": "steps/s", "ms_per_step": round(ms3, 5), "n_angles": na,
+        "gpu_launches_per_step": L, "note": "each layer: mamba3_siso_step_fused_batched (the preparation inside the step)",
+        "roofline": roofline(fused_bytes, fms, peak, peak_src, ncu_traffic("m3_step", out["workload"] + "-fused")),
+    }
     out["with_prepare"] = {
         "value": round(1e3 / ms2, 2), "unit": "steps/s", "ms_per_step": round(ms2, 5),
         "n_angles": na, "gpu_launches_per_step": 2 * L,

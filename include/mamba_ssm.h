@@ -319,6 +319,33 @@ MAMBA_API int mamba3_siso_step_prepare(void* k, void* q, int kq_dtype, float* al
                                        void* stream);
 
 /*
+ * mamba3_siso_step_fused_batched - one Mamba-3 SISO token in one launch: the
+ * step's inputs made exactly as mamba3_siso_step_prepare makes them (the angle
+ * state advanced, k_in and q_in turned in pairs into k and q, alpha / beta /
+ * gamma), then the step of mamba3_siso_step_batched on them, on the `layer`
+ * slabs of the four persistent states.  (inference.rs steps F4c, F5 and F6 of
+ * `step_layer_kernels`; the page launches them separately.)  k and q stay in
+ * f32 registers and shared memory and never reach global memory, so the result
+ * equals the two calls with f32 k and q bit for bit.
+ *
+ *   y          [B][H][P] dense, dtype y_dtype (out)
+ *   x          [B][H][P] dense, dtype x_dtype
+ *   k_in, q_in [B][H][N] f32; dt, A, lam [B][H] f32; angles [B][n_angles] f32
+ *              (NULL when n_angles = 0); D [H] f32 or NULL
+ *   ssm_state, k_state, v_state as for mamba3_siso_step_batched (the k state
+ *              receives the turned k)
+ *   angle_state base of [n_layers][B][H][n_angles] f32 (NULL when n_angles = 0)
+ * N (d_state) in {16, 32, 64, 128}; 2 n_angles <= N; P * N / 8 <= 2048.
+ * Errors: as for mamba_ssm_step_batched.
+ */
+MAMBA_API int mamba3_siso_step_fused_batched(void* y, int y_dtype, const void* x, int x_dtype, const float* k_in,
+                                             const float* q_in, const float* dt, const float* A, const float* lam,
+                                             const float* angles, const float* D, float* ssm_state, float* k_state,
+                                             float* v_state, float* angle_state, int64_t layer, int64_t n_layers,
+                                             int64_t B, int64_t H, int64_t P, int64_t N, int64_t n_angles,
+                                             void* stream);
+
+/*
  * Graph-captured decode driver.  (inference.rs `capture_graph` / `step`: after
  * a warm-up step the engine records its whole T=1 step chain into a CUDA graph
  * once and replays it every token, cutting the launch overhead from ~50 us to

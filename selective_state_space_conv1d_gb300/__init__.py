@@ -10,6 +10,7 @@ C-ABI entry points (include/mamba_ssm.h), each backed by hand-written CUDA kerne
   mamba_decode_graph_*          n_steps x n_layers fused steps recorded as one CUDA graph
   mamba3_siso_step_batched      T=1 step of the Mamba-3 SISO (trapezoidal) recurrence
   mamba3_siso_step_prepare      its inputs: angle state advanced, k and q rotated, alpha/beta/gamma
+  mamba3_siso_step_fused_batched  both in one launch (k and q never leave the SM)
   mamba_linear_bf16             a projection of the layer on the tensor cores (tcgen05)
   mamba_rmsnorm                 RMSNorm of the f32 residual stream
   mamba_layer_prefill / _step   the whole Mamba-1 block (norm, projections, mixer, residual)
@@ -39,6 +40,7 @@ from ._binding import (  # noqa: F401
     load,
     mamba3_siso_step_batched,
     mamba3_siso_step_prepare,
+    mamba3_siso_step_fused_batched,
     mamba_conv1d_silu_prefill,
     mamba_conv1d_silu_step,
     mamba_device_faults,

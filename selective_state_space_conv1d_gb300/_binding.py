@@ -39,6 +39,7 @@ ABI_SYMBOLS = (
     "mamba_mixer_prefill",
     "mamba3_siso_step_batched",
     "mamba3_siso_step_prepare",
+    "mamba3_siso_step_fused_batched",
     "mamba_linear_bf16",
     "mamba_rmsnorm",
     "mamba_layer_workspace_bytes",
@@ -112,6 +113,8 @@ def load(path: str | None = None):
         lib.mamba3_siso_step_batched.restype = ctypes.c_int
         lib.mamba3_siso_step_prepare.argtypes = [vp, vp, i32] + [vp] * 10 + [i64] * 6 + [vp]
         lib.mamba3_siso_step_prepare.restype = ctypes.c_int
+        lib.mamba3_siso_step_fused_batched.argtypes = [vp, i32, vp, i32] + [vp] * 11 + [i64] * 7 + [vp]
+        lib.mamba3_siso_step_fused_batched.restype = ctypes.c_int
         lib.mamba_linear_bf16.argtypes = [vp, i64, i32, vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]
         lib.mamba_linear_bf16.restype = ctypes.c_int
         lib.mamba_rmsnorm.argtypes = [vp, i64, i32, vp, i64, vp, ctypes.c_float, i64, i64, vp]
@@ -474,6 +477,43 @@ def mamba3_siso_step_prepare(k, q, alpha, beta, gamma, k_in, q_in, dt, A, lam, a
     _check(load().mamba3_siso_step_prepare(
         _ptr(k), _ptr(q), _dtype_code(k), _ptr(alpha), _ptr(beta), _ptr(gamma), _ptr(k_in), _ptr(q_in), _ptr(dt),
         _ptr(A), _ptr(lam), _ptr(angles), _ptr(angle_state), int(layer), L, Bsz, H, N, na, _stream(stream, k_in)))
+
+
+def mamba3_siso_step_fused_batched(y, x, k_in, q_in, dt, A, lam, angles, ssm_state, k_state, v_state, angle_state,
+                                   layer, D=None, *, stream=None):
+    """One Mamba-3 SISO token in one launch: the step's inputs made as
+    mamba3_siso_step_prepare makes them, then the step, on slab `layer` of
+    ssm_state [L, B, H, P, N], k_state [L, B, H, N], v_state [L, B, H, P] and
+    angle_state [L, B, H, n_angles] (all updated in place).
+
+    y, x: contiguous [B, H, P]; k_in, q_in: f32 [B, H, N]; dt, A, lam: f32
+    [B, H]; angles: f32 [B, n_angles], or None (with angle_state None) for no
+    rotation; D: f32 [H]."""
+    Bsz, H, P = x.shape
+    N = k_in.shape[2]
+    L = ssm_state.shape[0]
+    for st, nm, shp in ((ssm_state, "ssm_state", (L, Bsz, H, P, N)), (k_state, "k_state", (L, Bsz, H, N)),
+                        (v_state, "v_state", (L, Bsz, H, P))):
+        _f32_param(st, nm, shp)
+    for t, nm in ((k_in, "k_in"), (q_in, "q_in")):
+        _f32_param(t, nm, (Bsz, H, N))
+    for t, nm in ((dt, "dt"), (A, "A"), (lam, "lam")):
+        _f32_param(t, nm, (Bsz, H))
+    _f32_param(D, "D", (H,))
+    for t, nm in ((y, "y"), (x, "x")):
+        if tuple(t.shape) != (Bsz, H, P) or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous {(Bsz, H, P)} tensor")
+    if (angles is None) != (angle_state is None):
+        raise ValueError("angles and angle_state go together")
+    na = 0
+    if angles is not None:
+        na = angles.shape[1] if angles.dim() == 2 else -1
+        _f32_param(angles, "angles", (Bsz, na))
+        _f32_param(angle_state, "angle_state", (L, Bsz, H, na))
+    _check(load().mamba3_siso_step_fused_batched(
+        _ptr(y), _dtype_code(y), _ptr(x), _dtype_code(x), _ptr(k_in), _ptr(q_in), _ptr(dt), _ptr(A), _ptr(lam),
+        _ptr(angles), _ptr(D), _ptr(ssm_state), _ptr(k_state), _ptr(v_state), _ptr(angle_state), int(layer), L, Bsz,
+        H, P, N, na, _stream(stream, x)))
 
 
 def mamba_ssm_step_batched(y, u, dt, Bm, Cm, ssm_state, layer, A_log, D=None, dt_bias=None,

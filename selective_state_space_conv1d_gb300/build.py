@@ -22,7 +22,7 @@ SOURCES = ["api.cu", "conv1d.cu", "scan_prefill.cu", "ssm_step.cu", "noalloc.cu"
            "m3_prepare.cu", "selftest.cu", "gemm.cu", "rmsnorm.cu"]
 # scan_inst.cu is compiled once per (storage dtype, d_state): small parallel units
 SCAN_INST = [(bf16, n) for n in (1, 2, 4, 8, 16, 32, 64) for bf16 in (0, 1)]
-HEADERS = [os.path.join(CSRC, h) for h in ("async_copy.cuh", "device_math.cuh", "launch.h", "scan_kernel.cuh")] + [
+HEADERS = [os.path.join(CSRC, h) for h in ("async_copy.cuh", "device_math.cuh", "launch.h", "m3_math.cuh", "scan_kernel.cuh")] + [
     os.path.join(INCLUDE, "mamba_ssm.h")
 ]
 

@@ -668,6 +668,68 @@ int mamba3_siso_step_prepare(void* k, void* q, int kq_dtype, float* alpha, float
   return ok();
 }
 
+int mamba3_siso_step_fused_batched(void* y, int y_dtype, const void* x, int x_dtype, const float* k_in,
+                                   const float* q_in, const float* dt, const float* A, const float* lam,
+                                   const float* angles, const float* D, float* ssm_state, float* k_state,
+                                   float* v_state, float* angle_state, int64_t layer, int64_t n_layers, int64_t B,
+                                   int64_t H, int64_t P, int64_t N, int64_t n_angles, void* stream) {
+  int rc;
+  if ((rc = check_dtype("y_dtype", y_dtype)) || (rc = check_dtype("x_dtype", x_dtype))) return rc;
+  if (B < 0 || H < 0 || P < 0 || n_angles < 0)
+    return fail(MAMBA_ERR_INVALID_ARG, "negative size (B=%lld H=%lld P=%lld n_angles=%lld)", (long long)B,
+                (long long)H, (long long)P, (long long)n_angles);
+  if (N != 16 && N != 32 && N != 64 && N != 128)
+    return fail(MAMBA_ERR_UNSUPPORTED, "d_state=%lld not in {16,32,64,128}", (long long)N);
+  if (2 * n_angles > N)
+    return fail(MAMBA_ERR_INVALID_ARG, "n_angles=%lld rotates more than the d_state=%lld components",
+                (long long)n_angles, (long long)N);
+  if (P * (N / 8) > mamba::m3_max_items())
+    return fail(MAMBA_ERR_UNSUPPORTED, "headdim * d_state / 8 = %lld exceeds %d", (long long)(P * (N / 8)),
+                mamba::m3_max_items());
+  if (n_layers < 1 || layer < 0 || layer >= n_layers)
+    return fail(MAMBA_ERR_INVALID_ARG, "layer=%lld outside [0, n_layers=%lld)", (long long)layer, (long long)n_layers);
+  if (B == 0 || H == 0 || P == 0) return ok();
+  if (!sizes_ok(B, H, P * N) || !sizes_ok(n_layers, B * H, P * N) ||
+      (n_angles > 0 && !sizes_ok(n_layers, B * H, n_angles)))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  if (!y || !x || !k_in || !q_in || !dt || !A || !lam || !ssm_state || !k_state || !v_state)
+    return fail(MAMBA_ERR_INVALID_ARG, "y, x, k_in, q_in, dt, A, lam and the three step states must not be NULL");
+  if (n_angles > 0 && (!angles || !angle_state))
+    return fail(MAMBA_ERR_INVALID_ARG, "angles and angle_state must not be NULL when n_angles > 0");
+  if (reinterpret_cast<uintptr_t>(ssm_state) & 15) return fail(MAMBA_ERR_INVALID_ARG, "ssm_state must be 16-byte aligned");
+  const int es = es_of(x_dtype), esy = es_of(y_dtype);
+  const int64_t BH = B * H;
+  int64_t by = 0, bx = 0, bk = 0, bs = 0, bh = 0, bss = 0, bks = 0, bvs = 0, ban = 0, bth = 0;
+  if (!span_bytes(1, BH * P, BH * P, esy, &by) || !span_bytes(1, BH * P, BH * P, es, &bx) ||
+      !span_bytes(1, BH * N, BH * N, 4, &bk) || !span_bytes(1, BH, BH, 4, &bs) || !span_bytes(1, H, H, 4, &bh) ||
+      !span_bytes(BH * P, N, N, 4, &bss) || !span_bytes(1, BH * N, BH * N, 4, &bks) ||
+      !span_bytes(1, BH * P, BH * P, 4, &bvs) || !span_bytes(1, B * n_angles, B * n_angles, 4, &ban) ||
+      !span_bytes(1, BH * n_angles, BH * n_angles, 4, &bth))
+    return fail(MAMBA_ERR_INVALID_ARG, "extent overflow");
+  mamba::DeviceInfo dev;
+  if ((rc = current_device(&dev))) return rc;
+  int dev_id = 0;
+  cudaGetDevice(&dev_id);
+  float* sslab = ssm_state + layer * BH * P * N;
+  float* kslab = k_state + layer * BH * N;
+  float* vslab = v_state + layer * BH * P;
+  float* th = n_angles > 0 ? angle_state + layer * BH * n_angles : nullptr;
+  const float* an = n_angles > 0 ? angles : nullptr;
+  Range ins[] = {range_of("x", x, bx),        range_of("k_in", k_in, bk), range_of("q_in", q_in, bk),
+                 range_of("dt", dt, bs),      range_of("A", A, bs),       range_of("lam", lam, bs),
+                 range_of("angles", an, ban), range_of("D", D, bh)};
+  Range outs[] = {range_of("y", y, by), range_of("ssm_state", sslab, bss), range_of("k_state", kslab, bks),
+                  range_of("v_state", vslab, bvs), range_of("angle_state", th, bth)};
+  if ((rc = check_pointers(ins, 8, dev_id)) || (rc = check_pointers(outs, 5, dev_id))) return rc;
+  if ((rc = check_overlaps(outs, 5, ins, 8))) return rc;
+  mamba::M3StepArgs a{y, y_dtype == MAMBA_BF16, x, nullptr, nullptr, x_dtype == MAMBA_BF16, nullptr, nullptr, nullptr,
+                      D, sslab, kslab, vslab, B, H, (int)P, (int)N, k_in, q_in, dt, A, lam, an, th,
+                      (int)n_angles};
+  cudaError_t e = mamba::launch_m3_step_batched(a, dev, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail("mamba3_siso_step_fused_batched launch", e);
+  return ok();
+}
+
 int mamba_linear_bf16(void* c, int64_t ld_c, int c_dtype, const void* a, int64_t ld_a, const void* w, int64_t ld_w,
                       const float* residual, int64_t ld_r, int64_t M, int64_t N, int64_t K, void* stream) {
   int rc;

@@ -189,13 +189,23 @@ struct M3StepArgs {
   float* v_state;       // [B][H][P]
   int64_t B, H;
   int P, N;
+  // the fused form (k_in non-null): k, q and alpha / beta / gamma are not
+  // given but made in the step from these, as the preparation makes them
+  const float* k_in;    // [B][H][N] f32 (B after norm and bias)
+  const float* q_in;    // [B][H][N] f32 (C after norm and bias)
+  const float* dt;      // [B][H]
+  const float* A;       // [B][H]
+  const float* lam;     // [B][H]
+  const float* angles;  // [B][na]
+  float* theta;         // this layer's angle state [B][H][na] (null when na == 0)
+  int na;
 };
 // hd * ds / 8 must not exceed this
 int m3_max_items();
 cudaError_t launch_m3_step_batched(const M3StepArgs& a, const DeviceInfo& dev, cudaStream_t stream);
 
 // The Mamba-3 step's inputs: angle state advanced, k and q rotated in pairs,
-// alpha / beta / gamma (m3_step.cu).
+// alpha / beta / gamma (m3_prepare.cu).
 struct M3PrepArgs {
   void* k;              // [B][H][N] out, kq_bf16 ? bf16 : f32
   void* q;              // [B][H][N] out

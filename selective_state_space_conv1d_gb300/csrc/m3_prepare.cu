@@ -30,6 +30,7 @@
 
 #include "device_math.cuh"
 #include "launch.h"
+#include "m3_math.cuh"
 
 namespace mamba {
 namespace {
@@ -47,13 +48,12 @@ __global__ void __launch_bounds__(256) m3_prepare_kernel(M3PrepArgs a) {
   float ke = a.k_in[e], ko = a.k_in[e + 1], qe = a.q_in[e], qo = a.q_in[e + 1];
   if (j < a.na) {
     const int64_t b = bh / a.H;
-    const float t = a.theta[bh * a.na + j] + d * a.angles[b * a.na + j];
+    const float t = m3_advance_angle(a.theta[bh * a.na + j], d, a.angles[b * a.na + j]);
     a.theta[bh * a.na + j] = t;
     float sn, cs;
     sincosf(t, &sn, &cs);
-    const float k0 = cs * ke - sn * ko, k1 = sn * ke + cs * ko;
-    const float q0 = cs * qe - sn * qo, q1 = sn * qe + cs * qo;
-    ke = k0; ko = k1; qe = q0; qo = q1;
+    m3_rotate(sn, cs, ke, ko);
+    m3_rotate(sn, cs, qe, qo);
   }
   Tkq* K = reinterpret_cast<Tkq*>(a.k);
   Tkq* Q = reinterpret_cast<Tkq*>(a.q);
@@ -62,11 +62,10 @@ __global__ void __launch_bounds__(256) m3_prepare_kernel(M3PrepArgs a) {
   Q[e] = from_f32<Tkq>(qe);
   Q[e + 1] = from_f32<Tkq>(qo);
   if (j == 0) {
-    const float al = expf(d * a.A[bh]);
-    const float lam = a.lam[bh];
-    a.alpha[bh] = al;
-    a.beta[bh] = (1.0f - lam) * d * al;
-    a.gamma[bh] = lam * d;
+    const M3Weights w = m3_weights(d, a.A[bh], a.lam[bh]);
+    a.alpha[bh] = w.alpha;
+    a.beta[bh] = w.beta;
+    a.gamma[bh] = w.gamma;
   }
 }
 

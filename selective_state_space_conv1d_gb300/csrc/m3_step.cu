@@ -26,6 +26,7 @@
 #include "async_copy.cuh"
 #include "device_math.cuh"
 #include "launch.h"
+#include "m3_math.cuh"
 
 namespace mamba {
 namespace {
@@ -34,8 +35,35 @@ constexpr int kM3Threads = 256;
 constexpr int kM3Group = 8;        // states per thread and row
 constexpr int kM3MaxItems = 8;     // (row, group) items per thread: hd * ds / 8 <= 2048
 
-// ITEMS: (row, group) items per thread, all loaded before any arithmetic
-template <int N, typename Tin, typename Tout, int ITEMS>
+// The fused form's inputs of one (batch, head): k_in and q_in turned pair by
+// pair by the advanced angle state into the staged k and q (the thread of a
+// pair reads and writes its own angle), exactly as the preparation kernel does.
+template <int N>
+__device__ __forceinline__ void m3_stage_rotated(const M3StepArgs& a, int64_t bh, int tid, int nthreads, float* s_k,
+                                                 float* s_q) {
+  const float d = a.dt[bh];
+  const int64_t b = bh / a.H;
+  for (int j = tid; j < N / 2; j += nthreads) {
+    float ke = a.k_in[bh * N + 2 * j], ko = a.k_in[bh * N + 2 * j + 1];
+    float qe = a.q_in[bh * N + 2 * j], qo = a.q_in[bh * N + 2 * j + 1];
+    if (j < a.na) {
+      const float t = m3_advance_angle(a.theta[bh * a.na + j], d, a.angles[b * a.na + j]);
+      a.theta[bh * a.na + j] = t;
+      float sn, cs;
+      sincosf(t, &sn, &cs);
+      m3_rotate(sn, cs, ke, ko);
+      m3_rotate(sn, cs, qe, qo);
+    }
+    s_k[2 * j] = ke;
+    s_k[2 * j + 1] = ko;
+    s_q[2 * j] = qe;
+    s_q[2 * j + 1] = qo;
+  }
+}
+
+// ITEMS: (row, group) items per thread, all loaded before any arithmetic;
+// PREP: the fused form (k, q and alpha / beta / gamma made here)
+template <int N, typename Tin, typename Tout, int ITEMS, bool PREP>
 __global__ void __launch_bounds__(kM3Threads) m3_step_kernel(M3StepArgs a) {
   grid_dependency_begin();
   constexpr int NG = N / kM3Group;  // threads per row
@@ -51,16 +79,31 @@ __global__ void __launch_bounds__(kM3Threads) m3_step_kernel(M3StepArgs a) {
   const Tin* Q = reinterpret_cast<const Tin*>(a.q);
   float* ks = a.k_state + bh * N;
   float* vs = a.v_state + bh * P;
-  for (int i = threadIdx.x; i < N; i += kM3Threads) {
-    s_kp[i] = ks[i];
-    s_k[i] = to_f32(K[bh * N + i]);
-    s_q[i] = to_f32(Q[bh * N + i]);
+  if constexpr (PREP) {
+    m3_stage_rotated<N>(a, bh, threadIdx.x, kM3Threads, s_k, s_q);
+    for (int i = threadIdx.x; i < N; i += kM3Threads) s_kp[i] = ks[i];
+  } else {
+    for (int i = threadIdx.x; i < N; i += kM3Threads) {
+      s_kp[i] = ks[i];
+      s_k[i] = to_f32(K[bh * N + i]);
+      s_q[i] = to_f32(Q[bh * N + i]);
+    }
   }
   for (int i = threadIdx.x; i < P; i += kM3Threads) {
     s_vp[i] = vs[i];
     s_x[i] = to_f32(X[bh * P + i]);
   }
-  const float alpha = a.alpha[bh], beta = a.beta[bh], gamma = a.gamma[bh];
+  float alpha, beta, gamma;
+  if constexpr (PREP) {
+    const M3Weights w = m3_weights(a.dt[bh], a.A[bh], a.lam[bh]);
+    alpha = w.alpha;
+    beta = w.beta;
+    gamma = w.gamma;
+  } else {
+    alpha = a.alpha[bh];
+    beta = a.beta[bh];
+    gamma = a.gamma[bh];
+  }
   const float Dh = a.D ? a.D[head] : 0.0f;
   __syncthreads();
 
@@ -141,29 +184,40 @@ __device__ int g_m3_faults = 0;
 
 __host__ __device__ constexpr int m3_align16(int x) { return (x + 15) & ~15; }
 
-// byte offsets of one stage's parts for headdim P, d_state N, input size es
+// byte offsets of one stage's parts for headdim P, d_state N, x of es bytes,
+// k and q of kq_es bytes, and na angles (the fused form's angle state)
 struct M3Tile {
-  int state, kprev, vprev, x, k, q, bytes;
-  __host__ __device__ static M3Tile make(int P, int N, int es) {
+  int state, kprev, vprev, x, k, q, th, bytes;
+  __host__ __device__ static M3Tile make(int P, int N, int es, int kq_es, int na) {
     M3Tile t{};
     t.state = 0;
     t.kprev = t.state + P * N * 4;
     t.vprev = t.kprev + N * 4;
     t.x = t.vprev + P * 4;
     t.k = t.x + m3_align16(P * es);
-    t.q = t.k + m3_align16(N * es);
-    t.bytes = (t.q + m3_align16(N * es) + 127) & ~127;
+    t.q = t.k + m3_align16(N * kq_es);
+    t.th = t.q + m3_align16(N * kq_es);
+    t.bytes = (t.th + m3_align16(na * 4) + 127) & ~127;
     return t;
   }
 };
 
-template <int N, typename Tin, typename Tout>
+// PREP: the fused form.  The stage then carries k_in and q_in (f32) and the
+// tile's angles; every consumer thread keeps the same 8-state group for all
+// its items (the consumer count is a multiple of N / 8), so it turns that
+// group's pairs once per tile from the staged angles, and the first thread of
+// each group writes the advanced angles back (nothing reads them from global
+// memory in this launch after the stage is filled).
+template <int N, typename Tin, typename Tout, bool PREP>
 __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a, int stages, int64_t n_tiles) {
   constexpr int NG = N / kM3Group;
   constexpr int es = sizeof(Tin);
+  constexpr int kq_es = PREP ? 4 : es;
+  static_assert(m3ring::kConsumers % NG == 0, "a consumer thread keeps one 8-state group");
   extern __shared__ __align__(128) unsigned char smem[];
   const int P = a.P;
-  const M3Tile L = M3Tile::make(P, N, es);
+  const int na = PREP ? a.na : 0;
+  const M3Tile L = M3Tile::make(P, N, es, kq_es, na);
   const uint32_t bars = smem_u32(smem);
   const auto full = [&](int s) { return bars + 8u * s; };
   const auto empty = [&](int s) { return bars + 8u * (m3ring::kMaxStages + s); };
@@ -184,8 +238,8 @@ __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a,
     // ---- producer ----
     if (lane != 0) return;
     const char* X = reinterpret_cast<const char*>(a.x);
-    const char* K = reinterpret_cast<const char*>(a.k);
-    const char* Q = reinterpret_cast<const char*>(a.q);
+    const char* K = reinterpret_cast<const char*>(PREP ? static_cast<const void*>(a.k_in) : a.k);
+    const char* Q = reinterpret_cast<const char*>(PREP ? static_cast<const void*>(a.q_in) : a.q);
     const uint32_t ring0 = bars + m3ring::kBarBytes;
     int issued = 0, s = 0;
     uint32_t phase = 0;
@@ -196,14 +250,15 @@ __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a,
       }
       const int64_t bh = t_begin + i;
       const uint32_t st = ring0 + (uint32_t)(s * L.bytes), fb = full(s);
-      const uint32_t bytes = P * N * 4 + N * 4 + P * 4 + P * es + 2 * N * es;
+      const uint32_t bytes = P * N * 4 + N * 4 + P * 4 + P * es + 2 * N * kq_es + na * 4;
       mbar_arrive_expect_tx(fb, bytes);
       bulk_g2s(st + L.state, a.ssm_state + bh * (int64_t)P * N, P * N * 4, fb);
       bulk_g2s(st + L.kprev, a.k_state + bh * N, N * 4, fb);
       bulk_g2s(st + L.vprev, a.v_state + bh * P, P * 4, fb);
       bulk_g2s(st + L.x, X + bh * P * es, P * es, fb);
-      bulk_g2s(st + L.k, K + bh * N * es, N * es, fb);
-      bulk_g2s(st + L.q, Q + bh * N * es, N * es, fb);
+      bulk_g2s(st + L.k, K + bh * N * kq_es, N * kq_es, fb);
+      bulk_g2s(st + L.q, Q + bh * N * kq_es, N * kq_es, fb);
+      if (na > 0) bulk_g2s(st + L.th, a.theta + bh * na, na * 4, fb);
       issued = i + 1;
       if (++s == stages) {
         s = 0;
@@ -224,8 +279,33 @@ __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a,
     const int64_t bh = t_begin + i;
     const int head = (int)(bh % a.H);
     // per-(batch, head) scalars, fetched while the stage lands
-    const float alpha = a.alpha[bh], beta = a.beta[bh], gamma = a.gamma[bh];
+    float alpha, beta, gamma;
+    if constexpr (PREP) {
+      const M3Weights w = m3_weights(a.dt[bh], a.A[bh], a.lam[bh]);
+      alpha = w.alpha;
+      beta = w.beta;
+      gamma = w.gamma;
+    } else {
+      alpha = a.alpha[bh];
+      beta = a.beta[bh];
+      gamma = a.gamma[bh];
+    }
     const float Dh = a.D ? a.D[head] : 0.0f;
+    // the fused form: lane l turns pairs l, l + 32, ... of the tile (each
+    // warp all of them: no exchange between warps); their raw angles and dt
+    // are fetched while the stage lands
+    constexpr int kPairsPerLane = (N / 2 + 31) / 32;
+    float ang[kPairsPerLane];
+    float d = 0.0f;
+    if constexpr (PREP) {
+      d = a.dt[bh];
+      const int64_t b = bh / a.H;
+#pragma unroll
+      for (int r = 0; r < kPairsPerLane; ++r) {
+        const int j = lane + 32 * r;
+        ang[r] = j < na ? a.angles[b * na + j] : 0.0f;
+      }
+    }
     if (!__all_sync(0xffffffffu, mbar_wait(full(s), phase, m3ring::kWaitLimit))) {
       if (lane == 0) atomicOr(&g_m3_faults, MAMBA_FAULT_RING_WAIT);
       break;
@@ -238,6 +318,51 @@ __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a,
     const Tin* s_k = reinterpret_cast<const Tin*>(sp + L.k);
     const Tin* s_q = reinterpret_cast<const Tin*>(sp + L.q);
     float* hs = a.ssm_state + bh * (int64_t)P * N;
+    // the fused form: this thread's group of k and q, turned.  Each lane
+    // advances its pairs' angles from the staged ones (warp 0 stores them)
+    // and takes their sine and cosine; a thread gathers its group's four
+    // pairs from the lanes that own them.
+    float kr[kM3Group], qr[kM3Group];
+    if constexpr (PREP) {
+      const int g0 = (threadIdx.x % NG) * kM3Group;
+      const float* s_kf = reinterpret_cast<const float*>(sp + L.k);
+      const float* s_qf = reinterpret_cast<const float*>(sp + L.q);
+      const float* s_th = reinterpret_cast<const float*>(sp + L.th);
+      float sn_l[kPairsPerLane], cs_l[kPairsPerLane];
+#pragma unroll
+      for (int r = 0; r < kPairsPerLane; ++r) {
+        const int j = lane + 32 * r;
+        float t = 0.0f;
+        if (j < na) {
+          t = m3_advance_angle(s_th[j], d, ang[r]);
+          if (warp == 0) a.theta[bh * na + j] = t;
+        }
+        sincosf(t, &sn_l[r], &cs_l[r]);
+      }
+#pragma unroll
+      for (int j = 0; j < kM3Group; ++j) {
+        kr[j] = s_kf[g0 + j];
+        qr[j] = s_qf[g0 + j];
+      }
+#pragma unroll
+      for (int i2 = 0; i2 < kM3Group / 2; ++i2) {
+        const int j = g0 / 2 + i2;  // this thread's pair; owned by lane j % 32, slot j / 32
+        float sn = 0.0f, cs = 1.0f;
+#pragma unroll
+        for (int r = 0; r < kPairsPerLane; ++r) {
+          const float sr = __shfl_sync(0xffffffffu, sn_l[r], j % 32);
+          const float cr = __shfl_sync(0xffffffffu, cs_l[r], j % 32);
+          if (j / 32 == r) {
+            sn = sr;
+            cs = cr;
+          }
+        }
+        if (j < na) {
+          m3_rotate(sn, cs, kr[2 * i2], kr[2 * i2 + 1]);
+          m3_rotate(sn, cs, qr[2 * i2], qr[2 * i2 + 1]);
+        }
+      }
+    }
     for (int idx0 = 0; idx0 < items; idx0 += m3ring::kConsumers) {  // uniform over the warps
       const int idx = idx0 + threadIdx.x;
       const bool valid = idx < items;
@@ -258,8 +383,13 @@ __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a,
 #pragma unroll
       for (int j = 0; j < kM3Group; ++j) {
         kp[j] = s_kp[n0 + j];
-        kc[j] = to_f32(s_k[n0 + j]);
-        qc[j] = to_f32(s_q[n0 + j]);
+        if constexpr (PREP) {
+          kc[j] = kr[j];
+          qc[j] = qr[j];
+        } else {
+          kc[j] = to_f32(s_k[n0 + j]);
+          qc[j] = to_f32(s_q[n0 + j]);
+        }
       }
 #pragma unroll
       for (int j = 0; j < kM3Group; j += 2) {
@@ -283,8 +413,16 @@ __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a,
         if (q == 0) reinterpret_cast<Tout*>(a.y)[bh * P + p] = from_f32<Tout>(fmaf(Dh, xp, part));
       }
     }
-    // hand the current k and x on (read from the stage, before releasing it)
-    for (int j = threadIdx.x; j < N; j += m3ring::kConsumers) a.k_state[bh * N + j] = to_f32(s_k[j]);
+    // hand the current k and x on (read from the stage, before releasing it;
+    // the fused form's turned k from the first thread of each group)
+    if constexpr (PREP) {
+      if (threadIdx.x < NG) {
+#pragma unroll
+        for (int j = 0; j < kM3Group; ++j) a.k_state[bh * N + threadIdx.x * kM3Group + j] = kr[j];
+      }
+    } else {
+      for (int j = threadIdx.x; j < N; j += m3ring::kConsumers) a.k_state[bh * N + j] = to_f32(s_k[j]);
+    }
     for (int j = threadIdx.x; j < P; j += m3ring::kConsumers) a.v_state[bh * P + j] = to_f32(s_x[j]);
     __syncwarp();
     if (lane == 0) mbar_arrive(empty(s));
@@ -296,76 +434,80 @@ __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a,
 }
 
 bool m3_ring_eligible(const M3StepArgs& a) {
+  const bool prep = a.k_in != nullptr;
   const int es = a.in_bf16 ? 2 : 4;
+  const int kq_es = prep ? 4 : es;
+  const int na = prep ? a.na : 0;
   const auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; };
-  if ((a.P * 4) % 16 || (a.P * es) % 16 || (a.N * es) % 16) return false;
-  if (!al(a.ssm_state) || !al(a.k_state) || !al(a.v_state) || !al(a.x) || !al(a.k) || !al(a.q)) return false;
-  return 2 * M3Tile::make(a.P, a.N, es).bytes + m3ring::kBarBytes <= 200 * 1024;
+  if ((a.P * 4) % 16 || (a.P * es) % 16 || (a.N * kq_es) % 16 || (na * 4) % 16) return false;
+  if (!al(a.ssm_state) || !al(a.k_state) || !al(a.v_state) || !al(a.x)) return false;
+  if (prep ? (!al(a.k_in) || !al(a.q_in) || (na > 0 && !al(a.theta))) : (!al(a.k) || !al(a.q))) return false;
+  return 2 * M3Tile::make(a.P, a.N, es, kq_es, na).bytes + m3ring::kBarBytes <= 200 * 1024;
 }
 
-template <int N, typename Tin, typename Tout>
+template <int N, typename Tin, typename Tout, bool PREP>
 cudaError_t launch_m3_ring(const M3StepArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
   const int es = sizeof(Tin);
-  const M3Tile L = M3Tile::make(a.P, N, es);
+  const M3Tile L = M3Tile::make(a.P, N, es, PREP ? 4 : es, PREP ? a.na : 0);
   int stages = m3ring::kRingBytes / L.bytes;
   stages = stages < 2 ? 2 : (stages > m3ring::kMaxStages ? m3ring::kMaxStages : stages);
   const int smem = m3ring::kBarBytes + stages * L.bytes;
+  auto kern = m3_ring_kernel<N, Tin, Tout, PREP>;
   static std::atomic<int> attr_set[64];
   int dev_id = 0;
   cudaError_t e = cudaGetDevice(&dev_id);
   if (e != cudaSuccess) return e;
   if (dev_id < 0 || dev_id >= 64) return cudaErrorInvalidDevice;
   if (!attr_set[dev_id].load(std::memory_order_relaxed)) {
-    if ((e = cudaFuncSetAttribute(m3_ring_kernel<N, Tin, Tout>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  200 * 1024)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024)) != cudaSuccess)
       return e;
     attr_set[dev_id].store(1, std::memory_order_relaxed);
   }
   int occ = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, m3_ring_kernel<N, Tin, Tout>, m3ring::kThreads,
-                                                         smem)) != cudaSuccess)
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, m3ring::kThreads, smem)) != cudaSuccess)
     return e;
   occ = occ < 1 ? 1 : occ;
   const int64_t n_tiles = a.B * a.H;
   const int64_t resident = (int64_t)dev.sm_count * occ;
   const int64_t grid = n_tiles < resident ? n_tiles : resident;
-  return launch_pdl(true, m3_ring_kernel<N, Tin, Tout>, dim3((unsigned)grid), dim3(m3ring::kThreads), smem, stream, a,
-                    stages, n_tiles);
+  return launch_pdl(true, kern, dim3((unsigned)grid), dim3(m3ring::kThreads), smem, stream, a, stages, n_tiles);
 }
 
-template <int N, typename Tin, typename Tout, int ITEMS>
+template <int N, typename Tin, typename Tout, int ITEMS, bool PREP>
 cudaError_t launch_m3_i(const M3StepArgs& a, cudaStream_t s) {
   const int64_t blocks = a.B * a.H;
   if (blocks > 0x7FFFFFFF) return cudaErrorInvalidConfiguration;
   const size_t smem = 2 * (size_t)a.P * sizeof(float);
-  return launch_pdl(true, m3_step_kernel<N, Tin, Tout, ITEMS>, dim3((unsigned)blocks), dim3(kM3Threads), smem, s, a);
+  return launch_pdl(true, m3_step_kernel<N, Tin, Tout, ITEMS, PREP>, dim3((unsigned)blocks), dim3(kM3Threads), smem,
+                    s, a);
 }
 
-template <int N, typename Tin, typename Tout>
+template <int N, typename Tin, typename Tout, bool PREP>
 cudaError_t launch_m3_o(const M3StepArgs& a, cudaStream_t s) {
   const int64_t per_thread = ((int64_t)a.P * (N / kM3Group) + kM3Threads - 1) / kM3Threads;
-  if (per_thread <= 1) return launch_m3_i<N, Tin, Tout, 1>(a, s);
-  if (per_thread <= 2) return launch_m3_i<N, Tin, Tout, 2>(a, s);
-  if (per_thread <= 4) return launch_m3_i<N, Tin, Tout, 4>(a, s);
-  if (per_thread <= kM3MaxItems) return launch_m3_i<N, Tin, Tout, kM3MaxItems>(a, s);
+  if (per_thread <= 1) return launch_m3_i<N, Tin, Tout, 1, PREP>(a, s);
+  if (per_thread <= 2) return launch_m3_i<N, Tin, Tout, 2, PREP>(a, s);
+  if (per_thread <= 4) return launch_m3_i<N, Tin, Tout, 4, PREP>(a, s);
+  if (per_thread <= kM3MaxItems) return launch_m3_i<N, Tin, Tout, kM3MaxItems, PREP>(a, s);
   return cudaErrorInvalidValue;
 }
 
-template <int N, typename Tin>
+template <int N, typename Tin, bool PREP>
 cudaError_t launch_m3_t(const M3StepArgs& a, const DeviceInfo& dev, bool ring, cudaStream_t s) {
   if (ring)
-    return a.y_bf16 ? launch_m3_ring<N, Tin, __nv_bfloat16>(a, dev, s) : launch_m3_ring<N, Tin, float>(a, dev, s);
-  return a.y_bf16 ? launch_m3_o<N, Tin, __nv_bfloat16>(a, s) : launch_m3_o<N, Tin, float>(a, s);
+    return a.y_bf16 ? launch_m3_ring<N, Tin, __nv_bfloat16, PREP>(a, dev, s)
+                    : launch_m3_ring<N, Tin, float, PREP>(a, dev, s);
+  return a.y_bf16 ? launch_m3_o<N, Tin, __nv_bfloat16, PREP>(a, s) : launch_m3_o<N, Tin, float, PREP>(a, s);
 }
 
-template <typename Tin>
+template <typename Tin, bool PREP>
 cudaError_t launch_m3_n(const M3StepArgs& a, const DeviceInfo& dev, cudaStream_t s) {
   const bool ring = m3_ring_eligible(a);
   switch (a.N) {
-    case 16: return launch_m3_t<16, Tin>(a, dev, ring, s);
-    case 32: return launch_m3_t<32, Tin>(a, dev, ring, s);
-    case 64: return launch_m3_t<64, Tin>(a, dev, ring, s);
-    case 128: return launch_m3_t<128, Tin>(a, dev, ring, s);
+    case 16: return launch_m3_t<16, Tin, PREP>(a, dev, ring, s);
+    case 32: return launch_m3_t<32, Tin, PREP>(a, dev, ring, s);
+    case 64: return launch_m3_t<64, Tin, PREP>(a, dev, ring, s);
+    case 128: return launch_m3_t<128, Tin, PREP>(a, dev, ring, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -375,7 +517,9 @@ cudaError_t launch_m3_n(const M3StepArgs& a, const DeviceInfo& dev, cudaStream_t
 int m3_max_items() { return kM3MaxItems * kM3Threads; }
 
 cudaError_t launch_m3_step_batched(const M3StepArgs& a, const DeviceInfo& dev, cudaStream_t stream) {
-  return a.in_bf16 ? launch_m3_n<__nv_bfloat16>(a, dev, stream) : launch_m3_n<float>(a, dev, stream);
+  if (a.k_in != nullptr)
+    return a.in_bf16 ? launch_m3_n<__nv_bfloat16, true>(a, dev, stream) : launch_m3_n<float, true>(a, dev, stream);
+  return a.in_bf16 ? launch_m3_n<__nv_bfloat16, false>(a, dev, stream) : launch_m3_n<float, false>(a, dev, stream);
 }
 
 int read_m3_faults(bool clear) {

@@ -13,6 +13,7 @@ times, then times one more call with CUDA events and prints it.
   --what fused     fused conv1d + SiLU and selective-scan prefill  [B, T, Di]
   --what m3        Mamba-3 SISO step on layer 1: --B batch, --H heads, --P headdim, --N d_state
   --what m3prep    one Mamba-3 SISO token on layer 1: the step's inputs prepared (N/2 rotated pairs), then the step
+  --what m3fused   the same token in one launch (the preparation inside the step)
   --what linear    projection GEMM: --M rows, --Nout outputs, --K inputs (--out f32|bf16, --residual)
   --what rmsnorm   RMSNorm of --M rows of --dm (f32 in, bf16 out)
   --what block     whole Mamba-1 block prefill: --B, --T, --dm, --Di, --N, --R (dt_rank), d_conv 4
@@ -32,7 +33,7 @@ from . import _binding as m
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--what", default="scan", choices=("scan", "conv", "step", "mixer", "convstep", "fused", "m3", "m3prep", "linear",
+    ap.add_argument("--what", default="scan", choices=("scan", "conv", "step", "mixer", "convstep", "fused", "m3", "m3prep", "m3fused", "linear",
                                                            "rmsnorm", "block", "blockstep"))
     ap.add_argument("--M", type=int, default=2048)
     ap.add_argument("--Nout", type=int, default=3072)
@@ -92,7 +93,7 @@ def main(argv=None):
         cs = torch.zeros((a.L, a.B, a.Di, 4), device="cuda")
         ss = torch.zeros((a.L, a.B, a.Di, a.N), device="cuda")
         f = lambda: m.mamba_layer_step(hid, wts, cs, ss, 1)
-    elif a.what in ("m3", "m3prep"):
+    elif a.what in ("m3", "m3prep", "m3fused"):
         BH = (a.B, a.H)
         st = torch.randn((a.L, a.B, a.H, a.P, a.N), generator=g, device="cuda")
         ks = torch.randn((a.L, a.B, a.H, a.N), generator=g, device="cuda")
@@ -104,7 +105,7 @@ def main(argv=None):
         Dh = torch.ones(a.H, device="cuda")
         y = torch.empty((a.B, a.H, a.P), device="cuda")
         f = lambda: m.mamba3_siso_step_batched(y, x, k, q, al, be, ga, st, ks, vs, 1, Dh)
-        if a.what == "m3prep":
+        if a.what in ("m3prep", "m3fused"):
             na = a.N // 2
             u01 = lambda s_: torch.rand(s_, generator=g, device="cuda")
             th = (u01((a.L, a.B, a.H, na)) - 0.5) * 100.0
@@ -117,6 +118,10 @@ def main(argv=None):
             def f():
                 m.mamba3_siso_step_prepare(k, q, al, be, ga, kin, qin, dt, Ad, lam, ang, th, 1)
                 m.mamba3_siso_step_batched(y, x, k, q, al, be, ga, st, ks, vs, 1, Dh)
+
+            if a.what == "m3fused":
+                def f():
+                    m.mamba3_siso_step_fused_batched(y, x, kin, qin, dt, Ad, lam, ang, st, ks, vs, th, 1, Dh)
     elif a.what in ("scan", "conv", "fused"):
         sh = (a.B, a.T, a.Di)
         x, u, dt, z = r(sh), r(sh), r(sh, 0.1), r(sh)

@@ -212,6 +212,20 @@ def test_m3_prepare_rejects_bad_arguments_on_host(lib):
     assert call(B=0, k_in=None) == m.MAMBA_OK                   # empty batch: nothing to do
 
 
+def test_m3_fused_rejects_bad_arguments_on_host(lib):
+    def call(N=64, na=32, layer=0, L=1, P=64, angles=FAKE, state=FAKE, k_in=FAKE, B=2):
+        return lib.mamba3_siso_step_fused_batched(FAKE, 0, FAKE, 0, k_in, FAKE, FAKE, FAKE, FAKE, angles, None, FAKE,
+                                                  FAKE, FAKE, state, layer, L, B, 3, P, N, na, None)
+    assert call(N=8, na=4) == m.MAMBA_ERR_UNSUPPORTED           # d_state outside {16, 32, 64, 128}
+    assert call(N=16, na=9) == m.MAMBA_ERR_INVALID_ARG          # more angles than pairs
+    assert call(P=1024, N=128) == m.MAMBA_ERR_UNSUPPORTED       # headdim * d_state / 8 too large
+    assert call(layer=1, L=1) == m.MAMBA_ERR_INVALID_ARG
+    assert call(angles=None) == m.MAMBA_ERR_INVALID_ARG
+    assert call(state=None) == m.MAMBA_ERR_INVALID_ARG
+    assert call(k_in=None) == m.MAMBA_ERR_INVALID_ARG
+    assert call(B=0, k_in=None) == m.MAMBA_OK
+
+
 def test_m3_prepare_wrapper_refuses_mismatched_tensors_before_any_call():
     import torch
     B, H, N, na = 2, 3, 8, 2

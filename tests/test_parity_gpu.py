@@ -1025,3 +1025,75 @@ def test_m3_prepare_then_step_decodes_like_the_oracle(cuda_lib, P, N, na, dtype)
     for s_dev, s_h in ((st, st_h), (ks, ks_h), (vs, vs_h), (th, th_h)):
         assert np.array_equal(to_host(s_dev[0]), s_h[0])
     assert m.mamba_device_faults(clear=True) == 0
+
+
+# ------------------------------------------ Mamba-3 token in one launch ----
+
+@pytest.mark.parametrize("P,N,na,aligned,y_dtype", [
+    (64, 64, 32, True, "f32"), (64, 64, 32, False, "f32"), (32, 128, 12, True, "bf16"), (48, 16, 3, True, "f32"),
+    (100, 16, 8, False, "f32"), (64, 32, 0, True, "f32"),
+])
+def test_m3_fused_token_equals_prepare_then_step_bitwise(cuda_lib, P, N, na, aligned, y_dtype):
+    """mamba3_siso_step_fused_batched equals mamba3_siso_step_prepare (f32 k,
+    q) followed by mamba3_siso_step_batched, bit for bit, over four tokens: y
+    and all four states.  Aligned buffers with n_angles a multiple of 4 take
+    the fused copy ring; a k state 4 bytes off a 16-byte boundary, or an odd
+    n_angles, the per-(batch, head) kernel."""
+    m = cuda_lib
+    L, layer, Bsz, H = 2, 1, 3, 5
+    st_h, ks_h, vs_h = synth.m3_states(SEED + 7, L, Bsz, H, P, N)
+    th_h = synth.m3_angle_state(SEED + 7, L, Bsz, H, max(na, 1))
+    D = to_dev(synth.normal(SEED + 7, "m3_D", (H,), 1.0))
+    two = [to_dev(a) for a in (st_h, ks_h, vs_h, th_h)]
+    one = [to_dev(a) for a in (st_h, ks_h, vs_h, th_h)]
+    if not aligned:
+        one[1] = _offset_like(one[1])
+    ytd = torch.bfloat16 if y_dtype == "bf16" else torch.float32
+    for step in range(4):
+        inp = synth.m3_prepare_inputs(SEED + 7, layer, step, Bsz, H, N, na)
+        d = {n: to_dev(v) for n, v in inp.items()}
+        x = to_dev(synth.normal(SEED + 7, "m3_x", (Bsz, H, P), 1.0, "f32", layer, step))
+        ang = d["angles"] if na else None
+        k, q, al, be, ga = _m3p_call(m, inp, na, two[3], layer)
+        y2 = torch.empty((Bsz, H, P), device="cuda", dtype=ytd)
+        m.mamba3_siso_step_batched(y2, x, k, q, al, be, ga, two[0], two[1], two[2], layer, D)
+        y1 = torch.empty((Bsz, H, P), device="cuda", dtype=ytd)
+        m.mamba3_siso_step_fused_batched(y1, x, d["k_in"], d["q_in"], d["dt"], d["A"], d["lam"], ang, one[0], one[1],
+                                         one[2], one[3] if na else None, layer, D)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2), f"y differs at token {step}"
+        for i, nm in enumerate(("ssm", "k", "v", "angle")):
+            assert torch.equal(one[i], two[i]), f"{nm} state differs at token {step}"
+    assert m.mamba_device_faults(clear=True) == 0
+
+
+@pytest.mark.parametrize("P,N,na,x_dtype", [(64, 64, 32, "bf16"), (32, 16, 8, "f32"), (16, 128, 64, "bf16")])
+def test_m3_fused_tokens_decode_like_the_oracle(cuda_lib, P, N, na, x_dtype):
+    """Five Mamba-3 SISO tokens, each one fused launch, against the chain of
+    oracle calls (the preparation, then the step): y and all four states."""
+    m = cuda_lib
+    L, layer, Bsz, H = 2, 0, 4, 3
+    st_h, ks_h, vs_h = synth.m3_states(SEED + 9, L, Bsz, H, P, N)
+    th_h = synth.m3_angle_state(SEED + 9, L, Bsz, H, na)
+    st, ks, vs, th = to_dev(st_h), to_dev(ks_h), to_dev(vs_h), to_dev(th_h)
+    ref = [a.astype(np.float64).copy() for a in (st_h, ks_h, vs_h, th_h)]
+    D_h = synth.normal(SEED + 9, "m3_D", (H,), 1.0)
+    for step in range(5):
+        inp = synth.m3_prepare_inputs(SEED + 9, layer, step, Bsz, H, N, na)
+        d = {n: to_dev(v) for n, v in inp.items()}
+        x_h = synth.normal(SEED + 9, "m3_x", (Bsz, H, P), 1.0, x_dtype, layer, step)
+        y = torch.empty((Bsz, H, P), device="cuda")
+        m.mamba3_siso_step_fused_batched(y, to_dev(x_h, x_dtype), d["k_in"], d["q_in"], d["dt"], d["A"], d["lam"],
+                                         d["angles"], st, ks, vs, th, layer, to_dev(D_h))
+        torch.cuda.synchronize()
+        rk, rq, ral, rbe, rga = oracle.m3_prepare(inp["k_in"], inp["q_in"], inp["dt"], inp["A"], inp["lam"],
+                                                  inp["angles"], ref[3], layer)
+        y_ref = oracle.m3_step(x_h, rk, rq, ral, rbe, rga, ref[0], ref[1], ref[2], layer, D_h)
+        assert_within(to_host(y), y_ref, f"m3 fused y token {step}")
+        assert_within(to_host(st[layer]), ref[0][layer], f"m3 fused ssm state token {step}")
+        assert_within(to_host(ks[layer]), ref[1][layer], f"m3 fused k state token {step}")
+        assert_within(to_host(th[layer]), ref[3][layer], f"m3 fused angle state token {step}")
+        assert np.array_equal(to_host(vs[layer]), ref[2][layer])
+    for s_dev, s_h in ((st, st_h), (ks, ks_h), (vs, vs_h), (th, th_h)):
+        assert np.array_equal(to_host(s_dev[1]), s_h[1])
+    assert m.mamba_device_faults(clear=True) == 0
