@@ -15,6 +15,22 @@ __device__ __forceinline__ float m3_advance_angle(float theta, float dt, float a
   return fmaf(dt, angle, theta);
 }
 
+// sin t and cos t of an accumulated angle of any size.  t is reduced to
+// r = t - 2 pi k, k = rint(t / (2 pi)), |r| <= pi, by the two-constant method
+// of Cody and Waite: 2 pi split into a float head (its nearest float) and a
+// float tail (the rest), each product with k formed exactly inside an FMA, so
+// r is within a few float ulps of the exact reduction however large k is.  On
+// [-pi, pi] the MUFU sine and cosine are accurate to about 2^-21 absolute.
+constexpr float kTwoPiHead = 6.2831854820251465f;     // float(2 pi)
+constexpr float kTwoPiTail = -1.7484555314695172e-7f;  // float(2 pi - kTwoPiHead)
+constexpr float kInvTwoPi = 0.15915493667125702f;      // float(1 / (2 pi))
+__device__ __forceinline__ void m3_sincos(float t, float* sn, float* cs) {
+  const float k = rintf(__fmul_rn(t, kInvTwoPi));
+  const float r = fmaf(-k, kTwoPiTail, fmaf(-k, kTwoPiHead, t));
+  *sn = __sinf(r);
+  *cs = __cosf(r);
+}
+
 // the pair (e, o) turned by +t, given sin t and cos t: (cos t e - sin t o, sin t e + cos t o)
 __device__ __forceinline__ void m3_rotate(float sn, float cs, float& e, float& o) {
   const float e2 = fmaf(cs, e, -__fmul_rn(sn, o));

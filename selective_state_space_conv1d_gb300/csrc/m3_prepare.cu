@@ -21,8 +21,9 @@
 // q_in (consecutive threads, consecutive pairs), advances and stores its angle,
 // rotates and stores both pairs; the thread of pair 0 writes alpha, beta and
 // gamma.  The accumulated angle grows without bound over a stream of tokens,
-// so the rotation takes the library's sincosf, which reduces any argument
-// accurately.  The kernel signals its dependents at entry, so the step that
+// so its sine and cosine come from an explicit range reduction and the MUFU
+// sine and cosine (m3_math.cuh), the same arithmetic as the fused step's.  The
+// kernel signals its dependents at entry, so the step that
 // reads its outputs is scheduled while it runs (the step waits for it to
 // complete before its first global access).
 #include <cuda_bf16.h>
@@ -51,7 +52,7 @@ __global__ void __launch_bounds__(256) m3_prepare_kernel(M3PrepArgs a) {
     const float t = m3_advance_angle(a.theta[bh * a.na + j], d, a.angles[b * a.na + j]);
     a.theta[bh * a.na + j] = t;
     float sn, cs;
-    sincosf(t, &sn, &cs);
+    m3_sincos(t, &sn, &cs);
     m3_rotate(sn, cs, ke, ko);
     m3_rotate(sn, cs, qe, qo);
   }

@@ -50,7 +50,7 @@ __device__ __forceinline__ void m3_stage_rotated(const M3StepArgs& a, int64_t bh
       const float t = m3_advance_angle(a.theta[bh * a.na + j], d, a.angles[b * a.na + j]);
       a.theta[bh * a.na + j] = t;
       float sn, cs;
-      sincosf(t, &sn, &cs);
+      m3_sincos(t, &sn, &cs);
       m3_rotate(sn, cs, ke, ko);
       m3_rotate(sn, cs, qe, qo);
     }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(m3ring::kThreads) m3_ring_kernel(M3StepArgs a,
           t = m3_advance_angle(s_th[j], d, ang[r]);
           if (warp == 0) a.theta[bh * na + j] = t;
         }
-        sincosf(t, &sn_l[r], &cs_l[r]);
+        m3_sincos(t, &sn_l[r], &cs_l[r]);
       }
 #pragma unroll
       for (int j = 0; j < kM3Group; ++j) {
