@@ -200,10 +200,14 @@ constexpr int kThreads = kConsumers + 32;  // + one producer warp (lane 0 issues
 constexpr int kMaxStages = 16;
 constexpr int kBarBytes = 2 * kMaxStages * 8;  // full[kMaxStages], empty[kMaxStages]
 constexpr long long kWaitLimit = 1ll << 31;    // SM cycles (about a second)
+// shared memory per CTA for the stages: 32 KB (5 stages of the 6 KB decode
+// tile).  Measured on the 24-layer batch-128 fused decode: 24-48 KB rings run
+// a layer in 7.03-7.09 us, 64 KB in 7.14, 96 KB in 7.9 (fewer CTAs per SM),
+// 12-16 KB in 7.29 (too few bytes in flight per CTA)
 #ifndef MAMBA_STEP_RING_BYTES
-#define MAMBA_STEP_RING_BYTES (64 * 1024)
+#define MAMBA_STEP_RING_BYTES (32 * 1024)
 #endif
-constexpr int kRingBytes = MAMBA_STEP_RING_BYTES;  // shared memory per CTA for the stages
+constexpr int kRingBytes = MAMBA_STEP_RING_BYTES;
 }  // namespace ring
 
 __host__ __device__ constexpr int align16(int x) { return (x + 15) & ~15; }
