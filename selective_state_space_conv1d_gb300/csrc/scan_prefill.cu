@@ -17,7 +17,7 @@
 //    balance over the 152 SMs.  (Splitting a channel's states over several
 //    lanes doubles the warps but costs more instructions per channel-row than
 //    the extra occupancy returns; narrow shapes get occupancy from the T split.)
-//  * u, dt, z, B, C stream in chunks of TC rows through a 3-deep cp.async ring
+//  * u, dt, z, B, C stream in chunks of TC rows through a 2-deep cp.async ring
 //    (16-byte copies, L2-only): HBM sees one read of every input and one write
 //    of y.  bf16 B/C rows are widened to f32 once per chunk in shared memory.
 //  * A lane keeps all N states of its channel in registers (f32) and walks the
