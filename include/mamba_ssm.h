@@ -399,6 +399,40 @@ MAMBA_API int64_t mamba_decode_graph_kernels(const MambaDecodeGraph* graph);
 MAMBA_API int mamba_decode_graph_destroy(MambaDecodeGraph* graph);
 
 /*
+ * mamba3_decode_graph_create - the Mamba-3 decode recorded once as a CUDA graph
+ * (the Mamba-3 page's engine, "T=1 step + CUDA Graph": its step chain per layer
+ * captured once and replayed per token; device pointers fixed at capture).
+ * Records n_steps x n_layers one-launch tokens (mamba3_siso_step_fused_batched),
+ * step-major: entry io[s * n_layers + l] is token s of layer l, on slab l of
+ * the four states, with D[l] (D may be NULL, or hold NULL entries).  Every
+ * token is validated exactly as the direct call validates it, before the graph
+ * is instantiated; on an error nothing is created and *out is NULL.  Launched,
+ * counted and freed with mamba_decode_graph_launch / _kernels / _destroy; the
+ * buffers stay the caller's and must outlive the graph (write the next
+ * tokens' inputs into the same buffers between launches).
+ *
+ *   io       [n_steps * n_layers] per-token buffers, shapes and dtypes as for
+ *            mamba3_siso_step_fused_batched (angles NULL when n_angles = 0)
+ *   ssm_state [n_layers][B][H][P][N], k_state [n_layers][B][H][N],
+ *   v_state  [n_layers][B][H][P], angle_state [n_layers][B][H][n_angles] (f32)
+ */
+typedef struct Mamba3TokenIO {
+  void* y;             /* [B][H][P], y_dtype (out) */
+  const void* x;       /* [B][H][P], x_dtype */
+  const float* k_in;   /* [B][H][N] */
+  const float* q_in;   /* [B][H][N] */
+  const float* dt;     /* [B][H] */
+  const float* A;      /* [B][H] */
+  const float* lam;    /* [B][H] */
+  const float* angles; /* [B][n_angles] or NULL */
+} Mamba3TokenIO;
+
+MAMBA_API int mamba3_decode_graph_create(MambaDecodeGraph** out, const Mamba3TokenIO* io, const float* const* D,
+                                         int64_t n_steps, int64_t n_layers, int y_dtype, int x_dtype,
+                                         float* ssm_state, float* k_state, float* v_state, float* angle_state,
+                                         int64_t B, int64_t H, int64_t P, int64_t N, int64_t n_angles);
+
+/*
  * One linear layer of the Mamba-1 block on the tensor cores (bf16 operands,
  * f32 accumulation):  C[M][N] = A[M][K] . W[N][K]^T (+ R[M][N]).
  * (inference.rs step chain F2 in_proj, F5 x_proj, F6 dt_proj and F11

@@ -11,6 +11,7 @@ C-ABI entry points (include/mamba_ssm.h), each backed by hand-written CUDA kerne
   mamba3_siso_step_batched      T=1 step of the Mamba-3 SISO (trapezoidal) recurrence
   mamba3_siso_step_prepare      its inputs: angle state advanced, k and q rotated, alpha/beta/gamma
   mamba3_siso_step_fused_batched  both in one launch (k and q never leave the SM)
+  mamba3_decode_graph_create    n_steps x n_layers such tokens recorded once as a CUDA graph
   mamba_linear_bf16             a projection of the layer on the tensor cores (tcgen05)
   mamba_rmsnorm                 RMSNorm of the f32 residual stream
   mamba_layer_prefill / _step   the whole Mamba-1 block (norm, projections, mixer, residual)
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: F401
     ABI_SYMBOLS,
     DecodeGraph,
     LayerDecodeGraph,
+    Mamba3DecodeGraph,
     LIB_PATH,
     MAMBA_BF16,
     MAMBA_ERR_CUDA,

@@ -40,6 +40,7 @@ ABI_SYMBOLS = (
     "mamba3_siso_step_batched",
     "mamba3_siso_step_prepare",
     "mamba3_siso_step_fused_batched",
+    "mamba3_decode_graph_create",
     "mamba_linear_bf16",
     "mamba_rmsnorm",
     "mamba_layer_workspace_bytes",
@@ -131,6 +132,9 @@ def load(path: str | None = None):
         lib.mamba_decode_graph_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i64, i32, i32, vp, vp,
                                                   i64, i64, i64, i64]
         lib.mamba_decode_graph_create.restype = ctypes.c_int
+        lib.mamba3_decode_graph_create.argtypes = [ctypes.POINTER(vp), vp, vp, i64, i64, i32, i32, vp, vp, vp, vp,
+                                                   i64, i64, i64, i64, i64]
+        lib.mamba3_decode_graph_create.restype = ctypes.c_int
         lib.mamba_decode_graph_launch.argtypes = [vp, vp]
         lib.mamba_decode_graph_launch.restype = ctypes.c_int
         lib.mamba_decode_graph_kernels.argtypes = [vp]
@@ -908,3 +912,72 @@ class DecodeGraph:
             self.close()
         except Exception:
             pass
+
+
+class _M3TokenIO(ctypes.Structure):
+    _fields_ = [("y", ctypes.c_void_p), ("x", ctypes.c_void_p), ("k_in", ctypes.c_void_p),
+                ("q_in", ctypes.c_void_p), ("dt", ctypes.c_void_p), ("A", ctypes.c_void_p),
+                ("lam", ctypes.c_void_p), ("angles", ctypes.c_void_p)]
+
+
+class Mamba3DecodeGraph(DecodeGraph):
+    """The Mamba-3 SISO decode recorded once as a CUDA graph
+    (mamba3_decode_graph_create): io is n_steps lists of n_layers dicts with y,
+    x, k_in, q_in, dt, A, lam and angles (or None) -- the tensors of
+    mamba3_siso_step_fused_batched -- and D a list of n_layers [H] tensors (or
+    None).  One launch() replays the n_steps x n_layers one-launch tokens on
+    the given (or current) stream over slab l of the four states; write the
+    next tokens' inputs into the same tensors between launches."""
+
+    def __init__(self, io, ssm_state, k_state, v_state, angle_state=None, D=None):
+        lib = load()
+        n_steps = len(io)
+        n_layers = len(io[0]) if n_steps else 0
+        if n_layers == 0 or any(len(row) != n_layers for row in io):
+            raise ValueError("io must be n_steps lists of n_layers entries")
+        x0, k0 = io[0][0]["x"], io[0][0]["k_in"]
+        Bsz, H, P = x0.shape
+        N = k0.shape[2]
+        a0 = io[0][0].get("angles")
+        na = 0 if a0 is None else a0.shape[1]
+        if (na > 0) != (angle_state is not None):
+            raise ValueError("angles and angle_state go together")
+        for st, nm, shp in ((ssm_state, "ssm_state", (n_layers, Bsz, H, P, N)),
+                            (k_state, "k_state", (n_layers, Bsz, H, N)), (v_state, "v_state", (n_layers, Bsz, H, P)),
+                            (angle_state, "angle_state", (n_layers, Bsz, H, na))):
+            _f32_param(st, nm, shp)
+        Dp = None
+        if D is not None:
+            if len(D) != n_layers:
+                raise ValueError("D must hold one entry per layer")
+            for d in D:
+                _f32_param(d, "D", (H,))
+            Dp = (ctypes.c_void_p * n_layers)(*[_ptr(d) for d in D])
+        Q = (_M3TokenIO * (n_steps * n_layers))()
+        y_code = _dtype_code(io[0][0]["y"])
+        for s_, row in enumerate(io):
+            for l, q in enumerate(row):
+                for k, shp in (("y", (Bsz, H, P)), ("x", (Bsz, H, P))):
+                    t = q[k]
+                    if tuple(t.shape) != shp or not t.is_contiguous():
+                        raise ValueError(f"io[{s_}][{l}]['{k}'] must be a contiguous {shp} tensor")
+                if _dtype_code(q["y"]) != y_code or q["x"].dtype != x0.dtype:
+                    raise ValueError("every y, and every x, must have one dtype")
+                for k in ("k_in", "q_in"):
+                    _f32_param(q[k], k, (Bsz, H, N))
+                for k in ("dt", "A", "lam"):
+                    _f32_param(q[k], k, (Bsz, H))
+                if na:
+                    _f32_param(q["angles"], "angles", (Bsz, na))
+                elif q.get("angles") is not None:
+                    raise ValueError("angles given for one token and not for another")
+                Q[s_ * n_layers + l] = _M3TokenIO(_ptr(q["y"]), _ptr(q["x"]), _ptr(q["k_in"]), _ptr(q["q_in"]),
+                                                  _ptr(q["dt"]), _ptr(q["A"]), _ptr(q["lam"]), _ptr(q.get("angles")))
+        h = ctypes.c_void_p()
+        _check(lib.mamba3_decode_graph_create(ctypes.byref(h), Q, Dp, n_steps, n_layers, y_code, _dtype_code(x0),
+                                              _ptr(ssm_state), _ptr(k_state), _ptr(v_state), _ptr(angle_state), Bsz,
+                                              H, P, N, na))
+        self._keep = (io, D, Q, Dp)
+        self._h = h
+        self._device = x0.device
+        self.n_steps, self.n_layers = n_steps, n_layers

@@ -12,6 +12,10 @@
 // Mamba-1 blocks (the pages' full F1-F12 chain per layer): n_layers
 // mamba_layer_step calls; the graph handle is the same type.
 //
+// mamba3_decode_graph_create records n_steps x n_layers Mamba-3 SISO tokens,
+// each the public mamba3_siso_step_fused_batched call (the Mamba-3 page's
+// "T=1 step + CUDA Graph": steps F4c-F6 per layer, captured once).
+//
 // Capture runs on a private stream in relaxed mode: the first call of a kernel
 // instance configures it (shared-memory opt-in, occupancy query), which is not
 // a stream operation and must not be refused inside the capture.  Nothing runs
@@ -102,6 +106,74 @@ extern "C" int mamba_decode_graph_create(MambaDecodeGraph** out, const MambaMixe
     cudaGraphExecDestroy(exec);
     cudaGraphDestroy(graph);
     return mamba::set_last_error(MAMBA_ERR_CUDA, "mamba_decode_graph_create: out of host memory");
+  }
+  g->graph = graph;
+  g->exec = exec;
+  g->device = dev;
+  g->kernels = kernels;
+  *out = g;
+  return mamba::set_last_error(MAMBA_OK, "");
+}
+
+extern "C" int mamba3_decode_graph_create(MambaDecodeGraph** out, const Mamba3TokenIO* io, const float* const* D,
+                                          int64_t n_steps, int64_t n_layers, int y_dtype, int x_dtype,
+                                          float* ssm_state, float* k_state, float* v_state, float* angle_state,
+                                          int64_t B, int64_t H, int64_t P, int64_t N, int64_t n_angles) {
+  if (!out) return mamba::set_last_error(MAMBA_ERR_INVALID_ARG, "mamba3_decode_graph_create: out is NULL");
+  *out = nullptr;
+  if (!io) return mamba::set_last_error(MAMBA_ERR_INVALID_ARG, "mamba3_decode_graph_create: io must not be NULL");
+  if (n_steps < 1 || n_layers < 1 || n_steps > (int64_t(1) << 20) || n_layers > (int64_t(1) << 20) ||
+      n_steps * n_layers > (int64_t(1) << 24))
+    return mamba::set_last_error(MAMBA_ERR_INVALID_ARG,
+                                 "mamba3_decode_graph_create: n_steps and n_layers must be >= 1 (at most 2^24 "
+                                 "tokens x layers in one graph)");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_error("cudaGetDevice", e);
+  cudaStream_t s = nullptr;
+  if ((e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking)) != cudaSuccess)
+    return cuda_error("cudaStreamCreateWithFlags", e);
+  if ((e = cudaStreamBeginCapture(s, cudaStreamCaptureModeRelaxed)) != cudaSuccess) {
+    cudaStreamDestroy(s);
+    return cuda_error("cudaStreamBeginCapture", e);
+  }
+  int rc = MAMBA_OK;
+  std::string msg;
+  int64_t kernels = 0;
+  for (int64_t st = 0; st < n_steps && rc == MAMBA_OK; ++st) {
+    for (int64_t l = 0; l < n_layers; ++l) {
+      const Mamba3TokenIO& q = io[st * n_layers + l];
+      rc = mamba3_siso_step_fused_batched(q.y, y_dtype, q.x, x_dtype, q.k_in, q.q_in, q.dt, q.A, q.lam, q.angles,
+                                          D ? D[l] : nullptr, ssm_state, k_state, v_state, angle_state, l,
+                                          n_layers, B, H, P, N, n_angles, s);
+      if (rc != MAMBA_OK) {
+        char head[96];
+        snprintf(head, sizeof(head), "mamba3_decode_graph_create: step %lld, layer %lld: ", (long long)st,
+                 (long long)l);
+        msg = std::string(head) + mamba_last_error();
+        break;
+      }
+      if (B > 0 && H > 0 && P > 0) ++kernels;
+    }
+  }
+  cudaGraph_t graph = nullptr;
+  e = cudaStreamEndCapture(s, &graph);  // ends the capture on every path
+  cudaStreamDestroy(s);
+  if (rc != MAMBA_OK || e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    if (rc != MAMBA_OK) return mamba::set_last_error(rc, msg.c_str());
+    return cuda_error("cudaStreamEndCapture", e);
+  }
+  cudaGraphExec_t exec = nullptr;
+  if ((e = cudaGraphInstantiate(&exec, graph, 0)) != cudaSuccess) {
+    cudaGraphDestroy(graph);
+    return cuda_error("cudaGraphInstantiate", e);
+  }
+  MambaDecodeGraph* g = new (std::nothrow) MambaDecodeGraph;
+  if (!g) {
+    cudaGraphExecDestroy(exec);
+    cudaGraphDestroy(graph);
+    return mamba::set_last_error(MAMBA_ERR_CUDA, "mamba3_decode_graph_create: out of host memory");
   }
   g->graph = graph;
   g->exec = exec;

@@ -175,6 +175,18 @@ def test_decode_graph_rejects_bad_arguments_on_host(lib):
     assert lib.mamba_decode_graph_destroy(None) == m.MAMBA_OK
 
 
+def test_m3_decode_graph_rejects_bad_arguments_on_host(lib):
+    h = ctypes.c_void_p()
+    # out NULL, io NULL, no tokens or layers: refused before any device call
+    args = lambda n_steps=1, n_layers=1: (FAKE, None, n_steps, n_layers, 0, 0, FAKE, FAKE, FAKE, FAKE, 2, 3, 64, 64, 32)
+    assert lib.mamba3_decode_graph_create(None, *args()) == m.MAMBA_ERR_INVALID_ARG
+    assert lib.mamba3_decode_graph_create(ctypes.byref(h), None, *args()[1:]) == m.MAMBA_ERR_INVALID_ARG
+    assert h.value is None
+    for n_steps, n_layers in ((0, 1), (1, 0), (-1, 4), (1 << 21, 1)):
+        assert lib.mamba3_decode_graph_create(ctypes.byref(h), *args(n_steps, n_layers)) == m.MAMBA_ERR_INVALID_ARG
+        assert "n_steps" in m.mamba_last_error()
+
+
 def test_mixer_prefill_refuses_other_d_conv_on_host(lib):
     for K, code in ((0, m.MAMBA_ERR_UNSUPPORTED), (5, m.MAMBA_ERR_UNSUPPORTED), (8, m.MAMBA_ERR_UNSUPPORTED)):
         rc = lib.mamba_mixer_prefill(FAKE, 64, 0, FAKE, 64, FAKE, 64, None, 0, FAKE, 16, FAKE, 16, 0,

@@ -1097,3 +1097,48 @@ def test_m3_fused_tokens_decode_like_the_oracle(cuda_lib, P, N, na, x_dtype):
     for s_dev, s_h in ((st, st_h), (ks, ks_h), (vs, vs_h), (th, th_h)):
         assert np.array_equal(to_host(s_dev[1]), s_h[1])
     assert m.mamba_device_faults(clear=True) == 0
+
+
+@pytest.mark.parametrize("P,N,na,aligned", [(64, 64, 32, True), (48, 16, 3, True), (32, 32, 8, False)])
+def test_m3_decode_graph_replays_the_direct_calls_bitwise(cuda_lib, P, N, na, aligned):
+    """A recorded n_steps x n_layers Mamba-3 decode graph, launched twice, gives
+    the same y and four states, bit for bit, as the same one-launch tokens
+    called directly (both step kernels: a k state 4 bytes off a 16-byte
+    boundary takes the per-(batch, head) one)."""
+    m = cuda_lib
+    L, S, Bsz, H = 3, 2, 4, 5
+    st_h, ks_h, vs_h = synth.m3_states(SEED + 11, L, Bsz, H, P, N)
+    th_h = synth.m3_angle_state(SEED + 11, L, Bsz, H, na)
+    g_states = [to_dev(a) for a in (st_h, ks_h, vs_h, th_h)]
+    d_states = [to_dev(a) for a in (st_h, ks_h, vs_h, th_h)]
+    if not aligned:
+        g_states[1], d_states[1] = _offset_like(g_states[1]), _offset_like(d_states[1])
+    D = [to_dev(synth.normal(SEED + 11, "m3_D", (H,), 1.0, layer=l)) for l in range(L)]
+    io = []
+    for s in range(S):
+        row = []
+        for l in range(L):
+            inp = {k: to_dev(v) for k, v in synth.m3_prepare_inputs(SEED + 11, l, s, Bsz, H, N, na).items()}
+            inp["x"] = to_dev(synth.normal(SEED + 11, "m3_x", (Bsz, H, P), 1.0, "f32", l, s))
+            inp["y"] = torch.empty((Bsz, H, P), device="cuda")
+            row.append(inp)
+        io.append(row)
+    with m.Mamba3DecodeGraph(io, *g_states, D=D) as g:
+        assert g.kernels == S * L
+        for rep in range(2):
+            g.launch()
+            torch.cuda.synchronize()
+            ys = {}
+            for s in range(S):
+                for l in range(L):
+                    q = io[s][l]
+                    ys[s, l] = torch.empty((Bsz, H, P), device="cuda")
+                    m.mamba3_siso_step_fused_batched(ys[s, l], q["x"], q["k_in"], q["q_in"], q["dt"], q["A"],
+                                                     q["lam"], q["angles"], *d_states, l, D[l])
+            torch.cuda.synchronize()
+            for (s, l), y in ys.items():
+                assert torch.equal(y, io[s][l]["y"]), f"y differs (launch {rep}, token {s}, layer {l})"
+            for i, nm in enumerate(("ssm", "k", "v", "angle")):
+                assert torch.equal(g_states[i], d_states[i]), f"{nm} state differs after launch {rep}"
+    assert m.mamba_device_faults(clear=True) == 0
+
