@@ -1142,3 +1142,34 @@ def test_m3_decode_graph_replays_the_direct_calls_bitwise(cuda_lib, P, N, na, al
                 assert torch.equal(g_states[i], d_states[i]), f"{nm} state differs after launch {rep}"
     assert m.mamba_device_faults(clear=True) == 0
 
+
+
+def test_m3_fused_token_equals_prepare_then_step_at_the_decode_shape(cuda_lib):
+    """At the bench's decode shape (batch 128 x 24 heads, headdim 64, d_state 64,
+    32 rotated pairs) every copy-ring CTA walks several (batch, head) tiles and
+    reuses its stages: the one-launch token still equals the preparation + step
+    bit for bit over two tokens, and the other layer's slabs stay untouched."""
+    m = cuda_lib
+    L, layer, Bsz, H, P, N, na = 2, 1, 128, 24, 64, 64, 32
+    st_h, ks_h, vs_h = synth.m3_states(SEED + 13, L, Bsz, H, P, N)
+    th_h = synth.m3_angle_state(SEED + 13, L, Bsz, H, na)
+    two = [to_dev(a) for a in (st_h, ks_h, vs_h, th_h)]
+    one = [to_dev(a) for a in (st_h, ks_h, vs_h, th_h)]
+    D = to_dev(synth.normal(SEED + 13, "m3_D", (H,), 1.0))
+    for step in range(2):
+        inp = synth.m3_prepare_inputs(SEED + 13, layer, step, Bsz, H, N, na)
+        d = {n: to_dev(v) for n, v in inp.items()}
+        x = to_dev(synth.normal(SEED + 13, "m3_x", (Bsz, H, P), 1.0, "f32", layer, step))
+        k, q, al, be, ga = _m3p_call(m, inp, na, two[3], layer)
+        y2 = torch.empty((Bsz, H, P), device="cuda")
+        m.mamba3_siso_step_batched(y2, x, k, q, al, be, ga, two[0], two[1], two[2], layer, D)
+        y1 = torch.empty((Bsz, H, P), device="cuda")
+        m.mamba3_siso_step_fused_batched(y1, x, d["k_in"], d["q_in"], d["dt"], d["A"], d["lam"], d["angles"],
+                                         *one, layer, D)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2), f"y differs at token {step}"
+        for i, nm in enumerate(("ssm", "k", "v", "angle")):
+            assert torch.equal(one[i], two[i]), f"{nm} state differs at token {step}"
+    for i, a in enumerate((st_h, ks_h, vs_h, th_h)):
+        assert np.array_equal(to_host(one[i][0]), a[0])
+    assert m.mamba_device_faults(clear=True) == 0
