@@ -143,6 +143,60 @@ def test_kernels_conv_worked_example(cuda_lib):
     assert np.array_equal(cs.cpu().numpy().reshape(1, 1, 3), st_ref)
 
 
+def _m3p_case():
+    g = _load("m3_prepare_worked_example.json")
+    i, e = g["inputs"], g["expected"]
+    arr = lambda v, *shape: np.asarray(v, np.float64).reshape(*shape)
+    inp = dict(k_in=arr(i["k_in"], 1, 1, 16), q_in=arr(i["q_in"], 1, 1, 16), dt=arr(i["dt"], 1, 1),
+               A=arr(i["A"], 1, 1), lam=arr(i["lam"], 1, 1), angles=arr(i["angles"], 1, 2),
+               angle_state=arr(i["angle_state"], 1, 1, 1, 2))
+    exp = dict(angle_state=arr(e["angle_state"], 1, 1, 2), k=arr(e["k"], 1, 1, 16), q=arr(e["q"], 1, 1, 16),
+               alpha=e["alpha_times_e"] / math.e, beta=e["beta_times_e"] / math.e, gamma=e["gamma"])
+    return inp, exp
+
+
+def test_oracle_m3_prepare_worked_example():
+    inp, exp = _m3p_case()
+    st = inp["angle_state"].copy()
+    k, q, al, be, ga = oracle.m3_prepare(inp["k_in"], inp["q_in"], inp["dt"], inp["A"], inp["lam"], inp["angles"],
+                                         st, 0)
+    np.testing.assert_allclose(st[0], exp["angle_state"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(k, exp["k"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose(q, exp["q"], rtol=0, atol=1e-15)
+    np.testing.assert_allclose([al[0, 0], be[0, 0], ga[0, 0]], [exp["alpha"], exp["beta"], exp["gamma"]],
+                               rtol=1e-15, atol=0)
+
+
+@pytest.mark.gpu
+def test_kernels_m3_prepare_worked_example(cuda_lib):
+    """The preparation kernel and the one-launch token (whose k state receives
+    the turned k) against the hand-derived values."""
+    import torch
+
+    m = cuda_lib
+    inp, exp = _m3p_case()
+    d = lambda a: torch.tensor(np.asarray(a, np.float32), device="cuda").contiguous()
+    st = d(inp["angle_state"])
+    k, q = torch.empty((1, 1, 16), device="cuda"), torch.empty((1, 1, 16), device="cuda")
+    al, be, ga = (torch.empty((1, 1), device="cuda") for _ in range(3))
+    m.mamba3_siso_step_prepare(k, q, al, be, ga, d(inp["k_in"]), d(inp["q_in"]), d(inp["dt"]), d(inp["A"]),
+                               d(inp["lam"]), d(inp["angles"]), st, 0)
+    torch.cuda.synchronize()
+    _within(st.cpu().numpy()[0], exp["angle_state"])
+    _within(k.cpu().numpy(), exp["k"])
+    _within(q.cpu().numpy(), exp["q"])
+    _within(np.array([al.item(), be.item(), ga.item()]), np.array([exp["alpha"], exp["beta"], exp["gamma"]]))
+    # the same token in one launch: the k state receives the turned k
+    h, ks, vs = (torch.zeros(s, device="cuda") for s in ((1, 1, 1, 1, 16), (1, 1, 1, 16), (1, 1, 1, 1)))
+    st2 = d(inp["angle_state"])
+    y = torch.empty((1, 1, 1), device="cuda")
+    m.mamba3_siso_step_fused_batched(y, torch.ones((1, 1, 1), device="cuda"), d(inp["k_in"]), d(inp["q_in"]),
+                                     d(inp["dt"]), d(inp["A"]), d(inp["lam"]), d(inp["angles"]), h, ks, vs, st2, 0)
+    torch.cuda.synchronize()
+    _within(ks.cpu().numpy()[0], exp["k"])
+    _within(st2.cpu().numpy()[0], exp["angle_state"])
+
+
 @pytest.mark.gpu
 def test_kernels_m3_worked_example(cuda_lib):
     import torch
