@@ -54,6 +54,14 @@ KERNEL_SOURCES["fused"] = KERNEL_SOURCES["scan"]
 KERNEL_SOURCES["gemm"] = ["selective_state_space_conv1d_gb300/csrc/gemm.cu",
                           "selective_state_space_conv1d_gb300/csrc/async_copy.cuh"]
 KERNEL_SOURCES["rmsnorm"] = ["selective_state_space_conv1d_gb300/csrc/rmsnorm.cu"]
+# the whole block step: every kernel it launches
+KERNEL_SOURCES["block"] = ["selective_state_space_conv1d_gb300/csrc/api.cu",
+                           "selective_state_space_conv1d_gb300/csrc/gemm.cu",
+                           "selective_state_space_conv1d_gb300/csrc/rmsnorm.cu",
+                           "selective_state_space_conv1d_gb300/csrc/conv1d.cu",
+                           "selective_state_space_conv1d_gb300/csrc/ssm_step.cu",
+                           "selective_state_space_conv1d_gb300/csrc/async_copy.cuh",
+                           "selective_state_space_conv1d_gb300/csrc/device_math.cuh"]
 KERNEL_SOURCES["m3_step"] = ["selective_state_space_conv1d_gb300/csrc/m3_step.cu",
                              "selective_state_space_conv1d_gb300/csrc/m3_math.cuh",
                              "selective_state_space_conv1d_gb300/csrc/device_math.cuh"]
@@ -1136,7 +1144,7 @@ def run_block_decode(torch, m, synth, device, n_steps=32, L=24, Bsz=128):
                           "kernels), launched per token after a copy of the token's hidden state"},
     }
     peak, peak_src = hbm_peak()
-    out["roofline"] = roofline(L * (w_bytes + state_bytes), ms, peak, peak_src, None)
+    out["roofline"] = roofline(L * (w_bytes + state_bytes), ms, peak, peak_src, ncu_traffic("block", out["workload"]))
     out["roofline_kernel"] = ("whole 24-layer step (7 kernels per layer; each is latency-bound: the bytes are "
                               "the layers' weights and the state read and written once)")
     return out
