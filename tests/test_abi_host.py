@@ -238,6 +238,30 @@ def test_m3_fused_rejects_bad_arguments_on_host(lib):
     assert call(B=0, k_in=None) == m.MAMBA_OK
 
 
+def test_m3_fused_and_graph_wrappers_refuse_mismatched_tensors_before_any_call():
+    import torch
+    B, H, P, N, na, L = 2, 3, 8, 16, 4, 2
+    f = lambda *s: torch.zeros(*s)
+    tok = dict(y=f(B, H, P), x=f(B, H, P), k_in=f(B, H, N), q_in=f(B, H, N), dt=f(B, H), A=f(B, H), lam=f(B, H),
+               angles=f(B, na))
+    states = dict(ssm_state=f(L, B, H, P, N), k_state=f(L, B, H, N), v_state=f(L, B, H, P), angle_state=f(L, B, H, na))
+    bad = [dict(k_in=f(B, H, N + 2)), dict(dt=f(B, H + 1)), dict(angles=None), dict(x=f(B, H, P + 1)),
+           dict(lam=f(B, H).double()), dict(angle_state=f(L, B, H, na + 1)), dict(ssm_state=f(L, B, H, P, N)[:, :, :, :, ::2])]
+    for b in bad:
+        kw = {**tok, **states, **b}
+        with pytest.raises(ValueError):
+            m.mamba3_siso_step_fused_batched(kw["y"], kw["x"], kw["k_in"], kw["q_in"], kw["dt"], kw["A"], kw["lam"],
+                                             kw["angles"], kw["ssm_state"], kw["k_state"], kw["v_state"],
+                                             kw["angle_state"], 0)
+    for b in bad:
+        kw = {**tok, **states, **b}
+        io = [[{k: kw[k] for k in tok}] * L]
+        with pytest.raises(ValueError):
+            m.Mamba3DecodeGraph(io, kw["ssm_state"], kw["k_state"], kw["v_state"], kw["angle_state"])
+    with pytest.raises(ValueError):  # D needs one entry per layer
+        m.Mamba3DecodeGraph([[dict(tok)] * L], *states.values(), D=[f(H)])
+
+
 def test_m3_prepare_wrapper_refuses_mismatched_tensors_before_any_call():
     import torch
     B, H, N, na = 2, 3, 8, 2
