@@ -555,3 +555,32 @@ def test_m3_prepare_without_angles_copies_and_keeps_other_slabs():
                                               np.ascontiguousarray(angles[pb]), stP, 1)
     for u, v in ((kP, k), (qP, q), (alP, al), (beP, be), (gaP, ga), (stP[1], st[1])):
         np.testing.assert_array_equal(u, perm(v))
+
+
+def test_m3_prepare_and_step_discretise_the_ode_to_the_rule_s_order():
+    """The preparation's weights and the step together integrate
+    dh/dt = A h + k x(t).  For x(t) = sin(w t), h(0) = 0 the exact state is
+    k (w e^{At} - A sin wt - w cos wt) / (A^2 + w^2).  The trapezoid weights
+    (lam = 1/2) are second order: halving dt quarters the error at t = 1; the
+    end-point rule (lam = 1) is first order: halving dt halves it."""
+    A, w = -2.0, 3.0
+    exact = (w * np.exp(A) - A * np.sin(w) - w * np.cos(w)) / (A * A + w * w)
+
+    def run(n, lam):
+        d = 1.0 / n
+        st = np.zeros((1, 1, 1, 1, 2))
+        ks = np.array([1.0, 0.0]).reshape(1, 1, 1, 2)   # the previous token's k (constant)
+        vs = np.zeros((1, 1, 1, 1))                      # the previous token's x: x(0) = 0
+        k_in = np.array([1.0, 0.0]).reshape(1, 1, 2)
+        for i in range(1, n + 1):
+            k, q, al, be, ga = oracle.m3_prepare(k_in, k_in, np.full((1, 1), d), np.full((1, 1), A),
+                                                 np.full((1, 1), lam), None, None, 0)
+            x = np.full((1, 1, 1), np.sin(w * i * d))
+            oracle.m3_step(x, k, q, al, be, ga, st, ks, vs, 0)
+        return abs(st[0, 0, 0, 0, 0] - exact)
+
+    e1, e2, e3 = (run(n, 0.5) for n in (50, 100, 200))
+    assert 3.6 < e1 / e2 < 4.4 and 3.6 < e2 / e3 < 4.4, (e1, e2, e3)
+    f1, f2 = run(100, 1.0), run(200, 1.0)
+    assert 1.8 < f1 / f2 < 2.2, (f1, f2)
+    assert e2 < f1 / 10
